@@ -1,0 +1,317 @@
+"""Pins for the fp64 oracle: each test checks it against something other than
+itself -- the pages' printed figures, closed forms, a library routine, or
+invariants of the mathematics.  CPU only."""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+RNG = np.random.default_rng(12345)
+
+
+def _bf16(x):
+    return O.round_to_bf16(np.asarray(x, np.float64))
+
+
+def _rand_head(L, rng, std_c=1.0, std_w=0.02):
+    rows = _bf16(rng.normal(0, std_c, (L, O.ROW_DIM)))
+    W_UK = _bf16(rng.normal(0, std_w, (128, 512)))
+    W_UV = _bf16(rng.normal(0, std_w, (128, 512)))
+    q_nope = _bf16(rng.normal(0, 1, 128))
+    q_pe = _bf16(rng.normal(0, 1, 64))
+    return q_nope, q_pe, rows, W_UK, W_UV
+
+
+# ----------------------------------------------------------------- bf16 ---- #
+
+def test_bf16_rounding_matches_torch_on_fp32_values():
+    # For inputs that are exact fp32 values the one-step fp64 -> bf16 rounding
+    # must equal torch's fp32 -> bf16 conversion (round to nearest even).
+    x32 = RNG.normal(0, 3, 20000).astype(np.float32)
+    x32 = np.concatenate([x32, np.float32([1e-40, -3e-39, 3.3e38, 0.0, -0.0, 1.0, 65504.0])])
+    ref = torch.from_numpy(x32).to(torch.bfloat16).to(torch.float64).numpy()
+    got = O.round_to_bf16(x32.astype(np.float64))
+    np.testing.assert_array_equal(got, ref)
+
+
+def test_bf16_rounding_ties_to_even():
+    assert O.round_to_bf16(1 + 2.0 ** -8) == 1.0                      # halfway, keep even 1.0
+    assert O.round_to_bf16(1 + 3 * 2.0 ** -8) == 1 + 2 * 2.0 ** -7    # halfway, round up to even
+    assert O.round_to_bf16(-(1 + 2.0 ** -8 + 2.0 ** -20)) == -(1 + 2.0 ** -7)
+    assert np.isinf(O.round_to_bf16(3.5e38))
+    bits = O.f64_to_bf16_bits(np.array([1.0, -2.0, 0.5]))
+    np.testing.assert_array_equal(bits, np.array([0x3F80, 0xC000, 0x3F00], np.uint16))
+    np.testing.assert_array_equal(O.bf16_bits_to_f64(bits), [1.0, -2.0, 0.5])
+
+
+# ------------------------------------------------------- cache footprint ---- #
+
+def test_cache_footprint_matches_page_figures():
+    g = json.load(open(os.path.join(GOLDEN, "page_figures.json")))
+    e = g["v2lite_latent_bytes_per_token"]
+    assert O.latent_cache_bytes_per_token(e["layers"], e["latent_dim"], e["rope_dim"], e["elem_bytes"]) == e["value"]
+    e = g["v2lite_latent_mib_at_32k"]
+    assert O.latent_cache_bytes_per_token(e["layers"]) * e["tokens"] / 2 ** 20 == e["value_mib"]
+    e = g["v2lite_per_head_mib_at_32k"]
+    naive = O.per_head_cache_bytes_per_token(e["layers"], e["kv_heads"], e["key_dim"], e["value_dim"], e["elem_bytes"])
+    assert naive * e["tokens"] / 2 ** 20 == e["value_mib"]
+    # "Both runtimes used a ninth of the calculation"
+    assert 8.5 < naive / O.latent_cache_bytes_per_token(27) < 9.5
+    e = g["v3_latent_bytes_per_token_per_layer"]
+    assert O.latent_cache_bytes_per_token(e["layers"]) == e["value"]
+    e3 = g["v3_mha_equivalent_bytes_per_token_per_layer"]
+    mha = O.per_head_cache_bytes_per_token(1, e3["kv_heads"], e3["key_dim"], e3["value_dim"], e3["elem_bytes"])
+    assert mha == e3["value"] and round(mha / O.latent_cache_bytes_per_token(1)) == e3["ratio_rounded"]
+    e = g["kimi_linear_7_mla_layers_mib_at_32k"]
+    assert O.latent_cache_bytes_per_token(e["layers"]) * e["tokens"] / 2 ** 20 == e["value_mib"]
+    e = g["llama70b_kv_bytes_at_100k"]
+    b = O.per_head_cache_bytes_per_token(e["layers"], e["kv_heads"], e["head_dim"], e["head_dim"], e["elem_bytes"])
+    assert round(b * e["tokens"] / 1e9) == e["value_gb"]
+    for k in ("llama2_7b_kib_per_token", "falcon7b_kib_per_token"):
+        e = g[k]
+        b = O.per_head_cache_bytes_per_token(e["layers"], e["kv_heads"], e["head_dim"], e["head_dim"], e["elem_bytes"])
+        assert b / 1024 == e["value_kib"]
+    # INT8 latent row: 576 one-byte codes + fp32 scale and zero point
+    assert O.latent_cache_bytes_per_token(1, elem_bytes=1, side_bytes_per_row=8) == 584
+
+
+# ------------------------------------------------------------------ RoPE ---- #
+
+def test_rope_closed_forms():
+    x = np.zeros(64)
+    x[0], x[32] = 1.0, 1.0
+    # pair 0 turns at 1 rad per position; pair 16 at theta**(-1/2) = 0.01 rad per position
+    r = O.rope_rotate(x[None], np.array([1]), 10000.0)[0]
+    assert r[0] == pytest.approx(math.cos(1.0), abs=1e-15) and r[1] == pytest.approx(math.sin(1.0), abs=1e-15)
+    r = O.rope_rotate(x[None], np.array([100]), 10000.0)[0]
+    assert r[32] == pytest.approx(math.cos(1.0), abs=1e-13) and r[33] == pytest.approx(math.sin(1.0), abs=1e-13)
+    np.testing.assert_array_equal(O.rope_rotate(x[None], np.array([0]), 10000.0)[0], x)
+    np.testing.assert_array_equal(O.rope_rotate(x[None], np.array([777]), 0.0)[0], x)
+
+
+def test_rope_invariants():
+    q = RNG.normal(size=(64,))
+    k = RNG.normal(size=(64,))
+    for m, n in [(0, 0), (5, 3), (1000, 998), (1 << 20, (1 << 20) - 2)]:
+        rq = O.rope_rotate(q[None], np.array([m]), 10000.0)[0]
+        rk = O.rope_rotate(k[None], np.array([n]), 10000.0)[0]
+        assert np.linalg.norm(rq) == pytest.approx(np.linalg.norm(q), rel=1e-12)
+        # the score depends on positions only through m - n
+        r0 = O.rope_rotate(q[None], np.array([m - n]), 10000.0)[0]
+        assert rq @ rk == pytest.approx(r0 @ k, rel=1e-9, abs=1e-9)
+
+
+# ------------------------------------------------------------------ INT8 ---- #
+
+def test_int8_worked_examples():
+    g = json.load(open(os.path.join(GOLDEN, "int8_worked_examples.json")))
+    for case in g["cases"]:
+        codes, s, zp = O.quantize_tokens_int8(np.array(case["row"], np.float32))
+        np.testing.assert_array_equal(codes[0], np.array(case["codes"], np.int8), err_msg=case["why"])
+        assert zp[0] == case["zero_point"]
+        assert s[0] == np.float32(np.float32(case["scale_num"]) / np.float32(case["scale_den"]))
+
+
+def test_int8_error_bound_and_zero():
+    rows = (RNG.normal(0, 1, (200, 576)) * RNG.uniform(0.01, 100, (200, 1))).astype(np.float32)
+    rows[:, 7] = 0.0
+    rows[3] = np.abs(rows[3])   # all non-negative row
+    rows[4] = -np.abs(rows[4])  # all non-positive row
+    codes, s, zp = O.quantize_tokens_int8(rows)
+    xh = O.dequantize_tokens_int8(codes, s, zp)
+    err = np.abs(xh - rows.astype(np.float64))
+    assert np.all(err <= s[:, None].astype(np.float64) * (0.5 + 1e-5))
+    np.testing.assert_array_equal(xh[:, 7], 0.0)
+    assert codes.min() >= -128 and codes.max() <= 127
+    # monotone: larger input never gets a smaller code
+    order = np.argsort(rows, axis=1, kind="stable")
+    assert np.all(np.diff(np.take_along_axis(codes.astype(int), order, 1), axis=1) >= 0)
+
+
+# ------------------------------------------------------ paged addressing ---- #
+
+def test_append_then_gather_roundtrip_and_injective_slots():
+    P, B, maxp = 16, 3, 5
+    perm = RNG.permutation(B * maxp)
+    table = perm.reshape(B, maxp).astype(np.int32)
+    cache = np.zeros((B * maxp, P, 576), np.uint16)
+    lens = [1, 37, 80]
+    seq_ids = [b for b in range(B) for _ in range(lens[b])]
+    pos = [t for b in range(B) for t in range(lens[b])]
+    src = _bf16(RNG.normal(0, 1, (len(pos), 576)))
+    O.append_tokens(cache, None, table, seq_ids, pos, O.f64_to_bf16_bits(src[:, :512]),
+                    O.f64_to_bf16_bits(src[:, 512:]), 0.0, P, int8=False)
+    slots = {O.page_slot(table, b, t, P) for b, t in zip(seq_ids, pos)}
+    assert len(slots) == len(pos)
+    off = 0
+    for b in range(B):
+        rows = O.gather_rows(cache, None, table, b, lens[b], P, int8=False)
+        np.testing.assert_array_equal(rows, src[off:off + lens[b]])
+        off += lens[b]
+    # with RoPE on, the stored key is the bf16 rounding of the fp64 rotation
+    cache2 = np.zeros_like(cache)
+    O.append_tokens(cache2, None, table, seq_ids, pos, O.f64_to_bf16_bits(src[:, :512]),
+                    O.f64_to_bf16_bits(src[:, 512:]), 10000.0, P, int8=False)
+    rows = O.gather_rows(cache2, None, table, 2, lens[2], P, int8=False)
+    want = _bf16(O.rope_rotate(src[off - lens[2]:off, 512:], np.arange(lens[2]), 10000.0))
+    np.testing.assert_array_equal(rows[:, 512:], want)
+
+
+# ------------------------------------------------------------- attention ---- #
+
+@pytest.mark.parametrize("L", [1, 2, 7, 64, 300])
+def test_absorbed_equals_unabsorbed(L):
+    rng = np.random.default_rng(L)
+    q_nope, q_pe, rows, W_UK, W_UV = _rand_head(L, rng)
+    o1, l1, _ = O.attend_unabsorbed(q_nope, q_pe, rows, W_UK, W_UV, 1 / math.sqrt(192))
+    o2, l2, _ = O.attend_absorbed(q_nope, q_pe, rows, W_UK, W_UV, 1 / math.sqrt(192))
+    np.testing.assert_allclose(o1, o2, rtol=1e-12, atol=1e-15)
+    assert l1 == pytest.approx(l2, rel=1e-13)
+
+
+def test_closed_forms():
+    rng = np.random.default_rng(7)
+    q_nope, q_pe, rows, W_UK, W_UV = _rand_head(9, rng)
+    scale = 0.3
+    # one token: the softmax weight is 1, so o = W^UV c_0 and lse = the score
+    o, lse, p = O.attend_unabsorbed(q_nope, q_pe, rows[:1], W_UK, W_UV, scale)
+    np.testing.assert_allclose(o, W_UV @ rows[0, :512], rtol=1e-13)
+    s0 = scale * (q_nope @ (W_UK @ rows[0, :512]) + q_pe @ rows[0, 512:])
+    assert lse == pytest.approx(s0, rel=1e-13) and p[0] == 1.0
+    # equal rows: o = W^UV c for any query, lse = s + ln L
+    eq = np.repeat(rows[:1], 9, axis=0)
+    o, lse, _ = O.attend_unabsorbed(q_nope, q_pe, eq, W_UK, W_UV, scale)
+    np.testing.assert_allclose(o, W_UV @ rows[0, :512], rtol=1e-12)
+    assert lse == pytest.approx(s0 + math.log(9), rel=1e-12)
+    # zero query: uniform weights, o = W^UV mean(c), lse = ln L
+    o, lse, p = O.attend_unabsorbed(np.zeros(128), np.zeros(64), rows, W_UK, W_UV, scale)
+    np.testing.assert_allclose(o, W_UV @ rows[:, :512].mean(axis=0), rtol=1e-12, atol=1e-16)
+    assert lse == pytest.approx(math.log(9), rel=1e-14)
+    np.testing.assert_allclose(p, np.full(9, 1 / 9), rtol=1e-14)
+    # empty sequence
+    o, lse, p = O.attend_unabsorbed(q_nope, q_pe, rows[:0], W_UK, W_UV, scale)
+    assert np.all(o == 0) and lse == -math.inf and p.size == 0
+
+
+@pytest.mark.parametrize("H,L", [(1, 1), (4, 8), (3, 33)])
+def test_library_sdpa_on_expanded_keys(H, L):
+    """torch's scaled_dot_product_attention in fp64 on CPU, fed explicitly
+    expanded per-head keys [W^UK c_t | k_pe_t] (192) and values W^UV c_t
+    (128), must equal the oracle."""
+    rng = np.random.default_rng(100 + H * L)
+    rows = _bf16(rng.normal(0, 1, (L, 576)))
+    W_UK = _bf16(rng.normal(0, 0.05, (H, 128, 512)))
+    W_UV = _bf16(rng.normal(0, 0.05, (H, 128, 512)))
+    q_nope = rng.normal(0, 1, (H, 128))
+    q_pe = rng.normal(0, 1, (H, 64))
+    scale = 1 / math.sqrt(192)
+    K = np.stack([np.concatenate([rows[:, :512] @ W_UK[h].T, rows[:, 512:]], axis=1) for h in range(H)])
+    V = np.stack([rows[:, :512] @ W_UV[h].T for h in range(H)])
+    Q = np.concatenate([q_nope, q_pe], axis=1)[:, None, :]
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        torch.from_numpy(Q)[None], torch.from_numpy(K)[None], torch.from_numpy(V)[None], scale=scale)[0, :, 0].numpy()
+    for h in range(H):
+        o, _, p = O.attend_unabsorbed(q_nope[h], q_pe[h], rows, W_UK[h], W_UV[h], scale)
+        np.testing.assert_allclose(o, ref[h], rtol=1e-10, atol=1e-14)
+        assert abs(p.sum() - 1.0) <= 1e-12
+
+
+def test_brute_force_scores_tiny():
+    """<= 8 tokens: every score from plain Python loops over explicitly built keys."""
+    rng = np.random.default_rng(3)
+    q_nope, q_pe, rows, W_UK, W_UV = _rand_head(6, rng, std_w=0.1)
+    scale = 0.25
+    scores = []
+    for t in range(6):
+        key = [sum(W_UK[k, m] * rows[t, m] for m in range(512)) for k in range(128)] + list(rows[t, 512:])
+        qv = list(q_nope) + list(q_pe)
+        scores.append(scale * sum(a * b for a, b in zip(qv, key)))
+    mx = max(scores)
+    z = sum(math.exp(s - mx) for s in scores)
+    _, lse, p = O.attend_unabsorbed(q_nope, q_pe, rows, W_UK, W_UV, scale)
+    np.testing.assert_allclose(p, [math.exp(s - mx) / z for s in scores], rtol=1e-11)
+    assert lse == pytest.approx(mx + math.log(z), rel=1e-12)
+
+
+@pytest.mark.parametrize("bounds", [[1], [5, 6], [0, 0, 10], [3, 17, 50, 99]])
+def test_split_combine_invariance(bounds):
+    rng = np.random.default_rng(sum(bounds) + 1)
+    q_nope, q_pe, rows, W_UK, W_UV = _rand_head(100, rng)
+    o, lse, _ = O.attend_unabsorbed(q_nope, q_pe, rows, W_UK, W_UV, 0.1)
+    o2, lse2 = O.attend_split(q_nope, q_pe, rows, W_UK, W_UV, 0.1, bounds)
+    np.testing.assert_allclose(o2, o, rtol=1e-12, atol=1e-16)
+    assert lse2 == pytest.approx(lse, rel=1e-13)
+    # combine of nothing but empty parts
+    oz, lz = O.combine_partials(np.zeros((3, 512)), np.full(3, -np.inf))
+    assert np.all(oz == 0) and lz == -math.inf
+
+
+@pytest.mark.parametrize("int8", [False, True])
+def test_decode_page_permutation_invariance(int8):
+    rng = np.random.default_rng(11)
+    B, H, P, maxp = 3, 2, 16, 6
+    lens = [96, 1, 50]
+    npg = B * maxp
+    if int8:
+        cache = rng.integers(-128, 128, (npg, P, 576)).astype(np.int8)
+        sz = np.stack([rng.uniform(0.01, 0.1, (npg, P)), rng.integers(-128, 128, (npg, P))], -1).astype(np.float32)
+    else:
+        cache = O.f64_to_bf16_bits(rng.normal(0, 1, (npg, P, 576)))
+        sz = None
+    table = np.arange(npg, dtype=np.int32).reshape(B, maxp)
+    W_UK = _bf16(rng.normal(0, 0.02, (H, 128, 512)))
+    W_UV = _bf16(rng.normal(0, 0.02, (H, 128, 512)))
+    qn = _bf16(rng.normal(0, 1, (B, H, 128)))
+    qp = _bf16(rng.normal(0, 1, (B, H, 64)))
+    out1, lse1 = O.decode(qn, qp, cache, sz, table, lens, W_UK, W_UV, 0.07, P, int8)
+    perm = rng.permutation(npg)          # physical page p moves to perm[p]
+    cache2 = np.empty_like(cache)
+    cache2[perm] = cache
+    sz2 = None
+    if int8:
+        sz2 = np.empty_like(sz)
+        sz2[perm] = sz
+    out2, lse2 = O.decode(qn, qp, cache2, sz2, perm[table].astype(np.int32), lens, W_UK, W_UV, 0.07, P, int8)
+    np.testing.assert_array_equal(out1, out2)
+    np.testing.assert_array_equal(lse1, lse2)
+    # absorbed cross-check over the whole batch
+    out3, lse3 = O.decode(qn, qp, cache, sz, table, lens, W_UK, W_UV, 0.07, P, int8, absorbed=True)
+    np.testing.assert_allclose(out3, out1, rtol=1e-11, atol=1e-15)
+
+
+# ------------------------------------------------ planted-mistake checks ---- #
+
+def test_pins_catch_planted_mistakes(monkeypatch):
+    """Plant plausible mistakes in the oracle (on the CPU) and check that the
+    library pin above would have caught each of them."""
+    rng = np.random.default_rng(5)
+    H, L = 2, 5
+    rows = _bf16(rng.normal(0, 1, (L, 576)))
+    W_UK = _bf16(rng.normal(0, 0.05, (H, 128, 512)))
+    W_UV = _bf16(rng.normal(0, 0.05, (H, 128, 512)))
+    q_nope = rng.normal(0, 1, (H, 128))
+    q_pe = rng.normal(0, 1, (H, 64))
+    K = np.stack([np.concatenate([rows[:, :512] @ W_UK[h].T, rows[:, 512:]], axis=1) for h in range(H)])
+    V = np.stack([rows[:, :512] @ W_UV[h].T for h in range(H)])
+    Q = np.concatenate([q_nope, q_pe], axis=1)[:, None, :]
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        torch.from_numpy(Q)[None], torch.from_numpy(K)[None], torch.from_numpy(V)[None], scale=0.2)[0, :, 0].numpy()
+
+    def dropped_rope(qn, qp, r, wk, wv, sc):
+        return O.attend_unabsorbed(qn, np.zeros_like(qp), r, wk, wv, sc)
+
+    def swapped_weights(qn, qp, r, wk, wv, sc):
+        return O.attend_unabsorbed(qn, qp, r, wv, wk, sc)
+
+    def wrong_sign(qn, qp, r, wk, wv, sc):
+        return O.attend_unabsorbed(qn, qp, r, wk, wv, -sc)
+
+    for bad in (dropped_rope, swapped_weights, wrong_sign):
+        o = np.stack([bad(q_nope[h], q_pe[h], rows, W_UK[h], W_UV[h], 0.2)[0] for h in range(H)])
+        assert not np.allclose(o, ref, rtol=1e-6), bad.__name__
