@@ -1,0 +1,121 @@
+// append.cu -- write new tokens into the paged latent cache.
+//
+// "The Architecture of Memory", decode phase: the new token's key/value state
+// is appended to the cache; in MLA that state is one 576-wide row, the latent
+// c_t plus the decoupled RoPE key ("Beyond the Attention Bottleneck", "The RoPE
+// Compatibility Problem": only the positional key carries RoPE, rotated here
+// once at its position).  Pages are found through the page table
+// ("PagedAttention: Virtual Memory for LLMs").  INT8 caches quantise the row
+// per token with an asymmetric min/max scale and zero point ("KV Cache
+// Optimization", section 3; "The Architecture of Memory", KIVI section).
+#include "params.cuh"
+
+namespace mla {
+
+
+// One warp per token.  Lane l owns latent values [16l, 16l + 16) and RoPE pair l.
+template <bool kInt8>
+__global__ void __launch_bounds__(256) append_kernel(AppendParams p) {
+  const int lane = threadIdx.x & 31;
+  const int i = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (i >= p.n_tokens) return;
+  const int b = p.seq_ids[i], pos = p.positions[i];
+  bool ok = b >= 0 && b < p.num_seqs && pos >= 0 && pos / p.page_size < p.max_pages;
+  int page = -1;
+  if (ok) {
+    page = p.block_table[size_t(b) * p.max_pages + pos / p.page_size];
+    ok = page >= 0 && page < p.num_pages;
+  }
+  if (!ok) {
+    if (lane == 0) set_status(p.status, MLA_ERR_DEVICE_BOUNDS);
+    return;
+  }
+  const size_t row = size_t(page) * p.page_size + pos % p.page_size;
+
+  // latent part: 16 bf16 per lane, two 16-byte loads
+  const uint4* src = reinterpret_cast<const uint4*>(p.c_kv + size_t(i) * kLatent) + 2 * lane;
+  uint4 c0 = src[0], c1 = src[1];
+
+  // RoPE pair `lane`: angle = pos * theta^(-2 lane / 64), evaluated in fp64
+  const __nv_bfloat162 kp = reinterpret_cast<const __nv_bfloat162*>(p.k_pe + size_t(i) * kRope)[lane];
+  __nv_bfloat162 kr = kp;
+  if (p.rope_theta > 0.0) {
+    const double inv_freq = pow(p.rope_theta, -double(2 * lane) / double(kRope));
+    const double ang = __dmul_rn(double(pos), inv_freq);
+    double sn, cs;
+    sincos(ang, &sn, &cs);
+    const double x0 = double(__low2float(kp)), x1 = double(__high2float(kp));
+    const double y0 = __dsub_rn(__dmul_rn(x0, cs), __dmul_rn(x1, sn));
+    const double y1 = __dadd_rn(__dmul_rn(x0, sn), __dmul_rn(x1, cs));
+    kr = __halves2bfloat162(__double2bfloat16(y0), __double2bfloat16(y1));
+  }
+
+  if constexpr (!kInt8) {
+    __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.cache) + row * kRow;
+    reinterpret_cast<uint4*>(dst)[2 * lane] = c0;
+    reinterpret_cast<uint4*>(dst)[2 * lane + 1] = c1;
+    reinterpret_cast<__nv_bfloat162*>(dst + kLatent)[lane] = kr;
+  } else {
+    // the row's 576 bf16 values, as exact fp32
+    float v[18];
+    const __nv_bfloat162* c0h = reinterpret_cast<const __nv_bfloat162*>(&c0);
+    const __nv_bfloat162* c1h = reinterpret_cast<const __nv_bfloat162*>(&c1);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      v[2 * j] = __low2float(c0h[j]);
+      v[2 * j + 1] = __high2float(c0h[j]);
+      v[8 + 2 * j] = __low2float(c1h[j]);
+      v[8 + 2 * j + 1] = __high2float(c1h[j]);
+    }
+    v[16] = __low2float(kr);
+    v[17] = __high2float(kr);
+    float lo = 0.f, hi = 0.f;  // the range always includes 0
+#pragma unroll
+    for (int j = 0; j < 18; ++j) {
+      lo = fminf(lo, v[j]);
+      hi = fmaxf(hi, v[j]);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+      hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+    }
+    // IEEE fp32, round to nearest even, no contraction, in the documented order
+    float s = __fdiv_rn(__fsub_rn(hi, lo), 255.f);
+    if (s == 0.f) s = 1.f;
+    float zp = rintf(__fsub_rn(-128.f, __fdiv_rn(lo, s)));
+    zp = fminf(fmaxf(zp, -128.f), 127.f);
+    int8_t q[18];
+#pragma unroll
+    for (int j = 0; j < 18; ++j) {
+      float c = __fadd_rn(rintf(__fdiv_rn(v[j], s)), zp);
+      c = fminf(fmaxf(c, -128.f), 127.f);
+      q[j] = int8_t(int(c));
+    }
+    int8_t* dst = static_cast<int8_t*>(p.cache) + row * kRow;
+    uint4 packed;
+    int8_t* pk = reinterpret_cast<int8_t*>(&packed);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) pk[j] = q[j];
+    reinterpret_cast<uint4*>(dst)[lane] = packed;
+    char2 tail;
+    tail.x = q[16];
+    tail.y = q[17];
+    reinterpret_cast<char2*>(dst + kLatent)[lane] = tail;
+    if (lane == 0) {
+      p.scale_zero[row * 2] = s;
+      p.scale_zero[row * 2 + 1] = zp;
+    }
+  }
+}
+
+cudaError_t launch_append(const AppendParams& p, bool int8, cudaStream_t stream) {
+  if (p.n_tokens == 0) return cudaSuccess;
+  const int warps = 8;
+  const int grid = (p.n_tokens + warps - 1) / warps;
+  if (int8) append_kernel<true><<<grid, warps * 32, 0, stream>>>(p);
+  else append_kernel<false><<<grid, warps * 32, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace mla

@@ -1,0 +1,249 @@
+// mla_api.cu -- the C ABI of libmla_gb300 (declared in include/mla.h):
+// argument validation, sizing of the decode work plan, and kernel launches
+// on the caller's stream.  Allocates nothing.
+#include <atomic>
+#include <cstdint>
+#include <cstdio>
+
+#include "mla_device.cuh"
+
+#include "params.cuh"
+
+using namespace mla;
+
+namespace {
+
+constexpr int kVersion = 100;  // 0.1.0
+
+std::atomic<cudaEvent_t> g_ev_start{nullptr}, g_ev_stop{nullptr};
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int head_chunk(int heads) { return (heads % 32 == 0) ? 32 : 16; }
+
+int sm_count() {
+  static int cached[128] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+  if (dev >= 0 && dev < 128 && cached[dev] > 0) return cached[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+  if (dev >= 0 && dev < 128) cached[dev] = n;
+  return n;
+}
+
+int effective_splits(const mla_dims* d, int num_splits) {
+  if (num_splits > 0) return num_splits;
+  const int n = sm_count();
+  if (n <= 0) return -1;
+  const int groups = d->num_heads / head_chunk(d->num_heads);
+  return n / groups > 0 ? n / groups : 1;
+}
+
+}  // namespace
+
+extern "C" {
+
+int mla_version(void) { return kVersion; }
+
+const char* mla_status_string(int s) {
+  switch (s) {
+    case MLA_OK: return "ok";
+    case MLA_ERR_INVALID_ARG: return "invalid argument";
+    case MLA_ERR_UNSUPPORTED: return "unsupported dimensions";
+    case MLA_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case MLA_ERR_CUDA: return "CUDA call failed";
+    case MLA_ERR_DEVICE_TIMEOUT: return "device: bounded wait ran out";
+    case MLA_ERR_DEVICE_BOUNDS: return "device: page-table entry, position or length out of range";
+    default: return "unknown status";
+  }
+}
+
+int mla_check_dims(const mla_dims* d) {
+  if (!d) return MLA_ERR_INVALID_ARG;
+  if (d->num_heads <= 0 || d->kv_lora_rank <= 0 || d->rope_dim <= 0 || d->qk_nope_dim <= 0 ||
+      d->v_head_dim <= 0 || d->page_size <= 0)
+    return MLA_ERR_INVALID_ARG;
+  if (d->cache_dtype != MLA_CACHE_BF16 && d->cache_dtype != MLA_CACHE_INT8) return MLA_ERR_INVALID_ARG;
+  if (d->kv_lora_rank != kLatent || d->rope_dim != kRope || d->qk_nope_dim != kNope || d->v_head_dim != kVDim)
+    return MLA_ERR_UNSUPPORTED;
+  if (d->page_size != 16 && d->page_size != 32 && d->page_size != 64 && d->page_size != 128)
+    return MLA_ERR_UNSUPPORTED;
+  if (d->num_heads != 16 && d->num_heads % 32 != 0) return MLA_ERR_UNSUPPORTED;
+  return MLA_OK;
+}
+
+int mla_cache_append(const mla_dims* d, void* cache, float* cache_scale_zero, int32_t num_pages,
+                     const int32_t* block_table, int32_t num_seqs, int32_t max_pages_per_seq,
+                     const int32_t* seq_ids, const int32_t* positions, int32_t n_tokens, const void* c_kv,
+                     const void* k_pe, double rope_theta, int32_t* device_status, mla_stream_t stream) {
+  int st = mla_check_dims(d);
+  if (st != MLA_OK) return st;
+  if (n_tokens < 0 || num_pages <= 0 || num_seqs <= 0 || max_pages_per_seq <= 0) return MLA_ERR_INVALID_ARG;
+  if (n_tokens == 0) return MLA_OK;
+  const bool int8 = d->cache_dtype == MLA_CACHE_INT8;
+  if (!cache || !block_table || !seq_ids || !positions || !c_kv || !k_pe) return MLA_ERR_INVALID_ARG;
+  if (int8 && !cache_scale_zero) return MLA_ERR_INVALID_ARG;
+  if (!aligned(cache, 16) || !aligned(c_kv, 16) || !aligned(k_pe, 4) || !aligned(block_table, 4) ||
+      !aligned(seq_ids, 4) || !aligned(positions, 4) || (int8 && !aligned(cache_scale_zero, 8)))
+    return MLA_ERR_INVALID_ARG;
+  AppendParams p;
+  p.cache = cache;
+  p.scale_zero = cache_scale_zero;
+  p.block_table = block_table;
+  p.seq_ids = seq_ids;
+  p.positions = positions;
+  p.c_kv = static_cast<const __nv_bfloat16*>(c_kv);
+  p.k_pe = static_cast<const __nv_bfloat16*>(k_pe);
+  p.status = device_status;
+  p.rope_theta = rope_theta;
+  p.n_tokens = n_tokens;
+  p.num_seqs = num_seqs;
+  p.max_pages = max_pages_per_seq;
+  p.num_pages = num_pages;
+  p.page_size = d->page_size;
+  return launch_append(p, int8, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
+int mla_auto_num_splits(const mla_dims* d, int32_t batch) {
+  int st = mla_check_dims(d);
+  if (st != MLA_OK) return st;
+  if (batch <= 0) return MLA_ERR_INVALID_ARG;
+  const int s = effective_splits(d, 0);
+  return s > 0 ? s : MLA_ERR_CUDA;
+}
+
+size_t mla_decode_workspace_size(const mla_dims* d, int32_t batch, int32_t num_splits) {
+  if (mla_check_dims(d) != MLA_OK || batch <= 0 || num_splits < 0) return 0;
+  const int s = effective_splits(d, num_splits);
+  if (s <= 0) return 0;
+  return workspace_layout(batch, d->num_heads, s).total;
+}
+
+int mla_decode(const mla_dims* d, const void* q_nope, const void* q_pe, const void* cache,
+               const float* cache_scale_zero, int32_t num_pages, const int32_t* block_table,
+               int32_t max_pages_per_seq, const int32_t* seq_lens, int32_t batch, const void* W_UK,
+               const void* W_UV, float softmax_scale, int32_t num_splits, void* workspace,
+               size_t workspace_bytes, void* out, float* lse_out, mla_stream_t stream) {
+  int st = mla_check_dims(d);
+  if (st != MLA_OK) return st;
+  const bool int8 = d->cache_dtype == MLA_CACHE_INT8;
+  if (batch <= 0 || num_pages <= 0 || max_pages_per_seq <= 0 || num_splits < 0) return MLA_ERR_INVALID_ARG;
+  if (!(softmax_scale > 0.f) || softmax_scale == INFINITY) return MLA_ERR_INVALID_ARG;
+  if (!q_nope || !q_pe || !cache || !block_table || !seq_lens || !W_UK || !W_UV || !out) return MLA_ERR_INVALID_ARG;
+  if (int8 && !cache_scale_zero) return MLA_ERR_INVALID_ARG;
+  if (!aligned(cache, 16) || !aligned(q_nope, 4) || !aligned(q_pe, 4) || !aligned(W_UK, 4) || !aligned(W_UV, 4) ||
+      !aligned(out, 4) || !aligned(block_table, 4) || !aligned(seq_lens, 4) || (lse_out && !aligned(lse_out, 4)) ||
+      (int8 && !aligned(cache_scale_zero, 8)))
+    return MLA_ERR_INVALID_ARG;
+  if ((long long)max_pages_per_seq * d->page_size > (1LL << 31) - 1) return MLA_ERR_INVALID_ARG;
+  const int S = effective_splits(d, num_splits);
+  if (S <= 0) return MLA_ERR_CUDA;
+  const WorkspaceLayout L = workspace_layout(batch, d->num_heads, S);
+  if (!workspace || !aligned(workspace, 256) || workspace_bytes < L.total) return MLA_ERR_WORKSPACE;
+
+  const int H = d->num_heads, hc = head_chunk(H), groups = H / hc;
+  char* ws = static_cast<char*>(workspace);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+
+  AbsorbParams ap;
+  ap.q_nope = static_cast<const __nv_bfloat16*>(q_nope);
+  ap.q_pe = static_cast<const __nv_bfloat16*>(q_pe);
+  ap.W_UK = static_cast<const __nv_bfloat16*>(W_UK);
+  ap.q_full = reinterpret_cast<__nv_bfloat16*>(ws + L.q_full);
+  ap.q_sum = reinterpret_cast<float*>(ws + L.q_sum);
+  ap.seq_lens = seq_lens;
+  ap.tile_start = reinterpret_cast<int*>(ws + L.tile_start);
+  ap.seg_base = reinterpret_cast<int*>(ws + L.seg_base);
+  ap.len_checked = reinterpret_cast<int*>(ws + L.len_checked);
+  ap.status = reinterpret_cast<int*>(ws + L.status);
+  ap.batch = batch;
+  ap.heads = H;
+  ap.max_len = max_pages_per_seq * d->page_size;
+  ap.num_splits = S;
+  if (launch_absorb(ap, s) != cudaSuccess) return MLA_ERR_CUDA;
+
+  DecodeParams dp;
+  dp.q_full = ap.q_full;
+  dp.q_sum = ap.q_sum;
+  dp.cache = cache;
+  dp.scale_zero = cache_scale_zero;
+  dp.block_table = block_table;
+  dp.tile_start = ap.tile_start;
+  dp.seg_base = ap.seg_base;
+  dp.len = ap.len_checked;
+  dp.partial_o = reinterpret_cast<float*>(ws + L.partial_o);
+  dp.partial_lse = reinterpret_cast<float*>(ws + L.partial_lse);
+  dp.status = ap.status;
+  dp.batch = batch;
+  dp.heads = H;
+  dp.head_group = hc;
+  dp.num_groups = groups;
+  dp.page_size = d->page_size;
+  dp.max_pages = max_pages_per_seq;
+  dp.num_pages = num_pages;
+  dp.num_splits = S;
+  dp.scale_log2 = softmax_scale * kLog2e;
+  const int nsm = sm_count();
+  const int per_group = nsm / groups > 0 ? nsm / groups : 1;
+  const int ctas_per_group = S < per_group ? S : per_group;
+  cudaEvent_t ev0 = g_ev_start.load(), ev1 = g_ev_stop.load();
+  if (ev0 && ev1 && cudaEventRecord(ev0, s) != cudaSuccess) return MLA_ERR_CUDA;
+  if (launch_decode_attention(dp, hc, int8, ctas_per_group * groups, s) != cudaSuccess) return MLA_ERR_CUDA;
+  if (ev0 && ev1 && cudaEventRecord(ev1, s) != cudaSuccess) return MLA_ERR_CUDA;
+
+  CombineUVParams cp;
+  cp.partial_o = dp.partial_o;
+  cp.partial_lse = dp.partial_lse;
+  cp.seg_base = dp.seg_base;
+  cp.W_UV = static_cast<const __nv_bfloat16*>(W_UV);
+  cp.out = static_cast<__nv_bfloat16*>(out);
+  cp.lse_out = lse_out;
+  cp.batch = batch;
+  cp.heads = H;
+  if (launch_combine_uv(cp, s) != cudaSuccess) return MLA_ERR_CUDA;
+  return MLA_OK;
+}
+
+int mla_combine(const mla_dims* d, const float* partial_o, const float* partial_lse, int32_t batch,
+                int32_t num_splits, float* o_lat_out, float* lse_out, mla_stream_t stream) {
+  int st = mla_check_dims(d);
+  if (st != MLA_OK) return st;
+  if (batch <= 0 || num_splits <= 0) return MLA_ERR_INVALID_ARG;
+  if (!partial_o || !partial_lse || !o_lat_out) return MLA_ERR_INVALID_ARG;
+  if (!aligned(partial_o, 4) || !aligned(partial_lse, 4) || !aligned(o_lat_out, 4) || (lse_out && !aligned(lse_out, 4)))
+    return MLA_ERR_INVALID_ARG;
+  CombineParams p;
+  p.partial_o = partial_o;
+  p.partial_lse = partial_lse;
+  p.o_lat = o_lat_out;
+  p.lse_out = lse_out;
+  p.batch = batch;
+  p.splits = num_splits;
+  p.heads = d->num_heads;
+  p.dim = d->kv_lora_rank;
+  return launch_combine(p, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
+int mla_read_status_word(const int32_t* device_status, int32_t* status_out, mla_stream_t stream) {
+  if (!device_status || !status_out) return MLA_ERR_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MLA_ERR_CUDA;
+  if (cudaMemcpy(status_out, device_status, sizeof(int32_t), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return MLA_ERR_CUDA;
+  return MLA_OK;
+}
+
+int mla_read_device_status(const void* workspace, int32_t* status_out, mla_stream_t stream) {
+  if (!workspace) return MLA_ERR_INVALID_ARG;
+  return mla_read_status_word(static_cast<const int32_t*>(workspace), status_out, stream);
+}
+
+int mla_set_timing_events(mla_event_t start, mla_event_t stop) {
+  if ((start == nullptr) != (stop == nullptr)) return MLA_ERR_INVALID_ARG;
+  g_ev_start.store(reinterpret_cast<cudaEvent_t>(start));
+  g_ev_stop.store(reinterpret_cast<cudaEvent_t>(stop));
+  return MLA_OK;
+}
+
+}  // extern "C"

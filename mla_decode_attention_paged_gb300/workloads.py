@@ -59,6 +59,15 @@ WORKLOADS = {
 }
 
 
+def num_splits_for(w: Workload, auto_splits: int) -> int:
+    """KV partitions to run ``w`` with: the automatic count, raised where the
+    workload asks for a minimum number of chunks per sequence (equal-length
+    sequences get num_splits / batch chunks each)."""
+    if w.min_splits_per_seq:
+        return max(auto_splits, w.min_splits_per_seq * w.batch)
+    return 0
+
+
 def generator(seed: int, device="cpu") -> torch.Generator:
     g = torch.Generator(device=device)
     g.manual_seed(seed)

@@ -1,0 +1,100 @@
+"""CPU-only checks of the C ABI: the library builds, loads, exports every
+symbol include/mla.h declares, and rejects bad arguments on the host before
+touching the GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import mla_decode_attention_paged_gb300 as mla
+from mla_decode_attention_paged_gb300 import build as mla_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    mla_build.build()
+    return mla.load_library()
+
+
+def _declared_functions():
+    text = open(os.path.join(ROOT, "include", "mla.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\**\s+\**(mla_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_symbols_exported(lib):
+    declared = _declared_functions()
+    assert len(declared) >= 10, declared
+    assert set(declared) == set(mla.EXPORTED_SYMBOLS)
+    for name in declared:
+        assert hasattr(lib, name), name
+
+
+def test_version_and_status_strings(lib):
+    assert mla.version() >= 100
+    assert mla.status_string(0) == "ok"
+    for s in range(-6, 0):
+        assert mla.status_string(s) != "unknown status"
+
+
+def test_check_dims(lib):
+    assert mla.check_dims(mla.dims(16, 64)) == mla.MLA_OK
+    assert mla.check_dims(mla.dims(128, 16, int8=True)) == mla.MLA_OK
+    assert mla.check_dims(mla.dims(64, 32)) == mla.MLA_OK
+    assert mla.check_dims(mla.dims(24, 64)) == mla.MLA_ERR_UNSUPPORTED
+    assert mla.check_dims(mla.dims(16, 48)) == mla.MLA_ERR_UNSUPPORTED
+    assert mla.check_dims(mla.dims(16, 64, kv_lora_rank=256)) == mla.MLA_ERR_UNSUPPORTED
+    assert mla.check_dims(mla.dims(0, 64)) == mla.MLA_ERR_INVALID_ARG
+    d = mla.dims(16, 64)
+    d.cache_dtype = 7
+    assert mla.check_dims(d) == mla.MLA_ERR_INVALID_ARG
+    assert lib.mla_check_dims(None) == mla.MLA_ERR_INVALID_ARG
+
+
+def test_workspace_size_explicit_splits(lib):
+    d = mla.dims(16, 64)
+    small = lib.mla_decode_workspace_size(ctypes.byref(d), 1, 4)
+    big = lib.mla_decode_workspace_size(ctypes.byref(d), 32, 152)
+    assert 0 < small < big
+    # partials dominate: (splits + batch) * H * 512 fp32
+    assert big >= (152 + 32) * 16 * 512 * 4
+    assert lib.mla_decode_workspace_size(ctypes.byref(d), 0, 4) == 0
+    assert lib.mla_decode_workspace_size(ctypes.byref(d), 4, -1) == 0
+
+
+def test_host_validation_rejects_before_launch(lib):
+    d = mla.dims(16, 64)
+    fake = ctypes.c_void_p(0x10000)  # never dereferenced: validation fails first
+    args = [ctypes.byref(d), fake, fake, fake, None, 4, fake, 8, fake, 2, fake, fake, ctypes.c_float(0.1), 4,
+            fake, ctypes.c_size_t(1 << 30), fake, None, None]
+    a = list(args); a[1] = None                       # q_nope missing
+    assert lib.mla_decode(*a) == mla.MLA_ERR_INVALID_ARG
+    a = list(args); a[9] = 0                          # batch 0
+    assert lib.mla_decode(*a) == mla.MLA_ERR_INVALID_ARG
+    a = list(args); a[12] = ctypes.c_float(-1.0)      # negative scale
+    assert lib.mla_decode(*a) == mla.MLA_ERR_INVALID_ARG
+    a = list(args); a[3] = ctypes.c_void_p(0x10008)   # cache not 16-byte aligned
+    assert lib.mla_decode(*a) == mla.MLA_ERR_INVALID_ARG
+    a = list(args); a[14] = ctypes.c_void_p(0x10040)  # workspace not 256-byte aligned
+    assert lib.mla_decode(*a) == mla.MLA_ERR_WORKSPACE
+    a = list(args); a[15] = ctypes.c_size_t(16)       # workspace too small
+    assert lib.mla_decode(*a) == mla.MLA_ERR_WORKSPACE
+    di = mla.dims(16, 64, int8=True)
+    a = list(args); a[0] = ctypes.byref(di)           # INT8 without scale/zero array
+    assert lib.mla_decode(*a) == mla.MLA_ERR_INVALID_ARG
+    # append
+    assert lib.mla_cache_append(ctypes.byref(d), None, None, 4, fake, 2, 8, fake, fake, 3, fake, fake,
+                                ctypes.c_double(1e4), None, None) == mla.MLA_ERR_INVALID_ARG
+    assert lib.mla_cache_append(ctypes.byref(d), fake, None, 4, fake, 2, 8, fake, fake, 0, fake, fake,
+                                ctypes.c_double(1e4), None, None) == mla.MLA_OK  # no tokens: no-op
+    assert lib.mla_cache_append(ctypes.byref(di), fake, None, 4, fake, 2, 8, fake, fake, 3, fake, fake,
+                                ctypes.c_double(1e4), None, None) == mla.MLA_ERR_INVALID_ARG
+    # combine
+    assert lib.mla_combine(ctypes.byref(d), fake, fake, 2, 0, fake, None, None) == mla.MLA_ERR_INVALID_ARG
+    assert lib.mla_combine(ctypes.byref(d), None, fake, 2, 3, fake, None, None) == mla.MLA_ERR_INVALID_ARG
+    # timing hook: both or neither
+    assert lib.mla_set_timing_events(fake, None) == mla.MLA_ERR_INVALID_ARG
+    assert lib.mla_set_timing_events(None, None) == mla.MLA_OK

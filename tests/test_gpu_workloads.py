@@ -1,0 +1,55 @@
+"""Parity at the full sizes of the five benchmark workloads, in the launch
+configuration bench.py times.  The oracle cannot evaluate every output at
+these sizes, so each test checks a seeded sample of sequences: the
+un-absorbed oracle on some heads of each sampled sequence, and the absorbed
+fp64 form (pinned to the un-absorbed one in test_oracle.py) on all heads."""
+import numpy as np
+import pytest
+import torch
+
+import mla_decode_attention_paged_gb300 as mla
+from mla_decode_attention_paged_gb300 import workloads as W
+from harness import assert_parity, dims_of, gpu_cache, gpu_decode, oracle_cache, oracle_decode
+
+pytestmark = pytest.mark.gpu
+
+# workload key -> (sampled sequences rule, un-absorbed heads per sampled sequence)
+SAMPLES = {
+    "tiny": (None, None),
+    "v2lite": ([0, 31], None),
+    "ctx1m": ([1], [0, 15]),
+    "ragged": ("longest+3", [0, 37, 64, 127]),
+    "int8": ([0, 57, 127], [0, 31, 96, 127]),
+}
+
+
+def _sample_seqs(rule, seq_lens, batch):
+    if rule is None:
+        return list(range(batch))
+    if rule == "longest+3":
+        lens = seq_lens.cpu().numpy()
+        g = np.random.default_rng(2024)
+        others = g.choice([b for b in range(batch) if b != int(lens.argmax())], 3, replace=False)
+        return sorted({int(lens.argmax()), *map(int, others)})
+    return rule
+
+
+@pytest.mark.parametrize("key", ["tiny", "v2lite", "ctx1m", "ragged", "int8"])
+def test_full_size_workload(cuda_lib, key):
+    w = W.WORKLOADS[key]
+    inp = W.make_decode_inputs(w, device="cuda")
+    cache, sz = gpu_cache(inp, w)
+    splits = W.num_splits_for(w, mla.auto_num_splits(dims_of(w), w.batch))
+    out, lse = gpu_decode(inp, w, cache, sz, num_splits=splits)
+    del cache, sz
+    torch.cuda.empty_cache()
+    rule, heads = SAMPLES[key]
+    seqs = _sample_seqs(rule, inp["seq_lens"], w.batch)
+    oc = oracle_cache(inp, w, seqs)
+    all_pairs = [(b, h) for b in seqs for h in range(w.heads)]
+    un_pairs = all_pairs if heads is None else [(b, h) for b in seqs for h in heads]
+    ref_o, ref_l = oracle_decode(inp, w, un_pairs, cache_override=oc)
+    assert_parity(out, lse, ref_o, ref_l, un_pairs, w.name + " (un-absorbed oracle)")
+    if heads is not None:
+        ref_o, ref_l = oracle_decode(inp, w, all_pairs, absorbed=True, cache_override=oc)
+        assert_parity(out, lse, ref_o, ref_l, all_pairs, w.name + " (absorbed oracle, all heads)")
