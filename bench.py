@@ -1,0 +1,366 @@
+"""Benchmark of one decode step of paged MLA attention on GB300.
+
+A step is the whole hot path for one layer: append the new token of every
+sequence into the paged cache (mla_cache_append), then mla_decode (query
+absorption, split-KV tensor-core attention, LSE combine + W^UV projection).
+Inputs are seeded synthetic tensors of the workload's shapes, resident in HBM
+before timing; the cache is larger than L2, so no flush is needed between
+steps.  Prints one JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload v2lite]
+  python bench.py --impl reference ...   # the fp64 oracle on the host cores
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MLA decode tokens/s and latent-cache HBM GB/s (fraction of 8 TB/s), 1×GB300"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="v2lite")
+    ap.add_argument("--num-splits", type=int, default=None)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    return ap.parse_args()
+
+
+def dist_setup(n):
+    import torch
+    rank, world = int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1))
+    if world > 1:
+        import torch.distributed as dist
+        local = int(os.environ.get("LOCAL_RANK", 0))
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    return rank, world
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_traffic(workload_name: str, tokens: int):
+    """DRAM bytes per attention launch from the committed ncu summary, scaled
+    to this launch's tokens; None if absent or taken on a different kernel."""
+    path = os.path.join(ROOT, "profiles", "attention_dram_traffic.json")
+    if not os.path.exists(path):
+        return None
+    d = json.load(open(path))
+    src = os.path.join(ROOT, "mla_decode_attention_paged_gb300", "csrc", "decode_tc.cu")
+    if hashlib.sha256(open(src, "rb").read()).hexdigest() != d.get("kernel_sha256"):
+        return None
+    e = d.get("workloads", {}).get(workload_name)
+    if not e:
+        return None
+    return e["dram_bytes_per_token"] * tokens
+
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in getattr(self, "lines", []):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 7:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx.append(float(f[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[3:7]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def cpu_baseline(w, inp, seconds):
+    """The fp64 oracle as it stands, on the host cores, over whole sequences
+    (all heads) of this workload until about `seconds` have passed."""
+    import numpy as np
+    import oracle as O
+    from mla_decode_attention_paged_gb300 import workloads as W
+    try:
+        from threadpoolctl import threadpool_info
+        cores = max([i.get("num_threads", 0) for i in threadpool_info()] + [1])
+    except Exception:
+        cores = os.cpu_count()
+    f64 = lambda t: O.bf16_bits_to_f64(W.bf16_to_bits(t))
+    qn, qp, wk, wv = f64(inp["q_nope"]), f64(inp["q_pe"]), f64(inp["W_UK"]), f64(inp["W_UV"])
+    table = inp["block_table"].cpu().numpy()
+    lens = inp["seq_lens"].cpu().numpy()
+    import torch
+    done, el, tokens_attended = 0, 0.0, 0
+    while el < seconds:
+        b = done % w.batch
+        n = (int(lens[b]) + w.page_size - 1) // w.page_size
+        tab = np.full_like(table, -1)
+        tab[b, :n] = np.arange(n)
+        if w.int8 and "src_c_kv" in inp:   # the oracle's own append builds this sequence's pages
+            a = int(lens[:b].sum())
+            cache = np.zeros((n, w.page_size, 576), np.int8)
+            sz = np.zeros((n, w.page_size, 2), np.float32)
+            O.append_tokens(cache, sz, tab, [b] * int(lens[b]), list(range(int(lens[b]))),
+                            W.bf16_to_bits(inp["src_c_kv"][a:a + int(lens[b])]),
+                            W.bf16_to_bits(inp["src_k_pe"][a:a + int(lens[b])]), w.rope_theta, w.page_size, True)
+        else:
+            idx = torch.as_tensor(table[b, :n].astype(np.int64), device=inp["cache_dev"].device)
+            sub = inp["cache_dev"].index_select(0, idx)
+            if w.int8:
+                cache, sz = sub.cpu().numpy(), inp["sz_dev"].index_select(0, idx).cpu().numpy()
+            else:
+                cache, sz = W.bf16_to_bits(sub), None
+        t_start = time.perf_counter()   # time the oracle itself, not the page gather
+        O.decode(qn, qp, cache, sz, tab, lens, wk, wv, inp["scale"], w.page_size, w.int8,
+                 pairs=[(b, h) for h in range(w.heads)])
+        el += time.perf_counter() - t_start
+        done += 1
+        tokens_attended += int(lens[b])
+    return {"value": done / el, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"{done} whole sequence(s) x {w.heads} heads of {w.name} ({tokens_attended} cached tokens, "
+                      f"un-absorbed fp64 oracle), {el:.1f} s"}
+
+
+def run_ours(args, rank, world):
+    import torch
+    import mla_decode_attention_paged_gb300 as mla
+    from mla_decode_attention_paged_gb300 import workloads as W
+
+    dev = torch.device("cuda", torch.cuda.current_device())
+    mla.load_library(build_if_missing=True)
+    w = W.WORKLOADS[args.workload]
+    inp = W.make_decode_inputs(w, device=dev)
+    d = mla.dims(w.heads, w.page_size, int8=w.int8)
+    B, H = w.batch, w.heads
+    seq_lens = inp["seq_lens"]
+    table = inp["block_table"].to(dev)
+    npg = inp["num_pages"]
+    # the cache: drawn directly (bf16) or written through the library's append (INT8)
+    if w.int8:
+        cache = torch.zeros((npg, w.page_size, 576), dtype=torch.int8, device=dev)
+        sz = torch.zeros((npg, w.page_size, 2), dtype=torch.float32, device=dev)
+        mla.cache_append(d, cache, sz, table, inp["src_seq_ids"], inp["src_positions"], inp["src_c_kv"],
+                         inp["src_k_pe"], w.rope_theta)
+        del inp["src_c_kv"], inp["src_k_pe"]
+    else:
+        cache, sz = inp["cache"], None
+    inp["cache_dev"], inp["sz_dev"] = cache, sz
+    # the step's new token per sequence: the last position of each sequence
+    g = W.generator(w.seed + 1000, dev)
+    new_c = W.draw_bf16((B, 512), 1.0, g)
+    new_k = W.draw_bf16((B, 64), 1.0, g)
+    seq_ids = torch.arange(B, dtype=torch.int32, device=dev)
+    positions = (seq_lens.to(dev) - 1).clamp(min=0).to(torch.int32)
+    auto = mla.auto_num_splits(d, B)
+    splits = args.num_splits if args.num_splits is not None else (W.num_splits_for(w, auto) or auto)
+    ws = torch.empty(mla.decode_workspace_size(d, B, splits), dtype=torch.uint8, device=dev)
+    out = torch.empty((B, H, 128), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((B, H), dtype=torch.float32, device=dev)
+    q_nope, q_pe, W_UK, W_UV = inp["q_nope"], inp["q_pe"], inp["W_UK"], inp["W_UV"]
+    seq_lens = seq_lens.to(dev)
+
+    def step():
+        mla.cache_append(d, cache, sz, table, seq_ids, positions, new_c, new_k, w.rope_theta)
+        mla.decode(d, q_nope, q_pe, cache, sz, table, seq_lens, W_UK, W_UV, inp["scale"], num_splits=splits,
+                   workspace=ws, out=out, lse_out=lse)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert mla.read_device_status(ws) == mla.MLA_OK
+    # attention-kernel timing through the library's event hook, one pair per step
+    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for a, b in kev:  # create the underlying events
+        a.record(); b.record()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(dev.index) as clk:
+        e0.record()
+        for i in range(args.steps):
+            mla.set_timing_events(*kev[i])
+            step()
+        e1.record()
+        torch.cuda.synchronize()
+    mla.set_timing_events(None, None)
+    if world > 1:
+        torch.distributed.barrier()
+    ms_total = e0.elapsed_time(e1)
+    kern_ms = statistics.mean(a.elapsed_time(b) for a, b in kev)
+    if world > 1:
+        t = torch.tensor([ms_total], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_total = float(t.item())
+    ms = ms_total / args.steps
+    lens_sum = int(seq_lens.to(torch.int64).sum())
+    bytes_per_token = 584 if w.int8 else 1152
+    cache_bytes = lens_sum * bytes_per_token
+    tokens_per_s = B * world / (ms / 1e3)
+    step_cache_gbs = cache_bytes / (ms / 1e3) / 1e9
+
+    # e2e: the same step through the public API from pinned host buffers
+    pin = lambda t: t.cpu().pin_memory()
+    h_in = {k: pin(v) for k, v in dict(q_nope=q_nope, q_pe=q_pe, new_c=new_c, new_k=new_k, seq_ids=seq_ids,
+                                       positions=positions, table=table, seq_lens=seq_lens).items()}
+    d_in = {k: torch.empty_like(v, device=dev) for k, v in h_in.items()}
+    h_out = torch.empty((B, H, 128), dtype=torch.bfloat16).pin_memory()
+    h_lse = torch.empty((B, H), dtype=torch.float32).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in h_in.values())
+    d2h = h_out.numel() * 2 + h_lse.numel() * 4
+
+    def e2e_step():
+        for k in h_in:
+            d_in[k].copy_(h_in[k], non_blocking=True)
+        mla.cache_append(d, cache, sz, d_in["table"], d_in["seq_ids"], d_in["positions"], d_in["new_c"],
+                         d_in["new_k"], w.rope_theta)
+        mla.decode(d, d_in["q_nope"], d_in["q_pe"], cache, sz, d_in["table"], d_in["seq_lens"], W_UK, W_UV,
+                   inp["scale"], num_splits=splits, workspace=ws, out=out, lse_out=lse)
+        h_out.copy_(out, non_blocking=True)
+        h_lse.copy_(lse, non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    torch.cuda.synchronize()
+    x0, x1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    x0.record()
+    for _ in range(args.steps):
+        e2e_step()
+    x1.record()
+    torch.cuda.synchronize()
+    e2e_ms = x0.elapsed_time(x1) / args.steps
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    peak, peak_src = peaks()
+    achieved = cache_bytes / (kern_ms / 1e3) / 1e9
+    traffic = kernel_traffic(w.name, lens_sum)
+    res = {
+        "metric": METRIC, "value": round(tokens_per_s, 1), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "int8" if w.int8 else "bf16",
+        "data": "synthetic (seeded; random-init weights of DeepSeek-V2 MLA shapes)",
+        "config": {"workload": w.name, "batch": B, "heads": H, "context": w.context, "page_size": w.page_size,
+                   "num_splits": splits, "cache_bytes": cache_bytes,
+                   "l2": "inputs larger than L2 (no flush): the cache read each step exceeds the 126 MB L2"
+                   if cache_bytes > 200e6 else "cache smaller than L2",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "cache_gbs": round(step_cache_gbs, 1),
+        "frac_of_8tbs": round(step_cache_gbs / NOMINAL_HBM_GBS, 4),
+        "attention_kernel_ms": round(kern_ms, 5),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "peak_source": peak_src,
+                     "traffic": traffic, "kernel": "decode_tc_kernel (split-KV attention)",
+                     "algorithmic_bytes_per_launch": cache_bytes},
+        "e2e": {"value": round(B * world / (e2e_ms / 1e3), 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 5)},
+        "gpu_launches": 4 * args.steps,
+        "clocks": clk.summary(),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = cpu_baseline(w, inp, args.cpu_seconds)
+    return res
+
+
+def run_reference(args, rank, world):
+    """The oracle (the reference arm): bounded samples of the same workload on the host cores."""
+    import torch
+    import oracle as O  # noqa: F401
+    from mla_decode_attention_paged_gb300 import workloads as W
+    if rank != 0:
+        return None
+    w = W.WORKLOADS[args.workload]
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    inp = W.make_decode_inputs(w.scaled(batch=min(w.batch, 4)) if w.int8 else w, device=dev)
+    inp["cache_dev"], inp["sz_dev"] = inp.get("cache"), None
+    per_step = max(1.0, min(6.0, 150.0 / max(args.steps + args.warmup, 1)))
+    for _ in range(args.warmup):
+        cpu_baseline(w, inp, per_step * 0.2)
+    vals, samples = [], []
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        r = cpu_baseline(w, inp, per_step)
+        vals.append(1.0 / r["value"])
+        samples.append(r["sample"])
+    el = time.perf_counter() - t0
+    v = args.steps / sum(vals)
+    cb = {"value": round(v, 5), "unit": "tokens/s", "cores": r["cores"], "kind": "oracle",
+          "sample": f"per step: {samples[0]}"}
+    return {"metric": METRIC, "value": round(v, 5), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(1e3 * el / args.steps, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+            "config": {"workload": w.name, "batch": w.batch, "heads": w.heads, "context": w.context,
+                       "page_size": w.page_size}, "impl": "reference", "cpu_baseline": cb,
+            "e2e": {"value": round(v, 5), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse()
+    rank, world = dist_setup(args.gpus)
+    res = run_reference(args, rank, world) if args.impl == "reference" else run_ours(args, rank, world)
+    if rank == 0 and res is not None:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

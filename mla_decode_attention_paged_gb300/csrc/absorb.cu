@@ -47,7 +47,9 @@ __device__ void compute_plan(const AbsorbParams& p) {
     carry = 0;
   }
   __syncthreads();
-  const long long W = p.tile_start[p.batch], S = p.num_splits;
+  const long long W = p.tile_start[p.batch];
+  const long long S = p.num_splits < W ? p.num_splits : (W > 0 ? W : 1);
+  if (threadIdx.x == 0) p.status[1] = int(S);  // effective split count, read by the later kernels
   // pass 2: segments per sequence (partitions its tiles touch) -> seg_base
   for (int base = 0; base < p.batch; base += blockDim.x) {
     const int b = base + threadIdx.x;

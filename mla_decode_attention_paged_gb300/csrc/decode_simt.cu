@@ -17,10 +17,10 @@ __global__ void __launch_bounds__(256) decode_simt_kernel(DecodeParams p) {
   float* rowscale = reinterpret_cast<float*>(rowidx + kTile);  // [128][2] (INT8)
 
   const int G = p.num_groups, g = blockIdx.x % G, cp = blockIdx.x / G, Cp = gridDim.x / G;
-  const long long S = p.num_splits;
+  const long long S = p.status[1];  // effective split count from the plan
   const long long pa = (cp * S) / Cp, pb = ((cp + 1) * S) / Cp;
   TileWalker walk;
-  walk.init(p.tile_start, p.seg_base, p.len, p.batch, p.num_splits, pa, pb);
+  walk.init(p.tile_start, p.seg_base, p.len, p.batch, int(S), pa, pb);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int h0 = g * HC;
   float acc_o[HC][2];
@@ -180,7 +180,7 @@ static cudaError_t launch_simt_t(const DecodeParams& p, int grid, cudaStream_t s
   return cudaGetLastError();
 }
 
-cudaError_t launch_decode_attention(const DecodeParams& p, int hc, bool int8, int grid, cudaStream_t stream) {
+cudaError_t launch_decode_simt(const DecodeParams& p, int hc, bool int8, int grid, cudaStream_t stream) {
   if (hc == 16) return int8 ? launch_simt_t<16, true>(p, grid, stream) : launch_simt_t<16, false>(p, grid, stream);
   return int8 ? launch_simt_t<32, true>(p, grid, stream) : launch_simt_t<32, false>(p, grid, stream);
 }

@@ -1,0 +1,459 @@
+// decode_tc.cu -- split-KV MLA decode attention on the sm_100-family tensor
+// cores (tcgen05 + TMEM), fed by TMA.
+//
+// What it computes ("The Weight Absorption Trick"; "Seven Ways LLMs Handle
+// Attention", section 5; "Flash-Decoding and FlashInfer"): for one head group
+// of one sequence and one contiguous range of its tokens, with
+// q_full[h] = [W^UK_h^T q_nope_h | q_pe_h] (576 wide) and the cached rows
+// c_t = [latent | RoPE key] (576 wide),
+//     s[t][h] = scale * q_full[h] . c_t          (all heads share the row)
+//     o_lat[h] = sum_t softmax(s[., h])_t * c_t[0:512]
+// and emits o_lat (normalised within the range) with the range's lse.
+//
+// Orientation: both products are taken transposed so that the 128 tokens of
+// a tile are the MMA's M extent and the heads its N extent, so no head is
+// padded (16 or 32 heads per CTA):
+//     S^T [128 tok x HC]  = C_tile [128 x 576]  * Q^T       (A K-major)
+//     O^T [512 x HC]     += C_tile^T [512 x 128] * P^T      (A MN-major)
+// The same swizzled shared-memory tile, loaded once by TMA, is the A operand
+// of both products; each page is read from HBM once for all heads of the group.
+//
+// Warp roles (256 threads):
+//   warp 0     TMA producer: Q of each segment, then each tile's pages
+//              (4 "pair" slots of two 64-wide latent boxes + 1 RoPE slot)
+//   warp 1     TMEM allocation; lane 0 issues the MMAs
+//   warps 4-7  softmax (one thread per token row of S^T) and epilogue
+// Every wait is bounded: on timeout the CTA records MLA_ERR_DEVICE_TIMEOUT,
+// drains, frees its tensor memory and returns.
+#include "blackwell_ptx.cuh"
+#include "params.cuh"
+
+namespace mla {
+namespace {
+
+using namespace ptx;
+
+constexpr int kThreads = 256;
+constexpr uint32_t kBoxBytes = 16384;           // 128 rows x 128 B (64 bf16)
+constexpr uint32_t kPairBytes = 2 * kBoxBytes;  // latent dims [128c, 128c + 128)
+constexpr int kNumRope = 2;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+constexpr float kRescaleThreshold = 8.f;        // log2 units
+
+template <int HC>
+struct Cfg {
+  static constexpr int kNumPair = HC == 16 ? 5 : 4;
+  static constexpr uint32_t kQBytes = 9 * HC * 128;
+  static constexpr uint32_t kPBytes = kTile * HC * 2;
+  static constexpr uint32_t kOffPair = 0;
+  static constexpr uint32_t kOffRope = kOffPair + kNumPair * kPairBytes;
+  static constexpr uint32_t kOffQ = kOffRope + kNumRope * kBoxBytes;
+  static constexpr uint32_t kOffP = kOffQ + kQBytes;
+  static constexpr uint32_t kOffMisc = kOffP + 2 * kPBytes;
+  static constexpr uint32_t kMiscBytes = 2048;
+  static constexpr uint32_t kSmem = kOffMisc + kMiscBytes + 1024;  // +1024: base alignment slack
+  static constexpr uint32_t kTmemCols = HC == 16 ? 128 : 256;      // S^T x2 + O^T x4 = 6 * HC
+  static constexpr uint32_t kColS = 0;                             // + buf * HC
+  static constexpr uint32_t kColO = 2 * HC;                        // + c * HC
+};
+
+struct Barriers {
+  uint64_t full_pair[5], empty_pair[5], full_rope[kNumRope], empty_rope[kNumRope];
+  uint64_t q_full, q_empty, s_full[2], p_full[2], o_full, o_free, drain;
+  uint32_t tmem_base;
+  int abort;
+};
+
+__device__ __forceinline__ bool bar_any(bool pred) {  // OR over the 128 softmax threads (named barrier 1)
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, 1, 128, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(uint32_t(pred))
+      : "memory");
+  return r != 0;
+}
+
+__device__ __forceinline__ void fail(Barriers* B, int* status) {
+  B->abort = 1;
+  set_status(status, MLA_ERR_DEVICE_TIMEOUT);
+}
+
+template <int HC>
+__global__ void __launch_bounds__(kThreads, 1)
+    decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_cache, const __grid_constant__ CUtensorMap tmap_q,
+                     DecodeParams p) {
+  using C = Cfg<HC>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  Barriers* B = reinterpret_cast<Barriers*>(smem + C::kOffMisc);
+  float* red = reinterpret_cast<float*>(smem + C::kOffMisc + 512);  // [2][4][HC] then [4][HC] for l
+  const uint32_t sbase = smem_u32(smem);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < C::kNumPair; ++i) {
+      mbar_init(&B->full_pair[i], 1);
+      mbar_init(&B->empty_pair[i], 1);
+    }
+    for (int i = 0; i < kNumRope; ++i) {
+      mbar_init(&B->full_rope[i], 1);
+      mbar_init(&B->empty_rope[i], 1);
+    }
+    mbar_init(&B->q_full, 1);
+    mbar_init(&B->q_empty, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&B->s_full[i], 1);
+      mbar_init(&B->p_full[i], 128);
+    }
+    mbar_init(&B->o_full, 1);
+    mbar_init(&B->o_free, 128);
+    mbar_init(&B->drain, 1);
+    B->abort = 0;
+    fence_mbar_init();
+    prefetch_tensormap(&tmap_cache);
+    prefetch_tensormap(&tmap_q);
+  }
+  if (warp == 1) {
+    tmem_alloc(&B->tmem_base, C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = B->tmem_base;
+
+  const int G = p.num_groups, g = blockIdx.x % G, cp = blockIdx.x / G, Cp = gridDim.x / G;
+  const long long S = p.status[1];  // effective split count from the plan
+  const long long pa = (cp * S) / Cp, pb = ((cp + 1) * S) / Cp;
+  const volatile int* abort_flag = &B->abort;
+
+  if (warp == 0 && lane == 0) {
+    // ------------------------------------------------------------ producer
+    TileWalker walk;
+    walk.init(p.tile_start, p.seg_base, p.len, p.batch, int(S), pa, pb);
+    const int P = p.page_size, pages_per_tile = kTile / P;
+    const uint32_t box_bytes_per_page = uint32_t(P) * 128;
+    uint32_t pair_it = 0, rope_it = 0, seg = 0;
+    TileInfo t;
+    while (walk.next(t)) {
+      if (t.first) {
+        if (seg > 0 && !mbar_wait(&B->q_empty, (seg - 1) & 1, abort_flag, kWaitLimitNs)) { fail(B, p.status); break; }
+        mbar_arrive_expect_tx(&B->q_full, C::kQBytes);
+        const int qrow = t.b * p.heads + g * HC;
+        for (int j = 0; j < 9; ++j) tma_load_2d(smem + C::kOffQ + j * HC * 128, &tmap_q, 64 * j, qrow, &B->q_full);
+        ++seg;
+      }
+      const int npg = (t.valid + P - 1) / P;
+      int rows[kTile / 16];
+      for (int i = 0; i < npg; ++i) {
+        int pg = p.block_table[size_t(t.b) * p.max_pages + t.tile * pages_per_tile + i];
+        if (pg < 0 || pg >= p.num_pages) {
+          set_status(p.status, MLA_ERR_DEVICE_BOUNDS);
+          pg = 0;  // stay in bounds; this sequence's result is unspecified
+        }
+        rows[i] = pg * P;
+      }
+      bool ok = true;
+      for (int c = 0; c < 4 && ok; ++c, ++pair_it) {
+        const uint32_t slot = pair_it % C::kNumPair;
+        if (!mbar_wait(&B->empty_pair[slot], ((pair_it / C::kNumPair) & 1) ^ 1, abort_flag, kWaitLimitNs)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(&B->full_pair[slot], 2 * npg * box_bytes_per_page);
+        uint8_t* dst = smem + C::kOffPair + slot * kPairBytes;
+        for (int i = 0; i < npg; ++i) {
+          tma_load_2d(dst + i * box_bytes_per_page, &tmap_cache, 128 * c, rows[i], &B->full_pair[slot]);
+          tma_load_2d(dst + kBoxBytes + i * box_bytes_per_page, &tmap_cache, 128 * c + 64, rows[i],
+                      &B->full_pair[slot]);
+        }
+      }
+      if (!ok) { fail(B, p.status); break; }
+      {
+        const uint32_t slot = rope_it % kNumRope;
+        if (!mbar_wait(&B->empty_rope[slot], ((rope_it / kNumRope) & 1) ^ 1, abort_flag, kWaitLimitNs)) {
+          fail(B, p.status);
+          break;
+        }
+        mbar_arrive_expect_tx(&B->full_rope[slot], npg * box_bytes_per_page);
+        uint8_t* dst = smem + C::kOffRope + slot * kBoxBytes;
+        for (int i = 0; i < npg; ++i)
+          tma_load_2d(dst + i * box_bytes_per_page, &tmap_cache, kLatent, rows[i], &B->full_rope[slot]);
+        ++rope_it;
+      }
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ------------------------------------------------------------ MMA issuer
+    TileWalker walk;
+    walk.init(p.tile_start, p.seg_base, p.len, p.batch, int(S), pa, pb);
+    constexpr uint32_t id_qk = idesc_bf16_f32(128, HC, false, false);
+    constexpr uint32_t id_pv = idesc_bf16_f32(128, HC, true, true);
+    uint32_t pair_it = 0, rope_it = 0, tile_i = 0, seg = 0;
+    TileInfo t;
+    bool ok = true;
+    while (ok && walk.next(t)) {
+      const uint32_t buf = tile_i & 1;
+      if (t.first && !(ok = mbar_wait(&B->q_full, seg & 1, abort_flag, kWaitLimitNs))) break;
+      tc_fence_after();
+      const uint32_t d_s = tmem + C::kColS + buf * HC;
+      for (int c = 0; c < 4; ++c) {
+        const uint32_t it = pair_it + c, slot = it % C::kNumPair;
+        if (!(ok = mbar_wait(&B->full_pair[slot], (it / C::kNumPair) & 1, abort_flag, kWaitLimitNs))) break;
+        tc_fence_after();
+        for (int half = 0; half < 2; ++half) {
+          const int j = 2 * c + half;
+          const uint32_t a0 = sbase + C::kOffPair + slot * kPairBytes + half * kBoxBytes;
+          const uint32_t b0 = sbase + C::kOffQ + j * HC * 128;
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            mma_bf16(d_s, smem_desc(a0 + 32 * k, 16, 1024, kSwizzle128B), smem_desc(b0 + 32 * k, 16, 1024, kSwizzle128B),
+                     id_qk, (j | k) != 0);
+        }
+      }
+      if (!ok) break;
+      const uint32_t rslot = rope_it % kNumRope;
+      if (!(ok = mbar_wait(&B->full_rope[rslot], (rope_it / kNumRope) & 1, abort_flag, kWaitLimitNs))) break;
+      tc_fence_after();
+      {
+        const uint32_t a0 = sbase + C::kOffRope + rslot * kBoxBytes;
+        const uint32_t b0 = sbase + C::kOffQ + 8 * HC * 128;
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          mma_bf16(d_s, smem_desc(a0 + 32 * k, 16, 1024, kSwizzle128B), smem_desc(b0 + 32 * k, 16, 1024, kSwizzle128B),
+                   id_qk, 1);
+      }
+      mma_commit(&B->s_full[buf]);
+      mma_commit(&B->empty_rope[rslot]);
+      ++rope_it;
+      if (t.last) mma_commit(&B->q_empty);
+      // PV: O^T[c] (+)= C_tile^T[128c .. 128c + 128) * P^T
+      if (!(ok = mbar_wait(&B->p_full[buf], (tile_i >> 1) & 1, abort_flag, kWaitLimitNs))) break;
+      if (t.first && seg > 0 && !(ok = mbar_wait(&B->o_free, (seg - 1) & 1, abort_flag, kWaitLimitNs))) break;
+      tc_fence_after();
+      const int nk = (t.valid + 15) >> 4;
+      const uint32_t pbase = sbase + C::kOffP + buf * C::kPBytes;
+      for (int c = 0; c < 4; ++c) {
+        const uint32_t slot = (pair_it + c) % C::kNumPair;
+        const uint32_t a0 = sbase + C::kOffPair + slot * kPairBytes;
+        for (int k = 0; k < nk; ++k)
+          mma_bf16(tmem + C::kColO + c * HC, smem_desc(a0 + 2048 * k, kBoxBytes, 1024, kSwizzle128B),
+                   smem_desc(pbase + 256 * k, 128, 2048, kSwizzleNone), id_pv, !(t.first && k == 0));
+        mma_commit(&B->empty_pair[slot]);
+      }
+      pair_it += 4;
+      if (t.last) {
+        mma_commit(&B->o_full);
+        ++seg;
+      }
+      ++tile_i;
+    }
+    if (!ok) fail(B, p.status);
+    // all issued MMAs complete before teardown
+    mma_commit(&B->drain);
+    mbar_wait(&B->drain, 0, abort_flag, kWaitLimitNs);
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ softmax / epilogue
+    const int q4 = warp - 4, st = threadIdx.x - 128;  // st = token row of S^T = TMEM lane
+    const uint32_t lane_off = uint32_t(q4 * 32) << 16;
+    TileWalker walk;
+    walk.init(p.tile_start, p.seg_base, p.len, p.batch, int(S), pa, pb);
+    float m_run[HC], l_run[HC];
+    uint32_t pair_it = 0, tile_i = 0, seg = 0;
+    TileInfo t;
+    while (walk.next(t)) {
+      const uint32_t buf = tile_i & 1;
+      const bool ok = mbar_wait(&B->s_full[buf], (tile_i >> 1) & 1, abort_flag, kWaitLimitNs);
+      tc_fence_after();
+      float x[HC];
+      if (ok) {
+#pragma unroll
+        for (int h0 = 0; h0 < HC; h0 += 16) {
+          float v[16];
+          tmem_ld16(tmem + lane_off + C::kColS + buf * HC + h0, v);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) x[h0 + i] = v[i];
+        }
+      }
+      const bool valid = st < t.valid;
+#pragma unroll
+      for (int h = 0; h < HC; ++h) x[h] = valid ? x[h] * p.scale_log2 : -INFINITY;
+      // tile max per head: warp butterfly, then across the 4 warps through shared memory
+      float* rm = red + buf * 4 * HC;
+#pragma unroll
+      for (int h = 0; h < HC; ++h) {
+        float v = x[h];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+        if (lane == (h & 31)) rm[q4 * HC + h] = v;
+      }
+      if (bar_any(!ok)) break;
+      float alpha[HC];
+      bool rescale = false;
+#pragma unroll
+      for (int h = 0; h < HC; ++h) {
+        const float mt = fmaxf(fmaxf(rm[h], rm[HC + h]), fmaxf(rm[2 * HC + h], rm[3 * HC + h]));
+        if (t.first) {
+          m_run[h] = mt;
+          l_run[h] = 0.f;
+          alpha[h] = 1.f;
+        } else if (mt > m_run[h] + kRescaleThreshold) {
+          alpha[h] = exp2f(m_run[h] - mt);
+          m_run[h] = mt;
+          l_run[h] *= alpha[h];
+          rescale = true;
+        } else {
+          alpha[h] = 1.f;
+        }
+      }
+      if (rescale) {  // uniform across the 128 threads; PV of the previous tile is complete
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int h0 = 0; h0 < HC; h0 += 16) {
+            float v[16];
+            const uint32_t a = tmem + lane_off + C::kColO + c * HC + h0;
+            tmem_ld16(a, v);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) v[i] *= alpha[h0 + i];
+            tmem_st16(a, v);
+          }
+        tmem_st_wait();
+      }
+      // probabilities -> P^T (bf16, MN-major, no swizzle: 8x8 core matrices)
+      uint8_t* pt = smem + C::kOffP + buf * C::kPBytes;
+#pragma unroll
+      for (int h0 = 0; h0 < HC; h0 += 8) {
+        uint32_t packed[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const __nv_bfloat16 lo = __float2bfloat16_rn(exp2f(x[h0 + 2 * i] - m_run[h0 + 2 * i]));
+          const __nv_bfloat16 hi = __float2bfloat16_rn(exp2f(x[h0 + 2 * i + 1] - m_run[h0 + 2 * i + 1]));
+          l_run[h0 + 2 * i] += __bfloat162float(lo);
+          l_run[h0 + 2 * i + 1] += __bfloat162float(hi);
+          packed[i] = uint32_t(__bfloat16_as_ushort(lo)) | (uint32_t(__bfloat16_as_ushort(hi)) << 16);
+        }
+        *reinterpret_cast<uint4*>(pt + (h0 / 8) * 2048 + (st / 8) * 128 + (st % 8) * 16) =
+            make_uint4(packed[0], packed[1], packed[2], packed[3]);
+      }
+      // ragged tail: rows [valid, ceil16(valid)) of the latent boxes feed the
+      // last PV k-step with zero weight; make them finite zeros
+      if (st >= t.valid && st < ((t.valid + 15) & ~15)) {
+        for (int c = 0; c < 4; ++c) {
+          uint8_t* row = smem + C::kOffPair + ((pair_it + c) % C::kNumPair) * kPairBytes + st * 128;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            reinterpret_cast<uint4*>(row)[i] = make_uint4(0, 0, 0, 0);
+            reinterpret_cast<uint4*>(row + kBoxBytes)[i] = make_uint4(0, 0, 0, 0);
+          }
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(&B->p_full[buf]);
+      pair_it += 4;
+      ++tile_i;
+      if (t.last) {
+        const bool ok2 = mbar_wait(&B->o_full, seg & 1, abort_flag, kWaitLimitNs);
+        tc_fence_after();
+        float* rl = red + 8 * HC;
+#pragma unroll
+        for (int h = 0; h < HC; ++h) {
+          float v = l_run[h];
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+          if (lane == (h & 31)) rl[q4 * HC + h] = v;
+        }
+        if (bar_any(!ok2)) break;
+        float inv_l[HC];
+#pragma unroll
+        for (int h = 0; h < HC; ++h) inv_l[h] = 1.f / (rl[h] + rl[HC + h] + rl[2 * HC + h] + rl[3 * HC + h]);
+        float* dst = p.partial_o + (size_t(t.seg) * p.heads + g * HC) * kLatent;
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int h0 = 0; h0 < HC; h0 += 16) {
+            float v[16];
+            tmem_ld16(tmem + lane_off + C::kColO + c * HC + h0, v);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) dst[(h0 + i) * kLatent + c * 128 + st] = v[i] * inv_l[h0 + i];
+          }
+        tc_fence_before();
+        mbar_arrive(&B->o_free);
+#pragma unroll
+        for (int h = 0; h < HC; ++h)
+          if (st == h) p.partial_lse[size_t(t.seg) * p.heads + g * HC + h] = (m_run[h] - log2f(inv_l[h])) * kLn2;
+        ++seg;
+        // the next segment's first tile reuses rl only after further named barriers
+      }
+    }
+  }
+  // ---------------------------------------------------------------- teardown
+  __syncthreads();
+  if (B->abort) {  // let copies already issued land before the CTA's shared memory is released
+    const uint64_t t0 = global_timer_ns();
+    while (global_timer_ns() - t0 < 20000) {
+    }
+  }
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, C::kTmemCols);
+}
+
+// ----- host side: tensor maps and launch ---------------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    fn = reinterpret_cast<EncodeTiledFn>(f);
+  }
+  return fn;
+}
+
+bool make_map_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint32_t box_inner,
+                 uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {inner, rows};
+  cuuint64_t strides[1] = {inner * 2};
+  cuuint32_t box[2] = {box_inner, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int HC>
+cudaError_t launch_tc(const DecodeParams& p, int grid, cudaStream_t stream) {
+  CUtensorMap mc, mq;
+  if (!make_map_2d(&mc, p.cache, kRow, uint64_t(p.num_pages) * p.page_size, 64, p.page_size)) return cudaErrorInvalidValue;
+  if (!make_map_2d(&mq, p.q_full, kRow, uint64_t(p.batch) * p.heads, 64, HC)) return cudaErrorInvalidValue;
+  static bool attr[128] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 128 || !attr[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<HC>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(Cfg<HC>::kSmem));
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 128) attr[dev] = true;
+  }
+  decode_tc_kernel<HC><<<grid, kThreads, Cfg<HC>::kSmem, stream>>>(mc, mq, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_decode_tc(const DecodeParams& p, int hc, int grid, cudaStream_t stream) {
+  return hc == 16 ? launch_tc<16>(p, grid, stream) : launch_tc<32>(p, grid, stream);
+}
+
+}  // namespace mla

@@ -137,6 +137,7 @@ int mla_decode(const mla_dims* d, const void* q_nope, const void* q_pe, const vo
       (int8 && !aligned(cache_scale_zero, 8)))
     return MLA_ERR_INVALID_ARG;
   if ((long long)max_pages_per_seq * d->page_size > (1LL << 31) - 1) return MLA_ERR_INVALID_ARG;
+  if ((long long)num_pages * d->page_size > (1LL << 31) - 1) return MLA_ERR_INVALID_ARG;  // row index is int32
   const int S = effective_splits(d, num_splits);
   if (S <= 0) return MLA_ERR_CUDA;
   const WorkspaceLayout L = workspace_layout(batch, d->num_heads, S);
@@ -189,7 +190,9 @@ int mla_decode(const mla_dims* d, const void* q_nope, const void* q_pe, const vo
   const int ctas_per_group = S < per_group ? S : per_group;
   cudaEvent_t ev0 = g_ev_start.load(), ev1 = g_ev_stop.load();
   if (ev0 && ev1 && cudaEventRecord(ev0, s) != cudaSuccess) return MLA_ERR_CUDA;
-  if (launch_decode_attention(dp, hc, int8, ctas_per_group * groups, s) != cudaSuccess) return MLA_ERR_CUDA;
+  const cudaError_t le = int8 ? launch_decode_simt(dp, hc, true, ctas_per_group * groups, s)
+                              : launch_decode_tc(dp, hc, ctas_per_group * groups, s);
+  if (le != cudaSuccess) return MLA_ERR_CUDA;
   if (ev0 && ev1 && cudaEventRecord(ev1, s) != cudaSuccess) return MLA_ERR_CUDA;
 
   CombineUVParams cp;

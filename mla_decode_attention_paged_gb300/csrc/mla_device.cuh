@@ -21,7 +21,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
 // Workspace layout of mla_decode (all offsets 256-byte aligned):
-//   [0]            int32 status word (+ padding)
+//   [0]            int32 status word, int32 effective split count (+ padding)
 //   tile_start     int32 [B + 1]   prefix sum of ceil(len_b / kTile)
 //   seg_base       int32 [B + 1]   prefix sum of the number of segments per sequence
 //   len_checked    int32 [B]       seq_lens after range checks (0 if rejected)
@@ -74,6 +74,9 @@ struct TileInfo {
   bool last;    // last tile of its segment
 };
 
+// The plan kernel stores S_eff = min(num_splits, W) next to the status word,
+// so that every partition is non-empty (partition starts strictly increase)
+// and the segments of a sequence are exactly the partitions its tiles touch.
 // Walks the units of one CTA: partitions [pa, pb) of the list.
 struct TileWalker {
   const int* tile_start;

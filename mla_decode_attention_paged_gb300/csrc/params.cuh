@@ -56,6 +56,7 @@ cudaError_t launch_absorb(const AbsorbParams& p, cudaStream_t stream);
 cudaError_t launch_append(const AppendParams& p, bool int8, cudaStream_t stream);
 cudaError_t launch_combine_uv(const CombineUVParams& p, cudaStream_t stream);
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream);
-cudaError_t launch_decode_attention(const DecodeParams& p, int hc, bool int8, int grid, cudaStream_t stream);
+cudaError_t launch_decode_simt(const DecodeParams& p, int hc, bool int8, int grid, cudaStream_t stream);
+cudaError_t launch_decode_tc(const DecodeParams& p, int hc, int grid, cudaStream_t stream);
 
 }  // namespace mla

@@ -109,11 +109,15 @@ def draw_bf16(shape, std: float, g: torch.Generator) -> torch.Tensor:
 
 def draw_int8_cache(num_pages: int, page_size: int, g: torch.Generator):
     """Random INT8 codes [num_pages, P, 576] and (scale, zero point) fp32
-    [num_pages, P, 2] for decode-only tests of the quantised cache."""
+    [num_pages, P, 2] for decode-only tests of the quantised cache.
+
+    Zero points are drawn from [-8, 8], as for rows whose range is roughly
+    centred on 0 (per-token quantisation of zero-mean rows puts the zero
+    point near 0); scales are uniform in [0.002, 0.032]."""
     codes = torch.randint(-128, 128, (num_pages, page_size, LATENT_DIM + ROPE_DIM), generator=g,
                           device=g.device, dtype=torch.int32).to(torch.int8)
     scale = torch.rand((num_pages, page_size), generator=g, device=g.device) * 0.03 + 0.002
-    zp = torch.randint(-128, 128, (num_pages, page_size), generator=g, device=g.device).to(torch.float32)
+    zp = torch.randint(-8, 9, (num_pages, page_size), generator=g, device=g.device).to(torch.float32)
     return codes, torch.stack([scale, zp], dim=-1).contiguous()
 
 
