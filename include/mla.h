@@ -144,7 +144,7 @@ size_t mla_decode_workspace_size(const mla_dims* dims, int32_t batch, int32_t nu
  *
  *   q_nope      bf16 [batch, H, 128]
  *   q_pe        bf16 [batch, H, 64], already rotated for the new position
- *   cache, cache_scale_zero   as for mla_cache_append (16-byte aligned)
+ *   cache, cache_scale_zero   as for mla_cache_append (both 16-byte aligned)
  *   block_table int32 [batch, max_pages_per_seq]
  *   seq_lens    int32 [batch] (device): tokens attended by each sequence,
  *               including the one being decoded; 0 gives out = 0, lse = -inf.

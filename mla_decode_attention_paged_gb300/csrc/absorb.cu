@@ -6,12 +6,14 @@
 // latent space once per step, q_lat = W^UK_h^T q_nope (512 wide), and the
 // attention kernel then scores the 576-wide cached rows directly with
 // q_full = [q_lat | q_pe].
+#include <cuda_fp16.h>
+
 #include "params.cuh"
 
 namespace mla {
 
 
-constexpr int kAbsorbB = 32;  // sequences per block
+constexpr int kAbsorbB = 8;  // sequences per block
 
 // Block (0, 0) also computes the work plan before its share of the absorption.
 __device__ void compute_plan(const AbsorbParams& p) {
@@ -68,8 +70,11 @@ __device__ void compute_plan(const AbsorbParams& p) {
   if (threadIdx.x == 0) p.seg_base[p.batch] = carry;
 }
 
-// grid (H, ceil(B / 32)), block 512: thread m computes latent dim m of
-// q_lat for 32 sequences of head h, fp32 accumulation over the 128 content dims.
+// grid (H, ceil(B / 8)), block 512: thread m computes latent dim m of q_lat
+// for 8 sequences of head h, fp32 accumulation over the 128 content dims.
+// INT8 caches take q_full in fp16 (their tensor-core path runs on fp16
+// operands); bf16 caches in bf16.
+template <bool kF16>
 __global__ void __launch_bounds__(512) absorb_kernel(AbsorbParams p) {
   if (blockIdx.x == 0 && blockIdx.y == 0) {
     compute_plan(p);
@@ -92,7 +97,7 @@ __global__ void __launch_bounds__(512) absorb_kernel(AbsorbParams p) {
 #pragma unroll
   for (int i = 0; i < kAbsorbB; ++i) acc[i] = 0.f;
   const __nv_bfloat16* w = p.W_UK + size_t(h) * kNope * kLatent + m;
-#pragma unroll 4
+#pragma unroll 8
   for (int k = 0; k < kNope; ++k) {
     const float wk = bf2f(w[size_t(k) * kLatent]);
 #pragma unroll
@@ -104,20 +109,34 @@ __global__ void __launch_bounds__(512) absorb_kernel(AbsorbParams p) {
       acc[4 * i4 + 3] = fmaf(wk, q.w, acc[4 * i4 + 3]);
     }
   }
-  // write q_full[b][h][0:512] and accumulate the per-(b, h) sum of the rounded values
+  // write q_full[b][h][0:512] (and the RoPE part) and the sum of the rounded values
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint16_t* qf = reinterpret_cast<uint16_t*>(p.q_full);
 #pragma unroll
   for (int i = 0; i < kAbsorbB; ++i) {
     float r = 0.f;
     if (i < nb) {
-      const __nv_bfloat16 v = __float2bfloat16_rn(acc[i]);
-      p.q_full[(size_t(b0 + i) * p.heads + h) * kRow + m] = v;
-      r = bf2f(v);
-    }
-    if (threadIdx.x < kRope && i < nb) {
-      const __nv_bfloat16 v = p.q_pe[(size_t(b0 + i) * p.heads + h) * kRope + threadIdx.x];
-      p.q_full[(size_t(b0 + i) * p.heads + h) * kRow + kLatent + threadIdx.x] = v;
-      r += bf2f(v);
+      const size_t row = (size_t(b0 + i) * p.heads + h) * kRow;
+      if constexpr (kF16) {
+        const __half v = __float2half_rn(acc[i]);
+        qf[row + m] = __half_as_ushort(v);
+        r = __half2float(v);
+      } else {
+        const __nv_bfloat16 v = __float2bfloat16_rn(acc[i]);
+        qf[row + m] = __bfloat16_as_ushort(v);
+        r = bf2f(v);
+      }
+      if (threadIdx.x < kRope) {
+        const float pe = bf2f(p.q_pe[(size_t(b0 + i) * p.heads + h) * kRope + threadIdx.x]);
+        if constexpr (kF16) {
+          const __half v = __float2half_rn(pe);
+          qf[row + kLatent + threadIdx.x] = __half_as_ushort(v);
+          r += __half2float(v);
+        } else {
+          qf[row + kLatent + threadIdx.x] = __bfloat16_as_ushort(__float2bfloat16_rn(pe));
+          r += pe;
+        }
+      }
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) r += __shfl_xor_sync(0xffffffffu, r, o);
@@ -132,9 +151,10 @@ __global__ void __launch_bounds__(512) absorb_kernel(AbsorbParams p) {
   }
 }
 
-cudaError_t launch_absorb(const AbsorbParams& p, cudaStream_t stream) {
+cudaError_t launch_absorb(const AbsorbParams& p, bool fp16_out, cudaStream_t stream) {
   dim3 grid(p.heads, (p.batch + kAbsorbB - 1) / kAbsorbB);
-  absorb_kernel<<<grid, 512, 0, stream>>>(p);
+  if (fp16_out) absorb_kernel<true><<<grid, 512, 0, stream>>>(p);
+  else absorb_kernel<false><<<grid, 512, 0, stream>>>(p);
   return cudaGetLastError();
 }
 

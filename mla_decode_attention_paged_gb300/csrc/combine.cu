@@ -9,85 +9,102 @@
 namespace mla {
 
 
-constexpr int kCombB = 32;   // sequences per block
-constexpr int kCombMK = 64;  // latent dims per W^UV tile
+constexpr int kCombB = 8;     // sequences per block
+constexpr int kCombJ = 64;    // output dims per block (of 128)
+constexpr int kSegChunk = 256;
 
-// grid (H, ceil(B / 32)), block 256.  Phase 1 merges the partials of 32
-// sequences of head h into shared memory; phase 2 multiplies them by W^UV_h.
+// grid (H, ceil(B / 8), 128 / 64), block 256.  Phase 1 merges the segments of
+// 8 sequences of head h into shared memory (weights exp(lse_s - lse) computed
+// once per segment); phase 2 multiplies them by rows [64z, 64z + 64) of W^UV_h.
 __global__ void __launch_bounds__(256) combine_uv_kernel(CombineUVParams p) {
-  extern __shared__ float smem[];
-  float* o_lat = smem;                          // [32][512]
-  float* w_tile = smem + kCombB * kLatent;      // [128][kCombMK + 1]
-  const int h = blockIdx.x, b0 = blockIdx.y * kCombB;
+  __shared__ float o_lat[kCombB][kLatent];
+  __shared__ float wts[kSegChunk];
+  __shared__ float red[8];
+  __shared__ float s_mx, s_inv_z;
+  const int h = blockIdx.x, b0 = blockIdx.y * kCombB, j0 = blockIdx.z * kCombJ;
   const int nb = min(kCombB, p.batch - b0);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
   for (int i = 0; i < kCombB; ++i) {
-    float* row = o_lat + i * kLatent;
     if (i >= nb) {
-      for (int m = threadIdx.x; m < kLatent; m += blockDim.x) row[m] = 0.f;
+      for (int m = tid; m < kLatent; m += blockDim.x) o_lat[i][m] = 0.f;
       continue;
     }
     const int b = b0 + i;
     const int s0 = p.seg_base[b], s1 = p.seg_base[b + 1];
+    // lse of the merged result: max, then sum of exp(lse_s - max)
     float mx = -INFINITY;
-    for (int s = s0; s < s1; ++s) mx = fmaxf(mx, p.partial_lse[size_t(s) * p.heads + h]);
+    for (int s = s0 + tid; s < s1; s += blockDim.x) mx = fmaxf(mx, p.partial_lse[size_t(s) * p.heads + h]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    if (lane == 0) red[warp] = mx;
+    __syncthreads();
+    if (tid == 0) {
+      float v = red[0];
+      for (int k = 1; k < 8; ++k) v = fmaxf(v, red[k]);
+      s_mx = v;
+    }
+    __syncthreads();
+    mx = s_mx;
     float z = 0.f;
     if (mx != -INFINITY)
-      for (int s = s0; s < s1; ++s) z += expf(p.partial_lse[size_t(s) * p.heads + h] - mx);
-    const float inv_z = mx != -INFINITY ? 1.f / z : 0.f;
-    for (int m = threadIdx.x; m < kLatent; m += blockDim.x) {
-      float acc = 0.f;
-      if (mx != -INFINITY)
-        for (int s = s0; s < s1; ++s) {
-          const float w = expf(p.partial_lse[size_t(s) * p.heads + h] - mx);
-          acc = fmaf(w, p.partial_o[(size_t(s) * p.heads + h) * kLatent + m], acc);
-        }
-      row[m] = acc * inv_z;
+      for (int s = s0 + tid; s < s1; s += blockDim.x) z += expf(p.partial_lse[size_t(s) * p.heads + h] - mx);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+    __syncthreads();
+    if (lane == 0) red[warp] = z;
+    __syncthreads();
+    if (tid == 0) {
+      float v = 0.f;
+      for (int k = 0; k < 8; ++k) v += red[k];
+      s_inv_z = mx != -INFINITY ? 1.f / v : 0.f;
+      if (p.lse_out && blockIdx.z == 0)
+        p.lse_out[size_t(b) * p.heads + h] = mx != -INFINITY ? mx + logf(v) : -INFINITY;
     }
-    if (threadIdx.x == 0 && p.lse_out)
-      p.lse_out[size_t(b) * p.heads + h] = mx != -INFINITY ? mx + logf(z) : -INFINITY;
+    __syncthreads();
+    const float inv_z = s_inv_z;
+    float acc0 = 0.f, acc1 = 0.f;
+    if (mx != -INFINITY) {
+      for (int c0 = s0; c0 < s1; c0 += kSegChunk) {
+        const int n = min(kSegChunk, s1 - c0);
+        __syncthreads();
+        for (int k = tid; k < n; k += blockDim.x) wts[k] = expf(p.partial_lse[size_t(c0 + k) * p.heads + h] - mx) * inv_z;
+        __syncthreads();
+        for (int k = 0; k < n; ++k) {
+          const float* src = p.partial_o + (size_t(c0 + k) * p.heads + h) * kLatent;
+          acc0 = fmaf(wts[k], src[tid], acc0);
+          acc1 = fmaf(wts[k], src[tid + 256], acc1);
+        }
+      }
+    }
+    o_lat[i][tid] = acc0;
+    o_lat[i][tid + 256] = acc1;
+    __syncthreads();
   }
 
-  // out[b][h][j] = sum_m W_UV[h][j][m] * o_lat[b][m]; thread -> (j, half of the 32 sequences)
-  const int j = threadIdx.x & 127, half = threadIdx.x >> 7;
-  float acc[kCombB / 2];
-#pragma unroll
-  for (int i = 0; i < kCombB / 2; ++i) acc[i] = 0.f;
-  const __nv_bfloat16* W = p.W_UV + size_t(h) * kVDim * kLatent;
-  for (int m0 = 0; m0 < kLatent; m0 += kCombMK) {
-    __syncthreads();
-    for (int idx = threadIdx.x; idx < kVDim * kCombMK; idx += blockDim.x) {
-      const int jj = idx / kCombMK, mm = idx % kCombMK;
-      w_tile[jj * (kCombMK + 1) + mm] = bf2f(W[size_t(jj) * kLatent + m0 + mm]);
-    }
-    __syncthreads();
+  // out[b][h][j] = sum_m W_UV[h][j][m] * o_lat[b][m]; thread -> (j, pair of sequences)
+  const int j = j0 + (tid & 63), bp = tid >> 6;
+  const uint4* wrow = reinterpret_cast<const uint4*>(p.W_UV + (size_t(h) * kVDim + j) * kLatent);
+  float a0 = 0.f, a1 = 0.f;
 #pragma unroll 4
-    for (int mm = 0; mm < kCombMK; ++mm) {
-      const float w = w_tile[j * (kCombMK + 1) + mm];
+  for (int k8 = 0; k8 < kLatent / 8; ++k8) {
+    const uint4 wv = wrow[k8];
+    const __nv_bfloat162* w2 = reinterpret_cast<const __nv_bfloat162*>(&wv);
 #pragma unroll
-      for (int i = 0; i < kCombB / 2; ++i)
-        acc[i] = fmaf(w, o_lat[(half * (kCombB / 2) + i) * kLatent + m0 + mm], acc[i]);
+    for (int e = 0; e < 4; ++e) {
+      const float2 wf = __bfloat1622float2(w2[e]);
+      const int m = 8 * k8 + 2 * e;
+      a0 = fmaf(wf.x, o_lat[2 * bp][m], fmaf(wf.y, o_lat[2 * bp][m + 1], a0));
+      a1 = fmaf(wf.x, o_lat[2 * bp + 1][m], fmaf(wf.y, o_lat[2 * bp + 1][m + 1], a1));
     }
   }
-#pragma unroll
-  for (int i = 0; i < kCombB / 2; ++i) {
-    const int bi = half * (kCombB / 2) + i;
-    if (bi < nb) p.out[(size_t(b0 + bi) * p.heads + h) * kVDim + j] = __float2bfloat16_rn(acc[i]);
-  }
+  if (2 * bp < nb) p.out[(size_t(b0 + 2 * bp) * p.heads + h) * kVDim + j] = __float2bfloat16_rn(a0);
+  if (2 * bp + 1 < nb) p.out[(size_t(b0 + 2 * bp + 1) * p.heads + h) * kVDim + j] = __float2bfloat16_rn(a1);
 }
 
 cudaError_t launch_combine_uv(const CombineUVParams& p, cudaStream_t stream) {
-  const size_t smem = (kCombB * kLatent + kVDim * (kCombMK + 1)) * sizeof(float);
-  static bool attr_set[128] = {};  // per device; a repeated set is harmless
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 128 || !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(combine_uv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
-    if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 128) attr_set[dev] = true;
-  }
-  dim3 grid(p.heads, (p.batch + kCombB - 1) / kCombB);
-  combine_uv_kernel<<<grid, 256, smem, stream>>>(p);
+  dim3 grid(p.heads, (p.batch + kCombB - 1) / kCombB, kVDim / kCombJ);
+  combine_uv_kernel<<<grid, 256, 0, stream>>>(p);
   return cudaGetLastError();
 }
 

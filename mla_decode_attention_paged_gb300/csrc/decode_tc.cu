@@ -20,9 +20,21 @@
 //
 // Warp roles (256 threads):
 //   warp 0     TMA producer: Q of each segment, then each tile's pages
-//              (4 "pair" slots of two 64-wide latent boxes + 1 RoPE slot)
+//              (4 "pair" slots of two 64-wide latent boxes + 1 RoPE slot);
+//              it also prefetches the pages of the tiles two ahead into L2
+//              ("The Architecture of Memory", "Leveraging Tensor Cores and
+//              Asynchronous Prefetching")
 //   warp 1     TMEM allocation; lane 0 issues the MMAs
+//   warps 2-3  INT8 caches only: expand the TMA-loaded int8 codes in place
+//              into fp16 operand tiles
 //   warps 4-7  softmax (one thread per token row of S^T) and epilogue
+//
+// INT8 caches: value = s_t (code - zp_t) per token.  A code v in [-128, 127]
+// is written as the fp16 number 1152 + v (bit pattern 0x6400 | (v + 128),
+// exact), the MMAs run on fp16 operands (Q in fp16), and the bias and zero
+// point fold into zp'_t = zp_t + 1152:
+//     s[t][h]   = scale * s_t * (q_h . code'_t - zp'_t * sum(q_h))
+//     o_lat[h]  = (sum_t w_t code'_t - sum_t w_t zp'_t) / l,  w_t = p_t s_t
 // Every wait is bounded: on timeout the CTA records MLA_ERR_DEVICE_TIMEOUT,
 // drains, frees its tensor memory and returns.
 #include "blackwell_ptx.cuh"
@@ -39,6 +51,8 @@ constexpr uint32_t kPairBytes = 2 * kBoxBytes;  // latent dims [128c, 128c + 128
 constexpr int kNumRope = 2;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 constexpr float kRescaleThreshold = 8.f;        // log2 units
+constexpr int kPrefetchTiles = 2;               // L2 prefetch distance (tiles)
+constexpr float kCodeBias = 1152.f;             // fp16 value of code 0 after expansion
 
 template <int HC>
 struct Cfg {
@@ -59,6 +73,7 @@ struct Cfg {
 
 struct Barriers {
   uint64_t full_pair[5], empty_pair[5], full_rope[kNumRope], empty_rope[kNumRope];
+  uint64_t full_i8_pair[5], full_i8_rope[kNumRope];  // INT8: TMA landed, codes not yet expanded
   uint64_t q_full, q_empty, s_full[2], p_full[2], o_full, o_free, drain;
   uint32_t tmem_base;
   int abort;
@@ -77,12 +92,49 @@ __device__ __forceinline__ bool bar_any(bool pred) {  // OR over the 128 softmax
   return r != 0;
 }
 
+__device__ __forceinline__ bool converters_any(bool pred) {  // OR over the 64 INT8 expansion threads (barrier 2)
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, 2, 64, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(uint32_t(pred))
+      : "memory");
+  return r != 0;
+}
+
 __device__ __forceinline__ void fail(Barriers* B, int* status) {
   B->abort = 1;
   set_status(status, MLA_ERR_DEVICE_TIMEOUT);
 }
 
-template <int HC>
+// 16 int8 codes -> 16 fp16 values 1152 + code, as two 16-byte halves.
+__device__ __forceinline__ void expand_codes(uint4 v, uint4& lo, uint4& hi) {
+  const uint32_t w[4] = {v.x ^ 0x80808080u, v.y ^ 0x80808080u, v.z ^ 0x80808080u, v.w ^ 0x80808080u};
+  uint32_t o[8];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    o[2 * i] = __byte_perm(w[i], 0x64646464u, 0x4140);      // bytes 0,1 -> 0x64xx 0x64xx
+    o[2 * i + 1] = __byte_perm(w[i], 0x64646464u, 0x4342);  // bytes 2,3
+  }
+  lo = make_uint4(o[0], o[1], o[2], o[3]);
+  hi = make_uint4(o[4], o[5], o[6], o[7]);
+}
+
+// Physical page of token `tok` of sequence b (range-checked; out-of-range
+// entries are reported and replaced by page 0 to stay in bounds).
+__device__ __forceinline__ int page_of(const DecodeParams& p, int b, int tok) {
+  int pg = p.block_table[size_t(b) * p.max_pages + tok / p.page_size];
+  if (pg < 0 || pg >= p.num_pages) {
+    set_status(p.status, MLA_ERR_DEVICE_BOUNDS);
+    pg = 0;
+  }
+  return pg;
+}
+
+template <int HC, bool kInt8>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_cache, const __grid_constant__ CUtensorMap tmap_q,
                      DecodeParams p) {
@@ -90,18 +142,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Barriers* B = reinterpret_cast<Barriers*>(smem + C::kOffMisc);
-  float* red = reinterpret_cast<float*>(smem + C::kOffMisc + 512);  // [2][4][HC] then [4][HC] for l
+  float* red = reinterpret_cast<float*>(smem + C::kOffMisc + 512);  // [2][4][HC] maxima, then [4][HC] sums
   const uint32_t sbase = smem_u32(smem);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  constexpr uint32_t kFullCount = kInt8 ? 64 : 1;  // INT8: the 64 expansion threads complete a slot
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::kNumPair; ++i) {
-      mbar_init(&B->full_pair[i], 1);
+      mbar_init(&B->full_pair[i], kFullCount);
       mbar_init(&B->empty_pair[i], 1);
+      mbar_init(&B->full_i8_pair[i], 1);
     }
     for (int i = 0; i < kNumRope; ++i) {
-      mbar_init(&B->full_rope[i], 1);
+      mbar_init(&B->full_rope[i], kFullCount);
       mbar_init(&B->empty_rope[i], 1);
+      mbar_init(&B->full_i8_rope[i], 1);
     }
     mbar_init(&B->q_full, 1);
     mbar_init(&B->q_empty, 1);
@@ -130,16 +185,29 @@ __global__ void __launch_bounds__(kThreads, 1)
   const long long S = p.status[1];  // effective split count from the plan
   const long long pa = (cp * S) / Cp, pb = ((cp + 1) * S) / Cp;
   const volatile int* abort_flag = &B->abort;
+  const int P = p.page_size;
+  constexpr uint32_t kRowBytes = kInt8 ? kRow : 2 * kRow;
 
   if (warp == 0 && lane == 0) {
     // ------------------------------------------------------------ producer
-    TileWalker walk;
+    TileWalker walk, ahead;
     walk.init(p.tile_start, p.seg_base, p.len, p.batch, int(S), pa, pb);
-    const int P = p.page_size, pages_per_tile = kTile / P;
-    const uint32_t box_bytes_per_page = uint32_t(P) * 128;
+    ahead = walk;
+    const char* cache = static_cast<const char*>(p.cache);
+    auto prefetch_tile = [&](const TileInfo& a) {
+      const int npg = (a.valid + P - 1) / P;
+      for (int i = 0; i < npg; ++i) {
+        const int pg = page_of(p, a.b, a.tile * kTile + i * P);
+        prefetch_l2(cache + size_t(pg) * P * kRowBytes, uint32_t(P) * kRowBytes);
+        if (kInt8) prefetch_l2(p.scale_zero + size_t(pg) * P * 2, uint32_t(P) * 8);
+      }
+    };
+    TileInfo t, ta;
+    for (int k = 0; k < kPrefetchTiles && ahead.next(ta); ++k) prefetch_tile(ta);
+    const uint32_t page_bytes = uint32_t(P) * 128;  // one 64-column box of P rows (bf16)
     uint32_t pair_it = 0, rope_it = 0, seg = 0;
-    TileInfo t;
     while (walk.next(t)) {
+      if (ahead.next(ta)) prefetch_tile(ta);
       if (t.first) {
         if (seg > 0 && !mbar_wait(&B->q_empty, (seg - 1) & 1, abort_flag, kWaitLimitNs)) { fail(B, p.status); break; }
         mbar_arrive_expect_tx(&B->q_full, C::kQBytes);
@@ -149,14 +217,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const int npg = (t.valid + P - 1) / P;
       int rows[kTile / 16];
-      for (int i = 0; i < npg; ++i) {
-        int pg = p.block_table[size_t(t.b) * p.max_pages + t.tile * pages_per_tile + i];
-        if (pg < 0 || pg >= p.num_pages) {
-          set_status(p.status, MLA_ERR_DEVICE_BOUNDS);
-          pg = 0;  // stay in bounds; this sequence's result is unspecified
-        }
-        rows[i] = pg * P;
-      }
+      for (int i = 0; i < npg; ++i) rows[i] = page_of(p, t.b, t.tile * kTile + i * P) * P;
       bool ok = true;
       for (int c = 0; c < 4 && ok; ++c, ++pair_it) {
         const uint32_t slot = pair_it % C::kNumPair;
@@ -164,12 +225,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
           break;
         }
-        mbar_arrive_expect_tx(&B->full_pair[slot], 2 * npg * box_bytes_per_page);
         uint8_t* dst = smem + C::kOffPair + slot * kPairBytes;
-        for (int i = 0; i < npg; ++i) {
-          tma_load_2d(dst + i * box_bytes_per_page, &tmap_cache, 128 * c, rows[i], &B->full_pair[slot]);
-          tma_load_2d(dst + kBoxBytes + i * box_bytes_per_page, &tmap_cache, 128 * c + 64, rows[i],
-                      &B->full_pair[slot]);
+        if constexpr (!kInt8) {
+          mbar_arrive_expect_tx(&B->full_pair[slot], 2 * npg * page_bytes);
+          for (int i = 0; i < npg; ++i) {
+            tma_load_2d(dst + i * page_bytes, &tmap_cache, 128 * c, rows[i], &B->full_pair[slot]);
+            tma_load_2d(dst + kBoxBytes + i * page_bytes, &tmap_cache, 128 * c + 64, rows[i], &B->full_pair[slot]);
+          }
+        } else {  // int8 codes of columns [128c, 128c + 128) into the slot's back half, as two [128 x 64 B] blocks
+          mbar_arrive_expect_tx(&B->full_i8_pair[slot], npg * page_bytes);
+          for (int i = 0; i < npg; ++i) {
+            tma_load_2d(dst + kBoxBytes + i * P * 64, &tmap_cache, 128 * c, rows[i], &B->full_i8_pair[slot]);
+            tma_load_2d(dst + kBoxBytes + 8192 + i * P * 64, &tmap_cache, 128 * c + 64, rows[i],
+                        &B->full_i8_pair[slot]);
+          }
         }
       }
       if (!ok) { fail(B, p.status); break; }
@@ -179,10 +248,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           fail(B, p.status);
           break;
         }
-        mbar_arrive_expect_tx(&B->full_rope[slot], npg * box_bytes_per_page);
         uint8_t* dst = smem + C::kOffRope + slot * kBoxBytes;
-        for (int i = 0; i < npg; ++i)
-          tma_load_2d(dst + i * box_bytes_per_page, &tmap_cache, kLatent, rows[i], &B->full_rope[slot]);
+        if constexpr (!kInt8) {
+          mbar_arrive_expect_tx(&B->full_rope[slot], npg * page_bytes);
+          for (int i = 0; i < npg; ++i) tma_load_2d(dst + i * page_bytes, &tmap_cache, kLatent, rows[i], &B->full_rope[slot]);
+        } else {
+          mbar_arrive_expect_tx(&B->full_i8_rope[slot], npg * P * 64);
+          for (int i = 0; i < npg; ++i)
+            tma_load_2d(dst + 8192 + i * P * 64, &tmap_cache, kLatent, rows[i], &B->full_i8_rope[slot]);
+        }
         ++rope_it;
       }
     }
@@ -190,8 +264,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ MMA issuer
     TileWalker walk;
     walk.init(p.tile_start, p.seg_base, p.len, p.batch, int(S), pa, pb);
-    constexpr uint32_t id_qk = idesc_bf16_f32(128, HC, false, false);
-    constexpr uint32_t id_pv = idesc_bf16_f32(128, HC, true, true);
+    constexpr uint32_t id_qk = idesc_f32acc(128, HC, false, false, kInt8);
+    constexpr uint32_t id_pv = idesc_f32acc(128, HC, true, true, kInt8);
     uint32_t pair_it = 0, rope_it = 0, tile_i = 0, seg = 0;
     TileInfo t;
     bool ok = true;
@@ -255,17 +329,82 @@ __global__ void __launch_bounds__(kThreads, 1)
     // all issued MMAs complete before teardown
     mma_commit(&B->drain);
     mbar_wait(&B->drain, 0, abort_flag, kWaitLimitNs);
+  } else if (kInt8 && (warp == 2 || warp == 3)) {
+    // ------------------------------------------------------------ INT8 expansion
+    // Thread ct reads 16-byte chunk (ct % 4) of rows ct/4 + 16j of each
+    // [128 x 64 B] code block, then writes the 16 fp16 values into the
+    // swizzled operand box at the same rows.
+    const int ct = threadIdx.x - 64, ch = ct & 3, r0 = ct >> 2;
+    TileWalker walk;
+    walk.init(p.tile_start, p.seg_base, p.len, p.batch, int(S), pa, pb);
+    uint32_t pair_it = 0, rope_it = 0;
+    TileInfo t;
+    bool ok = true;
+    while (ok && walk.next(t)) {
+      for (int c = 0; c < 5 && ok; ++c) {
+        const bool rope = c == 4;
+        const uint32_t it = rope ? rope_it : pair_it, nslot = rope ? kNumRope : C::kNumPair;
+        const uint32_t slot = it % nslot;
+        uint64_t* full_i8 = rope ? &B->full_i8_rope[slot] : &B->full_i8_pair[slot];
+        uint8_t* base = smem + (rope ? C::kOffRope + slot * kBoxBytes : C::kOffPair + slot * kPairBytes);
+        const bool landed = mbar_wait(full_i8, (it / nslot) & 1, abort_flag, kWaitLimitNs);
+        const int nblk = rope ? 1 : 2;
+        const uint8_t* src = base + (rope ? 8192 : kBoxBytes);
+        uint4 v[16];
+#pragma unroll
+        for (int k = 0; k < 2; ++k)
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            if (k < nblk) v[k * 8 + j] = *reinterpret_cast<const uint4*>(src + k * 8192 + (r0 + 16 * j) * 64 + ch * 16);
+        // every thread has read its codes before the expansion overwrites them;
+        // a timeout anywhere stops all 64 threads together
+        if (converters_any(!landed)) {
+          ok = false;
+          break;
+        }
+#pragma unroll
+        for (int k = 0; k < 2; ++k)
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            if (k < nblk) {
+              const int r = r0 + 16 * j;
+              uint4 lo, hi;
+              expand_codes(v[k * 8 + j], lo, hi);
+              uint8_t* row = base + k * kBoxBytes + r * 128;
+              *reinterpret_cast<uint4*>(row + (((2 * ch) ^ (r & 7)) << 4)) = lo;
+              *reinterpret_cast<uint4*>(row + (((2 * ch + 1) ^ (r & 7)) << 4)) = hi;
+            }
+        fence_proxy_async_smem();
+        mbar_arrive(rope ? &B->full_rope[slot] : &B->full_pair[slot]);
+        if (rope) ++rope_it; else ++pair_it;
+      }
+      if (!ok) fail(B, p.status);
+    }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ softmax / epilogue
     const int q4 = warp - 4, st = threadIdx.x - 128;  // st = token row of S^T = TMEM lane
     const uint32_t lane_off = uint32_t(q4 * 32) << 16;
     TileWalker walk;
     walk.init(p.tile_start, p.seg_base, p.len, p.batch, int(S), pa, pb);
-    float m_run[HC], l_run[HC];
+    float m_run[HC], l_run[HC], corr[HC], qsum[HC];
     uint32_t pair_it = 0, tile_i = 0, seg = 0;
     TileInfo t;
     while (walk.next(t)) {
       const uint32_t buf = tile_i & 1;
+      const bool valid = st < t.valid;
+      float tok_s = 0.f, tok_z = 0.f;  // INT8: this row's scale and biased zero point
+      if (kInt8) {
+        if (t.first)
+#pragma unroll
+          for (int h = 0; h < HC; ++h) qsum[h] = p.q_sum[size_t(t.b) * p.heads + g * HC + h];
+        if (valid) {
+          const int tok = t.tile * kTile + st;
+          const float2 sz = *reinterpret_cast<const float2*>(p.scale_zero +
+                                                             (size_t(page_of(p, t.b, tok)) * P + tok % P) * 2);
+          tok_s = sz.x;
+          tok_z = sz.y + kCodeBias;
+        }
+      }
       const bool ok = mbar_wait(&B->s_full[buf], (tile_i >> 1) & 1, abort_flag, kWaitLimitNs);
       tc_fence_after();
       float x[HC];
@@ -278,9 +417,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int i = 0; i < 16; ++i) x[h0 + i] = v[i];
         }
       }
-      const bool valid = st < t.valid;
+      const float row_scale = kInt8 ? p.scale_log2 * tok_s : p.scale_log2;
 #pragma unroll
-      for (int h = 0; h < HC; ++h) x[h] = valid ? x[h] * p.scale_log2 : -INFINITY;
+      for (int h = 0; h < HC; ++h) {
+        const float raw = kInt8 ? fmaf(-tok_z, qsum[h], x[h]) : x[h];
+        x[h] = valid ? raw * row_scale : -INFINITY;
+      }
       // tile max per head: warp butterfly, then across the 4 warps through shared memory
       float* rm = red + buf * 4 * HC;
 #pragma unroll
@@ -299,11 +441,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (t.first) {
           m_run[h] = mt;
           l_run[h] = 0.f;
+          corr[h] = 0.f;
           alpha[h] = 1.f;
         } else if (mt > m_run[h] + kRescaleThreshold) {
           alpha[h] = exp2f(m_run[h] - mt);
           m_run[h] = mt;
           l_run[h] *= alpha[h];
+          corr[h] *= alpha[h];
           rescale = true;
         } else {
           alpha[h] = 1.f;
@@ -323,25 +467,36 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         tmem_st_wait();
       }
-      // probabilities -> P^T (bf16, MN-major, no swizzle: 8x8 core matrices)
+      // probabilities -> P^T (16-bit, MN-major, no swizzle: 8x8 core matrices)
       uint8_t* pt = smem + C::kOffP + buf * C::kPBytes;
 #pragma unroll
       for (int h0 = 0; h0 < HC; h0 += 8) {
         uint32_t packed[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          const __nv_bfloat16 lo = __float2bfloat16_rn(exp2f(x[h0 + 2 * i] - m_run[h0 + 2 * i]));
-          const __nv_bfloat16 hi = __float2bfloat16_rn(exp2f(x[h0 + 2 * i + 1] - m_run[h0 + 2 * i + 1]));
-          l_run[h0 + 2 * i] += __bfloat162float(lo);
-          l_run[h0 + 2 * i + 1] += __bfloat162float(hi);
-          packed[i] = uint32_t(__bfloat16_as_ushort(lo)) | (uint32_t(__bfloat16_as_ushort(hi)) << 16);
+          const int ha = h0 + 2 * i, hb = ha + 1;
+          const float pa_ = exp2f(x[ha] - m_run[ha]), pb_ = exp2f(x[hb] - m_run[hb]);
+          if constexpr (kInt8) {
+            const __half wa = __float2half_rn(pa_ * tok_s), wb = __float2half_rn(pb_ * tok_s);
+            l_run[ha] += pa_;
+            l_run[hb] += pb_;
+            corr[ha] = fmaf(__half2float(wa), tok_z, corr[ha]);
+            corr[hb] = fmaf(__half2float(wb), tok_z, corr[hb]);
+            packed[i] = uint32_t(__half_as_ushort(wa)) | (uint32_t(__half_as_ushort(wb)) << 16);
+          } else {
+            const __nv_bfloat16 wa = __float2bfloat16_rn(pa_), wb = __float2bfloat16_rn(pb_);
+            l_run[ha] += __bfloat162float(wa);
+            l_run[hb] += __bfloat162float(wb);
+            packed[i] = uint32_t(__bfloat16_as_ushort(wa)) | (uint32_t(__bfloat16_as_ushort(wb)) << 16);
+          }
         }
         *reinterpret_cast<uint4*>(pt + (h0 / 8) * 2048 + (st / 8) * 128 + (st % 8) * 16) =
             make_uint4(packed[0], packed[1], packed[2], packed[3]);
       }
-      // ragged tail: rows [valid, ceil16(valid)) of the latent boxes feed the
-      // last PV k-step with zero weight; make them finite zeros
-      if (st >= t.valid && st < ((t.valid + 15) & ~15)) {
+      // bf16 ragged tail: rows [valid, ceil16(valid)) of the latent boxes feed
+      // the last PV k-step with zero weight; make them finite zeros (the INT8
+      // expansion always produces finite values)
+      if (!kInt8 && st >= t.valid && st < ((t.valid + 15) & ~15)) {
         for (int c = 0; c < 4; ++c) {
           uint8_t* row = smem + C::kOffPair + ((pair_it + c) % C::kNumPair) * kPairBytes + st * 128;
 #pragma unroll
@@ -359,18 +514,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (t.last) {
         const bool ok2 = mbar_wait(&B->o_full, seg & 1, abort_flag, kWaitLimitNs);
         tc_fence_after();
-        float* rl = red + 8 * HC;
+        float* rl = red + 8 * HC;  // [4][HC] sums of l, then (INT8) [4][HC] sums of corr
 #pragma unroll
         for (int h = 0; h < HC; ++h) {
           float v = l_run[h];
 #pragma unroll
           for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
           if (lane == (h & 31)) rl[q4 * HC + h] = v;
+          if (kInt8) {
+            float c = corr[h];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
+            if (lane == (h & 31)) rl[4 * HC + q4 * HC + h] = c;
+          }
         }
         if (bar_any(!ok2)) break;
         float inv_l[HC];
 #pragma unroll
-        for (int h = 0; h < HC; ++h) inv_l[h] = 1.f / (rl[h] + rl[HC + h] + rl[2 * HC + h] + rl[3 * HC + h]);
+        for (int h = 0; h < HC; ++h) {
+          inv_l[h] = 1.f / (rl[h] + rl[HC + h] + rl[2 * HC + h] + rl[3 * HC + h]);
+          if (kInt8) corr[h] = rl[4 * HC + h] + rl[5 * HC + h] + rl[6 * HC + h] + rl[7 * HC + h];
+        }
         float* dst = p.partial_o + (size_t(t.seg) * p.heads + g * HC) * kLatent;
 #pragma unroll
         for (int c = 0; c < 4; ++c)
@@ -379,7 +543,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             float v[16];
             tmem_ld16(tmem + lane_off + C::kColO + c * HC + h0, v);
 #pragma unroll
-            for (int i = 0; i < 16; ++i) dst[(h0 + i) * kLatent + c * 128 + st] = v[i] * inv_l[h0 + i];
+            for (int i = 0; i < 16; ++i)
+              dst[(h0 + i) * kLatent + c * 128 + st] = (kInt8 ? v[i] - corr[h0 + i] : v[i]) * inv_l[h0 + i];
           }
         tc_fence_before();
         mbar_arrive(&B->o_free);
@@ -387,7 +552,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int h = 0; h < HC; ++h)
           if (st == h) p.partial_lse[size_t(t.seg) * p.heads + g * HC + h] = (m_run[h] - log2f(inv_l[h])) * kLn2;
         ++seg;
-        // the next segment's first tile reuses rl only after further named barriers
       }
     }
   }
@@ -420,40 +584,49 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-bool make_map_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint32_t box_inner,
-                 uint32_t box_rows) {
+// 2-D map over a row-major [rows, inner] tensor of 1- or 2-byte elements.
+bool make_map_2d(CUtensorMap* m, const void* base, int elem_bytes, uint64_t inner, uint64_t rows, uint32_t box_inner,
+                 uint32_t box_rows, bool swizzle128) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {inner, rows};
-  cuuint64_t strides[1] = {inner * 2};
+  cuuint64_t strides[1] = {inner * elem_bytes};
   cuuint32_t box[2] = {box_inner, box_rows};
   cuuint32_t estr[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+  return fn(m, elem_bytes == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+            const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int HC>
+template <int HC, bool kInt8>
 cudaError_t launch_tc(const DecodeParams& p, int grid, cudaStream_t stream) {
   CUtensorMap mc, mq;
-  if (!make_map_2d(&mc, p.cache, kRow, uint64_t(p.num_pages) * p.page_size, 64, p.page_size)) return cudaErrorInvalidValue;
-  if (!make_map_2d(&mq, p.q_full, kRow, uint64_t(p.batch) * p.heads, 64, HC)) return cudaErrorInvalidValue;
+  const uint64_t rows = uint64_t(p.num_pages) * p.page_size;
+  if (!make_map_2d(&mc, p.cache, kInt8 ? 1 : 2, kRow, rows, 64, p.page_size, !kInt8)) return cudaErrorInvalidValue;
+  // q_full holds bf16 (or, for INT8 caches, fp16) values; TMA moves 2-byte elements either way
+  if (!make_map_2d(&mq, p.q_full, 2, kRow, uint64_t(p.batch) * p.heads, 64, HC, true)) return cudaErrorInvalidValue;
   static bool attr[128] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 128 || !attr[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<HC>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(Cfg<HC>::kSmem));
+    cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<HC, kInt8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         int(Cfg<HC>::kSmem));
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 128) attr[dev] = true;
   }
-  decode_tc_kernel<HC><<<grid, kThreads, Cfg<HC>::kSmem, stream>>>(mc, mq, p);
+  decode_tc_kernel<HC, kInt8><<<grid, kThreads, Cfg<HC>::kSmem, stream>>>(mc, mq, p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_decode_tc(const DecodeParams& p, int hc, int grid, cudaStream_t stream) {
-  return hc == 16 ? launch_tc<16>(p, grid, stream) : launch_tc<32>(p, grid, stream);
+// Head-group size the attention kernel uses for `heads` query heads.
+int decode_head_group(int heads, bool int8) { return (!int8 && heads % 32 == 0) ? 32 : 16; }
+
+cudaError_t launch_decode_tc(const DecodeParams& p, int hc, bool int8, int grid, cudaStream_t stream) {
+  if (int8) return launch_tc<16, true>(p, grid, stream);
+  return hc == 16 ? launch_tc<16, false>(p, grid, stream) : launch_tc<32, false>(p, grid, stream);
 }
 
 }  // namespace mla

@@ -19,8 +19,6 @@ std::atomic<cudaEvent_t> g_ev_start{nullptr}, g_ev_stop{nullptr};
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-int head_chunk(int heads) { return (heads % 32 == 0) ? 32 : 16; }
-
 int sm_count() {
   static int cached[128] = {};
   int dev = 0;
@@ -36,7 +34,7 @@ int effective_splits(const mla_dims* d, int num_splits) {
   if (num_splits > 0) return num_splits;
   const int n = sm_count();
   if (n <= 0) return -1;
-  const int groups = d->num_heads / head_chunk(d->num_heads);
+  const int groups = d->num_heads / decode_head_group(d->num_heads, d->cache_dtype == MLA_CACHE_INT8);
   return n / groups > 0 ? n / groups : 1;
 }
 
@@ -134,7 +132,7 @@ int mla_decode(const mla_dims* d, const void* q_nope, const void* q_pe, const vo
   if (int8 && !cache_scale_zero) return MLA_ERR_INVALID_ARG;
   if (!aligned(cache, 16) || !aligned(q_nope, 4) || !aligned(q_pe, 4) || !aligned(W_UK, 4) || !aligned(W_UV, 4) ||
       !aligned(out, 4) || !aligned(block_table, 4) || !aligned(seq_lens, 4) || (lse_out && !aligned(lse_out, 4)) ||
-      (int8 && !aligned(cache_scale_zero, 8)))
+      (int8 && !aligned(cache_scale_zero, 16)))
     return MLA_ERR_INVALID_ARG;
   if ((long long)max_pages_per_seq * d->page_size > (1LL << 31) - 1) return MLA_ERR_INVALID_ARG;
   if ((long long)num_pages * d->page_size > (1LL << 31) - 1) return MLA_ERR_INVALID_ARG;  // row index is int32
@@ -143,7 +141,7 @@ int mla_decode(const mla_dims* d, const void* q_nope, const void* q_pe, const vo
   const WorkspaceLayout L = workspace_layout(batch, d->num_heads, S);
   if (!workspace || !aligned(workspace, 256) || workspace_bytes < L.total) return MLA_ERR_WORKSPACE;
 
-  const int H = d->num_heads, hc = head_chunk(H), groups = H / hc;
+  const int H = d->num_heads, hc = decode_head_group(H, int8), groups = H / hc;
   char* ws = static_cast<char*>(workspace);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 
@@ -162,7 +160,7 @@ int mla_decode(const mla_dims* d, const void* q_nope, const void* q_pe, const vo
   ap.heads = H;
   ap.max_len = max_pages_per_seq * d->page_size;
   ap.num_splits = S;
-  if (launch_absorb(ap, s) != cudaSuccess) return MLA_ERR_CUDA;
+  if (launch_absorb(ap, int8, s) != cudaSuccess) return MLA_ERR_CUDA;
 
   DecodeParams dp;
   dp.q_full = ap.q_full;
@@ -190,9 +188,7 @@ int mla_decode(const mla_dims* d, const void* q_nope, const void* q_pe, const vo
   const int ctas_per_group = S < per_group ? S : per_group;
   cudaEvent_t ev0 = g_ev_start.load(), ev1 = g_ev_stop.load();
   if (ev0 && ev1 && cudaEventRecord(ev0, s) != cudaSuccess) return MLA_ERR_CUDA;
-  const cudaError_t le = int8 ? launch_decode_simt(dp, hc, true, ctas_per_group * groups, s)
-                              : launch_decode_tc(dp, hc, ctas_per_group * groups, s);
-  if (le != cudaSuccess) return MLA_ERR_CUDA;
+  if (launch_decode_tc(dp, hc, int8, ctas_per_group * groups, s) != cudaSuccess) return MLA_ERR_CUDA;
   if (ev0 && ev1 && cudaEventRecord(ev1, s) != cudaSuccess) return MLA_ERR_CUDA;
 
   CombineUVParams cp;

@@ -10,7 +10,7 @@ struct AbsorbParams {
   const __nv_bfloat16* q_nope;  // [B, H, 128]
   const __nv_bfloat16* q_pe;    // [B, H, 64]
   const __nv_bfloat16* W_UK;    // [H, 128, 512]
-  __nv_bfloat16* q_full;        // [B, H, 576]
+  __nv_bfloat16* q_full;        // [B, H, 576] (fp16 bit patterns for INT8 caches)
   float* q_sum;                 // [B, H]
   // plan
   const int* seq_lens;
@@ -52,11 +52,11 @@ struct CombineParams {
   int batch, splits, heads, dim;
 };
 
-cudaError_t launch_absorb(const AbsorbParams& p, cudaStream_t stream);
+cudaError_t launch_absorb(const AbsorbParams& p, bool fp16_out, cudaStream_t stream);
 cudaError_t launch_append(const AppendParams& p, bool int8, cudaStream_t stream);
 cudaError_t launch_combine_uv(const CombineUVParams& p, cudaStream_t stream);
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream);
-cudaError_t launch_decode_simt(const DecodeParams& p, int hc, bool int8, int grid, cudaStream_t stream);
-cudaError_t launch_decode_tc(const DecodeParams& p, int hc, int grid, cudaStream_t stream);
+cudaError_t launch_decode_tc(const DecodeParams& p, int hc, bool int8, int grid, cudaStream_t stream);
+int decode_head_group(int heads, bool int8);
 
 }  // namespace mla
