@@ -30,13 +30,18 @@
 //   warps 4-7  softmax (one thread per token row of S^T) and epilogue
 //
 // INT8 caches: value = s_t (code - zp_t) per token.  A code v in [-128, 127]
-// is written as the fp16 number 1152 + v (bit pattern 0x6400 | (v + 128),
-// exact), the MMAs run on fp16 operands (Q in fp16), and the bias and zero
-// point fold into zp'_t = zp_t + 1152:
-//     s[t][h]   = scale * s_t * (q_h . code'_t - zp'_t * sum(q_h))
-//     o_lat[h]  = (sum_t w_t code'_t - sum_t w_t zp'_t) / l,  w_t = p_t s_t
+// is expanded to fp16 exactly (bit pattern 0x6400 | (v + 128) is 1152 + v,
+// and subtracting 1152 in fp16 is exact), the MMAs run on fp16 operands (Q in
+// fp16), and scale and zero point are applied outside the MMAs:
+//     s[t][h]   = scale * s_t * (q_h . code_t - zp_t * sum(q_h))
+//     o_lat[h]  = (sum_t w_t code_t - sum_t w_t zp_t) / l,  w_t = p_t s_t
+// (Leaving the +1152 bias in the operands would make the PV accumulator sum
+// ~1152 * sum(w) over thousands of tokens and lose the result to fp32
+// cancellation.)
 // Every wait is bounded: on timeout the CTA records MLA_ERR_DEVICE_TIMEOUT,
 // drains, frees its tensor memory and returns.
+#include <cuda_fp16.h>
+
 #include "blackwell_ptx.cuh"
 #include "params.cuh"
 
@@ -52,7 +57,6 @@ constexpr int kNumRope = 2;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 constexpr float kRescaleThreshold = 8.f;        // log2 units
 constexpr int kPrefetchTiles = 2;               // L2 prefetch distance (tiles)
-constexpr float kCodeBias = 1152.f;             // fp16 value of code 0 after expansion
 
 template <int HC>
 struct Cfg {
@@ -110,14 +114,18 @@ __device__ __forceinline__ void fail(Barriers* B, int* status) {
   set_status(status, MLA_ERR_DEVICE_TIMEOUT);
 }
 
-// 16 int8 codes -> 16 fp16 values 1152 + code, as two 16-byte halves.
+// 16 int8 codes -> 16 fp16 values equal to the codes, as two 16-byte halves.
+__device__ __forceinline__ uint32_t codes_to_half2(uint32_t biased_bits) {  // (1152 + a, 1152 + b) -> (a, b)
+  const __half2 h = __hsub2(*reinterpret_cast<const __half2*>(&biased_bits), __floats2half2_rn(1152.f, 1152.f));
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
 __device__ __forceinline__ void expand_codes(uint4 v, uint4& lo, uint4& hi) {
   const uint32_t w[4] = {v.x ^ 0x80808080u, v.y ^ 0x80808080u, v.z ^ 0x80808080u, v.w ^ 0x80808080u};
   uint32_t o[8];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    o[2 * i] = __byte_perm(w[i], 0x64646464u, 0x4140);      // bytes 0,1 -> 0x64xx 0x64xx
-    o[2 * i + 1] = __byte_perm(w[i], 0x64646464u, 0x4342);  // bytes 2,3
+    o[2 * i] = codes_to_half2(__byte_perm(w[i], 0x64646464u, 0x4140));      // bytes 0,1 -> 0x64xx 0x64xx
+    o[2 * i + 1] = codes_to_half2(__byte_perm(w[i], 0x64646464u, 0x4342));  // bytes 2,3
   }
   lo = make_uint4(o[0], o[1], o[2], o[3]);
   hi = make_uint4(o[4], o[5], o[6], o[7]);
@@ -392,7 +400,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     while (walk.next(t)) {
       const uint32_t buf = tile_i & 1;
       const bool valid = st < t.valid;
-      float tok_s = 0.f, tok_z = 0.f;  // INT8: this row's scale and biased zero point
+      float tok_s = 0.f, tok_z = 0.f;  // INT8: this row's scale and zero point
       if (kInt8) {
         if (t.first)
 #pragma unroll
@@ -402,7 +410,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float2 sz = *reinterpret_cast<const float2*>(p.scale_zero +
                                                              (size_t(page_of(p, t.b, tok)) * P + tok % P) * 2);
           tok_s = sz.x;
-          tok_z = sz.y + kCodeBias;
+          tok_z = sz.y;
         }
       }
       const bool ok = mbar_wait(&B->s_full[buf], (tile_i >> 1) & 1, abort_flag, kWaitLimitNs);
