@@ -173,6 +173,38 @@ int mla_decode(const mla_dims* dims, const void* q_nope, const void* q_pe, const
                void* workspace, size_t workspace_bytes, void* out, float* lse_out,
                mla_stream_t stream);
 
+/* Size of the fixed scratch array used by mla_decode_no_alloc. */
+#define MLA_NO_ALLOC_WORKSPACE_BYTES (16u << 20)
+
+/*
+ * mla_decode_no_alloc -- mla_decode without a caller workspace.  The pages
+ * have no counterpart to this entry point; it serves callers that cannot
+ * allocate device memory: for example, a serving loop that must not call
+ * cudaMalloc on its decode path (the call can synchronise the device and
+ * stall every stream), or a plain C host that embeds this library inside a
+ * process whose device memory is budgeted up front and owned by someone else.
+ *
+ * Arguments and results are those of mla_decode, minus the workspace.  The
+ * scratch is one device array of MLA_NO_ALLOC_WORKSPACE_BYTES (16 MiB) that
+ * lives in the library for as long as the process has it loaded, on every
+ * GPU it runs on.  A call whose mla_decode_workspace_size(dims, batch,
+ * num_splits) exceeds that size returns MLA_ERR_WORKSPACE without launching
+ * anything; use mla_decode with a caller workspace for such shapes.  The
+ * call allocates nothing.  The first call on a device looks up the array's
+ * device address (cudaGetSymbolAddress) with that device current, so make a
+ * first call on each device before any stream capture.  All calls on a
+ * device share the one array: calls that may overlap on the GPU (different
+ * streams, or different host threads) race on it and must be serialised by
+ * the caller.  device_status (optional, int32 on the device) receives a
+ * copy of the call's device status word, as mla_read_device_status would
+ * report it for mla_decode.
+ */
+int mla_decode_no_alloc(const mla_dims* dims, const void* q_nope, const void* q_pe, const void* cache,
+                        const float* cache_scale_zero, int32_t num_pages, const int32_t* block_table,
+                        int32_t max_pages_per_seq, const int32_t* seq_lens, int32_t batch,
+                        const void* W_UK, const void* W_UV, float softmax_scale, int32_t num_splits,
+                        void* out, float* lse_out, int32_t* device_status, mla_stream_t stream);
+
 /*
  * mla_combine -- merge per-chunk partial results by log-sum-exp ("The
  * Architecture of Memory", "Flash-Decoding and FlashInfer").

@@ -18,7 +18,7 @@ from . import build as _build
 
 __all__ = [
     "MLAError", "Dims", "dims", "load_library", "check_dims", "cache_append", "auto_num_splits",
-    "decode_workspace_size", "decode", "combine", "read_device_status", "read_status_word",
+    "decode_workspace_size", "decode", "decode_no_alloc", "combine", "read_device_status", "read_status_word",
     "set_timing_events", "status_string", "version",
     "MLA_OK", "MLA_ERR_INVALID_ARG", "MLA_ERR_UNSUPPORTED", "MLA_ERR_WORKSPACE", "MLA_ERR_CUDA",
     "MLA_ERR_DEVICE_TIMEOUT", "MLA_ERR_DEVICE_BOUNDS", "MLA_CACHE_BF16", "MLA_CACHE_INT8",
@@ -38,8 +38,9 @@ MLA_CACHE_INT8 = 1
 EXPORTED_SYMBOLS = (
     "mla_check_dims", "mla_cache_append", "mla_auto_num_splits", "mla_decode_workspace_size",
     "mla_decode", "mla_combine", "mla_read_device_status", "mla_read_status_word",
-    "mla_status_string", "mla_set_timing_events", "mla_version",
+    "mla_status_string", "mla_set_timing_events", "mla_version", "mla_decode_no_alloc",
 )
+NO_ALLOC_WORKSPACE_BYTES = 16 << 20  # MLA_NO_ALLOC_WORKSPACE_BYTES in include/mla.h
 
 
 class MLAError(RuntimeError):
@@ -85,6 +86,8 @@ def load_library(build_if_missing: bool = False, path: str | None = None):
         "mla_decode_workspace_size": (ctypes.c_size_t, [DP, _I, _I]),
         "mla_decode": (_I, [DP, _P, _P, _P, _P, _I, _P, _I, _P, _I, _P, _P, ctypes.c_float, _I, _P,
                             ctypes.c_size_t, _P, _P, _P]),
+        "mla_decode_no_alloc": (_I, [DP, _P, _P, _P, _P, _I, _P, _I, _P, _I, _P, _P, ctypes.c_float, _I, _P, _P,
+                                     _P, _P]),
         "mla_combine": (_I, [DP, _P, _P, _I, _I, _P, _P, _P]),
         "mla_read_device_status": (_I, [_P, ctypes.POINTER(ctypes.c_int32), _P]),
         "mla_read_status_word": (_I, [_P, ctypes.POINTER(ctypes.c_int32), _P]),
@@ -199,6 +202,30 @@ def decode(d: Dims, q_nope, q_pe, cache, scale_zero, block_table, seq_lens, W_UK
         _ptr(workspace, None, "workspace", dev), workspace.numel() * workspace.element_size(),
         _ptr(out, torch.bfloat16, "out", dev), _ptr(lse_out, torch.float32, "lse_out", dev), _stream(stream))
     _check(st, "mla_decode")
+    return out, lse_out
+
+
+def decode_no_alloc(d: Dims, q_nope, q_pe, cache, scale_zero, block_table, seq_lens, W_UK, W_UV,
+                    softmax_scale: float, num_splits: int = 0, out: torch.Tensor | None = None,
+                    lse_out: torch.Tensor | None = None, device_status: torch.Tensor | None = None, stream=None):
+    """mla_decode_no_alloc: mla_decode on the library's fixed scratch array, for
+    callers that cannot allocate device memory (outputs are still the
+    caller's).  Returns (out, lse)."""
+    int8 = d.cache_dtype == MLA_CACHE_INT8
+    B = q_nope.shape[0]
+    dev = q_nope.device
+    if out is None:
+        out = torch.empty((B, d.num_heads, d.v_head_dim), dtype=torch.bfloat16, device=dev)
+    st = _L().mla_decode_no_alloc(
+        ctypes.byref(d), _ptr(q_nope, torch.bfloat16, "q_nope"), _ptr(q_pe, torch.bfloat16, "q_pe", dev),
+        _ptr(cache, torch.int8 if int8 else torch.bfloat16, "cache", dev),
+        _ptr(scale_zero, torch.float32, "scale_zero", dev) if int8 else None, cache.shape[0],
+        _ptr(block_table, torch.int32, "block_table", dev), block_table.shape[1],
+        _ptr(seq_lens, torch.int32, "seq_lens", dev), B, _ptr(W_UK, torch.bfloat16, "W_UK", dev),
+        _ptr(W_UV, torch.bfloat16, "W_UV", dev), float(softmax_scale), int(num_splits),
+        _ptr(out, torch.bfloat16, "out", dev), _ptr(lse_out, torch.float32, "lse_out", dev),
+        _ptr(device_status, torch.int32, "device_status", dev), _stream(stream))
+    _check(st, "mla_decode_no_alloc")
     return out, lse_out
 
 
