@@ -18,15 +18,17 @@
 // The same swizzled shared-memory tile, loaded once by TMA, is the A operand
 // of both products; each page is read from HBM once for all heads of the group.
 //
-// Warp roles (256 threads):
+// Warp roles (256 threads; INT8 caches 288):
 //   warp 0     TMA producer: Q of each segment, then each tile's pages
 //              (4 "pair" slots of two 64-wide latent boxes + 1 RoPE slot);
 //              it also prefetches the pages of the tiles two ahead into L2
 //              ("The Architecture of Memory", "Leveraging Tensor Cores and
 //              Asynchronous Prefetching")
-//   warp 1     TMEM allocation; lane 0 issues the MMAs
-//   warps 2-3  INT8 caches only: expand the TMA-loaded int8 codes in place
-//              into fp16 operand tiles
+//   warp 1     TMEM allocation; lane 0 issues the QK^T MMAs
+//   warp 2     lane 0 issues the PV MMAs (two issuers keep the tensor pipe
+//              busier than one with these small N = 16/32 MMAs)
+//   warps 3, 8 INT8 caches only (288 threads): expand the TMA-loaded int8
+//              codes in place into fp16 operand tiles
 //   warps 4-7  softmax (one thread per token row of S^T) and epilogue
 //
 // INT8 caches: value = s_t (code - zp_t) per token.  A code v in [-128, 127]
@@ -50,13 +52,17 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kThreads = 256;
+constexpr int kThreadsBf16 = 256;  // INT8 adds a ninth warp for code expansion
+constexpr int kThreadsInt8 = 288;
 constexpr uint32_t kBoxBytes = 16384;           // 128 rows x 128 B (64 bf16)
 constexpr uint32_t kPairBytes = 2 * kBoxBytes;  // latent dims [128c, 128c + 128)
 constexpr int kNumRope = 2;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 constexpr float kRescaleThreshold = 8.f;        // log2 units
-constexpr int kPrefetchTiles = 2;               // L2 prefetch distance (tiles)
+constexpr int kPrefetchTiles = 0;               // L2 prefetch distance (tiles); 0 = off
+// Cache pages are read once: the prefetch marks them evict-last so they
+// survive until the TMA reads them, and the TMA read marks them evict-first.
+constexpr bool kL2Hints = false;
 
 template <int HC>
 struct Cfg {
@@ -68,7 +74,7 @@ struct Cfg {
   static constexpr uint32_t kOffQ = kOffRope + kNumRope * kBoxBytes;
   static constexpr uint32_t kOffP = kOffQ + kQBytes;
   static constexpr uint32_t kOffMisc = kOffP + 2 * kPBytes;
-  static constexpr uint32_t kMiscBytes = 2048;
+  static constexpr uint32_t kMiscBytes = 4096;
   static constexpr uint32_t kSmem = kOffMisc + kMiscBytes + 1024;  // +1024: base alignment slack
   static constexpr uint32_t kTmemCols = HC == 16 ? 128 : 256;      // S^T x2 + O^T x4 = 6 * HC
   static constexpr uint32_t kColS = 0;                             // + buf * HC
@@ -78,7 +84,7 @@ struct Cfg {
 struct Barriers {
   uint64_t full_pair[5], empty_pair[5], full_rope[kNumRope], empty_rope[kNumRope];
   uint64_t full_i8_pair[5], full_i8_rope[kNumRope];  // INT8: TMA landed, codes not yet expanded
-  uint64_t q_full, q_empty, s_full[2], p_full[2], o_full, o_free, drain;
+  uint64_t q_full, q_empty, s_full[2], p_full[2], pv_done[2], o_full, o_free, drain[2];
   uint32_t tmem_base;
   int abort;
 };
@@ -107,6 +113,33 @@ __device__ __forceinline__ bool converters_any(bool pred) {  // OR over the 64 I
       : "r"(uint32_t(pred))
       : "memory");
   return r != 0;
+}
+__device__ __forceinline__ void converters_sync() { asm volatile("bar.sync 2, 64;" ::: "memory"); }
+
+// Reduces N (16 or 32) values per lane over the 32 lanes of a warp with
+// log2(32) exchange rounds in which every lane keeps half of its values and
+// trades the other half (N - 1 shuffles instead of 5 N).  Returns, in every
+// lane, the reduction of value index h = lane >> (32 / N - 1)... that is
+// h = lane / 2 for N = 16 (lanes 2h and 2h + 1) and h = lane for N = 32.
+template <int N, bool kMax>
+__device__ __forceinline__ float warp_transpose_reduce(float (&v)[N], int lane) {
+  static_assert(N == 16 || N == 32, "16 or 32 values per lane");
+#pragma unroll
+  for (int w = N / 2, o = 16; w >= 1; w >>= 1, o >>= 1) {
+    const bool upper = lane & o;
+#pragma unroll
+    for (int i = 0; i < w; ++i) {
+      const float keep = upper ? v[i + w] : v[i];
+      const float send = upper ? v[i] : v[i + w];
+      const float got = __shfl_xor_sync(0xffffffffu, send, o);
+      v[i] = kMax ? fmaxf(keep, got) : keep + got;
+    }
+  }
+  if (N == 16) {
+    const float got = __shfl_xor_sync(0xffffffffu, v[0], 1);
+    v[0] = kMax ? fmaxf(v[0], got) : v[0] + got;
+  }
+  return v[0];
 }
 
 __device__ __forceinline__ void fail(Barriers* B, int* status) {
@@ -143,17 +176,17 @@ __device__ __forceinline__ int page_of(const DecodeParams& p, int b, int tok) {
 }
 
 template <int HC, bool kInt8>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kInt8 ? kThreadsInt8 : kThreadsBf16, 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_cache, const __grid_constant__ CUtensorMap tmap_q,
                      DecodeParams p) {
   using C = Cfg<HC>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Barriers* B = reinterpret_cast<Barriers*>(smem + C::kOffMisc);
-  float* red = reinterpret_cast<float*>(smem + C::kOffMisc + 512);  // [2][4][HC] maxima, then [4][HC] sums
+  float* red = reinterpret_cast<float*>(smem + C::kOffMisc + 1024);  // [2][HC][4] maxima, [HC][4] sums x2
   const uint32_t sbase = smem_u32(smem);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  constexpr uint32_t kFullCount = kInt8 ? 64 : 1;  // INT8: the 64 expansion threads complete a slot
+  constexpr uint32_t kFullCount = 1;  // TMA (bf16) or the expansion warp's lane 0 (INT8) completes a slot
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::kNumPair; ++i) {
@@ -172,9 +205,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&B->s_full[i], 1);
       mbar_init(&B->p_full[i], 128);
     }
+    mbar_init(&B->pv_done[0], 1);
+    mbar_init(&B->pv_done[1], 1);
     mbar_init(&B->o_full, 1);
     mbar_init(&B->o_free, 128);
-    mbar_init(&B->drain, 1);
+    mbar_init(&B->drain[0], 1);
+    mbar_init(&B->drain[1], 1);
     B->abort = 0;
     fence_mbar_init();
     prefetch_tensormap(&tmap_cache);
@@ -202,13 +238,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     walk.init(p.tile_start, p.seg_base, p.len, p.batch, int(S), pa, pb);
     ahead = walk;
     const char* cache = static_cast<const char*>(p.cache);
+    const uint64_t pol_keep = policy_evict_last(), pol_stream = policy_evict_first();
     auto prefetch_tile = [&](const TileInfo& a) {
       const int npg = (a.valid + P - 1) / P;
       for (int i = 0; i < npg; ++i) {
         const int pg = page_of(p, a.b, a.tile * kTile + i * P);
-        prefetch_l2(cache + size_t(pg) * P * kRowBytes, uint32_t(P) * kRowBytes);
-        if (kInt8) prefetch_l2(p.scale_zero + size_t(pg) * P * 2, uint32_t(P) * 8);
+        if (kL2Hints) {
+          prefetch_l2_hint(cache + size_t(pg) * P * kRowBytes, uint32_t(P) * kRowBytes, pol_keep);
+          if (kInt8) prefetch_l2_hint(p.scale_zero + size_t(pg) * P * 2, uint32_t(P) * 8, pol_keep);
+        } else {
+          prefetch_l2(cache + size_t(pg) * P * kRowBytes, uint32_t(P) * kRowBytes);
+          if (kInt8) prefetch_l2(p.scale_zero + size_t(pg) * P * 2, uint32_t(P) * 8);
+        }
       }
+    };
+    auto load = [&](void* dst, int x, int y, uint64_t* bar) {
+      if (kL2Hints) tma_load_2d_hint(dst, &tmap_cache, x, y, bar, pol_stream);
+      else tma_load_2d(dst, &tmap_cache, x, y, bar);
     };
     TileInfo t, ta;
     for (int k = 0; k < kPrefetchTiles && ahead.next(ta); ++k) prefetch_tile(ta);
@@ -237,15 +283,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         if constexpr (!kInt8) {
           mbar_arrive_expect_tx(&B->full_pair[slot], 2 * npg * page_bytes);
           for (int i = 0; i < npg; ++i) {
-            tma_load_2d(dst + i * page_bytes, &tmap_cache, 128 * c, rows[i], &B->full_pair[slot]);
-            tma_load_2d(dst + kBoxBytes + i * page_bytes, &tmap_cache, 128 * c + 64, rows[i], &B->full_pair[slot]);
+            load(dst + i * page_bytes, 128 * c, rows[i], &B->full_pair[slot]);
+            load(dst + kBoxBytes + i * page_bytes, 128 * c + 64, rows[i], &B->full_pair[slot]);
           }
         } else {  // int8 codes of columns [128c, 128c + 128) into the slot's back half, as two [128 x 64 B] blocks
           mbar_arrive_expect_tx(&B->full_i8_pair[slot], npg * page_bytes);
           for (int i = 0; i < npg; ++i) {
-            tma_load_2d(dst + kBoxBytes + i * P * 64, &tmap_cache, 128 * c, rows[i], &B->full_i8_pair[slot]);
-            tma_load_2d(dst + kBoxBytes + 8192 + i * P * 64, &tmap_cache, 128 * c + 64, rows[i],
-                        &B->full_i8_pair[slot]);
+            load(dst + kBoxBytes + i * P * 64, 128 * c, rows[i], &B->full_i8_pair[slot]);
+            load(dst + kBoxBytes + 8192 + i * P * 64, 128 * c + 64, rows[i], &B->full_i8_pair[slot]);
           }
         }
       }
@@ -259,95 +304,133 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint8_t* dst = smem + C::kOffRope + slot * kBoxBytes;
         if constexpr (!kInt8) {
           mbar_arrive_expect_tx(&B->full_rope[slot], npg * page_bytes);
-          for (int i = 0; i < npg; ++i) tma_load_2d(dst + i * page_bytes, &tmap_cache, kLatent, rows[i], &B->full_rope[slot]);
+          for (int i = 0; i < npg; ++i) load(dst + i * page_bytes, kLatent, rows[i], &B->full_rope[slot]);
         } else {
           mbar_arrive_expect_tx(&B->full_i8_rope[slot], npg * P * 64);
           for (int i = 0; i < npg; ++i)
-            tma_load_2d(dst + 8192 + i * P * 64, &tmap_cache, kLatent, rows[i], &B->full_i8_rope[slot]);
+            load(dst + 8192 + i * P * 64, kLatent, rows[i], &B->full_i8_rope[slot]);
         }
         ++rope_it;
       }
     }
   } else if (warp == 1 && lane == 0) {
-    // ------------------------------------------------------------ MMA issuer
+    // ------------------------------------------------------------ QK issuer
+    // S^T[k & 1] = C_tile * Q^T, pair by pair as the data lands.  Before
+    // overwriting S^T[k & 1] it waits for the softmax of tile k - 2 (which
+    // read it) to finish.  Descriptors advance by one add per MMA.
     TileWalker walk;
     walk.init(p.tile_start, p.seg_base, p.len, p.batch, int(S), pa, pb);
     constexpr uint32_t id_qk = idesc_f32acc(128, HC, false, false, kInt8);
-    constexpr uint32_t id_pv = idesc_f32acc(128, HC, true, true, kInt8);
-    uint32_t pair_it = 0, rope_it = 0, tile_i = 0, seg = 0;
+    constexpr uint64_t kDescK = smem_desc(0, 16, 1024, kSwizzle128B);  // K-major SW128
+    uint32_t k = 0, seg = 0;
     TileInfo t;
     bool ok = true;
     while (ok && walk.next(t)) {
-      const uint32_t buf = tile_i & 1;
+      if (k >= 2 && !(ok = mbar_wait(&B->p_full[k & 1], ((k - 2) >> 1) & 1, abort_flag, kWaitLimitNs))) break;
       if (t.first && !(ok = mbar_wait(&B->q_full, seg & 1, abort_flag, kWaitLimitNs))) break;
-      tc_fence_after();
-      const uint32_t d_s = tmem + C::kColS + buf * HC;
-      for (int c = 0; c < 4; ++c) {
-        const uint32_t it = pair_it + c, slot = it % C::kNumPair;
+      const uint32_t d_s = tmem + C::kColS + (k & 1) * HC;
+      for (int c = 0; c < 4 && ok; ++c) {
+        const uint32_t it = 4 * k + c, slot = it % C::kNumPair;
         if (!(ok = mbar_wait(&B->full_pair[slot], (it / C::kNumPair) & 1, abort_flag, kWaitLimitNs))) break;
         tc_fence_after();
-        for (int half = 0; half < 2; ++half) {
-          const int j = 2 * c + half;
-          const uint32_t a0 = sbase + C::kOffPair + slot * kPairBytes + half * kBoxBytes;
-          const uint32_t b0 = sbase + C::kOffQ + j * HC * 128;
+        const uint64_t a0 = kDescK | ((sbase + C::kOffPair + slot * kPairBytes) >> 4);
+        const uint64_t b0 = kDescK | ((sbase + C::kOffQ + 2 * c * HC * 128) >> 4);
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
-            mma_bf16(d_s, smem_desc(a0 + 32 * k, 16, 1024, kSwizzle128B), smem_desc(b0 + 32 * k, 16, 1024, kSwizzle128B),
-                     id_qk, (j | k) != 0);
-        }
+        for (int kk = 0; kk < 4; ++kk) mma_bf16(d_s, a0 + 2 * kk, b0 + 2 * kk, id_qk, (c | kk) != 0);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) mma_bf16(d_s, a0 + kBoxBytes / 16 + 2 * kk, b0 + HC * 128 / 16 + 2 * kk, id_qk, 1);
       }
       if (!ok) break;
-      const uint32_t rslot = rope_it % kNumRope;
-      if (!(ok = mbar_wait(&B->full_rope[rslot], (rope_it / kNumRope) & 1, abort_flag, kWaitLimitNs))) break;
+      const uint32_t rslot = k % kNumRope;
+      if (!(ok = mbar_wait(&B->full_rope[rslot], (k / kNumRope) & 1, abort_flag, kWaitLimitNs))) break;
       tc_fence_after();
       {
-        const uint32_t a0 = sbase + C::kOffRope + rslot * kBoxBytes;
-        const uint32_t b0 = sbase + C::kOffQ + 8 * HC * 128;
+        const uint64_t a0 = kDescK | ((sbase + C::kOffRope + rslot * kBoxBytes) >> 4);
+        const uint64_t b0 = kDescK | ((sbase + C::kOffQ + 8 * HC * 128) >> 4);
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
-          mma_bf16(d_s, smem_desc(a0 + 32 * k, 16, 1024, kSwizzle128B), smem_desc(b0 + 32 * k, 16, 1024, kSwizzle128B),
-                   id_qk, 1);
+        for (int kk = 0; kk < 4; ++kk) mma_bf16(d_s, a0 + 2 * kk, b0 + 2 * kk, id_qk, 1);
       }
-      mma_commit(&B->s_full[buf]);
+      mma_commit(&B->s_full[k & 1]);
       mma_commit(&B->empty_rope[rslot]);
-      ++rope_it;
-      if (t.last) mma_commit(&B->q_empty);
-      // PV: O^T[c] (+)= C_tile^T[128c .. 128c + 128) * P^T
-      if (!(ok = mbar_wait(&B->p_full[buf], (tile_i >> 1) & 1, abort_flag, kWaitLimitNs))) break;
+      if (t.last) {
+        mma_commit(&B->q_empty);
+        ++seg;
+      }
+      ++k;
+    }
+    if (!ok) fail(B, p.status);
+    mma_commit(&B->drain[0]);  // every MMA this thread issued completes before teardown
+    mbar_wait(&B->drain[0], 0, abort_flag, kWaitLimitNs);
+  } else if (warp == 2 && lane == 0) {
+    // ------------------------------------------------------------ PV issuer
+    // O^T[c] (+)= C_tile^T[128c .. 128c + 128) * P^T once the softmax of the
+    // tile is done; each pair slot is released as soon as its MMAs complete.
+    TileWalker walk;
+    walk.init(p.tile_start, p.seg_base, p.len, p.batch, int(S), pa, pb);
+    constexpr uint32_t id_pv = idesc_f32acc(128, HC, true, true, kInt8);
+    constexpr uint64_t kDescMN = smem_desc(0, kBoxBytes, 1024, kSwizzle128B);  // MN-major SW128
+    constexpr uint64_t kDescP = smem_desc(0, 128, 2048, kSwizzleNone);        // P^T core matrices
+    uint32_t k = 0, seg = 0;
+    TileInfo t;
+    bool ok = true;
+    while (ok && walk.next(t)) {
+      if (!(ok = mbar_wait(&B->p_full[k & 1], (k >> 1) & 1, abort_flag, kWaitLimitNs))) break;
       if (t.first && seg > 0 && !(ok = mbar_wait(&B->o_free, (seg - 1) & 1, abort_flag, kWaitLimitNs))) break;
       tc_fence_after();
       const int nk = (t.valid + 15) >> 4;
-      const uint32_t pbase = sbase + C::kOffP + buf * C::kPBytes;
+      const uint64_t bd = kDescP | ((sbase + C::kOffP + (k & 1) * C::kPBytes) >> 4);
+#pragma unroll
       for (int c = 0; c < 4; ++c) {
-        const uint32_t slot = (pair_it + c) % C::kNumPair;
-        const uint32_t a0 = sbase + C::kOffPair + slot * kPairBytes;
-        for (int k = 0; k < nk; ++k)
-          mma_bf16(tmem + C::kColO + c * HC, smem_desc(a0 + 2048 * k, kBoxBytes, 1024, kSwizzle128B),
-                   smem_desc(pbase + 256 * k, 128, 2048, kSwizzleNone), id_pv, !(t.first && k == 0));
+        const uint32_t slot = (4 * k + c) % C::kNumPair;
+        const uint64_t ad = kDescMN | ((sbase + C::kOffPair + slot * kPairBytes) >> 4);
+        const uint32_t d_o = tmem + C::kColO + c * HC;
+        if (nk == 8) {
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) mma_bf16(d_o, ad + 128 * kk, bd + 16 * kk, id_pv, !(t.first && kk == 0));
+        } else {
+          for (int kk = 0; kk < nk; ++kk) mma_bf16(d_o, ad + 128 * kk, bd + 16 * kk, id_pv, !(t.first && kk == 0));
+        }
         mma_commit(&B->empty_pair[slot]);
       }
-      pair_it += 4;
+      mma_commit(&B->pv_done[k & 1]);
       if (t.last) {
         mma_commit(&B->o_full);
         ++seg;
       }
-      ++tile_i;
+      ++k;
     }
     if (!ok) fail(B, p.status);
-    // all issued MMAs complete before teardown
-    mma_commit(&B->drain);
-    mbar_wait(&B->drain, 0, abort_flag, kWaitLimitNs);
-  } else if (kInt8 && (warp == 2 || warp == 3)) {
+    mma_commit(&B->drain[1]);
+    mbar_wait(&B->drain[1], 0, abort_flag, kWaitLimitNs);
+  } else if (kInt8 && (warp == 3 || warp == 8)) {
     // ------------------------------------------------------------ INT8 expansion
-    // Thread ct reads 16-byte chunk (ct % 4) of rows ct/4 + 16j of each
-    // [128 x 64 B] code block, then writes the 16 fp16 values into the
-    // swizzled operand box at the same rows.
-    const int ct = threadIdx.x - 64, ch = ct & 3, r0 = ct >> 2;
+    // Warps 3 and 8 turn each landed [128 x 64 B] code block into a swizzled
+    // fp16 operand box.  Pair slots hold the codes of boxes 2c and 2c+1 in
+    // their back half: block 0 (at +16 KB) expands into [0, 16 KB) without
+    // overlap; block 1 (at +24 KB) overlaps its destination, so all 64
+    // threads read it before any of them writes.  The RoPE slot's block sits
+    // at +8 KB and overlaps too.
+    const int ct = (warp == 3 ? 0 : 32) + lane, ch = ct & 3, r0 = ct >> 2;  // rows r0 + 16j
     TileWalker walk;
     walk.init(p.tile_start, p.seg_base, p.len, p.batch, int(S), pa, pb);
     uint32_t pair_it = 0, rope_it = 0;
     TileInfo t;
     bool ok = true;
+    auto read_block = [&](const uint8_t* src, uint4 (&v)[8]) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[j] = *reinterpret_cast<const uint4*>(src + (r0 + 16 * j) * 64 + ch * 16);
+    };
+    auto write_block = [&](const uint4 (&v)[8], uint8_t* dst) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int r = r0 + 16 * j;
+        uint4 lo, hi;
+        expand_codes(v[j], lo, hi);
+        uint8_t* row = dst + r * 128;
+        *reinterpret_cast<uint4*>(row + (((2 * ch) ^ (r & 7)) << 4)) = lo;
+        *reinterpret_cast<uint4*>(row + (((2 * ch + 1) ^ (r & 7)) << 4)) = hi;
+      }
+    };
     while (ok && walk.next(t)) {
       for (int c = 0; c < 5 && ok; ++c) {
         const bool rope = c == 4;
@@ -356,39 +439,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint64_t* full_i8 = rope ? &B->full_i8_rope[slot] : &B->full_i8_pair[slot];
         uint8_t* base = smem + (rope ? C::kOffRope + slot * kBoxBytes : C::kOffPair + slot * kPairBytes);
         const bool landed = mbar_wait(full_i8, (it / nslot) & 1, abort_flag, kWaitLimitNs);
-        const int nblk = rope ? 1 : 2;
-        const uint8_t* src = base + (rope ? 8192 : kBoxBytes);
-        uint4 v[16];
-#pragma unroll
-        for (int k = 0; k < 2; ++k)
-#pragma unroll
-          for (int j = 0; j < 8; ++j)
-            if (k < nblk) v[k * 8 + j] = *reinterpret_cast<const uint4*>(src + k * 8192 + (r0 + 16 * j) * 64 + ch * 16);
-        // every thread has read its codes before the expansion overwrites them;
-        // a timeout anywhere stops all 64 threads together
+        uint4 v[8];
+        if (!rope) {
+          read_block(base + kBoxBytes, v);
+          write_block(v, base);
+        }
+        read_block(base + (rope ? 8192 : kBoxBytes + 8192), v);
+        // all codes of the overlapping block read before any write; a timeout
+        // anywhere stops the 64 threads together
         if (converters_any(!landed)) {
           ok = false;
           break;
         }
-#pragma unroll
-        for (int k = 0; k < 2; ++k)
-#pragma unroll
-          for (int j = 0; j < 8; ++j)
-            if (k < nblk) {
-              const int r = r0 + 16 * j;
-              uint4 lo, hi;
-              expand_codes(v[k * 8 + j], lo, hi);
-              uint8_t* row = base + k * kBoxBytes + r * 128;
-              *reinterpret_cast<uint4*>(row + (((2 * ch) ^ (r & 7)) << 4)) = lo;
-              *reinterpret_cast<uint4*>(row + (((2 * ch + 1) ^ (r & 7)) << 4)) = hi;
-            }
+        write_block(v, base + (rope ? 0 : kBoxBytes));
         fence_proxy_async_smem();
-        mbar_arrive(rope ? &B->full_rope[slot] : &B->full_pair[slot]);
+        converters_sync();
+        if (ct == 0) mbar_arrive(rope ? &B->full_rope[slot] : &B->full_pair[slot]);
         if (rope) ++rope_it; else ++pair_it;
       }
-      if (!ok) fail(B, p.status);
     }
-  } else if (warp >= 4) {
+    if (!ok) fail(B, p.status);
+  } else if (warp >= 4 && warp < 8) {
     // ------------------------------------------------------------ softmax / epilogue
     const int q4 = warp - 4, st = threadIdx.x - 128;  // st = token row of S^T = TMEM lane
     const uint32_t lane_off = uint32_t(q4 * 32) << 16;
@@ -413,7 +484,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           tok_z = sz.y;
         }
       }
-      const bool ok = mbar_wait(&B->s_full[buf], (tile_i >> 1) & 1, abort_flag, kWaitLimitNs);
+      // S^T of this tile; and PV of tile k - 2, which read the P^T buffer
+      // this tile writes, must be complete
+      bool ok = mbar_wait(&B->s_full[buf], (tile_i >> 1) & 1, abort_flag, kWaitLimitNs);
+      if (tile_i >= 2) ok = ok && mbar_wait(&B->pv_done[buf], ((tile_i - 2) >> 1) & 1, abort_flag, kWaitLimitNs);
       tc_fence_after();
       float x[HC];
       if (ok) {
@@ -431,37 +505,56 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float raw = kInt8 ? fmaf(-tok_z, qsum[h], x[h]) : x[h];
         x[h] = valid ? raw * row_scale : -INFINITY;
       }
-      // tile max per head: warp butterfly, then across the 4 warps through shared memory
-      float* rm = red + buf * 4 * HC;
+      // Running max.  It only has to bound the scores to within
+      // kRescaleThreshold (log2 units), so in the common case every thread
+      // checks its own scores against it and the 128 threads OR that flag in
+      // the barrier they need anyway.  The first tile of a segment, and a
+      // tile that breaks the bound, take the exact path: per-head tile max
+      // (transpose-reduce in the warp, then across the 4 warps through shared
+      // memory) and, where the max moved, a rescale of O^T and l.
+      bool over = false;
+      if (!t.first) {
 #pragma unroll
-      for (int h = 0; h < HC; ++h) {
-        float v = x[h];
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-        if (lane == (h & 31)) rm[q4 * HC + h] = v;
+        for (int h = 0; h < HC; ++h) over |= x[h] > m_run[h] + kRescaleThreshold;
       }
-      if (bar_any(!ok)) break;
       float alpha[HC];
       bool rescale = false;
+      if (t.first || bar_any(over || !ok)) {
+        float* rm = red + buf * 4 * HC;
+        {
+          float tmp[HC];
 #pragma unroll
-      for (int h = 0; h < HC; ++h) {
-        const float mt = fmaxf(fmaxf(rm[h], rm[HC + h]), fmaxf(rm[2 * HC + h], rm[3 * HC + h]));
-        if (t.first) {
-          m_run[h] = mt;
-          l_run[h] = 0.f;
-          corr[h] = 0.f;
-          alpha[h] = 1.f;
-        } else if (mt > m_run[h] + kRescaleThreshold) {
-          alpha[h] = exp2f(m_run[h] - mt);
-          m_run[h] = mt;
-          l_run[h] *= alpha[h];
-          corr[h] *= alpha[h];
-          rescale = true;
-        } else {
-          alpha[h] = 1.f;
+          for (int h = 0; h < HC; ++h) tmp[h] = x[h];
+          const float wm = warp_transpose_reduce<HC, true>(tmp, lane);
+          if (HC == 32 || !(lane & 1)) rm[(HC == 32 ? lane : lane >> 1) * 4 + q4] = wm;
+        }
+        if (bar_any(!ok)) break;
+#pragma unroll
+        for (int h = 0; h < HC; ++h) {
+          const float4 m4 = reinterpret_cast<const float4*>(rm)[h];
+          const float mt = fmaxf(fmaxf(m4.x, m4.y), fmaxf(m4.z, m4.w));
+          if (t.first) {
+            m_run[h] = mt;
+            l_run[h] = 0.f;
+            corr[h] = 0.f;
+            alpha[h] = 1.f;
+          } else if (mt > m_run[h] + kRescaleThreshold) {
+            alpha[h] = exp2f(m_run[h] - mt);
+            m_run[h] = mt;
+            l_run[h] *= alpha[h];
+            corr[h] *= alpha[h];
+            rescale = true;
+          } else {
+            alpha[h] = 1.f;
+          }
         }
       }
-      if (rescale) {  // uniform across the 128 threads; PV of the previous tile is complete
+      if (rescale) {
+        // uniform across the 128 threads.  QK of this tile may have been
+        // issued before PV of the previous one: wait for that PV first.
+        const bool ok3 = mbar_wait(&B->pv_done[(tile_i - 1) & 1], ((tile_i - 1) >> 1) & 1, abort_flag, kWaitLimitNs);
+        tc_fence_after();
+        if (bar_any(!ok3)) break;
 #pragma unroll
         for (int c = 0; c < 4; ++c)
 #pragma unroll
@@ -522,26 +615,33 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (t.last) {
         const bool ok2 = mbar_wait(&B->o_full, seg & 1, abort_flag, kWaitLimitNs);
         tc_fence_after();
-        float* rl = red + 8 * HC;  // [4][HC] sums of l, then (INT8) [4][HC] sums of corr
+        float* rl = red + 8 * HC;   // [HC][4] sums of l
+        float* rc = red + 12 * HC;  // [HC][4] sums of corr (INT8)
+        {
+          const int hw = HC == 32 ? lane : lane >> 1;
+          const bool writer = HC == 32 || !(lane & 1);
+          float tmp[HC];
 #pragma unroll
-        for (int h = 0; h < HC; ++h) {
-          float v = l_run[h];
-#pragma unroll
-          for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-          if (lane == (h & 31)) rl[q4 * HC + h] = v;
+          for (int h = 0; h < HC; ++h) tmp[h] = l_run[h];
+          const float ls = warp_transpose_reduce<HC, false>(tmp, lane);
+          if (writer) rl[hw * 4 + q4] = ls;
           if (kInt8) {
-            float c = corr[h];
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
-            if (lane == (h & 31)) rl[4 * HC + q4 * HC + h] = c;
+            for (int h = 0; h < HC; ++h) tmp[h] = corr[h];
+            const float cs = warp_transpose_reduce<HC, false>(tmp, lane);
+            if (writer) rc[hw * 4 + q4] = cs;
           }
         }
         if (bar_any(!ok2)) break;
         float inv_l[HC];
 #pragma unroll
         for (int h = 0; h < HC; ++h) {
-          inv_l[h] = 1.f / (rl[h] + rl[HC + h] + rl[2 * HC + h] + rl[3 * HC + h]);
-          if (kInt8) corr[h] = rl[4 * HC + h] + rl[5 * HC + h] + rl[6 * HC + h] + rl[7 * HC + h];
+          const float4 l4 = reinterpret_cast<const float4*>(rl)[h];
+          inv_l[h] = 1.f / ((l4.x + l4.y) + (l4.z + l4.w));
+          if (kInt8) {
+            const float4 c4 = reinterpret_cast<const float4*>(rc)[h];
+            corr[h] = (c4.x + c4.y) + (c4.z + c4.w);
+          }
         }
         float* dst = p.partial_o + (size_t(t.seg) * p.heads + g * HC) * kLatent;
 #pragma unroll
@@ -623,7 +723,7 @@ cudaError_t launch_tc(const DecodeParams& p, int grid, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 128) attr[dev] = true;
   }
-  decode_tc_kernel<HC, kInt8><<<grid, kThreads, Cfg<HC>::kSmem, stream>>>(mc, mq, p);
+  decode_tc_kernel<HC, kInt8><<<grid, kInt8 ? kThreadsInt8 : kThreadsBf16, Cfg<HC>::kSmem, stream>>>(mc, mq, p);
   return cudaGetLastError();
 }
 
