@@ -15,20 +15,33 @@
 // padded (16 or 32 heads per CTA):
 //     S^T [128 tok x HC]  = C_tile [128 x 576]  * Q^T       (A K-major)
 //     O^T [512 x HC]     += C_tile^T [512 x 128] * P^T      (A MN-major)
-// The same swizzled shared-memory tile, loaded once by TMA, is the A operand
-// of both products; each page is read from HBM once for all heads of the group.
+// Each page is read from HBM once for all heads of the group.
 //
-// Warp roles (256 threads; INT8 caches 288):
-//   warp 0     TMA producer: Q of each segment, then each tile's pages
-//              (4 "pair" slots of two 64-wide latent boxes + 1 RoPE slot);
-//              it also prefetches the pages of the tiles two ahead into L2
-//              ("The Architecture of Memory", "Leveraging Tensor Cores and
-//              Asynchronous Prefetching")
+// bf16 caches: two shared-memory rings.  The QK ring holds single 64-column
+// boxes ([128 tok x 64] SW128, 16 KB); every box is released as soon as its
+// four QK MMAs complete, so HBM reads never wait for the softmax.  The PV ring
+// holds pairs of latent boxes (128 columns = one O^T chunk) that a second
+// producer reads again for the PV product, from L2 (the QK read a few
+// microseconds earlier brought the lines there).  A single ring serving both
+// products has to keep a whole 147 KB tile resident from its QK until its
+// PV, which serialises load -> QK -> softmax -> PV per tile.
+// INT8 caches (73 KB per tile): one ring of pair slots + RoPE slots serves
+// both products; the codes are expanded in place.
+//
+// Warp roles (288 threads; 256 for 32-head bf16 groups):
+//   warp 0     TMA producer: Q of each segment; bf16: QK ring 0 (16 heads:
+//              boxes 0, 2, 4, 6, 8 of each tile; 32 heads: all 9 boxes);
+//              INT8: the pair and RoPE slots (codes)
 //   warp 1     TMEM allocation; lane 0 issues the QK^T MMAs
-//   warp 2     lane 0 issues the PV MMAs (two issuers keep the tensor pipe
-//              busier than one with these small N = 16/32 MMAs)
-//   warps 3, 8 INT8 caches only (288 threads): expand the TMA-loaded int8
-//              codes in place into fp16 operand tiles
+//   warp 2     PV: lane 0 issues the MMAs (a second issuer keeps the tensor
+//              pipe busier than one with these small N = 16/32 MMAs); bf16:
+//              the warp also clears the ragged tail rows of the last tile
+//   warp 3     bf16, 16 heads: QK ring 1 producer (boxes 1, 3, 5, 7): one
+//              thread cannot issue TMA copies fast enough for an SM's share
+//              of HBM; bf16, 32 heads: the PV-ring producer
+//   warp 8     bf16, 16 heads: the PV-ring producer
+//   warps 3, 8 INT8: expand the TMA-loaded int8 codes in place into fp16
+//              operand tiles
 //   warps 4-7  softmax (one thread per token row of S^T) and epilogue
 //
 // INT8 caches: value = s_t (code - zp_t) per token.  A code v in [-128, 127]
@@ -52,24 +65,34 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kThreadsBf16 = 256;  // INT8 adds a ninth warp for code expansion
-constexpr int kThreadsInt8 = 288;
+// Nine warps leave three on one SM sub-partition (16K registers each), which
+// caps a thread at 168 registers: enough except for the 32-head bf16 softmax,
+// which runs with eight warps and a single QK producer.
 constexpr uint32_t kBoxBytes = 16384;           // 128 rows x 128 B (64 bf16)
 constexpr uint32_t kPairBytes = 2 * kBoxBytes;  // latent dims [128c, 128c + 128)
-constexpr int kNumRope = 2;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 constexpr float kRescaleThreshold = 8.f;        // log2 units
-constexpr int kPrefetchTiles = 0;               // L2 prefetch distance (tiles); 0 = off
-// Cache pages are read once: the prefetch marks them evict-last so they
-// survive until the TMA reads them, and the TMA read marks them evict-first.
+// bf16: the QK read of a page is its first use and the PV read its last; the
+// hints keep the lines in L2 between the two and let them go after.
 constexpr bool kL2Hints = false;
+// bf16: the PV-ring producer reads tile k only once tile k's last QK box has
+// landed (when true).  A gated PV read finds its lines in L2 and holds its
+// ring slot only for an L2 round trip before the PV MMAs need it.
+constexpr bool kPvGate = true;
 
-template <int HC>
+template <int HC, bool kInt8>
 struct Cfg {
-  static constexpr int kNumPair = HC == 16 ? 5 : 4;
+  static constexpr int kThreads = (kInt8 || HC == 16) ? 288 : 256;
+  static constexpr int kQkRings = (!kInt8 && HC == 16) ? 2 : 1;   // bf16 QK producers (rings)
+  static constexpr int kQkSlots = kInt8 ? 0 : 6;                  // bf16 QK ring slots (single boxes), all rings
+  static constexpr int kQkRing = kQkSlots / kQkRings;
+  static constexpr int kPvProducerWarp = kQkRings == 2 ? 8 : 3;
+  static constexpr int kNumPair = kInt8 ? 5 : (HC == 16 ? 3 : 2);  // bf16 PV ring / INT8 shared ring
+  static constexpr int kNumRope = kInt8 ? 2 : 0;
   static constexpr uint32_t kQBytes = 9 * HC * 128;
   static constexpr uint32_t kPBytes = kTile * HC * 2;
-  static constexpr uint32_t kOffPair = 0;
+  static constexpr uint32_t kOffQk = 0;
+  static constexpr uint32_t kOffPair = kOffQk + kQkSlots * kBoxBytes;
   static constexpr uint32_t kOffRope = kOffPair + kNumPair * kPairBytes;
   static constexpr uint32_t kOffQ = kOffRope + kNumRope * kBoxBytes;
   static constexpr uint32_t kOffP = kOffQ + kQBytes;
@@ -79,15 +102,38 @@ struct Cfg {
   static constexpr uint32_t kTmemCols = HC == 16 ? 128 : 256;      // S^T x2 + O^T x4 = 6 * HC
   static constexpr uint32_t kColS = 0;                             // + buf * HC
   static constexpr uint32_t kColO = 2 * HC;                        // + c * HC
+  static_assert(kSmem <= 232448, "dynamic shared memory of one CTA");
+  static_assert(kQkRing <= 8 && kNumPair <= 5 && kNumRope <= 2, "barrier arrays");
 };
 
 struct Barriers {
-  uint64_t full_pair[5], empty_pair[5], full_rope[kNumRope], empty_rope[kNumRope];
-  uint64_t full_i8_pair[5], full_i8_rope[kNumRope];  // INT8: TMA landed, codes not yet expanded
+  uint64_t full_qk[2][8], empty_qk[2][8];            // bf16 QK rings
+  uint64_t full_pair[5], empty_pair[5];              // bf16 PV ring; INT8 shared ring
+  uint64_t full_rope[2], empty_rope[2];              // INT8
+  uint64_t full_i8_pair[5], full_i8_rope[2];         // INT8: TMA landed, codes not yet expanded
   uint64_t q_full, q_empty, s_full[2], p_full[2], pv_done[2], o_full, o_free, drain[2];
   uint32_t tmem_base;
   int abort;
+  int qk_progress;  // bf16: tiles the QK side has finished with (see kPvGate)
 };
+
+__device__ __forceinline__ void publish_progress(int* counter, int value) {
+  *reinterpret_cast<volatile int*>(counter) = value;
+}
+// Waits until *counter > k; false on abort or after limit_ns.
+__device__ __forceinline__ bool wait_progress(const int* counter, int k, const volatile int* abort,
+                                              uint64_t limit_ns) {
+  const volatile int* c = counter;
+  if (*c > k) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (*c > k) return true;
+    if ((i & 63) == 0) {
+      if (*abort) return false;
+      if (global_timer_ns() - t0 > limit_ns) return false;
+    }
+  }
+}
 
 __device__ __forceinline__ bool bar_any(bool pred) {  // OR over the 128 softmax threads (named barrier 1)
   uint32_t r;
@@ -175,11 +221,34 @@ __device__ __forceinline__ int page_of(const DecodeParams& p, int b, int tok) {
   return pg;
 }
 
+// Physical pages of one tile, loaded a tile before they are needed: a
+// producer that read the block table just in time would stall a full global
+// load latency at every tile.  Checked (and clamped to page 0) at use.
+struct TilePages {
+  int raw[kTile / 16];
+  int npg;
+  __device__ __forceinline__ void fetch(const DecodeParams& p, const TileInfo& a) {
+    npg = (a.valid + p.page_size - 1) / p.page_size;
+    const int* bt = p.block_table + size_t(a.b) * p.max_pages + a.tile * (kTile / p.page_size);
+#pragma unroll
+    for (int i = 0; i < kTile / 16; ++i) raw[i] = i < npg ? __ldg(bt + i) : 0;
+  }
+  // first cache row (page * P) of page i of the tile
+  __device__ __forceinline__ int row(const DecodeParams& p, int i) const {
+    int pg = raw[i];
+    if (pg < 0 || pg >= p.num_pages) {
+      set_status(p.status, MLA_ERR_DEVICE_BOUNDS);
+      pg = 0;
+    }
+    return pg * p.page_size;
+  }
+};
+
 template <int HC, bool kInt8>
-__global__ void __launch_bounds__(kInt8 ? kThreadsInt8 : kThreadsBf16, 1)
+__global__ void __launch_bounds__(Cfg<HC, kInt8>::kThreads, 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_cache, const __grid_constant__ CUtensorMap tmap_q,
                      DecodeParams p) {
-  using C = Cfg<HC>;
+  using C = Cfg<HC, kInt8>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Barriers* B = reinterpret_cast<Barriers*>(smem + C::kOffMisc);
@@ -189,12 +258,17 @@ __global__ void __launch_bounds__(kInt8 ? kThreadsInt8 : kThreadsBf16, 1)
   constexpr uint32_t kFullCount = 1;  // TMA (bf16) or the expansion warp's lane 0 (INT8) completes a slot
 
   if (threadIdx.x == 0) {
+    for (int r = 0; r < C::kQkRings; ++r)
+      for (int i = 0; i < C::kQkRing; ++i) {
+        mbar_init(&B->full_qk[r][i], 1);
+        mbar_init(&B->empty_qk[r][i], 1);
+      }
     for (int i = 0; i < C::kNumPair; ++i) {
       mbar_init(&B->full_pair[i], kFullCount);
       mbar_init(&B->empty_pair[i], 1);
       mbar_init(&B->full_i8_pair[i], 1);
     }
-    for (int i = 0; i < kNumRope; ++i) {
+    for (int i = 0; i < C::kNumRope; ++i) {
       mbar_init(&B->full_rope[i], kFullCount);
       mbar_init(&B->empty_rope[i], 1);
       mbar_init(&B->full_i8_rope[i], 1);
@@ -212,6 +286,7 @@ __global__ void __launch_bounds__(kInt8 ? kThreadsInt8 : kThreadsBf16, 1)
     mbar_init(&B->drain[0], 1);
     mbar_init(&B->drain[1], 1);
     B->abort = 0;
+    B->qk_progress = 0;
     fence_mbar_init();
     prefetch_tensormap(&tmap_cache);
     prefetch_tensormap(&tmap_q);
@@ -230,128 +305,181 @@ __global__ void __launch_bounds__(kInt8 ? kThreadsInt8 : kThreadsBf16, 1)
   const long long pa = (cp * S) / Cp, pb = ((cp + 1) * S) / Cp;
   const volatile int* abort_flag = &B->abort;
   const int P = p.page_size;
-  constexpr uint32_t kRowBytes = kInt8 ? kRow : 2 * kRow;
 
-  if (warp == 0 && lane == 0) {
-    // ------------------------------------------------------------ producer
-    TileWalker walk, ahead;
+  if ((warp == 0 || (C::kQkRings == 2 && warp == 3)) && lane == 0) {
+    // ------------------------------------------------------------ producers
+    // bf16, 16 heads: warp 0 fills QK ring 0 with boxes 0, 2, 4, 6, 8 of
+    // every tile (and loads Q), warp 3 fills ring 1 with boxes 1, 3, 5, 7:
+    // one thread cannot issue TMA copies fast enough to stream an SM's share
+    // of HBM and also keep up with the rest of the kernel.
+    const int qr = warp == 0 ? 0 : 1;
+    TileWalker walk;
     walk.init(p.tile_start, p.seg_base, p.len, p.batch, int(S), pa, pb);
-    ahead = walk;
-    const char* cache = static_cast<const char*>(p.cache);
-    const uint64_t pol_keep = policy_evict_last(), pol_stream = policy_evict_first();
-    auto prefetch_tile = [&](const TileInfo& a) {
-      const int npg = (a.valid + P - 1) / P;
-      for (int i = 0; i < npg; ++i) {
-        const int pg = page_of(p, a.b, a.tile * kTile + i * P);
-        if (kL2Hints) {
-          prefetch_l2_hint(cache + size_t(pg) * P * kRowBytes, uint32_t(P) * kRowBytes, pol_keep);
-          if (kInt8) prefetch_l2_hint(p.scale_zero + size_t(pg) * P * 2, uint32_t(P) * 8, pol_keep);
-        } else {
-          prefetch_l2(cache + size_t(pg) * P * kRowBytes, uint32_t(P) * kRowBytes);
-          if (kInt8) prefetch_l2(p.scale_zero + size_t(pg) * P * 2, uint32_t(P) * 8);
-        }
-      }
-    };
+    const uint64_t pol_keep = policy_evict_last();
     auto load = [&](void* dst, int x, int y, uint64_t* bar) {
-      if (kL2Hints) tma_load_2d_hint(dst, &tmap_cache, x, y, bar, pol_stream);
+      if (kL2Hints && !kInt8) tma_load_2d_hint(dst, &tmap_cache, x, y, bar, pol_keep);
       else tma_load_2d(dst, &tmap_cache, x, y, bar);
     };
-    TileInfo t, ta;
-    for (int k = 0; k < kPrefetchTiles && ahead.next(ta); ++k) prefetch_tile(ta);
     const uint32_t page_bytes = uint32_t(P) * 128;  // one 64-column box of P rows (bf16)
-    uint32_t pair_it = 0, rope_it = 0, seg = 0;
-    while (walk.next(t)) {
-      if (ahead.next(ta)) prefetch_tile(ta);
-      if (t.first) {
-        if (seg > 0 && !mbar_wait(&B->q_empty, (seg - 1) & 1, abort_flag, kWaitLimitNs)) { fail(B, p.status); break; }
+    uint32_t box_it = 0, pair_it = 0, rope_it = 0, seg = 0;
+    TileInfo t, tn;
+    TileWalker look = walk;
+    TilePages pages, next_pages;
+    if (look.next(tn)) next_pages.fetch(p, tn);
+    bool ok = true;
+    while (ok && walk.next(t)) {
+      pages = next_pages;
+      if (look.next(tn)) next_pages.fetch(p, tn);
+      if (t.first && qr == 0) {
+        if (seg > 0 && !(ok = mbar_wait(&B->q_empty, (seg - 1) & 1, abort_flag, kWaitLimitNs))) break;
         mbar_arrive_expect_tx(&B->q_full, C::kQBytes);
         const int qrow = t.b * p.heads + g * HC;
         for (int j = 0; j < 9; ++j) tma_load_2d(smem + C::kOffQ + j * HC * 128, &tmap_q, 64 * j, qrow, &B->q_full);
         ++seg;
       }
-      const int npg = (t.valid + P - 1) / P;
+      const int npg = pages.npg;
       int rows[kTile / 16];
-      for (int i = 0; i < npg; ++i) rows[i] = page_of(p, t.b, t.tile * kTile + i * P) * P;
-      bool ok = true;
-      for (int c = 0; c < 4 && ok; ++c, ++pair_it) {
-        const uint32_t slot = pair_it % C::kNumPair;
-        if (!mbar_wait(&B->empty_pair[slot], ((pair_it / C::kNumPair) & 1) ^ 1, abort_flag, kWaitLimitNs)) {
-          ok = false;
-          break;
+#pragma unroll
+      for (int i = 0; i < kTile / 16; ++i) rows[i] = i < npg ? pages.row(p, i) : 0;
+      if constexpr (!kInt8) {
+        // the tile's boxes j = qr, qr + 2, ...: latent columns [64j, 64j + 64), box 8 the RoPE key
+        for (int j = qr; j < 9; j += C::kQkRings, ++box_it) {
+          const uint32_t slot = box_it % C::kQkRing;
+          if (!(ok = mbar_wait(&B->empty_qk[qr][slot], ((box_it / C::kQkRing) & 1) ^ 1, abort_flag, kWaitLimitNs)))
+            break;
+          uint8_t* dst = smem + C::kOffQk + (qr * C::kQkRing + slot) * kBoxBytes;
+          mbar_arrive_expect_tx(&B->full_qk[qr][slot], npg * page_bytes);
+#pragma unroll
+          for (int i = 0; i < kTile / 16; ++i)
+            if (i < npg) load(dst + i * page_bytes, 64 * j, rows[i], &B->full_qk[qr][slot]);
         }
-        uint8_t* dst = smem + C::kOffPair + slot * kPairBytes;
-        if constexpr (!kInt8) {
-          mbar_arrive_expect_tx(&B->full_pair[slot], 2 * npg * page_bytes);
-          for (int i = 0; i < npg; ++i) {
-            load(dst + i * page_bytes, 128 * c, rows[i], &B->full_pair[slot]);
-            load(dst + kBoxBytes + i * page_bytes, 128 * c + 64, rows[i], &B->full_pair[slot]);
-          }
-        } else {  // int8 codes of columns [128c, 128c + 128) into the slot's back half, as two [128 x 64 B] blocks
+      } else {
+        for (int c = 0; c < 4; ++c, ++pair_it) {
+          const uint32_t slot = pair_it % C::kNumPair;
+          if (!(ok = mbar_wait(&B->empty_pair[slot], ((pair_it / C::kNumPair) & 1) ^ 1, abort_flag, kWaitLimitNs)))
+            break;
+          // int8 codes of columns [128c, 128c + 128) into the slot's back half, as two [128 x 64 B] blocks
+          uint8_t* dst = smem + C::kOffPair + slot * kPairBytes;
           mbar_arrive_expect_tx(&B->full_i8_pair[slot], npg * page_bytes);
-          for (int i = 0; i < npg; ++i) {
-            load(dst + kBoxBytes + i * P * 64, 128 * c, rows[i], &B->full_i8_pair[slot]);
-            load(dst + kBoxBytes + 8192 + i * P * 64, 128 * c + 64, rows[i], &B->full_i8_pair[slot]);
-          }
+#pragma unroll
+          for (int i = 0; i < kTile / 16; ++i)
+            if (i < npg) {
+              load(dst + kBoxBytes + i * P * 64, 128 * c, rows[i], &B->full_i8_pair[slot]);
+              load(dst + kBoxBytes + 8192 + i * P * 64, 128 * c + 64, rows[i], &B->full_i8_pair[slot]);
+            }
         }
-      }
-      if (!ok) { fail(B, p.status); break; }
-      {
-        const uint32_t slot = rope_it % kNumRope;
-        if (!mbar_wait(&B->empty_rope[slot], ((rope_it / kNumRope) & 1) ^ 1, abort_flag, kWaitLimitNs)) {
-          fail(B, p.status);
+        if (!ok) break;
+        const uint32_t slot = rope_it % C::kNumRope;
+        if (!(ok = mbar_wait(&B->empty_rope[slot], ((rope_it / C::kNumRope) & 1) ^ 1, abort_flag, kWaitLimitNs)))
           break;
-        }
         uint8_t* dst = smem + C::kOffRope + slot * kBoxBytes;
-        if constexpr (!kInt8) {
-          mbar_arrive_expect_tx(&B->full_rope[slot], npg * page_bytes);
-          for (int i = 0; i < npg; ++i) load(dst + i * page_bytes, kLatent, rows[i], &B->full_rope[slot]);
-        } else {
-          mbar_arrive_expect_tx(&B->full_i8_rope[slot], npg * P * 64);
-          for (int i = 0; i < npg; ++i)
-            load(dst + 8192 + i * P * 64, kLatent, rows[i], &B->full_i8_rope[slot]);
-        }
+        mbar_arrive_expect_tx(&B->full_i8_rope[slot], npg * P * 64);
+#pragma unroll
+        for (int i = 0; i < kTile / 16; ++i)
+          if (i < npg) load(dst + 8192 + i * P * 64, kLatent, rows[i], &B->full_i8_rope[slot]);
         ++rope_it;
       }
     }
+    if (!ok) fail(B, p.status);
+  } else if (!kInt8 && warp == C::kPvProducerWarp && lane == 0) {
+    // ------------------------------------------------------------ PV-ring producer (bf16)
+    // Each tile's latent columns again, pair by pair, for the PV product.
+    TileWalker walk;
+    walk.init(p.tile_start, p.seg_base, p.len, p.batch, int(S), pa, pb);
+    const uint64_t pol_last_use = policy_evict_first();
+    const uint32_t page_bytes = uint32_t(P) * 128;
+    uint32_t pair_it = 0;
+    int k = 0;
+    TileInfo t, tn;
+    TileWalker look = walk;
+    TilePages pages, next_pages;
+    if (look.next(tn)) next_pages.fetch(p, tn);
+    bool ok = true;
+    while (ok && walk.next(t)) {
+      pages = next_pages;
+      if (look.next(tn)) next_pages.fetch(p, tn);
+      const int npg = pages.npg;
+      int rows[kTile / 16];
+#pragma unroll
+      for (int i = 0; i < kTile / 16; ++i) rows[i] = i < npg ? pages.row(p, i) : 0;
+      if (kPvGate && !(ok = wait_progress(&B->qk_progress, k, abort_flag, kWaitLimitNs))) break;
+      ++k;
+      for (int c = 0; c < 4; ++c, ++pair_it) {
+        const uint32_t slot = pair_it % C::kNumPair;
+        if (!(ok = mbar_wait(&B->empty_pair[slot], ((pair_it / C::kNumPair) & 1) ^ 1, abort_flag, kWaitLimitNs)))
+          break;
+        uint8_t* dst = smem + C::kOffPair + slot * kPairBytes;
+        mbar_arrive_expect_tx(&B->full_pair[slot], 2 * npg * page_bytes);
+#pragma unroll
+        for (int i = 0; i < kTile / 16; ++i)
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            if (i >= npg) continue;
+            if (kL2Hints)
+              tma_load_2d_hint(dst + h * kBoxBytes + i * page_bytes, &tmap_cache, 128 * c + 64 * h, rows[i],
+                               &B->full_pair[slot], pol_last_use);
+            else
+              tma_load_2d(dst + h * kBoxBytes + i * page_bytes, &tmap_cache, 128 * c + 64 * h, rows[i],
+                          &B->full_pair[slot]);
+          }
+      }
+    }
+    if (!ok) fail(B, p.status);
   } else if (warp == 1 && lane == 0) {
     // ------------------------------------------------------------ QK issuer
-    // S^T[k & 1] = C_tile * Q^T, pair by pair as the data lands.  Before
+    // S^T[k & 1] = C_tile * Q^T, box by box as the data lands.  Before
     // overwriting S^T[k & 1] it waits for the softmax of tile k - 2 (which
     // read it) to finish.  Descriptors advance by one add per MMA.
     TileWalker walk;
     walk.init(p.tile_start, p.seg_base, p.len, p.batch, int(S), pa, pb);
     constexpr uint32_t id_qk = idesc_f32acc(128, HC, false, false, kInt8);
     constexpr uint64_t kDescK = smem_desc(0, 16, 1024, kSwizzle128B);  // K-major SW128
-    uint32_t k = 0, seg = 0;
+    uint32_t k = 0, seg = 0, box_it[2] = {0, 0};
     TileInfo t;
     bool ok = true;
     while (ok && walk.next(t)) {
       if (k >= 2 && !(ok = mbar_wait(&B->p_full[k & 1], ((k - 2) >> 1) & 1, abort_flag, kWaitLimitNs))) break;
       if (t.first && !(ok = mbar_wait(&B->q_full, seg & 1, abort_flag, kWaitLimitNs))) break;
       const uint32_t d_s = tmem + C::kColS + (k & 1) * HC;
-      for (int c = 0; c < 4 && ok; ++c) {
-        const uint32_t it = 4 * k + c, slot = it % C::kNumPair;
-        if (!(ok = mbar_wait(&B->full_pair[slot], (it / C::kNumPair) & 1, abort_flag, kWaitLimitNs))) break;
+      if constexpr (!kInt8) {
+        for (int j = 0; j < 9; ++j) {
+          const int r = j % C::kQkRings;
+          const uint32_t slot = box_it[r] % C::kQkRing, par = (box_it[r] / C::kQkRing) & 1;
+          ++box_it[r];
+          if (!(ok = mbar_wait(&B->full_qk[r][slot], par, abort_flag, kWaitLimitNs))) break;
+          if (kPvGate && j == 8) publish_progress(&B->qk_progress, int(k) + 1);
+          tc_fence_after();
+          const uint64_t a0 = kDescK | ((sbase + C::kOffQk + (r * C::kQkRing + slot) * kBoxBytes) >> 4);
+          const uint64_t b0 = kDescK | ((sbase + C::kOffQ + j * HC * 128) >> 4);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) mma_bf16(d_s, a0 + 2 * kk, b0 + 2 * kk, id_qk, (j | kk) != 0);
+          mma_commit(&B->empty_qk[r][slot]);
+        }
+        if (!ok) break;
+      } else {
+        for (int c = 0; c < 4; ++c) {
+          const uint32_t it = 4 * k + c, slot = it % C::kNumPair;
+          if (!(ok = mbar_wait(&B->full_pair[slot], (it / C::kNumPair) & 1, abort_flag, kWaitLimitNs))) break;
+          tc_fence_after();
+          const uint64_t a0 = kDescK | ((sbase + C::kOffPair + slot * kPairBytes) >> 4);
+          const uint64_t b0 = kDescK | ((sbase + C::kOffQ + 2 * c * HC * 128) >> 4);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) mma_bf16(d_s, a0 + 2 * kk, b0 + 2 * kk, id_qk, (c | kk) != 0);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_bf16(d_s, a0 + kBoxBytes / 16 + 2 * kk, b0 + HC * 128 / 16 + 2 * kk, id_qk, 1);
+        }
+        if (!ok) break;
+        const uint32_t rslot = k % C::kNumRope;
+        if (!(ok = mbar_wait(&B->full_rope[rslot], (k / C::kNumRope) & 1, abort_flag, kWaitLimitNs))) break;
         tc_fence_after();
-        const uint64_t a0 = kDescK | ((sbase + C::kOffPair + slot * kPairBytes) >> 4);
-        const uint64_t b0 = kDescK | ((sbase + C::kOffQ + 2 * c * HC * 128) >> 4);
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) mma_bf16(d_s, a0 + 2 * kk, b0 + 2 * kk, id_qk, (c | kk) != 0);
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) mma_bf16(d_s, a0 + kBoxBytes / 16 + 2 * kk, b0 + HC * 128 / 16 + 2 * kk, id_qk, 1);
-      }
-      if (!ok) break;
-      const uint32_t rslot = k % kNumRope;
-      if (!(ok = mbar_wait(&B->full_rope[rslot], (k / kNumRope) & 1, abort_flag, kWaitLimitNs))) break;
-      tc_fence_after();
-      {
         const uint64_t a0 = kDescK | ((sbase + C::kOffRope + rslot * kBoxBytes) >> 4);
         const uint64_t b0 = kDescK | ((sbase + C::kOffQ + 8 * HC * 128) >> 4);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) mma_bf16(d_s, a0 + 2 * kk, b0 + 2 * kk, id_qk, 1);
+        mma_commit(&B->empty_rope[rslot]);
       }
       mma_commit(&B->s_full[k & 1]);
-      mma_commit(&B->empty_rope[rslot]);
       if (t.last) {
         mma_commit(&B->q_empty);
         ++seg;
@@ -361,104 +489,132 @@ __global__ void __launch_bounds__(kInt8 ? kThreadsInt8 : kThreadsBf16, 1)
     if (!ok) fail(B, p.status);
     mma_commit(&B->drain[0]);  // every MMA this thread issued completes before teardown
     mbar_wait(&B->drain[0], 0, abort_flag, kWaitLimitNs);
-  } else if (warp == 2 && lane == 0) {
+  } else if (warp == 2) {
     // ------------------------------------------------------------ PV issuer
     // O^T[c] (+)= C_tile^T[128c .. 128c + 128) * P^T once the softmax of the
     // tile is done; each pair slot is released as soon as its MMAs complete.
+    // The whole warp walks the tiles; lane 0 waits and issues.
     TileWalker walk;
     walk.init(p.tile_start, p.seg_base, p.len, p.batch, int(S), pa, pb);
     constexpr uint32_t id_pv = idesc_f32acc(128, HC, true, true, kInt8);
     constexpr uint64_t kDescMN = smem_desc(0, kBoxBytes, 1024, kSwizzle128B);  // MN-major SW128
     constexpr uint64_t kDescP = smem_desc(0, 128, 2048, kSwizzleNone);        // P^T core matrices
-    uint32_t k = 0, seg = 0;
+    uint32_t k = 0, seg = 0, pair_it = 0;
     TileInfo t;
     bool ok = true;
     while (ok && walk.next(t)) {
-      if (!(ok = mbar_wait(&B->p_full[k & 1], (k >> 1) & 1, abort_flag, kWaitLimitNs))) break;
-      if (t.first && seg > 0 && !(ok = mbar_wait(&B->o_free, (seg - 1) & 1, abort_flag, kWaitLimitNs))) break;
-      tc_fence_after();
+      bool w = true;
+      if (lane == 0) {
+        w = mbar_wait(&B->p_full[k & 1], (k >> 1) & 1, abort_flag, kWaitLimitNs);
+        if (w && t.first && seg > 0) w = mbar_wait(&B->o_free, (seg - 1) & 1, abort_flag, kWaitLimitNs);
+      }
+      if (!(ok = __shfl_sync(0xffffffffu, w, 0))) break;
       const int nk = (t.valid + 15) >> 4;
+      const int tail_rows = 16 * nk - t.valid;  // rows the last k-step reads past the sequence's end
       const uint64_t bd = kDescP | ((sbase + C::kOffP + (k & 1) * C::kPBytes) >> 4);
-#pragma unroll
+#pragma unroll 1
       for (int c = 0; c < 4; ++c) {
-        const uint32_t slot = (4 * k + c) % C::kNumPair;
-        const uint64_t ad = kDescMN | ((sbase + C::kOffPair + slot * kPairBytes) >> 4);
-        const uint32_t d_o = tmem + C::kColO + c * HC;
-        if (nk == 8) {
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk) mma_bf16(d_o, ad + 128 * kk, bd + 16 * kk, id_pv, !(t.first && kk == 0));
-        } else {
-          for (int kk = 0; kk < nk; ++kk) mma_bf16(d_o, ad + 128 * kk, bd + 16 * kk, id_pv, !(t.first && kk == 0));
+        const uint32_t slot = kInt8 ? (4 * k + c) % C::kNumPair : pair_it % C::kNumPair;
+        if constexpr (!kInt8) {
+          if (lane == 0) w = mbar_wait(&B->full_pair[slot], (pair_it / C::kNumPair) & 1, abort_flag, kWaitLimitNs);
+          if (!(ok = __shfl_sync(0xffffffffu, w, 0))) break;
+          ++pair_it;
+          if (tail_rows) {
+            // they meet zero weights in P^T but must be finite: clear them
+            // (rows past the loaded pages hold whatever the slot held before)
+            uint8_t* base = smem + C::kOffPair + slot * kPairBytes;
+            for (int i = lane; i < tail_rows * 16; i += 32)
+              *reinterpret_cast<uint4*>(base + ((i >> 3) & 1) * kBoxBytes + (t.valid + (i >> 4)) * 128 +
+                                        (i & 7) * 16) = make_uint4(0, 0, 0, 0);
+            fence_proxy_async_smem();
+            __syncwarp();
+          }
         }
-        mma_commit(&B->empty_pair[slot]);
+        if (lane == 0) {
+          tc_fence_after();
+          const uint64_t ad = kDescMN | ((sbase + C::kOffPair + slot * kPairBytes) >> 4);
+          const uint32_t d_o = tmem + C::kColO + c * HC;
+          if (nk == 8) {
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) mma_bf16(d_o, ad + 128 * kk, bd + 16 * kk, id_pv, !(t.first && kk == 0));
+          } else {
+            for (int kk = 0; kk < nk; ++kk) mma_bf16(d_o, ad + 128 * kk, bd + 16 * kk, id_pv, !(t.first && kk == 0));
+          }
+          mma_commit(&B->empty_pair[slot]);
+        }
       }
-      mma_commit(&B->pv_done[k & 1]);
-      if (t.last) {
-        mma_commit(&B->o_full);
-        ++seg;
+      if (!ok) break;
+      if (lane == 0) {
+        mma_commit(&B->pv_done[k & 1]);
+        if (t.last) mma_commit(&B->o_full);
       }
+      if (t.last) ++seg;
       ++k;
     }
-    if (!ok) fail(B, p.status);
-    mma_commit(&B->drain[1]);
-    mbar_wait(&B->drain[1], 0, abort_flag, kWaitLimitNs);
-  } else if (kInt8 && (warp == 3 || warp == 8)) {
-    // ------------------------------------------------------------ INT8 expansion
-    // Warps 3 and 8 turn each landed [128 x 64 B] code block into a swizzled
-    // fp16 operand box.  Pair slots hold the codes of boxes 2c and 2c+1 in
-    // their back half: block 0 (at +16 KB) expands into [0, 16 KB) without
-    // overlap; block 1 (at +24 KB) overlaps its destination, so all 64
-    // threads read it before any of them writes.  The RoPE slot's block sits
-    // at +8 KB and overlaps too.
-    const int ct = (warp == 3 ? 0 : 32) + lane, ch = ct & 3, r0 = ct >> 2;  // rows r0 + 16j
-    TileWalker walk;
-    walk.init(p.tile_start, p.seg_base, p.len, p.batch, int(S), pa, pb);
-    uint32_t pair_it = 0, rope_it = 0;
-    TileInfo t;
-    bool ok = true;
-    auto read_block = [&](const uint8_t* src, uint4 (&v)[8]) {
-#pragma unroll
-      for (int j = 0; j < 8; ++j) v[j] = *reinterpret_cast<const uint4*>(src + (r0 + 16 * j) * 64 + ch * 16);
-    };
-    auto write_block = [&](const uint4 (&v)[8], uint8_t* dst) {
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int r = r0 + 16 * j;
-        uint4 lo, hi;
-        expand_codes(v[j], lo, hi);
-        uint8_t* row = dst + r * 128;
-        *reinterpret_cast<uint4*>(row + (((2 * ch) ^ (r & 7)) << 4)) = lo;
-        *reinterpret_cast<uint4*>(row + (((2 * ch + 1) ^ (r & 7)) << 4)) = hi;
-      }
-    };
-    while (ok && walk.next(t)) {
-      for (int c = 0; c < 5 && ok; ++c) {
-        const bool rope = c == 4;
-        const uint32_t it = rope ? rope_it : pair_it, nslot = rope ? kNumRope : C::kNumPair;
-        const uint32_t slot = it % nslot;
-        uint64_t* full_i8 = rope ? &B->full_i8_rope[slot] : &B->full_i8_pair[slot];
-        uint8_t* base = smem + (rope ? C::kOffRope + slot * kBoxBytes : C::kOffPair + slot * kPairBytes);
-        const bool landed = mbar_wait(full_i8, (it / nslot) & 1, abort_flag, kWaitLimitNs);
-        uint4 v[8];
-        if (!rope) {
-          read_block(base + kBoxBytes, v);
-          write_block(v, base);
-        }
-        read_block(base + (rope ? 8192 : kBoxBytes + 8192), v);
-        // all codes of the overlapping block read before any write; a timeout
-        // anywhere stops the 64 threads together
-        if (converters_any(!landed)) {
-          ok = false;
-          break;
-        }
-        write_block(v, base + (rope ? 0 : kBoxBytes));
-        fence_proxy_async_smem();
-        converters_sync();
-        if (ct == 0) mbar_arrive(rope ? &B->full_rope[slot] : &B->full_pair[slot]);
-        if (rope) ++rope_it; else ++pair_it;
-      }
+    if (lane == 0) {
+      if (!ok) fail(B, p.status);
+      mma_commit(&B->drain[1]);
+      mbar_wait(&B->drain[1], 0, abort_flag, kWaitLimitNs);
     }
-    if (!ok) fail(B, p.status);
+  } else if (kInt8 && (warp == 3 || warp == 8)) {
+    if constexpr (kInt8) {
+      // ------------------------------------------------------------ INT8 expansion
+      // Warps 3 and 8 turn each landed [128 x 64 B] code block into a swizzled
+      // fp16 operand box.  Pair slots hold the codes of boxes 2c and 2c+1 in
+      // their back half: block 0 (at +16 KB) expands into [0, 16 KB) without
+      // overlap; block 1 (at +24 KB) overlaps its destination, so all 64
+      // threads read it before any of them writes.  The RoPE slot's block sits
+      // at +8 KB and overlaps too.
+      const int ct = (warp == 3 ? 0 : 32) + lane, ch = ct & 3, r0 = ct >> 2;  // rows r0 + 16j
+      TileWalker walk;
+      walk.init(p.tile_start, p.seg_base, p.len, p.batch, int(S), pa, pb);
+      uint32_t pair_it = 0, rope_it = 0;
+      TileInfo t;
+      bool ok = true;
+      auto read_block = [&](const uint8_t* src, uint4 (&v)[8]) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[j] = *reinterpret_cast<const uint4*>(src + (r0 + 16 * j) * 64 + ch * 16);
+      };
+      auto write_block = [&](const uint4 (&v)[8], uint8_t* dst) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int r = r0 + 16 * j;
+          uint4 lo, hi;
+          expand_codes(v[j], lo, hi);
+          uint8_t* row = dst + r * 128;
+          *reinterpret_cast<uint4*>(row + (((2 * ch) ^ (r & 7)) << 4)) = lo;
+          *reinterpret_cast<uint4*>(row + (((2 * ch + 1) ^ (r & 7)) << 4)) = hi;
+        }
+      };
+      while (ok && walk.next(t)) {
+        for (int c = 0; c < 5 && ok; ++c) {
+          const bool rope = c == 4;
+          const uint32_t it = rope ? rope_it : pair_it, nslot = rope ? C::kNumRope : C::kNumPair;
+          const uint32_t slot = it % nslot;
+          uint64_t* full_i8 = rope ? &B->full_i8_rope[slot] : &B->full_i8_pair[slot];
+          uint8_t* base = smem + (rope ? C::kOffRope + slot * kBoxBytes : C::kOffPair + slot * kPairBytes);
+          const bool landed = mbar_wait(full_i8, (it / nslot) & 1, abort_flag, kWaitLimitNs);
+          uint4 v[8];
+          if (!rope) {
+            read_block(base + kBoxBytes, v);
+            write_block(v, base);
+          }
+          read_block(base + (rope ? 8192 : kBoxBytes + 8192), v);
+          // all codes of the overlapping block read before any write; a timeout
+          // anywhere stops the 64 threads together
+          if (converters_any(!landed)) {
+            ok = false;
+            break;
+          }
+          write_block(v, base + (rope ? 0 : kBoxBytes));
+          fence_proxy_async_smem();
+          converters_sync();
+          if (ct == 0) mbar_arrive(rope ? &B->full_rope[slot] : &B->full_pair[slot]);
+          if (rope) ++rope_it; else ++pair_it;
+        }
+      }
+      if (!ok) fail(B, p.status);
+    }
   } else if (warp >= 4 && warp < 8) {
     // ------------------------------------------------------------ softmax / epilogue
     const int q4 = warp - 4, st = threadIdx.x - 128;  // st = token row of S^T = TMEM lane
@@ -466,7 +622,7 @@ __global__ void __launch_bounds__(kInt8 ? kThreadsInt8 : kThreadsBf16, 1)
     TileWalker walk;
     walk.init(p.tile_start, p.seg_base, p.len, p.batch, int(S), pa, pb);
     float m_run[HC], l_run[HC], corr[HC], qsum[HC];
-    uint32_t pair_it = 0, tile_i = 0, seg = 0;
+    uint32_t tile_i = 0, seg = 0;
     TileInfo t;
     while (walk.next(t)) {
       const uint32_t buf = tile_i & 1;
@@ -594,23 +750,9 @@ __global__ void __launch_bounds__(kInt8 ? kThreadsInt8 : kThreadsBf16, 1)
         *reinterpret_cast<uint4*>(pt + (h0 / 8) * 2048 + (st / 8) * 128 + (st % 8) * 16) =
             make_uint4(packed[0], packed[1], packed[2], packed[3]);
       }
-      // bf16 ragged tail: rows [valid, ceil16(valid)) of the latent boxes feed
-      // the last PV k-step with zero weight; make them finite zeros (the INT8
-      // expansion always produces finite values)
-      if (!kInt8 && st >= t.valid && st < ((t.valid + 15) & ~15)) {
-        for (int c = 0; c < 4; ++c) {
-          uint8_t* row = smem + C::kOffPair + ((pair_it + c) % C::kNumPair) * kPairBytes + st * 128;
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            reinterpret_cast<uint4*>(row)[i] = make_uint4(0, 0, 0, 0);
-            reinterpret_cast<uint4*>(row + kBoxBytes)[i] = make_uint4(0, 0, 0, 0);
-          }
-        }
-      }
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(&B->p_full[buf]);
-      pair_it += 4;
       ++tile_i;
       if (t.last) {
         const bool ok2 = mbar_wait(&B->o_full, seg & 1, abort_flag, kWaitLimitNs);
@@ -719,11 +861,11 @@ cudaError_t launch_tc(const DecodeParams& p, int grid, cudaStream_t stream) {
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 128 || !attr[dev]) {
     cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<HC, kInt8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         int(Cfg<HC>::kSmem));
+                                         int(Cfg<HC, kInt8>::kSmem));
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 128) attr[dev] = true;
   }
-  decode_tc_kernel<HC, kInt8><<<grid, kInt8 ? kThreadsInt8 : kThreadsBf16, Cfg<HC>::kSmem, stream>>>(mc, mq, p);
+  decode_tc_kernel<HC, kInt8><<<grid, Cfg<HC, kInt8>::kThreads, Cfg<HC, kInt8>::kSmem, stream>>>(mc, mq, p);
   return cudaGetLastError();
 }
 
