@@ -1,6 +1,7 @@
 // blackwell_ptx.cuh -- thin inline-PTX wrappers for the sm_100-family
-// features the attention kernel uses: mbarriers, TMA tensor loads, L2
-// prefetch, tensor memory (TMEM) and the tcgen05 tensor-core MMA.
+// features the attention kernels use: mbarriers, thread-block clusters and
+// distributed shared memory, TMA tensor loads, L2 prefetch, tensor memory
+// (TMEM) and the tcgen05 tensor-core MMA.
 #pragma once
 
 #include <cstdint>
@@ -62,10 +63,11 @@ __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
 
 // Waits for the phase of `bar` with parity `parity` to complete.  Gives up
 // (returns false) when *abort becomes non-zero or after `limit_ns` of wall
-// time; never spins forever.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const volatile int* abort,
-                                          uint64_t limit_ns) {
-  if (mbar_try_wait(bar, parity)) return true;
+// time; never spins forever.  The spin loop is kept out of line so that the
+// many call sites stay small (the kernels' hot loops must fit the
+// instruction caches).
+static __device__ __noinline__ bool mbar_wait_spin(uint64_t* bar, uint32_t parity, const volatile int* abort,
+                                            uint64_t limit_ns) {
   const uint64_t t0 = global_timer_ns();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -74,6 +76,65 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
       if (global_timer_ns() - t0 > limit_ns) return false;
     }
   }
+}
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const volatile int* abort,
+                                          uint64_t limit_ns) {
+  return mbar_try_wait(bar, parity) || mbar_wait_spin(bar, parity, abort, limit_ns);
+}
+
+// ----- thread-block clusters ------------------------------------------------------
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// All threads of all CTAs of the cluster; orders earlier shared-memory writes
+// (and mbarrier inits) before later accesses by the other CTAs.
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Address, in the cluster's shared window, of the same offset in CTA `rank`'s shared memory.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t local_addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local_addr), "r"(rank));
+  return r;
+}
+// 16-byte store into another CTA's shared memory that completes 16 bytes of
+// transaction count on that CTA's mbarrier (both cluster-window addresses).
+__device__ __forceinline__ void st_async_v4(uint32_t remote_addr, float a, float b, float c, float d,
+                                            uint32_t remote_bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+                   remote_addr),
+               "f"(a), "f"(b), "f"(c), "f"(d), "r"(remote_bar)
+               : "memory");
+}
+// try_wait with cluster-scope acquire: data another CTA delivered with the
+// phase is visible after it returns true.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+static __device__ __noinline__ bool mbar_wait_cluster_spin(uint64_t* bar, uint32_t parity, const volatile int* abort,
+                                                    uint64_t limit_ns) {
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    if ((i & 63) == 0) {
+      if (*abort) return false;
+      if (global_timer_ns() - t0 > limit_ns) return false;
+    }
+  }
+}
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, const volatile int* abort,
+                                                  uint64_t limit_ns) {
+  return mbar_try_wait_cluster(bar, parity) || mbar_wait_cluster_spin(bar, parity, abort, limit_ns);
 }
 
 // ----- fences -----------------------------------------------------------------
@@ -194,6 +255,12 @@ __host__ __device__ constexpr uint32_t idesc_f32acc(int M, int N, bool a_mn_majo
   return (1u << 4) | (uint32_t(!f16) << 7) | (uint32_t(!f16) << 10) | (uint32_t(a_mn_major) << 15) |
          (uint32_t(b_mn_major) << 16) | (uint32_t(N >> 3) << 17) | (uint32_t(M >> 4) << 24);
 }
+
+// Start-address field of a descriptor for shared address `saddr`.  Inside a
+// cluster, a CTA's shared addresses carry its rank above bit 23; the field
+// holds bits 4-17 only, so the rest must not spill into the neighbouring
+// (leading byte offset) field.
+__device__ __forceinline__ uint64_t desc_addr(uint32_t saddr) { return uint64_t((saddr >> 4) & 0x3FFFu); }
 
 // D[tmem] (+)= A[smem] * B[smem]; issued by one thread.
 __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,

@@ -1,0 +1,125 @@
+// decode_common.cuh -- pieces shared by the attention kernels: the softmax
+// warps' reductions, page lookups and TMA tensor-map construction.
+#pragma once
+
+#include <cuda.h>
+
+#include "params.cuh"
+
+namespace mla {
+namespace dc {
+
+__device__ __forceinline__ bool bar_any(bool pred) {  // OR over the 128 softmax threads (named barrier 1)
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, 1, 128, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(uint32_t(pred))
+      : "memory");
+  return r != 0;
+}
+
+// Reduces N (16 or 32) values per lane over the 32 lanes of a warp with
+// log2(32) exchange rounds in which every lane keeps half of its values and
+// trades the other half (N - 1 shuffles instead of 5 N).  Returns, in every
+// lane, the reduction of value index h = lane >> (32 / N - 1)... that is
+// h = lane / 2 for N = 16 (lanes 2h and 2h + 1) and h = lane for N = 32.
+template <int N, bool kMax>
+__device__ __forceinline__ float warp_transpose_reduce(float (&v)[N], int lane) {
+  static_assert(N == 16 || N == 32, "16 or 32 values per lane");
+#pragma unroll
+  for (int w = N / 2, o = 16; w >= 1; w >>= 1, o >>= 1) {
+    const bool upper = lane & o;
+#pragma unroll
+    for (int i = 0; i < w; ++i) {
+      const float keep = upper ? v[i + w] : v[i];
+      const float send = upper ? v[i] : v[i + w];
+      const float got = __shfl_xor_sync(0xffffffffu, send, o);
+      v[i] = kMax ? fmaxf(keep, got) : keep + got;
+    }
+  }
+  if (N == 16) {
+    const float got = __shfl_xor_sync(0xffffffffu, v[0], 1);
+    v[0] = kMax ? fmaxf(v[0], got) : v[0] + got;
+  }
+  return v[0];
+}
+
+// Physical page of token `tok` of sequence b (range-checked; out-of-range
+// entries are reported and replaced by page 0 to stay in bounds).
+__device__ __forceinline__ int page_of(const DecodeParams& p, int b, int tok) {
+  int pg = p.block_table[size_t(b) * p.max_pages + tok / p.page_size];
+  if (pg < 0 || pg >= p.num_pages) {
+    set_status(p.status, MLA_ERR_DEVICE_BOUNDS);
+    pg = 0;
+  }
+  return pg;
+}
+
+// Reports an out-of-range page id (kept out of line: rare, and called from
+// several warp roles' hot loops).
+static __device__ __noinline__ void report_bad_page(int* status) { set_status(status, MLA_ERR_DEVICE_BOUNDS); }
+
+// Physical pages of one tile, loaded a tile before they are needed: a
+// producer that read the block table just in time would stall a full global
+// load latency at every tile.  Checked (and clamped to page 0) at use.
+struct TilePages {
+  int raw[kTile / 16];
+  int npg;
+  __device__ __forceinline__ void fetch(const DecodeParams& p, const TileInfo& a) {
+    npg = (a.valid + p.page_size - 1) / p.page_size;
+    const int* bt = p.block_table + size_t(a.b) * p.max_pages + a.tile * (kTile / p.page_size);
+#pragma unroll
+    for (int i = 0; i < kTile / 16; ++i) raw[i] = i < npg ? __ldg(bt + i) : 0;
+  }
+  // first cache row (page * P) of each page of the tile into rows[0, npg)
+  __device__ __forceinline__ void rows(const DecodeParams& p, int (&r)[kTile / 16]) const {
+    bool bad = false;
+#pragma unroll
+    for (int i = 0; i < kTile / 16; ++i) {
+      const bool out = uint32_t(raw[i]) >= uint32_t(p.num_pages);
+      bad |= out;
+      r[i] = (out ? 0 : raw[i]) * p.page_size;
+    }
+    if (bad) report_bad_page(p.status);
+  }
+};
+
+// ----- host side: tensor maps ----------------------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+inline EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    fn = reinterpret_cast<EncodeTiledFn>(f);
+  }
+  return fn;
+}
+
+// 2-D map over a row-major [rows, inner] tensor of 1- or 2-byte elements.
+inline bool make_map_2d(CUtensorMap* m, const void* base, int elem_bytes, uint64_t inner, uint64_t rows,
+                        uint32_t box_inner, uint32_t box_rows, CUtensorMapSwizzle swizzle) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {inner, rows};
+  cuuint64_t strides[1] = {inner * elem_bytes};
+  cuuint32_t box[2] = {box_inner, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, elem_bytes == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+            const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace dc
+}  // namespace mla

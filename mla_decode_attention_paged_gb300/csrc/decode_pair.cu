@@ -1,0 +1,589 @@
+// decode_pair.cu -- split-KV MLA decode attention for bf16 caches on CTA
+// pairs (thread-block clusters of two), tcgen05 tensor cores fed by TMA.
+//
+// What it computes ("The Weight Absorption Trick"; "Seven Ways LLMs Handle
+// Attention", section 5; "Flash-Decoding and FlashInfer"): for one head group
+// of one sequence and one contiguous range of its tokens, with
+// q_full[h] = [W^UK_h^T q_nope_h | q_pe_h] (576 wide) and the cached rows
+// c_t = [latent | RoPE key] (576 wide),
+//     s[t][h] = scale * q_full[h] . c_t
+//     o_lat[h] = sum_t softmax(s[., h])_t * c_t[0:512]
+// and emits o_lat (normalised within the range) with the range's lse.
+//
+// Why pairs.  Both products read the same cached tile (the latent part is K
+// of QK^T and V of PV), so a tile must stay in shared memory from its QK^T
+// until its PV, across the softmax in between.  A 128-token tile is 147 KB;
+// one SM holds about 1.3 of them, which serialises load -> QK^T -> softmax ->
+// PV.  Here the two CTAs of a cluster (two SMs) split every tile by columns:
+// CTA r holds latent columns [256 r, 256 r + 256) and RoPE columns
+// [512 + 32 r, 512 + 32 r + 32): 72 KB per tile, about 2.6 tiles per SM.
+//   * QK^T: each CTA forms the partial scores over its columns, S_r^T
+//     [128 tok x HC] = C_r [128 x 288] * Q_r^T, and sends them to its peer
+//     through distributed shared memory (8 KB for 16 heads);
+//   * both CTAs add the two partials (in the same order of operands, so
+//     both get the same bits), run the same softmax and hold the same P^T;
+//   * PV: each CTA accumulates its own 256 latent columns of O^T.
+// Every page is read from HBM once for all heads of the group.
+//
+// Orientation as in the single-CTA kernel: the 128 tokens of a tile are the
+// MMA's M extent and the heads its N extent:
+//     S_r^T [128 x HC]    = C_r [128 x 288] * Q_r^T          (A K-major)
+//     O_r^T [256 x HC]   += C_r^T [256 x 128] * P^T          (A MN-major)
+//
+// Warp roles (256 threads per CTA):
+//   warp 0     TMA producer: Q of each segment and each tile's first latent
+//              pair (128 columns)
+//   warp 1     TMEM allocation; lane 0 issues the QK^T MMAs
+//   warp 2     PV: lane 0 issues the MMAs; the warp clears the ragged tail
+//              rows of a sequence's last tile first
+//   warp 3     TMA producer: each tile's second latent pair and RoPE half
+//   warps 4-7  exchange of partial scores, softmax (one thread per token
+//              row), epilogue
+// Every wait is bounded: on timeout the CTA records MLA_ERR_DEVICE_TIMEOUT,
+// drains, frees its tensor memory and returns (its peer then times out on the
+// exchange and does the same).
+#include "blackwell_ptx.cuh"
+#include "decode_common.cuh"
+#include "params.cuh"
+
+namespace mla {
+namespace {
+
+using namespace ptx;
+using namespace dc;
+
+constexpr int kPairThreads = 256;
+constexpr uint32_t kBoxBytes = 16384;           // [128 tokens x 64 columns] bf16, 128-byte swizzle
+constexpr uint32_t kPairBytes = 2 * kBoxBytes;  // 128 latent columns: one O^T chunk
+constexpr uint32_t kRopeBytes = 8192;           // [128 tokens x 32 columns] bf16, 64-byte swizzle
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+constexpr float kRescaleThreshold = 8.f;          // log2 units
+
+template <int HC>
+struct PairCfg {
+  static constexpr int kNumPair = HC == 16 ? 5 : 4;  // latent pair slots (two per tile)
+  static constexpr int kNumRope = 3;                 // RoPE-half slots (one per tile)
+  static constexpr uint32_t kQBytes = 4 * HC * 128 + HC * 64;  // four latent boxes + RoPE half
+  static constexpr uint32_t kPBytes = kTile * HC * 2;          // P^T, bf16
+  static constexpr uint32_t kXBytes = kTile * HC * 4;          // the peer's partial S^T, fp32
+  static constexpr uint32_t kOffPair = 0;
+  static constexpr uint32_t kOffRope = kOffPair + kNumPair * kPairBytes;
+  static constexpr uint32_t kOffQ = kOffRope + kNumRope * kRopeBytes;
+  static constexpr uint32_t kOffQRope = kOffQ + 4 * HC * 128;
+  static constexpr uint32_t kOffP = kOffQ + ((kQBytes + 1023) & ~1023u);
+  static constexpr uint32_t kOffX = kOffP + 2 * kPBytes;
+  static constexpr uint32_t kOffMisc = kOffX + 2 * kXBytes;
+  static constexpr uint32_t kMiscBytes = 2048;
+  static constexpr uint32_t kSmem = kOffMisc + kMiscBytes + 1024;  // +1024: base alignment slack
+  static constexpr uint32_t kTmemCols = HC == 16 ? 64 : 128;       // S^T x2 + O^T x2 = 4 * HC
+  static constexpr uint32_t kColS = 0;                             // + buf * HC
+  static constexpr uint32_t kColO = 2 * HC;                        // + c * HC
+  static_assert(kSmem <= 232448, "dynamic shared memory of one CTA");
+  static_assert(kOffQ % 1024 == 0 && kOffQRope % 512 == 0, "swizzle atoms");
+};
+
+struct PairBarriers {
+  uint64_t full_pair[5], empty_pair[5], full_rope[3], empty_rope[3];
+  uint64_t q_full, q_empty, s_full[2], x_full[2], p_full[2], pv_done[2], o_full, o_free, drain[2];
+  uint32_t tmem_base;
+  int abort;
+};
+
+// 2^x with the hardware approximation (relative error about 2^-22, far
+// below the bf16 rounding the probabilities get next); flushes subnormal
+// results to zero, which only affects weights below 2^-126.
+__device__ __forceinline__ float ex2_ftz(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ void fail(PairBarriers* B, int* status) {
+  B->abort = 1;
+  set_status(status, MLA_ERR_DEVICE_TIMEOUT);
+}
+
+template <int HC>
+__global__ void __launch_bounds__(kPairThreads, 1)
+    decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_latent, const __grid_constant__ CUtensorMap tmap_rope,
+                       const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_qrope,
+                       DecodeParams p) {
+  using C = PairCfg<HC>;
+  extern __shared__ uint8_t smem_raw[];
+  // the same offset in both CTAs: the peer's exchange buffer and barriers are found by mapa
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  PairBarriers* B = reinterpret_cast<PairBarriers*>(smem + C::kOffMisc);
+  float* red = reinterpret_cast<float*>(smem + C::kOffMisc + 512);  // [2][HC][4] maxima, [HC][4] sums
+  const uint32_t sbase = smem_u32(smem);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank(), peer = rank ^ 1;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < C::kNumPair; ++i) {
+      mbar_init(&B->full_pair[i], 1);
+      mbar_init(&B->empty_pair[i], 1);
+    }
+    for (int i = 0; i < C::kNumRope; ++i) {
+      mbar_init(&B->full_rope[i], 1);
+      mbar_init(&B->empty_rope[i], 1);
+    }
+    mbar_init(&B->q_full, 1);
+    mbar_init(&B->q_empty, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&B->s_full[i], 1);
+      mbar_init(&B->x_full[i], 1);  // armed by one local thread; the peer's bytes complete it
+      mbar_init(&B->p_full[i], 128);
+      mbar_init(&B->pv_done[i], 1);
+      mbar_init(&B->drain[i], 1);
+    }
+    mbar_init(&B->o_full, 1);
+    mbar_init(&B->o_free, 128);
+    B->abort = 0;
+    fence_mbar_init();
+    prefetch_tensormap(&tmap_latent);
+    prefetch_tensormap(&tmap_rope);
+    prefetch_tensormap(&tmap_q);
+    prefetch_tensormap(&tmap_qrope);
+  }
+  if (warp == 1) {
+    tmem_alloc(&B->tmem_base, C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  cluster_sync();  // both CTAs' barriers exist before either sends to the other
+  tc_fence_after();
+  const uint32_t tmem = B->tmem_base;
+
+  const int G = p.num_groups, pair = blockIdx.x >> 1, g = pair % G, cp = pair / G, Cp = (gridDim.x >> 1) / G;
+  const long long S = p.status[1];  // effective split count from the plan
+  const long long pa = (cp * S) / Cp, pb = ((cp + 1) * S) / Cp;
+  const volatile int* abort_flag = &B->abort;
+  const int P = p.page_size;
+  const int lat0 = 256 * int(rank), rope0 = kLatent + 32 * int(rank);  // this CTA's columns
+
+  if ((warp == 0 || warp == 3) && lane == 0) {
+    // ------------------------------------------------------------ producers
+    // One thread cannot issue TMA copies fast enough for an SM's share of
+    // HBM (about 0.15-0.2 us per 8 KB box), so two warps share the work:
+    // warp 0 loads Q and the first latent pair of every tile, warp 3 the
+    // second pair and the RoPE half.  Both fill the same pair ring.
+    const int role = warp == 0 ? 0 : 1;
+    TileWalker walk;
+    walk.init(p.tile_start, p.seg_base, p.len, p.batch, int(S), pa, pb);
+    const uint32_t page_bytes = uint32_t(P) * 128, rope_page_bytes = uint32_t(P) * 64;
+    uint32_t pair_it = 0, rope_it = 0, seg = 0;
+    TileInfo t, tn;
+    TileWalker look = walk;
+    TilePages pages, next_pages;
+    if (look.next(tn)) next_pages.fetch(p, tn);
+    bool ok = true;
+    while (ok && walk.next(t)) {
+      pages = next_pages;
+      if (look.next(tn)) next_pages.fetch(p, tn);
+      if (t.first && role == 0) {
+        if (seg > 0 && !(ok = mbar_wait(&B->q_empty, (seg - 1) & 1, abort_flag, kWaitLimitNs))) break;
+        mbar_arrive_expect_tx(&B->q_full, C::kQBytes);
+        const int qrow = t.b * p.heads + g * HC;
+        for (int j = 0; j < 4; ++j)
+          tma_load_2d(smem + C::kOffQ + j * HC * 128, &tmap_q, lat0 + 64 * j, qrow, &B->q_full);
+        tma_load_2d(smem + C::kOffQRope, &tmap_qrope, rope0, qrow, &B->q_full);
+        ++seg;
+      }
+      const int npg = pages.npg;
+      int rows[kTile / 16];
+      pages.rows(p, rows);
+      {
+        const int c = role;
+        const uint32_t it = pair_it + c;
+        pair_it += 2;
+        const uint32_t slot = it % C::kNumPair;
+        if (!(ok = mbar_wait(&B->empty_pair[slot], ((it / C::kNumPair) & 1) ^ 1, abort_flag, kWaitLimitNs))) break;
+        uint8_t* dst = smem + C::kOffPair + slot * kPairBytes;
+        mbar_arrive_expect_tx(&B->full_pair[slot], 2 * npg * page_bytes);
+#pragma unroll 1
+        for (int i = 0; i < npg; ++i) {
+          tma_load_2d(dst + i * page_bytes, &tmap_latent, lat0 + 128 * c, rows[i], &B->full_pair[slot]);
+          tma_load_2d(dst + kBoxBytes + i * page_bytes, &tmap_latent, lat0 + 128 * c + 64, rows[i], &B->full_pair[slot]);
+        }
+      }
+      if (role == 0) continue;
+      const uint32_t slot = rope_it % C::kNumRope;
+      if (!(ok = mbar_wait(&B->empty_rope[slot], ((rope_it / C::kNumRope) & 1) ^ 1, abort_flag, kWaitLimitNs)))
+        break;
+      uint8_t* dst = smem + C::kOffRope + slot * kRopeBytes;
+      mbar_arrive_expect_tx(&B->full_rope[slot], npg * rope_page_bytes);
+#pragma unroll 1
+      for (int i = 0; i < npg; ++i) tma_load_2d(dst + i * rope_page_bytes, &tmap_rope, rope0, rows[i], &B->full_rope[slot]);
+      ++rope_it;
+    }
+    if (!ok) fail(B, p.status);
+  } else if (warp == 1 && lane == 0) {
+    // ------------------------------------------------------------ QK issuer
+    // S_r^T[k & 1] = C_r * Q_r^T: two latent pairs (16 MMAs) and the RoPE half
+    // (2 MMAs).  Before overwriting S^T[k & 1] it waits for the softmax of
+    // tile k - 2 (which read it) to finish.
+    TileWalker walk;
+    walk.init(p.tile_start, p.seg_base, p.len, p.batch, int(S), pa, pb);
+    constexpr uint32_t id_qk = idesc_f32acc(128, HC, false, false, false);
+    constexpr uint64_t kDescK = smem_desc(0, 16, 1024, kSwizzle128B);   // K-major, 128-byte swizzle
+    constexpr uint64_t kDescK64 = smem_desc(0, 16, 512, kSwizzle64B);   // K-major, 64-byte swizzle
+    uint32_t k = 0, seg = 0, pair_it = 0;
+    TileInfo t;
+    bool ok = true;
+    while (ok && walk.next(t)) {
+      if (k >= 2 && !(ok = mbar_wait(&B->p_full[k & 1], ((k - 2) >> 1) & 1, abort_flag, kWaitLimitNs))) break;
+      if (t.first && !(ok = mbar_wait(&B->q_full, seg & 1, abort_flag, kWaitLimitNs))) break;
+      const uint32_t d_s = tmem + C::kColS + (k & 1) * HC;
+      for (int c = 0; c < 2; ++c, ++pair_it) {
+        const uint32_t slot = pair_it % C::kNumPair;
+        if (!(ok = mbar_wait(&B->full_pair[slot], (pair_it / C::kNumPair) & 1, abort_flag, kWaitLimitNs))) break;
+        tc_fence_after();
+        const uint64_t a0 = kDescK | desc_addr(sbase + C::kOffPair + slot * kPairBytes);
+        const uint64_t b0 = kDescK | desc_addr(sbase + C::kOffQ + 2 * c * HC * 128);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) mma_bf16(d_s, a0 + 2 * kk, b0 + 2 * kk, id_qk, (c | kk) != 0);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          mma_bf16(d_s, a0 + kBoxBytes / 16 + 2 * kk, b0 + HC * 128 / 16 + 2 * kk, id_qk, 1);
+      }
+      if (!ok) break;
+      const uint32_t rslot = k % C::kNumRope;
+      if (!(ok = mbar_wait(&B->full_rope[rslot], (k / C::kNumRope) & 1, abort_flag, kWaitLimitNs))) break;
+      tc_fence_after();
+      {
+        const uint64_t a0 = kDescK64 | desc_addr(sbase + C::kOffRope + rslot * kRopeBytes);
+        const uint64_t b0 = kDescK64 | desc_addr(sbase + C::kOffQRope);
+        mma_bf16(d_s, a0, b0, id_qk, 1);
+        mma_bf16(d_s, a0 + 2, b0 + 2, id_qk, 1);
+      }
+      mma_commit(&B->s_full[k & 1]);
+      mma_commit(&B->empty_rope[rslot]);
+      if (t.last) {
+        mma_commit(&B->q_empty);
+        ++seg;
+      }
+      ++k;
+    }
+    if (!ok) fail(B, p.status);
+    mma_commit(&B->drain[0]);  // every MMA this thread issued completes before teardown
+    mbar_wait(&B->drain[0], 0, abort_flag, kWaitLimitNs);
+  } else if (warp == 2) {
+    // ------------------------------------------------------------ PV issuer
+    // O_r^T[c] (+)= C_r^T[128c .. 128c + 128) * P^T once the softmax of the
+    // tile is done; each pair slot is released as soon as its MMAs complete.
+    TileWalker walk;
+    walk.init(p.tile_start, p.seg_base, p.len, p.batch, int(S), pa, pb);
+    constexpr uint32_t id_pv = idesc_f32acc(128, HC, true, true, false);
+    constexpr uint64_t kDescMN = smem_desc(0, kBoxBytes, 1024, kSwizzle128B);  // MN-major, 128-byte swizzle
+    constexpr uint64_t kDescP = smem_desc(0, 128, 2048, kSwizzleNone);        // P^T core matrices
+    uint32_t k = 0, seg = 0, pair_it = 0;
+    TileInfo t;
+    bool ok = true;
+    while (ok && walk.next(t)) {
+      bool w = true;
+      if (lane == 0) {
+        w = mbar_wait(&B->p_full[k & 1], (k >> 1) & 1, abort_flag, kWaitLimitNs);
+        if (w && t.first && seg > 0) w = mbar_wait(&B->o_free, (seg - 1) & 1, abort_flag, kWaitLimitNs);
+      }
+      if (!(ok = __shfl_sync(0xffffffffu, w, 0))) break;
+      const int nk = (t.valid + 15) >> 4;
+      const int tail_rows = 16 * nk - t.valid;  // rows the last k-step reads past the sequence's end
+      const uint64_t bd = kDescP | desc_addr(sbase + C::kOffP + (k & 1) * C::kPBytes);
+      for (int c = 0; c < 2; ++c, ++pair_it) {
+        const uint32_t slot = pair_it % C::kNumPair;
+        if (tail_rows) {
+          // they meet zero weights in P^T but must be finite: clear them (rows
+          // past the loaded pages hold whatever the slot held before)
+          uint8_t* base = smem + C::kOffPair + slot * kPairBytes;
+          for (int i = lane; i < tail_rows * 16; i += 32)
+            *reinterpret_cast<uint4*>(base + ((i >> 3) & 1) * kBoxBytes + (t.valid + (i >> 4)) * 128 + (i & 7) * 16) =
+                make_uint4(0, 0, 0, 0);
+          fence_proxy_async_smem();
+          __syncwarp();
+        }
+        if (lane == 0) {
+          tc_fence_after();
+          const uint64_t ad = kDescMN | desc_addr(sbase + C::kOffPair + slot * kPairBytes);
+          const uint32_t d_o = tmem + C::kColO + c * HC;
+          if (nk == 8) {
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) mma_bf16(d_o, ad + 128 * kk, bd + 16 * kk, id_pv, !(t.first && kk == 0));
+          } else {
+            for (int kk = 0; kk < nk; ++kk) mma_bf16(d_o, ad + 128 * kk, bd + 16 * kk, id_pv, !(t.first && kk == 0));
+          }
+          mma_commit(&B->empty_pair[slot]);
+        }
+      }
+      if (lane == 0) {
+        mma_commit(&B->pv_done[k & 1]);
+        if (t.last) mma_commit(&B->o_full);
+      }
+      if (t.last) ++seg;
+      ++k;
+    }
+    if (lane == 0) {
+      if (!ok) fail(B, p.status);
+      mma_commit(&B->drain[1]);
+      mbar_wait(&B->drain[1], 0, abort_flag, kWaitLimitNs);
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ exchange / softmax / epilogue
+    const int q4 = warp - 4, st = threadIdx.x - 128;  // st = token row of S^T = TMEM lane
+    const uint32_t lane_off = uint32_t(q4 * 32) << 16;
+    // this thread's row of the peer's exchange buffer; 16-byte chunks rotated by row to spread banks
+    constexpr int kChunks = HC / 4;
+    const uint32_t x_local = sbase + C::kOffX + st * HC * 4;
+    const uint32_t x_remote = mapa_shared(x_local, peer);
+    TileWalker walk;
+    walk.init(p.tile_start, p.seg_base, p.len, p.batch, int(S), pa, pb);
+    float m_run[HC], l_run[HC];
+    uint32_t tile_i = 0, seg = 0;
+    TileInfo t;
+    while (walk.next(t)) {
+      const uint32_t buf = tile_i & 1;
+      const bool valid = st < t.valid;
+      // S_r^T of this tile; and PV of tile k - 2, which read the P^T buffer
+      // this tile writes, must be complete
+      bool ok = mbar_wait(&B->s_full[buf], (tile_i >> 1) & 1, abort_flag, kWaitLimitNs);
+      tc_fence_after();
+      float x[HC];
+      if (ok) {
+#pragma unroll
+        for (int h0 = 0; h0 < HC; h0 += 16) {
+          float v[16];
+          tmem_ld16(tmem + lane_off + C::kColS + buf * HC + h0, v);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) x[h0 + i] = v[i];
+        }
+        // partial scores to the peer; the peer's partial scores from it
+        const uint32_t rbar = mapa_shared(smem_u32(&B->x_full[buf]), peer);
+#pragma unroll
+        for (int v = 0; v < kChunks; ++v) {
+          const uint32_t off = buf * C::kXBytes + ((v ^ (st % kChunks)) * 16);
+          st_async_v4(x_remote + off, x[4 * v], x[4 * v + 1], x[4 * v + 2], x[4 * v + 3], rbar);
+        }
+        if (st == 0) mbar_arrive_expect_tx(&B->x_full[buf], C::kXBytes);
+        ok = mbar_wait_cluster(&B->x_full[buf], (tile_i >> 1) & 1, abort_flag, kWaitLimitNs);
+        if (ok) {
+          const float* xr = reinterpret_cast<const float*>(smem + C::kOffX + buf * C::kXBytes + st * HC * 4);
+#pragma unroll
+          for (int v = 0; v < kChunks; ++v) {
+            const float4 y = *reinterpret_cast<const float4*>(xr + 4 * (v ^ (st % kChunks)));
+            // rank 0 adds (own + peer) = (S_0 + S_1), rank 1 adds (S_0 + S_1) too
+            if (rank == 0) {
+              x[4 * v] += y.x; x[4 * v + 1] += y.y; x[4 * v + 2] += y.z; x[4 * v + 3] += y.w;
+            } else {
+              x[4 * v] = y.x + x[4 * v]; x[4 * v + 1] = y.y + x[4 * v + 1];
+              x[4 * v + 2] = y.z + x[4 * v + 2]; x[4 * v + 3] = y.w + x[4 * v + 3];
+            }
+          }
+        }
+      }
+#pragma unroll
+      for (int h = 0; h < HC; ++h) x[h] = valid ? x[h] * p.scale_log2 : -INFINITY;
+      // Running max: it only has to bound the scores to within
+      // kRescaleThreshold (log2 units).  The first tile of a segment, and a
+      // tile that breaks the bound, take the exact path (per-head tile max and,
+      // where it moved, a rescale of O^T and l); otherwise one vote suffices.
+      bool over = false;
+      if (!t.first) {
+#pragma unroll
+        for (int h = 0; h < HC; ++h) over |= x[h] > m_run[h] + kRescaleThreshold;
+      }
+      float alpha[HC];
+      bool rescale = false;
+      if (t.first || bar_any(over || !ok)) {
+        float* rm = red + buf * 4 * HC;
+        {
+          float tmp[HC];
+#pragma unroll
+          for (int h = 0; h < HC; ++h) tmp[h] = x[h];
+          const float wm = warp_transpose_reduce<HC, true>(tmp, lane);
+          if (HC == 32 || !(lane & 1)) rm[(HC == 32 ? lane : lane >> 1) * 4 + q4] = wm;
+        }
+        if (bar_any(!ok)) break;
+#pragma unroll
+        for (int h = 0; h < HC; ++h) {
+          const float4 m4 = reinterpret_cast<const float4*>(rm)[h];
+          const float mt = fmaxf(fmaxf(m4.x, m4.y), fmaxf(m4.z, m4.w));
+          if (t.first) {
+            m_run[h] = mt;
+            l_run[h] = 0.f;
+            alpha[h] = 1.f;
+          } else if (mt > m_run[h] + kRescaleThreshold) {
+            alpha[h] = exp2f(m_run[h] - mt);
+            m_run[h] = mt;
+            l_run[h] *= alpha[h];
+            rescale = true;
+          } else {
+            alpha[h] = 1.f;
+          }
+        }
+      }
+      if (rescale) {
+        // uniform across the 128 threads.  QK of this tile may have been
+        // issued before PV of the previous one: wait for that PV first.
+        const bool ok3 = mbar_wait(&B->pv_done[(tile_i - 1) & 1], ((tile_i - 1) >> 1) & 1, abort_flag, kWaitLimitNs);
+        tc_fence_after();
+        if (bar_any(!ok3)) break;
+#pragma unroll
+        for (int c = 0; c < 2; ++c)
+#pragma unroll
+          for (int h0 = 0; h0 < HC; h0 += 16) {
+            float v[16];
+            const uint32_t a = tmem + lane_off + C::kColO + c * HC + h0;
+            tmem_ld16(a, v);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) v[i] *= alpha[h0 + i];
+            tmem_st16(a, v);
+          }
+        tmem_st_wait();
+      }
+      // PV of tile k - 2, which read the P^T buffer this tile writes, must be complete
+      if (tile_i >= 2 && bar_any(!mbar_wait(&B->pv_done[buf], ((tile_i - 2) >> 1) & 1, abort_flag, kWaitLimitNs)))
+        break;
+      // probabilities -> P^T (bf16, MN-major, no swizzle: 8x8 core matrices)
+      uint8_t* pt = smem + C::kOffP + buf * C::kPBytes;
+#pragma unroll
+      for (int h0 = 0; h0 < HC; h0 += 8) {
+        uint32_t packed[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int ha = h0 + 2 * i, hb = ha + 1;
+          const __nv_bfloat16 wa = __float2bfloat16_rn(ex2_ftz(x[ha] - m_run[ha]));
+          const __nv_bfloat16 wb = __float2bfloat16_rn(ex2_ftz(x[hb] - m_run[hb]));
+          l_run[ha] += __bfloat162float(wa);
+          l_run[hb] += __bfloat162float(wb);
+          packed[i] = uint32_t(__bfloat16_as_ushort(wa)) | (uint32_t(__bfloat16_as_ushort(wb)) << 16);
+        }
+        *reinterpret_cast<uint4*>(pt + (h0 / 8) * 2048 + (st / 8) * 128 + (st % 8) * 16) =
+            make_uint4(packed[0], packed[1], packed[2], packed[3]);
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(&B->p_full[buf]);
+      ++tile_i;
+      if (t.last) {
+        const bool ok2 = mbar_wait(&B->o_full, seg & 1, abort_flag, kWaitLimitNs);
+        tc_fence_after();
+        float* rl = red + 8 * HC;  // [HC][4] sums of l
+        {
+          float tmp[HC];
+#pragma unroll
+          for (int h = 0; h < HC; ++h) tmp[h] = l_run[h];
+          const float ls = warp_transpose_reduce<HC, false>(tmp, lane);
+          if (HC == 32 || !(lane & 1)) rl[(HC == 32 ? lane : lane >> 1) * 4 + q4] = ls;
+        }
+        if (bar_any(!ok2)) break;
+        float inv_l[HC];
+#pragma unroll
+        for (int h = 0; h < HC; ++h) {
+          const float4 l4 = reinterpret_cast<const float4*>(rl)[h];
+          inv_l[h] = __frcp_rn((l4.x + l4.y) + (l4.z + l4.w));
+        }
+        float* dst = p.partial_o + (size_t(t.seg) * p.heads + g * HC) * kLatent + lat0;
+#pragma unroll
+        for (int c = 0; c < 2; ++c)
+#pragma unroll
+          for (int h0 = 0; h0 < HC; h0 += 16) {
+            float v[16];
+            tmem_ld16(tmem + lane_off + C::kColO + c * HC + h0, v);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) dst[(h0 + i) * kLatent + c * 128 + st] = v[i] * inv_l[h0 + i];
+          }
+        tc_fence_before();
+        mbar_arrive(&B->o_free);
+        if (rank == 0 && st < HC) {  // thread h writes head h's lse
+          float mh = 0.f, ih = 1.f;
+#pragma unroll
+          for (int h = 0; h < HC; ++h)
+            if (st == h) {
+              mh = m_run[h];
+              ih = inv_l[h];
+            }
+          p.partial_lse[size_t(t.seg) * p.heads + g * HC + st] = (mh - log2f(ih)) * kLn2;
+        }
+        ++seg;
+      }
+    }
+  }
+  // ---------------------------------------------------------------- teardown
+  __syncthreads();
+  if (B->abort) {  // let copies already issued land before the CTA's shared memory is released
+    const uint64_t t0 = global_timer_ns();
+    while (global_timer_ns() - t0 < 20000) {
+    }
+  }
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, C::kTmemCols);
+  cluster_sync();  // the peer may still be sending into this CTA's shared memory until here
+}
+
+template <int HC>
+cudaError_t launch_pair(const DecodeParams& p, int pairs_per_group, cudaStream_t stream) {
+  CUtensorMap ml, mr, mq, mqr;
+  const uint64_t rows = uint64_t(p.num_pages) * p.page_size, qrows = uint64_t(p.batch) * p.heads;
+  if (!make_map_2d(&ml, p.cache, 2, kRow, rows, 64, p.page_size, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_map_2d(&mr, p.cache, 2, kRow, rows, 32, p.page_size, CU_TENSOR_MAP_SWIZZLE_64B) ||
+      !make_map_2d(&mq, p.q_full, 2, kRow, qrows, 64, HC, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_map_2d(&mqr, p.q_full, 2, kRow, qrows, 32, HC, CU_TENSOR_MAP_SWIZZLE_64B))
+    return cudaErrorInvalidValue;
+  static bool attr[128] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 128 || !attr[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(decode_pair_kernel<HC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         int(PairCfg<HC>::kSmem));
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 128) attr[dev] = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * pairs_per_group * p.num_groups);
+  cfg.blockDim = dim3(kPairThreads);
+  cfg.dynamicSmemBytes = PairCfg<HC>::kSmem;
+  cfg.stream = stream;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = 2;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_pair_kernel<HC>, ml, mr, mq, mqr, p);
+}
+
+template <int HC>
+int max_pairs() {  // clusters of two that can be resident at once on this device
+  static int cached[128] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 128 && cached[dev] > 0) return cached[dev];
+  if (cudaFuncSetAttribute(decode_pair_kernel<HC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           int(PairCfg<HC>::kSmem)) != cudaSuccess)
+    return 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2);
+  cfg.blockDim = dim3(kPairThreads);
+  cfg.dynamicSmemBytes = PairCfg<HC>::kSmem;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = 2;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, decode_pair_kernel<HC>, &cfg) != cudaSuccess || n <= 0) return 0;
+  if (dev >= 0 && dev < 128) cached[dev] = n;
+  return n;
+}
+
+}  // namespace
+
+int decode_pair_capacity(int hc) { return hc == 16 ? max_pairs<16>() : max_pairs<32>(); }
+
+cudaError_t launch_decode_pair(const DecodeParams& p, int hc, int pairs_per_group, cudaStream_t stream) {
+  return hc == 16 ? launch_pair<16>(p, pairs_per_group, stream) : launch_pair<32>(p, pairs_per_group, stream);
+}
+
+}  // namespace mla

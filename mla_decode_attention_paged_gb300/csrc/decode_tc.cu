@@ -58,12 +58,14 @@
 #include <cuda_fp16.h>
 
 #include "blackwell_ptx.cuh"
+#include "decode_common.cuh"
 #include "params.cuh"
 
 namespace mla {
 namespace {
 
 using namespace ptx;
+using namespace dc;
 
 // Nine warps leave three on one SM sub-partition (16K registers each), which
 // caps a thread at 168 registers: enough except for the 32-head bf16 softmax,
@@ -135,19 +137,6 @@ __device__ __forceinline__ bool wait_progress(const int* counter, int k, const v
   }
 }
 
-__device__ __forceinline__ bool bar_any(bool pred) {  // OR over the 128 softmax threads (named barrier 1)
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\t"
-      "setp.ne.u32 p, %1, 0;\n\t"
-      "bar.red.or.pred q, 1, 128, p;\n\t"
-      "selp.u32 %0, 1, 0, q;\n\t}"
-      : "=r"(r)
-      : "r"(uint32_t(pred))
-      : "memory");
-  return r != 0;
-}
-
 __device__ __forceinline__ bool converters_any(bool pred) {  // OR over the 64 INT8 expansion threads (barrier 2)
   uint32_t r;
   asm volatile(
@@ -161,32 +150,6 @@ __device__ __forceinline__ bool converters_any(bool pred) {  // OR over the 64 I
   return r != 0;
 }
 __device__ __forceinline__ void converters_sync() { asm volatile("bar.sync 2, 64;" ::: "memory"); }
-
-// Reduces N (16 or 32) values per lane over the 32 lanes of a warp with
-// log2(32) exchange rounds in which every lane keeps half of its values and
-// trades the other half (N - 1 shuffles instead of 5 N).  Returns, in every
-// lane, the reduction of value index h = lane >> (32 / N - 1)... that is
-// h = lane / 2 for N = 16 (lanes 2h and 2h + 1) and h = lane for N = 32.
-template <int N, bool kMax>
-__device__ __forceinline__ float warp_transpose_reduce(float (&v)[N], int lane) {
-  static_assert(N == 16 || N == 32, "16 or 32 values per lane");
-#pragma unroll
-  for (int w = N / 2, o = 16; w >= 1; w >>= 1, o >>= 1) {
-    const bool upper = lane & o;
-#pragma unroll
-    for (int i = 0; i < w; ++i) {
-      const float keep = upper ? v[i + w] : v[i];
-      const float send = upper ? v[i] : v[i + w];
-      const float got = __shfl_xor_sync(0xffffffffu, send, o);
-      v[i] = kMax ? fmaxf(keep, got) : keep + got;
-    }
-  }
-  if (N == 16) {
-    const float got = __shfl_xor_sync(0xffffffffu, v[0], 1);
-    v[0] = kMax ? fmaxf(v[0], got) : v[0] + got;
-  }
-  return v[0];
-}
 
 __device__ __forceinline__ void fail(Barriers* B, int* status) {
   B->abort = 1;
@@ -209,40 +172,6 @@ __device__ __forceinline__ void expand_codes(uint4 v, uint4& lo, uint4& hi) {
   lo = make_uint4(o[0], o[1], o[2], o[3]);
   hi = make_uint4(o[4], o[5], o[6], o[7]);
 }
-
-// Physical page of token `tok` of sequence b (range-checked; out-of-range
-// entries are reported and replaced by page 0 to stay in bounds).
-__device__ __forceinline__ int page_of(const DecodeParams& p, int b, int tok) {
-  int pg = p.block_table[size_t(b) * p.max_pages + tok / p.page_size];
-  if (pg < 0 || pg >= p.num_pages) {
-    set_status(p.status, MLA_ERR_DEVICE_BOUNDS);
-    pg = 0;
-  }
-  return pg;
-}
-
-// Physical pages of one tile, loaded a tile before they are needed: a
-// producer that read the block table just in time would stall a full global
-// load latency at every tile.  Checked (and clamped to page 0) at use.
-struct TilePages {
-  int raw[kTile / 16];
-  int npg;
-  __device__ __forceinline__ void fetch(const DecodeParams& p, const TileInfo& a) {
-    npg = (a.valid + p.page_size - 1) / p.page_size;
-    const int* bt = p.block_table + size_t(a.b) * p.max_pages + a.tile * (kTile / p.page_size);
-#pragma unroll
-    for (int i = 0; i < kTile / 16; ++i) raw[i] = i < npg ? __ldg(bt + i) : 0;
-  }
-  // first cache row (page * P) of page i of the tile
-  __device__ __forceinline__ int row(const DecodeParams& p, int i) const {
-    int pg = raw[i];
-    if (pg < 0 || pg >= p.num_pages) {
-      set_status(p.status, MLA_ERR_DEVICE_BOUNDS);
-      pg = 0;
-    }
-    return pg * p.page_size;
-  }
-};
 
 template <int HC, bool kInt8>
 __global__ void __launch_bounds__(Cfg<HC, kInt8>::kThreads, 1)
@@ -339,8 +268,7 @@ __global__ void __launch_bounds__(Cfg<HC, kInt8>::kThreads, 1)
       }
       const int npg = pages.npg;
       int rows[kTile / 16];
-#pragma unroll
-      for (int i = 0; i < kTile / 16; ++i) rows[i] = i < npg ? pages.row(p, i) : 0;
+      pages.rows(p, rows);
       if constexpr (!kInt8) {
         // the tile's boxes j = qr, qr + 2, ...: latent columns [64j, 64j + 64), box 8 the RoPE key
         for (int j = qr; j < 9; j += C::kQkRings, ++box_it) {
@@ -349,9 +277,8 @@ __global__ void __launch_bounds__(Cfg<HC, kInt8>::kThreads, 1)
             break;
           uint8_t* dst = smem + C::kOffQk + (qr * C::kQkRing + slot) * kBoxBytes;
           mbar_arrive_expect_tx(&B->full_qk[qr][slot], npg * page_bytes);
-#pragma unroll
-          for (int i = 0; i < kTile / 16; ++i)
-            if (i < npg) load(dst + i * page_bytes, 64 * j, rows[i], &B->full_qk[qr][slot]);
+#pragma unroll 1
+          for (int i = 0; i < npg; ++i) load(dst + i * page_bytes, 64 * j, rows[i], &B->full_qk[qr][slot]);
         }
       } else {
         for (int c = 0; c < 4; ++c, ++pair_it) {
@@ -361,12 +288,11 @@ __global__ void __launch_bounds__(Cfg<HC, kInt8>::kThreads, 1)
           // int8 codes of columns [128c, 128c + 128) into the slot's back half, as two [128 x 64 B] blocks
           uint8_t* dst = smem + C::kOffPair + slot * kPairBytes;
           mbar_arrive_expect_tx(&B->full_i8_pair[slot], npg * page_bytes);
-#pragma unroll
-          for (int i = 0; i < kTile / 16; ++i)
-            if (i < npg) {
-              load(dst + kBoxBytes + i * P * 64, 128 * c, rows[i], &B->full_i8_pair[slot]);
-              load(dst + kBoxBytes + 8192 + i * P * 64, 128 * c + 64, rows[i], &B->full_i8_pair[slot]);
-            }
+#pragma unroll 1
+          for (int i = 0; i < npg; ++i) {
+            load(dst + kBoxBytes + i * P * 64, 128 * c, rows[i], &B->full_i8_pair[slot]);
+            load(dst + kBoxBytes + 8192 + i * P * 64, 128 * c + 64, rows[i], &B->full_i8_pair[slot]);
+          }
         }
         if (!ok) break;
         const uint32_t slot = rope_it % C::kNumRope;
@@ -374,9 +300,8 @@ __global__ void __launch_bounds__(Cfg<HC, kInt8>::kThreads, 1)
           break;
         uint8_t* dst = smem + C::kOffRope + slot * kBoxBytes;
         mbar_arrive_expect_tx(&B->full_i8_rope[slot], npg * P * 64);
-#pragma unroll
-        for (int i = 0; i < kTile / 16; ++i)
-          if (i < npg) load(dst + 8192 + i * P * 64, kLatent, rows[i], &B->full_i8_rope[slot]);
+#pragma unroll 1
+        for (int i = 0; i < npg; ++i) load(dst + 8192 + i * P * 64, kLatent, rows[i], &B->full_i8_rope[slot]);
         ++rope_it;
       }
     }
@@ -400,8 +325,7 @@ __global__ void __launch_bounds__(Cfg<HC, kInt8>::kThreads, 1)
       if (look.next(tn)) next_pages.fetch(p, tn);
       const int npg = pages.npg;
       int rows[kTile / 16];
-#pragma unroll
-      for (int i = 0; i < kTile / 16; ++i) rows[i] = i < npg ? pages.row(p, i) : 0;
+      pages.rows(p, rows);
       if (kPvGate && !(ok = wait_progress(&B->qk_progress, k, abort_flag, kWaitLimitNs))) break;
       ++k;
       for (int c = 0; c < 4; ++c, ++pair_it) {
@@ -410,11 +334,10 @@ __global__ void __launch_bounds__(Cfg<HC, kInt8>::kThreads, 1)
           break;
         uint8_t* dst = smem + C::kOffPair + slot * kPairBytes;
         mbar_arrive_expect_tx(&B->full_pair[slot], 2 * npg * page_bytes);
-#pragma unroll
-        for (int i = 0; i < kTile / 16; ++i)
+#pragma unroll 1
+        for (int i = 0; i < npg; ++i)
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
-            if (i >= npg) continue;
             if (kL2Hints)
               tma_load_2d_hint(dst + h * kBoxBytes + i * page_bytes, &tmap_cache, 128 * c + 64 * h, rows[i],
                                &B->full_pair[slot], pol_last_use);
@@ -449,8 +372,8 @@ __global__ void __launch_bounds__(Cfg<HC, kInt8>::kThreads, 1)
           if (!(ok = mbar_wait(&B->full_qk[r][slot], par, abort_flag, kWaitLimitNs))) break;
           if (kPvGate && j == 8) publish_progress(&B->qk_progress, int(k) + 1);
           tc_fence_after();
-          const uint64_t a0 = kDescK | ((sbase + C::kOffQk + (r * C::kQkRing + slot) * kBoxBytes) >> 4);
-          const uint64_t b0 = kDescK | ((sbase + C::kOffQ + j * HC * 128) >> 4);
+          const uint64_t a0 = kDescK | desc_addr(sbase + C::kOffQk + (r * C::kQkRing + slot) * kBoxBytes);
+          const uint64_t b0 = kDescK | desc_addr(sbase + C::kOffQ + j * HC * 128);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) mma_bf16(d_s, a0 + 2 * kk, b0 + 2 * kk, id_qk, (j | kk) != 0);
           mma_commit(&B->empty_qk[r][slot]);
@@ -461,8 +384,8 @@ __global__ void __launch_bounds__(Cfg<HC, kInt8>::kThreads, 1)
           const uint32_t it = 4 * k + c, slot = it % C::kNumPair;
           if (!(ok = mbar_wait(&B->full_pair[slot], (it / C::kNumPair) & 1, abort_flag, kWaitLimitNs))) break;
           tc_fence_after();
-          const uint64_t a0 = kDescK | ((sbase + C::kOffPair + slot * kPairBytes) >> 4);
-          const uint64_t b0 = kDescK | ((sbase + C::kOffQ + 2 * c * HC * 128) >> 4);
+          const uint64_t a0 = kDescK | desc_addr(sbase + C::kOffPair + slot * kPairBytes);
+          const uint64_t b0 = kDescK | desc_addr(sbase + C::kOffQ + 2 * c * HC * 128);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) mma_bf16(d_s, a0 + 2 * kk, b0 + 2 * kk, id_qk, (c | kk) != 0);
 #pragma unroll
@@ -473,8 +396,8 @@ __global__ void __launch_bounds__(Cfg<HC, kInt8>::kThreads, 1)
         const uint32_t rslot = k % C::kNumRope;
         if (!(ok = mbar_wait(&B->full_rope[rslot], (k / C::kNumRope) & 1, abort_flag, kWaitLimitNs))) break;
         tc_fence_after();
-        const uint64_t a0 = kDescK | ((sbase + C::kOffRope + rslot * kBoxBytes) >> 4);
-        const uint64_t b0 = kDescK | ((sbase + C::kOffQ + 8 * HC * 128) >> 4);
+        const uint64_t a0 = kDescK | desc_addr(sbase + C::kOffRope + rslot * kBoxBytes);
+        const uint64_t b0 = kDescK | desc_addr(sbase + C::kOffQ + 8 * HC * 128);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) mma_bf16(d_s, a0 + 2 * kk, b0 + 2 * kk, id_qk, 1);
         mma_commit(&B->empty_rope[rslot]);
@@ -511,7 +434,7 @@ __global__ void __launch_bounds__(Cfg<HC, kInt8>::kThreads, 1)
       if (!(ok = __shfl_sync(0xffffffffu, w, 0))) break;
       const int nk = (t.valid + 15) >> 4;
       const int tail_rows = 16 * nk - t.valid;  // rows the last k-step reads past the sequence's end
-      const uint64_t bd = kDescP | ((sbase + C::kOffP + (k & 1) * C::kPBytes) >> 4);
+      const uint64_t bd = kDescP | desc_addr(sbase + C::kOffP + (k & 1) * C::kPBytes);
 #pragma unroll 1
       for (int c = 0; c < 4; ++c) {
         const uint32_t slot = kInt8 ? (4 * k + c) % C::kNumPair : pair_it % C::kNumPair;
@@ -532,7 +455,7 @@ __global__ void __launch_bounds__(Cfg<HC, kInt8>::kThreads, 1)
         }
         if (lane == 0) {
           tc_fence_after();
-          const uint64_t ad = kDescMN | ((sbase + C::kOffPair + slot * kPairBytes) >> 4);
+          const uint64_t ad = kDescMN | desc_addr(sbase + C::kOffPair + slot * kPairBytes);
           const uint32_t d_o = tmem + C::kColO + c * HC;
           if (nk == 8) {
 #pragma unroll
@@ -817,45 +740,16 @@ __global__ void __launch_bounds__(Cfg<HC, kInt8>::kThreads, 1)
 }
 
 // ----- host side: tensor maps and launch ---------------------------------------
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  if (!fn) {
-    void* f = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
-        q != cudaDriverEntryPointSuccess)
-      return nullptr;
-    fn = reinterpret_cast<EncodeTiledFn>(f);
-  }
-  return fn;
-}
-
-// 2-D map over a row-major [rows, inner] tensor of 1- or 2-byte elements.
-bool make_map_2d(CUtensorMap* m, const void* base, int elem_bytes, uint64_t inner, uint64_t rows, uint32_t box_inner,
-                 uint32_t box_rows, bool swizzle128) {
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[2] = {inner, rows};
-  cuuint64_t strides[1] = {inner * elem_bytes};
-  cuuint32_t box[2] = {box_inner, box_rows};
-  cuuint32_t estr[2] = {1, 1};
-  return fn(m, elem_bytes == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
-            const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-            swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 template <int HC, bool kInt8>
 cudaError_t launch_tc(const DecodeParams& p, int grid, cudaStream_t stream) {
   CUtensorMap mc, mq;
   const uint64_t rows = uint64_t(p.num_pages) * p.page_size;
-  if (!make_map_2d(&mc, p.cache, kInt8 ? 1 : 2, kRow, rows, 64, p.page_size, !kInt8)) return cudaErrorInvalidValue;
+  if (!make_map_2d(&mc, p.cache, kInt8 ? 1 : 2, kRow, rows, 64, p.page_size,
+                   kInt8 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
   // q_full holds bf16 (or, for INT8 caches, fp16) values; TMA moves 2-byte elements either way
-  if (!make_map_2d(&mq, p.q_full, 2, kRow, uint64_t(p.batch) * p.heads, 64, HC, true)) return cudaErrorInvalidValue;
+  if (!make_map_2d(&mq, p.q_full, 2, kRow, uint64_t(p.batch) * p.heads, 64, HC, CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
   static bool attr[128] = {};
   int dev = 0;
   cudaGetDevice(&dev);

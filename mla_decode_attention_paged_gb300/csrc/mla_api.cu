@@ -183,12 +183,17 @@ int mla_decode(const mla_dims* d, const void* q_nope, const void* q_pe, const vo
   dp.num_pages = num_pages;
   dp.num_splits = S;
   dp.scale_log2 = softmax_scale * kLog2e;
-  const int nsm = sm_count();
-  const int per_group = nsm / groups > 0 ? nsm / groups : 1;
-  const int ctas_per_group = S < per_group ? S : per_group;
+  // bf16 caches run on CTA pairs (two SMs share each tile); INT8 caches, and
+  // devices that cannot place the pairs, on single CTAs
+  const int pair_cap = int8 ? 0 : decode_pair_capacity(hc);
+  const int units = pair_cap > 0 ? pair_cap : sm_count();
+  const int per_group = units / groups > 0 ? units / groups : 1;
+  const int per_group_used = S < per_group ? S : per_group;
   cudaEvent_t ev0 = g_ev_start.load(), ev1 = g_ev_stop.load();
   if (ev0 && ev1 && cudaEventRecord(ev0, s) != cudaSuccess) return MLA_ERR_CUDA;
-  if (launch_decode_tc(dp, hc, int8, ctas_per_group * groups, s) != cudaSuccess) return MLA_ERR_CUDA;
+  const cudaError_t le = pair_cap > 0 ? launch_decode_pair(dp, hc, per_group_used, s)
+                                      : launch_decode_tc(dp, hc, int8, per_group_used * groups, s);
+  if (le != cudaSuccess) return MLA_ERR_CUDA;
   if (ev0 && ev1 && cudaEventRecord(ev1, s) != cudaSuccess) return MLA_ERR_CUDA;
 
   CombineUVParams cp;

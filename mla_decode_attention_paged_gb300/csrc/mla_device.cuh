@@ -82,11 +82,15 @@ struct TileWalker {
   const int* tile_start;
   const int* seg_base;
   const int* len;
-  long long W, S, u, u_end, p;
-  int b;
+  long long W, S, u, u_end;
+  long long p, p_start, p_next;  // current partition and its units [p_start, p_next)
+  long long s_b, e_b;            // units of sequence b: [s_b, e_b)
+  int b, len_b, seg_b;           // seg_b = first segment of sequence b minus its first partition
 
-  __device__ void init(const int* ts, const int* sb, const int* ln, int batch, int num_splits, long long pa,
-                       long long pb) {
+  // init and the boundary crossings are rare and hold the 64-bit divisions:
+  // kept out of line so that each warp role's copy of the walker stays small
+  __device__ __noinline__ void init(const int* ts, const int* sb, const int* ln, int batch, int num_splits,
+                                    long long pa, long long pb) {
     tile_start = ts;
     seg_base = sb;
     len = ln;
@@ -95,6 +99,8 @@ struct TileWalker {
     u = part_start(pa, W, S);
     u_end = part_start(pb, W, S);
     p = pa;
+    p_start = u;
+    p_next = part_start(pa + 1, W, S);
     // first sequence whose tiles reach past u (binary search over tile_start)
     int lo = 0, hi = batch;  // answer in [0, batch)
     while (lo < hi) {
@@ -102,20 +108,40 @@ struct TileWalker {
       if (ts[mid + 1] <= u) lo = mid + 1; else hi = mid;
     }
     b = lo;
+    enter_sequence();
   }
 
+  __device__ __noinline__ void enter_sequence() {
+    s_b = tile_start[b];
+    e_b = tile_start[b + 1];
+    len_b = len[b];
+    seg_b = seg_base[b] - int(part_of(s_b, W, S));
+  }
+
+  __device__ __noinline__ void enter_partition() {
+    while (p_next <= u) {
+      ++p;
+      p_start = p_next;
+      p_next = part_start(p + 1, W, S);
+    }
+  }
+
+  // Divisions only when a partition boundary is crossed; the plan's
+  // arrays are read only when a sequence boundary is.
   __device__ bool next(TileInfo& t) {
     if (u >= u_end) return false;
-    while (tile_start[b + 1] <= u) ++b;
-    while (part_start(p + 1, W, S) <= u) ++p;
-    const long long s_b = tile_start[b], e_b = tile_start[b + 1];
+    if (e_b <= u) {
+      do ++b; while (tile_start[b + 1] <= u);
+      enter_sequence();
+    }
+    if (p_next <= u) enter_partition();
     t.b = b;
     t.tile = int(u - s_b);
-    int v = len[b] - t.tile * kTile;
+    const int v = len_b - t.tile * kTile;
     t.valid = v > kTile ? kTile : v;
-    t.first = (u == s_b) || (u == part_start(p, W, S));
-    t.last = (u + 1 == e_b) || (u + 1 == part_start(p + 1, W, S));
-    t.seg = seg_base[b] + int(p - part_of(s_b, W, S));
+    t.first = (u == s_b) || (u == p_start);
+    t.last = (u + 1 == e_b) || (u + 1 == p_next);
+    t.seg = seg_b + int(p);
     ++u;
     return true;
   }

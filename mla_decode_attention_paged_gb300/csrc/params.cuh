@@ -58,5 +58,8 @@ cudaError_t launch_combine_uv(const CombineUVParams& p, cudaStream_t stream);
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream);
 cudaError_t launch_decode_tc(const DecodeParams& p, int hc, bool int8, int grid, cudaStream_t stream);
 int decode_head_group(int heads, bool int8);
+// bf16 caches: CTA-pair kernel.  Capacity = clusters of two resident at once (0 if none).
+int decode_pair_capacity(int hc);
+cudaError_t launch_decode_pair(const DecodeParams& p, int hc, int pairs_per_group, cudaStream_t stream);
 
 }  // namespace mla
