@@ -62,20 +62,27 @@ def peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_traffic(workload_name: str, tokens: int):
+def attention_kernel(int8: bool):
+    """(source file, kernel name) of the attention kernel the library runs for this cache type."""
+    name = "decode_tc.cu" if int8 else "decode_pair.cu"
+    return (os.path.join(ROOT, "mla_decode_attention_paged_gb300", "csrc", name),
+            "decode_tc_kernel (single-CTA split-KV attention, INT8 cache)" if int8
+            else "decode_pair_kernel (split-KV attention on CTA pairs)")
+
+
+def kernel_traffic(workload_name: str, tokens: int, int8: bool):
     """DRAM bytes per attention launch from the committed ncu summary, scaled
     to this launch's tokens; None if absent or taken on a different kernel."""
     path = os.path.join(ROOT, "profiles", "attention_dram_traffic.json")
     if not os.path.exists(path):
         return None
-    d = json.load(open(path))
-    src = os.path.join(ROOT, "mla_decode_attention_paged_gb300", "csrc", "decode_tc.cu")
-    if hashlib.sha256(open(src, "rb").read()).hexdigest() != d.get("kernel_sha256"):
-        return None
-    e = d.get("workloads", {}).get(workload_name)
+    e = json.load(open(path)).get("workloads", {}).get(workload_name)
     if not e:
         return None
-    return e["dram_bytes_per_token"] * tokens
+    src, _ = attention_kernel(int8)
+    if hashlib.sha256(open(src, "rb").read()).hexdigest() != e.get("kernel_sha256"):
+        return None
+    return round(e["dram_bytes_per_token"] * tokens)
 
 
 class ClockSampler:
@@ -291,7 +298,7 @@ def run_ours(args, rank, world):
 
     peak, peak_src = peaks()
     achieved = cache_bytes / (kern_ms / 1e3) / 1e9
-    traffic = kernel_traffic(w.name, lens_sum)
+    traffic = kernel_traffic(w.name, lens_sum, w.int8)
     res = {
         "metric": METRIC, "value": round(tokens_per_s, 1), "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True,
@@ -307,7 +314,7 @@ def run_ours(args, rank, world):
         "attention_kernel_ms": round(kern_ms, 5),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_source": peak_src,
-                     "traffic": traffic, "kernel": "decode_tc_kernel (split-KV attention)",
+                     "traffic": traffic, "kernel": attention_kernel(w.int8)[1],
                      "algorithmic_bytes_per_launch": cache_bytes},
         "e2e": {"value": round(B * world / (e2e_ms / 1e3), 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 5)},

@@ -61,7 +61,7 @@ constexpr float kRescaleThreshold = 8.f;          // log2 units
 
 template <int HC>
 struct PairCfg {
-  static constexpr int kNumPair = HC == 16 ? 5 : 4;  // latent pair slots (two per tile)
+  static constexpr int kNumPair = 4;  // latent pair slots (two per tile; an even count keeps both producers in step)
   static constexpr int kNumRope = 3;                 // RoPE-half slots (one per tile)
   static constexpr uint32_t kQBytes = 4 * HC * 128 + HC * 64;  // four latent boxes + RoPE half
   static constexpr uint32_t kPBytes = kTile * HC * 2;          // P^T, bf16
