@@ -554,7 +554,13 @@ __global__ void __launch_bounds__(Cfg<HC, kInt8>::kThreads, 1)
       if (kInt8) {
         if (t.first)
 #pragma unroll
-          for (int h = 0; h < HC; ++h) qsum[h] = p.q_sum[size_t(t.b) * p.heads + g * HC + h];
+          for (int h = 0; h < HC; ++h) {
+            const float* qs = p.q_sum + (size_t(t.b) * p.heads + g * HC + h) * kQSumParts;
+            float s = qs[0];
+#pragma unroll
+            for (int c = 1; c < kQSumParts; ++c) s += qs[c];
+            qsum[h] = s;
+          }
         if (valid) {
           const int tok = t.tile * kTile + st;
           const float2 sz = *reinterpret_cast<const float2*>(p.scale_zero +

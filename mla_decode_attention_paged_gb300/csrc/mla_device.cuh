@@ -16,6 +16,7 @@ constexpr int kRope = 64;              // d_rope
 constexpr int kRow = kLatent + kRope;  // 576 numbers per token per layer
 constexpr int kNope = 128;             // per-head content query width
 constexpr int kVDim = 128;             // per-head value width
+constexpr int kQSumParts = 8;          // q_sum partials per (sequence, head)
 constexpr int kTile = 128;             // tokens per decode tile (one MMA M extent)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -26,11 +27,13 @@ constexpr float kLn2 = 0.6931471805599453f;
 //   seg_base       int32 [B + 1]   prefix sum of the number of segments per sequence
 //   len_checked    int32 [B]       seq_lens after range checks (0 if rejected)
 //   q_full         bf16  [B, H, 576]  [W^UK_h^T q_nope | q_pe] per (b, h)
-//   q_sum          fp32  [B, H]       sum of q_full's 576 bf16 values (INT8 caches)
+//   q_sum          fp32  [B, H, 8]    partial sums of q_full's 576 values (INT8 caches):
+//                                     part c covers latent dims [64c, 64c + 64), part 0 also the RoPE part
 //   partial_lse    fp32  [NSEG, H]
 //   partial_o      fp32  [NSEG, H, 512]   NSEG = num_splits + B (upper bound)
+//   o_lat          fp32  [B, H, 512]      merged latent outputs
 struct WorkspaceLayout {
-  size_t status, tile_start, seg_base, len_checked, q_full, q_sum, partial_lse, partial_o, total;
+  size_t status, tile_start, seg_base, len_checked, q_full, q_sum, partial_lse, partial_o, o_lat, total;
 };
 
 __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -43,10 +46,11 @@ __host__ __device__ inline WorkspaceLayout workspace_layout(int batch, int heads
   L.seg_base = off;     off = align256(off + 4 * size_t(batch + 1));
   L.len_checked = off;  off = align256(off + 4 * size_t(batch));
   L.q_full = off;       off = align256(off + 2 * size_t(batch) * heads * kRow);
-  L.q_sum = off;        off = align256(off + 4 * size_t(batch) * heads);
+  L.q_sum = off;        off = align256(off + 4 * size_t(batch) * heads * kQSumParts);
   const size_t nseg = size_t(num_splits) + batch;
   L.partial_lse = off;  off = align256(off + 4 * nseg * heads);
   L.partial_o = off;    off = align256(off + 4 * nseg * heads * kLatent);
+  L.o_lat = off;        off = align256(off + 4 * size_t(batch) * heads * kLatent);
   L.total = off;
   return L;
 }
@@ -149,7 +153,7 @@ struct TileWalker {
 
 struct DecodeParams {
   const __nv_bfloat16* q_full;   // [B, H, 576]
-  const float* q_sum;            // [B, H] (INT8)
+  const float* q_sum;            // [B, H, kQSumParts] (INT8)
   const void* cache;             // bf16 or int8 [num_pages, P, 576]
   const float* scale_zero;       // [num_pages, P, 2] (INT8)
   const int* block_table;        // [B, max_pages]

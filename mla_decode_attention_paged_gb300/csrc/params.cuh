@@ -11,7 +11,7 @@ struct AbsorbParams {
   const __nv_bfloat16* q_pe;    // [B, H, 64]
   const __nv_bfloat16* W_UK;    // [H, 128, 512]
   __nv_bfloat16* q_full;        // [B, H, 576] (fp16 bit patterns for INT8 caches)
-  float* q_sum;                 // [B, H]
+  float* q_sum;                 // [B, H, kQSumParts]
   // plan
   const int* seq_lens;
   int* tile_start;
@@ -38,10 +38,12 @@ struct CombineUVParams {
   const float* partial_o;     // [NSEG, H, 512]
   const float* partial_lse;   // [NSEG, H]
   const int* seg_base;        // [B + 1]
+  float* o_lat;               // [B, H, 512] merged latent outputs (written by the merge kernel)
   const __nv_bfloat16* W_UV;  // [H, 128, 512]
   __nv_bfloat16* out;         // [B, H, 128]
   float* lse_out;             // [B, H] or null
   int batch, heads;
+  int max_segments;           // num_splits + batch: bound on the segments of all sequences
 };
 
 struct CombineParams {
