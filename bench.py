@@ -48,10 +48,26 @@ def dist_setup(n):
     rank, world = int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1))
     if world > 1:
         import torch.distributed as dist
-        local = int(os.environ.get("LOCAL_RANK", 0))
-        torch.cuda.set_device(local)
+        if torch.cuda.is_available():
+            torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
         dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
     return rank, world
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    """The slowest rank's value (the whole job ends when the last rank does)."""
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank: float, world: int, ms: float) -> float:
+    """Units all ranks processed per second, over the slowest rank's time (weak scaling)."""
+    return units_per_rank * world / (ms / 1e3)
 
 
 def peaks():
@@ -250,16 +266,13 @@ def run_ours(args, rank, world):
         torch.distributed.barrier()
     ms_total = e0.elapsed_time(e1)
     kern_ms = statistics.mean(a.elapsed_time(b) for a, b in kev)
-    if world > 1:
-        t = torch.tensor([ms_total], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = max_over_ranks(ms_total, world)
     ms = ms_total / args.steps
     lens_sum = int(seq_lens.to(torch.int64).sum())
     bytes_per_token = 584 if w.int8 else 1152
     cache_bytes = lens_sum * bytes_per_token
-    tokens_per_s = B * world / (ms / 1e3)
-    step_cache_gbs = cache_bytes / (ms / 1e3) / 1e9
+    tokens_per_s = whole_job_rate(B, world, ms)
+    step_cache_gbs = whole_job_rate(cache_bytes, world, ms) / 1e9
 
     # e2e: the same step through the public API from pinned host buffers
     pin = lambda t: t.cpu().pin_memory()
@@ -291,10 +304,7 @@ def run_ours(args, rank, world):
     x1.record()
     torch.cuda.synchronize()
     e2e_ms = x0.elapsed_time(x1) / args.steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e2e_ms, world)
 
     peak, peak_src = peaks()
     achieved = cache_bytes / (kern_ms / 1e3) / 1e9
@@ -316,7 +326,7 @@ def run_ours(args, rank, world):
                      "frac": round(achieved / peak, 4), "peak_source": peak_src,
                      "traffic": traffic, "kernel": attention_kernel(w.int8)[1],
                      "algorithmic_bytes_per_launch": cache_bytes},
-        "e2e": {"value": round(B * world / (e2e_ms / 1e3), 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+        "e2e": {"value": round(whole_job_rate(B, world, e2e_ms), 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 5)},
         "gpu_launches": 4 * args.steps,
         "clocks": clk.summary(),

@@ -40,8 +40,7 @@ __global__ void __launch_bounds__(256) append_kernel(AppendParams p) {
   const __nv_bfloat162 kp = reinterpret_cast<const __nv_bfloat162*>(p.k_pe + size_t(i) * kRope)[lane];
   __nv_bfloat162 kr = kp;
   if (p.rope_theta > 0.0) {
-    const double inv_freq = pow(p.rope_theta, -double(2 * lane) / double(kRope));
-    const double ang = __dmul_rn(double(pos), inv_freq);
+    const double ang = __dmul_rn(double(pos), p.inv_freq[lane]);
     double sn, cs;
     sincos(ang, &sn, &cs);
     const double x0 = double(__low2float(kp)), x1 = double(__high2float(kp));
@@ -111,7 +110,9 @@ __global__ void __launch_bounds__(256) append_kernel(AppendParams p) {
 
 cudaError_t launch_append(const AppendParams& p, bool int8, cudaStream_t stream) {
   if (p.n_tokens == 0) return cudaSuccess;
-  const int warps = 8;
+  // a decode step appends one token per sequence: one warp per block spreads
+  // the fp64 RoPE over as many SMs as there are tokens
+  const int warps = p.n_tokens < 2048 ? 1 : 8;
   const int grid = (p.n_tokens + warps - 1) / warps;
   if (int8) append_kernel<true><<<grid, warps * 32, 0, stream>>>(p);
   else append_kernel<false><<<grid, warps * 32, 0, stream>>>(p);

@@ -2,6 +2,7 @@
 // argument validation, sizing of the decode work plan, and kernel launches
 // on the caller's stream.  Allocates nothing.
 #include <atomic>
+#include <cmath>
 #include <cstdint>
 #include <cstdio>
 
@@ -95,6 +96,9 @@ int mla_cache_append(const mla_dims* d, void* cache, float* cache_scale_zero, in
   p.k_pe = static_cast<const __nv_bfloat16*>(k_pe);
   p.status = device_status;
   p.rope_theta = rope_theta;
+  // the frequencies depend only on theta: one fp64 pow per pair here instead
+  // of one per token and pair on the device's slow fp64 units
+  for (int i = 0; i < kRope / 2; ++i) p.inv_freq[i] = rope_theta > 0.0 ? std::pow(rope_theta, -double(2 * i) / double(kRope)) : 0.0;
   p.n_tokens = n_tokens;
   p.num_seqs = num_seqs;
   p.max_pages = max_pages_per_seq;

@@ -31,6 +31,7 @@ struct AppendParams {
   const __nv_bfloat16* k_pe;     // [N, 64]
   int* status;                   // optional
   double rope_theta;
+  double inv_freq[kRope / 2];    // theta^(-2i/64), evaluated on the host in fp64
   int n_tokens, num_seqs, max_pages, num_pages, page_size;
 };
 
