@@ -237,6 +237,16 @@ const char* mla_status_string(int status);
  * Pass NULLs to clear.  Process-wide; not for concurrent profiling. */
 int mla_set_timing_events(mla_event_t start, mla_event_t stop);
 
+/* Test hook for the device-side failure detection (no counterpart on the
+ * pages).  While enabled (non-zero), every mla_decode launches its attention
+ * kernel with the first cache-page barrier of each CTA expecting 16 bytes more
+ * than its copies deliver: that wait cannot complete, runs into its time
+ * limit (about 2 s), and the kernel records MLA_ERR_DEVICE_TIMEOUT in the
+ * workspace status word, releases its resources and returns; the device and
+ * the context stay usable.  Nothing faults, traps or hangs.  Process-wide; 0
+ * (the default) disables it.  Returns MLA_OK. */
+int mla_test_inject_wait_timeout(int32_t enable);
+
 /* Library version: major * 10000 + minor * 100 + patch. */
 int mla_version(void);
 

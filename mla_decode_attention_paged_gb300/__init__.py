@@ -39,6 +39,7 @@ EXPORTED_SYMBOLS = (
     "mla_check_dims", "mla_cache_append", "mla_auto_num_splits", "mla_decode_workspace_size",
     "mla_decode", "mla_combine", "mla_read_device_status", "mla_read_status_word",
     "mla_status_string", "mla_set_timing_events", "mla_version", "mla_decode_no_alloc",
+    "mla_test_inject_wait_timeout",
 )
 NO_ALLOC_WORKSPACE_BYTES = 16 << 20  # MLA_NO_ALLOC_WORKSPACE_BYTES in include/mla.h
 
@@ -94,6 +95,7 @@ def load_library(build_if_missing: bool = False, path: str | None = None):
         "mla_status_string": (ctypes.c_char_p, [ctypes.c_int]),
         "mla_set_timing_events": (_I, [_P, _P]),
         "mla_version": (ctypes.c_int, []),
+        "mla_test_inject_wait_timeout": (_I, [_I]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -258,6 +260,12 @@ def read_status_word(word: torch.Tensor, stream=None) -> int:
     _check(_L().mla_read_status_word(_ptr(word, torch.int32, "status word"), ctypes.byref(v), _stream(stream)),
            "mla_read_status_word")
     return v.value
+
+
+def test_inject_wait_timeout(enable: bool) -> None:
+    """Test hook: make the attention kernel's first page wait of each CTA unsatisfiable
+    (it times out and the status word reports MLA_ERR_DEVICE_TIMEOUT)."""
+    _check(_L().mla_test_inject_wait_timeout(1 if enable else 0), "mla_test_inject_wait_timeout")
 
 
 def set_timing_events(start: torch.cuda.Event | None, stop: torch.cuda.Event | None) -> None:

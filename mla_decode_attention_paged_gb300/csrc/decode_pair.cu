@@ -199,7 +199,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
         const uint32_t slot = it % C::kNumPair;
         if (!(ok = mbar_wait(&B->empty_pair[slot], ((it / C::kNumPair) & 1) ^ 1, abort_flag, kWaitLimitNs))) break;
         uint8_t* dst = smem + C::kOffPair + slot * kPairBytes;
-        mbar_arrive_expect_tx(&B->full_pair[slot], 2 * npg * page_bytes);
+        mbar_arrive_expect_tx(&B->full_pair[slot], 2 * npg * page_bytes + (p.inject_wait_timeout && it == 0 ? 16 : 0));
 #pragma unroll 1
         for (int i = 0; i < npg; ++i) {
           tma_load_2d(dst + i * page_bytes, &tmap_latent, lat0 + 128 * c, rows[i], &B->full_pair[slot]);

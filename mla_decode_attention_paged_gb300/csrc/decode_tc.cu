@@ -276,7 +276,7 @@ __global__ void __launch_bounds__(Cfg<HC, kInt8>::kThreads, 1)
           if (!(ok = mbar_wait(&B->empty_qk[qr][slot], ((box_it / C::kQkRing) & 1) ^ 1, abort_flag, kWaitLimitNs)))
             break;
           uint8_t* dst = smem + C::kOffQk + (qr * C::kQkRing + slot) * kBoxBytes;
-          mbar_arrive_expect_tx(&B->full_qk[qr][slot], npg * page_bytes);
+          mbar_arrive_expect_tx(&B->full_qk[qr][slot], npg * page_bytes + (p.inject_wait_timeout && box_it == 0 ? 16 : 0));
 #pragma unroll 1
           for (int i = 0; i < npg; ++i) load(dst + i * page_bytes, 64 * j, rows[i], &B->full_qk[qr][slot]);
         }
@@ -287,7 +287,7 @@ __global__ void __launch_bounds__(Cfg<HC, kInt8>::kThreads, 1)
             break;
           // int8 codes of columns [128c, 128c + 128) into the slot's back half, as two [128 x 64 B] blocks
           uint8_t* dst = smem + C::kOffPair + slot * kPairBytes;
-          mbar_arrive_expect_tx(&B->full_i8_pair[slot], npg * page_bytes);
+          mbar_arrive_expect_tx(&B->full_i8_pair[slot], npg * page_bytes + (p.inject_wait_timeout && pair_it == 0 ? 16 : 0));
 #pragma unroll 1
           for (int i = 0; i < npg; ++i) {
             load(dst + kBoxBytes + i * P * 64, 128 * c, rows[i], &B->full_i8_pair[slot]);

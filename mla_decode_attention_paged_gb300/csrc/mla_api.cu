@@ -17,6 +17,7 @@ namespace {
 constexpr int kVersion = 100;  // 0.1.0
 
 std::atomic<cudaEvent_t> g_ev_start{nullptr}, g_ev_stop{nullptr};
+std::atomic<int> g_inject_wait_timeout{0};
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -187,6 +188,7 @@ int mla_decode(const mla_dims* d, const void* q_nope, const void* q_pe, const vo
   dp.num_pages = num_pages;
   dp.num_splits = S;
   dp.scale_log2 = softmax_scale * kLog2e;
+  dp.inject_wait_timeout = g_inject_wait_timeout.load();
   // bf16 caches run on CTA pairs (two SMs share each tile); INT8 caches, and
   // devices that cannot place the pairs, on single CTAs
   const int pair_cap = int8 ? 0 : decode_pair_capacity(hc);
@@ -247,6 +249,11 @@ int mla_read_status_word(const int32_t* device_status, int32_t* status_out, mla_
 int mla_read_device_status(const void* workspace, int32_t* status_out, mla_stream_t stream) {
   if (!workspace) return MLA_ERR_INVALID_ARG;
   return mla_read_status_word(static_cast<const int32_t*>(workspace), status_out, stream);
+}
+
+int mla_test_inject_wait_timeout(int32_t enable) {
+  g_inject_wait_timeout.store(enable != 0);
+  return MLA_OK;
 }
 
 int mla_set_timing_events(mla_event_t start, mla_event_t stop) {

@@ -165,6 +165,7 @@ struct DecodeParams {
   int* status;
   int batch, heads, head_group, num_groups, page_size, max_pages, num_pages, num_splits;
   float scale_log2;              // softmax_scale * log2(e)
+  int inject_wait_timeout;       // test hook (mla_test_inject_wait_timeout): 16 bytes never delivered
 };
 
 __device__ inline void set_status(int* status, int code) {
