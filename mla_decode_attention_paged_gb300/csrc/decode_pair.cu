@@ -58,6 +58,7 @@ constexpr uint32_t kPairBytes = 2 * kBoxBytes;  // 128 latent columns: one O^T c
 constexpr uint32_t kRopeBytes = 8192;           // [128 tokens x 32 columns] bf16, 64-byte swizzle
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 constexpr float kRescaleThreshold = 8.f;          // log2 units
+constexpr bool kPrefetchNext = true;              // L2 prefetch of the next tile's boxes
 
 template <int HC>
 struct PairCfg {
@@ -173,13 +174,23 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     const uint32_t page_bytes = uint32_t(P) * 128, rope_page_bytes = uint32_t(P) * 64;
     uint32_t pair_it = 0, rope_it = 0, seg = 0;
     TileInfo t, tn;
+    // page ids two tiles ahead: tile k + 1's are in registers (and arrived)
+    // when tile k starts, for the L2 prefetch; tile k + 2's are on their way
     TileWalker look = walk;
-    TilePages pages, next_pages;
-    if (look.next(tn)) next_pages.fetch(p, tn);
+    TilePages pages, next_pages, next2_pages;
+    bool have_next = look.next(tn), have_next2 = false;
+    if (have_next) next_pages.fetch(p, tn);
+    if (have_next) {
+      have_next2 = look.next(tn);
+      if (have_next2) next2_pages.fetch(p, tn);
+    }
     bool ok = true;
     while (ok && walk.next(t)) {
       pages = next_pages;
-      if (look.next(tn)) next_pages.fetch(p, tn);
+      next_pages = next2_pages;
+      have_next = have_next2;
+      have_next2 = have_next && look.next(tn);
+      if (have_next2) next2_pages.fetch(p, tn);
       if (t.first && role == 0) {
         if (seg > 0 && !(ok = mbar_wait(&B->q_empty, (seg - 1) & 1, abort_flag, kWaitLimitNs))) break;
         mbar_arrive_expect_tx(&B->q_full, C::kQBytes);
@@ -192,6 +203,18 @@ __global__ void __launch_bounds__(kPairThreads, 1)
       const int npg = pages.npg;
       int rows[kTile / 16];
       pages.rows(p, rows);
+      if (kPrefetchNext && have_next) {
+        // the next tile's boxes into L2 now: its copies, issued once a slot
+        // frees, then find them there instead of waiting on DRAM
+        int nrows[kTile / 16];
+        next_pages.rows(p, nrows);
+#pragma unroll 1
+        for (int i = 0; i < next_pages.npg; ++i) {
+          tma_prefetch_2d(&tmap_latent, lat0 + 128 * role, nrows[i]);
+          tma_prefetch_2d(&tmap_latent, lat0 + 128 * role + 64, nrows[i]);
+          if (role == 1) tma_prefetch_2d(&tmap_rope, rope0, nrows[i]);
+        }
+      }
       {
         const int c = role;
         const uint32_t it = pair_it + c;
