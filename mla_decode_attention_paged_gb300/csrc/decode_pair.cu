@@ -203,9 +203,11 @@ __global__ void __launch_bounds__(kPairThreads, 1)
       const int npg = pages.npg;
       int rows[kTile / 16];
       pages.rows(p, rows);
-      if (kPrefetchNext && have_next) {
+      if (kPrefetchNext && have_next && G == 1) {
         // the next tile's boxes into L2 now: its copies, issued once a slot
-        // frees, then find them there instead of waiting on DRAM
+        // frees, then find them there instead of waiting on DRAM (with
+        // several head groups each tile is read by every group, and the
+        // extra requests cost more than they save)
         int nrows[kTile / 16];
         next_pages.rows(p, nrows);
 #pragma unroll 1
