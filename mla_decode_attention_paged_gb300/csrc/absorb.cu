@@ -8,13 +8,17 @@
 // q_full = [q_lat | q_pe].
 #include <cuda_fp16.h>
 
+#include "blackwell_ptx.cuh"
+#include "decode_common.cuh"
 #include "params.cuh"
 
 namespace mla {
 
+using namespace ptx;
 
-
-// Block (0, 0) also computes the work plan before its share of the absorption.
+// The work plan (checked lengths, each sequence's first tile and first
+// segment, the effective split count), built by one extra CTA of the
+// absorption grid (its first) while the others absorb.
 __device__ void compute_plan(const AbsorbParams& p) {
   __shared__ int scan_tmp[32];
   __shared__ int carry;
@@ -69,9 +73,6 @@ __device__ void compute_plan(const AbsorbParams& p) {
   if (threadIdx.x == 0) p.seg_base[p.batch] = carry;
 }
 
-constexpr int kAbsM = 64;   // latent dims per block
-constexpr int kAbsB = 32;   // sequences per pass
-
 template <bool kF16>
 __device__ __forceinline__ float round_out(float v, uint16_t* dst) {  // store as bf16/fp16, return the stored value
   if constexpr (kF16) {
@@ -85,96 +86,204 @@ __device__ __forceinline__ float round_out(float v, uint16_t* dst) {  // store a
   }
 }
 
-// grid (H, 512 / 64), block 256.  Block (h, c) computes latent dims
-// [64c, 64c + 64) of q_lat = W^UK_h^T q_nope for every sequence, with W^UK_h's
-// columns staged in shared memory; thread (m, g) handles dim m for 8
-// sequences per pass, fp32 accumulation over the 128 content dims.  Blocks
-// (h, 0) also copy the RoPE part.  Part c of q_sum[b][h] is the sum of the
-// rounded values the block wrote (part 0 includes the RoPE part).  INT8
-// caches take q_full in fp16 (their tensor-core path runs on fp16 operands);
-// bf16 caches in bf16.
-template <bool kF16>
-__global__ void __launch_bounds__(256) absorb_kernel(AbsorbParams p) {
-  if (blockIdx.x == 0 && blockIdx.y == 0) {
+// ---------------------------------------------------------------------------
+// Absorption on the tensor cores.  Per head the product is a small GEMM,
+// q_lat^T [512 x B] = W^UK_h^T [512 x 128] * q_nope_h^T [128 x B]; a CTA takes
+// one 128-row tile of latent dims (the MMA's M) and NB sequences (its N):
+//   A = W^UK_h[:, m0:m0+128]^T   MN-major (W^UK rows are 512 latent dims long)
+//   B = q_nope[b0:b0+NB, h, :]^T K-major  (q_nope rows are 128 content dims)
+// both staged by the CTA's threads into 128-byte-swizzled shared memory, eight
+// K = 16 MMAs into an fp32 TMEM accumulator, then one thread per latent dim
+// rounds its column of sequences to bf16 (fp16 for INT8 caches) and stores it.
+// Part c of q_sum[b][h] is the sum of the rounded values of latent dims
+// [64c, 64c + 64) (part 0 also the RoPE part): INT8 caches need the sum of
+// exactly the query the tensor cores see (bf16 caches do not use it).  INT8 caches take q_full in fp16
+// (their tensor-core path runs on fp16 operands); bf16 caches in bf16.
+constexpr int kAbsThreads = 128;
+constexpr int kAbsMTile = 128;                               // latent dims per CTA
+constexpr uint32_t kAbsBlockBytes = kNope * 64 * 2;          // [128 k x 64 m] bf16, one swizzle column block
+constexpr uint32_t kAbsWBytes = 2 * kAbsBlockBytes;          // 32 KB
+constexpr uint64_t kAbsWaitNs = 2000000000ull;
+
+template <int NB>
+struct AbsCfg {
+  static constexpr uint32_t kQBox = NB * 128;                // [NB x 64 k] bf16
+  static constexpr uint32_t kOffQ = kAbsWBytes;
+  static constexpr uint32_t kOffMisc = kOffQ + 2 * kQBox;
+  static constexpr uint32_t kSmem = kOffMisc + 64 + NB * 4 * 4 + NB * 4 + 1024;
+  static constexpr uint32_t kTmemCols = NB < 32 ? 32 : NB;
+};
+
+template <bool kF16, int NB>
+__global__ void __launch_bounds__(kAbsThreads) absorb_kernel(AbsorbParams p) {
+  using C = AbsCfg<NB>;
+  if (blockIdx.x == 0) {  // the first CTA (scheduled first) builds the work plan
+    griddep_wait();
+    griddep_launch_dependents();
     compute_plan(p);
-    __syncthreads();
+    return;
   }
-  __shared__ __align__(16) __nv_bfloat16 ws[kNope][kAbsM];
-  __shared__ __align__(16) float qs[kAbsB][kNope];
-  __shared__ float red[kAbsB][2];
-  const int h = blockIdx.x, c = blockIdx.y, tid = threadIdx.x, lane = tid & 31;
-  const int m = tid & (kAbsM - 1), grp = tid >> 6;  // grp handles sequences 8 grp .. 8 grp + 7 of a pass
-  for (int idx = tid; idx < kNope * kAbsM / 8; idx += blockDim.x) {
-    const int k = idx >> 3, part = idx & 7;
-    reinterpret_cast<uint4*>(&ws[k][0])[part] =
-        *reinterpret_cast<const uint4*>(p.W_UK + (size_t(h) * kNope + k) * kLatent + c * kAbsM + part * 8);
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* mma_done = reinterpret_cast<uint64_t*>(smem + C::kOffMisc);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc + 8);
+  int* abort_flag = reinterpret_cast<int*>(smem + C::kOffMisc + 12);
+  float* red = reinterpret_cast<float*>(smem + C::kOffMisc + 64);  // [NB][4] per-warp sums
+  float* rope_sum = red + NB * 4;                                  // [NB]
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int per_head = 4 * ((p.batch + NB - 1) / NB);
+  const int tile = blockIdx.x - 1, h = tile / per_head, rem = tile % per_head, mt = rem & 3, b0 = (rem >> 2) * NB;
+  const int m0 = mt * kAbsMTile, nb = min(NB, p.batch - b0);
+  if (tid == 0) {
+    mbar_init(mma_done, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
   }
+  if (warp == 0) {
+    tmem_alloc(tmem_slot, C::kTmemCols);
+    tmem_relinquish();
+  }
+  griddep_wait();
+  griddep_launch_dependents();
+  // W^UK_h[k][m0 + m]: row k of 128 dims = 16 chunks of 8; chunk j goes to
+  // column block j / 8, 16-byte slot (j % 8) ^ (k % 8).  q_nope[b0 + r][h][:]:
+  // chunk j of row r goes to K block j / 8, slot (j % 8) ^ (r % 8).  Every
+  // load is issued before the first store, so the staging costs one memory
+  // round trip.
+  constexpr int kWPer = kNope * 16 / kAbsThreads, kQPer = NB * 16 / kAbsThreads;
+  uint4 wv[kWPer], qv[kQPer];
+#pragma unroll
+  for (int u = 0; u < kWPer; ++u) {
+    const int i = tid + u * kAbsThreads, k = i >> 4, j = i & 15;
+    wv[u] = *reinterpret_cast<const uint4*>(p.W_UK + (size_t(h) * kNope + k) * kLatent + m0 + 8 * j);
+  }
+#pragma unroll
+  for (int u = 0; u < kQPer; ++u) {
+    const int i = tid + u * kAbsThreads, r = i >> 4, j = i & 15;
+    qv[u] = make_uint4(0, 0, 0, 0);
+    if (r < nb) qv[u] = *reinterpret_cast<const uint4*>(p.q_nope + (size_t(b0 + r) * p.heads + h) * kNope + 8 * j);
+  }
+#pragma unroll
+  for (int u = 0; u < kWPer; ++u) {
+    const int i = tid + u * kAbsThreads, k = i >> 4, j = i & 15;
+    *reinterpret_cast<uint4*>(smem + (j >> 3) * kAbsBlockBytes + k * 128 + (((j & 7) ^ (k & 7)) << 4)) = wv[u];
+  }
+#pragma unroll
+  for (int u = 0; u < kQPer; ++u) {
+    const int i = tid + u * kAbsThreads, r = i >> 4, j = i & 15;
+    *reinterpret_cast<uint4*>(smem + C::kOffQ + (j >> 3) * C::kQBox + r * 128 + (((j & 7) ^ (r & 7)) << 4)) = qv[u];
+  }
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot, sbase = smem_u32(smem);
+  if (tid == 0) {
+    constexpr uint32_t idesc = idesc_f32acc(128, NB, true, false, false);
+    constexpr uint64_t kDescA = smem_desc(0, kAbsBlockBytes, 1024, kSwizzle128B);  // MN-major
+    constexpr uint64_t kDescB = smem_desc(0, 16, 1024, kSwizzle128B);              // K-major
+#pragma unroll
+    for (int kk = 0; kk < kNope / 16; ++kk)
+      mma_bf16(tmem, kDescA | desc_addr(sbase + kk * 2048),
+               kDescB | desc_addr(sbase + C::kOffQ + (kk >> 2) * C::kQBox + (kk & 3) * 32), idesc, kk > 0);
+    mma_commit(mma_done);
+  }
+  __syncwarp();  // lanes 1-31 must not start waiting while lane 0 still issues
+  // RoPE part (m-tile 0): eight threads per sequence, eight values (16 bytes) each
   uint16_t* qf = reinterpret_cast<uint16_t*>(p.q_full);
-  for (int b0 = 0; b0 < p.batch; b0 += kAbsB) {
-    const int nb = min(kAbsB, p.batch - b0);
-    __syncthreads();  // ws loaded; qs and red free
-    for (int idx = tid; idx < kAbsB * kNope / 8; idx += blockDim.x) {
-      const int i = idx >> 4, part = idx & 15;
-      uint4 v = make_uint4(0, 0, 0, 0);
-      if (i < nb) v = *reinterpret_cast<const uint4*>(p.q_nope + (size_t(b0 + i) * p.heads + h) * kNope + part * 8);
-      const __nv_bfloat162* v2 = reinterpret_cast<const __nv_bfloat162*>(&v);
+  if (mt == 0) {
+    constexpr int kPasses = NB * 8 / kAbsThreads > 0 ? NB * 8 / kAbsThreads : 1;
+    uint4 pe[kPasses];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float2 f = __bfloat1622float2(v2[e]);
-        qs[i][part * 8 + 2 * e] = f.x;
-        qs[i][part * 8 + 2 * e + 1] = f.y;
+    for (int u = 0; u < kPasses; ++u) {
+      const int r = (tid >> 3) + u * (kAbsThreads / 8);
+      pe[u] = make_uint4(0, 0, 0, 0);
+      if (r < nb)
+        pe[u] = *reinterpret_cast<const uint4*>(p.q_pe + (size_t(b0 + r) * p.heads + h) * kRope + (tid & 7) * 8);
+    }
+#pragma unroll
+    for (int u = 0; u < kPasses; ++u) {
+      const int r = (tid >> 3) + u * (kAbsThreads / 8);
+      const __nv_bfloat16* x = reinterpret_cast<const __nv_bfloat16*>(&pe[u]);
+      uint16_t o[8];
+      float rs = 0.f;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) rs += round_out<kF16>(bf2f(x[e]), &o[e]);
+      if (r < nb)
+        *reinterpret_cast<uint4*>(qf + (size_t(b0 + r) * p.heads + h) * kRow + kLatent + (tid & 7) * 8) =
+            *reinterpret_cast<const uint4*>(o);
+      if (kF16) {
+#pragma unroll
+        for (int off = 4; off > 0; off >>= 1) rs += __shfl_xor_sync(0xffffffffu, rs, off);
+        if ((tid & 7) == 0 && r < NB) rope_sum[r] = rs;
       }
     }
-    __syncthreads();
-    float acc[8];
+  }
+  const bool ok = mbar_wait(mma_done, 0, abort_flag, kAbsWaitNs);
+  tc_fence_after();
+  if (ok) {
+    // thread (warp, lane) holds latent dim m0 + 32 warp + lane for every sequence
+    const int m = m0 + 32 * warp + lane;
+#pragma unroll 1
+    for (int c = 0; c < NB; c += 16) {
+      float v[16];
+      tmem_ld16(tmem + (uint32_t(32 * warp) << 16) + c, v);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-#pragma unroll 4
-    for (int k = 0; k < kNope; k += 4) {
-      const float w0 = bf2f(ws[k][m]), w1 = bf2f(ws[k + 1][m]), w2 = bf2f(ws[k + 2][m]), w3 = bf2f(ws[k + 3][m]);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const float4 q = *reinterpret_cast<const float4*>(&qs[8 * grp + i][k]);  // same address across the warp
-        acc[i] = fmaf(w3, q.w, fmaf(w2, q.z, fmaf(w1, q.y, fmaf(w0, q.x, acc[i]))));
+      for (int i = 0; i < 16; ++i) {
+        const int r = c + i;
+        v[i] = r < nb ? round_out<kF16>(v[i], qf + (size_t(b0 + r) * p.heads + h) * kRow + m) : 0.f;
+      }
+      if (kF16) {  // INT8 caches: this warp's 32 dims summed per sequence; lanes 2i, 2i + 1 get sequence c + i
+        const float sum = dc::warp_transpose_reduce<16, false>(v, lane);
+        if (!(lane & 1)) red[(c + (lane >> 1)) * 4 + warp] = sum;
       }
     }
-    // round, store and sum this block's part of each sequence's q_full row
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int bi = 8 * grp + i;
-      float r = 0.f;
-      if (bi < nb) r = round_out<kF16>(acc[i], qf + (size_t(b0 + bi) * p.heads + h) * kRow + c * kAbsM + m);
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) r += __shfl_xor_sync(0xffffffffu, r, o);
-      if (lane == 0) red[bi][(tid >> 5) & 1] = r;
+  } else {
+    set_status(p.status, MLA_ERR_DEVICE_TIMEOUT);
+  }
+  tc_fence_before();
+  __syncthreads();
+  // part 2 mt + q of q_sum[b][h]: latent dims [m0 + 64 q, m0 + 64 q + 64), plus the RoPE part in part 0
+  if (kF16 && ok)
+    for (int i = tid; i < 2 * nb; i += kAbsThreads) {
+      const int r = i >> 1, q = i & 1;
+      float v = red[r * 4 + 2 * q] + red[r * 4 + 2 * q + 1];
+      if (mt == 0 && q == 0) v += rope_sum[r];
+      p.q_sum[(size_t(b0 + r) * p.heads + h) * kQSumParts + 2 * mt + q] = v;
     }
-    __syncthreads();
-    // RoPE part (blocks c == 0): eight threads per sequence, eight values each
-    const int bi = tid >> 3, r8 = tid & 7;
-    float rope = 0.f;
-    if (c == 0) {
-      if (bi < nb) {
-        const size_t row = size_t(b0 + bi) * p.heads + h;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int d = r8 * 8 + e;
-          rope += round_out<kF16>(bf2f(p.q_pe[row * kRope + d]), qf + row * kRow + kLatent + d);
-        }
-      }
-#pragma unroll
-      for (int o = 4; o > 0; o >>= 1) rope += __shfl_xor_sync(0xffffffffu, rope, o);
-    }
-    if (r8 == 0 && bi < nb)
-      p.q_sum[(size_t(b0 + bi) * p.heads + h) * kQSumParts + c] = (red[bi][0] + red[bi][1]) + rope;
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
   }
 }
 
+template <bool kF16, int NB>
+cudaError_t launch_absorb_nb(const AbsorbParams& p, cudaStream_t stream) {
+  using C = AbsCfg<NB>;
+  static bool attr[128] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 128 || !attr[dev]) {
+    const cudaError_t e = cudaFuncSetAttribute(absorb_kernel<kF16, NB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               int(C::kSmem));
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 128) attr[dev] = true;
+  }
+  const int tiles = p.heads * 4 * ((p.batch + NB - 1) / NB);
+  return launch_pdl(absorb_kernel<kF16, NB>, dim3(tiles + 1), dim3(kAbsThreads), C::kSmem, stream, 1, p);
+}
+
+template <bool kF16>
+cudaError_t launch_absorb_t(const AbsorbParams& p, cudaStream_t stream) {
+  if (p.batch <= 16) return launch_absorb_nb<kF16, 16>(p, stream);
+  if (p.batch <= 32) return launch_absorb_nb<kF16, 32>(p, stream);
+  if (p.batch <= 64) return launch_absorb_nb<kF16, 64>(p, stream);
+  return launch_absorb_nb<kF16, 128>(p, stream);
+}
+
 cudaError_t launch_absorb(const AbsorbParams& p, bool fp16_out, cudaStream_t stream) {
-  dim3 grid(p.heads, kLatent / kAbsM);
-  static_assert(kLatent / kAbsM == kQSumParts, "one q_sum part per block of latent dims");
-  if (fp16_out) absorb_kernel<true><<<grid, 256, 0, stream>>>(p);
-  else absorb_kernel<false><<<grid, 256, 0, stream>>>(p);
-  return cudaGetLastError();
+  static_assert(kLatent / 64 == kQSumParts, "one q_sum part per 64 latent dims");
+  return fp16_out ? launch_absorb_t<true>(p, stream) : launch_absorb_t<false>(p, stream);
 }
 
 }  // namespace mla

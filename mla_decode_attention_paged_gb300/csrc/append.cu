@@ -8,6 +8,7 @@
 // ("PagedAttention: Virtual Memory for LLMs").  INT8 caches quantise the row
 // per token with an asymmetric min/max scale and zero point ("KV Cache
 // Optimization", section 3; "The Architecture of Memory", KIVI section).
+#include "blackwell_ptx.cuh"
 #include "params.cuh"
 
 namespace mla {
@@ -16,6 +17,8 @@ namespace mla {
 // One warp per token.  Lane l owns latent values [16l, 16l + 16) and RoPE pair l.
 template <bool kInt8>
 __global__ void __launch_bounds__(256) append_kernel(AppendParams p) {
+  ptx::griddep_wait();
+  ptx::griddep_launch_dependents();
   const int lane = threadIdx.x & 31;
   const int i = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (i >= p.n_tokens) return;
@@ -114,9 +117,8 @@ cudaError_t launch_append(const AppendParams& p, bool int8, cudaStream_t stream)
   // the fp64 RoPE over as many SMs as there are tokens
   const int warps = p.n_tokens < 2048 ? 1 : 8;
   const int grid = (p.n_tokens + warps - 1) / warps;
-  if (int8) append_kernel<true><<<grid, warps * 32, 0, stream>>>(p);
-  else append_kernel<false><<<grid, warps * 32, 0, stream>>>(p);
-  return cudaGetLastError();
+  return int8 ? launch_pdl(append_kernel<true>, dim3(grid), dim3(warps * 32), 0, stream, 1, p)
+              : launch_pdl(append_kernel<false>, dim3(grid), dim3(warps * 32), 0, stream, 1, p);
 }
 
 }  // namespace mla

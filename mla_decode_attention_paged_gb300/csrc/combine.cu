@@ -4,152 +4,321 @@
 // value up-projection that the absorbed form applies last ("The Weight
 // Absorption Trick"; "Seven Ways LLMs Handle Attention", section 5: the value
 // expansion is absorbed into the output side): out_h = W^UV_h o_lat_h.
+#include "blackwell_ptx.cuh"
+#include "decode_common.cuh"
 #include "params.cuh"
 
 namespace mla {
 
+using namespace ptx;
 
-constexpr int kCombB = 8;     // sequences per block
-constexpr int kCombJ = 64;    // output dims per block (of 128)
+// ---------------------------------------------------------------------------
+// Merge and up-projection in one kernel.  A CTA takes one head h and NB
+// sequences:
+//   1. its 16 warps merge each sequence's segments (partial outputs of the
+//      split-KV ranges) with log-sum-exp weights into o_lat[b][h] (fp32), and
+//      store it in shared memory as two bf16 rows, hi = bf16(o) and
+//      lo = bf16(o - hi), which carry o to about 2^-16 relative;
+//   2. one thread issues D [128 x 2 NB] = W^UV_h [128 x 512] * [hi | lo]^T on
+//      the tensor cores (32 K = 16 MMAs, fp32 accumulation in TMEM; the hi
+//      rows are D's first NB columns, the lo rows its last NB), with W^UV_h
+//      (exact in bf16) brought in by TMA while the warps merge;
+//   3. one thread per output dim j stores out[b][h][j] = D[j][b] + D[j][NB + b]
+//      (bf16) for the tile's sequences.
+// Both operands are K-major with 128-byte swizzle, in blocks of 64 latent
+// dims: W^UV_h block kb = rows j x dims [64 kb, 64 kb + 64) (16 KB), and the
+// [hi | lo] block kb = 2 NB rows x the same dims.
+constexpr int kUVWarps = 16;
+constexpr int kUVThreads = 32 * kUVWarps;
+constexpr int kUVBatch = 4;                  // segment rows a warp loads at once
+constexpr uint32_t kUVWBlock = kVDim * 128;  // 16 KB
+constexpr uint32_t kUVWBytes = 8 * kUVWBlock;
+constexpr uint64_t kUVWaitNs = 2000000000ull;
 
-constexpr int kMergeWarps = 16;  // at most
+template <int NB>
+struct UVCfg {
+  static_assert(NB == 8 || NB == 16 || NB == 32, "MMA N = 2 NB in 16 .. 64");
+  static constexpr uint32_t kBBlock = 2 * NB * 128;
+  static constexpr uint32_t kOffB = kUVWBytes;
+  static constexpr uint32_t kOffX = kOffB + 8 * kBBlock;  // [kUVWarps][512] fp32 cross-warp sums
+  static constexpr uint32_t kOffSeg = kOffX + kUVWarps * kLatent * 4;  // seg_base of the tile, NB + 1 ints
+  static constexpr uint32_t kOffMisc = kOffSeg + 256;
+  static constexpr uint32_t kSmem = kOffMisc + 64 + 1024;
+  static constexpr uint32_t kTmemCols = 2 * NB < 32 ? 32 : 2 * NB;
+  static_assert(kSmem <= 232448, "dynamic shared memory of one CTA");
+};
 
-// grid (H, B), block 32 nw (nw <= 16 warps, chosen from the average number
-// of segments per sequence): the LSE merge of the segments of sequence b,
-// head h.  Warp w takes segments w, w + nw, ...; lane l accumulates latent
-// dims [16 l, 16 l + 16); the warps' sums are added in warp order (the result
-// does not depend on timing).
-__global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(CombineUVParams p) {
-  extern __shared__ __align__(16) float part_raw[];  // [nw][kLatent]
-  __shared__ float red[kMergeWarps];
-  const int nw = blockDim.x >> 5;
-  __shared__ float s_mx, s_z;
-  const int h = blockIdx.x, b = blockIdx.y, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int s0 = p.seg_base[b], s1 = p.seg_base[b + 1];
-  // lse of the merged result: max, then sum of exp(lse_s - max)
-  float mx = -INFINITY;
-  for (int s = s0 + tid; s < s1; s += blockDim.x) mx = fmaxf(mx, p.partial_lse[size_t(s) * p.heads + h]);
+// bf16 hi/lo split of 8 consecutive values of sequence row r, latent dims
+// [d, d + 8) (d a multiple of 8), into rows r (hi) and NB + r (lo) of the
+// swizzled B operand
+template <int NB>
+__device__ __forceinline__ void store_planes(uint8_t* bsm, int r, int d, const float* v) {
+  uint32_t ph[4], pl[4];
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-  if (lane == 0) red[warp] = mx;
-  __syncthreads();
-  if (tid == 0) {
-    float v = red[0];
-    for (int k = 1; k < nw; ++k) v = fmaxf(v, red[k]);
-    s_mx = v;
+  for (int e = 0; e < 4; ++e) {
+    const __nv_bfloat16 h0 = __float2bfloat16_rn(v[2 * e]), h1 = __float2bfloat16_rn(v[2 * e + 1]);
+    const __nv_bfloat16 l0 = __float2bfloat16_rn(v[2 * e] - __bfloat162float(h0));
+    const __nv_bfloat16 l1 = __float2bfloat16_rn(v[2 * e + 1] - __bfloat162float(h1));
+    ph[e] = uint32_t(__bfloat16_as_ushort(h0)) | (uint32_t(__bfloat16_as_ushort(h1)) << 16);
+    pl[e] = uint32_t(__bfloat16_as_ushort(l0)) | (uint32_t(__bfloat16_as_ushort(l1)) << 16);
   }
-  __syncthreads();
-  mx = s_mx;
-  float z = 0.f;
-  if (mx != -INFINITY)
-    for (int s = s0 + tid; s < s1; s += blockDim.x) z += expf(p.partial_lse[size_t(s) * p.heads + h] - mx);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
-  __syncthreads();
-  if (lane == 0) red[warp] = z;
-  __syncthreads();
+  // rows r and NB + r share r % 8, hence the 16-byte slot
+  const uint32_t off = (d >> 6) * UVCfg<NB>::kBBlock + r * 128 + ((((d >> 3) & 7) ^ (r & 7)) << 4);
+  *reinterpret_cast<uint4*>(bsm + off) = make_uint4(ph[0], ph[1], ph[2], ph[3]);
+  *reinterpret_cast<uint4*>(bsm + off + NB * 128) = make_uint4(pl[0], pl[1], pl[2], pl[3]);
+}
+
+template <int NB>
+__global__ void __launch_bounds__(kUVThreads, 1)
+    merge_uv_kernel(const __grid_constant__ CUtensorMap tmap_wuv, CombineUVParams p) {
+  using C = UVCfg<NB>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* w_full = reinterpret_cast<uint64_t*>(smem + C::kOffMisc);
+  uint64_t* mma_done = w_full + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc + 16);
+  int* abort_flag = reinterpret_cast<int*>(smem + C::kOffMisc + 20);
+  uint8_t* bsm = smem + C::kOffB;
+  float* xs = reinterpret_cast<float*>(smem + C::kOffX);
+  int* seg = reinterpret_cast<int*>(smem + C::kOffSeg);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int per_head = (p.batch + NB - 1) / NB;
+  const int h = blockIdx.x / per_head, b0 = (blockIdx.x % per_head) * NB, nb = min(NB, p.batch - b0);
   if (tid == 0) {
-    float v = 0.f;
-    for (int k = 0; k < nw; ++k) v += red[k];
-    s_z = v;
-    if (p.lse_out) p.lse_out[size_t(b) * p.heads + h] = mx != -INFINITY ? mx + logf(v) : -INFINITY;
+    mbar_init(w_full, 1);
+    mbar_init(mma_done, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    prefetch_tensormap(&tmap_wuv);
   }
+  if (warp == 0) {
+    tmem_alloc(tmem_slot, C::kTmemCols);
+    tmem_relinquish();
+  }
+  griddep_wait();
+  griddep_launch_dependents();
+  if (tid == 0) {
+    mbar_arrive_expect_tx(w_full, kUVWBytes);
+#pragma unroll
+    for (int kb = 0; kb < 8; ++kb) tma_load_2d(smem + kb * kUVWBlock, &tmap_wuv, 64 * kb, h * kVDim, w_full);
+  }
+  if (tid <= nb) seg[tid] = p.seg_base[b0 + tid];
   __syncthreads();
-  const float inv_z = mx != -INFINITY ? 1.f / s_z : 0.f;
-  float4 acc[4];
+
+  // ---- 1. merge.  wps warps per sequence (about kUVBatch segments each, as
+  // far as the tile's sequences still fit in one round), G = kUVWarps / wps
+  // sequences at a time
+  const int avg = (seg[nb] - seg[0] + nb - 1) / nb;
+  int g_min = 1;
+  while (g_min < kUVWarps && g_min < nb) g_min *= 2;
+  int wps = 1;
+  while (wps < kUVWarps / g_min && kUVBatch * wps < avg) wps *= 2;
+  const int G = kUVWarps / wps, wi = warp % wps;
+  for (int base = 0; base < nb; base += G) {
+    const int r = base + warp / wps;  // row of this warp's sequence in the tile
+    float acc[16];
 #pragma unroll
-  for (int q = 0; q < 4; ++q) acc[q] = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (mx != -INFINITY)
-    for (int s = s0 + warp; s < s1; s += nw) {
-      const float w = expf(p.partial_lse[size_t(s) * p.heads + h] - mx) * inv_z;
-      const float4* src = reinterpret_cast<const float4*>(p.partial_o + (size_t(s) * p.heads + h) * kLatent) + 4 * lane;
+    for (int i = 0; i < 16; ++i) acc[i] = 0.f;
+    if (r < nb) {
+      const int b = b0 + r, s0 = seg[r], n = seg[r + 1] - s0;
+      const float* lse = p.partial_lse + size_t(s0) * p.heads + h;
+      const float* po = p.partial_o + size_t(s0) * p.heads * kLatent + size_t(h) * kLatent + 16 * lane;
+      const size_t seg_stride = size_t(p.heads) * kLatent;
+      // the first batch of rows is requested together with the lse values
+      float4 v[kUVBatch][4];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const float4 v = src[q];
-        acc[q].x = fmaf(w, v.x, acc[q].x);
-        acc[q].y = fmaf(w, v.y, acc[q].y);
-        acc[q].z = fmaf(w, v.z, acc[q].z);
-        acc[q].w = fmaf(w, v.w, acc[q].w);
+      for (int u = 0; u < kUVBatch; ++u) {
+        const int i = wi + u * wps;
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          v[u][q] = i < n ? reinterpret_cast<const float4*>(po + i * seg_stride)[q] : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+      // max and sum of exp(lse - max) over the segments, kLseRegs x 32 lse
+      // values per pass (requested together); with at most that many
+      // segments, lane l keeps exp(lse_{32 j + l} - max) in e[j] for the weights
+      constexpr int kLseRegs = 4;
+      float mx = -INFINITY, z = 0.f, e[kLseRegs] = {};
+      for (int i0 = 0; i0 < n; i0 += 32 * kLseRegs) {
+        float l[kLseRegs];
+#pragma unroll
+        for (int j = 0; j < kLseRegs; ++j) {
+          const int i = i0 + 32 * j + lane;
+          l[j] = i < n ? lse[size_t(i) * p.heads] : -INFINITY;
+        }
+        float m2 = l[0];
+#pragma unroll
+        for (int j = 1; j < kLseRegs; ++j) m2 = fmaxf(m2, l[j]);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m2 = fmaxf(m2, __shfl_xor_sync(0xffffffffu, m2, o));
+        m2 = fmaxf(m2, mx);
+        if (m2 != -INFINITY) {
+          float zs = 0.f;
+#pragma unroll
+          for (int j = 0; j < kLseRegs; ++j) {
+            e[j] = expf(l[j] - m2);
+            zs += e[j];
+          }
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) zs += __shfl_xor_sync(0xffffffffu, zs, o);
+          z = (mx == -INFINITY ? 0.f : z * expf(mx - m2)) + zs;
+          mx = m2;
+        }
+      }
+      if (wi == 0 && lane == 0 && p.lse_out)
+        p.lse_out[size_t(b) * p.heads + h] = mx != -INFINITY ? mx + logf(z) : -INFINITY;
+      if (mx != -INFINITY) {
+        const float inv_z = 1.f / z;
+        // segments wi, wi + wps, ..., kUVBatch at a time
+        for (int k = wi;; ) {
+          float w[kUVBatch];
+#pragma unroll
+          for (int u = 0; u < kUVBatch; ++u) {
+            const int i = k + u * wps;
+            if (n <= 32 * kLseRegs) {
+              float ej = e[0];
+#pragma unroll
+              for (int j = 1; j < kLseRegs; ++j)
+                if ((i >> 5) == j) ej = e[j];
+              w[u] = __shfl_sync(0xffffffffu, ej, i & 31) * inv_z;
+            } else {
+              w[u] = i < n ? expf(lse[size_t(i) * p.heads] - mx) * inv_z : 0.f;
+            }
+            if (i >= n) w[u] = 0.f;
+          }
+#pragma unroll
+          for (int u = 0; u < kUVBatch; ++u)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              acc[4 * q] = fmaf(w[u], v[u][q].x, acc[4 * q]);
+              acc[4 * q + 1] = fmaf(w[u], v[u][q].y, acc[4 * q + 1]);
+              acc[4 * q + 2] = fmaf(w[u], v[u][q].z, acc[4 * q + 2]);
+              acc[4 * q + 3] = fmaf(w[u], v[u][q].w, acc[4 * q + 3]);
+            }
+          k += kUVBatch * wps;
+          if (k >= n) break;
+#pragma unroll
+          for (int u = 0; u < kUVBatch; ++u) {
+            const int i = k + u * wps;
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              v[u][q] = i < n ? reinterpret_cast<const float4*>(po + i * seg_stride)[q] : make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+        }
       }
     }
-  float* dst = p.o_lat + (size_t(b) * p.heads + h) * kLatent;
-  if (nw == 1) {
+    if (wps == 1) {  // lane l holds latent dims [16 l, 16 l + 16)
+      if (r < nb) {
+        store_planes<NB>(bsm, r, 16 * lane, acc);
+        store_planes<NB>(bsm, r, 16 * lane + 8, acc + 8);
+      }
+    } else {  // add the wps warps' sums in warp order
+      float4* mine = reinterpret_cast<float4*>(xs + warp * kLatent) + 4 * lane;
 #pragma unroll
-    for (int q = 0; q < 4; ++q) reinterpret_cast<float4*>(dst)[4 * lane + q] = acc[q];
-    return;
+      for (int q = 0; q < 4; ++q) mine[q] = make_float4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]);
+      __syncthreads();
+      if (wi == 0 && r < nb) {
+#pragma unroll 1
+        for (int k = 1; k < wps; ++k) {
+          const float4* other = reinterpret_cast<const float4*>(xs + (warp + k) * kLatent) + 4 * lane;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float4 x = other[q];
+            acc[4 * q] += x.x;
+            acc[4 * q + 1] += x.y;
+            acc[4 * q + 2] += x.z;
+            acc[4 * q + 3] += x.w;
+          }
+        }
+        store_planes<NB>(bsm, r, 16 * lane, acc);
+        store_planes<NB>(bsm, r, 16 * lane + 8, acc + 8);
+      }
+      __syncthreads();
+    }
   }
-  float4* mine = reinterpret_cast<float4*>(part_raw + warp * kLatent) + 4 * lane;
-#pragma unroll
-  for (int q = 0; q < 4; ++q) mine[q] = acc[q];
+  // rows past the batch: zeros (their output columns are discarded)
+  for (int i = tid; i < (NB - nb) * (kLatent / 8); i += kUVThreads) {
+    const float z8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    store_planes<NB>(bsm, nb + i / (kLatent / 8), 8 * (i % (kLatent / 8)), z8);
+  }
+  fence_proxy_async_smem();
+  tc_fence_before();
   __syncthreads();
-  for (int d = tid; d < kLatent; d += blockDim.x) {
-    float v = part_raw[d];
-    for (int k = 1; k < nw; ++k) v += part_raw[k * kLatent + d];
-    dst[d] = v;
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot, sbase = smem_u32(smem);
+
+  // ---- 2. D = W^UV_h [hi | lo]^T
+  bool ok = true;
+  if (tid == 0) {
+    ok = mbar_wait(w_full, 0, abort_flag, kUVWaitNs);
+    tc_fence_after();
+    if (ok) {
+      constexpr uint32_t idesc = idesc_f32acc(128, 2 * NB, false, false, false);
+      constexpr uint64_t kDesc = smem_desc(0, 16, 1024, kSwizzle128B);
+#pragma unroll
+      for (int kk = 0; kk < kLatent / 16; ++kk)
+        mma_bf16(tmem, kDesc | desc_addr(sbase + (kk >> 2) * kUVWBlock + (kk & 3) * 32),
+                 kDesc | desc_addr(sbase + C::kOffB + (kk >> 2) * C::kBBlock + (kk & 3) * 32), idesc, kk != 0);
+      mma_commit(mma_done);
+    } else {
+      *abort_flag = 1;
+    }
+  }
+  __syncthreads();
+  ok = *abort_flag == 0 && mbar_wait(mma_done, 0, abort_flag, kUVWaitNs);
+  tc_fence_after();
+  if (!ok && tid == 0) set_status(p.status, MLA_ERR_DEVICE_TIMEOUT);
+
+  // ---- 3. thread (warp, lane) of warps 0-3 holds output dim j = 32 warp + lane
+  if (ok && warp < 4) {
+    const int j = 32 * warp + lane;
+    const uint32_t row = uint32_t(32 * warp) << 16;
+#pragma unroll
+    for (int c = 0; c < NB; c += 8) {
+      float vh[8], vl[8];
+      tmem_ld8(tmem + row + c, vh);
+      tmem_ld8(tmem + row + NB + c, vl);
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        if (c + i < nb) p.out[(size_t(b0 + c + i) * p.heads + h) * kVDim + j] = __float2bfloat16_rn(vh[i] + vl[i]);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (!ok && tid == 0) {  // let a copy still in flight land before the CTA's shared memory is released
+    const uint64_t t0 = global_timer_ns();
+    while (global_timer_ns() - t0 < 20000) {
+    }
+  }
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
   }
 }
 
-// grid (H, ceil(B / 8), 128 / 64), block 256: out[b][h][j] = W^UV_h[j] . o_lat[b][h]
-// for 8 sequences and output rows [64 z, 64 z + 64).
-__global__ void __launch_bounds__(256) combine_uv_kernel(CombineUVParams p) {
-  __shared__ __align__(16) float o_lat[kCombB][kLatent];
-  const int h = blockIdx.x, b0 = blockIdx.y * kCombB, j0 = blockIdx.z * kCombJ;
-  const int nb = min(kCombB, p.batch - b0);
-  const int tid = threadIdx.x;
-  for (int idx = tid; idx < kCombB * kLatent / 4; idx += blockDim.x) {
-    const int i = idx / (kLatent / 4), q = idx % (kLatent / 4);
-    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (i < nb) v = reinterpret_cast<const float4*>(p.o_lat + (size_t(b0 + i) * p.heads + h) * kLatent)[q];
-    reinterpret_cast<float4*>(o_lat[i])[q] = v;
+template <int NB>
+cudaError_t launch_merge_uv(const CombineUVParams& p, cudaStream_t stream) {
+  using C = UVCfg<NB>;
+  CUtensorMap mw;
+  if (!dc::make_map_2d(&mw, p.W_UV, 2, kLatent, uint64_t(p.heads) * kVDim, 64, kVDim, CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
+  static bool attr[128] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 128 || !attr[dev]) {
+    const cudaError_t e =
+        cudaFuncSetAttribute(merge_uv_kernel<NB>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(C::kSmem));
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 128) attr[dev] = true;
   }
-  __syncthreads();
-
-  // out[b][h][j] = sum_m W_UV[h][j][m] * o_lat[b][m]: warp w takes rows j0 + w, j0 + w + 8, ...;
-  // lane l covers dims 128 r + 4 l + (0..3), r < 4 (coalesced rows, conflict-free shared reads)
-  const int warp = tid >> 5, lane = tid & 31;
-  for (int jj = warp; jj < kCombJ; jj += 8) {
-    const int j = j0 + jj;
-    const uint2* wrow = reinterpret_cast<const uint2*>(p.W_UV + (size_t(h) * kVDim + j) * kLatent);
-    float wf[16];
-#pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      const uint2 wv = wrow[32 * r + lane];
-      const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wv.x));
-      const float2 y = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wv.y));
-      wf[4 * r] = x.x;
-      wf[4 * r + 1] = x.y;
-      wf[4 * r + 2] = y.x;
-      wf[4 * r + 3] = y.y;
-    }
-    float acc[kCombB];
-#pragma unroll
-    for (int i = 0; i < kCombB; ++i) {
-      float a = 0.f;
-#pragma unroll
-      for (int r = 0; r < 4; ++r) {
-        const float4 o = reinterpret_cast<const float4*>(o_lat[i])[32 * r + lane];
-        a = fmaf(wf[4 * r], o.x, fmaf(wf[4 * r + 1], o.y, fmaf(wf[4 * r + 2], o.z, fmaf(wf[4 * r + 3], o.w, a))));
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
-      acc[i] = a;
-    }
-    float mine = acc[0];
-#pragma unroll
-    for (int i = 1; i < kCombB; ++i)
-      if (lane == i) mine = acc[i];
-    if (lane < nb) p.out[(size_t(b0 + lane) * p.heads + h) * kVDim + j] = __float2bfloat16_rn(mine);
-  }
+  const int grid = p.heads * ((p.batch + NB - 1) / NB);
+  return launch_pdl(merge_uv_kernel<NB>, dim3(grid), dim3(kUVThreads), C::kSmem, stream, 1, mw, p);
 }
 
 cudaError_t launch_combine_uv(const CombineUVParams& p, cudaStream_t stream) {
-  // about two segments per warp
-  int nw = 1;
-  while (nw < kMergeWarps && 2 * nw * p.batch < p.max_segments) nw *= 2;
-  merge_kernel<<<dim3(p.heads, p.batch), nw * 32, nw > 1 ? nw * kLatent * sizeof(float) : 0, stream>>>(p);
-  dim3 grid(p.heads, (p.batch + kCombB - 1) / kCombB, kVDim / kCombJ);
-  combine_uv_kernel<<<grid, 256, 0, stream>>>(p);
-  return cudaGetLastError();
+  // the largest tile that still gives every SM a CTA; 8 sequences when none does
+  if (p.heads * ((p.batch + 31) / 32) >= p.sm_count) return launch_merge_uv<32>(p, stream);
+  if (p.heads * ((p.batch + 15) / 16) >= p.sm_count) return launch_merge_uv<16>(p, stream);
+  return launch_merge_uv<8>(p, stream);
 }
 
 // ----- standalone combine (mla_combine) ---------------------------------------

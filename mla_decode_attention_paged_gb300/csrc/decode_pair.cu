@@ -1,5 +1,6 @@
 // decode_pair.cu -- split-KV MLA decode attention for bf16 caches on CTA
-// pairs (thread-block clusters of two), tcgen05 tensor cores fed by TMA.
+// clusters (thread-block clusters of two or four), tcgen05 tensor cores fed
+// by TMA.
 //
 // What it computes ("The Weight Absorption Trick"; "Seven Ways LLMs Handle
 // Attention", section 5; "Flash-Decoding and FlashInfer"): for one head group
@@ -10,38 +11,40 @@
 //     o_lat[h] = sum_t softmax(s[., h])_t * c_t[0:512]
 // and emits o_lat (normalised within the range) with the range's lse.
 //
-// Why pairs.  Both products read the same cached tile (the latent part is K
-// of QK^T and V of PV), so a tile must stay in shared memory from its QK^T
+// Why clusters.  Both products read the same cached tile (the latent part is
+// K of QK^T and V of PV), so a tile must stay in shared memory from its QK^T
 // until its PV, across the softmax in between.  A 128-token tile is 147 KB;
 // one SM holds about 1.3 of them, which serialises load -> QK^T -> softmax ->
-// PV.  Here the two CTAs of a cluster (two SMs) split every tile by columns:
-// CTA r holds latent columns [256 r, 256 r + 256) and RoPE columns
-// [512 + 32 r, 512 + 32 r + 32): 72 KB per tile, about 2.6 tiles per SM.
+// PV.  Here the NC CTAs of a cluster (NC SMs) split every tile by columns:
+// CTA r holds latent columns [512 r / NC, 512 (r + 1) / NC) and RoPE columns
+// [512 + 64 r / NC, 512 + 64 (r + 1) / NC): 147 / NC KB per tile, so each SM
+// keeps several tiles in flight (2 with pairs, 4 with clusters of four).
 //   * QK^T: each CTA forms the partial scores over its columns, S_r^T
-//     [128 tok x HC] = C_r [128 x 288] * Q_r^T, and sends them to its peer
-//     through distributed shared memory (8 KB for 16 heads);
-//   * both CTAs add the two partials (in the same order of operands, so
-//     both get the same bits), run the same softmax and hold the same P^T;
-//   * PV: each CTA accumulates its own 256 latent columns of O^T.
+//     [128 tok x HC] = C_r [128 x 576 / NC] * Q_r^T, and sends them to the
+//     other CTAs through distributed shared memory (8 KB each for 16 heads);
+//   * every CTA adds the NC partials in rank order (so all get the same
+//     bits), runs the same softmax and holds the same P^T;
+//   * PV: each CTA accumulates its own 512 / NC latent columns of O^T.
 // Every page is read from HBM once for all heads of the group.
 //
 // Orientation as in the single-CTA kernel: the 128 tokens of a tile are the
 // MMA's M extent and the heads its N extent:
-//     S_r^T [128 x HC]    = C_r [128 x 288] * Q_r^T          (A K-major)
-//     O_r^T [256 x HC]   += C_r^T [256 x 128] * P^T          (A MN-major)
+//     S_r^T [128 x HC]        = C_r [128 x 576 / NC] * Q_r^T       (A K-major)
+//     O_r^T [512 / NC x HC]  += C_r^T [512 / NC x 128] * P^T       (A MN-major)
 //
 // Warp roles (256 threads per CTA):
-//   warp 0     TMA producer: Q of each segment and each tile's first latent
-//              pair (128 columns)
+//   warp 0     TMA producer: Q of each segment and the first half of each
+//              tile's latent boxes
 //   warp 1     TMEM allocation; lane 0 issues the QK^T MMAs
 //   warp 2     PV: lane 0 issues the MMAs; the warp clears the ragged tail
 //              rows of a sequence's last tile first
-//   warp 3     TMA producer: each tile's second latent pair and RoPE half
+//   warp 3     TMA producer: the second half of the latent boxes and the
+//              RoPE columns
 //   warps 4-7  exchange of partial scores, softmax (one thread per token
 //              row), epilogue
 // Every wait is bounded: on timeout the CTA records MLA_ERR_DEVICE_TIMEOUT,
-// drains, frees its tensor memory and returns (its peer then times out on the
-// exchange and does the same).
+// drains, frees its tensor memory and returns (the other CTAs of its cluster
+// then time out on the exchange and do the same).
 #include "blackwell_ptx.cuh"
 #include "decode_common.cuh"
 #include "params.cuh"
@@ -55,36 +58,52 @@ using namespace dc;
 constexpr int kPairThreads = 256;
 constexpr uint32_t kBoxBytes = 16384;           // [128 tokens x 64 columns] bf16, 128-byte swizzle
 constexpr uint32_t kPairBytes = 2 * kBoxBytes;  // 128 latent columns: one O^T chunk
-constexpr uint32_t kRopeBytes = 8192;           // [128 tokens x 32 columns] bf16, 64-byte swizzle
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 constexpr float kRescaleThreshold = 8.f;          // log2 units
 constexpr bool kPrefetchNext = true;              // L2 prefetch of the next tile's boxes
+constexpr int kPairClusterHC16 = 2;               // CTAs per cluster for 16-head groups
+constexpr int kMaxSlots = 6;                      // barrier array size of each ring
 
-template <int HC>
+// HC heads per cluster, NC CTAs per cluster (2 or 4) splitting each tile's
+// columns: CTA r holds latent columns [r 512/NC, (r + 1) 512/NC) -- kChunks
+// chunks of 128 -- and RoPE columns [512 + r 64/NC, 512 + (r + 1) 64/NC).
+template <int HC, int NC>
 struct PairCfg {
-  static constexpr int kNumPair = 4;  // latent pair slots (two per tile; an even count keeps both producers in step)
-  static constexpr int kNumRope = 3;                 // RoPE-half slots (one per tile)
-  static constexpr uint32_t kQBytes = 4 * HC * 128 + HC * 64;  // four latent boxes + RoPE half
-  static constexpr uint32_t kPBytes = kTile * HC * 2;          // P^T, bf16
-  static constexpr uint32_t kXBytes = kTile * HC * 4;          // the peer's partial S^T, fp32
+  static_assert(NC == 2 || NC == 4, "clusters of two or four CTAs");
+  static constexpr int kChunks = 4 / NC;            // 128-column latent chunks per CTA and tile
+  static constexpr int kRopeCols = 64 / NC;         // RoPE columns per CTA (32: 64-byte rows, 16: 32-byte rows)
+  static constexpr uint32_t kRopeBytes = kTile * kRopeCols * 2;
+  static constexpr uint32_t kRopeSbo = 8 * kRopeCols * 2;  // 8-row swizzle atom
+  static constexpr uint32_t kRopeSwizzle = NC == 2 ? kSwizzle64B : kSwizzle32B;
+  static constexpr int kNumPair = 4;                // chunk slots: 4 / kChunks tiles (with two chunks per
+                                                    // tile an even count keeps both producers in step)
+  static constexpr int kNumRope = NC == 2 ? 3 : 4;  // RoPE slots (one per tile)
+  // the two producers split a tile's latent boxes: one chunk each, or with
+  // a single chunk one 64-column box each (both then arm the slot's barrier)
+  static constexpr int kBoxesPerProducer = kChunks == 2 ? 2 : 1;
+  static constexpr int kPairArrivals = kChunks == 2 ? 1 : 2;
+  static constexpr uint32_t kQBytes = kChunks * 2 * HC * 128 + HC * kRopeCols * 2;
+  static constexpr uint32_t kPBytes = kTile * HC * 2;  // P^T, bf16
+  static constexpr uint32_t kXBytes = kTile * HC * 4;  // one other CTA's partial S^T, fp32
   static constexpr uint32_t kOffPair = 0;
   static constexpr uint32_t kOffRope = kOffPair + kNumPair * kPairBytes;
-  static constexpr uint32_t kOffQ = kOffRope + kNumRope * kRopeBytes;
-  static constexpr uint32_t kOffQRope = kOffQ + 4 * HC * 128;
+  static constexpr uint32_t kOffQ = kOffRope + ((kNumRope * kRopeBytes + 1023) & ~1023u);
+  static constexpr uint32_t kOffQRope = kOffQ + kChunks * 2 * HC * 128;
   static constexpr uint32_t kOffP = kOffQ + ((kQBytes + 1023) & ~1023u);
-  static constexpr uint32_t kOffX = kOffP + 2 * kPBytes;
-  static constexpr uint32_t kOffMisc = kOffX + 2 * kXBytes;
+  static constexpr uint32_t kOffX = kOffP + 2 * kPBytes;  // [NC - 1 senders][2 buffers]
+  static constexpr uint32_t kOffMisc = kOffX + (NC - 1) * 2 * kXBytes;
   static constexpr uint32_t kMiscBytes = 2048;
   static constexpr uint32_t kSmem = kOffMisc + kMiscBytes + 1024;  // +1024: base alignment slack
-  static constexpr uint32_t kTmemCols = HC == 16 ? 64 : 128;       // S^T x2 + O^T x2 = 4 * HC
   static constexpr uint32_t kColS = 0;                             // + buf * HC
   static constexpr uint32_t kColO = 2 * HC;                        // + c * HC
+  static constexpr uint32_t kTmemCols = (2 + kChunks) * HC <= 64 ? 64 : ((2 + kChunks) * HC <= 128 ? 128 : 256);
   static_assert(kSmem <= 232448, "dynamic shared memory of one CTA");
-  static_assert(kOffQ % 1024 == 0 && kOffQRope % 512 == 0, "swizzle atoms");
+  static_assert(kNumPair <= kMaxSlots && kNumRope <= kMaxSlots, "barrier arrays");
+  static_assert(kOffQ % 1024 == 0 && kOffQRope % 256 == 0, "swizzle atoms");
 };
 
 struct PairBarriers {
-  uint64_t full_pair[5], empty_pair[5], full_rope[3], empty_rope[3];
+  uint64_t full_pair[kMaxSlots], empty_pair[kMaxSlots], full_rope[kMaxSlots], empty_rope[kMaxSlots];
   uint64_t q_full, q_empty, s_full[2], x_full[2], p_full[2], pv_done[2], o_full, o_free, drain[2];
   uint32_t tmem_base;
   int abort;
@@ -104,24 +123,24 @@ __device__ __forceinline__ void fail(PairBarriers* B, int* status) {
   set_status(status, MLA_ERR_DEVICE_TIMEOUT);
 }
 
-template <int HC>
+template <int HC, int NC>
 __global__ void __launch_bounds__(kPairThreads, 1)
     decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_latent, const __grid_constant__ CUtensorMap tmap_rope,
                        const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_qrope,
                        DecodeParams p) {
-  using C = PairCfg<HC>;
+  using C = PairCfg<HC, NC>;
   extern __shared__ uint8_t smem_raw[];
-  // the same offset in both CTAs: the peer's exchange buffer and barriers are found by mapa
+  // the same offset in every CTA: the others' exchange buffers and barriers are found by mapa
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   PairBarriers* B = reinterpret_cast<PairBarriers*>(smem + C::kOffMisc);
   float* red = reinterpret_cast<float*>(smem + C::kOffMisc + 512);  // [2][HC][4] maxima, [HC][4] sums
   const uint32_t sbase = smem_u32(smem);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t rank = cluster_ctarank(), peer = rank ^ 1;
+  const uint32_t rank = cluster_ctarank();
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::kNumPair; ++i) {
-      mbar_init(&B->full_pair[i], 1);
+      mbar_init(&B->full_pair[i], C::kPairArrivals);
       mbar_init(&B->empty_pair[i], 1);
     }
     for (int i = 0; i < C::kNumRope; ++i) {
@@ -132,7 +151,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     mbar_init(&B->q_empty, 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&B->s_full[i], 1);
-      mbar_init(&B->x_full[i], 1);  // armed by one local thread; the peer's bytes complete it
+      mbar_init(&B->x_full[i], 1);  // armed by one local thread; the other CTAs' bytes complete it
       mbar_init(&B->p_full[i], 128);
       mbar_init(&B->pv_done[i], 1);
       mbar_init(&B->drain[i], 1);
@@ -151,27 +170,29 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     tmem_relinquish();
   }
   tc_fence_before();
-  cluster_sync();  // both CTAs' barriers exist before either sends to the other
+  cluster_sync();  // every CTA's barriers exist before any sends to another
   tc_fence_after();
   const uint32_t tmem = B->tmem_base;
+  griddep_wait();  // the plan and Q come from the kernel before
+  griddep_launch_dependents();
 
-  const int G = p.num_groups, pair = blockIdx.x >> 1, g = pair % G, cp = pair / G, Cp = (gridDim.x >> 1) / G;
+  const int G = p.num_groups, clus = blockIdx.x / NC, g = clus % G, cp = clus / G, Cp = (gridDim.x / NC) / G;
   const long long S = p.status[1];  // effective split count from the plan
   const long long pa = (cp * S) / Cp, pb = ((cp + 1) * S) / Cp;
   const volatile int* abort_flag = &B->abort;
   const int P = p.page_size;
-  const int lat0 = 256 * int(rank), rope0 = kLatent + 32 * int(rank);  // this CTA's columns
+  const int lat0 = (kLatent / NC) * int(rank), rope0 = kLatent + C::kRopeCols * int(rank);  // this CTA's columns
 
   if ((warp == 0 || warp == 3) && lane == 0) {
     // ------------------------------------------------------------ producers
     // One thread cannot issue TMA copies fast enough for an SM's share of
     // HBM (about 0.15-0.2 us per 8 KB box), so two warps share the work:
-    // warp 0 loads Q and the first latent pair of every tile, warp 3 the
-    // second pair and the RoPE half.  Both fill the same pair ring.
+    // warp 0 loads Q and the first half of every tile's latent boxes, warp 3
+    // the second half and the RoPE columns.
     const int role = warp == 0 ? 0 : 1;
     TileWalker walk;
     walk.init(p.tile_start, p.seg_base, p.len, p.batch, int(S), pa, pb);
-    const uint32_t page_bytes = uint32_t(P) * 128, rope_page_bytes = uint32_t(P) * 64;
+    const uint32_t page_bytes = uint32_t(P) * 128, rope_page_bytes = uint32_t(P) * C::kRopeCols * 2;
     uint32_t pair_it = 0, rope_it = 0, seg = 0;
     TileInfo t, tn;
     // page ids two tiles ahead: tile k + 1's are in registers (and arrived)
@@ -195,7 +216,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
         if (seg > 0 && !(ok = mbar_wait(&B->q_empty, (seg - 1) & 1, abort_flag, kWaitLimitNs))) break;
         mbar_arrive_expect_tx(&B->q_full, C::kQBytes);
         const int qrow = t.b * p.heads + g * HC;
-        for (int j = 0; j < 4; ++j)
+        for (int j = 0; j < 2 * C::kChunks; ++j)
           tma_load_2d(smem + C::kOffQ + j * HC * 128, &tmap_q, lat0 + 64 * j, qrow, &B->q_full);
         tma_load_2d(smem + C::kOffQRope, &tmap_qrope, rope0, qrow, &B->q_full);
         ++seg;
@@ -212,30 +233,33 @@ __global__ void __launch_bounds__(kPairThreads, 1)
         next_pages.rows(p, nrows);
 #pragma unroll 1
         for (int i = 0; i < next_pages.npg; ++i) {
-          tma_prefetch_2d(&tmap_latent, lat0 + 128 * role, nrows[i]);
-          tma_prefetch_2d(&tmap_latent, lat0 + 128 * role + 64, nrows[i]);
+          for (int b = 0; b < C::kBoxesPerProducer; ++b)
+            tma_prefetch_2d(&tmap_latent, lat0 + 64 * (C::kBoxesPerProducer * role + b), nrows[i]);
           if (role == 1) tma_prefetch_2d(&tmap_rope, rope0, nrows[i]);
         }
       }
       {
-        const int c = role;
+        // boxes [kBoxesPerProducer * role, + kBoxesPerProducer) of this CTA's
+        // 64-column boxes; box j is box j % 2 of chunk j / 2
+        const int c = C::kChunks == 2 ? role : 0, b0 = C::kChunks == 2 ? 0 : role;
         const uint32_t it = pair_it + c;
-        pair_it += 2;
         const uint32_t slot = it % C::kNumPair;
         if (!(ok = mbar_wait(&B->empty_pair[slot], ((it / C::kNumPair) & 1) ^ 1, abort_flag, kWaitLimitNs))) break;
         uint8_t* dst = smem + C::kOffPair + slot * kPairBytes;
-        mbar_arrive_expect_tx(&B->full_pair[slot], 2 * npg * page_bytes + (p.inject_wait_timeout && it == 0 ? 16 : 0));
+        mbar_arrive_expect_tx(&B->full_pair[slot], C::kBoxesPerProducer * npg * page_bytes +
+                                                       (p.inject_wait_timeout && it == 0 ? 16 : 0));
 #pragma unroll 1
-        for (int i = 0; i < npg; ++i) {
-          tma_load_2d(dst + i * page_bytes, &tmap_latent, lat0 + 128 * c, rows[i], &B->full_pair[slot]);
-          tma_load_2d(dst + kBoxBytes + i * page_bytes, &tmap_latent, lat0 + 128 * c + 64, rows[i], &B->full_pair[slot]);
-        }
+        for (int i = 0; i < npg; ++i)
+          for (int b = b0; b < b0 + C::kBoxesPerProducer; ++b)
+            tma_load_2d(dst + b * kBoxBytes + i * page_bytes, &tmap_latent, lat0 + 128 * c + 64 * b, rows[i],
+                        &B->full_pair[slot]);
       }
+      pair_it += C::kChunks;
       if (role == 0) continue;
       const uint32_t slot = rope_it % C::kNumRope;
       if (!(ok = mbar_wait(&B->empty_rope[slot], ((rope_it / C::kNumRope) & 1) ^ 1, abort_flag, kWaitLimitNs)))
         break;
-      uint8_t* dst = smem + C::kOffRope + slot * kRopeBytes;
+      uint8_t* dst = smem + C::kOffRope + slot * C::kRopeBytes;
       mbar_arrive_expect_tx(&B->full_rope[slot], npg * rope_page_bytes);
 #pragma unroll 1
       for (int i = 0; i < npg; ++i) tma_load_2d(dst + i * rope_page_bytes, &tmap_rope, rope0, rows[i], &B->full_rope[slot]);
@@ -244,14 +268,14 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     if (!ok) fail(B, p.status);
   } else if (warp == 1 && lane == 0) {
     // ------------------------------------------------------------ QK issuer
-    // S_r^T[k & 1] = C_r * Q_r^T: two latent pairs (16 MMAs) and the RoPE half
-    // (2 MMAs).  Before overwriting S^T[k & 1] it waits for the softmax of
+    // S_r^T[k & 1] = C_r * Q_r^T: this CTA's latent chunks (8 MMAs each) and
+    // its RoPE columns (one MMA per 16).  Before overwriting S^T[k & 1] it waits for the softmax of
     // tile k - 2 (which read it) to finish.
     TileWalker walk;
     walk.init(p.tile_start, p.seg_base, p.len, p.batch, int(S), pa, pb);
     constexpr uint32_t id_qk = idesc_f32acc(128, HC, false, false, false);
     constexpr uint64_t kDescK = smem_desc(0, 16, 1024, kSwizzle128B);   // K-major, 128-byte swizzle
-    constexpr uint64_t kDescK64 = smem_desc(0, 16, 512, kSwizzle64B);   // K-major, 64-byte swizzle
+    constexpr uint64_t kDescRope = smem_desc(0, 16, C::kRopeSbo, C::kRopeSwizzle);  // K-major, narrow rows
     uint32_t k = 0, seg = 0, pair_it = 0;
     TileInfo t;
     bool ok = true;
@@ -259,7 +283,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
       if (k >= 2 && !(ok = mbar_wait(&B->p_full[k & 1], ((k - 2) >> 1) & 1, abort_flag, kWaitLimitNs))) break;
       if (t.first && !(ok = mbar_wait(&B->q_full, seg & 1, abort_flag, kWaitLimitNs))) break;
       const uint32_t d_s = tmem + C::kColS + (k & 1) * HC;
-      for (int c = 0; c < 2; ++c, ++pair_it) {
+      for (int c = 0; c < C::kChunks; ++c, ++pair_it) {
         const uint32_t slot = pair_it % C::kNumPair;
         if (!(ok = mbar_wait(&B->full_pair[slot], (pair_it / C::kNumPair) & 1, abort_flag, kWaitLimitNs))) break;
         tc_fence_after();
@@ -276,10 +300,10 @@ __global__ void __launch_bounds__(kPairThreads, 1)
       if (!(ok = mbar_wait(&B->full_rope[rslot], (k / C::kNumRope) & 1, abort_flag, kWaitLimitNs))) break;
       tc_fence_after();
       {
-        const uint64_t a0 = kDescK64 | desc_addr(sbase + C::kOffRope + rslot * kRopeBytes);
-        const uint64_t b0 = kDescK64 | desc_addr(sbase + C::kOffQRope);
-        mma_bf16(d_s, a0, b0, id_qk, 1);
-        mma_bf16(d_s, a0 + 2, b0 + 2, id_qk, 1);
+        const uint64_t a0 = kDescRope | desc_addr(sbase + C::kOffRope + rslot * C::kRopeBytes);
+        const uint64_t b0 = kDescRope | desc_addr(sbase + C::kOffQRope);
+#pragma unroll
+        for (int kk = 0; kk < C::kRopeCols / 16; ++kk) mma_bf16(d_s, a0 + 2 * kk, b0 + 2 * kk, id_qk, 1);
       }
       mma_commit(&B->s_full[k & 1]);
       mma_commit(&B->empty_rope[rslot]);
@@ -314,7 +338,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
       const int nk = (t.valid + 15) >> 4;
       const int tail_rows = 16 * nk - t.valid;  // rows the last k-step reads past the sequence's end
       const uint64_t bd = kDescP | desc_addr(sbase + C::kOffP + (k & 1) * C::kPBytes);
-      for (int c = 0; c < 2; ++c, ++pair_it) {
+      for (int c = 0; c < C::kChunks; ++c, ++pair_it) {
         const uint32_t slot = pair_it % C::kNumPair;
         if (tail_rows) {
           // they meet zero weights in P^T but must be finite: clear them (rows
@@ -355,10 +379,9 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     // ------------------------------------------------------------ exchange / softmax / epilogue
     const int q4 = warp - 4, st = threadIdx.x - 128;  // st = token row of S^T = TMEM lane
     const uint32_t lane_off = uint32_t(q4 * 32) << 16;
-    // this thread's row of the peer's exchange buffer; 16-byte chunks rotated by row to spread banks
-    constexpr int kChunks = HC / 4;
+    // this thread's row of an exchange buffer; 16-byte pieces rotated by row to spread banks
+    constexpr int kV4 = HC / 4;
     const uint32_t x_local = sbase + C::kOffX + st * HC * 4;
-    const uint32_t x_remote = mapa_shared(x_local, peer);
     TileWalker walk;
     walk.init(p.tile_start, p.seg_base, p.len, p.batch, int(S), pa, pb);
     float m_run[HC], l_run[HC];
@@ -380,27 +403,42 @@ __global__ void __launch_bounds__(kPairThreads, 1)
 #pragma unroll
           for (int i = 0; i < 16; ++i) x[h0 + i] = v[i];
         }
-        // partial scores to the peer; the peer's partial scores from it
-        const uint32_t rbar = mapa_shared(smem_u32(&B->x_full[buf]), peer);
+        // partial scores to every other CTA of the cluster: receiver rr keeps
+        // sender s's in its buffer slot (s - rr - 1) mod NC
 #pragma unroll
-        for (int v = 0; v < kChunks; ++v) {
-          const uint32_t off = buf * C::kXBytes + ((v ^ (st % kChunks)) * 16);
-          st_async_v4(x_remote + off, x[4 * v], x[4 * v + 1], x[4 * v + 2], x[4 * v + 3], rbar);
+        for (int j = 0; j < NC - 1; ++j) {
+          const uint32_t rr = (rank + 1 + j) % NC;
+          const uint32_t rbar = mapa_shared(smem_u32(&B->x_full[buf]), rr);
+          const uint32_t xr = mapa_shared(x_local + (buf * (NC - 1) + (NC - 2 - j)) * C::kXBytes, rr);
+#pragma unroll
+          for (int v = 0; v < kV4; ++v)
+            st_async_v4(xr + (v ^ (st % kV4)) * 16, x[4 * v], x[4 * v + 1], x[4 * v + 2], x[4 * v + 3], rbar);
         }
-        if (st == 0) mbar_arrive_expect_tx(&B->x_full[buf], C::kXBytes);
+        if (st == 0) mbar_arrive_expect_tx(&B->x_full[buf], (NC - 1) * C::kXBytes);
         ok = mbar_wait_cluster(&B->x_full[buf], (tile_i >> 1) & 1, abort_flag, kWaitLimitNs);
         if (ok) {
-          const float* xr = reinterpret_cast<const float*>(smem + C::kOffX + buf * C::kXBytes + st * HC * 4);
+          // S = ((S_0 + S_1) + S_2) + ... in rank order, so that every CTA
+          // of the cluster gets the same bits
 #pragma unroll
-          for (int v = 0; v < kChunks; ++v) {
-            const float4 y = *reinterpret_cast<const float4*>(xr + 4 * (v ^ (st % kChunks)));
-            // rank 0 adds (own + peer) = (S_0 + S_1), rank 1 adds (S_0 + S_1) too
-            if (rank == 0) {
-              x[4 * v] += y.x; x[4 * v + 1] += y.y; x[4 * v + 2] += y.z; x[4 * v + 3] += y.w;
-            } else {
-              x[4 * v] = y.x + x[4 * v]; x[4 * v + 1] = y.y + x[4 * v + 1];
-              x[4 * v + 2] = y.z + x[4 * v + 2]; x[4 * v + 3] = y.w + x[4 * v + 3];
+          for (int v = 0; v < kV4; ++v) {
+            float4 tot = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int s = 0; s < NC; ++s) {
+              float4 y;
+              if (s == int(rank)) {
+                y = make_float4(x[4 * v], x[4 * v + 1], x[4 * v + 2], x[4 * v + 3]);
+              } else {
+                const int slot = (s - int(rank) - 1 + NC) % NC;
+                y = *reinterpret_cast<const float4*>(smem + C::kOffX + (buf * (NC - 1) + slot) * C::kXBytes +
+                                                     st * HC * 4 + (v ^ (st % kV4)) * 16);
+              }
+              if (s == 0) {
+                tot = y;
+              } else {
+                tot.x += y.x; tot.y += y.y; tot.z += y.z; tot.w += y.w;
+              }
             }
+            x[4 * v] = tot.x; x[4 * v + 1] = tot.y; x[4 * v + 2] = tot.z; x[4 * v + 3] = tot.w;
           }
         }
       }
@@ -452,7 +490,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
         tc_fence_after();
         if (bar_any(!ok3)) break;
 #pragma unroll
-        for (int c = 0; c < 2; ++c)
+        for (int c = 0; c < C::kChunks; ++c)
 #pragma unroll
           for (int h0 = 0; h0 < HC; h0 += 16) {
             float v[16];
@@ -508,7 +546,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
         }
         float* dst = p.partial_o + (size_t(t.seg) * p.heads + g * HC) * kLatent + lat0;
 #pragma unroll
-        for (int c = 0; c < 2; ++c)
+        for (int c = 0; c < C::kChunks; ++c)
 #pragma unroll
           for (int h0 = 0; h0 < HC; h0 += 16) {
             float v[16];
@@ -541,74 +579,71 @@ __global__ void __launch_bounds__(kPairThreads, 1)
   }
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem, C::kTmemCols);
-  cluster_sync();  // the peer may still be sending into this CTA's shared memory until here
+  cluster_sync();  // other CTAs may still be sending into this CTA's shared memory until here
 }
 
-template <int HC>
-cudaError_t launch_pair(const DecodeParams& p, int pairs_per_group, cudaStream_t stream) {
+template <int HC, int NC>
+cudaError_t launch_pair(const DecodeParams& p, int clusters_per_group, cudaStream_t stream) {
+  using C = PairCfg<HC, NC>;
+  constexpr CUtensorMapSwizzle kRopeSw = NC == 2 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B;
   CUtensorMap ml, mr, mq, mqr;
   const uint64_t rows = uint64_t(p.num_pages) * p.page_size, qrows = uint64_t(p.batch) * p.heads;
   if (!make_map_2d(&ml, p.cache, 2, kRow, rows, 64, p.page_size, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_map_2d(&mr, p.cache, 2, kRow, rows, 32, p.page_size, CU_TENSOR_MAP_SWIZZLE_64B) ||
+      !make_map_2d(&mr, p.cache, 2, kRow, rows, C::kRopeCols, p.page_size, kRopeSw) ||
       !make_map_2d(&mq, p.q_full, 2, kRow, qrows, 64, HC, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_map_2d(&mqr, p.q_full, 2, kRow, qrows, 32, HC, CU_TENSOR_MAP_SWIZZLE_64B))
+      !make_map_2d(&mqr, p.q_full, 2, kRow, qrows, C::kRopeCols, HC, kRopeSw))
     return cudaErrorInvalidValue;
   static bool attr[128] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 128 || !attr[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(decode_pair_kernel<HC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         int(PairCfg<HC>::kSmem));
+    cudaError_t e = cudaFuncSetAttribute(decode_pair_kernel<HC, NC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         int(C::kSmem));
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 128) attr[dev] = true;
   }
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(2 * pairs_per_group * p.num_groups);
-  cfg.blockDim = dim3(kPairThreads);
-  cfg.dynamicSmemBytes = PairCfg<HC>::kSmem;
-  cfg.stream = stream;
-  cudaLaunchAttribute at[1];
-  at[0].id = cudaLaunchAttributeClusterDimension;
-  at[0].val.clusterDim.x = 2;
-  at[0].val.clusterDim.y = 1;
-  at[0].val.clusterDim.z = 1;
-  cfg.attrs = at;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_pair_kernel<HC>, ml, mr, mq, mqr, p);
+  return launch_pdl(decode_pair_kernel<HC, NC>, dim3(NC * clusters_per_group * p.num_groups), dim3(kPairThreads),
+                    C::kSmem, stream, NC, ml, mr, mq, mqr, p);
 }
 
-template <int HC>
-int max_pairs() {  // clusters of two that can be resident at once on this device
+template <int HC, int NC>
+int max_clusters() {  // clusters of NC that can be resident at once on this device
   static int cached[128] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 128 && cached[dev] > 0) return cached[dev];
-  if (cudaFuncSetAttribute(decode_pair_kernel<HC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           int(PairCfg<HC>::kSmem)) != cudaSuccess)
+  if (cudaFuncSetAttribute(decode_pair_kernel<HC, NC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           int(PairCfg<HC, NC>::kSmem)) != cudaSuccess)
     return 0;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(2);
+  cfg.gridDim = dim3(NC);
   cfg.blockDim = dim3(kPairThreads);
-  cfg.dynamicSmemBytes = PairCfg<HC>::kSmem;
+  cfg.dynamicSmemBytes = PairCfg<HC, NC>::kSmem;
   cudaLaunchAttribute at[1];
   at[0].id = cudaLaunchAttributeClusterDimension;
-  at[0].val.clusterDim.x = 2;
+  at[0].val.clusterDim.x = NC;
   at[0].val.clusterDim.y = 1;
   at[0].val.clusterDim.z = 1;
   cfg.attrs = at;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, decode_pair_kernel<HC>, &cfg) != cudaSuccess || n <= 0) return 0;
+  if (cudaOccupancyMaxActiveClusters(&n, decode_pair_kernel<HC, NC>, &cfg) != cudaSuccess || n <= 0) return 0;
   if (dev >= 0 && dev < 128) cached[dev] = n;
   return n;
 }
 
 }  // namespace
 
-int decode_pair_capacity(int hc) { return hc == 16 ? max_pairs<16>() : max_pairs<32>(); }
+int decode_pair_cluster_size(int hc) { return hc == 16 ? kPairClusterHC16 : 2; }
 
-cudaError_t launch_decode_pair(const DecodeParams& p, int hc, int pairs_per_group, cudaStream_t stream) {
-  return hc == 16 ? launch_pair<16>(p, pairs_per_group, stream) : launch_pair<32>(p, pairs_per_group, stream);
+int decode_pair_capacity(int hc) {
+  if (hc == 16) return max_clusters<16, kPairClusterHC16>();
+  return max_clusters<32, 2>();
+}
+
+cudaError_t launch_decode_pair(const DecodeParams& p, int hc, int clusters_per_group, cudaStream_t stream) {
+  return hc == 16 ? launch_pair<16, kPairClusterHC16>(p, clusters_per_group, stream)
+                  : launch_pair<32, 2>(p, clusters_per_group, stream);
 }
 
 }  // namespace mla

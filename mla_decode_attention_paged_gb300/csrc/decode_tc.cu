@@ -228,6 +228,8 @@ __global__ void __launch_bounds__(Cfg<HC, kInt8>::kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = B->tmem_base;
+  griddep_wait();  // the plan and Q come from the kernel before
+  griddep_launch_dependents();
 
   const int G = p.num_groups, g = blockIdx.x % G, cp = blockIdx.x / G, Cp = gridDim.x / G;
   const long long S = p.status[1];  // effective split count from the plan
@@ -765,8 +767,8 @@ cudaError_t launch_tc(const DecodeParams& p, int grid, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 128) attr[dev] = true;
   }
-  decode_tc_kernel<HC, kInt8><<<grid, Cfg<HC, kInt8>::kThreads, Cfg<HC, kInt8>::kSmem, stream>>>(mc, mq, p);
-  return cudaGetLastError();
+  return launch_pdl(decode_tc_kernel<HC, kInt8>, dim3(grid), dim3(Cfg<HC, kInt8>::kThreads), Cfg<HC, kInt8>::kSmem,
+                    stream, 1, mc, mq, p);
 }
 
 }  // namespace

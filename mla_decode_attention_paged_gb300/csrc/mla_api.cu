@@ -206,8 +206,8 @@ int mla_decode(const mla_dims* d, const void* q_nope, const void* q_pe, const vo
   cp.partial_o = dp.partial_o;
   cp.partial_lse = dp.partial_lse;
   cp.seg_base = dp.seg_base;
-  cp.o_lat = reinterpret_cast<float*>(ws + L.o_lat);
-  cp.max_segments = S + batch;
+  cp.status = dp.status;
+  cp.sm_count = sm_count();
   cp.W_UV = static_cast<const __nv_bfloat16*>(W_UV);
   cp.out = static_cast<__nv_bfloat16*>(out);
   cp.lse_out = lse_out;

@@ -31,9 +31,8 @@ constexpr float kLn2 = 0.6931471805599453f;
 //                                     part c covers latent dims [64c, 64c + 64), part 0 also the RoPE part
 //   partial_lse    fp32  [NSEG, H]
 //   partial_o      fp32  [NSEG, H, 512]   NSEG = num_splits + B (upper bound)
-//   o_lat          fp32  [B, H, 512]      merged latent outputs
 struct WorkspaceLayout {
-  size_t status, tile_start, seg_base, len_checked, q_full, q_sum, partial_lse, partial_o, o_lat, total;
+  size_t status, tile_start, seg_base, len_checked, q_full, q_sum, partial_lse, partial_o, total;
 };
 
 __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -50,7 +49,6 @@ __host__ __device__ inline WorkspaceLayout workspace_layout(int batch, int heads
   const size_t nseg = size_t(num_splits) + batch;
   L.partial_lse = off;  off = align256(off + 4 * nseg * heads);
   L.partial_o = off;    off = align256(off + 4 * nseg * heads * kLatent);
-  L.o_lat = off;        off = align256(off + 4 * size_t(batch) * heads * kLatent);
   L.total = off;
   return L;
 }

@@ -2,6 +2,8 @@
 // and the launch functions of each kernel file.
 #pragma once
 
+#include <utility>
+
 #include "mla_device.cuh"
 
 namespace mla {
@@ -39,12 +41,12 @@ struct CombineUVParams {
   const float* partial_o;     // [NSEG, H, 512]
   const float* partial_lse;   // [NSEG, H]
   const int* seg_base;        // [B + 1]
-  float* o_lat;               // [B, H, 512] merged latent outputs (written by the merge kernel)
   const __nv_bfloat16* W_UV;  // [H, 128, 512]
   __nv_bfloat16* out;         // [B, H, 128]
   float* lse_out;             // [B, H] or null
+  int* status;
   int batch, heads;
-  int max_segments;           // num_splits + batch: bound on the segments of all sequences
+  int sm_count;               // sizes the grid
 };
 
 struct CombineParams {
@@ -61,8 +63,39 @@ cudaError_t launch_combine_uv(const CombineUVParams& p, cudaStream_t stream);
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream);
 cudaError_t launch_decode_tc(const DecodeParams& p, int hc, bool int8, int grid, cudaStream_t stream);
 int decode_head_group(int heads, bool int8);
-// bf16 caches: CTA-pair kernel.  Capacity = clusters of two resident at once (0 if none).
+// Launches `kernel` with programmatic dependent launch (and, if cluster_x > 1,
+// thread-block clusters of cluster_x CTAs).  The kernels of the decode step
+// (append, absorb, attention, merge + up-projection) set up their shared
+// memory, barriers and tensor memory, then call griddep_wait() before their
+// first global-memory access and griddep_launch_dependents() after it, so
+// each launch and prologue overlaps the tail of the kernel before it.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                              unsigned cluster_x, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute at[2];
+  unsigned n = 0;
+  at[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[n].val.programmaticStreamSerializationAllowed = 1;
+  ++n;
+  if (cluster_x > 1) {
+    at[n].id = cudaLaunchAttributeClusterDimension;
+    at[n].val.clusterDim.x = cluster_x;
+    at[n].val.clusterDim.y = 1;
+    at[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  cfg.attrs = at;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+// bf16 caches: CTA-cluster kernel.  Capacity = clusters resident at once (0 if none).
 int decode_pair_capacity(int hc);
-cudaError_t launch_decode_pair(const DecodeParams& p, int hc, int pairs_per_group, cudaStream_t stream);
+cudaError_t launch_decode_pair(const DecodeParams& p, int hc, int clusters_per_group, cudaStream_t stream);
 
 }  // namespace mla
