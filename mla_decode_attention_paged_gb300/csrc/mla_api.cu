@@ -32,11 +32,17 @@ int sm_count() {
   return n;
 }
 
+// Automatic split count: one partition per resident attention unit of a
+// head group -- a CTA cluster for bf16 caches, a CTA for INT8 caches (more
+// partitions only add segment switches and partials to merge).
 int effective_splits(const mla_dims* d, int num_splits) {
   if (num_splits > 0) return num_splits;
-  const int n = sm_count();
+  const bool int8 = d->cache_dtype == MLA_CACHE_INT8;
+  const int hc = decode_head_group(d->num_heads, int8);
+  const int clusters = int8 ? 0 : decode_pair_capacity(hc);
+  const int n = clusters > 0 ? clusters : sm_count();
   if (n <= 0) return -1;
-  const int groups = d->num_heads / decode_head_group(d->num_heads, d->cache_dtype == MLA_CACHE_INT8);
+  const int groups = d->num_heads / hc;
   return n / groups > 0 ? n / groups : 1;
 }
 
