@@ -188,13 +188,18 @@ def cpu_baseline(w, inp, seconds):
             else:
                 cache, sz = W.bf16_to_bits(sub), None
         t_start = time.perf_counter()   # time the oracle itself, not the page gather
-        O.decode(qn, qp, cache, sz, tab, lens, wk, wv, inp["scale"], w.page_size, w.int8,
-                 pairs=[(b, h) for h in range(w.heads)])
+        if w.q_len == 1:
+            O.decode(qn, qp, cache, sz, tab, lens, wk, wv, inp["scale"], w.page_size, w.int8,
+                     pairs=[(b, h) for h in range(w.heads)])
+        else:
+            O.decode_multi_token(qn, qp, cache, sz, tab, lens, wk, wv, inp["scale"], w.page_size, w.int8,
+                                 triples=[(b, t, h) for t in range(w.q_len) for h in range(w.heads)])
         el += time.perf_counter() - t_start
         done += 1
         tokens_attended += int(lens[b])
-    return {"value": done / el, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-            "sample": f"{done} whole sequence(s) x {w.heads} heads of {w.name} ({tokens_attended} cached tokens, "
+    return {"value": done * w.q_len / el, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"{done} whole sequence(s) x {w.q_len} token(s) x {w.heads} heads of {w.name} "
+                      f"({tokens_attended} cached tokens, "
                       f"un-absorbed fp64 oracle), {el:.1f} s"}
 
 
@@ -208,7 +213,7 @@ def run_ours(args, rank, world):
     w = W.WORKLOADS[args.workload]
     inp = W.make_decode_inputs(w, device=dev)
     d = mla.dims(w.heads, w.page_size, int8=w.int8)
-    B, H = w.batch, w.heads
+    B, H, T = w.batch, w.heads, w.q_len
     seq_lens = inp["seq_lens"]
     table = inp["block_table"].to(dev)
     npg = inp["num_pages"]
@@ -222,24 +227,29 @@ def run_ours(args, rank, world):
     else:
         cache, sz = inp["cache"], None
     inp["cache_dev"], inp["sz_dev"] = cache, sz
-    # the step's new token per sequence: the last position of each sequence
+    # the step's new tokens: the last T positions of each sequence
     g = W.generator(w.seed + 1000, dev)
-    new_c = W.draw_bf16((B, 512), 1.0, g)
-    new_k = W.draw_bf16((B, 64), 1.0, g)
-    seq_ids = torch.arange(B, dtype=torch.int32, device=dev)
-    positions = (seq_lens.to(dev) - 1).clamp(min=0).to(torch.int32)
-    auto = mla.auto_num_splits(d, B)
+    new_c = W.draw_bf16((B * T, 512), 1.0, g)
+    new_k = W.draw_bf16((B * T, 64), 1.0, g)
+    seq_ids = torch.arange(B, dtype=torch.int32, device=dev).repeat_interleave(T)
+    positions = (seq_lens.to(dev).repeat_interleave(T) - T +
+                 torch.arange(T, dtype=torch.int32, device=dev).repeat(B)).clamp(min=0).to(torch.int32)
+    # the kernels see T * H heads per sequence; the automatic split count is theirs
+    d_rows = mla.dims(H * T, w.page_size, int8=w.int8)
+    auto = mla.auto_num_splits(d_rows if mla.check_dims(d_rows) == mla.MLA_OK else d, B)
     splits = args.num_splits if args.num_splits is not None else (W.num_splits_for(w, auto) or auto)
-    ws = torch.empty(mla.decode_workspace_size(d, B, splits), dtype=torch.uint8, device=dev)
-    out = torch.empty((B, H, 128), dtype=torch.bfloat16, device=dev)
-    lse = torch.empty((B, H), dtype=torch.float32, device=dev)
+    ws = torch.empty(mla.decode_multi_workspace_size(d, B, T, splits), dtype=torch.uint8, device=dev)
+    qshape = (B, H) if T == 1 else (B, T, H)
+    out = torch.empty(qshape + (128,), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(qshape, dtype=torch.float32, device=dev)
+    decode_fn = mla.decode if T == 1 else mla.decode_multi
     q_nope, q_pe, W_UK, W_UV = inp["q_nope"], inp["q_pe"], inp["W_UK"], inp["W_UV"]
     seq_lens = seq_lens.to(dev)
 
     def step():
         mla.cache_append(d, cache, sz, table, seq_ids, positions, new_c, new_k, w.rope_theta)
-        mla.decode(d, q_nope, q_pe, cache, sz, table, seq_lens, W_UK, W_UV, inp["scale"], num_splits=splits,
-                   workspace=ws, out=out, lse_out=lse)
+        decode_fn(d, q_nope, q_pe, cache, sz, table, seq_lens, W_UK, W_UV, inp["scale"], num_splits=splits,
+                  workspace=ws, out=out, lse_out=lse)
 
     for _ in range(args.warmup):
         step()
@@ -278,7 +288,7 @@ def run_ours(args, rank, world):
     lens_sum = int(seq_lens.to(torch.int64).sum())
     bytes_per_token = 584 if w.int8 else 1152
     cache_bytes = lens_sum * bytes_per_token
-    tokens_per_s = whole_job_rate(B, world, ms)
+    tokens_per_s = whole_job_rate(B * T, world, ms)
     step_cache_gbs = whole_job_rate(cache_bytes, world, ms) / 1e9
 
     # e2e: the same step through the public API from pinned host buffers
@@ -286,8 +296,8 @@ def run_ours(args, rank, world):
     h_in = {k: pin(v) for k, v in dict(q_nope=q_nope, q_pe=q_pe, new_c=new_c, new_k=new_k, seq_ids=seq_ids,
                                        positions=positions, table=table, seq_lens=seq_lens).items()}
     d_in = {k: torch.empty_like(v, device=dev) for k, v in h_in.items()}
-    h_out = torch.empty((B, H, 128), dtype=torch.bfloat16).pin_memory()
-    h_lse = torch.empty((B, H), dtype=torch.float32).pin_memory()
+    h_out = torch.empty(qshape + (128,), dtype=torch.bfloat16).pin_memory()
+    h_lse = torch.empty(qshape, dtype=torch.float32).pin_memory()
     h2d = sum(v.numel() * v.element_size() for v in h_in.values())
     d2h = h_out.numel() * 2 + h_lse.numel() * 4
 
@@ -296,8 +306,8 @@ def run_ours(args, rank, world):
             d_in[k].copy_(h_in[k], non_blocking=True)
         mla.cache_append(d, cache, sz, d_in["table"], d_in["seq_ids"], d_in["positions"], d_in["new_c"],
                          d_in["new_k"], w.rope_theta)
-        mla.decode(d, d_in["q_nope"], d_in["q_pe"], cache, sz, d_in["table"], d_in["seq_lens"], W_UK, W_UV,
-                   inp["scale"], num_splits=splits, workspace=ws, out=out, lse_out=lse)
+        decode_fn(d, d_in["q_nope"], d_in["q_pe"], cache, sz, d_in["table"], d_in["seq_lens"], W_UK, W_UV,
+                  inp["scale"], num_splits=splits, workspace=ws, out=out, lse_out=lse)
         h_out.copy_(out, non_blocking=True)
         h_lse.copy_(lse, non_blocking=True)
 
@@ -322,7 +332,7 @@ def run_ours(args, rank, world):
         "scaling": "weak", "vs_baseline": None, "dtype": "int8" if w.int8 else "bf16",
         "data": "synthetic (seeded; random-init weights of DeepSeek-V2 MLA shapes)",
         "config": {"workload": w.name, "batch": B, "heads": H, "context": w.context, "page_size": w.page_size,
-                   "num_splits": splits, "cache_bytes": cache_bytes,
+                   "q_len": T, "num_splits": splits, "cache_bytes": cache_bytes,
                    "l2": "inputs larger than L2 (no flush): the cache read each step exceeds the 126 MB L2"
                    if cache_bytes > 200e6 else "cache smaller than L2",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
@@ -333,7 +343,7 @@ def run_ours(args, rank, world):
                      "frac": round(achieved / peak, 4), "peak_source": peak_src,
                      "traffic": traffic, "kernel": attention_kernel(w.int8)[1],
                      "algorithmic_bytes_per_launch": cache_bytes},
-        "e2e": {"value": round(whole_job_rate(B, world, e2e_ms), 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+        "e2e": {"value": round(whole_job_rate(B * T, world, e2e_ms), 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 5)},
         "gpu_launches": 4 * args.steps,
         "clocks": clk.summary(),
@@ -371,7 +381,7 @@ def run_reference(args, rank, world):
             "warmup": args.warmup, "ms_per_step": round(1e3 * el / args.steps, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
             "config": {"workload": w.name, "batch": w.batch, "heads": w.heads, "context": w.context,
-                       "page_size": w.page_size}, "impl": "reference", "cpu_baseline": cb,
+                       "page_size": w.page_size, "q_len": w.q_len}, "impl": "reference", "cpu_baseline": cb,
             "e2e": {"value": round(v, 5), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 

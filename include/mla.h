@@ -173,6 +173,47 @@ int mla_decode(const mla_dims* dims, const void* q_nope, const void* q_pe, const
                void* workspace, size_t workspace_bytes, void* out, float* lse_out,
                mla_stream_t stream);
 
+/* Largest number of query tokens per sequence mla_decode_multi accepts. */
+#define MLA_MAX_Q_LEN 8
+
+/* Bytes of workspace mla_decode_multi needs for (dims, batch, q_len,
+ * num_splits); 0 if the arguments are invalid.  q_len = 1 gives
+ * mla_decode_workspace_size. */
+size_t mla_decode_multi_workspace_size(const mla_dims* dims, int32_t batch, int32_t q_len, int32_t num_splits);
+
+/*
+ * mla_decode_multi -- decode q_len query tokens per sequence against the
+ * paged cache in one pass: the verification read of speculative decoding
+ * ("The Architecture of Memory", "Speculative Decoding: Amortizing the Memory
+ * Fetch": the target model checks all drafted tokens in one forward pass that
+ * reads its cache once) with a causal mask among the new tokens (same page,
+ * "Tree Attention Verification": dense attention over the history, masked
+ * among the new tokens; this entry point takes a chain, not a tree).
+ *
+ * The q_len new tokens of sequence b are the last q_len tokens of its cache
+ * (append them first): query token t sits at position seq_lens[b] - q_len + t
+ * and attends to cache positions [0, seq_lens[b] - q_len + t], itself
+ * included.  A query whose position is below 0 (seq_lens[b] < q_len) attends
+ * to nothing: out = 0, lse = -inf.  Everything else is as for mla_decode:
+ *
+ *   q_nope      bf16 [batch, q_len, H, 128]
+ *   q_pe        bf16 [batch, q_len, H, 64], each rotated for its own position
+ *   out         bf16 [batch, q_len, H, 128]
+ *   lse_out     optional fp32 [batch, q_len, H]
+ *   q_len       1 .. MLA_MAX_Q_LEN; q_len = 1 is exactly mla_decode
+ *   workspace   at least mla_decode_multi_workspace_size(dims, batch, q_len,
+ *               num_splits) bytes.
+ * The work of the batch is that of a single-token decode with q_len * H
+ * heads, so num_splits = 0 picks the automatic count for q_len * H heads.
+ * Returns MLA_ERR_INVALID_ARG for q_len outside [1, MLA_MAX_Q_LEN].
+ */
+int mla_decode_multi(const mla_dims* dims, const void* q_nope, const void* q_pe, const void* cache,
+                     const float* cache_scale_zero, int32_t num_pages, const int32_t* block_table,
+                     int32_t max_pages_per_seq, const int32_t* seq_lens, int32_t batch, int32_t q_len,
+                     const void* W_UK, const void* W_UV, float softmax_scale, int32_t num_splits,
+                     void* workspace, size_t workspace_bytes, void* out, float* lse_out,
+                     mla_stream_t stream);
+
 /* Size of the fixed scratch array used by mla_decode_no_alloc. */
 #define MLA_NO_ALLOC_WORKSPACE_BYTES (16u << 20)
 

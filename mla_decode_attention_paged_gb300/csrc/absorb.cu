@@ -87,7 +87,9 @@ __device__ __forceinline__ float round_out(float v, uint16_t* dst) {  // store a
 }
 
 // ---------------------------------------------------------------------------
-// Absorption on the tensor cores.  Per head the product is a small GEMM,
+// Absorption on the tensor cores.  Per head (query row h of each sequence,
+// weight head h % heads_w: multi-token decode has q_len rows per weight
+// head) the product is a small GEMM,
 // q_lat^T [512 x B] = W^UK_h^T [512 x 128] * q_nope_h^T [128 x B]; a CTA takes
 // one 128-row tile of latent dims (the MMA's M) and NB sequences (its N):
 //   A = W^UK_h[:, m0:m0+128]^T   MN-major (W^UK rows are 512 latent dims long)
@@ -155,7 +157,7 @@ __global__ void __launch_bounds__(kAbsThreads) absorb_kernel(AbsorbParams p) {
 #pragma unroll
   for (int u = 0; u < kWPer; ++u) {
     const int i = tid + u * kAbsThreads, k = i >> 4, j = i & 15;
-    wv[u] = *reinterpret_cast<const uint4*>(p.W_UK + (size_t(h) * kNope + k) * kLatent + m0 + 8 * j);
+    wv[u] = *reinterpret_cast<const uint4*>(p.W_UK + (size_t(h % p.heads_w) * kNope + k) * kLatent + m0 + 8 * j);
   }
 #pragma unroll
   for (int u = 0; u < kQPer; ++u) {

@@ -13,8 +13,8 @@ namespace mla {
 using namespace ptx;
 
 // ---------------------------------------------------------------------------
-// Merge and up-projection in one kernel.  A CTA takes one head h and NB
-// sequences:
+// Merge and up-projection in one kernel.  A CTA takes one head h (query row
+// h of each sequence; weight head h % heads_w) and NB sequences:
 //   1. its 16 warps merge each sequence's segments (partial outputs of the
 //      split-KV ranges) with log-sum-exp weights into o_lat[b][h] (fp32), and
 //      store it in shared memory as two bf16 rows, hi = bf16(o) and
@@ -100,7 +100,8 @@ __global__ void __launch_bounds__(kUVThreads, 1)
   if (tid == 0) {
     mbar_arrive_expect_tx(w_full, kUVWBytes);
 #pragma unroll
-    for (int kb = 0; kb < 8; ++kb) tma_load_2d(smem + kb * kUVWBlock, &tmap_wuv, 64 * kb, h * kVDim, w_full);
+    for (int kb = 0; kb < 8; ++kb)
+      tma_load_2d(smem + kb * kUVWBlock, &tmap_wuv, 64 * kb, (h % p.heads_w) * kVDim, w_full);
   }
   if (tid <= nb) seg[tid] = p.seg_base[b0 + tid];
   __syncthreads();
@@ -299,7 +300,7 @@ template <int NB>
 cudaError_t launch_merge_uv(const CombineUVParams& p, cudaStream_t stream) {
   using C = UVCfg<NB>;
   CUtensorMap mw;
-  if (!dc::make_map_2d(&mw, p.W_UV, 2, kLatent, uint64_t(p.heads) * kVDim, 64, kVDim, CU_TENSOR_MAP_SWIZZLE_128B))
+  if (!dc::make_map_2d(&mw, p.W_UV, 2, kLatent, uint64_t(p.heads_w) * kVDim, 64, kVDim, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   static bool attr[128] = {};
   int dev = 0;

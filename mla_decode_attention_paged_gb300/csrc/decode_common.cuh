@@ -48,6 +48,26 @@ __device__ __forceinline__ float warp_transpose_reduce(float (&v)[N], int lane) 
   return v[0];
 }
 
+// Multi-token decode ("The Architecture of Memory", "Speculative Decoding"
+// and "Tree Attention Verification": the new tokens see the history and the
+// new tokens before them).  Row h of head group g is query token
+// (g HC + h) / heads_w, at position len - q_len + that token; the score of
+// cache position `pos` is masked for every row whose position is below pos.
+// Only tiles that reach past position len - q_len need it.
+__device__ __forceinline__ bool causal_tile(const DecodeParams& p, const TileInfo& t, int len) {
+  return p.q_len > 1 && t.tile * kTile + t.valid > len - p.q_len + 1;
+}
+template <int HC>
+__device__ __forceinline__ void causal_mask(float (&x)[HC], const DecodeParams& p, int g, int len, int pos) {
+  const int first = len - p.q_len;  // position of query token 0
+#pragma unroll
+  for (int h = 0; h < HC; ++h)
+    if (pos > first + (g * HC + h) / p.heads_w) x[h] = -INFINITY;
+}
+// Running max of a row with no unmasked score yet: finite, so that
+// exp2(x - max) of a masked score is 0 rather than NaN, and below any score.
+constexpr float kEmptyRowMax = -1e30f;
+
 // Physical page of token `tok` of sequence b (range-checked; out-of-range
 // entries are reported and replaced by page 0 to stay in bounds).
 __device__ __forceinline__ int page_of(const DecodeParams& p, int b, int tok) {

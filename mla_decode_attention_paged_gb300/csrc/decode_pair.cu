@@ -444,6 +444,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
       }
 #pragma unroll
       for (int h = 0; h < HC; ++h) x[h] = valid ? x[h] * p.scale_log2 : -INFINITY;
+      if (causal_tile(p, t, walk.len_b)) causal_mask<HC>(x, p, g, walk.len_b, t.tile * kTile + st);
       // Running max: it only has to bound the scores to within
       // kRescaleThreshold (log2 units).  The first tile of a segment, and a
       // tile that breaks the bound, take the exact path (per-head tile max and,
@@ -470,7 +471,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
           const float4 m4 = reinterpret_cast<const float4*>(rm)[h];
           const float mt = fmaxf(fmaxf(m4.x, m4.y), fmaxf(m4.z, m4.w));
           if (t.first) {
-            m_run[h] = mt;
+            m_run[h] = fmaxf(mt, kEmptyRowMax);  // a row masked in the whole tile stays empty
             l_run[h] = 0.f;
             alpha[h] = 1.f;
           } else if (mt > m_run[h] + kRescaleThreshold) {
@@ -542,7 +543,8 @@ __global__ void __launch_bounds__(kPairThreads, 1)
 #pragma unroll
         for (int h = 0; h < HC; ++h) {
           const float4 l4 = reinterpret_cast<const float4*>(rl)[h];
-          inv_l[h] = __frcp_rn((l4.x + l4.y) + (l4.z + l4.w));
+          const float l = (l4.x + l4.y) + (l4.z + l4.w);
+          inv_l[h] = l > 0.f ? __frcp_rn(l) : 0.f;  // 0: a row with no visible token (multi-token decode)
         }
         float* dst = p.partial_o + (size_t(t.seg) * p.heads + g * HC) * kLatent + lat0;
 #pragma unroll
@@ -564,7 +566,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
               mh = m_run[h];
               ih = inv_l[h];
             }
-          p.partial_lse[size_t(t.seg) * p.heads + g * HC + st] = (mh - log2f(ih)) * kLn2;
+          p.partial_lse[size_t(t.seg) * p.heads + g * HC + st] = ih > 0.f ? (mh - log2f(ih)) * kLn2 : -INFINITY;
         }
         ++seg;
       }

@@ -592,6 +592,7 @@ __global__ void __launch_bounds__(Cfg<HC, kInt8>::kThreads, 1)
         const float raw = kInt8 ? fmaf(-tok_z, qsum[h], x[h]) : x[h];
         x[h] = valid ? raw * row_scale : -INFINITY;
       }
+      if (causal_tile(p, t, walk.len_b)) causal_mask<HC>(x, p, g, walk.len_b, t.tile * kTile + st);
       // Running max.  It only has to bound the scores to within
       // kRescaleThreshold (log2 units), so in the common case every thread
       // checks its own scores against it and the 128 threads OR that flag in
@@ -621,7 +622,7 @@ __global__ void __launch_bounds__(Cfg<HC, kInt8>::kThreads, 1)
           const float4 m4 = reinterpret_cast<const float4*>(rm)[h];
           const float mt = fmaxf(fmaxf(m4.x, m4.y), fmaxf(m4.z, m4.w));
           if (t.first) {
-            m_run[h] = mt;
+            m_run[h] = fmaxf(mt, kEmptyRowMax);  // a row masked in the whole tile stays empty
             l_run[h] = 0.f;
             corr[h] = 0.f;
             alpha[h] = 1.f;
@@ -710,7 +711,8 @@ __global__ void __launch_bounds__(Cfg<HC, kInt8>::kThreads, 1)
 #pragma unroll
         for (int h = 0; h < HC; ++h) {
           const float4 l4 = reinterpret_cast<const float4*>(rl)[h];
-          inv_l[h] = 1.f / ((l4.x + l4.y) + (l4.z + l4.w));
+          const float l = (l4.x + l4.y) + (l4.z + l4.w);
+          inv_l[h] = l > 0.f ? 1.f / l : 0.f;  // 0: a row with no visible token (multi-token decode)
           if (kInt8) {
             const float4 c4 = reinterpret_cast<const float4*>(rc)[h];
             corr[h] = (c4.x + c4.y) + (c4.z + c4.w);
@@ -731,7 +733,9 @@ __global__ void __launch_bounds__(Cfg<HC, kInt8>::kThreads, 1)
         mbar_arrive(&B->o_free);
 #pragma unroll
         for (int h = 0; h < HC; ++h)
-          if (st == h) p.partial_lse[size_t(t.seg) * p.heads + g * HC + h] = (m_run[h] - log2f(inv_l[h])) * kLn2;
+          if (st == h)
+            p.partial_lse[size_t(t.seg) * p.heads + g * HC + h] =
+                inv_l[h] > 0.f ? (m_run[h] - log2f(inv_l[h])) * kLn2 : -INFINITY;
         ++seg;
       }
     }

@@ -32,6 +32,14 @@ int sm_count() {
   return n;
 }
 
+// Dimensions as the kernels see them for q_len query tokens per sequence:
+// every (token, head) pair is one row, q_len * H rows in all.
+mla_dims row_dims(const mla_dims* d, int q_len) {
+  mla_dims r = *d;
+  r.num_heads = d->num_heads * q_len;
+  return r;
+}
+
 // Automatic split count: one partition per resident attention unit of a
 // head group -- a CTA cluster for bf16 caches, a CTA for INT8 caches (more
 // partitions only add segment switches and partials to merge).
@@ -123,10 +131,15 @@ int mla_auto_num_splits(const mla_dims* d, int32_t batch) {
 }
 
 size_t mla_decode_workspace_size(const mla_dims* d, int32_t batch, int32_t num_splits) {
-  if (mla_check_dims(d) != MLA_OK || batch <= 0 || num_splits < 0) return 0;
-  const int s = effective_splits(d, num_splits);
+  return mla_decode_multi_workspace_size(d, batch, 1, num_splits);
+}
+
+size_t mla_decode_multi_workspace_size(const mla_dims* d, int32_t batch, int32_t q_len, int32_t num_splits) {
+  if (mla_check_dims(d) != MLA_OK || batch <= 0 || num_splits < 0 || q_len < 1 || q_len > MLA_MAX_Q_LEN) return 0;
+  const mla_dims dr = row_dims(d, q_len);
+  const int s = effective_splits(&dr, num_splits);
   if (s <= 0) return 0;
-  return workspace_layout(batch, d->num_heads, s).total;
+  return workspace_layout(batch, dr.num_heads, s).total;
 }
 
 int mla_decode(const mla_dims* d, const void* q_nope, const void* q_pe, const void* cache,
@@ -134,10 +147,21 @@ int mla_decode(const mla_dims* d, const void* q_nope, const void* q_pe, const vo
                int32_t max_pages_per_seq, const int32_t* seq_lens, int32_t batch, const void* W_UK,
                const void* W_UV, float softmax_scale, int32_t num_splits, void* workspace,
                size_t workspace_bytes, void* out, float* lse_out, mla_stream_t stream) {
+  return mla_decode_multi(d, q_nope, q_pe, cache, cache_scale_zero, num_pages, block_table, max_pages_per_seq,
+                          seq_lens, batch, 1, W_UK, W_UV, softmax_scale, num_splits, workspace, workspace_bytes, out,
+                          lse_out, stream);
+}
+
+int mla_decode_multi(const mla_dims* d, const void* q_nope, const void* q_pe, const void* cache,
+                     const float* cache_scale_zero, int32_t num_pages, const int32_t* block_table,
+                     int32_t max_pages_per_seq, const int32_t* seq_lens, int32_t batch, int32_t q_len,
+                     const void* W_UK, const void* W_UV, float softmax_scale, int32_t num_splits, void* workspace,
+                     size_t workspace_bytes, void* out, float* lse_out, mla_stream_t stream) {
   int st = mla_check_dims(d);
   if (st != MLA_OK) return st;
   const bool int8 = d->cache_dtype == MLA_CACHE_INT8;
   if (batch <= 0 || num_pages <= 0 || max_pages_per_seq <= 0 || num_splits < 0) return MLA_ERR_INVALID_ARG;
+  if (q_len < 1 || q_len > MLA_MAX_Q_LEN) return MLA_ERR_INVALID_ARG;
   if (!(softmax_scale > 0.f) || softmax_scale == INFINITY) return MLA_ERR_INVALID_ARG;
   if (!q_nope || !q_pe || !cache || !block_table || !seq_lens || !W_UK || !W_UV || !out) return MLA_ERR_INVALID_ARG;
   if (int8 && !cache_scale_zero) return MLA_ERR_INVALID_ARG;
@@ -147,12 +171,13 @@ int mla_decode(const mla_dims* d, const void* q_nope, const void* q_pe, const vo
     return MLA_ERR_INVALID_ARG;
   if ((long long)max_pages_per_seq * d->page_size > (1LL << 31) - 1) return MLA_ERR_INVALID_ARG;
   if ((long long)num_pages * d->page_size > (1LL << 31) - 1) return MLA_ERR_INVALID_ARG;  // row index is int32
-  const int S = effective_splits(d, num_splits);
+  const mla_dims dr = row_dims(d, q_len);  // the kernels' "heads": q_len * H rows per sequence
+  const int S = effective_splits(&dr, num_splits);
   if (S <= 0) return MLA_ERR_CUDA;
-  const WorkspaceLayout L = workspace_layout(batch, d->num_heads, S);
+  const WorkspaceLayout L = workspace_layout(batch, dr.num_heads, S);
   if (!workspace || !aligned(workspace, 256) || workspace_bytes < L.total) return MLA_ERR_WORKSPACE;
 
-  const int H = d->num_heads, hc = decode_head_group(H, int8), groups = H / hc;
+  const int H = dr.num_heads, hc = decode_head_group(H, int8), groups = H / hc;
   char* ws = static_cast<char*>(workspace);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 
@@ -169,6 +194,7 @@ int mla_decode(const mla_dims* d, const void* q_nope, const void* q_pe, const vo
   ap.status = reinterpret_cast<int*>(ws + L.status);
   ap.batch = batch;
   ap.heads = H;
+  ap.heads_w = d->num_heads;
   ap.max_len = max_pages_per_seq * d->page_size;
   ap.num_splits = S;
   if (launch_absorb(ap, int8, s) != cudaSuccess) return MLA_ERR_CUDA;
@@ -193,6 +219,8 @@ int mla_decode(const mla_dims* d, const void* q_nope, const void* q_pe, const vo
   dp.max_pages = max_pages_per_seq;
   dp.num_pages = num_pages;
   dp.num_splits = S;
+  dp.q_len = q_len;
+  dp.heads_w = d->num_heads;
   dp.scale_log2 = softmax_scale * kLog2e;
   dp.inject_wait_timeout = g_inject_wait_timeout.load();
   // bf16 caches run on CTA pairs (two SMs share each tile); INT8 caches, and
@@ -219,6 +247,7 @@ int mla_decode(const mla_dims* d, const void* q_nope, const void* q_pe, const vo
   cp.lse_out = lse_out;
   cp.batch = batch;
   cp.heads = H;
+  cp.heads_w = d->num_heads;
   if (launch_combine_uv(cp, s) != cudaSuccess) return MLA_ERR_CUDA;
   return MLA_OK;
 }

@@ -162,6 +162,9 @@ struct DecodeParams {
   float* partial_lse;            // [NSEG, H]
   int* status;
   int batch, heads, head_group, num_groups, page_size, max_pages, num_pages, num_splits;
+  // multi-token decode: row v of a sequence is query token v / heads_w, at
+  // position len - q_len + v / heads_w; it attends to positions up to its own
+  int q_len, heads_w;
   float scale_log2;              // softmax_scale * log2(e)
   int inject_wait_timeout;       // test hook (mla_test_inject_wait_timeout): 16 bytes never delivered
 };

@@ -8,10 +8,14 @@
 
 namespace mla {
 
+// Multi-token decode (q_len query tokens per sequence) runs the same kernels
+// over "rows": row v = t * heads_w + h of a sequence is query token t, head
+// h.  `heads` below counts rows (q_len * heads_w); the weights have heads_w
+// heads and row v uses head v % heads_w.
 struct AbsorbParams {
-  const __nv_bfloat16* q_nope;  // [B, H, 128]
-  const __nv_bfloat16* q_pe;    // [B, H, 64]
-  const __nv_bfloat16* W_UK;    // [H, 128, 512]
+  const __nv_bfloat16* q_nope;  // [B, heads, 128]
+  const __nv_bfloat16* q_pe;    // [B, heads, 64]
+  const __nv_bfloat16* W_UK;    // [heads_w, 128, 512]
   __nv_bfloat16* q_full;        // [B, H, 576] (fp16 bit patterns for INT8 caches)
   float* q_sum;                 // [B, H, kQSumParts]
   // plan
@@ -20,7 +24,7 @@ struct AbsorbParams {
   int* seg_base;
   int* len_checked;
   int* status;
-  int batch, heads, max_len, num_splits;
+  int batch, heads, heads_w, max_len, num_splits;
 };
 
 struct AppendParams {
@@ -41,11 +45,11 @@ struct CombineUVParams {
   const float* partial_o;     // [NSEG, H, 512]
   const float* partial_lse;   // [NSEG, H]
   const int* seg_base;        // [B + 1]
-  const __nv_bfloat16* W_UV;  // [H, 128, 512]
-  __nv_bfloat16* out;         // [B, H, 128]
-  float* lse_out;             // [B, H] or null
+  const __nv_bfloat16* W_UV;  // [heads_w, 128, 512]
+  __nv_bfloat16* out;         // [B, heads, 128]
+  float* lse_out;             // [B, heads] or null
   int* status;
-  int batch, heads;
+  int batch, heads, heads_w;
   int sm_count;               // sizes the grid
 };
 

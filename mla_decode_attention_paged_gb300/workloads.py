@@ -39,6 +39,7 @@ class Workload:
     int8: bool = False              # cache built from N(0,1) rows by the INT8 append
     min_splits_per_seq: int = 0     # the workload asks for at least this many KV chunks per sequence
     rope_theta: float = 10000.0     # used where the cache is built through the append
+    q_len: int = 1                  # query tokens per sequence (multi-token decode: the last q_len cached)
 
     @property
     def softmax_scale(self) -> float:
@@ -56,6 +57,11 @@ WORKLOADS = {
     "ctx1m": Workload("ctx1m_b2_h16_l1048576_p64", 2, 16, 1048576, 64, True, 1.0, 0.02, 1.0, 3,
                       min_splits_per_seq=148),
     "int8": Workload("int8_b128_h128_l8192_p64", 128, 128, 8192, 64, True, 1.0, 0.02, 1.0, 4, int8=True),
+    # multi-token decode (speculative verification) on the V2-Lite shape: 2 or 4 new tokens per sequence
+    "v2lite_mtp2": Workload("v2lite_mtp2_b32_t2_h16_l32768_p64", 32, 16, 32768, 64, True, 1.0, 0.02, 1.0, 5,
+                            q_len=2),
+    "v2lite_mtp4": Workload("v2lite_mtp4_b32_t4_h16_l32768_p64", 32, 16, 32768, 64, True, 1.0, 0.02, 1.0, 6,
+                            q_len=4),
 }
 
 
@@ -139,8 +145,9 @@ def make_decode_inputs(w: Workload, device="cpu"):
         d["cache"] = draw_bf16((num_pages, w.page_size, LATENT_DIM + ROPE_DIM), w.cache_std, g)
     d["W_UK"] = draw_bf16((w.heads, NOPE_DIM, LATENT_DIM), w.w_std, g)
     d["W_UV"] = draw_bf16((w.heads, V_DIM, LATENT_DIM), w.w_std, g)
-    d["q_nope"] = draw_bf16((w.batch, w.heads, NOPE_DIM), w.q_std, g)
-    d["q_pe"] = draw_bf16((w.batch, w.heads, ROPE_DIM), w.q_std, g)
+    qshape = (w.batch, w.heads) if w.q_len == 1 else (w.batch, w.q_len, w.heads)
+    d["q_nope"] = draw_bf16(qshape + (NOPE_DIM,), w.q_std, g)
+    d["q_pe"] = draw_bf16(qshape + (ROPE_DIM,), w.q_std, g)
     if w.int8:
         total = int(seq_lens.to(torch.int64).sum())
         d["src_c_kv"] = draw_bf16((total, LATENT_DIM), 1.0, g)

@@ -366,3 +366,42 @@ def decode(q_nope: np.ndarray, q_pe: np.ndarray, cache: np.ndarray, scale_zero: 
             out[b, h] = o
             lse[b, h] = l
     return out, lse
+
+
+def decode_multi_token(q_nope: np.ndarray, q_pe: np.ndarray, cache: np.ndarray, scale_zero: np.ndarray | None,
+                       block_table: np.ndarray, seq_lens: Sequence[int], W_UK: np.ndarray, W_UV: np.ndarray,
+                       scale: float, page_size: int, int8: bool, triples=None, absorbed: bool = False):
+    """Several new tokens of each sequence decoded in one pass: the
+    verification read of speculative decoding ([P4] "Speculative Decoding:
+    Amortizing the Memory Fetch": all drafted tokens are checked in one
+    forward pass that reads the cache once), causal among the new tokens
+    ([P4] "Tree Attention Verification": the history is attended densely and
+    each new token sees only the new tokens before it -- a chain here).
+
+    The T new tokens of sequence b are the last T of its L_b cached tokens
+    (appended before the call): query token t sits at position L_b - T + t and
+    attends to positions 0 .. L_b - T + t, itself included; a query whose
+    position is below 0 attends to nothing (o = 0, lse = -inf).
+
+    q_nope [B, T, H, 128], q_pe [B, T, H, 64] (each rotated for its own
+    position).  ``triples`` limits the work to a list of (b, t, h); others are
+    left NaN.  Returns (out [B, T, H, 128], lse [B, T, H]) in fp64.
+    """
+    B, T, H = q_nope.shape[0], q_nope.shape[1], q_nope.shape[2]
+    out = np.full((B, T, H, W_UV.shape[1]), np.nan)
+    lse = np.full((B, T, H), np.nan)
+    if triples is None:
+        triples = [(b, t, h) for b in range(B) for t in range(T) for h in range(H)]
+    by_seq: dict[int, list[tuple[int, int]]] = {}
+    for b, t, h in triples:
+        by_seq.setdefault(int(b), []).append((int(t), int(h)))
+    fn = attend_absorbed if absorbed else attend_unabsorbed
+    for b, th in by_seq.items():
+        L = int(seq_lens[b])
+        rows = gather_rows(cache, scale_zero, block_table, b, L, page_size, int8)
+        for t, h in th:
+            visible = max(0, L - T + t + 1)
+            o, l, _ = fn(q_nope[b, t, h], q_pe[b, t, h], rows[:visible], W_UK[h], W_UV[h], scale)
+            out[b, t, h] = o
+            lse[b, t, h] = l
+    return out, lse

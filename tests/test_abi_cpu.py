@@ -98,3 +98,22 @@ def test_host_validation_rejects_before_launch(lib):
     # timing hook: both or neither
     assert lib.mla_set_timing_events(fake, None) == mla.MLA_ERR_INVALID_ARG
     assert lib.mla_set_timing_events(None, None) == mla.MLA_OK
+
+
+def test_multi_token_workspace_and_validation(lib):
+    d = mla.dims(16, 64)
+    # q_len tokens of H heads need the workspace of a q_len * H-head decode
+    for T in (1, 2, 4, 8):
+        dT = mla.dims(16 * T, 64)
+        got = lib.mla_decode_multi_workspace_size(ctypes.byref(d), 32, T, 76)
+        assert got == lib.mla_decode_workspace_size(ctypes.byref(dT), 32, 76) > 0
+    assert lib.mla_decode_multi_workspace_size(ctypes.byref(d), 32, 0, 76) == 0
+    assert lib.mla_decode_multi_workspace_size(ctypes.byref(d), 32, mla.MAX_Q_LEN + 1, 76) == 0
+    fake = ctypes.c_void_p(0x10000)  # never dereferenced: validation fails first
+    args = [ctypes.byref(d), fake, fake, fake, None, 4, fake, 8, fake, 2, 2, fake, fake, ctypes.c_float(0.1), 4,
+            fake, ctypes.c_size_t(1 << 30), fake, None, None]
+    for bad_t in (0, -1, mla.MAX_Q_LEN + 1):
+        a = list(args); a[10] = bad_t
+        assert lib.mla_decode_multi(*a) == mla.MLA_ERR_INVALID_ARG
+    a = list(args); a[1] = None
+    assert lib.mla_decode_multi(*a) == mla.MLA_ERR_INVALID_ARG

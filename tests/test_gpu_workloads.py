@@ -53,3 +53,30 @@ def test_full_size_workload(cuda_lib, key):
     if heads is not None:
         ref_o, ref_l = oracle_decode(inp, w, all_pairs, absorbed=True, cache_override=oc)
         assert_parity(out, lse, ref_o, ref_l, all_pairs, w.name + " (absorbed oracle, all heads)")
+
+
+@pytest.mark.parametrize("key,seq", [("v2lite_mtp2", 9), ("v2lite_mtp4", 22)])
+def test_full_size_multi_token(cuda_lib, key, seq):
+    """Multi-token decode at the V2-Lite size (32 x 32,768 tokens, q_len 2 or
+    4), in bench.py's configuration: every (token, head) of one sampled
+    sequence against the un-absorbed oracle."""
+    import oracle as O
+    from harness import f64
+    w = W.WORKLOADS[key]
+    inp = W.make_decode_inputs(w, device="cuda")
+    d = dims_of(w)
+    T, H = w.q_len, w.heads
+    d_rows = mla.dims(H * T, w.page_size)
+    splits = mla.auto_num_splits(d_rows, w.batch)
+    out, lse = mla.decode_multi(d, inp["q_nope"], inp["q_pe"], inp["cache"], None, inp["block_table"],
+                                inp["seq_lens"], inp["W_UK"], inp["W_UV"], inp["scale"], num_splits=splits)
+    torch.cuda.synchronize()
+    cache, sz, table = oracle_cache(inp, w, [seq])
+    ref_o, ref_l = O.decode_multi_token(f64(inp["q_nope"]), f64(inp["q_pe"]), cache, sz, table,
+                                        inp["seq_lens"].cpu().numpy(), f64(inp["W_UK"]), f64(inp["W_UV"]),
+                                        inp["scale"], w.page_size, False,
+                                        triples=[(seq, t, h) for t in range(T) for h in range(H)])
+    B = w.batch
+    pairs = [(seq, v) for v in range(T * H)]
+    assert_parity(out.reshape(B, T * H, -1), lse.reshape(B, T * H), ref_o.reshape(B, T * H, -1),
+                  ref_l.reshape(B, T * H), pairs, w.name)

@@ -315,3 +315,99 @@ def test_pins_catch_planted_mistakes(monkeypatch):
     for bad in (dropped_rope, swapped_weights, wrong_sign):
         o = np.stack([bad(q_nope[h], q_pe[h], rows, W_UK[h], W_UV[h], 0.2)[0] for h in range(H)])
         assert not np.allclose(o, ref, rtol=1e-6), bad.__name__
+
+
+# ------------------------------------------------- multi-token decode ---- #
+
+def _mt_inputs(B, T, H, P, lens, seed):
+    rng = np.random.default_rng(seed)
+    maxp = max(1, -(-max(lens) // P))
+    npg = B * maxp
+    cache = O.f64_to_bf16_bits(rng.normal(0, 1, (npg, P, 576)))
+    table = rng.permutation(npg).astype(np.int32).reshape(B, maxp)
+    W_UK = _bf16(rng.normal(0, 0.05, (H, 128, 512)))
+    W_UV = _bf16(rng.normal(0, 0.05, (H, 128, 512)))
+    qn = _bf16(rng.normal(0, 1, (B, T, H, 128)))
+    qp = _bf16(rng.normal(0, 1, (B, T, H, 64)))
+    return cache, table, W_UK, W_UV, qn, qp
+
+
+def test_multi_token_single_query_is_decode():
+    cache, table, W_UK, W_UV, qn, qp = _mt_inputs(3, 1, 2, 16, [40, 1, 17], 21)
+    out, lse = O.decode_multi_token(qn, qp, cache, None, table, [40, 1, 17], W_UK, W_UV, 0.1, 16, False)
+    out1, lse1 = O.decode(qn[:, 0], qp[:, 0], cache, None, table, [40, 1, 17], W_UK, W_UV, 0.1, 16, False)
+    np.testing.assert_array_equal(out[:, 0], out1)
+    np.testing.assert_array_equal(lse[:, 0], lse1)
+
+
+@pytest.mark.parametrize("T,L", [(2, 2), (3, 9), (4, 33), (8, 20)])
+def test_multi_token_library_causal_lower_right(T, L):
+    """torch's scaled_dot_product_attention in fp64 with its own bottom-right
+    aligned causal mask (queries are the last T positions of the keys), on
+    explicitly expanded keys and values, must equal the oracle."""
+    from torch.nn.attention.bias import causal_lower_right
+    H, P = 2, 8
+    cache, table, W_UK, W_UV, qn, qp = _mt_inputs(1, T, H, P, [L], 40 + T * L)
+    scale = 1 / math.sqrt(192)
+    rows = O.gather_rows(cache, None, table, 0, L, P, False)
+    K = np.stack([np.concatenate([rows[:, :512] @ W_UK[h].T, rows[:, 512:]], axis=1) for h in range(H)])
+    V = np.stack([rows[:, :512] @ W_UV[h].T for h in range(H)])
+    Q = np.stack([np.concatenate([qn[0, :, h], qp[0, :, h]], axis=1) for h in range(H)])  # [H, T, 192]
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        torch.from_numpy(Q)[None], torch.from_numpy(K)[None], torch.from_numpy(V)[None],
+        attn_mask=causal_lower_right(T, L), scale=scale)[0].numpy()                          # [H, T, 128]
+    out, lse = O.decode_multi_token(qn, qp, cache, None, table, [L], W_UK, W_UV, scale, P, False)
+    np.testing.assert_allclose(out[0].transpose(1, 0, 2), ref, rtol=1e-10, atol=1e-14)
+    assert np.all(np.isfinite(lse))
+
+
+def test_multi_token_closed_forms():
+    T, H, P = 4, 2, 8
+    # T = L: the first query sees only token 0, so o = W^UV c_0 and lse = its score
+    cache, table, W_UK, W_UV, qn, qp = _mt_inputs(1, T, H, P, [T], 7)
+    out, lse = O.decode_multi_token(qn, qp, cache, None, table, [T], W_UK, W_UV, 0.3, P, False)
+    rows = O.gather_rows(cache, None, table, 0, T, P, False)
+    for h in range(H):
+        np.testing.assert_allclose(out[0, 0, h], W_UV[h] @ rows[0, :512], rtol=1e-12, atol=1e-15)
+        s0 = 0.3 * (qn[0, 0, h] @ (W_UK[h] @ rows[0, :512]) + qp[0, 0, h] @ rows[0, 512:])
+        assert lse[0, 0, h] == pytest.approx(s0, rel=1e-12, abs=1e-14)
+    # the last query sees the whole cache: single-token decode of the full sequence
+    cache, table, W_UK, W_UV, qn, qp = _mt_inputs(2, T, H, P, [37, 12], 8)
+    out, lse = O.decode_multi_token(qn, qp, cache, None, table, [37, 12], W_UK, W_UV, 0.3, P, False)
+    full, lfull = O.decode(qn[:, -1], qp[:, -1], cache, None, table, [37, 12], W_UK, W_UV, 0.3, P, False)
+    np.testing.assert_allclose(out[:, -1], full, rtol=1e-12, atol=1e-15)
+    np.testing.assert_allclose(lse[:, -1], lfull, rtol=1e-13)
+    # fewer cached tokens than queries: the queries below position 0 see nothing
+    cache, table, W_UK, W_UV, qn, qp = _mt_inputs(1, T, H, P, [2], 9)
+    out, lse = O.decode_multi_token(qn, qp, cache, None, table, [2], W_UK, W_UV, 0.3, P, False)
+    assert np.all(out[0, :2] == 0) and np.all(np.isneginf(lse[0, :2]))
+    assert np.all(np.isfinite(lse[0, 2:]))
+
+
+def test_multi_token_pins_catch_planted_mistakes(monkeypatch):
+    """An off-by-one in the visible length, or the top-left (not bottom-right)
+    alignment of the causal mask, planted in the oracle, must fail the
+    library pin."""
+    from torch.nn.attention.bias import causal_lower_right
+    T, L, H, P = 3, 11, 1, 8
+    cache, table, W_UK, W_UV, qn, qp = _mt_inputs(1, T, H, P, [L], 77)
+    rows = O.gather_rows(cache, None, table, 0, L, P, False)
+    K = np.concatenate([rows[:, :512] @ W_UK[0].T, rows[:, 512:]], axis=1)[None]
+    V = (rows[:, :512] @ W_UV[0].T)[None]
+    Q = np.concatenate([qn[0, :, 0], qp[0, :, 0]], axis=1)[None]
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        torch.from_numpy(Q)[None], torch.from_numpy(K)[None], torch.from_numpy(V)[None],
+        attn_mask=causal_lower_right(T, L), scale=0.2)[0, 0].numpy()
+    good = O.attend_unabsorbed
+
+    def off_by_one(qn_, qp_, r, wk, wv, sc):
+        return good(qn_, qp_, r[:-1], wk, wv, sc)
+
+    def top_left(qn_, qp_, r, wk, wv, sc):   # visible = t + 1 instead of L - T + t + 1
+        return good(qn_, qp_, r[:r.shape[0] - (L - T)], wk, wv, sc)
+
+    for bad in (off_by_one, top_left):
+        monkeypatch.setattr(O.mla_oracle, "attend_unabsorbed", bad)
+        out, _ = O.decode_multi_token(qn, qp, cache, None, table, [L], W_UK, W_UV, 0.2, P, False)
+        monkeypatch.setattr(O.mla_oracle, "attend_unabsorbed", good)
+        assert not np.allclose(out[0, :, 0], ref, rtol=1e-6), bad.__name__
