@@ -25,6 +25,7 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
+IDX_SETS = 4  # sparse workloads: top-k selections the steps cycle through
 METRIC = "MLA decode tokens/s and latent-cache HBM GB/s (fraction of 8 TB/s), 1×GB300"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
@@ -210,7 +211,11 @@ def cpu_baseline(w, inp, seconds):
             else:
                 cache, sz = W.bf16_to_bits(sub), None
         t_start = time.perf_counter()   # time the oracle itself, not the page gather
-        if w.q_len == 1:
+        if w.top_k:
+            idx = inp["token_indices"].cpu().numpy()
+            O.decode_sparse(qn, qp, cache, sz, tab, lens, idx, wk, wv, inp["scale"], w.page_size, w.int8,
+                            pairs=[(b, h) for h in range(w.heads)])
+        elif w.q_len == 1:
             O.decode(qn, qp, cache, sz, tab, lens, wk, wv, inp["scale"], w.page_size, w.int8,
                      pairs=[(b, h) for h in range(w.heads)])
         else:
@@ -218,7 +223,7 @@ def cpu_baseline(w, inp, seconds):
                                  triples=[(b, t, h) for t in range(w.q_len) for h in range(w.heads)])
         el += time.perf_counter() - t_start
         done += 1
-        tokens_attended += int(lens[b])
+        tokens_attended += int((inp["token_indices"][b] >= 0).sum()) if w.top_k else int(lens[b])
     return {"value": done * w.q_len / el, "unit": "tokens/s", "cores": cores, "kind": "oracle",
             "sample": f"{done} whole sequence(s) x {w.q_len} token(s) x {w.heads} heads of {w.name} "
                       f"({tokens_attended} cached tokens, "
@@ -260,21 +265,41 @@ def run_ours(args, rank, world):
     d_rows = mla.dims(H * T, w.page_size, int8=w.int8)
     auto = mla.auto_num_splits(d_rows if mla.check_dims(d_rows) == mla.MLA_OK else d, B)
     splits = args.num_splits if args.num_splits is not None else (W.num_splits_for(w, auto) or auto)
-    ws = torch.empty(mla.decode_multi_workspace_size(d, B, T, splits), dtype=torch.uint8, device=dev)
+    ws_bytes = (mla.decode_sparse_workspace_size(d, B, w.top_k, splits) if w.top_k
+                else mla.decode_multi_workspace_size(d, B, T, splits))
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     qshape = (B, H) if T == 1 else (B, T, H)
     out = torch.empty(qshape + (128,), dtype=torch.bfloat16, device=dev)
     lse = torch.empty(qshape, dtype=torch.float32, device=dev)
-    decode_fn = mla.decode if T == 1 else mla.decode_multi
     q_nope, q_pe, W_UK, W_UV = inp["q_nope"], inp["q_pe"], inp["W_UK"], inp["W_UV"]
     seq_lens = seq_lens.to(dev)
+    token_indices = inp.get("token_indices")
+    # sparse: the selection changes every step, cycling through kIdxSets seeded
+    # top-k sets (their rows together exceed L2, so no step finds its rows left
+    # there by the step before)
+    idx_sets = [token_indices]
+    if w.top_k:
+        idx_sets += [W.draw_token_indices(inp["seq_lens"].cpu(), w.top_k, 1.0, W.generator(w.seed + 2000 + r, dev)).to(dev)
+                     for r in range(1, IDX_SETS)]
 
-    def step():
+    def decode_fn(qn, qp, tab, lens, idx, o, l):
+        """The workload's decode call: mla_decode, mla_decode_multi or mla_decode_sparse."""
+        if w.top_k:
+            mla.decode_sparse(d, qn, qp, cache, sz, tab, lens, idx, W_UK, W_UV, inp["scale"], num_splits=splits,
+                              workspace=ws, out=o, lse_out=l)
+        elif T == 1:
+            mla.decode(d, qn, qp, cache, sz, tab, lens, W_UK, W_UV, inp["scale"], num_splits=splits, workspace=ws,
+                       out=o, lse_out=l)
+        else:
+            mla.decode_multi(d, qn, qp, cache, sz, tab, lens, W_UK, W_UV, inp["scale"], num_splits=splits,
+                             workspace=ws, out=o, lse_out=l)
+
+    def step(i):
         mla.cache_append(d, cache, sz, table, seq_ids, positions, new_c, new_k, w.rope_theta)
-        decode_fn(d, q_nope, q_pe, cache, sz, table, seq_lens, W_UK, W_UV, inp["scale"], num_splits=splits,
-                  workspace=ws, out=out, lse_out=lse)
+        decode_fn(q_nope, q_pe, table, seq_lens, idx_sets[i % len(idx_sets)], out, lse)
 
-    for _ in range(args.warmup):
-        step()
+    for i in range(args.warmup):
+        step(i)
     torch.cuda.synchronize()
     assert mla.read_device_status(ws) == mla.MLA_OK
     # attention-kernel timing through the library's event hook, one pair per step
@@ -291,14 +316,14 @@ def run_ours(args, rank, world):
         # between two kernels would end the overlap of their launches)
         e0.record()
         for i in range(args.steps):
-            step()
+            step(i)
         e1.record()
         torch.cuda.synchronize()
         # then K more steps with the library's event pair around the attention
         # launch: that kernel's own duration for the roofline
         for i in range(args.steps):
             mla.set_timing_events(*kev[i])
-            step()
+            step(i)
         torch.cuda.synchronize()
     mla.set_timing_events(None, None)
     if world > 1:
@@ -307,7 +332,8 @@ def run_ours(args, rank, world):
     kern_ms = statistics.mean(a.elapsed_time(b) for a, b in kev)
     ms_total = max_over_ranks(ms_total, world)
     ms = ms_total / args.steps
-    lens_sum = int(seq_lens.to(torch.int64).sum())
+    # tokens the attention reads: every cached one, or the selected ones (sparse)
+    lens_sum = int((token_indices >= 0).sum()) if w.top_k else int(seq_lens.to(torch.int64).sum())
     bytes_per_token = 584 if w.int8 else 1152
     cache_bytes = lens_sum * bytes_per_token
     tokens_per_s = whole_job_rate(B * T, world, ms)
@@ -317,27 +343,33 @@ def run_ours(args, rank, world):
     # step's inputs sit in one pinned staging buffer and go over in one copy;
     # the library writes out and lse into one device buffer that comes back in
     # one copy (every byte of the step's inputs and results still crosses).
-    h_in_buf, d_in_buf, _, d_in = staging(dict(q_nope=q_nope, q_pe=q_pe, new_c=new_c, new_k=new_k, seq_ids=seq_ids,
-                                               positions=positions, table=table, seq_lens=seq_lens), dev)
+    step_inputs = dict(q_nope=q_nope, q_pe=q_pe, new_c=new_c, new_k=new_k, seq_ids=seq_ids, positions=positions,
+                       table=table, seq_lens=seq_lens)
+    h_bufs = []
+    for r in range(len(idx_sets)):
+        if w.top_k:
+            step_inputs["token_indices"] = idx_sets[r]
+        h_in_buf, d_in_buf, _, d_in = staging(step_inputs, dev)
+        h_bufs.append(h_in_buf)
     h_out_buf, d_out_buf, _, d_out = staging(dict(out=out, lse=lse), dev)
     h2d = h_in_buf.numel()
     d2h = h_out_buf.numel()
 
-    def e2e_step():
-        d_in_buf.copy_(h_in_buf, non_blocking=True)
+    def e2e_step(i):
+        d_in_buf.copy_(h_bufs[i % len(h_bufs)], non_blocking=True)
         mla.cache_append(d, cache, sz, d_in["table"], d_in["seq_ids"], d_in["positions"], d_in["new_c"],
                          d_in["new_k"], w.rope_theta)
-        decode_fn(d, d_in["q_nope"], d_in["q_pe"], cache, sz, d_in["table"], d_in["seq_lens"], W_UK, W_UV,
-                  inp["scale"], num_splits=splits, workspace=ws, out=d_out["out"], lse_out=d_out["lse"])
+        decode_fn(d_in["q_nope"], d_in["q_pe"], d_in["table"], d_in["seq_lens"], d_in.get("token_indices"),
+                  d_out["out"], d_out["lse"])
         h_out_buf.copy_(d_out_buf, non_blocking=True)
 
-    for _ in range(args.warmup):
-        e2e_step()
+    for i in range(args.warmup):
+        e2e_step(i)
     torch.cuda.synchronize()
     x0, x1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     x0.record()
-    for _ in range(args.steps):
-        e2e_step()
+    for i in range(args.steps):
+        e2e_step(i)
     x1.record()
     torch.cuda.synchronize()
     e2e_ms = x0.elapsed_time(x1) / args.steps
@@ -352,9 +384,12 @@ def run_ours(args, rank, world):
         "scaling": "weak", "vs_baseline": None, "dtype": "int8" if w.int8 else "bf16",
         "data": "synthetic (seeded; random-init weights of DeepSeek-V2 MLA shapes)",
         "config": {"workload": w.name, "batch": B, "heads": H, "context": w.context, "page_size": w.page_size,
-                   "q_len": T, "num_splits": splits, "cache_bytes": cache_bytes,
-                   "l2": "inputs larger than L2 (no flush): the cache read each step exceeds the 126 MB L2"
-                   if cache_bytes > 200e6 else "cache smaller than L2",
+                   "q_len": T, "top_k": w.top_k or None, "num_splits": splits, "cache_bytes": cache_bytes,
+                   "l2": ("inputs larger than L2 (no flush): each step reads one of "
+                          f"{len(idx_sets)} top-k selections, {len(idx_sets) * cache_bytes / 1e6:.0f} MB of rows together"
+                          if w.top_k else
+                          "inputs larger than L2 (no flush): the cache read each step exceeds the 126 MB L2"
+                          if cache_bytes > 200e6 else "cache smaller than L2"),
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "cache_gbs": round(step_cache_gbs, 1),
         "frac_of_8tbs": round(step_cache_gbs / NOMINAL_HBM_GBS, 4),
@@ -365,7 +400,7 @@ def run_ours(args, rank, world):
                      "algorithmic_bytes_per_launch": cache_bytes},
         "e2e": {"value": round(whole_job_rate(B * T, world, e2e_ms), 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 5)},
-        "gpu_launches": 4 * args.steps,
+        "gpu_launches": (5 if w.top_k else 4) * args.steps,  # + the gather kernel for sparse decode
         "clocks": clk.summary(),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -214,6 +214,45 @@ int mla_decode_multi(const mla_dims* dims, const void* q_nope, const void* q_pe,
                      void* workspace, size_t workspace_bytes, void* out, float* lse_out,
                      mla_stream_t stream);
 
+/* Largest index-list length mla_decode_sparse accepts. */
+#define MLA_MAX_TOP_K (1 << 20)
+
+/* Bytes of workspace mla_decode_sparse needs for (dims, batch, top_k,
+ * num_splits); 0 if the arguments are invalid. */
+size_t mla_decode_sparse_workspace_size(const mla_dims* dims, int32_t batch, int32_t top_k, int32_t num_splits);
+
+/*
+ * mla_decode_sparse -- decode against a selection of each sequence's cached
+ * tokens: the attention of DeepSeek Sparse Attention on MLA ("Seven Ways LLMs
+ * Handle Attention", section 6, "Sparse attention: keep every token, read
+ * only some": the whole cache stays, and each new token attends only to the
+ * top-k tokens an indexer picked).  The indexer is not part of this library:
+ * the caller passes its choice.
+ *
+ *   token_indices  int32 [batch, top_k] (device): positions in sequence b's
+ *                  cache, each in [0, seq_lens[b]); -1 entries are padding.
+ *                  The attention of (b, h) runs over the rows at the listed
+ *                  positions, each listed entry once (a position listed
+ *                  twice counts twice).  Other values raise
+ *                  MLA_ERR_DEVICE_BOUNDS and the entry is skipped.
+ *   top_k          1 .. MLA_MAX_TOP_K
+ *   workspace      at least mla_decode_sparse_workspace_size(dims, batch,
+ *                  top_k, num_splits) bytes; its first 4 bytes hold the
+ *                  device status of this call.
+ * Everything else is as for mla_decode (q_len = 1).  A sequence with no
+ * valid entry gets out = 0, lse = -inf.  Listing every position 0 ..
+ * seq_lens[b] - 1 in order gives exactly mla_decode's result.  The selected
+ * rows are first copied, in list order, into pages inside the workspace
+ * (about top_k * 1,152 bytes per sequence for bf16 caches), which the decode
+ * then reads.
+ */
+int mla_decode_sparse(const mla_dims* dims, const void* q_nope, const void* q_pe, const void* cache,
+                      const float* cache_scale_zero, int32_t num_pages, const int32_t* block_table,
+                      int32_t max_pages_per_seq, const int32_t* seq_lens, int32_t batch,
+                      const int32_t* token_indices, int32_t top_k, const void* W_UK, const void* W_UV,
+                      float softmax_scale, int32_t num_splits, void* workspace, size_t workspace_bytes,
+                      void* out, float* lse_out, mla_stream_t stream);
+
 /* Size of the fixed scratch array used by mla_decode_no_alloc. */
 #define MLA_NO_ALLOC_WORKSPACE_BYTES (16u << 20)
 

@@ -18,10 +18,11 @@ from . import build as _build
 
 __all__ = [
     "MLAError", "Dims", "dims", "load_library", "check_dims", "cache_append", "auto_num_splits",
-    "decode_workspace_size", "decode", "decode_multi_workspace_size", "decode_multi", "decode_no_alloc", "combine", "read_device_status", "read_status_word",
+    "decode_workspace_size", "decode", "decode_multi_workspace_size", "decode_multi", "decode_sparse_workspace_size",
+    "decode_sparse", "decode_no_alloc", "combine", "read_device_status", "read_status_word",
     "set_timing_events", "status_string", "version",
     "MLA_OK", "MLA_ERR_INVALID_ARG", "MLA_ERR_UNSUPPORTED", "MLA_ERR_WORKSPACE", "MLA_ERR_CUDA",
-    "MLA_ERR_DEVICE_TIMEOUT", "MLA_ERR_DEVICE_BOUNDS", "MLA_CACHE_BF16", "MLA_CACHE_INT8", "MAX_Q_LEN",
+    "MLA_ERR_DEVICE_TIMEOUT", "MLA_ERR_DEVICE_BOUNDS", "MLA_CACHE_BF16", "MLA_CACHE_INT8", "MAX_Q_LEN", "MAX_TOP_K",
 ]
 
 MLA_OK = 0
@@ -34,6 +35,7 @@ MLA_ERR_DEVICE_BOUNDS = -6
 MLA_CACHE_BF16 = 0
 MLA_CACHE_INT8 = 1
 MAX_Q_LEN = 8  # MLA_MAX_Q_LEN in include/mla.h
+MAX_TOP_K = 1 << 20  # MLA_MAX_TOP_K in include/mla.h
 
 # every function include/mla.h declares
 EXPORTED_SYMBOLS = (
@@ -41,6 +43,7 @@ EXPORTED_SYMBOLS = (
     "mla_decode", "mla_combine", "mla_read_device_status", "mla_read_status_word",
     "mla_status_string", "mla_set_timing_events", "mla_version", "mla_decode_no_alloc",
     "mla_test_inject_wait_timeout", "mla_decode_multi_workspace_size", "mla_decode_multi",
+    "mla_decode_sparse_workspace_size", "mla_decode_sparse",
 )
 NO_ALLOC_WORKSPACE_BYTES = 16 << 20  # MLA_NO_ALLOC_WORKSPACE_BYTES in include/mla.h
 
@@ -91,6 +94,9 @@ def load_library(build_if_missing: bool = False, path: str | None = None):
         "mla_decode_multi_workspace_size": (ctypes.c_size_t, [DP, _I, _I, _I]),
         "mla_decode_multi": (_I, [DP, _P, _P, _P, _P, _I, _P, _I, _P, _I, _I, _P, _P, ctypes.c_float, _I, _P,
                                   ctypes.c_size_t, _P, _P, _P]),
+        "mla_decode_sparse_workspace_size": (ctypes.c_size_t, [DP, _I, _I, _I]),
+        "mla_decode_sparse": (_I, [DP, _P, _P, _P, _P, _I, _P, _I, _P, _I, _P, _I, _P, _P, ctypes.c_float, _I, _P,
+                                   ctypes.c_size_t, _P, _P, _P]),
         "mla_decode_no_alloc": (_I, [DP, _P, _P, _P, _P, _I, _P, _I, _P, _I, _P, _P, ctypes.c_float, _I, _P, _P,
                                      _P, _P]),
         "mla_combine": (_I, [DP, _P, _P, _I, _I, _P, _P, _P]),
@@ -245,6 +251,42 @@ def decode_multi(d: Dims, q_nope, q_pe, cache, scale_zero, block_table, seq_lens
         _ptr(workspace, None, "workspace", dev), workspace.numel() * workspace.element_size(),
         _ptr(out, torch.bfloat16, "out", dev), _ptr(lse_out, torch.float32, "lse_out", dev), _stream(stream))
     _check(st, "mla_decode_multi")
+    return out, lse_out
+
+
+def decode_sparse_workspace_size(d: Dims, batch: int, top_k: int, num_splits: int = 0) -> int:
+    n = _L().mla_decode_sparse_workspace_size(ctypes.byref(d), int(batch), int(top_k), int(num_splits))
+    if n == 0:
+        raise MLAError(MLA_ERR_INVALID_ARG, "mla_decode_sparse_workspace_size")
+    return n
+
+
+def decode_sparse(d: Dims, q_nope, q_pe, cache, scale_zero, block_table, seq_lens, token_indices, W_UK, W_UV,
+                  softmax_scale: float, num_splits: int = 0, workspace: torch.Tensor | None = None,
+                  out: torch.Tensor | None = None, lse_out: torch.Tensor | None = None, want_lse: bool = True,
+                  stream=None):
+    """mla_decode_sparse: attention over the listed positions of each sequence
+    (token_indices int32 [B, top_k], -1 = padding).  Returns (out bf16
+    [B, H, 128], lse fp32 [B, H] or None)."""
+    int8 = d.cache_dtype == MLA_CACHE_INT8
+    B, K = token_indices.shape
+    dev = q_nope.device
+    if workspace is None:
+        workspace = torch.empty(decode_sparse_workspace_size(d, B, K, num_splits), dtype=torch.uint8, device=dev)
+    if out is None:
+        out = torch.empty((B, d.num_heads, d.v_head_dim), dtype=torch.bfloat16, device=dev)
+    if lse_out is None and want_lse:
+        lse_out = torch.empty((B, d.num_heads), dtype=torch.float32, device=dev)
+    st = _L().mla_decode_sparse(
+        ctypes.byref(d), _ptr(q_nope, torch.bfloat16, "q_nope"), _ptr(q_pe, torch.bfloat16, "q_pe", dev),
+        _ptr(cache, torch.int8 if int8 else torch.bfloat16, "cache", dev),
+        _ptr(scale_zero, torch.float32, "scale_zero", dev) if int8 else None, cache.shape[0],
+        _ptr(block_table, torch.int32, "block_table", dev), block_table.shape[1],
+        _ptr(seq_lens, torch.int32, "seq_lens", dev), B, _ptr(token_indices, torch.int32, "token_indices", dev), K,
+        _ptr(W_UK, torch.bfloat16, "W_UK", dev), _ptr(W_UV, torch.bfloat16, "W_UV", dev), float(softmax_scale),
+        int(num_splits), _ptr(workspace, None, "workspace", dev), workspace.numel() * workspace.element_size(),
+        _ptr(out, torch.bfloat16, "out", dev), _ptr(lse_out, torch.float32, "lse_out", dev), _stream(stream))
+    _check(st, "mla_decode_sparse")
     return out, lse_out
 
 

@@ -24,7 +24,7 @@ __device__ void compute_plan(const AbsorbParams& p) {
   __shared__ int carry;
   if (threadIdx.x == 0) {
     carry = 0;
-    *p.status = MLA_OK;
+    if (p.reset_status) *p.status = MLA_OK;
   }
   __syncthreads();
   // pass 1: checked lengths, tiles per sequence, prefix sums -> tile_start

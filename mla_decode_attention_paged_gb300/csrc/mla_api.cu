@@ -54,6 +54,12 @@ int effective_splits(const mla_dims* d, int num_splits) {
   return n / groups > 0 ? n / groups : 1;
 }
 
+int decode_rows(const mla_dims* d, const void* q_nope, const void* q_pe, const void* cache,
+                const float* cache_scale_zero, int32_t num_pages, const int32_t* block_table,
+                int32_t max_pages_per_seq, const int32_t* seq_lens, int32_t batch, int32_t q_len, const void* W_UK,
+                const void* W_UV, float softmax_scale, int32_t num_splits, void* workspace, size_t workspace_bytes,
+                void* out, float* lse_out, mla_stream_t stream, bool reset_status);
+
 }  // namespace
 
 extern "C" {
@@ -157,6 +163,22 @@ int mla_decode_multi(const mla_dims* d, const void* q_nope, const void* q_pe, co
                      int32_t max_pages_per_seq, const int32_t* seq_lens, int32_t batch, int32_t q_len,
                      const void* W_UK, const void* W_UV, float softmax_scale, int32_t num_splits, void* workspace,
                      size_t workspace_bytes, void* out, float* lse_out, mla_stream_t stream) {
+  return decode_rows(d, q_nope, q_pe, cache, cache_scale_zero, num_pages, block_table, max_pages_per_seq, seq_lens,
+                     batch, q_len, W_UK, W_UV, softmax_scale, num_splits, workspace, workspace_bytes, out, lse_out,
+                     stream, true);
+}
+
+}  // extern "C"
+
+namespace {
+
+// mla_decode_multi; reset_status = false leaves the status word as a kernel
+// earlier in the same call (the sparse gather) set it.
+int decode_rows(const mla_dims* d, const void* q_nope, const void* q_pe, const void* cache,
+                const float* cache_scale_zero, int32_t num_pages, const int32_t* block_table,
+                int32_t max_pages_per_seq, const int32_t* seq_lens, int32_t batch, int32_t q_len, const void* W_UK,
+                const void* W_UV, float softmax_scale, int32_t num_splits, void* workspace, size_t workspace_bytes,
+                void* out, float* lse_out, mla_stream_t stream, bool reset_status) {
   int st = mla_check_dims(d);
   if (st != MLA_OK) return st;
   const bool int8 = d->cache_dtype == MLA_CACHE_INT8;
@@ -195,6 +217,7 @@ int mla_decode_multi(const mla_dims* d, const void* q_nope, const void* q_pe, co
   ap.batch = batch;
   ap.heads = H;
   ap.heads_w = d->num_heads;
+  ap.reset_status = reset_status ? 1 : 0;
   ap.max_len = max_pages_per_seq * d->page_size;
   ap.num_splits = S;
   if (launch_absorb(ap, int8, s) != cudaSuccess) return MLA_ERR_CUDA;
@@ -250,6 +273,92 @@ int mla_decode_multi(const mla_dims* d, const void* q_nope, const void* q_pe, co
   cp.heads_w = d->num_heads;
   if (launch_combine_uv(cp, s) != cudaSuccess) return MLA_ERR_CUDA;
   return MLA_OK;
+}
+
+// Workspace of mla_decode_sparse: the decode's own workspace first (so that
+// the call's status word is the workspace's first 4 bytes), then the
+// gathered cache [batch * pps pages, P, 576] (+ INT8 scale/zero), its page
+// table [batch, pps] and lengths [batch]; pps = ceil(top_k / P).
+struct SparseLayout {
+  size_t decode, cache, scale_zero, table, lens, total;
+  int pps;
+};
+
+SparseLayout sparse_layout(const mla_dims* d, int batch, int top_k, size_t decode_bytes) {
+  SparseLayout L;
+  const bool int8 = d->cache_dtype == MLA_CACHE_INT8;
+  L.pps = (top_k + d->page_size - 1) / d->page_size;
+  const size_t rows = size_t(batch) * L.pps * d->page_size;
+  size_t off = 0;
+  L.decode = off;      off = align256(off + decode_bytes);
+  L.cache = off;       off = align256(off + rows * (int8 ? 576 : 1152));
+  L.scale_zero = off;  off = align256(off + (int8 ? rows * 8 : 0));
+  L.table = off;       off = align256(off + size_t(batch) * L.pps * 4);
+  L.lens = off;        off = align256(off + size_t(batch) * 4);
+  L.total = off;
+  return L;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t mla_decode_sparse_workspace_size(const mla_dims* d, int32_t batch, int32_t top_k, int32_t num_splits) {
+  if (top_k < 1 || top_k > MLA_MAX_TOP_K) return 0;
+  const size_t dec = mla_decode_workspace_size(d, batch, num_splits);
+  if (dec == 0) return 0;
+  return sparse_layout(d, batch, top_k, dec).total;
+}
+
+int mla_decode_sparse(const mla_dims* d, const void* q_nope, const void* q_pe, const void* cache,
+                      const float* cache_scale_zero, int32_t num_pages, const int32_t* block_table,
+                      int32_t max_pages_per_seq, const int32_t* seq_lens, int32_t batch,
+                      const int32_t* token_indices, int32_t top_k, const void* W_UK, const void* W_UV,
+                      float softmax_scale, int32_t num_splits, void* workspace, size_t workspace_bytes, void* out,
+                      float* lse_out, mla_stream_t stream) {
+  int st = mla_check_dims(d);
+  if (st != MLA_OK) return st;
+  const bool int8 = d->cache_dtype == MLA_CACHE_INT8;
+  if (batch <= 0 || num_pages <= 0 || max_pages_per_seq <= 0 || num_splits < 0) return MLA_ERR_INVALID_ARG;
+  if (top_k < 1 || top_k > MLA_MAX_TOP_K || !token_indices || !aligned(token_indices, 4)) return MLA_ERR_INVALID_ARG;
+  if (!cache || !block_table || !seq_lens || (int8 && !cache_scale_zero)) return MLA_ERR_INVALID_ARG;
+  if (!aligned(cache, 16) || !aligned(block_table, 4) || !aligned(seq_lens, 4) ||
+      (int8 && !aligned(cache_scale_zero, 8)))
+    return MLA_ERR_INVALID_ARG;
+  if ((long long)max_pages_per_seq * d->page_size > (1LL << 31) - 1) return MLA_ERR_INVALID_ARG;
+  if ((long long)num_pages * d->page_size > (1LL << 31) - 1) return MLA_ERR_INVALID_ARG;
+  const size_t dec = mla_decode_workspace_size(d, batch, num_splits);
+  if (dec == 0) return MLA_ERR_CUDA;
+  const SparseLayout L = sparse_layout(d, batch, top_k, dec);
+  if ((long long)batch * L.pps * d->page_size > (1LL << 31) - 1) return MLA_ERR_INVALID_ARG;
+  if (!workspace || !aligned(workspace, 256) || workspace_bytes < L.total) return MLA_ERR_WORKSPACE;
+  char* ws = static_cast<char*>(workspace);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // the call's status word starts at MLA_OK before the gather can report into it
+  int* status = reinterpret_cast<int*>(ws + L.decode + workspace_layout(batch, d->num_heads, 1).status);
+  if (cudaMemsetAsync(status, 0, sizeof(int), s) != cudaSuccess) return MLA_ERR_CUDA;
+  GatherParams gp;
+  gp.cache = cache;
+  gp.scale_zero = cache_scale_zero;
+  gp.block_table = block_table;
+  gp.seq_lens = seq_lens;
+  gp.indices = token_indices;
+  gp.out_cache = ws + L.cache;
+  gp.out_scale_zero = int8 ? reinterpret_cast<float*>(ws + L.scale_zero) : nullptr;
+  gp.out_table = reinterpret_cast<int*>(ws + L.table);
+  gp.out_lens = reinterpret_cast<int*>(ws + L.lens);
+  gp.status = status;
+  gp.batch = batch;
+  gp.top_k = top_k;
+  gp.max_pages = max_pages_per_seq;
+  gp.num_pages = num_pages;
+  gp.page_size = d->page_size;
+  gp.pages_per_seq = L.pps;
+  if (launch_gather(gp, int8, s) != cudaSuccess) return MLA_ERR_CUDA;
+  // the dense decode over the gathered rows, with the lengths the gather wrote
+  return decode_rows(d, q_nope, q_pe, gp.out_cache, gp.out_scale_zero, batch * L.pps, gp.out_table, L.pps,
+                     gp.out_lens, batch, 1, W_UK, W_UV, softmax_scale, num_splits, ws + L.decode, dec, out, lse_out,
+                     stream, false);
 }
 
 int mla_combine(const mla_dims* d, const float* partial_o, const float* partial_lse, int32_t batch,

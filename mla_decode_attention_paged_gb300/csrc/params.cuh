@@ -25,6 +25,24 @@ struct AbsorbParams {
   int* len_checked;
   int* status;
   int batch, heads, heads_w, max_len, num_splits;
+  int reset_status;  // 1: the plan starts the call's status word at MLA_OK (0: a kernel before it did)
+};
+
+// Sparse (top-k) decode: the listed rows of each sequence, compacted in list
+// order into pages_per_seq pages of the gathered cache (sequence b owns pages
+// [b pages_per_seq, (b + 1) pages_per_seq)), its length and page-table row.
+struct GatherParams {
+  const void* cache;         // bf16 or int8 [num_pages, P, 576]
+  const float* scale_zero;   // [num_pages, P, 2] (INT8)
+  const int* block_table;    // [B, max_pages]
+  const int* seq_lens;       // [B]
+  const int* indices;        // [B, top_k], -1 = padding
+  void* out_cache;           // [B * pages_per_seq, P, 576]
+  float* out_scale_zero;     // [B * pages_per_seq, P, 2] (INT8)
+  int* out_table;            // [B, pages_per_seq]
+  int* out_lens;             // [B]
+  int* status;               // MLA_ERR_DEVICE_BOUNDS for bad entries (zeroed on the stream before the launch)
+  int batch, top_k, max_pages, num_pages, page_size, pages_per_seq;
 };
 
 struct AppendParams {
@@ -65,6 +83,7 @@ cudaError_t launch_absorb(const AbsorbParams& p, bool fp16_out, cudaStream_t str
 cudaError_t launch_append(const AppendParams& p, bool int8, cudaStream_t stream);
 cudaError_t launch_combine_uv(const CombineUVParams& p, cudaStream_t stream);
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream);
+cudaError_t launch_gather(const GatherParams& p, bool int8, cudaStream_t stream);
 cudaError_t launch_decode_tc(const DecodeParams& p, int hc, bool int8, int grid, cudaStream_t stream);
 int decode_head_group(int heads, bool int8);
 // Launches `kernel` with programmatic dependent launch (and, if cluster_x > 1,

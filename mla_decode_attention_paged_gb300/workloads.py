@@ -40,6 +40,7 @@ class Workload:
     min_splits_per_seq: int = 0     # the workload asks for at least this many KV chunks per sequence
     rope_theta: float = 10000.0     # used where the cache is built through the append
     q_len: int = 1                  # query tokens per sequence (multi-token decode: the last q_len cached)
+    top_k: int = 0                  # sparse decode: attend to top_k drawn positions per sequence (0: all)
 
     @property
     def softmax_scale(self) -> float:
@@ -62,6 +63,9 @@ WORKLOADS = {
                             q_len=2),
     "v2lite_mtp4": Workload("v2lite_mtp4_b32_t4_h16_l32768_p64", 32, 16, 32768, 64, True, 1.0, 0.02, 1.0, 6,
                             q_len=4),
+    # sparse decode (DeepSeek Sparse Attention's top-2048 selection) over the V2-Lite cache
+    "v2lite_topk2048": Workload("v2lite_topk2048_b32_h16_l32768_p64", 32, 16, 32768, 64, True, 1.0, 0.02, 1.0, 7,
+                                top_k=2048),
 }
 
 
@@ -148,6 +152,8 @@ def make_decode_inputs(w: Workload, device="cpu"):
     qshape = (w.batch, w.heads) if w.q_len == 1 else (w.batch, w.q_len, w.heads)
     d["q_nope"] = draw_bf16(qshape + (NOPE_DIM,), w.q_std, g)
     d["q_pe"] = draw_bf16(qshape + (ROPE_DIM,), w.q_std, g)
+    if w.top_k:
+        d["token_indices"] = draw_token_indices(seq_lens.cpu(), w.top_k, 1.0, g).to(device)
     if w.int8:
         total = int(seq_lens.to(torch.int64).sum())
         d["src_c_kv"] = draw_bf16((total, LATENT_DIM), 1.0, g)
@@ -156,6 +162,20 @@ def make_decode_inputs(w: Workload, device="cpu"):
         d["src_seq_ids"] = torch.repeat_interleave(torch.arange(w.batch, dtype=torch.int32), lens).to(device)
         d["src_positions"] = torch.cat([torch.arange(int(n), dtype=torch.int32) for n in lens]).to(device)
     return d
+
+
+def draw_token_indices(seq_lens: torch.Tensor, top_k: int, fill: float, g: torch.Generator) -> torch.Tensor:
+    """A sparse-attention selection per sequence (int32 [B, top_k]): about
+    ``fill * top_k`` distinct positions below the sequence's length (all of
+    them if it is shorter), in random order, then -1 padding."""
+    B = seq_lens.numel()
+    out = torch.full((B, top_k), -1, dtype=torch.int32)
+    for b in range(B):
+        L = int(seq_lens[b])
+        n = min(L, max(1, int(round(fill * top_k)))) if L > 0 else 0
+        if n:
+            out[b, :n] = torch.randperm(L, generator=g, device=g.device)[:n].to(torch.int32).cpu()
+    return out
 
 
 def bf16_to_bits(t: torch.Tensor):

@@ -405,3 +405,36 @@ def decode_multi_token(q_nope: np.ndarray, q_pe: np.ndarray, cache: np.ndarray, 
             out[b, t, h] = o
             lse[b, t, h] = l
     return out, lse
+
+
+def decode_sparse(q_nope: np.ndarray, q_pe: np.ndarray, cache: np.ndarray, scale_zero: np.ndarray | None,
+                  block_table: np.ndarray, seq_lens: Sequence[int], token_indices: np.ndarray, W_UK: np.ndarray,
+                  W_UV: np.ndarray, scale: float, page_size: int, int8: bool, pairs=None, absorbed: bool = False):
+    """Sparse decode over a given selection of cached tokens ([P3] section 6,
+    "Sparse attention: keep every token, read only some": the full cache is
+    kept and each new token attends only to the top-k tokens an indexer
+    picked; the indexer itself is not part of this path).
+
+    token_indices [B, k] int: positions in sequence b's cache; -1 entries are
+    padding and are skipped.  The attention of (b, h) runs over the rows at
+    the listed positions, in list order, each listed entry once.
+    Returns (out [B, H, 128], lse [B, H]) in fp64; ``pairs`` as for decode.
+    """
+    B, H = q_nope.shape[0], q_nope.shape[1]
+    out = np.full((B, H, W_UV.shape[1]), np.nan)
+    lse = np.full((B, H), np.nan)
+    if pairs is None:
+        pairs = [(b, h) for b in range(B) for h in range(H)]
+    by_seq: dict[int, list[int]] = {}
+    for b, h in pairs:
+        by_seq.setdefault(int(b), []).append(int(h))
+    fn = attend_absorbed if absorbed else attend_unabsorbed
+    for b, heads in by_seq.items():
+        rows = gather_rows(cache, scale_zero, block_table, b, int(seq_lens[b]), page_size, int8)
+        chosen = [int(i) for i in np.asarray(token_indices[b]).ravel() if int(i) >= 0]
+        sel = rows[chosen] if chosen else rows[:0]
+        for h in heads:
+            o, l, _ = fn(q_nope[b, h], q_pe[b, h], sel, W_UK[h], W_UV[h], scale)
+            out[b, h] = o
+            lse[b, h] = l
+    return out, lse

@@ -117,3 +117,22 @@ def test_multi_token_workspace_and_validation(lib):
         assert lib.mla_decode_multi(*a) == mla.MLA_ERR_INVALID_ARG
     a = list(args); a[1] = None
     assert lib.mla_decode_multi(*a) == mla.MLA_ERR_INVALID_ARG
+
+
+def test_sparse_workspace_and_validation(lib):
+    d = mla.dims(16, 64)
+    dec = lib.mla_decode_workspace_size(ctypes.byref(d), 32, 76)
+    sp = lib.mla_decode_sparse_workspace_size(ctypes.byref(d), 32, 2048, 76)
+    assert sp >= dec + 32 * 2048 * 1152   # the decode's workspace plus the gathered rows
+    assert lib.mla_decode_sparse_workspace_size(ctypes.byref(d), 32, 0, 76) == 0
+    assert lib.mla_decode_sparse_workspace_size(ctypes.byref(d), 32, mla.MAX_TOP_K + 1, 76) == 0
+    fake = ctypes.c_void_p(0x10000)  # never dereferenced: validation fails first
+    args = [ctypes.byref(d), fake, fake, fake, None, 4, fake, 8, fake, 2, fake, 64, fake, fake, ctypes.c_float(0.1),
+            4, fake, ctypes.c_size_t(1 << 30), fake, None, None]
+    for bad_k in (0, -3, mla.MAX_TOP_K + 1):
+        a = list(args); a[11] = bad_k
+        assert lib.mla_decode_sparse(*a) == mla.MLA_ERR_INVALID_ARG
+    a = list(args); a[10] = None                      # no index list
+    assert lib.mla_decode_sparse(*a) == mla.MLA_ERR_INVALID_ARG
+    a = list(args); a[16] = ctypes.c_void_p(0x10010)  # workspace not 256-byte aligned
+    assert lib.mla_decode_sparse(*a) == mla.MLA_ERR_WORKSPACE

@@ -80,3 +80,25 @@ def test_full_size_multi_token(cuda_lib, key, seq):
     pairs = [(seq, v) for v in range(T * H)]
     assert_parity(out.reshape(B, T * H, -1), lse.reshape(B, T * H), ref_o.reshape(B, T * H, -1),
                   ref_l.reshape(B, T * H), pairs, w.name)
+
+
+def test_full_size_sparse_topk(cuda_lib):
+    """Sparse decode at the V2-Lite size with DeepSeek Sparse Attention's
+    top-2048 selection per sequence, in bench.py's configuration: every head
+    of two sampled sequences against the un-absorbed oracle."""
+    import oracle as O
+    from harness import f64
+    w = W.WORKLOADS["v2lite_topk2048"]
+    inp = W.make_decode_inputs(w, device="cuda")
+    d = dims_of(w)
+    out, lse = mla.decode_sparse(d, inp["q_nope"], inp["q_pe"], inp["cache"], None, inp["block_table"],
+                                 inp["seq_lens"], inp["token_indices"], inp["W_UK"], inp["W_UV"], inp["scale"],
+                                 num_splits=mla.auto_num_splits(d, w.batch))
+    torch.cuda.synchronize()
+    seqs = [4, 27]
+    cache, sz, table = oracle_cache(inp, w, seqs)
+    pairs = [(b, h) for b in seqs for h in range(w.heads)]
+    ref_o, ref_l = O.decode_sparse(f64(inp["q_nope"]), f64(inp["q_pe"]), cache, sz, table,
+                                   inp["seq_lens"].cpu().numpy(), inp["token_indices"].cpu().numpy(),
+                                   f64(inp["W_UK"]), f64(inp["W_UV"]), inp["scale"], w.page_size, False, pairs=pairs)
+    assert_parity(out, lse, ref_o, ref_l, pairs, w.name)

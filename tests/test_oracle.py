@@ -411,3 +411,75 @@ def test_multi_token_pins_catch_planted_mistakes(monkeypatch):
         out, _ = O.decode_multi_token(qn, qp, cache, None, table, [L], W_UK, W_UV, 0.2, P, False)
         monkeypatch.setattr(O.mla_oracle, "attend_unabsorbed", good)
         assert not np.allclose(out[0, :, 0], ref, rtol=1e-6), bad.__name__
+
+
+# ---------------------------------------------------- sparse (top-k) decode ---- #
+
+def test_sparse_all_positions_is_dense_decode():
+    cache, table, W_UK, W_UV, qn, qp = _mt_inputs(2, 1, 2, 16, [40, 17], 101)
+    idx = np.full((2, 40), -1)
+    idx[0] = np.arange(40)
+    idx[1, :17] = np.arange(17)
+    out, lse = O.decode_sparse(qn[:, 0], qp[:, 0], cache, None, table, [40, 17], idx, W_UK, W_UV, 0.1, 16, False)
+    ref, lref = O.decode(qn[:, 0], qp[:, 0], cache, None, table, [40, 17], W_UK, W_UV, 0.1, 16, False)
+    np.testing.assert_array_equal(out, ref)
+    np.testing.assert_array_equal(lse, lref)
+
+
+def test_sparse_library_masked_sdpa_and_order_invariance():
+    """Attending to a subset of positions is SDPA over all positions with the
+    unselected ones masked out (torch, fp64, boolean mask); the list order and
+    padding entries do not matter."""
+    H, L, P = 2, 50, 8
+    cache, table, W_UK, W_UV, qn, qp = _mt_inputs(1, 1, H, P, [L], 102)
+    rng = np.random.default_rng(5)
+    chosen = rng.choice(L, 13, replace=False)
+    idx = np.concatenate([chosen, [-1, -1, -1]])[None]
+    out, lse = O.decode_sparse(qn[:, 0], qp[:, 0], cache, None, table, [L], idx, W_UK, W_UV, 0.2, P, False)
+    rows = O.gather_rows(cache, None, table, 0, L, P, False)
+    K = np.stack([np.concatenate([rows[:, :512] @ W_UK[h].T, rows[:, 512:]], axis=1) for h in range(H)])
+    V = np.stack([rows[:, :512] @ W_UV[h].T for h in range(H)])
+    Q = np.concatenate([qn[0, 0], qp[0, 0]], axis=1)[:, None, :]
+    mask = np.zeros((1, L), bool)
+    mask[0, chosen] = True
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        torch.from_numpy(Q)[None], torch.from_numpy(K)[None], torch.from_numpy(V)[None],
+        attn_mask=torch.from_numpy(mask), scale=0.2)[0, :, 0].numpy()
+    np.testing.assert_allclose(out[0], ref, rtol=1e-10, atol=1e-14)
+    shuffled = np.concatenate([[-1], rng.permutation(chosen), [-1]])[None]
+    out2, lse2 = O.decode_sparse(qn[:, 0], qp[:, 0], cache, None, table, [L], shuffled, W_UK, W_UV, 0.2, P, False)
+    np.testing.assert_allclose(out2, out, rtol=1e-12, atol=1e-16)
+    np.testing.assert_allclose(lse2, lse, rtol=1e-13)
+    # nothing selected: o = 0, lse = -inf
+    o3, l3 = O.decode_sparse(qn[:, 0], qp[:, 0], cache, None, table, [L], np.full((1, 4), -1), W_UK, W_UV, 0.2, P,
+                             False)
+    assert np.all(o3 == 0) and np.all(np.isneginf(l3))
+
+
+def test_sparse_pins_catch_planted_off_by_one(monkeypatch):
+    """A gather that is off by one position, planted in the oracle, must fail
+    the masked-SDPA pin."""
+    H, L, P = 1, 30, 8
+    cache, table, W_UK, W_UV, qn, qp = _mt_inputs(1, 1, H, P, [L], 103)
+    chosen = np.array([3, 17, 9, 25])
+    rows = O.gather_rows(cache, None, table, 0, L, P, False)
+    K = np.concatenate([rows[:, :512] @ W_UK[0].T, rows[:, 512:]], axis=1)[None]
+    V = (rows[:, :512] @ W_UV[0].T)[None]
+    Q = np.concatenate([qn[0, 0], qp[0, 0]], axis=1)[:, None, :]
+    mask = np.zeros((1, L), bool)
+    mask[0, chosen] = True
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        torch.from_numpy(Q)[None], torch.from_numpy(K)[None], torch.from_numpy(V)[None],
+        attn_mask=torch.from_numpy(mask), scale=0.2)[0, :, 0].numpy()
+    good_gather = O.gather_rows
+
+    def shifted(*a, **k):  # row i holds token i + 1
+        r = good_gather(*a, **k)
+        return np.concatenate([r[1:], r[:1]])
+
+    monkeypatch.setattr(O.mla_oracle, "gather_rows", shifted)
+    bad, _ = O.decode_sparse(qn[:, 0], qp[:, 0], cache, None, table, [L], chosen[None], W_UK, W_UV, 0.2, P, False)
+    monkeypatch.setattr(O.mla_oracle, "gather_rows", good_gather)
+    good, _ = O.decode_sparse(qn[:, 0], qp[:, 0], cache, None, table, [L], chosen[None], W_UK, W_UV, 0.2, P, False)
+    np.testing.assert_allclose(good[0], ref, rtol=1e-10, atol=1e-14)
+    assert not np.allclose(bad[0], ref, rtol=1e-6)
