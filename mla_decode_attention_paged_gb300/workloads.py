@@ -63,6 +63,8 @@ WORKLOADS = {
                             q_len=2),
     "v2lite_mtp4": Workload("v2lite_mtp4_b32_t4_h16_l32768_p64", 32, 16, 32768, 64, True, 1.0, 0.02, 1.0, 6,
                             q_len=4),
+    # the V2-Lite batch over an INT8 cache (half the bytes per token)
+    "int8_v2lite": Workload("int8_v2lite_b32_h16_l32768_p64", 32, 16, 32768, 64, True, 1.0, 0.02, 1.0, 8, int8=True),
     # sparse decode (DeepSeek Sparse Attention's top-2048 selection) over the V2-Lite cache
     "v2lite_topk2048": Workload("v2lite_topk2048_b32_h16_l32768_p64", 32, 16, 32768, 64, True, 1.0, 0.02, 1.0, 7,
                                 top_k=2048),
