@@ -327,6 +327,13 @@ int mla_set_timing_events(mla_event_t start, mla_event_t stop);
  * (the default) disables it.  Returns MLA_OK. */
 int mla_test_inject_wait_timeout(int32_t enable);
 
+/* Test hook (no counterpart on the pages): while enabled (non-zero), bf16
+ * decodes use the single-CTA attention kernel that serves devices on which
+ * the CTA-pair kernel cannot be placed (the pair kernel runs otherwise), so
+ * that this fallback stays tested on devices that never need it.
+ * Process-wide; 0 (the default) disables it.  Returns MLA_OK. */
+int mla_test_force_single_cta(int32_t enable);
+
 /* Library version: major * 10000 + minor * 100 + patch. */
 int mla_version(void);
 

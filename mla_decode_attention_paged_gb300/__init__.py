@@ -43,7 +43,7 @@ EXPORTED_SYMBOLS = (
     "mla_decode", "mla_combine", "mla_read_device_status", "mla_read_status_word",
     "mla_status_string", "mla_set_timing_events", "mla_version", "mla_decode_no_alloc",
     "mla_test_inject_wait_timeout", "mla_decode_multi_workspace_size", "mla_decode_multi",
-    "mla_decode_sparse_workspace_size", "mla_decode_sparse",
+    "mla_decode_sparse_workspace_size", "mla_decode_sparse", "mla_test_force_single_cta",
 )
 NO_ALLOC_WORKSPACE_BYTES = 16 << 20  # MLA_NO_ALLOC_WORKSPACE_BYTES in include/mla.h
 
@@ -106,6 +106,7 @@ def load_library(build_if_missing: bool = False, path: str | None = None):
         "mla_set_timing_events": (_I, [_P, _P]),
         "mla_version": (ctypes.c_int, []),
         "mla_test_inject_wait_timeout": (_I, [_I]),
+        "mla_test_force_single_cta": (_I, [_I]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -349,6 +350,12 @@ def test_inject_wait_timeout(enable: bool) -> None:
     """Test hook: make the attention kernel's first page wait of each CTA unsatisfiable
     (it times out and the status word reports MLA_ERR_DEVICE_TIMEOUT)."""
     _check(_L().mla_test_inject_wait_timeout(1 if enable else 0), "mla_test_inject_wait_timeout")
+
+
+def test_force_single_cta(enable: bool) -> None:
+    """Test hook: run bf16 decodes on the single-CTA attention kernel (the
+    fallback for devices that cannot place CTA pairs)."""
+    _check(_L().mla_test_force_single_cta(1 if enable else 0), "mla_test_force_single_cta")
 
 
 def set_timing_events(start: torch.cuda.Event | None, stop: torch.cuda.Event | None) -> None:

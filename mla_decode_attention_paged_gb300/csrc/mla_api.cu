@@ -18,6 +18,7 @@ constexpr int kVersion = 100;  // 0.1.0
 
 std::atomic<cudaEvent_t> g_ev_start{nullptr}, g_ev_stop{nullptr};
 std::atomic<int> g_inject_wait_timeout{0};
+std::atomic<int> g_force_single_cta{0};
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -47,7 +48,7 @@ int effective_splits(const mla_dims* d, int num_splits) {
   if (num_splits > 0) return num_splits;
   const bool int8 = d->cache_dtype == MLA_CACHE_INT8;
   const int hc = decode_head_group(d->num_heads, int8);
-  const int clusters = int8 ? 0 : decode_pair_capacity(hc);
+  const int clusters = int8 || g_force_single_cta.load() ? 0 : decode_pair_capacity(hc);
   const int n = clusters > 0 ? clusters : sm_count();
   if (n <= 0) return -1;
   const int groups = d->num_heads / hc;
@@ -248,7 +249,7 @@ int decode_rows(const mla_dims* d, const void* q_nope, const void* q_pe, const v
   dp.inject_wait_timeout = g_inject_wait_timeout.load();
   // bf16 caches run on CTA pairs (two SMs share each tile); INT8 caches, and
   // devices that cannot place the pairs, on single CTAs
-  const int pair_cap = int8 ? 0 : decode_pair_capacity(hc);
+  const int pair_cap = int8 || g_force_single_cta.load() ? 0 : decode_pair_capacity(hc);
   const int units = pair_cap > 0 ? pair_cap : sm_count();
   const int per_group = units / groups > 0 ? units / groups : 1;
   const int per_group_used = S < per_group ? S : per_group;
@@ -393,6 +394,11 @@ int mla_read_status_word(const int32_t* device_status, int32_t* status_out, mla_
 int mla_read_device_status(const void* workspace, int32_t* status_out, mla_stream_t stream) {
   if (!workspace) return MLA_ERR_INVALID_ARG;
   return mla_read_status_word(static_cast<const int32_t*>(workspace), status_out, stream);
+}
+
+int mla_test_force_single_cta(int32_t enable) {
+  g_force_single_cta.store(enable != 0);
+  return MLA_OK;
 }
 
 int mla_test_inject_wait_timeout(int32_t enable) {
