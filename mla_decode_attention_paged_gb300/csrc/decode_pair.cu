@@ -123,7 +123,10 @@ __device__ __forceinline__ void fail(PairBarriers* B, int* status) {
   set_status(status, MLA_ERR_DEVICE_TIMEOUT);
 }
 
-template <int HC, int NC>
+// kCausal: multi-token decode (q_len > 1) masks the scores of each row's
+// later positions on a sequence's last tiles; single-token decode does not
+// carry the per-tile check.
+template <int HC, int NC, bool kCausal>
 __global__ void __launch_bounds__(kPairThreads, 1)
     decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_latent, const __grid_constant__ CUtensorMap tmap_rope,
                        const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_qrope,
@@ -444,7 +447,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
       }
 #pragma unroll
       for (int h = 0; h < HC; ++h) x[h] = valid ? x[h] * p.scale_log2 : -INFINITY;
-      if (causal_tile(p, t, walk.len_b)) causal_mask<HC>(x, p, g, walk.len_b, t.tile * kTile + st);
+      if (kCausal && causal_tile(p, t, walk.len_b)) causal_mask<HC>(x, p, g, walk.len_b, t.tile * kTile + st);
       // Running max: it only has to bound the scores to within
       // kRescaleThreshold (log2 units).  The first tile of a segment, and a
       // tile that breaks the bound, take the exact path (per-head tile max and,
@@ -599,13 +602,15 @@ cudaError_t launch_pair(const DecodeParams& p, int clusters_per_group, cudaStrea
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 128 || !attr[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(decode_pair_kernel<HC, NC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         int(C::kSmem));
-    if (e != cudaSuccess) return e;
+    for (auto* k : {decode_pair_kernel<HC, NC, false>, decode_pair_kernel<HC, NC, true>}) {
+      const cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, int(C::kSmem));
+      if (e != cudaSuccess) return e;
+    }
     if (dev >= 0 && dev < 128) attr[dev] = true;
   }
-  return launch_pdl(decode_pair_kernel<HC, NC>, dim3(NC * clusters_per_group * p.num_groups), dim3(kPairThreads),
-                    C::kSmem, stream, NC, ml, mr, mq, mqr, p);
+  auto* kernel = p.q_len > 1 ? decode_pair_kernel<HC, NC, true> : decode_pair_kernel<HC, NC, false>;
+  return launch_pdl(kernel, dim3(NC * clusters_per_group * p.num_groups), dim3(kPairThreads), C::kSmem, stream, NC,
+                    ml, mr, mq, mqr, p);
 }
 
 template <int HC, int NC>
@@ -614,7 +619,7 @@ int max_clusters() {  // clusters of NC that can be resident at once on this dev
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 128 && cached[dev] > 0) return cached[dev];
-  if (cudaFuncSetAttribute(decode_pair_kernel<HC, NC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (cudaFuncSetAttribute(decode_pair_kernel<HC, NC, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            int(PairCfg<HC, NC>::kSmem)) != cudaSuccess)
     return 0;
   cudaLaunchConfig_t cfg = {};
@@ -629,7 +634,7 @@ int max_clusters() {  // clusters of NC that can be resident at once on this dev
   cfg.attrs = at;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, decode_pair_kernel<HC, NC>, &cfg) != cudaSuccess || n <= 0) return 0;
+  if (cudaOccupancyMaxActiveClusters(&n, decode_pair_kernel<HC, NC, false>, &cfg) != cudaSuccess || n <= 0) return 0;
   if (dev >= 0 && dev < 128) cached[dev] = n;
   return n;
 }

@@ -173,7 +173,8 @@ __device__ __forceinline__ void expand_codes(uint4 v, uint4& lo, uint4& hi) {
   hi = make_uint4(o[4], o[5], o[6], o[7]);
 }
 
-template <int HC, bool kInt8>
+// kCausal: multi-token decode (q_len > 1) only, as in the pair kernel.
+template <int HC, bool kInt8, bool kCausal>
 __global__ void __launch_bounds__(Cfg<HC, kInt8>::kThreads, 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_cache, const __grid_constant__ CUtensorMap tmap_q,
                      DecodeParams p) {
@@ -592,7 +593,7 @@ __global__ void __launch_bounds__(Cfg<HC, kInt8>::kThreads, 1)
         const float raw = kInt8 ? fmaf(-tok_z, qsum[h], x[h]) : x[h];
         x[h] = valid ? raw * row_scale : -INFINITY;
       }
-      if (causal_tile(p, t, walk.len_b)) causal_mask<HC>(x, p, g, walk.len_b, t.tile * kTile + st);
+      if (kCausal && causal_tile(p, t, walk.len_b)) causal_mask<HC>(x, p, g, walk.len_b, t.tile * kTile + st);
       // Running max.  It only has to bound the scores to within
       // kRescaleThreshold (log2 units), so in the common case every thread
       // checks its own scores against it and the 128 threads OR that flag in
@@ -766,13 +767,15 @@ cudaError_t launch_tc(const DecodeParams& p, int grid, cudaStream_t stream) {
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 128 || !attr[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<HC, kInt8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         int(Cfg<HC, kInt8>::kSmem));
-    if (e != cudaSuccess) return e;
+    for (auto* k : {decode_tc_kernel<HC, kInt8, false>, decode_tc_kernel<HC, kInt8, true>}) {
+      const cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 int(Cfg<HC, kInt8>::kSmem));
+      if (e != cudaSuccess) return e;
+    }
     if (dev >= 0 && dev < 128) attr[dev] = true;
   }
-  return launch_pdl(decode_tc_kernel<HC, kInt8>, dim3(grid), dim3(Cfg<HC, kInt8>::kThreads), Cfg<HC, kInt8>::kSmem,
-                    stream, 1, mc, mq, p);
+  auto* kernel = p.q_len > 1 ? decode_tc_kernel<HC, kInt8, true> : decode_tc_kernel<HC, kInt8, false>;
+  return launch_pdl(kernel, dim3(grid), dim3(Cfg<HC, kInt8>::kThreads), Cfg<HC, kInt8>::kSmem, stream, 1, mc, mq, p);
 }
 
 }  // namespace
