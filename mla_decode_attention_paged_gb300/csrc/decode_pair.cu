@@ -193,14 +193,14 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     // warp 0 loads Q and the first half of every tile's latent boxes, warp 3
     // the second half and the RoPE columns.
     const int role = warp == 0 ? 0 : 1;
-    TileWalker walk;
+    TileWalkerT<true> walk;
     walk.init(p.tile_start, p.seg_base, p.len, p.batch, int(S), pa, pb);
     const uint32_t page_bytes = uint32_t(P) * 128, rope_page_bytes = uint32_t(P) * C::kRopeCols * 2;
     uint32_t pair_it = 0, rope_it = 0, seg = 0;
     TileInfo t, tn;
     // page ids two tiles ahead: tile k + 1's are in registers (and arrived)
     // when tile k starts, for the L2 prefetch; tile k + 2's are on their way
-    TileWalker look = walk;
+    TileWalkerT<true> look = walk;
     TilePages pages, next_pages, next2_pages;
     bool have_next = look.next(tn), have_next2 = false;
     if (have_next) next_pages.fetch(p, tn);
@@ -274,7 +274,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     // S_r^T[k & 1] = C_r * Q_r^T: this CTA's latent chunks (8 MMAs each) and
     // its RoPE columns (one MMA per 16).  Before overwriting S^T[k & 1] it waits for the softmax of
     // tile k - 2 (which read it) to finish.
-    TileWalker walk;
+    TileWalkerT<true> walk;
     walk.init(p.tile_start, p.seg_base, p.len, p.batch, int(S), pa, pb);
     constexpr uint32_t id_qk = idesc_f32acc(128, HC, false, false, false);
     constexpr uint64_t kDescK = smem_desc(0, 16, 1024, kSwizzle128B);   // K-major, 128-byte swizzle
@@ -323,7 +323,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     // ------------------------------------------------------------ PV issuer
     // O_r^T[c] (+)= C_r^T[128c .. 128c + 128) * P^T once the softmax of the
     // tile is done; each pair slot is released as soon as its MMAs complete.
-    TileWalker walk;
+    TileWalkerT<true> walk;
     walk.init(p.tile_start, p.seg_base, p.len, p.batch, int(S), pa, pb);
     constexpr uint32_t id_pv = idesc_f32acc(128, HC, true, true, false);
     constexpr uint64_t kDescMN = smem_desc(0, kBoxBytes, 1024, kSwizzle128B);  // MN-major, 128-byte swizzle
@@ -385,7 +385,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     // this thread's row of an exchange buffer; 16-byte pieces rotated by row to spread banks
     constexpr int kV4 = HC / 4;
     const uint32_t x_local = sbase + C::kOffX + st * HC * 4;
-    TileWalker walk;
+    TileWalkerT<true> walk;
     walk.init(p.tile_start, p.seg_base, p.len, p.batch, int(S), pa, pb);
     float m_run[HC], l_run[HC];
     uint32_t tile_i = 0, seg = 0;

@@ -80,7 +80,16 @@ struct TileInfo {
 // so that every partition is non-empty (partition starts strictly increase)
 // and the segments of a sequence are exactly the partitions its tiles touch.
 // Walks the units of one CTA: partitions [pa, pb) of the list.
-struct TileWalker {
+//
+// kInline = false keeps the rare paths (init and the boundary crossings, which
+// hold the 64-bit divisions) out of line so that each warp role's copy of the
+// walker stays small where instruction-cache space is tight; their `this`
+// argument then puts the walker in local memory, which every tile's next()
+// reads and writes.  kInline = true inlines everything, and the walker lives
+// in registers (the CTA-pair kernel: 2.7% faster on V2-Lite; the single-CTA
+// kernel's larger code runs slower that way).
+template <bool kInline>
+struct TileWalkerT {
   const int* tile_start;
   const int* seg_base;
   const int* len;
@@ -89,10 +98,8 @@ struct TileWalker {
   long long s_b, e_b;            // units of sequence b: [s_b, e_b)
   int b, len_b, seg_b;           // seg_b = first segment of sequence b minus its first partition
 
-  // init and the boundary crossings are rare and hold the 64-bit divisions:
-  // kept out of line so that each warp role's copy of the walker stays small
-  __device__ __noinline__ void init(const int* ts, const int* sb, const int* ln, int batch, int num_splits,
-                                    long long pa, long long pb) {
+  __device__ __forceinline__ void init_body(const int* ts, const int* sb, const int* ln, int batch, int num_splits,
+                                            long long pa, long long pb) {
     tile_start = ts;
     seg_base = sb;
     len = ln;
@@ -110,33 +117,47 @@ struct TileWalker {
       if (ts[mid + 1] <= u) lo = mid + 1; else hi = mid;
     }
     b = lo;
-    enter_sequence();
+    enter_sequence_body();
   }
-
-  __device__ __noinline__ void enter_sequence() {
+  __device__ __forceinline__ void enter_sequence_body() {
     s_b = tile_start[b];
     e_b = tile_start[b + 1];
     len_b = len[b];
     seg_b = seg_base[b] - int(part_of(s_b, W, S));
   }
-
-  __device__ __noinline__ void enter_partition() {
+  __device__ __forceinline__ void enter_partition_body() {
     while (p_next <= u) {
       ++p;
       p_start = p_next;
       p_next = part_start(p + 1, W, S);
     }
   }
+  __device__ __noinline__ void init_out_of_line(const int* ts, const int* sb, const int* ln, int batch,
+                                                int num_splits, long long pa, long long pb) {
+    init_body(ts, sb, ln, batch, num_splits, pa, pb);
+  }
+  __device__ __noinline__ void enter_sequence_out_of_line() { enter_sequence_body(); }
+  __device__ __noinline__ void enter_partition_out_of_line() { enter_partition_body(); }
+
+  __device__ __forceinline__ void init(const int* ts, const int* sb, const int* ln, int batch, int num_splits,
+                                       long long pa, long long pb) {
+    if constexpr (kInline) init_body(ts, sb, ln, batch, num_splits, pa, pb);
+    else init_out_of_line(ts, sb, ln, batch, num_splits, pa, pb);
+  }
 
   // Divisions only when a partition boundary is crossed; the plan's
   // arrays are read only when a sequence boundary is.
-  __device__ bool next(TileInfo& t) {
+  __device__ __forceinline__ bool next(TileInfo& t) {
     if (u >= u_end) return false;
     if (e_b <= u) {
       do ++b; while (tile_start[b + 1] <= u);
-      enter_sequence();
+      if constexpr (kInline) enter_sequence_body();
+      else enter_sequence_out_of_line();
     }
-    if (p_next <= u) enter_partition();
+    if (p_next <= u) {
+      if constexpr (kInline) enter_partition_body();
+      else enter_partition_out_of_line();
+    }
     t.b = b;
     t.tile = int(u - s_b);
     const int v = len_b - t.tile * kTile;
@@ -148,6 +169,7 @@ struct TileWalker {
     return true;
   }
 };
+using TileWalker = TileWalkerT<false>;
 
 struct DecodeParams {
   const __nv_bfloat16* q_full;   // [B, H, 576]
