@@ -95,6 +95,11 @@ __global__ void __launch_bounds__(kUVThreads, 1)
     tmem_alloc(tmem_slot, C::kTmemCols);
     tmem_relinquish();
   }
+  // seg_base comes from the absorption kernel, two launches back: this grid
+  // starts only after every CTA of the attention kernel between them has
+  // waited for it, so it is complete and can be read before the wait below
+  // (which covers the partial results of the attention kernel itself)
+  if (tid <= nb) seg[tid] = p.seg_base[b0 + tid];
   griddep_wait();
   griddep_launch_dependents();
   if (tid == 0) {
@@ -103,7 +108,6 @@ __global__ void __launch_bounds__(kUVThreads, 1)
     for (int kb = 0; kb < 8; ++kb)
       tma_load_2d(smem + kb * kUVWBlock, &tmap_wuv, 64 * kb, (h % p.heads_w) * kVDim, w_full);
   }
-  if (tid <= nb) seg[tid] = p.seg_base[b0 + tid];
   __syncthreads();
 
   // ---- 1. merge.  wps warps per sequence (about kUVBatch segments each, as
