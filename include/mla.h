@@ -52,7 +52,7 @@ typedef struct CUevent_st* mla_event_t;
 typedef enum {
   MLA_OK = 0,
   MLA_ERR_INVALID_ARG = -1,     /* null/misaligned pointer, negative or inconsistent size   */
-  MLA_ERR_UNSUPPORTED = -2,     /* dimensions this build does not implement                */
+  MLA_ERR_UNSUPPORTED = -2,     /* dimensions this library does not implement              */
   MLA_ERR_WORKSPACE = -3,       /* workspace missing, misaligned or smaller than required  */
   MLA_ERR_CUDA = -4,            /* a CUDA runtime/driver call failed (launch, tensor map)  */
   MLA_ERR_DEVICE_TIMEOUT = -5,  /* device: a bounded wait inside a kernel ran out          */
@@ -66,7 +66,7 @@ typedef enum {
                           row; value = scale * (code - zero_point)                          */
 } mla_cache_dtype;
 
-/* Model dimensions.  This build implements kv_lora_rank = 512, rope_dim = 64,
+/* Model dimensions.  This library implements kv_lora_rank = 512, rope_dim = 64,
  * qk_nope_dim = 128, v_head_dim = 128 (the DeepSeek-V2/V3 shapes of "Seven
  * Ways LLMs Handle Attention", section 5), page_size in {16, 32, 64, 128},
  * and num_heads = 16 or any positive multiple of 32. */
@@ -80,7 +80,7 @@ typedef struct {
   int32_t cache_dtype;   /* mla_cache_dtype                                  */
 } mla_dims;
 
-/* Returns MLA_OK if this build implements `dims`, else MLA_ERR_INVALID_ARG
+/* Returns MLA_OK if this library implements `dims`, else MLA_ERR_INVALID_ARG
  * (null, non-positive sizes) or MLA_ERR_UNSUPPORTED. */
 int mla_check_dims(const mla_dims* dims);
 

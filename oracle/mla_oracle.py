@@ -31,7 +31,7 @@ explicitly expanded K/V), softmax normalisation, split/combine invariance,
 page-permutation invariance, RoPE invariants, INT8 error bound and worked
 examples, and the pages' own cache-size figures (tests/golden/).
 
-Readings where the pages are silent (each listed in the design doc):
+Readings where the pages are silent:
   * the 576-wide row is [latent 0..511 | RoPE key 512..575];
   * k_pe is rotated once, at append time, by the RoFormer pair rotation of
     (x[2i], x[2i+1]) with angle pos * theta**(-2i/64); the query's RoPE part

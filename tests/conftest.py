@@ -15,7 +15,7 @@ def pytest_configure(config):
 
 @pytest.fixture(scope="session")
 def cuda_lib():
-    """The built C-ABI library on a GPU machine (built on demand)."""
+    """The built C-ABI library on a machine with a GPU (built on demand)."""
     import torch
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
