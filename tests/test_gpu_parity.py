@@ -205,3 +205,16 @@ def test_append_out_of_range_sets_status(cuda_lib):
                      torch.tensor([3, 20, 0], dtype=torch.int32, device="cuda"), c, k, 0.0, st)
     assert mla.read_status_word(st) == mla.MLA_ERR_DEVICE_BOUNDS
     assert float(cache[0, 3, 0]) == 1.0 and float(cache.float().sum()) == 576.0
+
+
+def test_large_batch_plan_chunks(cuda_lib):
+    """More sequences than the plan CTA has threads (128): the length scan and
+    the segment scan each run in several passes."""
+    rng = np.random.default_rng(300)
+    lens = [int(x) for x in rng.integers(0, 400, 300)]
+    lens[0], lens[150], lens[299] = 0, 1, 128
+    _run_small(*_small(lens=tuple(lens), seed=300), num_splits=97)
+
+
+def test_256_heads(cuda_lib):
+    _run_small(*_small(heads=256, lens=(700, 1), seed=256))
