@@ -174,9 +174,12 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def cpu_baseline(w, inp, seconds):
+def cpu_baseline(w, inp, seconds, gpu_out=None, gpu_lse=None):
     """The fp64 oracle as it stands, on the host cores, over whole sequences
-    (all heads) of this workload until about `seconds` have passed."""
+    (all heads) of this workload until about `seconds` have passed.  Returns
+    (baseline dict, parity dict or None): given the GPU's out / lse of the
+    same step, the oracle's results for the sequences it ran are compared
+    with them (max abs error, max per-row relative error, max lse error)."""
     import numpy as np
     import oracle as O
     from mla_decode_attention_paged_gb300 import workloads as W
@@ -191,6 +194,27 @@ def cpu_baseline(w, inp, seconds):
     lens = inp["seq_lens"].cpu().numpy()
     import torch
     done, el, tokens_attended = 0, 0.0, 0
+    worst = {"abs": 0.0, "rel": 0.0, "lse": 0.0, "rows": 0, "bad": 0}
+
+    def compare(b, ref_o, ref_l):
+        g = np.asarray(gpu_out[b], np.float64).reshape(-1, ref_o.shape[-1])
+        r = ref_o[b].reshape(-1, ref_o.shape[-1])
+        gl = np.asarray(gpu_lse[b], np.float64).ravel()
+        rl = ref_l[b].ravel()
+        for i in range(r.shape[0]):
+            err = float(np.abs(g[i] - r[i]).max())
+            m = float(np.abs(r[i]).max())
+            worst["abs"] = max(worst["abs"], err)
+            if m > 0:
+                worst["rel"] = max(worst["rel"], err / m)
+            elif err > 0:
+                worst["bad"] += 1
+            if np.isinf(rl[i]):
+                worst["bad"] += int(not (np.isinf(gl[i]) and gl[i] < 0))
+            else:
+                worst["lse"] = max(worst["lse"], abs(float(gl[i]) - float(rl[i])))
+            worst["rows"] += 1
+
     while el < seconds:
         b = done % w.batch
         n = (int(lens[b]) + w.page_size - 1) // w.page_size
@@ -213,21 +237,31 @@ def cpu_baseline(w, inp, seconds):
         t_start = time.perf_counter()   # time the oracle itself, not the page gather
         if w.top_k:
             idx = inp["token_indices"].cpu().numpy()
-            O.decode_sparse(qn, qp, cache, sz, tab, lens, idx, wk, wv, inp["scale"], w.page_size, w.int8,
-                            pairs=[(b, h) for h in range(w.heads)])
+            ref = O.decode_sparse(qn, qp, cache, sz, tab, lens, idx, wk, wv, inp["scale"], w.page_size, w.int8,
+                                  pairs=[(b, h) for h in range(w.heads)])
         elif w.q_len == 1:
-            O.decode(qn, qp, cache, sz, tab, lens, wk, wv, inp["scale"], w.page_size, w.int8,
-                     pairs=[(b, h) for h in range(w.heads)])
+            ref = O.decode(qn, qp, cache, sz, tab, lens, wk, wv, inp["scale"], w.page_size, w.int8,
+                           pairs=[(b, h) for h in range(w.heads)])
         else:
-            O.decode_multi_token(qn, qp, cache, sz, tab, lens, wk, wv, inp["scale"], w.page_size, w.int8,
-                                 triples=[(b, t, h) for t in range(w.q_len) for h in range(w.heads)])
+            ref = O.decode_multi_token(qn, qp, cache, sz, tab, lens, wk, wv, inp["scale"], w.page_size, w.int8,
+                                       triples=[(b, t, h) for t in range(w.q_len) for h in range(w.heads)])
         el += time.perf_counter() - t_start
+        if gpu_out is not None and done < w.batch:
+            compare(b, *ref)
         done += 1
         tokens_attended += int((inp["token_indices"][b] >= 0).sum()) if w.top_k else int(lens[b])
-    return {"value": done * w.q_len / el, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+    base = {"value": done * w.q_len / el, "unit": "tokens/s", "cores": cores, "kind": "oracle",
             "sample": f"{done} whole sequence(s) x {w.q_len} token(s) x {w.heads} heads of {w.name} "
                       f"({tokens_attended} cached tokens, "
                       f"un-absorbed fp64 oracle), {el:.1f} s"}
+    parity = None
+    if gpu_out is not None:
+        ok = worst["abs"] <= 2e-2 and worst["rel"] <= 1e-2 and worst["lse"] <= 2e-2 and worst["bad"] == 0
+        parity = {"rows_checked": worst["rows"], "sequences": min(done, w.batch), "max_abs": worst["abs"],
+                  "max_rel_row": worst["rel"], "max_lse_abs": worst["lse"],
+                  "tolerance": {"abs": 2e-2, "rel_row": 1e-2, "lse_abs": 2e-2}, "pass": ok,
+                  "against": "un-absorbed fp64 oracle on the step's own inputs"}
+    return base, parity
 
 
 def run_ours(args, rank, world):
@@ -404,7 +438,12 @@ def run_ours(args, rank, world):
         "clocks": clk.summary(),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        res["cpu_baseline"] = cpu_baseline(w, inp, args.cpu_seconds)
+        # one more step with the first selection (sparse), so that out / lse
+        # are the results for the inputs the oracle reads
+        step(0)
+        torch.cuda.synchronize()
+        res["cpu_baseline"], res["parity"] = cpu_baseline(w, inp, args.cpu_seconds, out.float().cpu().numpy(),
+                                                          lse.cpu().numpy())
     return res
 
 
@@ -425,7 +464,7 @@ def run_reference(args, rank, world):
     vals, samples = [], []
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        r = cpu_baseline(w, inp, per_step)
+        r, _ = cpu_baseline(w, inp, per_step)
         vals.append(1.0 / r["value"])
         samples.append(r["sample"])
     el = time.perf_counter() - t0
