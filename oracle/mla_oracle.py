@@ -42,6 +42,13 @@ Readings where the pages are silent:
     widened to include 0, fp32 arithmetic in a fixed order (see
     ``quantize_tokens_int8``).  The exact recipe is a reading: parity of the
     recipe is pinned only by the error bound and worked examples.
+  * FP8: the E4M3 format (1 sign, 4 exponent bits with bias 7, 3 mantissa
+    bits, subnormals, no infinities, S.1111.111 = NaN, largest finite 448),
+    one fp32 scale per token from the row's largest magnitude, codes by
+    round-to-nearest-even with saturation (see ``quantize_tokens_fp8``).  The
+    pages name low-bit caches with per-token scaling but not this format: the
+    format comes from its own definition, pinned by its closed-form values,
+    brute-force nearest search and worked ties.
 """
 from __future__ import annotations
 
@@ -193,6 +200,82 @@ def dequantize_tokens_int8(codes: np.ndarray, scale: np.ndarray, zero_point: np.
 
 
 # --------------------------------------------------------------------------- #
+# FP8 (E4M3) per-token scaled quantisation ([P2] section 3 and [P4] KIVI       #
+# section: low-bit caches, scaled per token for the data mixed across tokens) #
+# --------------------------------------------------------------------------- #
+
+E4M3_MAX = 448.0  # largest finite E4M3 magnitude: (1 + 6/8) * 2**(15 - 7)
+
+
+def e4m3_value(codes) -> np.ndarray:
+    """Value of each FP8 E4M3 code (uint8), from the format's definition.
+
+    Bit 7 is the sign, bits 6..3 the exponent e (bias 7), bits 2..0 the
+    mantissa m.  e = 0 is subnormal: (m / 8) * 2**-6; otherwise
+    (1 + m / 8) * 2**(e - 7).  The code with e = 15 and m = 7 is NaN (the
+    format has no infinities), so the largest finite magnitude is
+    1.75 * 2**8 = 448.  Returns fp64 (every E4M3 value is exact there).
+    """
+    c = np.asarray(codes).astype(np.uint8).astype(np.int64)
+    e = (c >> 3) & 0xF
+    m = (c & 0x7).astype(np.float64)
+    mag = np.where(e == 0, (m / 8.0) * 2.0 ** -6, (1.0 + m / 8.0) * np.exp2(e.astype(np.float64) - 7.0))
+    mag = np.where((e == 15) & (c & 0x7 == 7), np.nan, mag)
+    return np.where(c & 0x80, -mag, mag)
+
+
+def e4m3_encode(x) -> np.ndarray:
+    """Nearest finite E4M3 code to each value (uint8).
+
+    Round to nearest, ties to the code with the even mantissa; magnitudes at
+    or beyond 448 saturate to 448 (the format has no infinity, and the code
+    above 448 is NaN); the sign is kept, so -0 and negative values that
+    round to zero give 0x80.  The search runs over the table of the 127
+    non-negative finite codes (their magnitudes rise with the code).
+    """
+    v = np.asarray(x, dtype=np.float64)
+    table = e4m3_value(np.arange(0x7F))          # codes 0x00 .. 0x7E, ascending magnitudes
+    a = np.minimum(np.abs(v), E4M3_MAX)
+    hi = np.clip(np.searchsorted(table, a, side="left"), 0, 0x7E)  # first code with magnitude >= a
+    lo = np.maximum(hi - 1, 0)
+    d_hi = table[hi] - a
+    d_lo = a - table[lo]
+    pick_lo = (d_lo < d_hi) | ((d_lo == d_hi) & (lo % 2 == 0))
+    code = np.where(pick_lo, lo, hi).astype(np.int64)
+    code = np.where(np.signbit(v), code | 0x80, code)
+    return code.astype(np.uint8)
+
+
+def quantize_tokens_fp8(rows: np.ndarray):
+    """Quantise each row (one token's 576 values) to E4M3 codes with one scale.
+
+    Per token, as for the INT8 cache, but symmetric: E4M3 already spaces its
+    values geometrically, so one scale that maps the row's largest magnitude
+    onto the format's largest finite value suffices.  In IEEE fp32 with
+    round-to-nearest-even, in this order:
+
+        a = max |x|          s = a / 448          (s = 1 if that is 0)
+        code = E4M3 nearest (ties to even, saturating) of  x / s
+
+    Returns (codes uint8 [N, D], scale fp32 [N]).
+    """
+    x = np.asarray(rows, dtype=np.float32)
+    if x.ndim == 1:
+        x = x[None, :]
+    f = np.float32
+    a = np.abs(x).max(axis=1).astype(np.float32)
+    s = (a / f(E4M3_MAX)).astype(np.float32)
+    s = np.where(s == f(0), f(1), s).astype(np.float32)
+    y = (x / s[:, None]).astype(np.float32)
+    return e4m3_encode(y), s
+
+
+def dequantize_tokens_fp8(codes: np.ndarray, scale: np.ndarray) -> np.ndarray:
+    """x_hat = scale * value(code), evaluated in fp64."""
+    return np.asarray(scale, dtype=np.float64)[..., None] * e4m3_value(codes)
+
+
+# --------------------------------------------------------------------------- #
 # Paged cache ([P2] section 7 "Paged Attention"; [P4] "PagedAttention")       #
 # --------------------------------------------------------------------------- #
 
@@ -208,12 +291,14 @@ def page_slot(block_table: np.ndarray, seq: int, pos: int, page_size: int):
 
 def append_tokens(cache: np.ndarray, scale_zero: np.ndarray | None, block_table: np.ndarray,
                   seq_ids: Sequence[int], positions: Sequence[int], c_kv_bits: np.ndarray,
-                  k_pe_bits: np.ndarray, rope_theta: float, page_size: int, int8: bool) -> None:
+                  k_pe_bits: np.ndarray, rope_theta: float, page_size: int, int8: bool, *,
+                  fp8: bool = False) -> None:
     """Write new tokens into the paged cache, in place ([P4] decode phase: "the
     new Key and Value are appended").
 
-    cache: bf16 bit patterns uint16 [num_pages, P, 576], or int8 codes with
-    scale_zero fp32 [num_pages, P, 2] holding (scale, zero_point).
+    cache: bf16 bit patterns uint16 [num_pages, P, 576]; int8 codes with
+    scale_zero fp32 [num_pages, P, 2] holding (scale, zero_point); or (fp8)
+    E4M3 codes uint8 with scale_zero fp32 [num_pages, P] holding the scale.
     c_kv_bits / k_pe_bits: bf16 bit patterns of the new latent [N, 512] and
     RoPE key [N, 64].  The RoPE key is rotated by the token's position in fp64
     and rounded to bf16; the stored row is [latent | rotated key].
@@ -229,16 +314,22 @@ def append_tokens(cache: np.ndarray, scale_zero: np.ndarray | None, block_table:
             cache[page, off] = q[0]
             scale_zero[page, off, 0] = s[0]
             scale_zero[page, off, 1] = z[0]
+        elif fp8:
+            q, s = quantize_tokens_fp8(row.astype(np.float32))
+            cache[page, off] = q[0]
+            scale_zero[page, off] = s[0]
         else:
             cache[page, off] = f64_to_bf16_bits(row)
 
 
 def gather_rows(cache: np.ndarray, scale_zero: np.ndarray | None, block_table: np.ndarray,
-                seq: int, length: int, page_size: int, int8: bool) -> np.ndarray:
+                seq: int, length: int, page_size: int, int8: bool, *, fp8: bool = False) -> np.ndarray:
     """The ``length`` cached rows of sequence ``seq`` in logical order, as fp64 [L, 576]."""
     t = np.arange(length)
     pages = block_table[seq, t // page_size].astype(np.int64)
     offs = t % page_size
+    if fp8:
+        return dequantize_tokens_fp8(cache[pages, offs], scale_zero[pages, offs])
     if int8:
         return dequantize_tokens_int8(cache[pages, offs], scale_zero[pages, offs, 0],
                                       scale_zero[pages, offs, 1])
@@ -341,7 +432,8 @@ def attend_split(q_nope, q_pe, rows, W_UK, W_UV, scale, bounds: Iterable[int]):
 
 def decode(q_nope: np.ndarray, q_pe: np.ndarray, cache: np.ndarray, scale_zero: np.ndarray | None,
            block_table: np.ndarray, seq_lens: Sequence[int], W_UK: np.ndarray, W_UV: np.ndarray,
-           scale: float, page_size: int, int8: bool, pairs=None, absorbed: bool = False):
+           scale: float, page_size: int, int8: bool, pairs=None, absorbed: bool = False, *,
+           fp8: bool = False):
     """Decode attention for a batch: for each requested (b, h) pair, read the
     sequence's rows through its page table and attend.
 
@@ -360,7 +452,7 @@ def decode(q_nope: np.ndarray, q_pe: np.ndarray, cache: np.ndarray, scale_zero: 
         by_seq.setdefault(int(b), []).append(int(h))
     fn = attend_absorbed if absorbed else attend_unabsorbed
     for b, heads in by_seq.items():
-        rows = gather_rows(cache, scale_zero, block_table, b, int(seq_lens[b]), page_size, int8)
+        rows = gather_rows(cache, scale_zero, block_table, b, int(seq_lens[b]), page_size, int8, fp8=fp8)
         for h in heads:
             o, l, _ = fn(q_nope[b, h], q_pe[b, h], rows, W_UK[h], W_UV[h], scale)
             out[b, h] = o
@@ -370,7 +462,8 @@ def decode(q_nope: np.ndarray, q_pe: np.ndarray, cache: np.ndarray, scale_zero: 
 
 def decode_multi_token(q_nope: np.ndarray, q_pe: np.ndarray, cache: np.ndarray, scale_zero: np.ndarray | None,
                        block_table: np.ndarray, seq_lens: Sequence[int], W_UK: np.ndarray, W_UV: np.ndarray,
-                       scale: float, page_size: int, int8: bool, triples=None, absorbed: bool = False):
+                       scale: float, page_size: int, int8: bool, triples=None, absorbed: bool = False, *,
+                       fp8: bool = False):
     """Several new tokens of each sequence decoded in one pass: the
     verification read of speculative decoding ([P4] "Speculative Decoding:
     Amortizing the Memory Fetch": all drafted tokens are checked in one
@@ -398,7 +491,7 @@ def decode_multi_token(q_nope: np.ndarray, q_pe: np.ndarray, cache: np.ndarray, 
     fn = attend_absorbed if absorbed else attend_unabsorbed
     for b, th in by_seq.items():
         L = int(seq_lens[b])
-        rows = gather_rows(cache, scale_zero, block_table, b, L, page_size, int8)
+        rows = gather_rows(cache, scale_zero, block_table, b, L, page_size, int8, fp8=fp8)
         for t, h in th:
             visible = max(0, L - T + t + 1)
             o, l, _ = fn(q_nope[b, t, h], q_pe[b, t, h], rows[:visible], W_UK[h], W_UV[h], scale)
@@ -409,7 +502,8 @@ def decode_multi_token(q_nope: np.ndarray, q_pe: np.ndarray, cache: np.ndarray, 
 
 def decode_sparse(q_nope: np.ndarray, q_pe: np.ndarray, cache: np.ndarray, scale_zero: np.ndarray | None,
                   block_table: np.ndarray, seq_lens: Sequence[int], token_indices: np.ndarray, W_UK: np.ndarray,
-                  W_UV: np.ndarray, scale: float, page_size: int, int8: bool, pairs=None, absorbed: bool = False):
+                  W_UV: np.ndarray, scale: float, page_size: int, int8: bool, pairs=None, absorbed: bool = False, *,
+                  fp8: bool = False):
     """Sparse decode over a given selection of cached tokens ([P3] section 6,
     "Sparse attention: keep every token, read only some": the full cache is
     kept and each new token attends only to the top-k tokens an indexer
@@ -430,7 +524,7 @@ def decode_sparse(q_nope: np.ndarray, q_pe: np.ndarray, cache: np.ndarray, scale
         by_seq.setdefault(int(b), []).append(int(h))
     fn = attend_absorbed if absorbed else attend_unabsorbed
     for b, heads in by_seq.items():
-        rows = gather_rows(cache, scale_zero, block_table, b, int(seq_lens[b]), page_size, int8)
+        rows = gather_rows(cache, scale_zero, block_table, b, int(seq_lens[b]), page_size, int8, fp8=fp8)
         chosen = [int(i) for i in np.asarray(token_indices[b]).ravel() if int(i) >= 0]
         sel = rows[chosen] if chosen else rows[:0]
         for h in heads:

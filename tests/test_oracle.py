@@ -134,6 +134,86 @@ def test_int8_error_bound_and_zero():
     assert np.all(np.diff(np.take_along_axis(codes.astype(int), order, 1), axis=1) >= 0)
 
 
+# ------------------------------------------------------------------- FP8 ---- #
+
+def _fp8_golden():
+    return json.load(open(os.path.join(GOLDEN, "fp8_e4m3_worked_examples.json")))
+
+
+def test_fp8_e4m3_worked_values():
+    g = _fp8_golden()
+    for case in g["decode"]:
+        v = O.e4m3_value(np.array([case["code"]], np.uint8))[0]
+        if case["value"] == "nan":
+            assert np.isnan(v), case["why"]
+        else:
+            assert v == case["value"] and np.signbit(v) == np.signbit(case["value"]), case["why"]
+    for case in g["encode"]:
+        c = O.e4m3_encode(np.array([case["value"]], np.float32))[0]
+        assert int(c) == case["code"], case["why"]
+    for case in g["quantize"]:
+        codes, s = O.quantize_tokens_fp8(np.array(case["row"], np.float32))
+        np.testing.assert_array_equal(codes[0], np.array(case["codes"], np.uint8), err_msg=case["why"])
+        assert s[0] == np.float32(np.float32(case["scale_num"]) / np.float32(case["scale_den"]))
+
+
+def test_fp8_e4m3_format_closed_forms():
+    v = O.e4m3_value(np.arange(256))
+    finite = ~np.isnan(v)
+    assert finite.sum() == 254                      # two NaN patterns, no infinities
+    assert np.nanmax(v) == 448.0 and np.nanmin(v) == -448.0
+    pos = v[:0x7F]
+    assert np.all(np.diff(pos) > 0)                 # magnitudes rise with the code
+    np.testing.assert_array_equal(v[0x80:0xFF], -pos)
+    # each binade [2^e, 2^(e+1)) holds 8 evenly spaced values; subnormals step by 2^-9
+    np.testing.assert_array_equal(np.diff(pos[:9]), np.full(8, 2.0 ** -9))
+    for e in range(1, 15):
+        np.testing.assert_array_equal(pos[8 * e: 8 * e + 8], 2.0 ** (e - 7) * (1 + np.arange(8) / 8))
+    # every finite code survives decode -> encode
+    codes = np.arange(256)[finite]
+    np.testing.assert_array_equal(O.e4m3_encode(v[finite]), codes.astype(np.uint8))
+
+
+def test_fp8_e4m3_encode_is_brute_force_nearest():
+    rng = np.random.default_rng(8)
+    x = np.concatenate([rng.normal(0, 1, 4000) * np.exp2(rng.uniform(-14, 10, 4000)),
+                        rng.uniform(-500, 500, 1000)]).astype(np.float32)
+    c = O.e4m3_encode(x)
+    allv = O.e4m3_value(np.arange(256))
+    fin = np.arange(256)[~np.isnan(allv)]
+    xd = x.astype(np.float64)
+    target = np.clip(xd, -448.0, 448.0)
+    d_all = np.abs(target[:, None] - allv[fin][None, :])
+    d_best = d_all.min(axis=1)
+    got = np.abs(target - O.e4m3_value(c))
+    np.testing.assert_array_equal(got, d_best)
+    ties = (d_all == d_best[:, None]).sum(axis=1) > 1
+    nonzero = O.e4m3_value(c) != 0
+    assert np.all((c[ties & nonzero] & 1) == 0)     # ties went to the even mantissa
+    assert np.all(np.signbit(O.e4m3_value(c)) == np.signbit(xd))
+
+
+def test_fp8_quantize_error_bound_and_extremes():
+    rows = (RNG.normal(0, 1, (200, 576)) * RNG.uniform(0.01, 100, (200, 1))).astype(np.float32)
+    rows[:, 7] = 0.0
+    rows[5] = 0.0                                   # an all-zero row
+    codes, s = O.quantize_tokens_fp8(rows)
+    xh = O.dequantize_tokens_fp8(codes, s)
+    x = rows.astype(np.float64)
+    sd = s[:, None].astype(np.float64)
+    # half a step of E4M3 at the value (2^-4 relative in a binade, 2^-10 among
+    # subnormals), plus the fp32 division's rounding
+    bound = np.maximum(np.abs(x) * 2.0 ** -4, sd * 2.0 ** -10) * (1 + 1e-6)
+    assert np.all(np.abs(xh - x) <= bound)
+    np.testing.assert_array_equal(xh[:, 7], 0.0)
+    assert s[5] == 1.0 and np.all(codes[5] == 0)
+    # the row's largest magnitude lands on +-448
+    live = np.arange(200) != 5
+    amax_at = np.abs(rows).argmax(axis=1)
+    top = O.e4m3_value(codes[np.arange(200), amax_at])
+    np.testing.assert_array_equal(np.abs(top[live]), 448.0)
+
+
 # ------------------------------------------------------ paged addressing ---- #
 
 def test_append_then_gather_roundtrip_and_injective_slots():
@@ -252,15 +332,19 @@ def test_split_combine_invariance(bounds):
     assert np.all(oz == 0) and lz == -math.inf
 
 
-@pytest.mark.parametrize("int8", [False, True])
-def test_decode_page_permutation_invariance(int8):
+@pytest.mark.parametrize("fmt", ["bf16", "int8", "fp8"])
+def test_decode_page_permutation_invariance(fmt):
     rng = np.random.default_rng(11)
     B, H, P, maxp = 3, 2, 16, 6
     lens = [96, 1, 50]
     npg = B * maxp
+    int8, fp8 = fmt == "int8", fmt == "fp8"
     if int8:
         cache = rng.integers(-128, 128, (npg, P, 576)).astype(np.int8)
         sz = np.stack([rng.uniform(0.01, 0.1, (npg, P)), rng.integers(-128, 128, (npg, P))], -1).astype(np.float32)
+    elif fp8:
+        cache = rng.choice(np.r_[0:0x7F, 0x80:0xFF], (npg, P, 576)).astype(np.uint8)
+        sz = rng.uniform(0.001, 0.01, (npg, P)).astype(np.float32)
     else:
         cache = O.f64_to_bf16_bits(rng.normal(0, 1, (npg, P, 576)))
         sz = None
@@ -269,19 +353,20 @@ def test_decode_page_permutation_invariance(int8):
     W_UV = _bf16(rng.normal(0, 0.02, (H, 128, 512)))
     qn = _bf16(rng.normal(0, 1, (B, H, 128)))
     qp = _bf16(rng.normal(0, 1, (B, H, 64)))
-    out1, lse1 = O.decode(qn, qp, cache, sz, table, lens, W_UK, W_UV, 0.07, P, int8)
+    out1, lse1 = O.decode(qn, qp, cache, sz, table, lens, W_UK, W_UV, 0.07, P, int8, fp8=fp8)
     perm = rng.permutation(npg)          # physical page p moves to perm[p]
     cache2 = np.empty_like(cache)
     cache2[perm] = cache
     sz2 = None
-    if int8:
+    if int8 or fp8:
         sz2 = np.empty_like(sz)
         sz2[perm] = sz
-    out2, lse2 = O.decode(qn, qp, cache2, sz2, perm[table].astype(np.int32), lens, W_UK, W_UV, 0.07, P, int8)
+    out2, lse2 = O.decode(qn, qp, cache2, sz2, perm[table].astype(np.int32), lens, W_UK, W_UV, 0.07, P, int8,
+                          fp8=fp8)
     np.testing.assert_array_equal(out1, out2)
     np.testing.assert_array_equal(lse1, lse2)
     # absorbed cross-check over the whole batch
-    out3, lse3 = O.decode(qn, qp, cache, sz, table, lens, W_UK, W_UV, 0.07, P, int8, absorbed=True)
+    out3, lse3 = O.decode(qn, qp, cache, sz, table, lens, W_UK, W_UV, 0.07, P, int8, absorbed=True, fp8=fp8)
     np.testing.assert_allclose(out3, out1, rtol=1e-11, atol=1e-15)
 
 
