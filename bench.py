@@ -79,15 +79,19 @@ def peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
-def attention_kernel(int8: bool):
-    """(source file, kernel name) of the attention kernel the library runs for this cache type."""
-    name = "decode_tc.cu" if int8 else "decode_pair.cu"
+def attention_kernel(fmt: str):
+    """(source file, kernel name) of the attention kernel the library runs for this cache format."""
+    name = "decode_pair.cu" if fmt == "bf16" else "decode_tc.cu"
     return (os.path.join(ROOT, "mla_decode_attention_paged_gb300", "csrc", name),
-            "decode_tc_kernel (single-CTA split-KV attention, INT8 cache)" if int8
-            else "decode_pair_kernel (split-KV attention on CTA pairs)")
+            "decode_pair_kernel (split-KV attention on CTA pairs)" if fmt == "bf16"
+            else f"decode_tc_kernel (single-CTA split-KV attention, {fmt.upper()} cache)")
 
 
-def kernel_traffic(workload_name: str, tokens: int, int8: bool):
+# bytes one cached token occupies: 576 values plus its quantisation parameters
+BYTES_PER_TOKEN = {"bf16": 1152, "int8": 584, "fp8": 580}
+
+
+def kernel_traffic(workload_name: str, tokens: int, fmt: str):
     """DRAM bytes per attention launch from the committed ncu summary, scaled
     to this launch's tokens; None if absent or taken on a different kernel."""
     path = os.path.join(ROOT, "profiles", "attention_dram_traffic.json")
@@ -96,7 +100,7 @@ def kernel_traffic(workload_name: str, tokens: int, int8: bool):
     e = json.load(open(path)).get("workloads", {}).get(workload_name)
     if not e:
         return None
-    src, _ = attention_kernel(int8)
+    src, _ = attention_kernel(fmt)
     if hashlib.sha256(open(src, "rb").read()).hexdigest() != e.get("kernel_sha256"):
         return None
     return round(e["dram_bytes_per_token"] * tokens)
@@ -220,17 +224,18 @@ def cpu_baseline(w, inp, seconds, gpu_out=None, gpu_lse=None):
         n = (int(lens[b]) + w.page_size - 1) // w.page_size
         tab = np.full_like(table, -1)
         tab[b, :n] = np.arange(n)
-        if w.int8 and "src_c_kv" in inp:   # the oracle's own append builds this sequence's pages
+        if w.quantised and "src_c_kv" in inp:   # the oracle's own append builds this sequence's pages
             a = int(lens[:b].sum())
-            cache = np.zeros((n, w.page_size, 576), np.int8)
-            sz = np.zeros((n, w.page_size, 2), np.float32)
+            cache = np.zeros((n, w.page_size, 576), np.int8 if w.int8 else np.uint8)
+            sz = np.zeros((n, w.page_size, 2) if w.int8 else (n, w.page_size), np.float32)
             O.append_tokens(cache, sz, tab, [b] * int(lens[b]), list(range(int(lens[b]))),
                             W.bf16_to_bits(inp["src_c_kv"][a:a + int(lens[b])]),
-                            W.bf16_to_bits(inp["src_k_pe"][a:a + int(lens[b])]), w.rope_theta, w.page_size, True)
+                            W.bf16_to_bits(inp["src_k_pe"][a:a + int(lens[b])]), w.rope_theta, w.page_size,
+                            w.int8, fp8=w.fp8)
         else:
             idx = torch.as_tensor(table[b, :n].astype(np.int64), device=inp["cache_dev"].device)
             sub = inp["cache_dev"].index_select(0, idx)
-            if w.int8:
+            if w.quantised:
                 cache, sz = sub.cpu().numpy(), inp["sz_dev"].index_select(0, idx).cpu().numpy()
             else:
                 cache, sz = W.bf16_to_bits(sub), None
@@ -238,13 +243,14 @@ def cpu_baseline(w, inp, seconds, gpu_out=None, gpu_lse=None):
         if w.top_k:
             idx = inp["token_indices"].cpu().numpy()
             ref = O.decode_sparse(qn, qp, cache, sz, tab, lens, idx, wk, wv, inp["scale"], w.page_size, w.int8,
-                                  pairs=[(b, h) for h in range(w.heads)])
+                                  pairs=[(b, h) for h in range(w.heads)], fp8=w.fp8)
         elif w.q_len == 1:
             ref = O.decode(qn, qp, cache, sz, tab, lens, wk, wv, inp["scale"], w.page_size, w.int8,
-                           pairs=[(b, h) for h in range(w.heads)])
+                           pairs=[(b, h) for h in range(w.heads)], fp8=w.fp8)
         else:
             ref = O.decode_multi_token(qn, qp, cache, sz, tab, lens, wk, wv, inp["scale"], w.page_size, w.int8,
-                                       triples=[(b, t, h) for t in range(w.q_len) for h in range(w.heads)])
+                                       triples=[(b, t, h) for t in range(w.q_len) for h in range(w.heads)],
+                                       fp8=w.fp8)
         el += time.perf_counter() - t_start
         if gpu_out is not None and done < w.batch:
             compare(b, *ref)
@@ -273,15 +279,16 @@ def run_ours(args, rank, world):
     mla.load_library(build_if_missing=True)
     w = W.WORKLOADS[args.workload]
     inp = W.make_decode_inputs(w, device=dev)
-    d = mla.dims(w.heads, w.page_size, int8=w.int8)
+    d = mla.dims(w.heads, w.page_size, int8=w.int8, fp8=w.fp8)
     B, H, T = w.batch, w.heads, w.q_len
     seq_lens = inp["seq_lens"]
     table = inp["block_table"].to(dev)
     npg = inp["num_pages"]
-    # the cache: drawn directly (bf16) or written through the library's append (INT8)
-    if w.int8:
-        cache = torch.zeros((npg, w.page_size, 576), dtype=torch.int8, device=dev)
-        sz = torch.zeros((npg, w.page_size, 2), dtype=torch.float32, device=dev)
+    # the cache: drawn directly (bf16) or written through the library's append (INT8, FP8)
+    if w.quantised:
+        cache = torch.zeros((npg, w.page_size, 576), dtype=torch.int8 if w.int8 else torch.uint8, device=dev)
+        sz = torch.zeros((npg, w.page_size, 2) if w.int8 else (npg, w.page_size), dtype=torch.float32,
+                         device=dev)
         mla.cache_append(d, cache, sz, table, inp["src_seq_ids"], inp["src_positions"], inp["src_c_kv"],
                          inp["src_k_pe"], w.rope_theta)
         del inp["src_c_kv"], inp["src_k_pe"]
@@ -296,7 +303,7 @@ def run_ours(args, rank, world):
     positions = (seq_lens.to(dev).repeat_interleave(T) - T +
                  torch.arange(T, dtype=torch.int32, device=dev).repeat(B)).clamp(min=0).to(torch.int32)
     # the kernels see T * H heads per sequence; the automatic split count is theirs
-    d_rows = mla.dims(H * T, w.page_size, int8=w.int8)
+    d_rows = mla.dims(H * T, w.page_size, int8=w.int8, fp8=w.fp8)
     auto = mla.auto_num_splits(d_rows if mla.check_dims(d_rows) == mla.MLA_OK else d, B)
     splits = args.num_splits if args.num_splits is not None else (W.num_splits_for(w, auto) or auto)
     ws_bytes = (mla.decode_sparse_workspace_size(d, B, w.top_k, splits) if w.top_k
@@ -368,7 +375,7 @@ def run_ours(args, rank, world):
     ms = ms_total / args.steps
     # tokens the attention reads: every cached one, or the selected ones (sparse)
     lens_sum = int((token_indices >= 0).sum()) if w.top_k else int(seq_lens.to(torch.int64).sum())
-    bytes_per_token = 584 if w.int8 else 1152
+    bytes_per_token = BYTES_PER_TOKEN[w.cache_format]
     cache_bytes = lens_sum * bytes_per_token
     tokens_per_s = whole_job_rate(B * T, world, ms)
     step_cache_gbs = whole_job_rate(cache_bytes, world, ms) / 1e9
@@ -411,11 +418,12 @@ def run_ours(args, rank, world):
 
     peak, peak_src = peaks()
     achieved = cache_bytes / (kern_ms / 1e3) / 1e9
-    traffic = kernel_traffic(w.name, lens_sum, w.int8)
+    traffic = kernel_traffic(w.name, lens_sum, w.cache_format)
     res = {
         "metric": METRIC, "value": round(tokens_per_s, 1), "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "int8" if w.int8 else "bf16",
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": {"bf16": "bf16", "int8": "int8", "fp8": "fp8_e4m3"}[w.cache_format],
         "data": "synthetic (seeded; random-init weights of DeepSeek-V2 MLA shapes)",
         "config": {"workload": w.name, "batch": B, "heads": H, "context": w.context, "page_size": w.page_size,
                    "q_len": T, "top_k": w.top_k or None, "num_splits": splits, "cache_bytes": cache_bytes,
@@ -430,7 +438,7 @@ def run_ours(args, rank, world):
         "attention_kernel_ms": round(kern_ms, 5),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_source": peak_src,
-                     "traffic": traffic, "kernel": attention_kernel(w.int8)[1],
+                     "traffic": traffic, "kernel": attention_kernel(w.cache_format)[1],
                      "algorithmic_bytes_per_launch": cache_bytes},
         "e2e": {"value": round(whole_job_rate(B * T, world, e2e_ms), 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 5)},
@@ -456,7 +464,7 @@ def run_reference(args, rank, world):
         return None
     w = W.WORKLOADS[args.workload]
     dev = "cuda" if torch.cuda.is_available() else "cpu"
-    inp = W.make_decode_inputs(w.scaled(batch=min(w.batch, 4)) if w.int8 else w, device=dev)
+    inp = W.make_decode_inputs(w.scaled(batch=min(w.batch, 4)) if w.quantised else w, device=dev)
     inp["cache_dev"], inp["sz_dev"] = inp.get("cache"), None
     per_step = max(1.0, min(6.0, 150.0 / max(args.steps + args.warmup, 1)))
     for _ in range(args.warmup):

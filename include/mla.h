@@ -62,8 +62,11 @@ typedef enum {
 
 typedef enum {
   MLA_CACHE_BF16 = 0,  /* cache rows are 576 bf16 values                                   */
-  MLA_CACHE_INT8 = 1   /* cache rows are 576 int8 codes plus fp32 (scale, zero point) per
+  MLA_CACHE_INT8 = 1,  /* cache rows are 576 int8 codes plus fp32 (scale, zero point) per
                           row; value = scale * (code - zero_point)                          */
+  MLA_CACHE_FP8 = 2    /* cache rows are 576 FP8 E4M3 codes (1 sign, 4 exponent bits with
+                          bias 7, 3 mantissa bits; no infinities; 0x7F/0xFF are NaN) plus
+                          one fp32 scale per row; value = scale * e4m3(code)                */
 } mla_cache_dtype;
 
 /* Model dimensions.  This library implements kv_lora_rank = 512, rope_dim = 64,
@@ -91,7 +94,7 @@ int mla_check_dims(const mla_dims* dims);
  * table); "Beyond the Attention Bottleneck", "The RoPE Compatibility
  * Problem" (the positional key carries RoPE); "KV Cache Optimization" section
  * 3 and "The Architecture of Memory", KIVI section (per-token min/max
- * quantisation) for MLA_CACHE_INT8.
+ * quantisation) for MLA_CACHE_INT8 and MLA_CACHE_FP8.
  *
  * For token i (0 <= i < n_tokens): b = seq_ids[i], pos = positions[i],
  * physical page = block_table[b * max_pages_per_seq + pos / P], slot = pos % P.
@@ -101,10 +104,14 @@ int mla_check_dims(const mla_dims* dims);
  * unrotated).  INT8 caches then quantise the 576 bf16 values of the row:
  * lo = min(min x, 0), hi = max(max x, 0), s = (hi - lo)/255 (1 if 0),
  * zp = clamp(rint(-128 - lo/s)), code = clamp(rint(x/s) + zp, -128, 127),
- * all in IEEE fp32 round-to-nearest-even, and store (s, zp).
+ * all in IEEE fp32 round-to-nearest-even, and store (s, zp).  FP8 caches
+ * take a = max |x|, s = a/448 (1 if 0) and code = the E4M3 value nearest
+ * to x/s (ties to the even mantissa, magnitudes past 448 saturate, the sign
+ * of zero kept), in IEEE fp32 round-to-nearest-even, and store s.
  *
- *   cache            bf16 [num_pages, P, 576] or int8 [num_pages, P, 576]
- *   cache_scale_zero fp32 [num_pages, P, 2] (INT8 only; NULL for bf16)
+ *   cache            bf16, int8 or E4M3 (uint8) [num_pages, P, 576]
+ *   cache_scale_zero fp32 [num_pages, P, 2] (INT8), fp32 [num_pages, P] (FP8),
+ *                    NULL for bf16
  *   block_table      int32 [num_seqs, max_pages_per_seq]
  *   seq_ids, positions  int32 [n_tokens]
  *   c_kv             bf16 [n_tokens, 512];  k_pe bf16 [n_tokens, 64]

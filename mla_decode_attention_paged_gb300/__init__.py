@@ -22,7 +22,7 @@ __all__ = [
     "decode_sparse", "decode_no_alloc", "combine", "read_device_status", "read_status_word",
     "set_timing_events", "status_string", "version",
     "MLA_OK", "MLA_ERR_INVALID_ARG", "MLA_ERR_UNSUPPORTED", "MLA_ERR_WORKSPACE", "MLA_ERR_CUDA",
-    "MLA_ERR_DEVICE_TIMEOUT", "MLA_ERR_DEVICE_BOUNDS", "MLA_CACHE_BF16", "MLA_CACHE_INT8", "MAX_Q_LEN", "MAX_TOP_K",
+    "MLA_ERR_DEVICE_TIMEOUT", "MLA_ERR_DEVICE_BOUNDS", "MLA_CACHE_BF16", "MLA_CACHE_INT8", "MLA_CACHE_FP8", "MAX_Q_LEN", "MAX_TOP_K",
 ]
 
 MLA_OK = 0
@@ -34,6 +34,7 @@ MLA_ERR_DEVICE_TIMEOUT = -5
 MLA_ERR_DEVICE_BOUNDS = -6
 MLA_CACHE_BF16 = 0
 MLA_CACHE_INT8 = 1
+MLA_CACHE_FP8 = 2
 MAX_Q_LEN = 8  # MLA_MAX_Q_LEN in include/mla.h
 MAX_TOP_K = 1 << 20  # MLA_MAX_TOP_K in include/mla.h
 
@@ -62,9 +63,13 @@ class Dims(ctypes.Structure):
 
 
 def dims(num_heads: int, page_size: int, int8: bool = False, kv_lora_rank: int = 512, rope_dim: int = 64,
-         qk_nope_dim: int = 128, v_head_dim: int = 128) -> Dims:
-    return Dims(num_heads, kv_lora_rank, rope_dim, qk_nope_dim, v_head_dim, page_size,
-                MLA_CACHE_INT8 if int8 else MLA_CACHE_BF16)
+         qk_nope_dim: int = 128, v_head_dim: int = 128, fp8: bool = False) -> Dims:
+    """Model dimensions; ``int8`` / ``fp8`` select a 1-byte cache (INT8 codes, or
+    FP8 E4M3 codes held as uint8 or torch.float8_e4m3fn) with per-token scales."""
+    if int8 and fp8:
+        raise ValueError("int8 and fp8 are exclusive")
+    code = MLA_CACHE_INT8 if int8 else MLA_CACHE_FP8 if fp8 else MLA_CACHE_BF16
+    return Dims(num_heads, kv_lora_rank, rope_dim, qk_nope_dim, v_head_dim, page_size, code)
 
 
 _lib = None
@@ -149,6 +154,20 @@ def _ptr(t: torch.Tensor | None, dtype=None, name="tensor", device=None):
     return t.data_ptr()
 
 
+def _cache_ptrs(d: Dims, cache: torch.Tensor, scale_zero: torch.Tensor | None, device=None):
+    """Pointers of the cache rows (bf16 values, int8 codes, or E4M3 codes) and of
+    their per-token scales (None for bf16 caches)."""
+    if d.cache_dtype == MLA_CACHE_FP8:
+        if isinstance(cache, torch.Tensor) and cache.dtype == torch.float8_e4m3fn:
+            cache = cache.view(torch.uint8)
+        want = torch.uint8
+    else:
+        want = torch.int8 if d.cache_dtype == MLA_CACHE_INT8 else torch.bfloat16
+    byte = d.cache_dtype != MLA_CACHE_BF16
+    return (_ptr(cache, want, "cache", device),
+            _ptr(scale_zero, torch.float32, "scale_zero", device) if byte else None)
+
+
 def _stream(stream) -> int | None:
     if stream is None:
         stream = torch.cuda.current_stream()
@@ -163,11 +182,9 @@ def cache_append(d: Dims, cache: torch.Tensor, scale_zero: torch.Tensor | None, 
                  seq_ids: torch.Tensor, positions: torch.Tensor, c_kv: torch.Tensor, k_pe: torch.Tensor,
                  rope_theta: float = 10000.0, device_status: torch.Tensor | None = None, stream=None) -> None:
     """mla_cache_append: write new tokens' rows into the paged cache (in place)."""
-    int8 = d.cache_dtype == MLA_CACHE_INT8
     dev = cache.device
     st = _L().mla_cache_append(
-        ctypes.byref(d), _ptr(cache, torch.int8 if int8 else torch.bfloat16, "cache"),
-        _ptr(scale_zero, torch.float32, "scale_zero", dev) if int8 else None, cache.shape[0],
+        ctypes.byref(d), *_cache_ptrs(d, cache, scale_zero, dev), cache.shape[0],
         _ptr(block_table, torch.int32, "block_table", dev), block_table.shape[0], block_table.shape[1],
         _ptr(seq_ids, torch.int32, "seq_ids", dev), _ptr(positions, torch.int32, "positions", dev),
         seq_ids.numel(), _ptr(c_kv, torch.bfloat16, "c_kv", dev), _ptr(k_pe, torch.bfloat16, "k_pe", dev),
@@ -196,7 +213,6 @@ def decode(d: Dims, q_nope, q_pe, cache, scale_zero, block_table, seq_lens, W_UK
 
     If ``workspace`` is None a uint8 buffer of the required size is taken from
     torch's allocator here (the library itself never allocates)."""
-    int8 = d.cache_dtype == MLA_CACHE_INT8
     B = q_nope.shape[0]
     dev = q_nope.device
     if workspace is None:
@@ -207,8 +223,7 @@ def decode(d: Dims, q_nope, q_pe, cache, scale_zero, block_table, seq_lens, W_UK
         lse_out = torch.empty((B, d.num_heads), dtype=torch.float32, device=dev)
     st = _L().mla_decode(
         ctypes.byref(d), _ptr(q_nope, torch.bfloat16, "q_nope"), _ptr(q_pe, torch.bfloat16, "q_pe", dev),
-        _ptr(cache, torch.int8 if int8 else torch.bfloat16, "cache", dev),
-        _ptr(scale_zero, torch.float32, "scale_zero", dev) if int8 else None, cache.shape[0],
+        *_cache_ptrs(d, cache, scale_zero, dev), cache.shape[0],
         _ptr(block_table, torch.int32, "block_table", dev), block_table.shape[1],
         _ptr(seq_lens, torch.int32, "seq_lens", dev), B, _ptr(W_UK, torch.bfloat16, "W_UK", dev),
         _ptr(W_UV, torch.bfloat16, "W_UV", dev), float(softmax_scale), int(num_splits),
@@ -233,7 +248,6 @@ def decode_multi(d: Dims, q_nope, q_pe, cache, scale_zero, block_table, seq_lens
     last q_len tokens of each cache, causal among themselves); q_nope bf16
     [B, T, H, 128], q_pe bf16 [B, T, H, 64].  Returns (out bf16 [B, T, H, 128],
     lse fp32 [B, T, H] or None)."""
-    int8 = d.cache_dtype == MLA_CACHE_INT8
     B, T = q_nope.shape[0], q_nope.shape[1]
     dev = q_nope.device
     if workspace is None:
@@ -244,8 +258,7 @@ def decode_multi(d: Dims, q_nope, q_pe, cache, scale_zero, block_table, seq_lens
         lse_out = torch.empty((B, T, d.num_heads), dtype=torch.float32, device=dev)
     st = _L().mla_decode_multi(
         ctypes.byref(d), _ptr(q_nope, torch.bfloat16, "q_nope"), _ptr(q_pe, torch.bfloat16, "q_pe", dev),
-        _ptr(cache, torch.int8 if int8 else torch.bfloat16, "cache", dev),
-        _ptr(scale_zero, torch.float32, "scale_zero", dev) if int8 else None, cache.shape[0],
+        *_cache_ptrs(d, cache, scale_zero, dev), cache.shape[0],
         _ptr(block_table, torch.int32, "block_table", dev), block_table.shape[1],
         _ptr(seq_lens, torch.int32, "seq_lens", dev), B, T, _ptr(W_UK, torch.bfloat16, "W_UK", dev),
         _ptr(W_UV, torch.bfloat16, "W_UV", dev), float(softmax_scale), int(num_splits),
@@ -269,7 +282,6 @@ def decode_sparse(d: Dims, q_nope, q_pe, cache, scale_zero, block_table, seq_len
     """mla_decode_sparse: attention over the listed positions of each sequence
     (token_indices int32 [B, top_k], -1 = padding).  Returns (out bf16
     [B, H, 128], lse fp32 [B, H] or None)."""
-    int8 = d.cache_dtype == MLA_CACHE_INT8
     B, K = token_indices.shape
     dev = q_nope.device
     if workspace is None:
@@ -280,8 +292,7 @@ def decode_sparse(d: Dims, q_nope, q_pe, cache, scale_zero, block_table, seq_len
         lse_out = torch.empty((B, d.num_heads), dtype=torch.float32, device=dev)
     st = _L().mla_decode_sparse(
         ctypes.byref(d), _ptr(q_nope, torch.bfloat16, "q_nope"), _ptr(q_pe, torch.bfloat16, "q_pe", dev),
-        _ptr(cache, torch.int8 if int8 else torch.bfloat16, "cache", dev),
-        _ptr(scale_zero, torch.float32, "scale_zero", dev) if int8 else None, cache.shape[0],
+        *_cache_ptrs(d, cache, scale_zero, dev), cache.shape[0],
         _ptr(block_table, torch.int32, "block_table", dev), block_table.shape[1],
         _ptr(seq_lens, torch.int32, "seq_lens", dev), B, _ptr(token_indices, torch.int32, "token_indices", dev), K,
         _ptr(W_UK, torch.bfloat16, "W_UK", dev), _ptr(W_UV, torch.bfloat16, "W_UV", dev), float(softmax_scale),
@@ -297,15 +308,13 @@ def decode_no_alloc(d: Dims, q_nope, q_pe, cache, scale_zero, block_table, seq_l
     """mla_decode_no_alloc: mla_decode on the library's fixed scratch array, for
     callers that cannot allocate device memory (outputs are still the
     caller's).  Returns (out, lse)."""
-    int8 = d.cache_dtype == MLA_CACHE_INT8
     B = q_nope.shape[0]
     dev = q_nope.device
     if out is None:
         out = torch.empty((B, d.num_heads, d.v_head_dim), dtype=torch.bfloat16, device=dev)
     st = _L().mla_decode_no_alloc(
         ctypes.byref(d), _ptr(q_nope, torch.bfloat16, "q_nope"), _ptr(q_pe, torch.bfloat16, "q_pe", dev),
-        _ptr(cache, torch.int8 if int8 else torch.bfloat16, "cache", dev),
-        _ptr(scale_zero, torch.float32, "scale_zero", dev) if int8 else None, cache.shape[0],
+        *_cache_ptrs(d, cache, scale_zero, dev), cache.shape[0],
         _ptr(block_table, torch.int32, "block_table", dev), block_table.shape[1],
         _ptr(seq_lens, torch.int32, "seq_lens", dev), B, _ptr(W_UK, torch.bfloat16, "W_UK", dev),
         _ptr(W_UV, torch.bfloat16, "W_UV", dev), float(softmax_scale), int(num_splits),

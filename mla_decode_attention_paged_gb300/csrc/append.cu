@@ -5,17 +5,27 @@
 // c_t plus the decoupled RoPE key ("Beyond the Attention Bottleneck", "The RoPE
 // Compatibility Problem": only the positional key carries RoPE, rotated here
 // once at its position).  Pages are found through the page table
-// ("PagedAttention: Virtual Memory for LLMs").  INT8 caches quantise the row
-// per token with an asymmetric min/max scale and zero point ("KV Cache
-// Optimization", section 3; "The Architecture of Memory", KIVI section).
+// ("PagedAttention: Virtual Memory for LLMs").  1-byte caches quantise the
+// row per token ("KV Cache Optimization", section 3; "The Architecture of
+// Memory", KIVI section): INT8 with an asymmetric min/max scale and zero
+// point, FP8 (E4M3) with one scale that maps the row's largest magnitude to
+// 448, the format's largest finite value.
 #include "blackwell_ptx.cuh"
 #include "params.cuh"
 
 namespace mla {
 
 
+// Two fp32 values to E4M3 codes (round to nearest even, saturating to
+// +-448), first value in the low byte.
+__device__ __forceinline__ uint32_t e4m3x2_rn_sat(float first, float second) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(second), "f"(first));
+  return r;
+}
+
 // One warp per token.  Lane l owns latent values [16l, 16l + 16) and RoPE pair l.
-template <bool kInt8>
+template <int kCode>
 __global__ void __launch_bounds__(256) append_kernel(AppendParams p) {
   ptx::griddep_wait();
   ptx::griddep_launch_dependents();
@@ -52,7 +62,7 @@ __global__ void __launch_bounds__(256) append_kernel(AppendParams p) {
     kr = __halves2bfloat162(__double2bfloat16(y0), __double2bfloat16(y1));
   }
 
-  if constexpr (!kInt8) {
+  if constexpr (kCode == kCodeBf16) {
     __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.cache) + row * kRow;
     reinterpret_cast<uint4*>(dst)[2 * lane] = c0;
     reinterpret_cast<uint4*>(dst)[2 * lane + 1] = c1;
@@ -71,6 +81,27 @@ __global__ void __launch_bounds__(256) append_kernel(AppendParams p) {
     }
     v[16] = __low2float(kr);
     v[17] = __high2float(kr);
+    if constexpr (kCode == kCodeE4m3) {
+      float a = 0.f;
+#pragma unroll
+      for (int j = 0; j < 18; ++j) a = fmaxf(a, fabsf(v[j]));
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+      // IEEE fp32, round to nearest even, in the documented order
+      float s = __fdiv_rn(a, 448.f);
+      if (s == 0.f) s = 1.f;
+      uint32_t w[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        w[j] = e4m3x2_rn_sat(__fdiv_rn(v[4 * j], s), __fdiv_rn(v[4 * j + 1], s)) |
+               (e4m3x2_rn_sat(__fdiv_rn(v[4 * j + 2], s), __fdiv_rn(v[4 * j + 3], s)) << 16);
+      uint8_t* dst = static_cast<uint8_t*>(p.cache) + row * kRow;
+      reinterpret_cast<uint4*>(dst)[lane] = make_uint4(w[0], w[1], w[2], w[3]);
+      reinterpret_cast<uint16_t*>(dst + kLatent)[lane] =
+          uint16_t(e4m3x2_rn_sat(__fdiv_rn(v[16], s), __fdiv_rn(v[17], s)));
+      if (lane == 0) p.scale_zero[row] = s;
+      return;
+    }
     float lo = 0.f, hi = 0.f;  // the range always includes 0
 #pragma unroll
     for (int j = 0; j < 18; ++j) {
@@ -111,14 +142,15 @@ __global__ void __launch_bounds__(256) append_kernel(AppendParams p) {
   }
 }
 
-cudaError_t launch_append(const AppendParams& p, bool int8, cudaStream_t stream) {
+cudaError_t launch_append(const AppendParams& p, int code, cudaStream_t stream) {
   if (p.n_tokens == 0) return cudaSuccess;
   // a decode step appends one token per sequence: one warp per block spreads
   // the fp64 RoPE over as many SMs as there are tokens
   const int warps = p.n_tokens < 2048 ? 1 : 8;
   const int grid = (p.n_tokens + warps - 1) / warps;
-  return int8 ? launch_pdl(append_kernel<true>, dim3(grid), dim3(warps * 32), 0, stream, 1, p)
-              : launch_pdl(append_kernel<false>, dim3(grid), dim3(warps * 32), 0, stream, 1, p);
+  if (code == kCodeInt8) return launch_pdl(append_kernel<kCodeInt8>, dim3(grid), dim3(warps * 32), 0, stream, 1, p);
+  if (code == kCodeE4m3) return launch_pdl(append_kernel<kCodeE4m3>, dim3(grid), dim3(warps * 32), 0, stream, 1, p);
+  return launch_pdl(append_kernel<kCodeBf16>, dim3(grid), dim3(warps * 32), 0, stream, 1, p);
 }
 
 }  // namespace mla

@@ -25,8 +25,8 @@
 // microseconds earlier brought the lines there).  A single ring serving both
 // products has to keep a whole 147 KB tile resident from its QK until its
 // PV, which serialises load -> QK -> softmax -> PV per tile.
-// INT8 caches (73 KB per tile): one ring of pair slots + RoPE slots serves
-// both products; the codes are expanded in place.
+// 1-byte caches (INT8 or FP8, 73 KB per tile): one ring of pair slots + RoPE
+// slots serves both products; the codes are expanded in place.
 //
 // Warp roles (288 threads; 256 for 32-head bf16 groups):
 //   warp 0     TMA producer: Q of each segment; bf16: QK ring 0 (16 heads:
@@ -40,7 +40,7 @@
 //              thread cannot issue TMA copies fast enough for an SM's share
 //              of HBM; bf16, 32 heads: the PV-ring producer
 //   warp 8     bf16, 16 heads: the PV-ring producer
-//   warps 3, 8 INT8: expand the TMA-loaded int8 codes in place into fp16
+//   warps 3, 8 INT8 / FP8: expand the TMA-loaded codes in place into fp16
 //              operand tiles
 //   warps 4-7  softmax (one thread per token row of S^T) and epilogue
 //
@@ -53,6 +53,11 @@
 // (Leaving the +1152 bias in the operands would make the PV accumulator sum
 // ~1152 * sum(w) over thousands of tokens and lose the result to fp32
 // cancellation.)
+// FP8 caches: value = s_t * e4m3(code), one scale per token.  Every E4M3 value
+// is exact in fp16 (see expand_e4m3), so the same fp16 MMAs apply, with no
+// zero-point terms:
+//     s[t][h]   = scale * s_t * (q_h . e4m3(code_t))
+//     o_lat[h]  = sum_t w_t e4m3(code_t) / l,  w_t = p_t s_t
 // Every wait is bounded: on timeout the CTA records MLA_ERR_DEVICE_TIMEOUT,
 // drains, frees its tensor memory and returns.
 #include <cuda_fp16.h>
@@ -82,15 +87,15 @@ constexpr bool kL2Hints = false;
 // ring slot only for an L2 round trip before the PV MMAs need it.
 constexpr bool kPvGate = true;
 
-template <int HC, bool kInt8>
+template <int HC, bool kByte>
 struct Cfg {
-  static constexpr int kThreads = (kInt8 || HC == 16) ? 288 : 256;
-  static constexpr int kQkRings = (!kInt8 && HC == 16) ? 2 : 1;   // bf16 QK producers (rings)
-  static constexpr int kQkSlots = kInt8 ? 0 : 6;                  // bf16 QK ring slots (single boxes), all rings
+  static constexpr int kThreads = (kByte || HC == 16) ? 288 : 256;
+  static constexpr int kQkRings = (!kByte && HC == 16) ? 2 : 1;   // bf16 QK producers (rings)
+  static constexpr int kQkSlots = kByte ? 0 : 6;                  // bf16 QK ring slots (single boxes), all rings
   static constexpr int kQkRing = kQkSlots / kQkRings;
   static constexpr int kPvProducerWarp = kQkRings == 2 ? 8 : 3;
-  static constexpr int kNumPair = kInt8 ? 5 : (HC == 16 ? 3 : 2);  // bf16 PV ring / INT8 shared ring
-  static constexpr int kNumRope = kInt8 ? 2 : 0;
+  static constexpr int kNumPair = kByte ? 5 : (HC == 16 ? 3 : 2);  // bf16 PV ring / INT8 shared ring
+  static constexpr int kNumRope = kByte ? 2 : 0;
   static constexpr uint32_t kQBytes = 9 * HC * 128;
   static constexpr uint32_t kPBytes = kTile * HC * 2;
   static constexpr uint32_t kOffQk = 0;
@@ -173,12 +178,39 @@ __device__ __forceinline__ void expand_codes(uint4 v, uint4& lo, uint4& hi) {
   hi = make_uint4(o[4], o[5], o[6], o[7]);
 }
 
+// 16 E4M3 codes -> 16 fp16 values equal to the codes' values.  A code's
+// magnitude bits (4 exponent, 3 mantissa) moved to fp16 bits 13..7 read as
+// an fp16 with the same exponent field and mantissa, i.e. the E4M3 value
+// times 2^(7 - 15) -- E4M3 subnormals becoming fp16 subnormals -- and the
+// product by 2^8 is exact (no value exceeds 448, none needs more than 4
+// significant bits).
+__device__ __forceinline__ uint32_t e4m3_pair_to_half2(uint32_t w, uint32_t sel) {
+  const uint32_t a = __byte_perm(w, 0u, sel);  // two codes into bits 15..8 and 31..24
+  const uint32_t h = (a & 0x80008000u) | ((a >> 1) & 0x3F803F80u);
+  const __half2 v = __hmul2(*reinterpret_cast<const __half2*>(&h), __floats2half2_rn(256.f, 256.f));
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+__device__ __forceinline__ void expand_e4m3(uint4 v, uint4& lo, uint4& hi) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint32_t o[8];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    o[2 * i] = e4m3_pair_to_half2(w[i], 0x1404);      // bytes 0,1
+    o[2 * i + 1] = e4m3_pair_to_half2(w[i], 0x3424);  // bytes 2,3
+  }
+  lo = make_uint4(o[0], o[1], o[2], o[3]);
+  hi = make_uint4(o[4], o[5], o[6], o[7]);
+}
+
+// kCode: CacheCode (bf16, INT8 or FP8 rows).
 // kCausal: multi-token decode (q_len > 1) only, as in the pair kernel.
-template <int HC, bool kInt8, bool kCausal>
-__global__ void __launch_bounds__(Cfg<HC, kInt8>::kThreads, 1)
+template <int HC, int kCode, bool kCausal>
+__global__ void __launch_bounds__(Cfg<HC, kCode != kCodeBf16>::kThreads, 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_cache, const __grid_constant__ CUtensorMap tmap_q,
                      DecodeParams p) {
-  using C = Cfg<HC, kInt8>;
+  constexpr bool kByte = kCode != kCodeBf16;  // 1-byte codes, expanded to fp16 in shared memory
+  constexpr bool kZp = kCode == kCodeInt8;    // per-token zero point (INT8)
+  using C = Cfg<HC, kByte>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Barriers* B = reinterpret_cast<Barriers*>(smem + C::kOffMisc);
@@ -249,7 +281,7 @@ __global__ void __launch_bounds__(Cfg<HC, kInt8>::kThreads, 1)
     walk.init(p.tile_start, p.seg_base, p.len, p.batch, int(S), pa, pb);
     const uint64_t pol_keep = policy_evict_last();
     auto load = [&](void* dst, int x, int y, uint64_t* bar) {
-      if (kL2Hints && !kInt8) tma_load_2d_hint(dst, &tmap_cache, x, y, bar, pol_keep);
+      if (kL2Hints && !kByte) tma_load_2d_hint(dst, &tmap_cache, x, y, bar, pol_keep);
       else tma_load_2d(dst, &tmap_cache, x, y, bar);
     };
     const uint32_t page_bytes = uint32_t(P) * 128;  // one 64-column box of P rows (bf16)
@@ -272,7 +304,7 @@ __global__ void __launch_bounds__(Cfg<HC, kInt8>::kThreads, 1)
       const int npg = pages.npg;
       int rows[kTile / 16];
       pages.rows(p, rows);
-      if constexpr (!kInt8) {
+      if constexpr (!kByte) {
         // the tile's boxes j = qr, qr + 2, ...: latent columns [64j, 64j + 64), box 8 the RoPE key
         for (int j = qr; j < 9; j += C::kQkRings, ++box_it) {
           const uint32_t slot = box_it % C::kQkRing;
@@ -309,7 +341,7 @@ __global__ void __launch_bounds__(Cfg<HC, kInt8>::kThreads, 1)
       }
     }
     if (!ok) fail(B, p.status);
-  } else if (!kInt8 && warp == C::kPvProducerWarp && lane == 0) {
+  } else if (!kByte && warp == C::kPvProducerWarp && lane == 0) {
     // ------------------------------------------------------------ PV-ring producer (bf16)
     // Each tile's latent columns again, pair by pair, for the PV product.
     TileWalker walk;
@@ -358,7 +390,7 @@ __global__ void __launch_bounds__(Cfg<HC, kInt8>::kThreads, 1)
     // read it) to finish.  Descriptors advance by one add per MMA.
     TileWalker walk;
     walk.init(p.tile_start, p.seg_base, p.len, p.batch, int(S), pa, pb);
-    constexpr uint32_t id_qk = idesc_f32acc(128, HC, false, false, kInt8);
+    constexpr uint32_t id_qk = idesc_f32acc(128, HC, false, false, kByte);
     constexpr uint64_t kDescK = smem_desc(0, 16, 1024, kSwizzle128B);  // K-major SW128
     uint32_t k = 0, seg = 0, box_it[2] = {0, 0};
     TileInfo t;
@@ -367,7 +399,7 @@ __global__ void __launch_bounds__(Cfg<HC, kInt8>::kThreads, 1)
       if (k >= 2 && !(ok = mbar_wait(&B->p_full[k & 1], ((k - 2) >> 1) & 1, abort_flag, kWaitLimitNs))) break;
       if (t.first && !(ok = mbar_wait(&B->q_full, seg & 1, abort_flag, kWaitLimitNs))) break;
       const uint32_t d_s = tmem + C::kColS + (k & 1) * HC;
-      if constexpr (!kInt8) {
+      if constexpr (!kByte) {
         for (int j = 0; j < 9; ++j) {
           const int r = j % C::kQkRings;
           const uint32_t slot = box_it[r] % C::kQkRing, par = (box_it[r] / C::kQkRing) & 1;
@@ -422,7 +454,7 @@ __global__ void __launch_bounds__(Cfg<HC, kInt8>::kThreads, 1)
     // The whole warp walks the tiles; lane 0 waits and issues.
     TileWalker walk;
     walk.init(p.tile_start, p.seg_base, p.len, p.batch, int(S), pa, pb);
-    constexpr uint32_t id_pv = idesc_f32acc(128, HC, true, true, kInt8);
+    constexpr uint32_t id_pv = idesc_f32acc(128, HC, true, true, kByte);
     constexpr uint64_t kDescMN = smem_desc(0, kBoxBytes, 1024, kSwizzle128B);  // MN-major SW128
     constexpr uint64_t kDescP = smem_desc(0, 128, 2048, kSwizzleNone);        // P^T core matrices
     uint32_t k = 0, seg = 0, pair_it = 0;
@@ -440,8 +472,8 @@ __global__ void __launch_bounds__(Cfg<HC, kInt8>::kThreads, 1)
       const uint64_t bd = kDescP | desc_addr(sbase + C::kOffP + (k & 1) * C::kPBytes);
 #pragma unroll 1
       for (int c = 0; c < 4; ++c) {
-        const uint32_t slot = kInt8 ? (4 * k + c) % C::kNumPair : pair_it % C::kNumPair;
-        if constexpr (!kInt8) {
+        const uint32_t slot = kByte ? (4 * k + c) % C::kNumPair : pair_it % C::kNumPair;
+        if constexpr (!kByte) {
           if (lane == 0) w = mbar_wait(&B->full_pair[slot], (pair_it / C::kNumPair) & 1, abort_flag, kWaitLimitNs);
           if (!(ok = __shfl_sync(0xffffffffu, w, 0))) break;
           ++pair_it;
@@ -482,8 +514,8 @@ __global__ void __launch_bounds__(Cfg<HC, kInt8>::kThreads, 1)
       mma_commit(&B->drain[1]);
       mbar_wait(&B->drain[1], 0, abort_flag, kWaitLimitNs);
     }
-  } else if (kInt8 && (warp == 3 || warp == 8)) {
-    if constexpr (kInt8) {
+  } else if (kByte && (warp == 3 || warp == 8)) {
+    if constexpr (kByte) {
       // ------------------------------------------------------------ INT8 expansion
       // Warps 3 and 8 turn each landed [128 x 64 B] code block into a swizzled
       // fp16 operand box.  Pair slots hold the codes of boxes 2c and 2c+1 in
@@ -506,7 +538,8 @@ __global__ void __launch_bounds__(Cfg<HC, kInt8>::kThreads, 1)
         for (int j = 0; j < 8; ++j) {
           const int r = r0 + 16 * j;
           uint4 lo, hi;
-          expand_codes(v[j], lo, hi);
+          if constexpr (kZp) expand_codes(v[j], lo, hi);
+          else expand_e4m3(v[j], lo, hi);
           uint8_t* row = dst + r * 128;
           *reinterpret_cast<uint4*>(row + (((2 * ch) ^ (r & 7)) << 4)) = lo;
           *reinterpret_cast<uint4*>(row + (((2 * ch + 1) ^ (r & 7)) << 4)) = hi;
@@ -553,9 +586,9 @@ __global__ void __launch_bounds__(Cfg<HC, kInt8>::kThreads, 1)
     while (walk.next(t)) {
       const uint32_t buf = tile_i & 1;
       const bool valid = st < t.valid;
-      float tok_s = 0.f, tok_z = 0.f;  // INT8: this row's scale and zero point
-      if (kInt8) {
-        if (t.first)
+      float tok_s = 0.f, tok_z = 0.f;  // 1-byte codes: this row's scale (and INT8 zero point)
+      if (kByte) {
+        if (kZp && t.first)
 #pragma unroll
           for (int h = 0; h < HC; ++h) {
             const float* qs = p.q_sum + (size_t(t.b) * p.heads + g * HC + h) * kQSumParts;
@@ -566,10 +599,14 @@ __global__ void __launch_bounds__(Cfg<HC, kInt8>::kThreads, 1)
           }
         if (valid) {
           const int tok = t.tile * kTile + st;
-          const float2 sz = *reinterpret_cast<const float2*>(p.scale_zero +
-                                                             (size_t(page_of(p, t.b, tok)) * P + tok % P) * 2);
-          tok_s = sz.x;
-          tok_z = sz.y;
+          const size_t row = size_t(page_of(p, t.b, tok)) * P + tok % P;
+          if (kZp) {
+            const float2 sz = *reinterpret_cast<const float2*>(p.scale_zero + row * 2);
+            tok_s = sz.x;
+            tok_z = sz.y;
+          } else {
+            tok_s = p.scale_zero[row];
+          }
         }
       }
       // S^T of this tile; and PV of tile k - 2, which read the P^T buffer
@@ -587,10 +624,10 @@ __global__ void __launch_bounds__(Cfg<HC, kInt8>::kThreads, 1)
           for (int i = 0; i < 16; ++i) x[h0 + i] = v[i];
         }
       }
-      const float row_scale = kInt8 ? p.scale_log2 * tok_s : p.scale_log2;
+      const float row_scale = kByte ? p.scale_log2 * tok_s : p.scale_log2;
 #pragma unroll
       for (int h = 0; h < HC; ++h) {
-        const float raw = kInt8 ? fmaf(-tok_z, qsum[h], x[h]) : x[h];
+        const float raw = kZp ? fmaf(-tok_z, qsum[h], x[h]) : x[h];
         x[h] = valid ? raw * row_scale : -INFINITY;
       }
       if (kCausal && causal_tile(p, t, walk.len_b)) causal_mask<HC>(x, p, g, walk.len_b, t.tile * kTile + st);
@@ -666,12 +703,14 @@ __global__ void __launch_bounds__(Cfg<HC, kInt8>::kThreads, 1)
         for (int i = 0; i < 4; ++i) {
           const int ha = h0 + 2 * i, hb = ha + 1;
           const float pa_ = exp2f(x[ha] - m_run[ha]), pb_ = exp2f(x[hb] - m_run[hb]);
-          if constexpr (kInt8) {
+          if constexpr (kByte) {
             const __half wa = __float2half_rn(pa_ * tok_s), wb = __float2half_rn(pb_ * tok_s);
             l_run[ha] += pa_;
             l_run[hb] += pb_;
-            corr[ha] = fmaf(__half2float(wa), tok_z, corr[ha]);
-            corr[hb] = fmaf(__half2float(wb), tok_z, corr[hb]);
+            if (kZp) {
+              corr[ha] = fmaf(__half2float(wa), tok_z, corr[ha]);
+              corr[hb] = fmaf(__half2float(wb), tok_z, corr[hb]);
+            }
             packed[i] = uint32_t(__half_as_ushort(wa)) | (uint32_t(__half_as_ushort(wb)) << 16);
           } else {
             const __nv_bfloat16 wa = __float2bfloat16_rn(pa_), wb = __float2bfloat16_rn(pb_);
@@ -700,7 +739,7 @@ __global__ void __launch_bounds__(Cfg<HC, kInt8>::kThreads, 1)
           for (int h = 0; h < HC; ++h) tmp[h] = l_run[h];
           const float ls = warp_transpose_reduce<HC, false>(tmp, lane);
           if (writer) rl[hw * 4 + q4] = ls;
-          if (kInt8) {
+          if (kZp) {
 #pragma unroll
             for (int h = 0; h < HC; ++h) tmp[h] = corr[h];
             const float cs = warp_transpose_reduce<HC, false>(tmp, lane);
@@ -714,7 +753,7 @@ __global__ void __launch_bounds__(Cfg<HC, kInt8>::kThreads, 1)
           const float4 l4 = reinterpret_cast<const float4*>(rl)[h];
           const float l = (l4.x + l4.y) + (l4.z + l4.w);
           inv_l[h] = l > 0.f ? 1.f / l : 0.f;  // 0: a row with no visible token (multi-token decode)
-          if (kInt8) {
+          if (kZp) {
             const float4 c4 = reinterpret_cast<const float4*>(rc)[h];
             corr[h] = (c4.x + c4.y) + (c4.z + c4.w);
           }
@@ -728,7 +767,7 @@ __global__ void __launch_bounds__(Cfg<HC, kInt8>::kThreads, 1)
             tmem_ld16(tmem + lane_off + C::kColO + c * HC + h0, v);
 #pragma unroll
             for (int i = 0; i < 16; ++i)
-              dst[(h0 + i) * kLatent + c * 128 + st] = (kInt8 ? v[i] - corr[h0 + i] : v[i]) * inv_l[h0 + i];
+              dst[(h0 + i) * kLatent + c * 128 + st] = (kZp ? v[i] - corr[h0 + i] : v[i]) * inv_l[h0 + i];
           }
         tc_fence_before();
         mbar_arrive(&B->o_free);
@@ -753,39 +792,42 @@ __global__ void __launch_bounds__(Cfg<HC, kInt8>::kThreads, 1)
 }
 
 // ----- host side: tensor maps and launch ---------------------------------------
-template <int HC, bool kInt8>
+template <int HC, int kCode>
 cudaError_t launch_tc(const DecodeParams& p, int grid, cudaStream_t stream) {
+  constexpr bool kByte = kCode != kCodeBf16;
+  using C = Cfg<HC, kByte>;
   CUtensorMap mc, mq;
   const uint64_t rows = uint64_t(p.num_pages) * p.page_size;
-  if (!make_map_2d(&mc, p.cache, kInt8 ? 1 : 2, kRow, rows, 64, p.page_size,
-                   kInt8 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B))
+  if (!make_map_2d(&mc, p.cache, kByte ? 1 : 2, kRow, rows, 64, p.page_size,
+                   kByte ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
-  // q_full holds bf16 (or, for INT8 caches, fp16) values; TMA moves 2-byte elements either way
+  // q_full holds bf16 (or, for 1-byte caches, fp16) values; TMA moves 2-byte elements either way
   if (!make_map_2d(&mq, p.q_full, 2, kRow, uint64_t(p.batch) * p.heads, 64, HC, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   static bool attr[128] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 128 || !attr[dev]) {
-    for (auto* k : {decode_tc_kernel<HC, kInt8, false>, decode_tc_kernel<HC, kInt8, true>}) {
-      const cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 int(Cfg<HC, kInt8>::kSmem));
+    for (auto* k : {decode_tc_kernel<HC, kCode, false>, decode_tc_kernel<HC, kCode, true>}) {
+      const cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, int(C::kSmem));
       if (e != cudaSuccess) return e;
     }
     if (dev >= 0 && dev < 128) attr[dev] = true;
   }
-  auto* kernel = p.q_len > 1 ? decode_tc_kernel<HC, kInt8, true> : decode_tc_kernel<HC, kInt8, false>;
-  return launch_pdl(kernel, dim3(grid), dim3(Cfg<HC, kInt8>::kThreads), Cfg<HC, kInt8>::kSmem, stream, 1, mc, mq, p);
+  auto* kernel = p.q_len > 1 ? decode_tc_kernel<HC, kCode, true> : decode_tc_kernel<HC, kCode, false>;
+  return launch_pdl(kernel, dim3(grid), dim3(C::kThreads), C::kSmem, stream, 1, mc, mq, p);
 }
 
 }  // namespace
 
-// Head-group size the attention kernel uses for `heads` query heads.
-int decode_head_group(int heads, bool int8) { return (!int8 && heads % 32 == 0) ? 32 : 16; }
+// Head-group size the attention kernel uses for `heads` query heads (1-byte
+// caches: 16, the expansion warps' register budget).
+int decode_head_group(int heads, bool byte_cache) { return (!byte_cache && heads % 32 == 0) ? 32 : 16; }
 
-cudaError_t launch_decode_tc(const DecodeParams& p, int hc, bool int8, int grid, cudaStream_t stream) {
-  if (int8) return launch_tc<16, true>(p, grid, stream);
-  return hc == 16 ? launch_tc<16, false>(p, grid, stream) : launch_tc<32, false>(p, grid, stream);
+cudaError_t launch_decode_tc(const DecodeParams& p, int hc, int code, int grid, cudaStream_t stream) {
+  if (code == kCodeInt8) return launch_tc<16, kCodeInt8>(p, grid, stream);
+  if (code == kCodeE4m3) return launch_tc<16, kCodeE4m3>(p, grid, stream);
+  return hc == 16 ? launch_tc<16, kCodeBf16>(p, grid, stream) : launch_tc<32, kCodeBf16>(p, grid, stream);
 }
 
 }  // namespace mla

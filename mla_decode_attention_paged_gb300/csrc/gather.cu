@@ -19,7 +19,7 @@ namespace mla {
 constexpr int kGatherEntries = 64;   // list entries per CTA
 constexpr int kGatherThreads = 256;  // 8 warps; a warp copies one row at a time
 
-template <bool kInt8>
+template <int kCode>
 __global__ void __launch_bounds__(kGatherThreads) gather_kernel(GatherParams p) {
   __shared__ int cnt[kGatherThreads / 32];   // per warp: valid entries before the chunk
   __shared__ int chunk_cnt[kGatherEntries / 32];  // per warp of the chunk: its valid entries
@@ -76,15 +76,16 @@ __global__ void __launch_bounds__(kGatherThreads) gather_kernel(GatherParams p) 
   __syncthreads();
   // copy the rows: warp w takes entries w, w + 8, ...
   const size_t base_row = size_t(b) * p.pages_per_seq * P;
-  constexpr int kRowBytes = kInt8 ? 576 : 1152, kPieces = kRowBytes / 16;
+  constexpr int kRowBytes = kCode == kCodeBf16 ? 1152 : 576, kPieces = kRowBytes / 16;
   for (int e = warp; e < kGatherEntries; e += kGatherThreads / 32) {
     const int d = dest[e];
     if (d < 0) continue;
     const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(p.cache) + size_t(srow[e]) * kRowBytes);
     uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.out_cache) + (base_row + d) * kRowBytes);
     for (int q = lane; q < kPieces; q += 32) dst[q] = src[q];
-    if (kInt8 && lane == 0)
+    if (kCode == kCodeInt8 && lane == 0)
       reinterpret_cast<float2*>(p.out_scale_zero)[base_row + d] = reinterpret_cast<const float2*>(p.scale_zero)[srow[e]];
+    if (kCode == kCodeE4m3 && lane == 0) p.out_scale_zero[base_row + d] = p.scale_zero[srow[e]];
   }
   // the last chunk of a sequence writes its length and page-table row
   if (blockIdx.x == gridDim.x - 1) {
@@ -93,10 +94,11 @@ __global__ void __launch_bounds__(kGatherThreads) gather_kernel(GatherParams p) 
   }
 }
 
-cudaError_t launch_gather(const GatherParams& p, bool int8, cudaStream_t stream) {
+cudaError_t launch_gather(const GatherParams& p, int code, cudaStream_t stream) {
   const dim3 grid((p.top_k + kGatherEntries - 1) / kGatherEntries, p.batch);
-  return int8 ? launch_pdl(gather_kernel<true>, grid, dim3(kGatherThreads), 0, stream, 1, p)
-              : launch_pdl(gather_kernel<false>, grid, dim3(kGatherThreads), 0, stream, 1, p);
+  if (code == kCodeInt8) return launch_pdl(gather_kernel<kCodeInt8>, grid, dim3(kGatherThreads), 0, stream, 1, p);
+  if (code == kCodeE4m3) return launch_pdl(gather_kernel<kCodeE4m3>, grid, dim3(kGatherThreads), 0, stream, 1, p);
+  return launch_pdl(gather_kernel<kCodeBf16>, grid, dim3(kGatherThreads), 0, stream, 1, p);
 }
 
 }  // namespace mla

@@ -22,6 +22,13 @@ std::atomic<int> g_force_single_cta{0};
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// Element code of the cache rows; 1-byte codes (INT8, FP8) carry per-token scales.
+int cache_code(const mla_dims* d) {
+  return d->cache_dtype == MLA_CACHE_INT8 ? kCodeInt8 : d->cache_dtype == MLA_CACHE_FP8 ? kCodeE4m3 : kCodeBf16;
+}
+// Bytes of per-token quantisation parameters: (scale, zero point) or a scale.
+size_t scale_bytes_per_row(int code) { return code == kCodeInt8 ? 8 : code == kCodeE4m3 ? 4 : 0; }
+
 int sm_count() {
   static int cached[128] = {};
   int dev = 0;
@@ -42,13 +49,13 @@ mla_dims row_dims(const mla_dims* d, int q_len) {
 }
 
 // Automatic split count: one partition per resident attention unit of a
-// head group -- a CTA cluster for bf16 caches, a CTA for INT8 caches (more
+// head group -- a CTA cluster for bf16 caches, a CTA for 1-byte caches (more
 // partitions only add segment switches and partials to merge).
 int effective_splits(const mla_dims* d, int num_splits) {
   if (num_splits > 0) return num_splits;
-  const bool int8 = d->cache_dtype == MLA_CACHE_INT8;
-  const int hc = decode_head_group(d->num_heads, int8);
-  const int clusters = int8 || g_force_single_cta.load() ? 0 : decode_pair_capacity(hc);
+  const bool byte = cache_code(d) != kCodeBf16;
+  const int hc = decode_head_group(d->num_heads, byte);
+  const int clusters = byte || g_force_single_cta.load() ? 0 : decode_pair_capacity(hc);
   const int n = clusters > 0 ? clusters : sm_count();
   if (n <= 0) return -1;
   const int groups = d->num_heads / hc;
@@ -85,7 +92,8 @@ int mla_check_dims(const mla_dims* d) {
   if (d->num_heads <= 0 || d->kv_lora_rank <= 0 || d->rope_dim <= 0 || d->qk_nope_dim <= 0 ||
       d->v_head_dim <= 0 || d->page_size <= 0)
     return MLA_ERR_INVALID_ARG;
-  if (d->cache_dtype != MLA_CACHE_BF16 && d->cache_dtype != MLA_CACHE_INT8) return MLA_ERR_INVALID_ARG;
+  if (d->cache_dtype != MLA_CACHE_BF16 && d->cache_dtype != MLA_CACHE_INT8 && d->cache_dtype != MLA_CACHE_FP8)
+    return MLA_ERR_INVALID_ARG;
   if (d->kv_lora_rank != kLatent || d->rope_dim != kRope || d->qk_nope_dim != kNope || d->v_head_dim != kVDim)
     return MLA_ERR_UNSUPPORTED;
   if (d->page_size != 16 && d->page_size != 32 && d->page_size != 64 && d->page_size != 128)
@@ -102,11 +110,12 @@ int mla_cache_append(const mla_dims* d, void* cache, float* cache_scale_zero, in
   if (st != MLA_OK) return st;
   if (n_tokens < 0 || num_pages <= 0 || num_seqs <= 0 || max_pages_per_seq <= 0) return MLA_ERR_INVALID_ARG;
   if (n_tokens == 0) return MLA_OK;
-  const bool int8 = d->cache_dtype == MLA_CACHE_INT8;
+  const int code = cache_code(d);
+  const bool byte = code != kCodeBf16;
   if (!cache || !block_table || !seq_ids || !positions || !c_kv || !k_pe) return MLA_ERR_INVALID_ARG;
-  if (int8 && !cache_scale_zero) return MLA_ERR_INVALID_ARG;
+  if (byte && !cache_scale_zero) return MLA_ERR_INVALID_ARG;
   if (!aligned(cache, 16) || !aligned(c_kv, 16) || !aligned(k_pe, 4) || !aligned(block_table, 4) ||
-      !aligned(seq_ids, 4) || !aligned(positions, 4) || (int8 && !aligned(cache_scale_zero, 8)))
+      !aligned(seq_ids, 4) || !aligned(positions, 4) || (byte && !aligned(cache_scale_zero, 8)))
     return MLA_ERR_INVALID_ARG;
   AppendParams p;
   p.cache = cache;
@@ -126,7 +135,7 @@ int mla_cache_append(const mla_dims* d, void* cache, float* cache_scale_zero, in
   p.max_pages = max_pages_per_seq;
   p.num_pages = num_pages;
   p.page_size = d->page_size;
-  return launch_append(p, int8, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+  return launch_append(p, code, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 
 int mla_auto_num_splits(const mla_dims* d, int32_t batch) {
@@ -182,15 +191,16 @@ int decode_rows(const mla_dims* d, const void* q_nope, const void* q_pe, const v
                 void* out, float* lse_out, mla_stream_t stream, bool reset_status) {
   int st = mla_check_dims(d);
   if (st != MLA_OK) return st;
-  const bool int8 = d->cache_dtype == MLA_CACHE_INT8;
+  const int code = cache_code(d);
+  const bool byte = code != kCodeBf16;
   if (batch <= 0 || num_pages <= 0 || max_pages_per_seq <= 0 || num_splits < 0) return MLA_ERR_INVALID_ARG;
   if (q_len < 1 || q_len > MLA_MAX_Q_LEN) return MLA_ERR_INVALID_ARG;
   if (!(softmax_scale > 0.f) || softmax_scale == INFINITY) return MLA_ERR_INVALID_ARG;
   if (!q_nope || !q_pe || !cache || !block_table || !seq_lens || !W_UK || !W_UV || !out) return MLA_ERR_INVALID_ARG;
-  if (int8 && !cache_scale_zero) return MLA_ERR_INVALID_ARG;
+  if (byte && !cache_scale_zero) return MLA_ERR_INVALID_ARG;
   if (!aligned(cache, 16) || !aligned(q_nope, 4) || !aligned(q_pe, 4) || !aligned(W_UK, 4) || !aligned(W_UV, 4) ||
       !aligned(out, 4) || !aligned(block_table, 4) || !aligned(seq_lens, 4) || (lse_out && !aligned(lse_out, 4)) ||
-      (int8 && !aligned(cache_scale_zero, 16)))
+      (byte && !aligned(cache_scale_zero, 16)))
     return MLA_ERR_INVALID_ARG;
   if ((long long)max_pages_per_seq * d->page_size > (1LL << 31) - 1) return MLA_ERR_INVALID_ARG;
   if ((long long)num_pages * d->page_size > (1LL << 31) - 1) return MLA_ERR_INVALID_ARG;  // row index is int32
@@ -200,7 +210,7 @@ int decode_rows(const mla_dims* d, const void* q_nope, const void* q_pe, const v
   const WorkspaceLayout L = workspace_layout(batch, dr.num_heads, S);
   if (!workspace || !aligned(workspace, 256) || workspace_bytes < L.total) return MLA_ERR_WORKSPACE;
 
-  const int H = dr.num_heads, hc = decode_head_group(H, int8), groups = H / hc;
+  const int H = dr.num_heads, hc = decode_head_group(H, byte), groups = H / hc;
   char* ws = static_cast<char*>(workspace);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 
@@ -221,7 +231,7 @@ int decode_rows(const mla_dims* d, const void* q_nope, const void* q_pe, const v
   ap.reset_status = reset_status ? 1 : 0;
   ap.max_len = max_pages_per_seq * d->page_size;
   ap.num_splits = S;
-  if (launch_absorb(ap, int8, s) != cudaSuccess) return MLA_ERR_CUDA;
+  if (launch_absorb(ap, byte, s) != cudaSuccess) return MLA_ERR_CUDA;
 
   DecodeParams dp;
   dp.q_full = ap.q_full;
@@ -247,16 +257,16 @@ int decode_rows(const mla_dims* d, const void* q_nope, const void* q_pe, const v
   dp.heads_w = d->num_heads;
   dp.scale_log2 = softmax_scale * kLog2e;
   dp.inject_wait_timeout = g_inject_wait_timeout.load();
-  // bf16 caches run on CTA pairs (two SMs share each tile); INT8 caches, and
-  // devices that cannot place the pairs, on single CTAs
-  const int pair_cap = int8 || g_force_single_cta.load() ? 0 : decode_pair_capacity(hc);
+  // bf16 caches run on CTA pairs (two SMs share each tile); 1-byte caches,
+  // and devices that cannot place the pairs, on single CTAs
+  const int pair_cap = byte || g_force_single_cta.load() ? 0 : decode_pair_capacity(hc);
   const int units = pair_cap > 0 ? pair_cap : sm_count();
   const int per_group = units / groups > 0 ? units / groups : 1;
   const int per_group_used = S < per_group ? S : per_group;
   cudaEvent_t ev0 = g_ev_start.load(), ev1 = g_ev_stop.load();
   if (ev0 && ev1 && cudaEventRecord(ev0, s) != cudaSuccess) return MLA_ERR_CUDA;
   const cudaError_t le = pair_cap > 0 ? launch_decode_pair(dp, hc, per_group_used, s)
-                                      : launch_decode_tc(dp, hc, int8, per_group_used * groups, s);
+                                      : launch_decode_tc(dp, hc, code, per_group_used * groups, s);
   if (le != cudaSuccess) return MLA_ERR_CUDA;
   if (ev0 && ev1 && cudaEventRecord(ev1, s) != cudaSuccess) return MLA_ERR_CUDA;
 
@@ -278,7 +288,7 @@ int decode_rows(const mla_dims* d, const void* q_nope, const void* q_pe, const v
 
 // Workspace of mla_decode_sparse: the decode's own workspace first (so that
 // the call's status word is the workspace's first 4 bytes), then the
-// gathered cache [batch * pps pages, P, 576] (+ INT8 scale/zero), its page
+// gathered cache [batch * pps pages, P, 576] (+ per-token scales), its page
 // table [batch, pps] and lengths [batch]; pps = ceil(top_k / P).
 struct SparseLayout {
   size_t decode, cache, scale_zero, table, lens, total;
@@ -287,13 +297,13 @@ struct SparseLayout {
 
 SparseLayout sparse_layout(const mla_dims* d, int batch, int top_k, size_t decode_bytes) {
   SparseLayout L;
-  const bool int8 = d->cache_dtype == MLA_CACHE_INT8;
+  const int code = cache_code(d);
   L.pps = (top_k + d->page_size - 1) / d->page_size;
   const size_t rows = size_t(batch) * L.pps * d->page_size;
   size_t off = 0;
   L.decode = off;      off = align256(off + decode_bytes);
-  L.cache = off;       off = align256(off + rows * (int8 ? 576 : 1152));
-  L.scale_zero = off;  off = align256(off + (int8 ? rows * 8 : 0));
+  L.cache = off;       off = align256(off + rows * (code == kCodeBf16 ? 1152 : 576));
+  L.scale_zero = off;  off = align256(off + rows * scale_bytes_per_row(code));
   L.table = off;       off = align256(off + size_t(batch) * L.pps * 4);
   L.lens = off;        off = align256(off + size_t(batch) * 4);
   L.total = off;
@@ -319,12 +329,13 @@ int mla_decode_sparse(const mla_dims* d, const void* q_nope, const void* q_pe, c
                       float* lse_out, mla_stream_t stream) {
   int st = mla_check_dims(d);
   if (st != MLA_OK) return st;
-  const bool int8 = d->cache_dtype == MLA_CACHE_INT8;
+  const int code = cache_code(d);
+  const bool byte = code != kCodeBf16;
   if (batch <= 0 || num_pages <= 0 || max_pages_per_seq <= 0 || num_splits < 0) return MLA_ERR_INVALID_ARG;
   if (top_k < 1 || top_k > MLA_MAX_TOP_K || !token_indices || !aligned(token_indices, 4)) return MLA_ERR_INVALID_ARG;
-  if (!cache || !block_table || !seq_lens || (int8 && !cache_scale_zero)) return MLA_ERR_INVALID_ARG;
+  if (!cache || !block_table || !seq_lens || (byte && !cache_scale_zero)) return MLA_ERR_INVALID_ARG;
   if (!aligned(cache, 16) || !aligned(block_table, 4) || !aligned(seq_lens, 4) ||
-      (int8 && !aligned(cache_scale_zero, 8)))
+      (byte && !aligned(cache_scale_zero, 8)))
     return MLA_ERR_INVALID_ARG;
   if ((long long)max_pages_per_seq * d->page_size > (1LL << 31) - 1) return MLA_ERR_INVALID_ARG;
   if ((long long)num_pages * d->page_size > (1LL << 31) - 1) return MLA_ERR_INVALID_ARG;
@@ -345,7 +356,7 @@ int mla_decode_sparse(const mla_dims* d, const void* q_nope, const void* q_pe, c
   gp.seq_lens = seq_lens;
   gp.indices = token_indices;
   gp.out_cache = ws + L.cache;
-  gp.out_scale_zero = int8 ? reinterpret_cast<float*>(ws + L.scale_zero) : nullptr;
+  gp.out_scale_zero = byte ? reinterpret_cast<float*>(ws + L.scale_zero) : nullptr;
   gp.out_table = reinterpret_cast<int*>(ws + L.table);
   gp.out_lens = reinterpret_cast<int*>(ws + L.lens);
   gp.status = status;
@@ -355,7 +366,7 @@ int mla_decode_sparse(const mla_dims* d, const void* q_nope, const void* q_pe, c
   gp.num_pages = num_pages;
   gp.page_size = d->page_size;
   gp.pages_per_seq = L.pps;
-  if (launch_gather(gp, int8, s) != cudaSuccess) return MLA_ERR_CUDA;
+  if (launch_gather(gp, code, s) != cudaSuccess) return MLA_ERR_CUDA;
   // the dense decode over the gathered rows, with the lengths the gather wrote
   return decode_rows(d, q_nope, q_pe, gp.out_cache, gp.out_scale_zero, batch * L.pps, gp.out_table, L.pps,
                      gp.out_lens, batch, 1, W_UK, W_UV, softmax_scale, num_splits, ws + L.decode, dec, out, lse_out,

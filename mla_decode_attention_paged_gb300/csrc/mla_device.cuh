@@ -175,7 +175,7 @@ struct DecodeParams {
   const __nv_bfloat16* q_full;   // [B, H, 576]
   const float* q_sum;            // [B, H, kQSumParts] (INT8)
   const void* cache;             // bf16 or int8 [num_pages, P, 576]
-  const float* scale_zero;       // [num_pages, P, 2] (INT8)
+  const float* scale_zero;       // [num_pages, P, 2] (INT8) or [num_pages, P] (FP8)
   const int* block_table;        // [B, max_pages]
   const int* tile_start;
   const int* seg_base;

@@ -8,6 +8,11 @@
 
 namespace mla {
 
+// Element type of the cached rows (mla_cache_dtype): bf16 values, INT8 codes
+// with a per-token (scale, zero point), or FP8 E4M3 codes with a per-token
+// scale.
+enum CacheCode : int { kCodeBf16 = 0, kCodeInt8 = 1, kCodeE4m3 = 2 };
+
 // Multi-token decode (q_len query tokens per sequence) runs the same kernels
 // over "rows": row v = t * heads_w + h of a sequence is query token t, head
 // h.  `heads` below counts rows (q_len * heads_w); the weights have heads_w
@@ -16,7 +21,7 @@ struct AbsorbParams {
   const __nv_bfloat16* q_nope;  // [B, heads, 128]
   const __nv_bfloat16* q_pe;    // [B, heads, 64]
   const __nv_bfloat16* W_UK;    // [heads_w, 128, 512]
-  __nv_bfloat16* q_full;        // [B, H, 576] (fp16 bit patterns for INT8 caches)
+  __nv_bfloat16* q_full;        // [B, H, 576] (fp16 bit patterns for 1-byte caches)
   float* q_sum;                 // [B, H, kQSumParts]
   // plan
   const int* seq_lens;
@@ -32,13 +37,13 @@ struct AbsorbParams {
 // order into pages_per_seq pages of the gathered cache (sequence b owns pages
 // [b pages_per_seq, (b + 1) pages_per_seq)), its length and page-table row.
 struct GatherParams {
-  const void* cache;         // bf16 or int8 [num_pages, P, 576]
-  const float* scale_zero;   // [num_pages, P, 2] (INT8)
+  const void* cache;         // bf16, int8 or e4m3 [num_pages, P, 576]
+  const float* scale_zero;   // [num_pages, P, 2] (INT8) or [num_pages, P] (FP8)
   const int* block_table;    // [B, max_pages]
   const int* seq_lens;       // [B]
   const int* indices;        // [B, top_k], -1 = padding
   void* out_cache;           // [B * pages_per_seq, P, 576]
-  float* out_scale_zero;     // [B * pages_per_seq, P, 2] (INT8)
+  float* out_scale_zero;     // [B * pages_per_seq, P, 2] (INT8) or [.., P] (FP8)
   int* out_table;            // [B, pages_per_seq]
   int* out_lens;             // [B]
   int* status;               // MLA_ERR_DEVICE_BOUNDS for bad entries (zeroed on the stream before the launch)
@@ -46,8 +51,8 @@ struct GatherParams {
 };
 
 struct AppendParams {
-  void* cache;                   // bf16 or int8 [num_pages, P, 576]
-  float* scale_zero;             // [num_pages, P, 2] (INT8)
+  void* cache;                   // bf16, int8 or e4m3 [num_pages, P, 576]
+  float* scale_zero;             // [num_pages, P, 2] (INT8) or [num_pages, P] (FP8)
   const int* block_table;        // [num_seqs, max_pages]
   const int* seq_ids;            // [N]
   const int* positions;          // [N]
@@ -80,12 +85,12 @@ struct CombineParams {
 };
 
 cudaError_t launch_absorb(const AbsorbParams& p, bool fp16_out, cudaStream_t stream);
-cudaError_t launch_append(const AppendParams& p, bool int8, cudaStream_t stream);
+cudaError_t launch_append(const AppendParams& p, int code, cudaStream_t stream);
 cudaError_t launch_combine_uv(const CombineUVParams& p, cudaStream_t stream);
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream);
-cudaError_t launch_gather(const GatherParams& p, bool int8, cudaStream_t stream);
-cudaError_t launch_decode_tc(const DecodeParams& p, int hc, bool int8, int grid, cudaStream_t stream);
-int decode_head_group(int heads, bool int8);
+cudaError_t launch_gather(const GatherParams& p, int code, cudaStream_t stream);
+cudaError_t launch_decode_tc(const DecodeParams& p, int hc, int code, int grid, cudaStream_t stream);
+int decode_head_group(int heads, bool byte_cache);
 // Launches `kernel` with programmatic dependent launch (and, if cluster_x > 1,
 // thread-block clusters of cluster_x CTAs).  The kernels of the decode step
 // (append, absorb, attention, merge + up-projection) set up their shared

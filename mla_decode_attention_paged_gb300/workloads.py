@@ -41,6 +41,16 @@ class Workload:
     rope_theta: float = 10000.0     # used where the cache is built through the append
     q_len: int = 1                  # query tokens per sequence (multi-token decode: the last q_len cached)
     top_k: int = 0                  # sparse decode: attend to top_k drawn positions per sequence (0: all)
+    fp8: bool = False               # cache built from N(0,1) rows by the FP8 (E4M3) append
+
+    @property
+    def quantised(self) -> bool:
+        """1-byte cache (INT8 or FP8) with per-token scales, built through an append."""
+        return self.int8 or self.fp8
+
+    @property
+    def cache_format(self) -> str:
+        return "int8" if self.int8 else "fp8" if self.fp8 else "bf16"
 
     @property
     def softmax_scale(self) -> float:
@@ -65,6 +75,8 @@ WORKLOADS = {
                             q_len=4),
     # the V2-Lite batch over an INT8 cache (half the bytes per token)
     "int8_v2lite": Workload("int8_v2lite_b32_h16_l32768_p64", 32, 16, 32768, 64, True, 1.0, 0.02, 1.0, 8, int8=True),
+    # the V2-Lite batch over an FP8 (E4M3) cache with one scale per token
+    "fp8_v2lite": Workload("fp8_v2lite_b32_h16_l32768_p64", 32, 16, 32768, 64, True, 1.0, 0.02, 1.0, 9, fp8=True),
     # sparse decode (DeepSeek Sparse Attention's top-2048 selection) over the V2-Lite cache
     "v2lite_topk2048": Workload("v2lite_topk2048_b32_h16_l32768_p64", 32, 16, 32768, 64, True, 1.0, 0.02, 1.0, 7,
                                 top_k=2048),
@@ -133,11 +145,23 @@ def draw_int8_cache(num_pages: int, page_size: int, g: torch.Generator):
     return codes, torch.stack([scale, zp], dim=-1).contiguous()
 
 
+def draw_fp8_cache(num_pages: int, page_size: int, g: torch.Generator):
+    """Random FP8 E4M3 codes uint8 [num_pages, P, 576] -- uniform over the 254
+    finite codes (0x7F and 0xFF, the NaN patterns, are skipped) -- and scales
+    fp32 [num_pages, P] uniform in [0.002, 0.01], for decode-only tests of the
+    quantised cache."""
+    v = torch.randint(0, 254, (num_pages, page_size, LATENT_DIM + ROPE_DIM), generator=g, device=g.device,
+                      dtype=torch.int32)
+    codes = (v + (v >= 0x7F).to(torch.int32)).to(torch.uint8)
+    scale = torch.rand((num_pages, page_size), generator=g, device=g.device) * 0.008 + 0.002
+    return codes, scale.contiguous()
+
+
 def make_decode_inputs(w: Workload, device="cpu"):
     """All inputs of one decode step for workload ``w``, drawn on ``device``.
 
     bf16 workloads: the physical cache pool is filled directly with
-    N(0, cache_std) values.  INT8 workloads: the generator returns N(0, 1)
+    N(0, cache_std) values.  INT8 and FP8 workloads: the generator returns N(0, 1)
     source rows (latent and RoPE key) for every token of every sequence, to be
     written through the append of whichever side is under test; no cache is
     drawn.
@@ -147,7 +171,7 @@ def make_decode_inputs(w: Workload, device="cpu"):
     table, num_pages = draw_page_table(seq_lens, w.page_size, w.shuffled, g)
     d = dict(workload=w, seq_lens=seq_lens.to(device), block_table=table.to(device), num_pages=num_pages,
              page_size=w.page_size, scale=w.softmax_scale)
-    if not w.int8:
+    if not w.quantised:
         d["cache"] = draw_bf16((num_pages, w.page_size, LATENT_DIM + ROPE_DIM), w.cache_std, g)
     d["W_UK"] = draw_bf16((w.heads, NOPE_DIM, LATENT_DIM), w.w_std, g)
     d["W_UV"] = draw_bf16((w.heads, V_DIM, LATENT_DIM), w.w_std, g)
@@ -156,7 +180,7 @@ def make_decode_inputs(w: Workload, device="cpu"):
     d["q_pe"] = draw_bf16(qshape + (ROPE_DIM,), w.q_std, g)
     if w.top_k:
         d["token_indices"] = draw_token_indices(seq_lens.cpu(), w.top_k, 1.0, g).to(device)
-    if w.int8:
+    if w.quantised:
         total = int(seq_lens.to(torch.int64).sum())
         d["src_c_kv"] = draw_bf16((total, LATENT_DIM), 1.0, g)
         d["src_k_pe"] = draw_bf16((total, ROPE_DIM), 1.0, g)

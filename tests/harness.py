@@ -25,18 +25,20 @@ def f64(t: torch.Tensor) -> np.ndarray:
 
 
 def dims_of(w: W.Workload) -> mla.Dims:
-    return mla.dims(w.heads, w.page_size, int8=w.int8)
+    return mla.dims(w.heads, w.page_size, int8=w.int8, fp8=w.fp8)
 
 
 def gpu_cache(inp: dict, w: W.Workload, rope_theta: float | None = None):
-    """Device cache for the library: the drawn bf16 pool, or for INT8 workloads
-    the pool built from the drawn source rows by the library's own append."""
-    if not w.int8:
+    """Device cache for the library: the drawn bf16 pool, or for INT8 / FP8
+    workloads the pool built from the drawn source rows by the library's own
+    append."""
+    if not w.quantised:
         return inp["cache"].cuda(), None
     theta = w.rope_theta if rope_theta is None else rope_theta
     npg, P = inp["num_pages"], w.page_size
-    cache = torch.zeros((npg, P, W.LATENT_DIM + W.ROPE_DIM), dtype=torch.int8, device="cuda")
-    sz = torch.zeros((npg, P, 2), dtype=torch.float32, device="cuda")
+    cache = torch.zeros((npg, P, W.LATENT_DIM + W.ROPE_DIM), dtype=torch.int8 if w.int8 else torch.uint8,
+                        device="cuda")
+    sz = torch.zeros((npg, P, 2) if w.int8 else (npg, P), dtype=torch.float32, device="cuda")
     mla.cache_append(dims_of(w), cache, sz, inp["block_table"].cuda(), inp["src_seq_ids"].cuda(),
                      inp["src_positions"].cuda(), inp["src_c_kv"].cuda(), inp["src_k_pe"].cuda(), theta)
     return cache, sz
@@ -55,19 +57,20 @@ def oracle_cache(inp: dict, w: W.Workload, seqs, rope_theta: float | None = None
         n = (lens[b] + P - 1) // P
         sub[b, :n] = [remap[int(p)] for p in table[b, :n]]
     npg = max(len(pages), 1)
-    if not w.int8:
+    if not w.quantised:
         idx = torch.tensor(pages, dtype=torch.int64, device=inp["cache"].device)
         cache = W.bf16_to_bits(inp["cache"].index_select(0, idx)) if pages else np.zeros((1, P, 576), np.uint16)
         return cache, None, sub
     theta = w.rope_theta if rope_theta is None else rope_theta
-    cache = np.zeros((npg, P, 576), np.int8)
-    sz = np.zeros((npg, P, 2), np.float32)
+    cache = np.zeros((npg, P, 576), np.int8 if w.int8 else np.uint8)
+    sz = np.zeros((npg, P, 2) if w.int8 else (npg, P), np.float32)
     starts = np.concatenate([[0], np.cumsum(lens)])
     for b in seqs:
         a, e = int(starts[b]), int(starts[b + 1])
         c_bits = W.bf16_to_bits(inp["src_c_kv"][a:e])
         k_bits = W.bf16_to_bits(inp["src_k_pe"][a:e])
-        O.append_tokens(cache, sz, sub, [b] * (e - a), list(range(e - a)), c_bits, k_bits, theta, P, int8=True)
+        O.append_tokens(cache, sz, sub, [b] * (e - a), list(range(e - a)), c_bits, k_bits, theta, P,
+                        int8=w.int8, fp8=w.fp8)
     return cache, sz, sub
 
 
@@ -76,7 +79,7 @@ def oracle_decode(inp: dict, w: W.Workload, pairs, absorbed=False, rope_theta=No
     cache, sz, table = cache_override if cache_override is not None else oracle_cache(inp, w, seqs, rope_theta)
     lens = inp["seq_lens"].cpu().numpy()
     return O.decode(f64(inp["q_nope"]), f64(inp["q_pe"]), cache, sz, table, lens, f64(inp["W_UK"]),
-                    f64(inp["W_UV"]), inp["scale"], w.page_size, w.int8, pairs=pairs, absorbed=absorbed)
+                    f64(inp["W_UV"]), inp["scale"], w.page_size, w.int8, pairs=pairs, absorbed=absorbed, fp8=w.fp8)
 
 
 def gpu_decode(inp: dict, w: W.Workload, cache, sz, num_splits=0, block_table=None):

@@ -43,6 +43,8 @@ def test_version_and_status_strings(lib):
 def test_check_dims(lib):
     assert mla.check_dims(mla.dims(16, 64)) == mla.MLA_OK
     assert mla.check_dims(mla.dims(128, 16, int8=True)) == mla.MLA_OK
+    assert mla.check_dims(mla.dims(16, 64, fp8=True)) == mla.MLA_OK
+    assert mla.check_dims(mla.dims(128, 128, fp8=True)) == mla.MLA_OK
     assert mla.check_dims(mla.dims(64, 32)) == mla.MLA_OK
     assert mla.check_dims(mla.dims(24, 64)) == mla.MLA_ERR_UNSUPPORTED
     assert mla.check_dims(mla.dims(16, 48)) == mla.MLA_ERR_UNSUPPORTED
@@ -50,6 +52,8 @@ def test_check_dims(lib):
     assert mla.check_dims(mla.dims(0, 64)) == mla.MLA_ERR_INVALID_ARG
     d = mla.dims(16, 64)
     d.cache_dtype = 7
+    assert mla.check_dims(d) == mla.MLA_ERR_INVALID_ARG
+    d.cache_dtype = 3
     assert mla.check_dims(d) == mla.MLA_ERR_INVALID_ARG
     assert lib.mla_check_dims(None) == mla.MLA_ERR_INVALID_ARG
 
@@ -85,12 +89,19 @@ def test_host_validation_rejects_before_launch(lib):
     di = mla.dims(16, 64, int8=True)
     a = list(args); a[0] = ctypes.byref(di)           # INT8 without scale/zero array
     assert lib.mla_decode(*a) == mla.MLA_ERR_INVALID_ARG
+    df = mla.dims(16, 64, fp8=True)
+    a = list(args); a[0] = ctypes.byref(df)           # FP8 without its scales
+    assert lib.mla_decode(*a) == mla.MLA_ERR_INVALID_ARG
+    a = list(args); a[0] = ctypes.byref(df); a[4] = ctypes.c_void_p(0x10004)  # scales not 16-byte aligned
+    assert lib.mla_decode(*a) == mla.MLA_ERR_INVALID_ARG
     # append
     assert lib.mla_cache_append(ctypes.byref(d), None, None, 4, fake, 2, 8, fake, fake, 3, fake, fake,
                                 ctypes.c_double(1e4), None, None) == mla.MLA_ERR_INVALID_ARG
     assert lib.mla_cache_append(ctypes.byref(d), fake, None, 4, fake, 2, 8, fake, fake, 0, fake, fake,
                                 ctypes.c_double(1e4), None, None) == mla.MLA_OK  # no tokens: no-op
     assert lib.mla_cache_append(ctypes.byref(di), fake, None, 4, fake, 2, 8, fake, fake, 3, fake, fake,
+                                ctypes.c_double(1e4), None, None) == mla.MLA_ERR_INVALID_ARG
+    assert lib.mla_cache_append(ctypes.byref(df), fake, None, 4, fake, 2, 8, fake, fake, 3, fake, fake,
                                 ctypes.c_double(1e4), None, None) == mla.MLA_ERR_INVALID_ARG
     # combine
     assert lib.mla_combine(ctypes.byref(d), fake, fake, 2, 0, fake, None, None) == mla.MLA_ERR_INVALID_ARG
@@ -124,6 +135,13 @@ def test_sparse_workspace_and_validation(lib):
     dec = lib.mla_decode_workspace_size(ctypes.byref(d), 32, 76)
     sp = lib.mla_decode_sparse_workspace_size(ctypes.byref(d), 32, 2048, 76)
     assert sp >= dec + 32 * 2048 * 1152   # the decode's workspace plus the gathered rows
+    # 1-byte caches gather 576-byte rows plus their scales: 8 (INT8) or 4 (FP8) bytes a row
+    di, df = mla.dims(16, 64, int8=True), mla.dims(16, 64, fp8=True)
+    deci = lib.mla_decode_workspace_size(ctypes.byref(di), 32, 76)
+    spi = lib.mla_decode_sparse_workspace_size(ctypes.byref(di), 32, 2048, 76)
+    spf = lib.mla_decode_sparse_workspace_size(ctypes.byref(df), 32, 2048, 76)
+    assert spi >= deci + 32 * 2048 * (576 + 8) and spf >= deci + 32 * 2048 * (576 + 4)
+    assert spf < spi < sp
     assert lib.mla_decode_sparse_workspace_size(ctypes.byref(d), 32, 0, 76) == 0
     assert lib.mla_decode_sparse_workspace_size(ctypes.byref(d), 32, mla.MAX_TOP_K + 1, 76) == 0
     fake = ctypes.c_void_p(0x10000)  # never dereferenced: validation fails first

@@ -17,7 +17,7 @@ from mla_decode_attention_paged_gb300 import workloads as W
 pytestmark = pytest.mark.gpu
 
 
-def _inputs(int8: bool, heads=16, lens=(700, 129), P=64, seed=31):
+def _inputs(fmt: str, heads=16, lens=(700, 129), P=64, seed=31):
     g = W.generator(seed)
     seq_lens = torch.tensor(lens, dtype=torch.int32)
     table, npg = W.draw_page_table(seq_lens, P, True, g)
@@ -25,12 +25,12 @@ def _inputs(int8: bool, heads=16, lens=(700, 129), P=64, seed=31):
              W_UV=W.draw_bf16((heads, 128, 512), 0.02, g).cuda(),
              q_nope=W.draw_bf16((len(lens), heads, 128), 1.0, g).cuda(),
              q_pe=W.draw_bf16((len(lens), heads, 64), 1.0, g).cuda(), sz=None)
-    if int8:
-        codes, sz = W.draw_int8_cache(npg, P, g)
+    if fmt != "bf16":
+        codes, sz = W.draw_int8_cache(npg, P, g) if fmt == "int8" else W.draw_fp8_cache(npg, P, g)
         x["cache"], x["sz"] = codes.cuda(), sz.cuda()
     else:
         x["cache"] = W.draw_bf16((npg, P, 576), 1.0, g).cuda()
-    return mla.dims(heads, P, int8=int8), x
+    return mla.dims(heads, P, int8=fmt == "int8", fp8=fmt == "fp8"), x
 
 
 def _decode(d, x, ws):
@@ -40,9 +40,9 @@ def _decode(d, x, ws):
     return out, lse
 
 
-@pytest.mark.parametrize("int8", [False, True], ids=["bf16-pairs", "int8"])
-def test_unsatisfiable_wait_reports_timeout_and_context_survives(cuda_lib, int8):
-    d, x = _inputs(int8)
+@pytest.mark.parametrize("fmt", ["bf16", "int8", "fp8"], ids=["bf16-pairs", "int8", "fp8"])
+def test_unsatisfiable_wait_reports_timeout_and_context_survives(cuda_lib, fmt):
+    d, x = _inputs(fmt)
     ws = torch.empty(mla.decode_workspace_size(d, 2, 8), dtype=torch.uint8, device="cuda")
     ref_out, ref_lse = _decode(d, x, ws)
     assert mla.read_device_status(ws) == mla.MLA_OK

@@ -18,13 +18,16 @@ from harness import assert_parity, f64
 pytestmark = pytest.mark.gpu
 
 
-def _mt(heads=16, T=2, P=64, lens=(300,), int8=False, seed=17):
+def _mt(heads=16, T=2, P=64, lens=(300,), int8=False, seed=17, fp8=False):
     g = W.generator(seed)
     seq_lens = torch.tensor(lens, dtype=torch.int32)
     table, npg = W.draw_page_table(seq_lens, P, True, g, spare_pages=3)
-    x = dict(seq_lens=seq_lens, table=table, P=P, heads=heads, T=T, int8=int8, scale=1.0 / np.sqrt(192.0))
+    x = dict(seq_lens=seq_lens, table=table, P=P, heads=heads, T=T, int8=int8, fp8=fp8,
+             scale=1.0 / np.sqrt(192.0))
     if int8:
         x["codes"], x["sz"] = W.draw_int8_cache(npg, P, g)
+    elif fp8:
+        x["codes"], x["sz"] = W.draw_fp8_cache(npg, P, g)
     else:
         x["cache"] = W.draw_bf16((npg, P, 576), 1.0, g)
     x["W_UK"] = W.draw_bf16((heads, 128, 512), 0.02, g)
@@ -35,8 +38,8 @@ def _mt(heads=16, T=2, P=64, lens=(300,), int8=False, seed=17):
 
 
 def _gpu(x, num_splits=0):
-    d = mla.dims(x["heads"], x["P"], int8=x["int8"])
-    if x["int8"]:
+    d = mla.dims(x["heads"], x["P"], int8=x["int8"], fp8=x["fp8"])
+    if x["int8"] or x["fp8"]:
         cache, sz = x["codes"].cuda(), x["sz"].cuda()
     else:
         cache, sz = x["cache"].cuda(), None
@@ -48,13 +51,13 @@ def _gpu(x, num_splits=0):
 
 
 def _oracle(x):
-    if x["int8"]:
+    if x["int8"] or x["fp8"]:
         cache, sz = x["codes"].numpy(), x["sz"].numpy()
     else:
         cache, sz = W.bf16_to_bits(x["cache"]), None
     return O.decode_multi_token(f64(x["q_nope"]), f64(x["q_pe"]), cache, sz, x["table"].numpy(),
                                 x["seq_lens"].numpy(), f64(x["W_UK"]), f64(x["W_UV"]), x["scale"], x["P"],
-                                x["int8"])
+                                x["int8"], fp8=x["fp8"])
 
 
 def _check(x, num_splits=0):
@@ -109,3 +112,7 @@ def test_q_len_out_of_range_is_refused(cuda_lib):
     with pytest.raises(mla.MLAError) as e:
         _gpu(x)
     assert e.value.status == mla.MLA_ERR_INVALID_ARG
+
+
+def test_multi_token_fp8(cuda_lib):
+    _check(_mt(T=3, lens=(200, 1030, 2), fp8=True, seed=72))

@@ -2,7 +2,7 @@
 
 Small cases compare every (b, h) element by element; they span several
 128-token tiles, ragged tails, every page size, single- and multi-chunk
-splits, 16/32/64/128 heads, bf16 and INT8 caches and the degenerate cases
+splits, 16/32/64/128 heads, bf16, INT8 and FP8 caches and the degenerate cases
 (empty sequence, one token, lengths at tile boundaries)."""
 import math
 
@@ -18,8 +18,9 @@ from harness import (assert_parity, dims_of, f64, gpu_cache, gpu_decode, oracle_
 pytestmark = pytest.mark.gpu
 
 
-def _small(heads=16, P=64, lens=(300,), int8=False, seed=7, std=1.0, shuffled=True):
-    w = W.Workload(f"small_h{heads}_p{P}", len(lens), heads, 0, P, shuffled, std, 0.02, 1.0, seed, int8=int8)
+def _small(heads=16, P=64, lens=(300,), int8=False, seed=7, std=1.0, shuffled=True, fp8=False):
+    w = W.Workload(f"small_h{heads}_p{P}", len(lens), heads, 0, P, shuffled, std, 0.02, 1.0, seed, int8=int8,
+                   fp8=fp8)
     g = W.generator(seed)
     seq_lens = torch.tensor(lens, dtype=torch.int32)
     table, npg = W.draw_page_table(seq_lens, P, shuffled, g, spare_pages=3)
@@ -27,6 +28,9 @@ def _small(heads=16, P=64, lens=(300,), int8=False, seed=7, std=1.0, shuffled=Tr
     if int8:
         codes, sz = W.draw_int8_cache(npg, P, g)
         inp["cache_i8"], inp["sz"] = codes, sz
+    elif fp8:
+        codes, sc = W.draw_fp8_cache(npg, P, g)
+        inp["cache_i8"], inp["sz"] = codes, sc
     else:
         inp["cache"] = W.draw_bf16((npg, P, 576), std, g)
     inp["W_UK"] = W.draw_bf16((heads, 128, 512), 0.02, g)
@@ -37,7 +41,7 @@ def _small(heads=16, P=64, lens=(300,), int8=False, seed=7, std=1.0, shuffled=Tr
 
 
 def _run_small(w, inp, num_splits=0):
-    if w.int8:
+    if w.quantised:
         cache, sz = inp["cache_i8"].cuda(), inp["sz"].cuda()
         oc = (inp["cache_i8"].numpy(), inp["sz"].numpy(), inp["block_table"].numpy())
     else:
@@ -84,6 +88,31 @@ def test_tile_boundaries_and_empty(cuda_lib):
 @pytest.mark.parametrize("heads", [16, 128])
 def test_int8_cache_decode(cuda_lib, heads):
     _run_small(*_small(heads=heads, lens=(200, 1030), int8=True))
+
+
+@pytest.mark.parametrize("heads", [16, 128])
+def test_fp8_cache_decode(cuda_lib, heads):
+    _run_small(*_small(heads=heads, lens=(200, 1030), fp8=True, seed=8))
+
+
+@pytest.mark.parametrize("P", [16, 128])
+def test_fp8_page_sizes_ragged(cuda_lib, P):
+    _run_small(*_small(P=P, lens=(1, 129, 700), fp8=True, seed=9))
+
+
+def test_fp8_tile_boundaries_empty_and_splits(cuda_lib):
+    w, inp = _small(lens=(0, 1, 127, 128, 129, 257), fp8=True, seed=10)
+    (_, _), out, lse = _run_small(w, inp, num_splits=7)
+    assert torch.all(out[0] == 0) and torch.all(torch.isneginf(lse[0]))
+
+
+def test_fp8_accepts_float8_tensor(cuda_lib):
+    """The E4M3 codes may be held as torch.float8_e4m3fn: same bits, same results."""
+    w, inp = _small(lens=(300,), fp8=True, seed=11)
+    codes, sc = inp["cache_i8"].cuda(), inp["sz"].cuda()
+    o1, l1 = gpu_decode(inp, w, codes, sc)
+    o2, l2 = gpu_decode(inp, w, codes.view(torch.float8_e4m3fn), sc)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
 
 
 def test_shuffled_table_bit_identical_and_deterministic(cuda_lib):
@@ -143,7 +172,7 @@ def test_combine_matches_oracle(cuda_lib):
 
 # ------------------------------------------------------------------ append --- #
 
-def _append_case(int8, theta, seed=5):
+def _append_case(int8, theta, seed=5, fp8=False):
     P, B, maxp = 16, 3, 6
     g = W.generator(seed)
     table, npg = W.draw_page_table(torch.tensor([maxp * P] * B, dtype=torch.int32), P, True, g)
@@ -154,19 +183,24 @@ def _append_case(int8, theta, seed=5):
     pos = (pos % (maxp * P)).to(torch.int32)
     c = W.draw_bf16((n, 512), 1.0, g)
     k = W.draw_bf16((n, 64), 1.0, g)
-    d = mla.dims(16, P, int8=int8)
+    d = mla.dims(16, P, int8=int8, fp8=fp8)
     if int8:
         cache = torch.zeros((npg, P, 576), dtype=torch.int8, device="cuda")
         sz = torch.zeros((npg, P, 2), dtype=torch.float32, device="cuda")
         ref = np.zeros((npg, P, 576), np.int8)
         rsz = np.zeros((npg, P, 2), np.float32)
+    elif fp8:
+        cache = torch.zeros((npg, P, 576), dtype=torch.uint8, device="cuda")
+        sz = torch.zeros((npg, P), dtype=torch.float32, device="cuda")
+        ref = np.zeros((npg, P, 576), np.uint8)
+        rsz = np.zeros((npg, P), np.float32)
     else:
         cache = torch.zeros((npg, P, 576), dtype=torch.bfloat16, device="cuda")
         sz, ref, rsz = None, np.zeros((npg, P, 576), np.uint16), None
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
     mla.cache_append(d, cache, sz, table.cuda(), seq_ids.cuda(), pos.cuda(), c.cuda(), k.cuda(), theta, st)
     O.append_tokens(ref, rsz, table.numpy(), seq_ids.tolist(), pos.tolist(), W.bf16_to_bits(c),
-                    W.bf16_to_bits(k), theta, P, int8=int8)
+                    W.bf16_to_bits(k), theta, P, int8=int8, fp8=fp8)
     assert mla.read_status_word(st) == mla.MLA_OK
     return cache, sz, ref, rsz
 
@@ -191,6 +225,43 @@ def test_append_int8_codes_bit_exact_without_rope(cuda_lib):
     cache, sz, ref, rsz = _append_case(True, 0.0)
     np.testing.assert_array_equal(cache.cpu().numpy(), ref)
     np.testing.assert_array_equal(sz.cpu().numpy(), rsz)
+
+
+def test_append_fp8_codes_bit_exact_without_rope(cuda_lib):
+    cache, sz, ref, rsz = _append_case(False, 0.0, fp8=True)
+    np.testing.assert_array_equal(cache.cpu().numpy(), ref)
+    np.testing.assert_array_equal(sz.cpu().numpy(), rsz)
+
+
+def test_append_fp8_ties_saturation_and_signed_zero(cuda_lib):
+    """A row whose largest magnitude is 448 has scale 1, so its codes are the
+    format's own rounding of the values: ties to the even mantissa, subnormal
+    ties, -0 and negative values that round to zero."""
+    P = 16
+    special = [448.0, 1.0625, -1.1875, 3 * 2.0 ** -10, 2.0 ** -10, -0.0, -(2.0 ** -10), 248.0, 15 * 2.0 ** -10,
+               -448.0, 1.09375, 240.0, -(2.0 ** -12), 0.5, 7 * 2.0 ** -9]
+    c = torch.zeros((2, 512), dtype=torch.float32)
+    c[0, :len(special)] = torch.tensor(special)
+    c[1, :] = torch.linspace(-3.0, 2.0, 512)          # an ordinary row: scale 3/448
+    c = c.to(torch.bfloat16)
+    assert all(float(v) == x for v, x in zip(c[0, :len(special)], special))  # all exact in bf16
+    k = torch.zeros((2, 64), dtype=torch.bfloat16)
+    table = torch.tensor([[0]], dtype=torch.int32)
+    d = mla.dims(16, P, fp8=True)
+    cache = torch.zeros((1, P, 576), dtype=torch.uint8, device="cuda")
+    sz = torch.zeros((1, P), dtype=torch.float32, device="cuda")
+    pos = torch.tensor([0, 1], dtype=torch.int32)
+    mla.cache_append(d, cache, sz, table.cuda(), torch.zeros(2, dtype=torch.int32, device="cuda"), pos.cuda(),
+                     c.cuda(), k.cuda(), 0.0)
+    ref = np.zeros((1, P, 576), np.uint8)
+    rsz = np.zeros((1, P), np.float32)
+    O.append_tokens(ref, rsz, table.numpy(), [0, 0], [0, 1], W.bf16_to_bits(c), W.bf16_to_bits(k), 0.0, P,
+                    int8=False, fp8=True)
+    got = cache.cpu().numpy()
+    np.testing.assert_array_equal(got, ref)
+    np.testing.assert_array_equal(sz.cpu().numpy(), rsz)
+    assert sz[0, 0].item() == 1.0
+    np.testing.assert_array_equal(got[0, 0, :len(special)], O.e4m3_encode(np.array(special, np.float32)))
 
 
 def test_append_out_of_range_sets_status(cuda_lib):

@@ -16,13 +16,15 @@ from harness import assert_parity, f64
 pytestmark = pytest.mark.gpu
 
 
-def _sp(heads=16, P=64, lens=(300,), top_k=100, fill=0.8, int8=False, seed=23):
+def _sp(heads=16, P=64, lens=(300,), top_k=100, fill=0.8, int8=False, seed=23, fp8=False):
     g = W.generator(seed)
     seq_lens = torch.tensor(lens, dtype=torch.int32)
     table, npg = W.draw_page_table(seq_lens, P, True, g, spare_pages=3)
-    x = dict(seq_lens=seq_lens, table=table, P=P, heads=heads, int8=int8, scale=1.0 / np.sqrt(192.0))
+    x = dict(seq_lens=seq_lens, table=table, P=P, heads=heads, int8=int8, fp8=fp8, scale=1.0 / np.sqrt(192.0))
     if int8:
         x["codes"], x["sz"] = W.draw_int8_cache(npg, P, g)
+    elif fp8:
+        x["codes"], x["sz"] = W.draw_fp8_cache(npg, P, g)
     else:
         x["cache"] = W.draw_bf16((npg, P, 576), 1.0, g)
     x["W_UK"] = W.draw_bf16((heads, 128, 512), 0.02, g)
@@ -34,8 +36,8 @@ def _sp(heads=16, P=64, lens=(300,), top_k=100, fill=0.8, int8=False, seed=23):
 
 
 def _gpu(x, num_splits=0, idx=None):
-    d = mla.dims(x["heads"], x["P"], int8=x["int8"])
-    cache, sz = (x["codes"].cuda(), x["sz"].cuda()) if x["int8"] else (x["cache"].cuda(), None)
+    d = mla.dims(x["heads"], x["P"], int8=x["int8"], fp8=x["fp8"])
+    cache, sz = (x["codes"].cuda(), x["sz"].cuda()) if (x["int8"] or x["fp8"]) else (x["cache"].cuda(), None)
     idx = x["idx"] if idx is None else idx
     ws = torch.empty(mla.decode_sparse_workspace_size(d, len(x["seq_lens"]), idx.shape[1], num_splits),
                      dtype=torch.uint8, device="cuda")
@@ -47,10 +49,11 @@ def _gpu(x, num_splits=0, idx=None):
 
 
 def _oracle(x, idx=None):
-    cache, sz = (x["codes"].numpy(), x["sz"].numpy()) if x["int8"] else (W.bf16_to_bits(x["cache"]), None)
+    quantised = x["int8"] or x["fp8"]
+    cache, sz = (x["codes"].numpy(), x["sz"].numpy()) if quantised else (W.bf16_to_bits(x["cache"]), None)
     return O.decode_sparse(f64(x["q_nope"]), f64(x["q_pe"]), cache, sz, x["table"].numpy(), x["seq_lens"].numpy(),
                            (x["idx"] if idx is None else idx).numpy(), f64(x["W_UK"]), f64(x["W_UV"]), x["scale"],
-                           x["P"], x["int8"])
+                           x["P"], x["int8"], fp8=x["fp8"])
 
 
 def _check(x, num_splits=0):
@@ -108,3 +111,8 @@ def test_sparse_empty_selection_and_bad_entry(cuda_lib):
     skipped[1, 3] = -1
     ref_o, ref_l = _oracle(x, skipped)
     assert_parity(out2, lse2, ref_o, ref_l, [(1, h) for h in range(16)], "sparse, bad entry skipped")
+
+
+@pytest.mark.parametrize("heads", [16, 128])
+def test_sparse_fp8(cuda_lib, heads):
+    _check(_sp(heads=heads, lens=(700, 3000), top_k=300, fp8=True, seed=heads + 7))

@@ -1,4 +1,4 @@
-"""Parity at the full sizes of the five benchmark workloads, in the launch
+"""Parity at the full sizes of the benchmark workloads, in the launch
 configuration bench.py times.  The oracle cannot evaluate every output at
 these sizes, so each test checks a seeded sample of sequences: the
 un-absorbed oracle on some heads of each sampled sequence, and the absorbed
@@ -20,6 +20,7 @@ SAMPLES = {
     "ctx1m": ([1], [0, 15]),
     "ragged": ("longest+3", [0, 37, 64, 127]),
     "int8": ([0, 57, 127], [0, 31, 96, 127]),
+    "fp8_v2lite": ([0, 31], [0, 15]),
 }
 
 
@@ -34,7 +35,7 @@ def _sample_seqs(rule, seq_lens, batch):
     return rule
 
 
-@pytest.mark.parametrize("key", ["tiny", "v2lite", "ctx1m", "ragged", "int8"])
+@pytest.mark.parametrize("key", ["tiny", "v2lite", "ctx1m", "ragged", "int8", "fp8_v2lite"])
 def test_full_size_workload(cuda_lib, key):
     w = W.WORKLOADS[key]
     inp = W.make_decode_inputs(w, device="cuda")
