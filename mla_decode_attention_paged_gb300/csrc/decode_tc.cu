@@ -94,7 +94,7 @@ struct Cfg {
   static constexpr int kQkSlots = kByte ? 0 : 6;                  // bf16 QK ring slots (single boxes), all rings
   static constexpr int kQkRing = kQkSlots / kQkRings;
   static constexpr int kPvProducerWarp = kQkRings == 2 ? 8 : 3;
-  static constexpr int kNumPair = kByte ? 5 : (HC == 16 ? 3 : 2);  // bf16 PV ring / INT8 shared ring
+  static constexpr int kNumPair = kByte ? 5 : (HC == 16 ? 3 : 2);  // bf16 PV ring / 1-byte shared ring
   static constexpr int kNumRope = kByte ? 2 : 0;
   static constexpr uint32_t kQBytes = 9 * HC * 128;
   static constexpr uint32_t kPBytes = kTile * HC * 2;
@@ -178,25 +178,21 @@ __device__ __forceinline__ void expand_codes(uint4 v, uint4& lo, uint4& hi) {
   hi = make_uint4(o[4], o[5], o[6], o[7]);
 }
 
-// 16 E4M3 codes -> 16 fp16 values equal to the codes' values.  A code's
-// magnitude bits (4 exponent, 3 mantissa) moved to fp16 bits 13..7 read as
-// an fp16 with the same exponent field and mantissa, i.e. the E4M3 value
-// times 2^(7 - 15) -- E4M3 subnormals becoming fp16 subnormals -- and the
-// product by 2^8 is exact (no value exceeds 448, none needs more than 4
-// significant bits).
-__device__ __forceinline__ uint32_t e4m3_pair_to_half2(uint32_t w, uint32_t sel) {
-  const uint32_t a = __byte_perm(w, 0u, sel);  // two codes into bits 15..8 and 31..24
-  const uint32_t h = (a & 0x80008000u) | ((a >> 1) & 0x3F803F80u);
-  const __half2 v = __hmul2(*reinterpret_cast<const __half2*>(&h), __floats2half2_rn(256.f, 256.f));
-  return *reinterpret_cast<const uint32_t*>(&v);
+// 16 E4M3 codes -> 16 fp16 values equal to the codes' values (every E4M3
+// value is exact in fp16: at most 4 significant bits, magnitudes 2^-9..448),
+// one conversion instruction per pair; byte k of each word becomes half k.
+__device__ __forceinline__ uint32_t e4m3x2_to_half2(uint32_t two_codes) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(uint16_t(two_codes)));
+  return r;
 }
 __device__ __forceinline__ void expand_e4m3(uint4 v, uint4& lo, uint4& hi) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
   uint32_t o[8];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    o[2 * i] = e4m3_pair_to_half2(w[i], 0x1404);      // bytes 0,1
-    o[2 * i + 1] = e4m3_pair_to_half2(w[i], 0x3424);  // bytes 2,3
+    o[2 * i] = e4m3x2_to_half2(w[i]);            // bytes 0,1
+    o[2 * i + 1] = e4m3x2_to_half2(w[i] >> 16);  // bytes 2,3
   }
   lo = make_uint4(o[0], o[1], o[2], o[3]);
   hi = make_uint4(o[4], o[5], o[6], o[7]);
