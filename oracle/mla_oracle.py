@@ -500,6 +500,37 @@ def decode_multi_token(q_nope: np.ndarray, q_pe: np.ndarray, cache: np.ndarray, 
     return out, lse
 
 
+def prefill_chunk(cache: np.ndarray, scale_zero: np.ndarray | None, block_table: np.ndarray,
+                  seq_lens: Sequence[int], c_kv_bits: np.ndarray, k_pe_bits: np.ndarray, rope_theta: float,
+                  q_nope: np.ndarray, q_pe: np.ndarray, W_UK: np.ndarray, W_UV: np.ndarray, scale: float,
+                  page_size: int, int8: bool, triples=None, absorbed: bool = False, *, fp8: bool = False):
+    """One chunk of chunked prefill ([P4] "The Prefill Phase: Compute-Bound
+    Parallelism": the prompt's tokens are processed together and their
+    key/value state is written to the cache, which decode then reads; a long
+    prompt goes in chunks, each attending to the cache the chunks before it
+    wrote).
+
+    Sequence b's chunk is the T tokens at positions L_b - T .. L_b - 1, L_b =
+    seq_lens[b] counting the chunk.  First every chunk token's row is
+    appended (``append_tokens``, in place on ``cache``; positions below 0 are
+    skipped), then query token t attends to positions 0 .. L_b - T + t
+    (``decode_multi_token``: the history and the chunk's tokens up to itself).
+
+    c_kv_bits [B, T, 512], k_pe_bits [B, T, 64] bf16 bit patterns; q_nope
+    [B, T, H, 128], q_pe [B, T, H, 64].  Returns (out [B, T, H, 128],
+    lse [B, T, H]); ``triples`` limits the attention to a list of (b, t, h).
+    """
+    B, T = q_nope.shape[0], q_nope.shape[1]
+    for b in range(B):
+        L = int(seq_lens[b])
+        ts = [t for t in range(T) if L - T + t >= 0]
+        if ts:
+            append_tokens(cache, scale_zero, block_table, [b] * len(ts), [L - T + t for t in ts],
+                          c_kv_bits[b, ts], k_pe_bits[b, ts], rope_theta, page_size, int8, fp8=fp8)
+    return decode_multi_token(q_nope, q_pe, cache, scale_zero, block_table, seq_lens, W_UK, W_UV, scale,
+                              page_size, int8, triples=triples, absorbed=absorbed, fp8=fp8)
+
+
 def decode_sparse(q_nope: np.ndarray, q_pe: np.ndarray, cache: np.ndarray, scale_zero: np.ndarray | None,
                   block_table: np.ndarray, seq_lens: Sequence[int], token_indices: np.ndarray, W_UK: np.ndarray,
                   W_UV: np.ndarray, scale: float, page_size: int, int8: bool, pairs=None, absorbed: bool = False, *,

@@ -568,3 +568,64 @@ def test_sparse_pins_catch_planted_off_by_one(monkeypatch):
     good, _ = O.decode_sparse(qn[:, 0], qp[:, 0], cache, None, table, [L], chosen[None], W_UK, W_UV, 0.2, P, False)
     np.testing.assert_allclose(good[0], ref, rtol=1e-10, atol=1e-14)
     assert not np.allclose(bad[0], ref, rtol=1e-6)
+
+
+# --------------------------------------------------------- chunked prefill ---- #
+
+def _prefill_inputs(B, T, H, P, maxp, seed):
+    rng = np.random.default_rng(seed)
+    npg = B * maxp
+    table = rng.permutation(npg).astype(np.int32).reshape(B, maxp)
+    W_UK = _bf16(rng.normal(0, 0.05, (H, 128, 512)))
+    W_UV = _bf16(rng.normal(0, 0.05, (H, 128, 512)))
+    c_bits = O.f64_to_bf16_bits(rng.normal(0, 1, (B, T, 512)))
+    k_bits = O.f64_to_bf16_bits(rng.normal(0, 1, (B, T, 64)))
+    qn = _bf16(rng.normal(0, 1, (B, T, H, 128)))
+    qp = _bf16(rng.normal(0, 1, (B, T, H, 64)))
+    return table, W_UK, W_UV, c_bits, k_bits, qn, qp
+
+
+def test_prefill_whole_prompt_is_causal_attention():
+    """A prompt prefilled in one chunk from an empty cache is ordinary causal
+    self-attention over the prompt: torch SDPA (fp64, is_causal) on
+    explicitly expanded keys and values (RoPE off so that the stored RoPE key
+    is the given one)."""
+    B, T, H, P = 1, 21, 2, 16
+    table, W_UK, W_UV, c_bits, k_bits, qn, qp = _prefill_inputs(B, T, H, P, 2, 3)
+    cache = np.zeros((2, P, 576), np.uint16)
+    out, lse = O.prefill_chunk(cache, None, table, [T], c_bits, k_bits, 0.0, qn, qp, W_UK, W_UV, 0.3, P, False)
+    rows = np.concatenate([O.bf16_bits_to_f64(c_bits[0]), O.bf16_bits_to_f64(k_bits[0])], axis=1)
+    for h in range(H):
+        K = np.concatenate([rows[:, :512] @ W_UK[h].T, rows[:, 512:]], axis=1)
+        V = rows[:, :512] @ W_UV[h].T
+        Q = np.concatenate([qn[0, :, h], qp[0, :, h]], axis=1)
+        ref = torch.nn.functional.scaled_dot_product_attention(
+            torch.from_numpy(Q)[None], torch.from_numpy(K)[None], torch.from_numpy(V)[None], scale=0.3,
+            is_causal=True)[0].numpy()
+        np.testing.assert_allclose(out[0, :, h], ref, rtol=1e-10, atol=1e-13)
+
+
+def test_prefill_in_chunks_matches_one_chunk_and_writes_the_cache():
+    """Two chunks (T1 then T2) leave the cache and the second chunk's outputs
+    exactly as one chunk of T1 + T2 leaves them for its last T2 tokens; the
+    rows land at positions L - T .. L - 1 of each sequence."""
+    B, T1, T2, H, P, maxp = 2, 9, 14, 2, 16, 4
+    hist = [5, 30]
+    table, W_UK, W_UV, c_bits, k_bits, qn, qp = _prefill_inputs(B, T1 + T2, H, P, maxp, 4)
+    base = O.f64_to_bf16_bits(np.random.default_rng(9).normal(0, 1, (B * maxp, P, 576)))
+    L = [h + T1 + T2 for h in hist]
+    one = base.copy()
+    o1, l1 = O.prefill_chunk(one, None, table, L, c_bits, k_bits, 1e4, qn, qp, W_UK, W_UV, 0.1, P, False)
+    two = base.copy()
+    O.prefill_chunk(two, None, table, [h + T1 for h in hist], c_bits[:, :T1], k_bits[:, :T1], 1e4,
+                    qn[:, :T1], qp[:, :T1], W_UK, W_UV, 0.1, P, False)
+    o2, l2 = O.prefill_chunk(two, None, table, L, c_bits[:, T1:], k_bits[:, T1:], 1e4, qn[:, T1:], qp[:, T1:],
+                             W_UK, W_UV, 0.1, P, False)
+    np.testing.assert_array_equal(one, two)
+    np.testing.assert_allclose(o2, o1[:, T1:], rtol=1e-12, atol=1e-15)
+    np.testing.assert_allclose(l2, l1[:, T1:], rtol=1e-12)
+    for b in range(B):
+        page, off = O.page_slot(table, b, hist[b], P)        # the chunk's first row
+        np.testing.assert_array_equal(one[page, off, :512], c_bits[b, 0])
+        page, off = O.page_slot(table, b, hist[b] - 1, P)    # the history before it is untouched
+        np.testing.assert_array_equal(one[page, off], base[page, off])
