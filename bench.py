@@ -29,6 +29,8 @@ IDX_SETS = 4  # sparse workloads: top-k selections the steps cycle through
 METRIC = "MLA decode tokens/s and latent-cache HBM GB/s (fraction of 8 TB/s), 1×GB300"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+PREFILL_METRIC = "MLA chunked-prefill tokens/s (chunk tokens written and attended), 1×GB300"
 
 
 def parse():
@@ -77,6 +79,26 @@ def peaks():
         d = json.load(open(path))
         return float(d["hbm_gbs"]), "measured"
     return FALLBACK_HBM_GBS, "fallback"
+
+
+def tensor_peak():
+    """Dense bf16 tensor-core TFLOP/s: the measured burst figure (a kernel timed alone), else the fallback."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        return float(json.load(open(path))["bf16_tflops"]), "measured"
+    return FALLBACK_BF16_TFLOPS, "fallback"
+
+
+def prefill_flops(seq_lens, chunk: int, heads: int) -> float:
+    """Algorithmic FLOPs of the chunk's attention in the absorbed form: each
+    (query token, head) scores every visible key over the 576-wide rows and
+    sums 512-wide latent values, 2 * 576 + 2 * 512 FLOPs per key."""
+    total = 0
+    for L in seq_lens:
+        first = int(L) - chunk            # position of the chunk's first token
+        vis = [max(0, first + t + 1) for t in range(chunk)]
+        total += sum(vis)
+    return float(total) * heads * (2 * 576 + 2 * 512)
 
 
 def attention_kernel(fmt: str):
@@ -178,12 +200,74 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def cpu_baseline_prefill(w, inp, seconds, gpu_out=None, gpu_lse=None):
+    """The oracle's chunked prefill on the host cores: per sampled sequence it
+    appends the chunk to that sequence's pages itself and attends three of
+    the chunk's tokens (first, middle, last) with every head, un-absorbed in
+    fp64, until about `seconds` have passed.  Returns (baseline, parity) as
+    cpu_baseline does, parity over the (token, head) rows computed."""
+    import numpy as np
+    import oracle as O
+    import torch
+    from mla_decode_attention_paged_gb300 import workloads as W
+    try:
+        from threadpoolctl import threadpool_info
+        cores = max([i.get("num_threads", 0) for i in threadpool_info()] + [1])
+    except Exception:
+        cores = os.cpu_count()
+    f64 = lambda t: O.bf16_bits_to_f64(W.bf16_to_bits(t))
+    qn, qp, wk, wv = f64(inp["q_nope"]), f64(inp["q_pe"]), f64(inp["W_UK"]), f64(inp["W_UV"])
+    c_bits, k_bits = W.bf16_to_bits(inp["chunk_c_kv"]), W.bf16_to_bits(inp["chunk_k_pe"])
+    table = inp["block_table"].cpu().numpy()
+    lens = inp["seq_lens"].cpu().numpy()
+    T, H = w.chunk, w.heads
+    toks = sorted({0, T // 2, T - 1})
+    done, el = 0, 0.0
+    worst = {"abs": 0.0, "rel": 0.0, "lse": 0.0, "rows": 0}
+    while el < seconds:
+        b = done % w.batch
+        n = (int(lens[b]) + w.page_size - 1) // w.page_size
+        tab = np.full_like(table, -1)
+        tab[b, :n] = np.arange(n)
+        # the sequence's pages: the history as cached; the oracle's own append rewrites the chunk's rows
+        idx = torch.as_tensor(table[b, :n].astype(np.int64), device=inp["cache_dev"].device)
+        cache = W.bf16_to_bits(inp["cache_dev"].index_select(0, idx))
+        triples = [(b, t, h) for t in toks for h in range(H)]
+        t_start = time.perf_counter()
+        ref_o, ref_l = O.prefill_chunk(cache, None, tab, lens, c_bits, k_bits, w.rope_theta, qn, qp, wk, wv,
+                                       inp["scale"], w.page_size, False, triples=triples)
+        el += time.perf_counter() - t_start
+        if gpu_out is not None and done < w.batch:
+            for _, t, h in triples:
+                g = np.asarray(gpu_out[b, t, h], np.float64)
+                r = ref_o[b, t, h]
+                err = float(np.abs(g - r).max())
+                worst["abs"] = max(worst["abs"], err)
+                worst["rel"] = max(worst["rel"], err / max(float(np.abs(r).max()), 1e-300))
+                worst["lse"] = max(worst["lse"], abs(float(gpu_lse[b, t, h]) - float(ref_l[b, t, h])))
+                worst["rows"] += 1
+        done += 1
+    base = {"value": done * len(toks) / el, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"{done} sequence(s) of {w.name}: the oracle appends the {T}-token chunk and attends "
+                      f"tokens {toks} with all {H} heads (un-absorbed fp64 oracle), {el:.1f} s"}
+    parity = None
+    if gpu_out is not None:
+        ok = worst["abs"] <= 2e-2 and worst["rel"] <= 1e-2 and worst["lse"] <= 2e-2
+        parity = {"rows_checked": worst["rows"], "sequences": min(done, w.batch), "max_abs": worst["abs"],
+                  "max_rel_row": worst["rel"], "max_lse_abs": worst["lse"],
+                  "tolerance": {"abs": 2e-2, "rel_row": 1e-2, "lse_abs": 2e-2}, "pass": ok,
+                  "against": "un-absorbed fp64 oracle on the step's own inputs"}
+    return base, parity
+
+
 def cpu_baseline(w, inp, seconds, gpu_out=None, gpu_lse=None):
     """The fp64 oracle as it stands, on the host cores, over whole sequences
     (all heads) of this workload until about `seconds` have passed.  Returns
     (baseline dict, parity dict or None): given the GPU's out / lse of the
     same step, the oracle's results for the sequences it ran are compared
     with them (max abs error, max per-row relative error, max lse error)."""
+    if w.chunk:
+        return cpu_baseline_prefill(w, inp, seconds, gpu_out, gpu_lse)
     import numpy as np
     import oracle as O
     from mla_decode_attention_paged_gb300 import workloads as W
@@ -280,7 +364,7 @@ def run_ours(args, rank, world):
     w = W.WORKLOADS[args.workload]
     inp = W.make_decode_inputs(w, device=dev)
     d = mla.dims(w.heads, w.page_size, int8=w.int8, fp8=w.fp8)
-    B, H, T = w.batch, w.heads, w.q_len
+    B, H, T = w.batch, w.heads, (w.chunk or w.q_len)
     seq_lens = inp["seq_lens"]
     table = inp["block_table"].to(dev)
     npg = inp["num_pages"]
@@ -307,6 +391,7 @@ def run_ours(args, rank, world):
     auto = mla.auto_num_splits(d_rows if mla.check_dims(d_rows) == mla.MLA_OK else d, B)
     splits = args.num_splits if args.num_splits is not None else (W.num_splits_for(w, auto) or auto)
     ws_bytes = (mla.decode_sparse_workspace_size(d, B, w.top_k, splits) if w.top_k
+                else mla.prefill_workspace_size(d, B, T, splits) if w.chunk
                 else mla.decode_multi_workspace_size(d, B, T, splits))
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     qshape = (B, H) if T == 1 else (B, T, H)
@@ -335,7 +420,17 @@ def run_ours(args, rank, world):
             mla.decode_multi(d, qn, qp, cache, sz, tab, lens, W_UK, W_UV, inp["scale"], num_splits=splits,
                              workspace=ws, out=o, lse_out=l)
 
+    chunk_c, chunk_k = inp.get("chunk_c_kv"), inp.get("chunk_k_pe")
+
+    def prefill_fn(qn, qp, tab, lens, c_kv, k_pe, o, l):
+        """The prefill workload's call: mla_prefill writes the chunk and attends it."""
+        mla.prefill(d, cache, sz, tab, lens, c_kv, k_pe, qn, qp, W_UK, W_UV, inp["scale"], rope_theta=w.rope_theta,
+                    num_splits=splits, workspace=ws, out=o, lse_out=l)
+
     def step(i):
+        if w.chunk:
+            prefill_fn(q_nope, q_pe, table, seq_lens, chunk_c, chunk_k, out, lse)
+            return
         mla.cache_append(d, cache, sz, table, seq_ids, positions, new_c, new_k, w.rope_theta)
         decode_fn(q_nope, q_pe, table, seq_lens, idx_sets[i % len(idx_sets)], out, lse)
 
@@ -384,8 +479,10 @@ def run_ours(args, rank, world):
     # step's inputs sit in one pinned staging buffer and go over in one copy;
     # the library writes out and lse into one device buffer that comes back in
     # one copy (every byte of the step's inputs and results still crosses).
-    step_inputs = dict(q_nope=q_nope, q_pe=q_pe, new_c=new_c, new_k=new_k, seq_ids=seq_ids, positions=positions,
-                       table=table, seq_lens=seq_lens)
+    step_inputs = (dict(q_nope=q_nope, q_pe=q_pe, c_kv=chunk_c, k_pe=chunk_k, table=table, seq_lens=seq_lens)
+                   if w.chunk else
+                   dict(q_nope=q_nope, q_pe=q_pe, new_c=new_c, new_k=new_k, seq_ids=seq_ids, positions=positions,
+                        table=table, seq_lens=seq_lens))
     h_bufs = []
     for r in range(len(idx_sets)):
         if w.top_k:
@@ -398,6 +495,11 @@ def run_ours(args, rank, world):
 
     def e2e_step(i):
         d_in_buf.copy_(h_bufs[i % len(h_bufs)], non_blocking=True)
+        if w.chunk:
+            prefill_fn(d_in["q_nope"], d_in["q_pe"], d_in["table"], d_in["seq_lens"], d_in["c_kv"], d_in["k_pe"],
+                       d_out["out"], d_out["lse"])
+            h_out_buf.copy_(d_out_buf, non_blocking=True)
+            return
         mla.cache_append(d, cache, sz, d_in["table"], d_in["seq_ids"], d_in["positions"], d_in["new_c"],
                          d_in["new_k"], w.rope_theta)
         decode_fn(d_in["q_nope"], d_in["q_pe"], d_in["table"], d_in["seq_lens"], d_in.get("token_indices"),
@@ -419,14 +521,28 @@ def run_ours(args, rank, world):
     peak, peak_src = peaks()
     achieved = cache_bytes / (kern_ms / 1e3) / 1e9
     traffic = kernel_traffic(w.name, lens_sum, w.cache_format)
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "peak_source": peak_src,
+                "traffic": traffic, "kernel": attention_kernel(w.cache_format)[1],
+                "algorithmic_bytes_per_launch": cache_bytes}
+    if w.chunk:
+        # prefill is compute-bound: FLOPs of the chunk's attention against the bf16 tensor peak
+        flops = prefill_flops(seq_lens.cpu().tolist(), T, H)
+        tpeak, tpeak_src = tensor_peak()
+        tflops = flops / (kern_ms / 1e3) / 1e12
+        roofline = {"bound": "tensor", "achieved": round(tflops, 2), "peak": tpeak, "unit": "TFLOP/s",
+                    "frac": round(tflops / tpeak, 4), "peak_source": tpeak_src, "traffic": None,
+                    "kernel": attention_kernel(w.cache_format)[1], "algorithmic_flops_per_launch": flops,
+                    "history_bytes_per_launch": cache_bytes}
     res = {
-        "metric": METRIC, "value": round(tokens_per_s, 1), "unit": "tokens/s", "n_gpus": world,
+        "metric": PREFILL_METRIC if w.chunk else METRIC, "value": round(tokens_per_s, 1), "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None,
         "dtype": {"bf16": "bf16", "int8": "int8", "fp8": "fp8_e4m3"}[w.cache_format],
         "data": "synthetic (seeded; random-init weights of DeepSeek-V2 MLA shapes)",
         "config": {"workload": w.name, "batch": B, "heads": H, "context": w.context, "page_size": w.page_size,
-                   "q_len": T, "top_k": w.top_k or None, "num_splits": splits, "cache_bytes": cache_bytes,
+                   "q_len": T, "top_k": w.top_k or None, "chunk": w.chunk or None, "num_splits": splits,
+                   "cache_bytes": cache_bytes,
                    "l2": ("inputs larger than L2 (no flush): each step reads one of "
                           f"{len(idx_sets)} top-k selections, {len(idx_sets) * cache_bytes / 1e6:.0f} MB of rows together"
                           if w.top_k else
@@ -436,10 +552,7 @@ def run_ours(args, rank, world):
         "cache_gbs": round(step_cache_gbs, 1),
         "frac_of_8tbs": round(step_cache_gbs / NOMINAL_HBM_GBS, 4),
         "attention_kernel_ms": round(kern_ms, 5),
-        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "peak_source": peak_src,
-                     "traffic": traffic, "kernel": attention_kernel(w.cache_format)[1],
-                     "algorithmic_bytes_per_launch": cache_bytes},
+        "roofline": roofline,
         "e2e": {"value": round(whole_job_rate(B * T, world, e2e_ms), 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 5)},
         "gpu_launches": (5 if w.top_k else 4) * args.steps,  # + the gather kernel for sparse decode
@@ -479,11 +592,13 @@ def run_reference(args, rank, world):
     v = args.steps / sum(vals)
     cb = {"value": round(v, 5), "unit": "tokens/s", "cores": r["cores"], "kind": "oracle",
           "sample": f"per step: {samples[0]}"}
-    return {"metric": METRIC, "value": round(v, 5), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+    return {"metric": PREFILL_METRIC if w.chunk else METRIC, "value": round(v, 5), "unit": "tokens/s",
+            "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(1e3 * el / args.steps, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
             "config": {"workload": w.name, "batch": w.batch, "heads": w.heads, "context": w.context,
-                       "page_size": w.page_size, "q_len": w.q_len}, "impl": "reference", "cpu_baseline": cb,
+                       "page_size": w.page_size, "q_len": w.q_len, "chunk": w.chunk or None}, "impl": "reference",
+            "cpu_baseline": cb,
             "e2e": {"value": round(v, 5), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 

@@ -221,6 +221,58 @@ int mla_decode_multi(const mla_dims* dims, const void* q_nope, const void* q_pe,
                      void* workspace, size_t workspace_bytes, void* out, float* lse_out,
                      mla_stream_t stream);
 
+/* Largest prefill chunk (new tokens per sequence) mla_prefill accepts. */
+#define MLA_MAX_PREFILL_CHUNK 2048
+
+/* Bytes of workspace mla_prefill needs for (dims, batch, chunk, num_splits);
+ * 0 if the arguments are invalid.  It holds the chunk's absorbed queries and
+ * the partial latent outputs, batch * chunk * H * (1,152 + 2,048 per
+ * partition) bytes and up. */
+size_t mla_prefill_workspace_size(const mla_dims* dims, int32_t batch, int32_t chunk, int32_t num_splits);
+
+/*
+ * mla_prefill -- one chunk of chunked prefill: write the chunk's rows into
+ * the paged cache, then attend each of its tokens to the cache up to and
+ * including itself.
+ * "The Architecture of Memory", "The Prefill Phase: Compute-Bound
+ * Parallelism" (the prompt's tokens are processed together and their
+ * key/value state goes into the cache that decode reads; a long prompt goes
+ * in chunks, each attending to what the chunks before it wrote).
+ *
+ * Sequence b's chunk is the `chunk` tokens at positions seq_lens[b] - chunk
+ * .. seq_lens[b] - 1 (seq_lens counts the cache after the chunk).  The call
+ *   1. writes token t's row [c_kv[b][t] | RoPE(pos, k_pe[b][t])] at position
+ *      pos = seq_lens[b] - chunk + t, exactly as mla_cache_append (1-byte
+ *      caches quantise it); a token whose position is below 0 or past the
+ *      page table is skipped and MLA_ERR_DEVICE_BOUNDS is recorded;
+ *   2. computes, for every head of query token t, attention over positions
+ *      0 .. pos, exactly as mla_decode_multi with q_len = chunk (a query
+ *      below position 0 gets out = 0, lse = -inf).
+ *
+ *   cache, cache_scale_zero, block_table  as for mla_cache_append /
+ *               mla_decode (the cache is written, then read)
+ *   seq_lens    int32 [batch] (device)
+ *   c_kv        bf16 [batch, chunk, 512];  k_pe bf16 [batch, chunk, 64]
+ *               (unrotated; the append rotates it by rope_theta)
+ *   q_nope      bf16 [batch, chunk, H, 128]
+ *   q_pe        bf16 [batch, chunk, H, 64], rotated for each token's position
+ *   out         bf16 [batch, chunk, H, 128]
+ *   lse_out     optional fp32 [batch, chunk, H]
+ *   chunk       1 .. MLA_MAX_PREFILL_CHUNK
+ *   workspace   at least mla_prefill_workspace_size(dims, batch, chunk,
+ *               num_splits) bytes; its first 4 bytes are the call's device
+ *               status (mla_read_device_status), covering the append too.
+ * The attention runs the decode kernels over chunk * H rows per sequence
+ * (head groups of 16 or 32 (token, head) rows), so every head group
+ * streams its sequence's cache: a first, functional form of prefill, far
+ * from the tensor-core roofline a query-tiled kernel would reach.
+ */
+int mla_prefill(const mla_dims* dims, void* cache, float* cache_scale_zero, int32_t num_pages,
+                const int32_t* block_table, int32_t max_pages_per_seq, const int32_t* seq_lens, int32_t batch,
+                int32_t chunk, const void* c_kv, const void* k_pe, double rope_theta, const void* q_nope,
+                const void* q_pe, const void* W_UK, const void* W_UV, float softmax_scale, int32_t num_splits,
+                void* workspace, size_t workspace_bytes, void* out, float* lse_out, mla_stream_t stream);
+
 /* Largest index-list length mla_decode_sparse accepts. */
 #define MLA_MAX_TOP_K (1 << 20)
 

@@ -22,7 +22,8 @@ __all__ = [
     "decode_sparse", "decode_no_alloc", "combine", "read_device_status", "read_status_word",
     "set_timing_events", "status_string", "version",
     "MLA_OK", "MLA_ERR_INVALID_ARG", "MLA_ERR_UNSUPPORTED", "MLA_ERR_WORKSPACE", "MLA_ERR_CUDA",
-    "MLA_ERR_DEVICE_TIMEOUT", "MLA_ERR_DEVICE_BOUNDS", "MLA_CACHE_BF16", "MLA_CACHE_INT8", "MLA_CACHE_FP8", "MAX_Q_LEN", "MAX_TOP_K",
+    "MLA_ERR_DEVICE_TIMEOUT", "MLA_ERR_DEVICE_BOUNDS", "MLA_CACHE_BF16", "MLA_CACHE_INT8", "MLA_CACHE_FP8",
+    "MAX_Q_LEN", "MAX_TOP_K", "MAX_PREFILL_CHUNK",
 ]
 
 MLA_OK = 0
@@ -36,6 +37,7 @@ MLA_CACHE_BF16 = 0
 MLA_CACHE_INT8 = 1
 MLA_CACHE_FP8 = 2
 MAX_Q_LEN = 8  # MLA_MAX_Q_LEN in include/mla.h
+MAX_PREFILL_CHUNK = 2048  # MLA_MAX_PREFILL_CHUNK in include/mla.h
 MAX_TOP_K = 1 << 20  # MLA_MAX_TOP_K in include/mla.h
 
 # every function include/mla.h declares
@@ -45,6 +47,7 @@ EXPORTED_SYMBOLS = (
     "mla_status_string", "mla_set_timing_events", "mla_version", "mla_decode_no_alloc",
     "mla_test_inject_wait_timeout", "mla_decode_multi_workspace_size", "mla_decode_multi",
     "mla_decode_sparse_workspace_size", "mla_decode_sparse", "mla_test_force_single_cta",
+    "mla_prefill_workspace_size", "mla_prefill",
 )
 NO_ALLOC_WORKSPACE_BYTES = 16 << 20  # MLA_NO_ALLOC_WORKSPACE_BYTES in include/mla.h
 
@@ -112,6 +115,9 @@ def load_library(build_if_missing: bool = False, path: str | None = None):
         "mla_version": (ctypes.c_int, []),
         "mla_test_inject_wait_timeout": (_I, [_I]),
         "mla_test_force_single_cta": (_I, [_I]),
+        "mla_prefill_workspace_size": (ctypes.c_size_t, [DP, _I, _I, _I]),
+        "mla_prefill": (_I, [DP, _P, _P, _I, _P, _I, _P, _I, _I, _P, _P, ctypes.c_double, _P, _P, _P, _P,
+                             ctypes.c_float, _I, _P, ctypes.c_size_t, _P, _P, _P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -265,6 +271,43 @@ def decode_multi(d: Dims, q_nope, q_pe, cache, scale_zero, block_table, seq_lens
         _ptr(workspace, None, "workspace", dev), workspace.numel() * workspace.element_size(),
         _ptr(out, torch.bfloat16, "out", dev), _ptr(lse_out, torch.float32, "lse_out", dev), _stream(stream))
     _check(st, "mla_decode_multi")
+    return out, lse_out
+
+
+def prefill_workspace_size(d: Dims, batch: int, chunk: int, num_splits: int = 0) -> int:
+    n = _L().mla_prefill_workspace_size(ctypes.byref(d), int(batch), int(chunk), int(num_splits))
+    if n == 0:
+        raise MLAError(MLA_ERR_INVALID_ARG, "mla_prefill_workspace_size")
+    return n
+
+
+def prefill(d: Dims, cache, scale_zero, block_table, seq_lens, c_kv, k_pe, q_nope, q_pe, W_UK, W_UV,
+            softmax_scale: float, rope_theta: float = 10000.0, num_splits: int = 0,
+            workspace: torch.Tensor | None = None, out: torch.Tensor | None = None,
+            lse_out: torch.Tensor | None = None, want_lse: bool = True, stream=None):
+    """mla_prefill: one chunk of chunk = q_nope.shape[1] tokens per sequence,
+    at positions seq_lens[b] - chunk .. seq_lens[b] - 1.  Writes c_kv bf16
+    [B, chunk, 512] / k_pe bf16 [B, chunk, 64] into the cache, then attends
+    q_nope bf16 [B, chunk, H, 128] / q_pe [B, chunk, H, 64] causally.  Returns
+    (out bf16 [B, chunk, H, 128], lse fp32 [B, chunk, H] or None)."""
+    B, T = q_nope.shape[0], q_nope.shape[1]
+    dev = q_nope.device
+    if workspace is None:
+        workspace = torch.empty(prefill_workspace_size(d, B, T, num_splits), dtype=torch.uint8, device=dev)
+    if out is None:
+        out = torch.empty((B, T, d.num_heads, d.v_head_dim), dtype=torch.bfloat16, device=dev)
+    if lse_out is None and want_lse:
+        lse_out = torch.empty((B, T, d.num_heads), dtype=torch.float32, device=dev)
+    cache_p, scale_p = _cache_ptrs(d, cache, scale_zero, dev)
+    st = _L().mla_prefill(
+        ctypes.byref(d), cache_p, scale_p, cache.shape[0], _ptr(block_table, torch.int32, "block_table", dev),
+        block_table.shape[1], _ptr(seq_lens, torch.int32, "seq_lens", dev), B, T,
+        _ptr(c_kv, torch.bfloat16, "c_kv", dev), _ptr(k_pe, torch.bfloat16, "k_pe", dev), float(rope_theta),
+        _ptr(q_nope, torch.bfloat16, "q_nope", dev), _ptr(q_pe, torch.bfloat16, "q_pe", dev),
+        _ptr(W_UK, torch.bfloat16, "W_UK", dev), _ptr(W_UV, torch.bfloat16, "W_UV", dev), float(softmax_scale),
+        int(num_splits), _ptr(workspace, None, "workspace", dev), workspace.numel() * workspace.element_size(),
+        _ptr(out, torch.bfloat16, "out", dev), _ptr(lse_out, torch.float32, "lse_out", dev), _stream(stream))
+    _check(st, "mla_prefill")
     return out, lse_out
 
 

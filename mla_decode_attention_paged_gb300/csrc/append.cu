@@ -32,7 +32,8 @@ __global__ void __launch_bounds__(256) append_kernel(AppendParams p) {
   const int lane = threadIdx.x & 31;
   const int i = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (i >= p.n_tokens) return;
-  const int b = p.seq_ids[i], pos = p.positions[i];
+  const int b = p.chunk > 0 ? i / p.chunk : p.seq_ids[i];
+  const int pos = p.chunk > 0 ? p.seq_lens[b] - p.chunk + i % p.chunk : p.positions[i];
   bool ok = b >= 0 && b < p.num_seqs && pos >= 0 && pos / p.page_size < p.max_pages;
   int page = -1;
   if (ok) {

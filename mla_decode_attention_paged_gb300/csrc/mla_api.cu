@@ -68,6 +68,35 @@ int decode_rows(const mla_dims* d, const void* q_nope, const void* q_pe, const v
                 const void* W_UV, float softmax_scale, int32_t num_splits, void* workspace, size_t workspace_bytes,
                 void* out, float* lse_out, mla_stream_t stream, bool reset_status);
 
+// Append parameters shared by mla_cache_append and mla_prefill (which then
+// set the token -> (sequence, position) mapping).
+AppendParams append_params(const mla_dims* d, void* cache, float* cache_scale_zero, int32_t num_pages,
+                           const int32_t* block_table, int32_t num_seqs, int32_t max_pages_per_seq, int32_t n_tokens,
+                           const void* c_kv, const void* k_pe, double rope_theta, int32_t* device_status) {
+  AppendParams p;
+  p.cache = cache;
+  p.scale_zero = cache_scale_zero;
+  p.block_table = block_table;
+  p.seq_ids = nullptr;
+  p.positions = nullptr;
+  p.seq_lens = nullptr;
+  p.chunk = 0;
+  p.c_kv = static_cast<const __nv_bfloat16*>(c_kv);
+  p.k_pe = static_cast<const __nv_bfloat16*>(k_pe);
+  p.status = device_status;
+  p.rope_theta = rope_theta;
+  // the frequencies depend only on theta: one fp64 pow per pair here instead
+  // of one per token and pair on the device's slow fp64 units
+  for (int i = 0; i < kRope / 2; ++i)
+    p.inv_freq[i] = rope_theta > 0.0 ? std::pow(rope_theta, -double(2 * i) / double(kRope)) : 0.0;
+  p.n_tokens = n_tokens;
+  p.num_seqs = num_seqs;
+  p.max_pages = max_pages_per_seq;
+  p.num_pages = num_pages;
+  p.page_size = d->page_size;
+  return p;
+}
+
 }  // namespace
 
 extern "C" {
@@ -117,24 +146,10 @@ int mla_cache_append(const mla_dims* d, void* cache, float* cache_scale_zero, in
   if (!aligned(cache, 16) || !aligned(c_kv, 16) || !aligned(k_pe, 4) || !aligned(block_table, 4) ||
       !aligned(seq_ids, 4) || !aligned(positions, 4) || (byte && !aligned(cache_scale_zero, 8)))
     return MLA_ERR_INVALID_ARG;
-  AppendParams p;
-  p.cache = cache;
-  p.scale_zero = cache_scale_zero;
-  p.block_table = block_table;
+  AppendParams p = append_params(d, cache, cache_scale_zero, num_pages, block_table, num_seqs, max_pages_per_seq,
+                                 n_tokens, c_kv, k_pe, rope_theta, device_status);
   p.seq_ids = seq_ids;
   p.positions = positions;
-  p.c_kv = static_cast<const __nv_bfloat16*>(c_kv);
-  p.k_pe = static_cast<const __nv_bfloat16*>(k_pe);
-  p.status = device_status;
-  p.rope_theta = rope_theta;
-  // the frequencies depend only on theta: one fp64 pow per pair here instead
-  // of one per token and pair on the device's slow fp64 units
-  for (int i = 0; i < kRope / 2; ++i) p.inv_freq[i] = rope_theta > 0.0 ? std::pow(rope_theta, -double(2 * i) / double(kRope)) : 0.0;
-  p.n_tokens = n_tokens;
-  p.num_seqs = num_seqs;
-  p.max_pages = max_pages_per_seq;
-  p.num_pages = num_pages;
-  p.page_size = d->page_size;
   return launch_append(p, code, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 
@@ -151,8 +166,14 @@ size_t mla_decode_workspace_size(const mla_dims* d, int32_t batch, int32_t num_s
 }
 
 size_t mla_decode_multi_workspace_size(const mla_dims* d, int32_t batch, int32_t q_len, int32_t num_splits) {
-  if (mla_check_dims(d) != MLA_OK || batch <= 0 || num_splits < 0 || q_len < 1 || q_len > MLA_MAX_Q_LEN) return 0;
-  const mla_dims dr = row_dims(d, q_len);
+  if (q_len > MLA_MAX_Q_LEN) return 0;
+  return mla_prefill_workspace_size(d, batch, q_len, num_splits);
+}
+
+size_t mla_prefill_workspace_size(const mla_dims* d, int32_t batch, int32_t chunk, int32_t num_splits) {
+  if (mla_check_dims(d) != MLA_OK || batch <= 0 || num_splits < 0 || chunk < 1 || chunk > MLA_MAX_PREFILL_CHUNK)
+    return 0;
+  const mla_dims dr = row_dims(d, chunk);
   const int s = effective_splits(&dr, num_splits);
   if (s <= 0) return 0;
   return workspace_layout(batch, dr.num_heads, s).total;
@@ -173,9 +194,49 @@ int mla_decode_multi(const mla_dims* d, const void* q_nope, const void* q_pe, co
                      int32_t max_pages_per_seq, const int32_t* seq_lens, int32_t batch, int32_t q_len,
                      const void* W_UK, const void* W_UV, float softmax_scale, int32_t num_splits, void* workspace,
                      size_t workspace_bytes, void* out, float* lse_out, mla_stream_t stream) {
+  if (q_len > MLA_MAX_Q_LEN) return MLA_ERR_INVALID_ARG;
   return decode_rows(d, q_nope, q_pe, cache, cache_scale_zero, num_pages, block_table, max_pages_per_seq, seq_lens,
                      batch, q_len, W_UK, W_UV, softmax_scale, num_splits, workspace, workspace_bytes, out, lse_out,
                      stream, true);
+}
+
+int mla_prefill(const mla_dims* d, void* cache, float* cache_scale_zero, int32_t num_pages, const int32_t* block_table,
+                int32_t max_pages_per_seq, const int32_t* seq_lens, int32_t batch, int32_t chunk, const void* c_kv,
+                const void* k_pe, double rope_theta, const void* q_nope, const void* q_pe, const void* W_UK,
+                const void* W_UV, float softmax_scale, int32_t num_splits, void* workspace, size_t workspace_bytes,
+                void* out, float* lse_out, mla_stream_t stream) {
+  int st = mla_check_dims(d);
+  if (st != MLA_OK) return st;
+  if (batch <= 0 || num_pages <= 0 || max_pages_per_seq <= 0 || chunk < 1 || chunk > MLA_MAX_PREFILL_CHUNK)
+    return MLA_ERR_INVALID_ARG;
+  const bool byte = cache_code(d) != kCodeBf16;
+  if (!cache || !block_table || !seq_lens || !c_kv || !k_pe || (byte && !cache_scale_zero)) return MLA_ERR_INVALID_ARG;
+  if (!aligned(c_kv, 16) || !aligned(k_pe, 4) || (byte && !aligned(cache_scale_zero, 16)))
+    return MLA_ERR_INVALID_ARG;
+  if ((long long)batch * chunk > (1LL << 31) - 1) return MLA_ERR_INVALID_ARG;
+  // everything decode_rows checks, before anything is launched
+  const size_t need = mla_prefill_workspace_size(d, batch, chunk, num_splits);
+  if (need == 0) return MLA_ERR_INVALID_ARG;
+  if (!workspace || !aligned(workspace, 256) || workspace_bytes < need) return MLA_ERR_WORKSPACE;
+  if (!q_nope || !q_pe || !W_UK || !W_UV || !out || !(softmax_scale > 0.f) || softmax_scale == INFINITY ||
+      !aligned(cache, 16) || !aligned(q_nope, 4) || !aligned(q_pe, 4) || !aligned(W_UK, 4) || !aligned(W_UV, 4) ||
+      !aligned(out, 4) || !aligned(block_table, 4) || !aligned(seq_lens, 4) || (lse_out && !aligned(lse_out, 4)))
+    return MLA_ERR_INVALID_ARG;
+  if ((long long)max_pages_per_seq * d->page_size > (1LL << 31) - 1) return MLA_ERR_INVALID_ARG;
+  if ((long long)num_pages * d->page_size > (1LL << 31) - 1) return MLA_ERR_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // the call's status word starts at MLA_OK before the append can report into it
+  int* status = reinterpret_cast<int*>(static_cast<char*>(workspace) + workspace_layout(batch, d->num_heads, 1).status);
+  if (cudaMemsetAsync(status, 0, sizeof(int), s) != cudaSuccess) return MLA_ERR_CUDA;
+  AppendParams ap = append_params(d, cache, cache_scale_zero, num_pages, block_table, batch, max_pages_per_seq,
+                                  batch * chunk, c_kv, k_pe, rope_theta, status);
+  ap.seq_lens = seq_lens;
+  ap.chunk = chunk;
+  if (launch_append(ap, cache_code(d), s) != cudaSuccess) return MLA_ERR_CUDA;
+  // the chunk's queries as multi-token rows over the cache that now holds the chunk
+  return decode_rows(d, q_nope, q_pe, cache, cache_scale_zero, num_pages, block_table, max_pages_per_seq, seq_lens,
+                     batch, chunk, W_UK, W_UV, softmax_scale, num_splits, workspace, workspace_bytes, out, lse_out,
+                     stream, false);
 }
 
 }  // extern "C"
@@ -194,7 +255,7 @@ int decode_rows(const mla_dims* d, const void* q_nope, const void* q_pe, const v
   const int code = cache_code(d);
   const bool byte = code != kCodeBf16;
   if (batch <= 0 || num_pages <= 0 || max_pages_per_seq <= 0 || num_splits < 0) return MLA_ERR_INVALID_ARG;
-  if (q_len < 1 || q_len > MLA_MAX_Q_LEN) return MLA_ERR_INVALID_ARG;
+  if (q_len < 1 || q_len > MLA_MAX_PREFILL_CHUNK) return MLA_ERR_INVALID_ARG;
   if (!(softmax_scale > 0.f) || softmax_scale == INFINITY) return MLA_ERR_INVALID_ARG;
   if (!q_nope || !q_pe || !cache || !block_table || !seq_lens || !W_UK || !W_UV || !out) return MLA_ERR_INVALID_ARG;
   if (byte && !cache_scale_zero) return MLA_ERR_INVALID_ARG;

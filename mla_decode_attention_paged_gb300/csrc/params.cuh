@@ -54,8 +54,11 @@ struct AppendParams {
   void* cache;                   // bf16, int8 or e4m3 [num_pages, P, 576]
   float* scale_zero;             // [num_pages, P, 2] (INT8) or [num_pages, P] (FP8)
   const int* block_table;        // [num_seqs, max_pages]
-  const int* seq_ids;            // [N]
-  const int* positions;          // [N]
+  const int* seq_ids;            // [N]   (chunk == 0)
+  const int* positions;          // [N]   (chunk == 0)
+  const int* seq_lens;           // [num_seqs] (chunk > 0: token i is token i % chunk of sequence
+                                 // i / chunk, at position seq_lens[b] - chunk + i % chunk)
+  int chunk;                     // 0: explicit seq_ids / positions; > 0: prefill chunk per sequence
   const __nv_bfloat16* c_kv;     // [N, 512]
   const __nv_bfloat16* k_pe;     // [N, 64]
   int* status;                   // optional

@@ -42,6 +42,8 @@ class Workload:
     q_len: int = 1                  # query tokens per sequence (multi-token decode: the last q_len cached)
     top_k: int = 0                  # sparse decode: attend to top_k drawn positions per sequence (0: all)
     fp8: bool = False               # cache built from N(0,1) rows by the FP8 (E4M3) append
+    chunk: int = 0                  # chunked prefill: the last `chunk` tokens of each sequence are the
+                                    # chunk, written and attended by one prefill call (0: decode)
 
     @property
     def quantised(self) -> bool:
@@ -77,6 +79,9 @@ WORKLOADS = {
     "int8_v2lite": Workload("int8_v2lite_b32_h16_l32768_p64", 32, 16, 32768, 64, True, 1.0, 0.02, 1.0, 8, int8=True),
     # the V2-Lite batch over an FP8 (E4M3) cache with one scale per token
     "fp8_v2lite": Workload("fp8_v2lite_b32_h16_l32768_p64", 32, 16, 32768, 64, True, 1.0, 0.02, 1.0, 9, fp8=True),
+    # chunked prefill on the V2-Lite shape: 4 sequences, a 512-token chunk after 8,192 cached tokens
+    "v2lite_prefill512": Workload("v2lite_prefill512_b4_h16_l8704_p64", 4, 16, 8704, 64, True, 1.0, 0.02, 1.0, 10,
+                                  chunk=512),
     # sparse decode (DeepSeek Sparse Attention's top-2048 selection) over the V2-Lite cache
     "v2lite_topk2048": Workload("v2lite_topk2048_b32_h16_l32768_p64", 32, 16, 32768, 64, True, 1.0, 0.02, 1.0, 7,
                                 top_k=2048),
@@ -175,9 +180,13 @@ def make_decode_inputs(w: Workload, device="cpu"):
         d["cache"] = draw_bf16((num_pages, w.page_size, LATENT_DIM + ROPE_DIM), w.cache_std, g)
     d["W_UK"] = draw_bf16((w.heads, NOPE_DIM, LATENT_DIM), w.w_std, g)
     d["W_UV"] = draw_bf16((w.heads, V_DIM, LATENT_DIM), w.w_std, g)
-    qshape = (w.batch, w.heads) if w.q_len == 1 else (w.batch, w.q_len, w.heads)
+    T = w.chunk or w.q_len
+    qshape = (w.batch, w.heads) if T == 1 else (w.batch, T, w.heads)
     d["q_nope"] = draw_bf16(qshape + (NOPE_DIM,), w.q_std, g)
     d["q_pe"] = draw_bf16(qshape + (ROPE_DIM,), w.q_std, g)
+    if w.chunk:  # the chunk's new rows (unrotated RoPE key), written by the prefill call
+        d["chunk_c_kv"] = draw_bf16((w.batch, w.chunk, LATENT_DIM), 1.0, g)
+        d["chunk_k_pe"] = draw_bf16((w.batch, w.chunk, ROPE_DIM), 1.0, g)
     if w.top_k:
         d["token_indices"] = draw_token_indices(seq_lens.cpu(), w.top_k, 1.0, g).to(device)
     if w.quantised:

@@ -130,6 +130,38 @@ def test_multi_token_workspace_and_validation(lib):
     assert lib.mla_decode_multi(*a) == mla.MLA_ERR_INVALID_ARG
 
 
+def test_prefill_workspace_and_validation(lib):
+    d = mla.dims(16, 64)
+    # a chunk of T tokens needs the workspace of T-token multi-token decode
+    for T in (1, 8, 64, 512):
+        dT = mla.dims(16 * T, 64)
+        got = lib.mla_prefill_workspace_size(ctypes.byref(d), 4, T, 3)
+        assert got == lib.mla_decode_workspace_size(ctypes.byref(dT), 4, 3) > 0
+    assert lib.mla_prefill_workspace_size(ctypes.byref(d), 4, 0, 3) == 0
+    assert lib.mla_prefill_workspace_size(ctypes.byref(d), 4, mla.MAX_PREFILL_CHUNK + 1, 3) == 0
+    assert mla.MAX_PREFILL_CHUNK > mla.MAX_Q_LEN
+    fake = ctypes.c_void_p(0x10000)  # never dereferenced: validation fails first
+    big = ctypes.c_size_t(1 << 40)
+    args = [ctypes.byref(d), fake, None, 4, fake, 8, fake, 2, 64, fake, fake, ctypes.c_double(1e4), fake, fake,
+            fake, fake, ctypes.c_float(0.1), 3, fake, big, fake, None, None]
+    for bad_chunk in (0, -2, mla.MAX_PREFILL_CHUNK + 1):
+        a = list(args); a[8] = bad_chunk
+        assert lib.mla_prefill(*a) == mla.MLA_ERR_INVALID_ARG
+    a = list(args); a[9] = None                       # no new rows
+    assert lib.mla_prefill(*a) == mla.MLA_ERR_INVALID_ARG
+    a = list(args); a[12] = None                      # no queries
+    assert lib.mla_prefill(*a) == mla.MLA_ERR_INVALID_ARG
+    a = list(args); a[9] = ctypes.c_void_p(0x10008)   # rows not 16-byte aligned
+    assert lib.mla_prefill(*a) == mla.MLA_ERR_INVALID_ARG
+    a = list(args); a[18] = ctypes.c_void_p(0x10040)  # workspace not 256-byte aligned
+    assert lib.mla_prefill(*a) == mla.MLA_ERR_WORKSPACE
+    a = list(args); a[19] = ctypes.c_size_t(64)       # workspace too small
+    assert lib.mla_prefill(*a) == mla.MLA_ERR_WORKSPACE
+    df = mla.dims(16, 64, fp8=True)
+    a = list(args); a[0] = ctypes.byref(df)           # FP8 cache without its scales
+    assert lib.mla_prefill(*a) == mla.MLA_ERR_INVALID_ARG
+
+
 def test_sparse_workspace_and_validation(lib):
     d = mla.dims(16, 64)
     dec = lib.mla_decode_workspace_size(ctypes.byref(d), 32, 76)
