@@ -512,8 +512,9 @@ def prefill_chunk(cache: np.ndarray, scale_zero: np.ndarray | None, block_table:
 
     Sequence b's chunk is the T tokens at positions L_b - T .. L_b - 1, L_b =
     seq_lens[b] counting the chunk.  First every chunk token's row is
-    appended (``append_tokens``, in place on ``cache``; positions below 0 are
-    skipped), then query token t attends to positions 0 .. L_b - T + t
+    appended (``append_tokens``, in place on ``cache``; a position below 0,
+    past the page table, or on a page-table entry below 0 is skipped), then
+    query token t attends to positions 0 .. L_b - T + t
     (``decode_multi_token``: the history and the chunk's tokens up to itself).
 
     c_kv_bits [B, T, 512], k_pe_bits [B, T, 64] bf16 bit patterns; q_nope
@@ -523,7 +524,8 @@ def prefill_chunk(cache: np.ndarray, scale_zero: np.ndarray | None, block_table:
     B, T = q_nope.shape[0], q_nope.shape[1]
     for b in range(B):
         L = int(seq_lens[b])
-        ts = [t for t in range(T) if L - T + t >= 0]
+        ts = [t for t in range(T) if 0 <= L - T + t < block_table.shape[1] * page_size
+              and block_table[b, (L - T + t) // page_size] >= 0]
         if ts:
             append_tokens(cache, scale_zero, block_table, [b] * len(ts), [L - T + t for t in ts],
                           c_kv_bits[b, ts], k_pe_bits[b, ts], rope_theta, page_size, int8, fp8=fp8)

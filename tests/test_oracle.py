@@ -629,3 +629,16 @@ def test_prefill_in_chunks_matches_one_chunk_and_writes_the_cache():
         np.testing.assert_array_equal(one[page, off, :512], c_bits[b, 0])
         page, off = O.page_slot(table, b, hist[b] - 1, P)    # the history before it is untouched
         np.testing.assert_array_equal(one[page, off], base[page, off])
+
+
+def test_prefill_skips_tokens_without_a_page():
+    """Tokens whose position is negative or whose page-table entry is -1 are
+    not written anywhere (a -1 entry must not alias the last page)."""
+    B, T, H, P = 2, 6, 1, 16
+    table, W_UK, W_UV, c_bits, k_bits, qn, qp = _prefill_inputs(B, T, H, P, 1, 5)
+    table = np.array([[0], [-1]], np.int32)     # sequence 1 has no page
+    cache = np.zeros((1, P, 576), np.uint16)
+    O.prefill_chunk(cache, None, table, [4, 10], c_bits, k_bits, 0.0, qn, qp, W_UK, W_UV, 0.1, P, False,
+                    triples=[])
+    np.testing.assert_array_equal(cache[0, :4, :512], c_bits[0, 2:])   # positions 0..3 = tokens 2..5
+    assert not cache[0, 4:].any()
