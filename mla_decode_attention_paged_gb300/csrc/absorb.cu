@@ -87,13 +87,14 @@ __device__ __forceinline__ float round_out(float v, uint16_t* dst) {  // store a
 }
 
 // ---------------------------------------------------------------------------
-// Absorption on the tensor cores.  Per head (query row h of each sequence,
-// weight head h % heads_w: multi-token decode has q_len rows per weight
-// head) the product is a small GEMM,
-// q_lat^T [512 x B] = W^UK_h^T [512 x 128] * q_nope_h^T [128 x B]; a CTA takes
-// one 128-row tile of latent dims (the MMA's M) and NB sequences (its N):
+// Absorption on the tensor cores.  Per weight head h the product is a GEMM
+// over every query column -- a (sequence, token) pair: multi-token decode and
+// prefill have q_len tokens per sequence, whose rows t * heads_w + h share
+// head h's weights --
+// q_lat^T [512 x cols] = W^UK_h^T [512 x 128] * q_nope_h^T [128 x cols]; a CTA
+// takes one 128-row tile of latent dims (the MMA's M) and NB columns (its N):
 //   A = W^UK_h[:, m0:m0+128]^T   MN-major (W^UK rows are 512 latent dims long)
-//   B = q_nope[b0:b0+NB, h, :]^T K-major  (q_nope rows are 128 content dims)
+//   B = q_nope[c0:c0+NB, h, :]^T K-major  (q_nope rows are 128 content dims)
 // both staged by the CTA's threads into 128-byte-swizzled shared memory, eight
 // K = 16 MMAs into an fp32 TMEM accumulator, then one thread per latent dim
 // rounds its column of sequences to bf16 (fp16 for INT8 caches) and stores it.
@@ -133,9 +134,10 @@ __global__ void __launch_bounds__(kAbsThreads) absorb_kernel(AbsorbParams p) {
   float* red = reinterpret_cast<float*>(smem + C::kOffMisc + 64);  // [NB][4] per-warp sums
   float* rope_sum = red + NB * 4;                                  // [NB]
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int per_head = 4 * ((p.batch + NB - 1) / NB);
+  // column c0 + r is row (c0 + r) * heads_w + h of q_nope, q_full and q_sum
+  const int per_head = 4 * ((p.cols + NB - 1) / NB);
   const int tile = blockIdx.x - 1, h = tile / per_head, rem = tile % per_head, mt = rem & 3, b0 = (rem >> 2) * NB;
-  const int m0 = mt * kAbsMTile, nb = min(NB, p.batch - b0);
+  const int m0 = mt * kAbsMTile, nb = min(NB, p.cols - b0);
   if (tid == 0) {
     mbar_init(mma_done, 1);
     *abort_flag = 0;
@@ -157,13 +159,13 @@ __global__ void __launch_bounds__(kAbsThreads) absorb_kernel(AbsorbParams p) {
 #pragma unroll
   for (int u = 0; u < kWPer; ++u) {
     const int i = tid + u * kAbsThreads, k = i >> 4, j = i & 15;
-    wv[u] = *reinterpret_cast<const uint4*>(p.W_UK + (size_t(h % p.heads_w) * kNope + k) * kLatent + m0 + 8 * j);
+    wv[u] = *reinterpret_cast<const uint4*>(p.W_UK + (size_t(h) * kNope + k) * kLatent + m0 + 8 * j);
   }
 #pragma unroll
   for (int u = 0; u < kQPer; ++u) {
     const int i = tid + u * kAbsThreads, r = i >> 4, j = i & 15;
     qv[u] = make_uint4(0, 0, 0, 0);
-    if (r < nb) qv[u] = *reinterpret_cast<const uint4*>(p.q_nope + (size_t(b0 + r) * p.heads + h) * kNope + 8 * j);
+    if (r < nb) qv[u] = *reinterpret_cast<const uint4*>(p.q_nope + (size_t(b0 + r) * p.heads_w + h) * kNope + 8 * j);
   }
 #pragma unroll
   for (int u = 0; u < kWPer; ++u) {
@@ -201,7 +203,7 @@ __global__ void __launch_bounds__(kAbsThreads) absorb_kernel(AbsorbParams p) {
       const int r = (tid >> 3) + u * (kAbsThreads / 8);
       pe[u] = make_uint4(0, 0, 0, 0);
       if (r < nb)
-        pe[u] = *reinterpret_cast<const uint4*>(p.q_pe + (size_t(b0 + r) * p.heads + h) * kRope + (tid & 7) * 8);
+        pe[u] = *reinterpret_cast<const uint4*>(p.q_pe + (size_t(b0 + r) * p.heads_w + h) * kRope + (tid & 7) * 8);
     }
 #pragma unroll
     for (int u = 0; u < kPasses; ++u) {
@@ -212,7 +214,7 @@ __global__ void __launch_bounds__(kAbsThreads) absorb_kernel(AbsorbParams p) {
 #pragma unroll
       for (int e = 0; e < 8; ++e) rs += round_out<kF16>(bf2f(x[e]), &o[e]);
       if (r < nb)
-        *reinterpret_cast<uint4*>(qf + (size_t(b0 + r) * p.heads + h) * kRow + kLatent + (tid & 7) * 8) =
+        *reinterpret_cast<uint4*>(qf + (size_t(b0 + r) * p.heads_w + h) * kRow + kLatent + (tid & 7) * 8) =
             *reinterpret_cast<const uint4*>(o);
       if (kF16) {
 #pragma unroll
@@ -233,7 +235,7 @@ __global__ void __launch_bounds__(kAbsThreads) absorb_kernel(AbsorbParams p) {
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
         const int r = c + i;
-        v[i] = r < nb ? round_out<kF16>(v[i], qf + (size_t(b0 + r) * p.heads + h) * kRow + m) : 0.f;
+        v[i] = r < nb ? round_out<kF16>(v[i], qf + (size_t(b0 + r) * p.heads_w + h) * kRow + m) : 0.f;
       }
       if (kF16) {  // INT8 caches: this warp's 32 dims summed per sequence; lanes 2i, 2i + 1 get sequence c + i
         const float sum = dc::warp_transpose_reduce<16, false>(v, lane);
@@ -251,7 +253,7 @@ __global__ void __launch_bounds__(kAbsThreads) absorb_kernel(AbsorbParams p) {
       const int r = i >> 1, q = i & 1;
       float v = red[r * 4 + 2 * q] + red[r * 4 + 2 * q + 1];
       if (mt == 0 && q == 0) v += rope_sum[r];
-      p.q_sum[(size_t(b0 + r) * p.heads + h) * kQSumParts + 2 * mt + q] = v;
+      p.q_sum[(size_t(b0 + r) * p.heads_w + h) * kQSumParts + 2 * mt + q] = v;
     }
   if (warp == 0) {
     tc_fence_after();
@@ -271,15 +273,15 @@ cudaError_t launch_absorb_nb(const AbsorbParams& p, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 128) attr[dev] = true;
   }
-  const int tiles = p.heads * 4 * ((p.batch + NB - 1) / NB);
+  const int tiles = p.heads_w * 4 * ((p.cols + NB - 1) / NB);
   return launch_pdl(absorb_kernel<kF16, NB>, dim3(tiles + 1), dim3(kAbsThreads), C::kSmem, stream, 1, p);
 }
 
 template <bool kF16>
 cudaError_t launch_absorb_t(const AbsorbParams& p, cudaStream_t stream) {
-  if (p.batch <= 16) return launch_absorb_nb<kF16, 16>(p, stream);
-  if (p.batch <= 32) return launch_absorb_nb<kF16, 32>(p, stream);
-  if (p.batch <= 64) return launch_absorb_nb<kF16, 64>(p, stream);
+  if (p.cols <= 16) return launch_absorb_nb<kF16, 16>(p, stream);
+  if (p.cols <= 32) return launch_absorb_nb<kF16, 32>(p, stream);
+  if (p.cols <= 64) return launch_absorb_nb<kF16, 64>(p, stream);
   return launch_absorb_nb<kF16, 128>(p, stream);
 }
 

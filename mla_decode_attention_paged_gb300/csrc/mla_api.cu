@@ -290,6 +290,7 @@ int decode_rows(const mla_dims* d, const void* q_nope, const void* q_pe, const v
   ap.heads = H;
   ap.heads_w = d->num_heads;
   ap.reset_status = reset_status ? 1 : 0;
+  ap.cols = batch * q_len;
   ap.max_len = max_pages_per_seq * d->page_size;
   ap.num_splits = S;
   if (launch_absorb(ap, byte, s) != cudaSuccess) return MLA_ERR_CUDA;

@@ -31,6 +31,11 @@ struct AbsorbParams {
   int* status;
   int batch, heads, heads_w, max_len, num_splits;
   int reset_status;  // 1: the plan starts the call's status word at MLA_OK (0: a kernel before it did)
+  // The absorption GEMM's view of the rows: row v = t * heads_w + h of
+  // sequence b is column b * q_len + t of weight head h, so each head's
+  // product covers every (sequence, token) column at once; cols = batch *
+  // q_len, q_nope / q_full / q_sum rows are at (column * heads_w + h).
+  int cols;
 };
 
 // Sparse (top-k) decode: the listed rows of each sequence, compacted in list
