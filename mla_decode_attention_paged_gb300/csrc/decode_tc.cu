@@ -28,7 +28,7 @@
 // 1-byte caches (INT8 or FP8, 73 KB per tile): one ring of pair slots + RoPE
 // slots serves both products; the codes are expanded in place.
 //
-// Warp roles (288 threads; 256 for 32-head bf16 groups):
+// Warp roles (288 threads; 256 for 32-head bf16 groups; 352 for 1-byte caches):
 //   warp 0     TMA producer: Q of each segment; bf16: QK ring 0 (16 heads:
 //              boxes 0, 2, 4, 6, 8 of each tile; 32 heads: all 9 boxes);
 //              INT8: the pair and RoPE slots (codes)
@@ -40,8 +40,8 @@
 //              thread cannot issue TMA copies fast enough for an SM's share
 //              of HBM; bf16, 32 heads: the PV-ring producer
 //   warp 8     bf16, 16 heads: the PV-ring producer
-//   warps 3, 8 INT8 / FP8: expand the TMA-loaded codes in place into fp16
-//              operand tiles
+//   warps 3, 8-10  INT8 / FP8: expand the TMA-loaded codes in place into
+//              fp16 operand tiles
 //   warps 4-7  softmax (one thread per token row of S^T) and epilogue
 //
 // INT8 caches: value = s_t (code - zp_t) per token.  A code v in [-128, 127]
@@ -72,7 +72,7 @@ namespace {
 using namespace ptx;
 using namespace dc;
 
-// Nine warps leave three on one SM sub-partition (16K registers each), which
+// Nine warps (eleven for 1-byte caches) leave three on one SM sub-partition (16K registers each), which
 // caps a thread at 168 registers: enough except for the 32-head bf16 softmax,
 // which runs with eight warps and a single QK producer.
 constexpr uint32_t kBoxBytes = 16384;           // 128 rows x 128 B (64 bf16)
@@ -89,7 +89,7 @@ constexpr bool kPvGate = true;
 
 template <int HC, bool kByte>
 struct Cfg {
-  static constexpr int kThreads = (kByte || HC == 16) ? 288 : 256;
+  static constexpr int kThreads = kByte ? 352 : (HC == 16 ? 288 : 256);
   static constexpr int kQkRings = (!kByte && HC == 16) ? 2 : 1;   // bf16 QK producers (rings)
   static constexpr int kQkSlots = kByte ? 0 : 6;                  // bf16 QK ring slots (single boxes), all rings
   static constexpr int kQkRing = kQkSlots / kQkRings;
@@ -142,19 +142,21 @@ __device__ __forceinline__ bool wait_progress(const int* counter, int k, const v
   }
 }
 
-__device__ __forceinline__ bool converters_any(bool pred) {  // OR over the 64 INT8 expansion threads (barrier 2)
+// 1-byte caches: four warps (3, 8, 9, 10) expand the codes, named barrier 2
+constexpr int kConvThreads = 128;
+__device__ __forceinline__ bool converters_any(bool pred) {  // OR over the expansion threads (barrier 2)
   uint32_t r;
   asm volatile(
       "{\n\t.reg .pred p, q;\n\t"
       "setp.ne.u32 p, %1, 0;\n\t"
-      "bar.red.or.pred q, 2, 64, p;\n\t"
+      "bar.red.or.pred q, 2, %2, p;\n\t"
       "selp.u32 %0, 1, 0, q;\n\t}"
       : "=r"(r)
-      : "r"(uint32_t(pred))
+      : "r"(uint32_t(pred)), "n"(kConvThreads)
       : "memory");
   return r != 0;
 }
-__device__ __forceinline__ void converters_sync() { asm volatile("bar.sync 2, 64;" ::: "memory"); }
+__device__ __forceinline__ void converters_sync() { asm volatile("bar.sync 2, %0;" ::"n"(kConvThreads) : "memory"); }
 
 __device__ __forceinline__ void fail(Barriers* B, int* status) {
   B->abort = 1;
@@ -510,29 +512,31 @@ __global__ void __launch_bounds__(Cfg<HC, kCode != kCodeBf16>::kThreads, 1)
       mma_commit(&B->drain[1]);
       mbar_wait(&B->drain[1], 0, abort_flag, kWaitLimitNs);
     }
-  } else if (kByte && (warp == 3 || warp == 8)) {
+  } else if (kByte && (warp == 3 || warp >= 8)) {
     if constexpr (kByte) {
-      // ------------------------------------------------------------ INT8 expansion
-      // Warps 3 and 8 turn each landed [128 x 64 B] code block into a swizzled
-      // fp16 operand box.  Pair slots hold the codes of boxes 2c and 2c+1 in
-      // their back half: block 0 (at +16 KB) expands into [0, 16 KB) without
-      // overlap; block 1 (at +24 KB) overlaps its destination, so all 64
-      // threads read it before any of them writes.  The RoPE slot's block sits
-      // at +8 KB and overlaps too.
-      const int ct = (warp == 3 ? 0 : 32) + lane, ch = ct & 3, r0 = ct >> 2;  // rows r0 + 16j
+      // ------------------------------------------------------------ code expansion
+      // Warps 3, 8, 9 and 10 turn each landed [128 x 64 B] code block into a
+      // swizzled fp16 operand box.  Pair slots hold the codes of boxes 2c and
+      // 2c+1 in their back half: block 0 (at +16 KB) expands into [0, 16 KB)
+      // without overlap; block 1 (at +24 KB) overlaps its destination, so all
+      // expansion threads read it before any of them writes.  The RoPE slot's
+      // block sits at +8 KB and overlaps too.
+      constexpr int kRowStep = kConvThreads / 4, kRowsPer = kTile / kRowStep;
+      const int ct = (warp == 3 ? 0 : 32 * (warp - 7)) + lane, ch = ct & 3, r0 = ct >> 2;  // rows r0 + kRowStep j
       TileWalker walk;
       walk.init(p.tile_start, p.seg_base, p.len, p.batch, int(S), pa, pb);
       uint32_t pair_it = 0, rope_it = 0;
       TileInfo t;
       bool ok = true;
-      auto read_block = [&](const uint8_t* src, uint4 (&v)[8]) {
+      auto read_block = [&](const uint8_t* src, uint4 (&v)[kRowsPer]) {
 #pragma unroll
-        for (int j = 0; j < 8; ++j) v[j] = *reinterpret_cast<const uint4*>(src + (r0 + 16 * j) * 64 + ch * 16);
+        for (int j = 0; j < kRowsPer; ++j)
+          v[j] = *reinterpret_cast<const uint4*>(src + (r0 + kRowStep * j) * 64 + ch * 16);
       };
-      auto write_block = [&](const uint4 (&v)[8], uint8_t* dst) {
+      auto write_block = [&](const uint4 (&v)[kRowsPer], uint8_t* dst) {
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const int r = r0 + 16 * j;
+        for (int j = 0; j < kRowsPer; ++j) {
+          const int r = r0 + kRowStep * j;
           uint4 lo, hi;
           if constexpr (kZp) expand_codes(v[j], lo, hi);
           else expand_e4m3(v[j], lo, hi);
@@ -549,14 +553,14 @@ __global__ void __launch_bounds__(Cfg<HC, kCode != kCodeBf16>::kThreads, 1)
           uint64_t* full_i8 = rope ? &B->full_i8_rope[slot] : &B->full_i8_pair[slot];
           uint8_t* base = smem + (rope ? C::kOffRope + slot * kBoxBytes : C::kOffPair + slot * kPairBytes);
           const bool landed = mbar_wait(full_i8, (it / nslot) & 1, abort_flag, kWaitLimitNs);
-          uint4 v[8];
+          uint4 v[kRowsPer];
           if (!rope) {
             read_block(base + kBoxBytes, v);
             write_block(v, base);
           }
           read_block(base + (rope ? 8192 : kBoxBytes + 8192), v);
           // all codes of the overlapping block read before any write; a timeout
-          // anywhere stops the 64 threads together
+          // anywhere stops the expansion threads together
           if (converters_any(!landed)) {
             ok = false;
             break;
