@@ -95,19 +95,21 @@ __global__ void __launch_bounds__(kUVThreads, 1)
     tmem_alloc(tmem_slot, C::kTmemCols);
     tmem_relinquish();
   }
-  // seg_base comes from the absorption kernel, two launches back: this grid
-  // starts only after every CTA of the attention kernel between them has
-  // waited for it, so it is complete and can be read before the wait below
-  // (which covers the partial results of the attention kernel itself)
-  if (tid <= nb) seg[tid] = p.seg_base[b0 + tid];
-  griddep_wait();
-  griddep_launch_dependents();
+  // This grid starts only after every CTA of the attention kernel has passed
+  // its own wait, i.e. after the absorption kernel (and, through its wait,
+  // everything before the call) completed.  So seg_base (written by the
+  // absorption kernel) and W^UV (an input no kernel of the call writes) can
+  // be read before the wait below, which covers the attention kernel's
+  // partial results: W^UV's copy then runs under the attention kernel's tail.
   if (tid == 0) {
     mbar_arrive_expect_tx(w_full, kUVWBytes);
 #pragma unroll
     for (int kb = 0; kb < 8; ++kb)
       tma_load_2d(smem + kb * kUVWBlock, &tmap_wuv, 64 * kb, (h % p.heads_w) * kVDim, w_full);
   }
+  if (tid <= nb) seg[tid] = p.seg_base[b0 + tid];
+  griddep_wait();
+  griddep_launch_dependents();
   __syncthreads();
 
   // ---- 1. merge.  wps warps per sequence (about kUVBatch segments each, as
