@@ -13,18 +13,19 @@ namespace mla {
 using namespace ptx;
 
 // ---------------------------------------------------------------------------
-// Merge and up-projection in one kernel.  A CTA takes one head h (query row
-// h of each sequence; weight head h % heads_w) and NB sequences:
-//   1. its 16 warps merge each sequence's segments (partial outputs of the
-//      split-KV ranges) with log-sum-exp weights into o_lat[b][h] (fp32), and
+// Merge and up-projection in one kernel.  A CTA takes one weight head h and
+// NB query columns -- a column c = b * q_len + t is query token t of
+// sequence b, whose row t * heads_w + h uses head h's weights:
+//   1. its 16 warps merge each column's segments (the partial outputs of its
+//      sequence's split-KV ranges) with log-sum-exp weights into o_lat (fp32), and
 //      store it in shared memory as two bf16 rows, hi = bf16(o) and
 //      lo = bf16(o - hi), which carry o to about 2^-16 relative;
 //   2. one thread issues D [128 x 2 NB] = W^UV_h [128 x 512] * [hi | lo]^T on
 //      the tensor cores (32 K = 16 MMAs, fp32 accumulation in TMEM; the hi
 //      rows are D's first NB columns, the lo rows its last NB), with W^UV_h
 //      (exact in bf16) brought in by TMA while the warps merge;
-//   3. one thread per output dim j stores out[b][h][j] = D[j][b] + D[j][NB + b]
-//      (bf16) for the tile's sequences.
+//   3. one thread per output dim j stores out[c][h][j] = D[j][c] + D[j][NB + c]
+//      (bf16) for the tile's columns.
 // Both operands are K-major with 128-byte swizzle, in blocks of 64 latent
 // dims: W^UV_h block kb = rows j x dims [64 kb, 64 kb + 64) (16 KB), and the
 // [hi | lo] block kb = 2 NB rows x the same dims.
@@ -41,8 +42,8 @@ struct UVCfg {
   static constexpr uint32_t kBBlock = 2 * NB * 128;
   static constexpr uint32_t kOffB = kUVWBytes;
   static constexpr uint32_t kOffX = kOffB + 8 * kBBlock;  // [kUVWarps][512] fp32 cross-warp sums
-  static constexpr uint32_t kOffSeg = kOffX + kUVWarps * kLatent * 4;  // seg_base of the tile, NB + 1 ints
-  static constexpr uint32_t kOffMisc = kOffSeg + 256;
+  static constexpr uint32_t kOffSeg = kOffX + kUVWarps * kLatent * 4;  // per column: first segment, row; NB + 1 ends
+  static constexpr uint32_t kOffMisc = kOffSeg + 512;
   static constexpr uint32_t kSmem = kOffMisc + 64 + 1024;
   static constexpr uint32_t kTmemCols = 2 * NB < 32 ? 32 : 2 * NB;
   static_assert(kSmem <= 232448, "dynamic shared memory of one CTA");
@@ -80,10 +81,13 @@ __global__ void __launch_bounds__(kUVThreads, 1)
   int* abort_flag = reinterpret_cast<int*>(smem + C::kOffMisc + 20);
   uint8_t* bsm = smem + C::kOffB;
   float* xs = reinterpret_cast<float*>(smem + C::kOffX);
-  int* seg = reinterpret_cast<int*>(smem + C::kOffSeg);
+  int* seg_lo = reinterpret_cast<int*>(smem + C::kOffSeg);  // [NB] first segment of the column's sequence
+  int* seg_hi = seg_lo + NB;                                  // [NB] its end
+  int* row_of = seg_hi + NB;                                  // [NB] the column's row within its sequence
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int per_head = (p.batch + NB - 1) / NB;
-  const int h = blockIdx.x / per_head, b0 = (blockIdx.x % per_head) * NB, nb = min(NB, p.batch - b0);
+  const int cols = p.batch * p.q_len;
+  const int per_head = (cols + NB - 1) / NB;
+  const int h = blockIdx.x / per_head, b0 = (blockIdx.x % per_head) * NB, nb = min(NB, cols - b0);
   if (tid == 0) {
     mbar_init(w_full, 1);
     mbar_init(mma_done, 1);
@@ -105,31 +109,38 @@ __global__ void __launch_bounds__(kUVThreads, 1)
     mbar_arrive_expect_tx(w_full, kUVWBytes);
 #pragma unroll
     for (int kb = 0; kb < 8; ++kb)
-      tma_load_2d(smem + kb * kUVWBlock, &tmap_wuv, 64 * kb, (h % p.heads_w) * kVDim, w_full);
+      tma_load_2d(smem + kb * kUVWBlock, &tmap_wuv, 64 * kb, h * kVDim, w_full);
   }
-  if (tid <= nb) seg[tid] = p.seg_base[b0 + tid];
+  if (tid < nb) {
+    const int b = (b0 + tid) / p.q_len;
+    seg_lo[tid] = p.seg_base[b];
+    seg_hi[tid] = p.seg_base[b + 1];
+    row_of[tid] = ((b0 + tid) % p.q_len) * p.heads_w + h;
+  }
   griddep_wait();
   griddep_launch_dependents();
   __syncthreads();
 
-  // ---- 1. merge.  wps warps per sequence (about kUVBatch segments each, as
-  // far as the tile's sequences still fit in one round), G = kUVWarps / wps
-  // sequences at a time
-  const int avg = (seg[nb] - seg[0] + nb - 1) / nb;
+  // ---- 1. merge.  wps warps per column (about kUVBatch segments each, as
+  // far as the tile's columns still fit in one round), G = kUVWarps / wps
+  // columns at a time
+  int nseg = 0;
+  for (int r = 0; r < nb; ++r) nseg += seg_hi[r] - seg_lo[r];
+  const int avg = (nseg + nb - 1) / nb;
   int g_min = 1;
   while (g_min < kUVWarps && g_min < nb) g_min *= 2;
   int wps = 1;
   while (wps < kUVWarps / g_min && kUVBatch * wps < avg) wps *= 2;
   const int G = kUVWarps / wps, wi = warp % wps;
   for (int base = 0; base < nb; base += G) {
-    const int r = base + warp / wps;  // row of this warp's sequence in the tile
+    const int r = base + warp / wps;  // this warp's column in the tile
     float acc[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) acc[i] = 0.f;
     if (r < nb) {
-      const int b = b0 + r, s0 = seg[r], n = seg[r + 1] - s0;
-      const float* lse = p.partial_lse + size_t(s0) * p.heads + h;
-      const float* po = p.partial_o + size_t(s0) * p.heads * kLatent + size_t(h) * kLatent + 16 * lane;
+      const int c = b0 + r, s0 = seg_lo[r], n = seg_hi[r] - s0, row = row_of[r];
+      const float* lse = p.partial_lse + size_t(s0) * p.heads + row;
+      const float* po = p.partial_o + size_t(s0) * p.heads * kLatent + size_t(row) * kLatent + 16 * lane;
       const size_t seg_stride = size_t(p.heads) * kLatent;
       // the first batch of rows is requested together with the lse values
       float4 v[kUVBatch][4];
@@ -172,7 +183,7 @@ __global__ void __launch_bounds__(kUVThreads, 1)
         }
       }
       if (wi == 0 && lane == 0 && p.lse_out)
-        p.lse_out[size_t(b) * p.heads + h] = mx != -INFINITY ? mx + logf(z) : -INFINITY;
+        p.lse_out[size_t(c) * p.heads_w + h] = mx != -INFINITY ? mx + logf(z) : -INFINITY;
       if (mx != -INFINITY) {
         const float inv_z = 1.f / z;
         // segments wi, wi + wps, ..., kUVBatch at a time
@@ -286,7 +297,7 @@ __global__ void __launch_bounds__(kUVThreads, 1)
       tmem_ld8(tmem + row + NB + c, vl);
 #pragma unroll
       for (int i = 0; i < 8; ++i)
-        if (c + i < nb) p.out[(size_t(b0 + c + i) * p.heads + h) * kVDim + j] = __float2bfloat16_rn(vh[i] + vl[i]);
+        if (c + i < nb) p.out[(size_t(b0 + c + i) * p.heads_w + h) * kVDim + j] = __float2bfloat16_rn(vh[i] + vl[i]);
     }
   }
   tc_fence_before();
@@ -317,14 +328,15 @@ cudaError_t launch_merge_uv(const CombineUVParams& p, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 128) attr[dev] = true;
   }
-  const int grid = p.heads * ((p.batch + NB - 1) / NB);
+  const int grid = p.heads_w * ((p.batch * p.q_len + NB - 1) / NB);
   return launch_pdl(merge_uv_kernel<NB>, dim3(grid), dim3(kUVThreads), C::kSmem, stream, 1, mw, p);
 }
 
 cudaError_t launch_combine_uv(const CombineUVParams& p, cudaStream_t stream) {
-  // the largest tile that still gives every SM a CTA; 8 sequences when none does
-  if (p.heads * ((p.batch + 31) / 32) >= p.sm_count) return launch_merge_uv<32>(p, stream);
-  if (p.heads * ((p.batch + 15) / 16) >= p.sm_count) return launch_merge_uv<16>(p, stream);
+  // the largest tile that still gives every SM a CTA; 8 columns when none does
+  const int cols = p.batch * p.q_len;
+  if (p.heads_w * ((cols + 31) / 32) >= p.sm_count) return launch_merge_uv<32>(p, stream);
+  if (p.heads_w * ((cols + 15) / 16) >= p.sm_count) return launch_merge_uv<16>(p, stream);
   return launch_merge_uv<8>(p, stream);
 }
 

@@ -344,6 +344,7 @@ int decode_rows(const mla_dims* d, const void* q_nope, const void* q_pe, const v
   cp.batch = batch;
   cp.heads = H;
   cp.heads_w = d->num_heads;
+  cp.q_len = q_len;
   if (launch_combine_uv(cp, s) != cudaSuccess) return MLA_ERR_CUDA;
   return MLA_OK;
 }

@@ -81,6 +81,7 @@ struct CombineUVParams {
   float* lse_out;             // [B, heads] or null
   int* status;
   int batch, heads, heads_w;
+  int q_len;                  // rows per sequence = q_len * heads_w; column c = b * q_len + t
   int sm_count;               // sizes the grid
 };
 
