@@ -97,11 +97,12 @@ __device__ __forceinline__ float round_out(float v, uint16_t* dst) {  // store a
 //   B = q_nope[c0:c0+NB, h, :]^T K-major  (q_nope rows are 128 content dims)
 // both staged by the CTA's threads into 128-byte-swizzled shared memory, eight
 // K = 16 MMAs into an fp32 TMEM accumulator, then one thread per latent dim
-// rounds its column of sequences to bf16 (fp16 for INT8 caches) and stores it.
-// Part c of q_sum[b][h] is the sum of the rounded values of latent dims
+// rounds its columns to bf16 (fp16 for 1-byte caches) and stores them.
+// Part c of q_sum[column][h] is the sum of the rounded values of latent dims
 // [64c, 64c + 64) (part 0 also the RoPE part): INT8 caches need the sum of
-// exactly the query the tensor cores see (bf16 caches do not use it).  INT8 caches take q_full in fp16
-// (their tensor-core path runs on fp16 operands); bf16 caches in bf16.
+// exactly the query the tensor cores see (bf16 and FP8 caches do not use
+// it).  1-byte caches take q_full in fp16 (their tensor-core path runs on
+// fp16 operands); bf16 caches in bf16.
 constexpr int kAbsThreads = 128;
 constexpr int kAbsMTile = 128;                               // latent dims per CTA
 constexpr uint32_t kAbsBlockBytes = kNope * 64 * 2;          // [128 k x 64 m] bf16, one swizzle column block
@@ -237,7 +238,7 @@ __global__ void __launch_bounds__(kAbsThreads) absorb_kernel(AbsorbParams p) {
         const int r = c + i;
         v[i] = r < nb ? round_out<kF16>(v[i], qf + (size_t(b0 + r) * p.heads_w + h) * kRow + m) : 0.f;
       }
-      if (kF16) {  // INT8 caches: this warp's 32 dims summed per sequence; lanes 2i, 2i + 1 get sequence c + i
+      if (kF16) {  // 1-byte caches: this warp's 32 dims summed per column; lanes 2i, 2i + 1 get column c + i
         const float sum = dc::warp_transpose_reduce<16, false>(v, lane);
         if (!(lane & 1)) red[(c + (lane >> 1)) * 4 + warp] = sum;
       }

@@ -31,7 +31,7 @@
 // Warp roles (288 threads; 256 for 32-head bf16 groups; 352 for 1-byte caches):
 //   warp 0     TMA producer: Q of each segment; bf16: QK ring 0 (16 heads:
 //              boxes 0, 2, 4, 6, 8 of each tile; 32 heads: all 9 boxes);
-//              INT8: the pair and RoPE slots (codes)
+//              1-byte caches: the pair and RoPE slots (codes)
 //   warp 1     TMEM allocation; lane 0 issues the QK^T MMAs
 //   warp 2     PV: lane 0 issues the MMAs (a second issuer keeps the tensor
 //              pipe busier than one with these small N = 16/32 MMAs); bf16:
@@ -115,9 +115,9 @@ struct Cfg {
 
 struct Barriers {
   uint64_t full_qk[2][8], empty_qk[2][8];            // bf16 QK rings
-  uint64_t full_pair[5], empty_pair[5];              // bf16 PV ring; INT8 shared ring
-  uint64_t full_rope[2], empty_rope[2];              // INT8
-  uint64_t full_i8_pair[5], full_i8_rope[2];         // INT8: TMA landed, codes not yet expanded
+  uint64_t full_pair[5], empty_pair[5];              // bf16 PV ring; 1-byte shared ring
+  uint64_t full_rope[2], empty_rope[2];              // 1-byte caches
+  uint64_t full_i8_pair[5], full_i8_rope[2];         // 1-byte caches: TMA landed, codes not yet expanded
   uint64_t q_full, q_empty, s_full[2], p_full[2], pv_done[2], o_full, o_free, drain[2];
   uint32_t tmem_base;
   int abort;
@@ -215,7 +215,7 @@ __global__ void __launch_bounds__(Cfg<HC, kCode != kCodeBf16>::kThreads, 1)
   float* red = reinterpret_cast<float*>(smem + C::kOffMisc + 1024);  // [2][HC][4] maxima, [HC][4] sums x2
   const uint32_t sbase = smem_u32(smem);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  constexpr uint32_t kFullCount = 1;  // TMA (bf16) or the expansion warp's lane 0 (INT8) completes a slot
+  constexpr uint32_t kFullCount = 1;  // TMA (bf16) or expansion thread 0 (1-byte caches) completes a slot
 
   if (threadIdx.x == 0) {
     for (int r = 0; r < C::kQkRings; ++r)

@@ -173,7 +173,7 @@ using TileWalker = TileWalkerT<false>;
 
 struct DecodeParams {
   const __nv_bfloat16* q_full;   // [B, H, 576]
-  const float* q_sum;            // [B, H, kQSumParts] (INT8)
+  const float* q_sum;            // [B, H, kQSumParts] (INT8: the zero-point term)
   const void* cache;             // bf16 or int8 [num_pages, P, 576]
   const float* scale_zero;       // [num_pages, P, 2] (INT8) or [num_pages, P] (FP8)
   const int* block_table;        // [B, max_pages]
