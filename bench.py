@@ -531,7 +531,7 @@ def run_ours(args, rank, world):
         tpeak, tpeak_src = tensor_peak()
         tflops = flops / (kern_ms / 1e3) / 1e12
         roofline = {"bound": "tensor", "achieved": round(tflops, 2), "peak": tpeak, "unit": "TFLOP/s",
-                    "frac": round(tflops / tpeak, 4), "peak_source": tpeak_src, "traffic": None,
+                    "frac": round(tflops / tpeak, 4), "peak_source": tpeak_src, "traffic": traffic,
                     "kernel": attention_kernel(w.cache_format)[1], "algorithmic_flops_per_launch": flops,
                     "history_bytes_per_launch": cache_bytes}
     res = {
