@@ -224,6 +224,11 @@ int mla_decode_multi(const mla_dims* dims, const void* q_nope, const void* q_pe,
 /* Largest prefill chunk (new tokens per sequence) mla_prefill accepts. */
 #define MLA_MAX_PREFILL_CHUNK 2048
 
+/* Largest number of query rows (batch * tokens per sequence * H) of one
+ * decode or prefill call; larger calls return MLA_ERR_INVALID_ARG (and their
+ * workspace size is 0). */
+#define MLA_MAX_QUERY_ROWS (1 << 26)
+
 /* Bytes of workspace mla_prefill needs for (dims, batch, chunk, num_splits);
  * 0 if the arguments are invalid.  It holds the chunk's absorbed queries and
  * the partial latent outputs, batch * chunk * H * (1,152 + 2,048 per

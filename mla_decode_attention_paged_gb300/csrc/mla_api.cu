@@ -15,6 +15,9 @@ using namespace mla;
 namespace {
 
 constexpr int kVersion = 100;  // 0.1.0
+// Largest batch * q_len * H of one call (2^26 query rows: 77 GB of absorbed
+// queries alone), so that grid sizes and row indices stay within int32.
+constexpr long long kMaxQueryRows = MLA_MAX_QUERY_ROWS;
 
 std::atomic<cudaEvent_t> g_ev_start{nullptr}, g_ev_stop{nullptr};
 std::atomic<int> g_inject_wait_timeout{0};
@@ -173,6 +176,7 @@ size_t mla_decode_multi_workspace_size(const mla_dims* d, int32_t batch, int32_t
 size_t mla_prefill_workspace_size(const mla_dims* d, int32_t batch, int32_t chunk, int32_t num_splits) {
   if (mla_check_dims(d) != MLA_OK || batch <= 0 || num_splits < 0 || chunk < 1 || chunk > MLA_MAX_PREFILL_CHUNK)
     return 0;
+  if ((long long)batch * chunk * d->num_heads > kMaxQueryRows) return 0;
   const mla_dims dr = row_dims(d, chunk);
   const int s = effective_splits(&dr, num_splits);
   if (s <= 0) return 0;
@@ -256,6 +260,8 @@ int decode_rows(const mla_dims* d, const void* q_nope, const void* q_pe, const v
   const bool byte = code != kCodeBf16;
   if (batch <= 0 || num_pages <= 0 || max_pages_per_seq <= 0 || num_splits < 0) return MLA_ERR_INVALID_ARG;
   if (q_len < 1 || q_len > MLA_MAX_PREFILL_CHUNK) return MLA_ERR_INVALID_ARG;
+  // query rows of the call: keeps every grid (absorption, merge) and row index in range
+  if ((long long)batch * q_len * d->num_heads > kMaxQueryRows) return MLA_ERR_INVALID_ARG;
   if (!(softmax_scale > 0.f) || softmax_scale == INFINITY) return MLA_ERR_INVALID_ARG;
   if (!q_nope || !q_pe || !cache || !block_table || !seq_lens || !W_UK || !W_UV || !out) return MLA_ERR_INVALID_ARG;
   if (byte && !cache_scale_zero) return MLA_ERR_INVALID_ARG;

@@ -140,6 +140,9 @@ def test_prefill_workspace_and_validation(lib):
     assert lib.mla_prefill_workspace_size(ctypes.byref(d), 4, 0, 3) == 0
     assert lib.mla_prefill_workspace_size(ctypes.byref(d), 4, mla.MAX_PREFILL_CHUNK + 1, 3) == 0
     assert mla.MAX_PREFILL_CHUNK > mla.MAX_Q_LEN
+    # more than 2^26 query rows (batch * chunk * H) are refused
+    assert lib.mla_prefill_workspace_size(ctypes.byref(mla.dims(128, 64)), 2048, 2048, 3) == 0
+    assert lib.mla_prefill_workspace_size(ctypes.byref(mla.dims(128, 64)), 256, 2048, 3) > 0
     fake = ctypes.c_void_p(0x10000)  # never dereferenced: validation fails first
     big = ctypes.c_size_t(1 << 40)
     args = [ctypes.byref(d), fake, None, 4, fake, 8, fake, 2, 64, fake, fake, ctypes.c_double(1e4), fake, fake,
