@@ -6,6 +6,7 @@
 // latent space once per step, q_lat = W^UK_h^T q_nope (512 wide), and the
 // attention kernel then scores the 576-wide cached rows directly with
 // q_full = [q_lat | q_pe].
+#include <atomic>
 #include <cuda_fp16.h>
 
 #include "blackwell_ptx.cuh"
@@ -265,7 +266,7 @@ __global__ void __launch_bounds__(kAbsThreads) absorb_kernel(AbsorbParams p) {
 template <bool kF16, int NB>
 cudaError_t launch_absorb_nb(const AbsorbParams& p, cudaStream_t stream) {
   using C = AbsCfg<NB>;
-  static bool attr[128] = {};
+  static std::atomic<bool> attr[128];  // per device: attributes set (zero-initialised)
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 128 || !attr[dev]) {

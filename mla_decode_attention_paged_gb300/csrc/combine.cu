@@ -4,6 +4,7 @@
 // value up-projection that the absorbed form applies last ("The Weight
 // Absorption Trick"; "Seven Ways LLMs Handle Attention", section 5: the value
 // expansion is absorbed into the output side): out_h = W^UV_h o_lat_h.
+#include <atomic>
 #include "blackwell_ptx.cuh"
 #include "decode_common.cuh"
 #include "params.cuh"
@@ -319,7 +320,7 @@ cudaError_t launch_merge_uv(const CombineUVParams& p, cudaStream_t stream) {
   CUtensorMap mw;
   if (!dc::make_map_2d(&mw, p.W_UV, 2, kLatent, uint64_t(p.heads_w) * kVDim, 64, kVDim, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
-  static bool attr[128] = {};
+  static std::atomic<bool> attr[128];  // per device: attributes set (zero-initialised)
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 128 || !attr[dev]) {

@@ -114,15 +114,15 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
 inline EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  if (!fn) {
+  // resolved once; the initialisation of a function-local static is thread-safe
+  static const EncodeTiledFn fn = []() -> EncodeTiledFn {
     void* f = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
         q != cudaDriverEntryPointSuccess)
       return nullptr;
-    fn = reinterpret_cast<EncodeTiledFn>(f);
-  }
+    return reinterpret_cast<EncodeTiledFn>(f);
+  }();
   return fn;
 }
 

@@ -45,6 +45,7 @@
 // Every wait is bounded: on timeout the CTA records MLA_ERR_DEVICE_TIMEOUT,
 // drains, frees its tensor memory and returns (the other CTAs of its cluster
 // then time out on the exchange and do the same).
+#include <atomic>
 #include "blackwell_ptx.cuh"
 #include "decode_common.cuh"
 #include "params.cuh"
@@ -598,7 +599,7 @@ cudaError_t launch_pair(const DecodeParams& p, int clusters_per_group, cudaStrea
       !make_map_2d(&mq, p.q_full, 2, kRow, qrows, 64, HC, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !make_map_2d(&mqr, p.q_full, 2, kRow, qrows, C::kRopeCols, HC, kRopeSw))
     return cudaErrorInvalidValue;
-  static bool attr[128] = {};
+  static std::atomic<bool> attr[128];  // per device: attributes set (zero-initialised)
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 128 || !attr[dev]) {
@@ -615,7 +616,7 @@ cudaError_t launch_pair(const DecodeParams& p, int clusters_per_group, cudaStrea
 
 template <int HC, int NC>
 int max_clusters() {  // clusters of NC that can be resident at once on this device
-  static int cached[128] = {};
+  static std::atomic<int> cached[128];  // per device (zero-initialised)
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 128 && cached[dev] > 0) return cached[dev];

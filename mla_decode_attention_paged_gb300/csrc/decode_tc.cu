@@ -60,6 +60,7 @@
 //     o_lat[h]  = sum_t w_t e4m3(code_t) / l,  w_t = p_t s_t
 // Every wait is bounded: on timeout the CTA records MLA_ERR_DEVICE_TIMEOUT,
 // drains, frees its tensor memory and returns.
+#include <atomic>
 #include <cuda_fp16.h>
 
 #include "blackwell_ptx.cuh"
@@ -804,7 +805,7 @@ cudaError_t launch_tc(const DecodeParams& p, int grid, cudaStream_t stream) {
   // q_full holds bf16 (or, for 1-byte caches, fp16) values; TMA moves 2-byte elements either way
   if (!make_map_2d(&mq, p.q_full, 2, kRow, uint64_t(p.batch) * p.heads, 64, HC, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
-  static bool attr[128] = {};
+  static std::atomic<bool> attr[128];  // per device: attributes set (zero-initialised)
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 128 || !attr[dev]) {

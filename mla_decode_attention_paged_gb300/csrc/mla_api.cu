@@ -33,7 +33,7 @@ int cache_code(const mla_dims* d) {
 size_t scale_bytes_per_row(int code) { return code == kCodeInt8 ? 8 : code == kCodeE4m3 ? 4 : 0; }
 
 int sm_count() {
-  static int cached[128] = {};
+  static std::atomic<int> cached[128];  // per device (zero-initialised)
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return -1;
   if (dev >= 0 && dev < 128 && cached[dev] > 0) return cached[dev];
