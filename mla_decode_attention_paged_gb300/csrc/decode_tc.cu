@@ -534,13 +534,19 @@ __global__ void __launch_bounds__(Cfg<HC, kCode != kCodeBf16>::kThreads, 1)
         for (int j = 0; j < kRowsPer; ++j)
           v[j] = *reinterpret_cast<const uint4*>(src + (r0 + kRowStep * j) * 64 + ch * 16);
       };
-      auto write_block = [&](const uint4 (&v)[kRowsPer], uint8_t* dst) {
+      // rows at and past the tile's valid length are written as zeros: PV reads
+      // them (with zero weight) up to the next multiple of 16, and a code there
+      // is whatever the cache page holds past the sequence -- for FP8 possibly
+      // a NaN pattern, and 0 * NaN would reach the output
+      auto write_block = [&](const uint4 (&v)[kRowsPer], uint8_t* dst, int valid) {
 #pragma unroll
         for (int j = 0; j < kRowsPer; ++j) {
           const int r = r0 + kRowStep * j;
-          uint4 lo, hi;
-          if constexpr (kZp) expand_codes(v[j], lo, hi);
-          else expand_e4m3(v[j], lo, hi);
+          uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
+          if (r < valid) {
+            if constexpr (kZp) expand_codes(v[j], lo, hi);
+            else expand_e4m3(v[j], lo, hi);
+          }
           uint8_t* row = dst + r * 128;
           *reinterpret_cast<uint4*>(row + (((2 * ch) ^ (r & 7)) << 4)) = lo;
           *reinterpret_cast<uint4*>(row + (((2 * ch + 1) ^ (r & 7)) << 4)) = hi;
@@ -557,7 +563,7 @@ __global__ void __launch_bounds__(Cfg<HC, kCode != kCodeBf16>::kThreads, 1)
           uint4 v[kRowsPer];
           if (!rope) {
             read_block(base + kBoxBytes, v);
-            write_block(v, base);
+            write_block(v, base, t.valid);
           }
           read_block(base + (rope ? 8192 : kBoxBytes + 8192), v);
           // all codes of the overlapping block read before any write; a timeout
@@ -566,7 +572,7 @@ __global__ void __launch_bounds__(Cfg<HC, kCode != kCodeBf16>::kThreads, 1)
             ok = false;
             break;
           }
-          write_block(v, base + (rope ? 0 : kBoxBytes));
+          write_block(v, base + (rope ? 0 : kBoxBytes), t.valid);
           fence_proxy_async_smem();
           converters_sync();
           if (ct == 0) mbar_arrive(rope ? &B->full_rope[slot] : &B->full_pair[slot]);

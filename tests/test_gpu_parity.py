@@ -115,6 +115,26 @@ def test_fp8_accepts_float8_tensor(cuda_lib):
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
 
 
+@pytest.mark.parametrize("fmt", ["bf16", "int8", "fp8"])
+def test_nan_patterns_past_the_sequence_end_do_not_reach_the_output(cuda_lib, fmt):
+    """The rows of a sequence's last page past its length are never part of
+    the attention; filled with NaN bit patterns (bf16 0x7FC0, E4M3 0x7F /
+    0xFF; any INT8 byte is a number) they must not reach the output."""
+    w, inp = _small(lens=(200, 1030, 77), int8=fmt == "int8", fp8=fmt == "fp8", seed=12)
+    P = w.page_size
+    table = inp["block_table"]
+    for b, L in enumerate(inp["seq_lens"].tolist()):
+        if L % P:
+            page = int(table[b, (L - 1) // P])
+            if fmt == "bf16":
+                inp["cache"].view(torch.int16)[page, L % P:] = 0x7FC0
+            else:
+                inp["cache_i8"].view(torch.uint8)[page, L % P:, 0::2] = 0x7F
+                inp["cache_i8"].view(torch.uint8)[page, L % P:, 1::2] = 0xFF
+    (_, _), out, lse = _run_small(w, inp)
+    assert torch.isfinite(out.float()).all() and torch.isfinite(lse).all()
+
+
 def test_shuffled_table_bit_identical_and_deterministic(cuda_lib):
     """Same rows reached through a different physical layout give bit-identical
     results for the same split plan; repeated runs are bit-identical."""
