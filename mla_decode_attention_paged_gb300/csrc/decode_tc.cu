@@ -539,17 +539,30 @@ __global__ void __launch_bounds__(Cfg<HC, kCode != kCodeBf16>::kThreads, 1)
       // is whatever the cache page holds past the sequence -- for FP8 possibly
       // a NaN pattern, and 0 * NaN would reach the output
       auto write_block = [&](const uint4 (&v)[kRowsPer], uint8_t* dst, int valid) {
+        if (valid >= kTile) {  // a full tile (all but a sequence's last): every row is a cached token
 #pragma unroll
-        for (int j = 0; j < kRowsPer; ++j) {
-          const int r = r0 + kRowStep * j;
-          uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
-          if (r < valid) {
+          for (int j = 0; j < kRowsPer; ++j) {
+            const int r = r0 + kRowStep * j;
+            uint4 lo, hi;
             if constexpr (kZp) expand_codes(v[j], lo, hi);
             else expand_e4m3(v[j], lo, hi);
+            uint8_t* row = dst + r * 128;
+            *reinterpret_cast<uint4*>(row + (((2 * ch) ^ (r & 7)) << 4)) = lo;
+            *reinterpret_cast<uint4*>(row + (((2 * ch + 1) ^ (r & 7)) << 4)) = hi;
           }
-          uint8_t* row = dst + r * 128;
-          *reinterpret_cast<uint4*>(row + (((2 * ch) ^ (r & 7)) << 4)) = lo;
-          *reinterpret_cast<uint4*>(row + (((2 * ch + 1) ^ (r & 7)) << 4)) = hi;
+        } else {
+#pragma unroll
+          for (int j = 0; j < kRowsPer; ++j) {
+            const int r = r0 + kRowStep * j;
+            uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
+            if (r < valid) {
+              if constexpr (kZp) expand_codes(v[j], lo, hi);
+              else expand_e4m3(v[j], lo, hi);
+            }
+            uint8_t* row = dst + r * 128;
+            *reinterpret_cast<uint4*>(row + (((2 * ch) ^ (r & 7)) << 4)) = lo;
+            *reinterpret_cast<uint4*>(row + (((2 * ch + 1) ^ (r & 7)) << 4)) = hi;
+          }
         }
       };
       while (ok && walk.next(t)) {
