@@ -103,3 +103,34 @@ def test_full_size_sparse_topk(cuda_lib):
                                    inp["seq_lens"].cpu().numpy(), inp["token_indices"].cpu().numpy(),
                                    f64(inp["W_UK"]), f64(inp["W_UV"]), inp["scale"], w.page_size, False, pairs=pairs)
     assert_parity(out, lse, ref_o, ref_l, pairs, w.name)
+
+
+def test_full_size_prefill_chunk(cuda_lib):
+    """Chunked prefill at the bench's size (4 sequences, a 512-token chunk
+    after 8,192 cached tokens, 16 heads), in bench.py's configuration: the
+    chunk's first, middle and last tokens of two sampled sequences, every
+    head, against the un-absorbed oracle, which appends the chunk to its own
+    copy of the history first."""
+    import oracle as O
+    from harness import f64
+    w = W.WORKLOADS["v2lite_prefill512"]
+    inp = W.make_decode_inputs(w, device="cuda")
+    d = dims_of(w)
+    T, H = w.chunk, w.heads
+    splits = mla.auto_num_splits(mla.dims(H * T, w.page_size), w.batch)
+    seqs = [0, 3]
+    cache, sz, table = oracle_cache(inp, w, seqs)      # the history as drawn, before the GPU writes the chunk
+    gpu_cache = inp["cache"].cuda()
+    out, lse = mla.prefill(d, gpu_cache, None, inp["block_table"], inp["seq_lens"], inp["chunk_c_kv"],
+                           inp["chunk_k_pe"], inp["q_nope"], inp["q_pe"], inp["W_UK"], inp["W_UV"], inp["scale"],
+                           rope_theta=w.rope_theta, num_splits=splits)
+    torch.cuda.synchronize()
+    triples = [(b, t, h) for b in seqs for t in (0, T // 2, T - 1) for h in range(H)]
+    ref_o, ref_l = O.prefill_chunk(cache, sz, table, inp["seq_lens"].cpu().numpy(),
+                                   W.bf16_to_bits(inp["chunk_c_kv"]), W.bf16_to_bits(inp["chunk_k_pe"]),
+                                   w.rope_theta, f64(inp["q_nope"]), f64(inp["q_pe"]), f64(inp["W_UK"]),
+                                   f64(inp["W_UV"]), inp["scale"], w.page_size, False, triples=triples)
+    B = w.batch
+    pairs = [(b, t * H + h) for b, t, h in triples]
+    assert_parity(out.reshape(B, T * H, -1), lse.reshape(B, T * H), ref_o.reshape(B, T * H, -1),
+                  ref_l.reshape(B, T * H), pairs, w.name)
