@@ -1,0 +1,36 @@
+"""bench.py's host-side arithmetic, on CPU: the roofline units it reports."""
+import os
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+import bench  # noqa: E402
+import oracle as O  # noqa: E402
+
+
+def test_bytes_per_token_match_the_cache_layout():
+    # one layer: 576 values, plus the per-token quantisation parameters
+    assert bench.BYTES_PER_TOKEN["bf16"] == O.latent_cache_bytes_per_token(1)
+    assert bench.BYTES_PER_TOKEN["int8"] == O.latent_cache_bytes_per_token(1, elem_bytes=1, side_bytes_per_row=8)
+    assert bench.BYTES_PER_TOKEN["fp8"] == O.latent_cache_bytes_per_token(1, elem_bytes=1, side_bytes_per_row=4)
+
+
+def test_prefill_flops_closed_forms():
+    per_key = 2 * 576 + 2 * 512
+    # a whole prompt as one chunk: token t sees t + 1 keys, sum = T (T + 1) / 2
+    assert bench.prefill_flops([10], 10, 3) == pytest.approx(3 * per_key * 55)
+    # a chunk after a history of h: token t sees h + t + 1 keys
+    h, T = 100, 8
+    assert bench.prefill_flops([h + T], T, 1) == pytest.approx(per_key * (T * h + T * (T + 1) // 2))
+    # a sequence shorter than the chunk: tokens at negative positions see nothing
+    assert bench.prefill_flops([3], 5, 1) == pytest.approx(per_key * (1 + 2 + 3))
+    # sequences add up
+    assert bench.prefill_flops([10, 108], 8, 2) == pytest.approx(
+        bench.prefill_flops([10], 8, 2) + bench.prefill_flops([108], 8, 2))
+
+
+def test_whole_job_rate_units():
+    # 32 tokens in 0.25 ms on one rank
+    assert bench.whole_job_rate(32, 1, 0.25) == pytest.approx(128000.0)
