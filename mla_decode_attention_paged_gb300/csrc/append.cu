@@ -33,8 +33,10 @@ __global__ void __launch_bounds__(256) append_kernel(AppendParams p) {
   const int i = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (i >= p.n_tokens) return;
   const int b = p.chunk > 0 ? i / p.chunk : p.seq_ids[i];
-  const int pos = p.chunk > 0 ? p.seq_lens[b] - p.chunk + i % p.chunk : p.positions[i];
-  bool ok = b >= 0 && b < p.num_seqs && pos >= 0 && pos / p.page_size < p.max_pages;
+  // 64-bit: a length near the int32 limits must not wrap into a valid position
+  const long long pos64 = p.chunk > 0 ? (long long)p.seq_lens[b] - p.chunk + i % p.chunk : p.positions[i];
+  bool ok = b >= 0 && b < p.num_seqs && pos64 >= 0 && pos64 / p.page_size < p.max_pages;
+  const int pos = int(pos64);  // in [0, max_pages * P) once ok
   int page = -1;
   if (ok) {
     page = p.block_table[size_t(b) * p.max_pages + pos / p.page_size];
