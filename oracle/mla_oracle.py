@@ -29,7 +29,10 @@ Pins (see tests/test_oracle.py): absorbed == un-absorbed, closed forms (one
 token, equal rows, zero query), a library special case (torch SDPA in fp64 on
 explicitly expanded K/V), softmax normalisation, split/combine invariance,
 page-permutation invariance, RoPE invariants, INT8 error bound and worked
-examples, and the pages' own cache-size figures (tests/golden/).
+examples, the FP8 E4M3 format's closed forms, brute-force nearest encoding
+and worked ties, multi-token decode against causal SDPA, sparse decode
+against masked SDPA, chunked prefill against causal SDPA and chunk-split
+invariance, and the pages' own cache-size figures (tests/golden/).
 
 Readings where the pages are silent:
   * the 576-wide row is [latent 0..511 | RoPE key 512..575];
@@ -42,6 +45,8 @@ Readings where the pages are silent:
     widened to include 0, fp32 arithmetic in a fixed order (see
     ``quantize_tokens_int8``).  The exact recipe is a reading: parity of the
     recipe is pinned only by the error bound and worked examples.
+  * a prefill chunk is the last `chunk` tokens of each sequence, appended
+    before its queries attend (the multi-token reading with chunk for q_len);
   * FP8: the E4M3 format (1 sign, 4 exponent bits with bias 7, 3 mantissa
     bits, subnormals, no infinities, S.1111.111 = NaN, largest finite 448),
     one fp32 scale per token from the row's largest magnitude, codes by
