@@ -309,13 +309,17 @@ def cpu_baseline(w, inp, seconds, gpu_out=None, gpu_lse=None):
         tab = np.full_like(table, -1)
         tab[b, :n] = np.arange(n)
         if w.quantised and "src_c_kv" in inp:   # the oracle's own append builds this sequence's pages
-            a = int(lens[:b].sum())
-            cache = np.zeros((n, w.page_size, 576), np.int8 if w.int8 else np.uint8)
-            sz = np.zeros((n, w.page_size, 2) if w.int8 else (n, w.page_size), np.float32)
-            O.append_tokens(cache, sz, tab, [b] * int(lens[b]), list(range(int(lens[b]))),
-                            W.bf16_to_bits(inp["src_c_kv"][a:a + int(lens[b])]),
-                            W.bf16_to_bits(inp["src_k_pe"][a:a + int(lens[b])]), w.rope_theta, w.page_size,
-                            w.int8, fp8=w.fp8)
+            built = inp.setdefault("oracle_pages", {})   # once per sequence (input set-up, not timed)
+            if b not in built:
+                a = int(lens[:b].sum())
+                cache = np.zeros((n, w.page_size, 576), np.int8 if w.int8 else np.uint8)
+                sz = np.zeros((n, w.page_size, 2) if w.int8 else (n, w.page_size), np.float32)
+                O.append_tokens(cache, sz, tab, [b] * int(lens[b]), list(range(int(lens[b]))),
+                                W.bf16_to_bits(inp["src_c_kv"][a:a + int(lens[b])]),
+                                W.bf16_to_bits(inp["src_k_pe"][a:a + int(lens[b])]), w.rope_theta, w.page_size,
+                                w.int8, fp8=w.fp8)
+                built[b] = (cache, sz)
+            cache, sz = built[b]
         else:
             idx = torch.as_tensor(table[b, :n].astype(np.int64), device=inp["cache_dev"].device)
             sub = inp["cache_dev"].index_select(0, idx)
