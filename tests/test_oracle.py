@@ -642,3 +642,58 @@ def test_prefill_skips_tokens_without_a_page():
                     triples=[])
     np.testing.assert_array_equal(cache[0, :4, :512], c_bits[0, 2:])   # positions 0..3 = tokens 2..5
     assert not cache[0, 4:].any()
+
+
+def test_fp8_and_prefill_pins_catch_planted_mistakes(monkeypatch):
+    """Plausible mistakes planted in the oracle (on the CPU): each must fail
+    the pin that guards it."""
+    g = _fp8_golden()
+    real_encode = O.e4m3_encode
+
+    def truncating_encode(x):            # rounds toward zero instead of to nearest even
+        v = np.asarray(x, dtype=np.float64)
+        table = O.e4m3_value(np.arange(0x7F))
+        a = np.minimum(np.abs(v), O.E4M3_MAX)
+        code = np.clip(np.searchsorted(table, a, side="right") - 1, 0, 0x7E)
+        return np.where(np.signbit(v), code | 0x80, code).astype(np.uint8)
+
+    def ties_away(x):                    # ties away from zero instead of to even
+        v = np.asarray(x, dtype=np.float64)
+        c = real_encode(x).astype(np.int64)
+        table = O.e4m3_value(np.arange(0x7F))
+        a = np.minimum(np.abs(v), O.E4M3_MAX)
+        mag = c & 0x7F
+        up = np.minimum(mag + 1, 0x7E)
+        tie = (np.abs(table[up] - a) == np.abs(a - table[mag])) & (up != mag)
+        return np.where(tie & (table[up] > table[mag]), (c & 0x80) | up, c).astype(np.uint8)
+
+    for bad in (truncating_encode, ties_away):
+        wrong = [case for case in g["encode"]
+                 if int(bad(np.array([case["value"]], np.float32))[0]) != case["code"]]
+        assert wrong, bad.__name__
+
+    # an exponent bias of 8 instead of 7 in the decoder halves every value
+    def bias8(codes):
+        return O.e4m3_value(codes) / 2
+    wrong = [case for case in g["decode"] if case["value"] != "nan"
+             and bias8(np.array([case["code"]], np.uint8))[0] != case["value"]]
+    assert wrong
+
+    # prefill: a query that also sees the next token (an off-by-one in the causal limit)
+    B, T, H, P = 1, 9, 1, 16
+    table, W_UK, W_UV, c_bits, k_bits, qn, qp = _prefill_inputs(B, T, H, P, 1, 6)
+    cache = np.zeros((1, P, 576), np.uint16)
+    good, _ = O.prefill_chunk(cache.copy(), None, table, [T], c_bits, k_bits, 0.0, qn, qp, W_UK, W_UV, 0.3, P,
+                              False)
+    real_multi = O.decode_multi_token
+
+    def one_too_many(qn_, qp_, cache_, sz_, tab_, lens_, wk_, wv_, sc_, P_, int8_, triples=None, absorbed=False,
+                     fp8=False):
+        return real_multi(qn_, qp_, cache_, sz_, tab_, [int(l) + 1 for l in lens_], wk_, wv_, sc_, P_, int8_,
+                          triples=triples, absorbed=absorbed, fp8=fp8)
+
+    import oracle.mla_oracle as OM          # prefill_chunk looks the name up in its own module
+    monkeypatch.setattr(OM, "decode_multi_token", one_too_many)
+    cache2 = np.zeros((1, P, 576), np.uint16)
+    bad, _ = O.prefill_chunk(cache2, None, table, [T], c_bits, k_bits, 0.0, qn, qp, W_UK, W_UV, 0.3, P, False)
+    assert not np.allclose(bad, good, rtol=1e-6)
