@@ -116,3 +116,8 @@ def test_q_len_out_of_range_is_refused(cuda_lib):
 
 def test_multi_token_fp8(cuda_lib):
     _check(_mt(T=3, lens=(200, 1030, 2), fp8=True, seed=72))
+
+
+@pytest.mark.parametrize("P,T", [(128, 2), (16, 5)])
+def test_multi_token_fp8_page_sizes(cuda_lib, P, T):
+    _check(_mt(T=T, P=P, lens=(700, 129, 3), fp8=True, seed=73 + P))

@@ -137,3 +137,12 @@ def test_prefill_then_decode_reads_what_prefill_wrote(cuda_lib):
     ref_o, ref_l = O.decode(f64(qn), f64(qp), ref_cache, None, x["table"].numpy(), x["seq_lens"].numpy(),
                             f64(x["W_UK"]), f64(x["W_UV"]), x["scale"], x["P"], False)
     assert_parity(out, lse, ref_o, ref_l, [(b, h) for b in range(B) for h in range(H)], "decode after prefill")
+
+
+@pytest.mark.parametrize("fmt,P,heads,theta", [("fp8", 16, 128, 10000.0), ("int8", 128, 16, 10000.0),
+                                               ("bf16", 32, 32, 10000.0)])
+def test_prefill_formats_pages_heads(cuda_lib, fmt, P, heads, theta):
+    """Quantised caches with RoPE on (the two appends may differ by a bf16
+    ulp in the rotated key, so only the attention is compared), page sizes
+    16 / 32 / 128, 16 to 128 heads."""
+    _check(_pf(heads=heads, P=P, hist=(200, 513), chunk=24, fmt=fmt, theta=theta, seed=48 + P), sample=12)

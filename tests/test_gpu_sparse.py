@@ -116,3 +116,8 @@ def test_sparse_empty_selection_and_bad_entry(cuda_lib):
 @pytest.mark.parametrize("heads", [16, 128])
 def test_sparse_fp8(cuda_lib, heads):
     _check(_sp(heads=heads, lens=(700, 3000), top_k=300, fp8=True, seed=heads + 7))
+
+
+@pytest.mark.parametrize("P", [16, 128])
+def test_sparse_fp8_page_sizes(cuda_lib, P):
+    _check(_sp(P=P, lens=(900, 2000), top_k=257, fp8=True, seed=91 + P))
