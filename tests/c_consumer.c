@@ -62,6 +62,14 @@ static int host_checks(void) {
   /* rejected on the host before anything runs: null queries */
   CHECK(mla_decode(&d, NULL, NULL, NULL, NULL, 1, NULL, 1, NULL, 1, NULL, NULL, 0.1f, 4, NULL, 0, NULL, NULL,
                    NULL) == MLA_ERR_INVALID_ARG);
+  /* FP8 caches and prefill chunks through the same header */
+  mla_dims d8 = d;
+  d8.cache_dtype = MLA_CACHE_FP8;
+  CHECK(mla_check_dims(&d8) == MLA_OK);
+  CHECK(mla_prefill_workspace_size(&d, 4, 512, 3) > mla_decode_workspace_size(&d, 4, 3));
+  CHECK(mla_prefill_workspace_size(&d, 4, MLA_MAX_PREFILL_CHUNK + 1, 3) == 0);
+  CHECK(mla_prefill(&d8, NULL, NULL, 1, NULL, 1, NULL, 1, 8, NULL, NULL, 1e4, NULL, NULL, NULL, NULL, 0.1f, 3,
+                    NULL, 0, NULL, NULL, NULL) == MLA_ERR_INVALID_ARG);
   return 0;
 }
 
