@@ -30,9 +30,12 @@ token, equal rows, zero query), a library special case (torch SDPA in fp64 on
 explicitly expanded K/V), softmax normalisation, split/combine invariance,
 page-permutation invariance, RoPE invariants, INT8 error bound and worked
 examples, the FP8 E4M3 format's closed forms, brute-force nearest encoding
-and worked ties, multi-token decode against causal SDPA, sparse decode
-against masked SDPA, chunked prefill against causal SDPA and chunk-split
-invariance, and the pages' own cache-size figures (tests/golden/).
+and worked ties, the 1-byte caches' append -> read-back round trip within
+each format's rounding bound (with planted layout mistakes it must catch),
+multi-token decode against causal SDPA, sparse decode against masked SDPA
+(out-of-range entries skipped), chunked prefill against causal SDPA and
+chunk-split invariance, and the pages' own cache-size figures
+(tests/golden/).
 
 Readings where the pages are silent:
   * the 576-wide row is [latent 0..511 | RoPE key 512..575];
@@ -549,7 +552,10 @@ def decode_sparse(q_nope: np.ndarray, q_pe: np.ndarray, cache: np.ndarray, scale
 
     token_indices [B, k] int: positions in sequence b's cache; -1 entries are
     padding and are skipped.  The attention of (b, h) runs over the rows at
-    the listed positions, in list order, each listed entry once.
+    the listed positions, in list order, each listed entry once.  The page
+    does not say what a position outside the sequence means; the reading
+    taken is that such an entry (below -1, or at or past seq_lens[b]) selects
+    nothing and is skipped like padding.
     Returns (out [B, H, 128], lse [B, H]) in fp64; ``pairs`` as for decode.
     """
     B, H = q_nope.shape[0], q_nope.shape[1]
@@ -562,8 +568,9 @@ def decode_sparse(q_nope: np.ndarray, q_pe: np.ndarray, cache: np.ndarray, scale
         by_seq.setdefault(int(b), []).append(int(h))
     fn = attend_absorbed if absorbed else attend_unabsorbed
     for b, heads in by_seq.items():
-        rows = gather_rows(cache, scale_zero, block_table, b, int(seq_lens[b]), page_size, int8, fp8=fp8)
-        chosen = [int(i) for i in np.asarray(token_indices[b]).ravel() if int(i) >= 0]
+        L = int(seq_lens[b])
+        rows = gather_rows(cache, scale_zero, block_table, b, L, page_size, int8, fp8=fp8)
+        chosen = [int(i) for i in np.asarray(token_indices[b]).ravel() if 0 <= int(i) < L]
         sel = rows[chosen] if chosen else rows[:0]
         for h in heads:
             o, l, _ = fn(q_nope[b, h], q_pe[b, h], sel, W_UK[h], W_UV[h], scale)

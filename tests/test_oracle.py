@@ -243,6 +243,79 @@ def test_append_then_gather_roundtrip_and_injective_slots():
     np.testing.assert_array_equal(rows[:, 512:], want)
 
 
+def _quantised_roundtrip_errors(fmt, gather):
+    """Append seeded rows to a 1-byte cache through a shuffled page table with
+    the oracle's own append, read them back with ``gather`` and return, per
+    element, (|read back - source|, the quantiser's bound for that element).
+
+    The bounds come from the formats alone, not from the oracle's dequantiser:
+    INT8 rounds x / s to the nearest integer, so the read-back is within s / 2
+    of x ("KV Cache Optimization", section 3: min/max quantisation); E4M3
+    keeps 3 mantissa bits, so x / s lands within half a step of a code, i.e.
+    within |x / s| * 2^-4 in the normal range and 2^-10 among the subnormals,
+    and the read-back within s times that."""
+    rng = np.random.default_rng(2024 if fmt == "int8" else 2025)
+    P, B, maxp = 16, 3, 6
+    table = rng.permutation(B * maxp).astype(np.int32).reshape(B, maxp)
+    lens = [5, 41, 96]
+    seq_ids = [b for b in range(B) for _ in range(lens[b])]
+    pos = [t for b in range(B) for t in range(lens[b])]
+    # rows of very different magnitudes, so that the per-token scales differ
+    src = _bf16(rng.normal(0, 1, (len(pos), 576)) * rng.uniform(0.01, 50, (len(pos), 1)) +
+                rng.uniform(-3, 3, (len(pos), 1)))
+    int8 = fmt == "int8"
+    cache = np.zeros((B * maxp, P, 576), np.int8 if int8 else np.uint8)
+    sz = np.zeros((B * maxp, P, 2) if int8 else (B * maxp, P), np.float32)
+    O.append_tokens(cache, sz, table, seq_ids, pos, O.f64_to_bf16_bits(src[:, :512]),
+                    O.f64_to_bf16_bits(src[:, 512:]), 0.0, P, int8=int8, fp8=not int8)
+    errs, bounds = [], []
+    off = 0
+    for b in range(B):
+        got = gather(cache, sz, table, b, lens[b], P, int8=int8, fp8=not int8)
+        x = src[off:off + lens[b]]
+        if int8:  # the token's range widened to include 0, as the recipe defines it
+            lo = np.minimum(x.min(axis=1), 0.0)
+            hi = np.maximum(x.max(axis=1), 0.0)
+            s = np.where(hi > lo, (hi - lo) / 255.0, 1.0)[:, None]
+            bound = np.broadcast_to(s * (0.5 + 1e-5), x.shape)
+        else:     # the token's largest magnitude maps to 448
+            s = (np.abs(x).max(axis=1) / 448.0)[:, None]
+            bound = np.maximum(np.abs(x) * 2.0 ** -4, s * 2.0 ** -10) * (1 + 1e-5)
+        errs.append(np.abs(got - x))
+        bounds.append(bound)
+        off += lens[b]
+    return np.concatenate(errs), np.concatenate(bounds)
+
+
+@pytest.mark.parametrize("fmt", ["int8", "fp8"])
+def test_quantised_gather_reads_back_within_the_quantiser_bound(fmt):
+    """The 1-byte read-back branch of gather_rows: every element of every
+    appended row comes back within the format's rounding bound of the source
+    value, through a shuffled page table."""
+    err, bound = _quantised_roundtrip_errors(fmt, O.gather_rows)
+    assert np.all(err <= bound)
+    assert np.mean(err) > 0  # the rows really went through the quantiser
+
+
+@pytest.mark.parametrize("fmt", ["int8", "fp8"])
+def test_quantised_gather_pin_catches_planted_mistakes(fmt):
+    """Layout mistakes planted in the read-back must fail the bound: (scale,
+    zero point) read in swapped order, and each token given its page
+    neighbour's parameters."""
+    good = O.gather_rows
+
+    def swapped_scale_zero(cache, sz, *a, **k):
+        return good(cache, sz[..., ::-1].copy(), *a, **k)
+
+    def neighbour_params(cache, sz, *a, **k):
+        return good(cache, np.roll(sz, 1, axis=1), *a, **k)
+
+    planted = [neighbour_params] + ([swapped_scale_zero] if fmt == "int8" else [])
+    for bad in planted:
+        err, bound = _quantised_roundtrip_errors(fmt, bad)
+        assert not np.all(err <= bound), bad.__name__
+
+
 # ------------------------------------------------------------- attention ---- #
 
 @pytest.mark.parametrize("L", [1, 2, 7, 64, 300])
@@ -539,6 +612,24 @@ def test_sparse_library_masked_sdpa_and_order_invariance():
     o3, l3 = O.decode_sparse(qn[:, 0], qp[:, 0], cache, None, table, [L], np.full((1, 4), -1), W_UK, W_UV, 0.2, P,
                              False)
     assert np.all(o3 == 0) and np.all(np.isneginf(l3))
+
+
+def test_sparse_out_of_range_entries_select_nothing():
+    """An entry at or past the sequence's length, or below -1, is skipped like
+    padding: the result equals that of the list without it, and a list made
+    only of such entries gives o = 0, lse = -inf."""
+    H, L, P = 2, 37, 8
+    cache, table, W_UK, W_UV, qn, qp = _mt_inputs(1, 1, H, P, [L], 104)
+    # the last page has slots 37..39 past the sequence's end, so a read past L would find data there
+    idx = np.array([[3, 37, 17, -7, 36, 39, 1000, 0]])
+    kept = np.array([[3, -1, 17, -1, 36, -1, -1, 0]])
+    out, lse = O.decode_sparse(qn[:, 0], qp[:, 0], cache, None, table, [L], idx, W_UK, W_UV, 0.2, P, False)
+    ref, lref = O.decode_sparse(qn[:, 0], qp[:, 0], cache, None, table, [L], kept, W_UK, W_UV, 0.2, P, False)
+    np.testing.assert_array_equal(out, ref)
+    np.testing.assert_array_equal(lse, lref)
+    o2, l2 = O.decode_sparse(qn[:, 0], qp[:, 0], cache, None, table, [L], np.array([[L, L + 5, -2]]), W_UK, W_UV,
+                             0.2, P, False)
+    assert np.all(o2 == 0) and np.all(np.isneginf(l2))
 
 
 def test_sparse_pins_catch_planted_off_by_one(monkeypatch):
