@@ -20,7 +20,10 @@ void* workspace_address(int dev) {
   if (p) return p;
   // In host code the array's name is only a host-side stand-in; the device
   // address must be asked for, with the device current.
-  if (cudaGetSymbolAddress(&p, g_no_alloc_workspace) != cudaSuccess || !p) return nullptr;
+  if (cudaGetSymbolAddress(&p, g_no_alloc_workspace) != cudaSuccess || !p) {
+    cudaGetLastError();  // leave no sticky runtime error behind for the caller's next check
+    return nullptr;
+  }
   g_workspace_addr[dev].store(p, std::memory_order_release);
   return p;
 }
@@ -32,9 +35,12 @@ extern "C" int mla_decode_no_alloc(const mla_dims* d, const void* q_nope, const 
                                    const void* W_UK, const void* W_UV, float softmax_scale, int32_t num_splits,
                                    void* out, float* lse_out, int32_t* device_status, mla_stream_t stream) {
   const size_t need = mla_decode_workspace_size(d, batch, num_splits);
-  if (need == 0) {
+  if (need == 0) {  // the status mla_decode gives for the same arguments
     const int st = mla_check_dims(d);
-    return st != MLA_OK ? st : MLA_ERR_INVALID_ARG;
+    if (st != MLA_OK) return st;
+    if (batch <= 0 || num_splits < 0 || (long long)batch * d->num_heads > MLA_MAX_QUERY_ROWS)
+      return MLA_ERR_INVALID_ARG;
+    return MLA_ERR_CUDA;  // valid arguments: the split count could not be resolved on this device
   }
   if (need > MLA_NO_ALLOC_WORKSPACE_BYTES) return MLA_ERR_WORKSPACE;  // larger than the fixed scratch
   if (device_status && (reinterpret_cast<uintptr_t>(device_status) & 3)) return MLA_ERR_INVALID_ARG;

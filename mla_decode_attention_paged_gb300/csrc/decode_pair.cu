@@ -1,6 +1,5 @@
 // decode_pair.cu -- split-KV MLA decode attention for bf16 caches on CTA
-// clusters (thread-block clusters of two or four), tcgen05 tensor cores fed
-// by TMA.
+// pairs (thread-block clusters of two), tcgen05 tensor cores fed by TMA.
 //
 // What it computes ("The Weight Absorption Trick"; "Seven Ways LLMs Handle
 // Attention", section 5; "Flash-Decoding and FlashInfer"): for one head group
@@ -11,26 +10,26 @@
 //     o_lat[h] = sum_t softmax(s[., h])_t * c_t[0:512]
 // and emits o_lat (normalised within the range) with the range's lse.
 //
-// Why clusters.  Both products read the same cached tile (the latent part is
+// Why pairs.  Both products read the same cached tile (the latent part is
 // K of QK^T and V of PV), so a tile must stay in shared memory from its QK^T
 // until its PV, across the softmax in between.  A 128-token tile is 147 KB;
 // one SM holds about 1.3 of them, which serialises load -> QK^T -> softmax ->
-// PV.  Here the NC CTAs of a cluster (NC SMs) split every tile by columns:
-// CTA r holds latent columns [512 r / NC, 512 (r + 1) / NC) and RoPE columns
-// [512 + 64 r / NC, 512 + 64 (r + 1) / NC): 147 / NC KB per tile, so each SM
-// keeps several tiles in flight (2 with pairs, 4 with clusters of four).
+// PV.  Here the two CTAs of a cluster (two SMs) split every tile by columns:
+// CTA r holds latent columns [256 r, 256 r + 256) and RoPE columns
+// [512 + 32 r, 512 + 32 r + 32): 72 KB per tile, so each SM keeps two tiles
+// in flight.
 //   * QK^T: each CTA forms the partial scores over its columns, S_r^T
-//     [128 tok x HC] = C_r [128 x 576 / NC] * Q_r^T, and sends them to the
-//     other CTAs through distributed shared memory (8 KB each for 16 heads);
-//   * every CTA adds the NC partials in rank order (so all get the same
-//     bits), runs the same softmax and holds the same P^T;
-//   * PV: each CTA accumulates its own 512 / NC latent columns of O^T.
+//     [128 tok x HC] = C_r [128 x 288] * Q_r^T, and sends them to the other
+//     CTA through distributed shared memory (8 KB for 16 heads);
+//   * both CTAs add the two partials in rank order (so both get the same
+//     bits), run the same softmax and hold the same P^T;
+//   * PV: each CTA accumulates its own 256 latent columns of O^T.
 // Every page is read from HBM once for all heads of the group.
 //
 // Orientation as in the single-CTA kernel: the 128 tokens of a tile are the
 // MMA's M extent and the heads its N extent:
-//     S_r^T [128 x HC]        = C_r [128 x 576 / NC] * Q_r^T       (A K-major)
-//     O_r^T [512 / NC x HC]  += C_r^T [512 / NC x 128] * P^T       (A MN-major)
+//     S_r^T [128 x HC]   = C_r [128 x 288] * Q_r^T           (A K-major)
+//     O_r^T [256 x HC]  += C_r^T [256 x 128] * P^T           (A MN-major)
 //
 // Warp roles (256 threads per CTA):
 //   warp 0     TMA producer: Q of each segment and the first half of each
@@ -43,8 +42,8 @@
 //   warps 4-7  exchange of partial scores, softmax (one thread per token
 //              row), epilogue
 // Every wait is bounded: on timeout the CTA records MLA_ERR_DEVICE_TIMEOUT,
-// drains, frees its tensor memory and returns (the other CTAs of its cluster
-// then time out on the exchange and do the same).
+// drains, frees its tensor memory and returns (the other CTA of its pair
+// then times out on the exchange and does the same).
 #include <atomic>
 #include "blackwell_ptx.cuh"
 #include "decode_common.cuh"
@@ -62,27 +61,22 @@ constexpr uint32_t kPairBytes = 2 * kBoxBytes;  // 128 latent columns: one O^T c
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 constexpr float kRescaleThreshold = 8.f;          // log2 units
 constexpr bool kPrefetchNext = true;              // L2 prefetch of the next tile's boxes
-constexpr int kPairClusterHC16 = 2;               // CTAs per cluster for 16-head groups
 constexpr int kMaxSlots = 6;                      // barrier array size of each ring
+constexpr int NC = 2;                             // CTAs per cluster
 
-// HC heads per cluster, NC CTAs per cluster (2 or 4) splitting each tile's
-// columns: CTA r holds latent columns [r 512/NC, (r + 1) 512/NC) -- kChunks
-// chunks of 128 -- and RoPE columns [512 + r 64/NC, 512 + (r + 1) 64/NC).
-template <int HC, int NC>
+// HC heads per pair; CTA r of the pair holds latent columns [256 r, 256 r +
+// 256) -- kChunks chunks of 128 -- and RoPE columns [512 + 32 r, + 32).
+template <int HC>
 struct PairCfg {
-  static_assert(NC == 2 || NC == 4, "clusters of two or four CTAs");
   static constexpr int kChunks = 4 / NC;            // 128-column latent chunks per CTA and tile
-  static constexpr int kRopeCols = 64 / NC;         // RoPE columns per CTA (32: 64-byte rows, 16: 32-byte rows)
+  static constexpr int kRopeCols = 64 / NC;         // RoPE columns per CTA (64-byte rows)
   static constexpr uint32_t kRopeBytes = kTile * kRopeCols * 2;
   static constexpr uint32_t kRopeSbo = 8 * kRopeCols * 2;  // 8-row swizzle atom
-  static constexpr uint32_t kRopeSwizzle = NC == 2 ? kSwizzle64B : kSwizzle32B;
-  static constexpr int kNumPair = 4;                // chunk slots: 4 / kChunks tiles (with two chunks per
-                                                    // tile an even count keeps both producers in step)
-  static constexpr int kNumRope = NC == 2 ? 3 : 4;  // RoPE slots (one per tile)
-  // the two producers split a tile's latent boxes: one chunk each, or with
-  // a single chunk one 64-column box each (both then arm the slot's barrier)
-  static constexpr int kBoxesPerProducer = kChunks == 2 ? 2 : 1;
-  static constexpr int kPairArrivals = kChunks == 2 ? 1 : 2;
+  static constexpr uint32_t kRopeSwizzle = kSwizzle64B;
+  static constexpr int kNumPair = 4;                // chunk slots: two tiles (an even count keeps both
+                                                    // producers, one chunk each, in step)
+  static constexpr int kNumRope = 3;                // RoPE slots (one per tile)
+  static constexpr int kBoxesPerProducer = 2;       // the two producers load one chunk (two boxes) each
   static constexpr uint32_t kQBytes = kChunks * 2 * HC * 128 + HC * kRopeCols * 2;
   static constexpr uint32_t kPBytes = kTile * HC * 2;  // P^T, bf16
   static constexpr uint32_t kXBytes = kTile * HC * 4;  // one other CTA's partial S^T, fp32
@@ -91,8 +85,8 @@ struct PairCfg {
   static constexpr uint32_t kOffQ = kOffRope + ((kNumRope * kRopeBytes + 1023) & ~1023u);
   static constexpr uint32_t kOffQRope = kOffQ + kChunks * 2 * HC * 128;
   static constexpr uint32_t kOffP = kOffQ + ((kQBytes + 1023) & ~1023u);
-  static constexpr uint32_t kOffX = kOffP + 2 * kPBytes;  // [NC - 1 senders][2 buffers]
-  static constexpr uint32_t kOffMisc = kOffX + (NC - 1) * 2 * kXBytes;
+  static constexpr uint32_t kOffX = kOffP + 2 * kPBytes;  // [2 buffers] of the peer's partials
+  static constexpr uint32_t kOffMisc = kOffX + 2 * kXBytes;
   static constexpr uint32_t kMiscBytes = 2048;
   static constexpr uint32_t kSmem = kOffMisc + kMiscBytes + 1024;  // +1024: base alignment slack
   static constexpr uint32_t kColS = 0;                             // + buf * HC
@@ -127,12 +121,12 @@ __device__ __forceinline__ void fail(PairBarriers* B, int* status) {
 // kCausal: multi-token decode (q_len > 1) masks the scores of each row's
 // later positions on a sequence's last tiles; single-token decode does not
 // carry the per-tile check.
-template <int HC, int NC, bool kCausal>
+template <int HC, bool kCausal>
 __global__ void __launch_bounds__(kPairThreads, 1)
     decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_latent, const __grid_constant__ CUtensorMap tmap_rope,
                        const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_qrope,
                        DecodeParams p) {
-  using C = PairCfg<HC, NC>;
+  using C = PairCfg<HC>;
   extern __shared__ uint8_t smem_raw[];
   // the same offset in every CTA: the others' exchange buffers and barriers are found by mapa
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -144,7 +138,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::kNumPair; ++i) {
-      mbar_init(&B->full_pair[i], C::kPairArrivals);
+      mbar_init(&B->full_pair[i], 1);
       mbar_init(&B->empty_pair[i], 1);
     }
     for (int i = 0; i < C::kNumRope; ++i) {
@@ -243,9 +237,8 @@ __global__ void __launch_bounds__(kPairThreads, 1)
         }
       }
       {
-        // boxes [kBoxesPerProducer * role, + kBoxesPerProducer) of this CTA's
-        // 64-column boxes; box j is box j % 2 of chunk j / 2
-        const int c = C::kChunks == 2 ? role : 0, b0 = C::kChunks == 2 ? 0 : role;
+        // producer `role` loads chunk `role` of this CTA's two (its two 64-column boxes)
+        const int c = role, b0 = 0;
         const uint32_t it = pair_it + c;
         const uint32_t slot = it % C::kNumPair;
         if (!(ok = mbar_wait(&B->empty_pair[slot], ((it / C::kNumPair) & 1) ^ 1, abort_flag, kWaitLimitNs))) break;
@@ -407,42 +400,26 @@ __global__ void __launch_bounds__(kPairThreads, 1)
 #pragma unroll
           for (int i = 0; i < 16; ++i) x[h0 + i] = v[i];
         }
-        // partial scores to every other CTA of the cluster: receiver rr keeps
-        // sender s's in its buffer slot (s - rr - 1) mod NC
-#pragma unroll
-        for (int j = 0; j < NC - 1; ++j) {
-          const uint32_t rr = (rank + 1 + j) % NC;
-          const uint32_t rbar = mapa_shared(smem_u32(&B->x_full[buf]), rr);
-          const uint32_t xr = mapa_shared(x_local + (buf * (NC - 1) + (NC - 2 - j)) * C::kXBytes, rr);
+        // partial scores to the peer CTA, into its buffer `buf`
+        {
+          const uint32_t peer = rank ^ 1u;
+          const uint32_t rbar = mapa_shared(smem_u32(&B->x_full[buf]), peer);
+          const uint32_t xr = mapa_shared(x_local + buf * C::kXBytes, peer);
 #pragma unroll
           for (int v = 0; v < kV4; ++v)
             st_async_v4(xr + (v ^ (st % kV4)) * 16, x[4 * v], x[4 * v + 1], x[4 * v + 2], x[4 * v + 3], rbar);
         }
-        if (st == 0) mbar_arrive_expect_tx(&B->x_full[buf], (NC - 1) * C::kXBytes);
+        if (st == 0) mbar_arrive_expect_tx(&B->x_full[buf], C::kXBytes);
         ok = mbar_wait_cluster(&B->x_full[buf], (tile_i >> 1) & 1, abort_flag, kWaitLimitNs);
         if (ok) {
-          // S = ((S_0 + S_1) + S_2) + ... in rank order, so that every CTA
-          // of the cluster gets the same bits
+          // S = S_0 + S_1 in rank order, so that both CTAs get the same bits
 #pragma unroll
           for (int v = 0; v < kV4; ++v) {
-            float4 tot = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-            for (int s = 0; s < NC; ++s) {
-              float4 y;
-              if (s == int(rank)) {
-                y = make_float4(x[4 * v], x[4 * v + 1], x[4 * v + 2], x[4 * v + 3]);
-              } else {
-                const int slot = (s - int(rank) - 1 + NC) % NC;
-                y = *reinterpret_cast<const float4*>(smem + C::kOffX + (buf * (NC - 1) + slot) * C::kXBytes +
-                                                     st * HC * 4 + (v ^ (st % kV4)) * 16);
-              }
-              if (s == 0) {
-                tot = y;
-              } else {
-                tot.x += y.x; tot.y += y.y; tot.z += y.z; tot.w += y.w;
-              }
-            }
-            x[4 * v] = tot.x; x[4 * v + 1] = tot.y; x[4 * v + 2] = tot.z; x[4 * v + 3] = tot.w;
+            const float4 y = *reinterpret_cast<const float4*>(smem + C::kOffX + buf * C::kXBytes + st * HC * 4 +
+                                                              (v ^ (st % kV4)) * 16);
+            const float4 own = make_float4(x[4 * v], x[4 * v + 1], x[4 * v + 2], x[4 * v + 3]);
+            const float4 s0 = rank == 0 ? own : y, s1 = rank == 0 ? y : own;
+            x[4 * v] = s0.x + s1.x; x[4 * v + 1] = s0.y + s1.y; x[4 * v + 2] = s0.z + s1.z; x[4 * v + 3] = s0.w + s1.w;
           }
         }
       }
@@ -588,45 +565,44 @@ __global__ void __launch_bounds__(kPairThreads, 1)
   cluster_sync();  // other CTAs may still be sending into this CTA's shared memory until here
 }
 
-template <int HC, int NC>
+template <int HC>
 cudaError_t launch_pair(const DecodeParams& p, int clusters_per_group, cudaStream_t stream) {
-  using C = PairCfg<HC, NC>;
-  constexpr CUtensorMapSwizzle kRopeSw = NC == 2 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B;
+  using C = PairCfg<HC>;
   CUtensorMap ml, mr, mq, mqr;
   const uint64_t rows = uint64_t(p.num_pages) * p.page_size, qrows = uint64_t(p.batch) * p.heads;
   if (!make_map_2d(&ml, p.cache, 2, kRow, rows, 64, p.page_size, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_map_2d(&mr, p.cache, 2, kRow, rows, C::kRopeCols, p.page_size, kRopeSw) ||
+      !make_map_2d(&mr, p.cache, 2, kRow, rows, C::kRopeCols, p.page_size, CU_TENSOR_MAP_SWIZZLE_64B) ||
       !make_map_2d(&mq, p.q_full, 2, kRow, qrows, 64, HC, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_map_2d(&mqr, p.q_full, 2, kRow, qrows, C::kRopeCols, HC, kRopeSw))
+      !make_map_2d(&mqr, p.q_full, 2, kRow, qrows, C::kRopeCols, HC, CU_TENSOR_MAP_SWIZZLE_64B))
     return cudaErrorInvalidValue;
   static std::atomic<bool> attr[128];  // per device: attributes set (zero-initialised)
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 128 || !attr[dev]) {
-    for (auto* k : {decode_pair_kernel<HC, NC, false>, decode_pair_kernel<HC, NC, true>}) {
+    for (auto* k : {decode_pair_kernel<HC, false>, decode_pair_kernel<HC, true>}) {
       const cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, int(C::kSmem));
       if (e != cudaSuccess) return e;
     }
     if (dev >= 0 && dev < 128) attr[dev] = true;
   }
-  auto* kernel = p.q_len > 1 ? decode_pair_kernel<HC, NC, true> : decode_pair_kernel<HC, NC, false>;
+  auto* kernel = p.q_len > 1 ? decode_pair_kernel<HC, true> : decode_pair_kernel<HC, false>;
   return launch_pdl(kernel, dim3(NC * clusters_per_group * p.num_groups), dim3(kPairThreads), C::kSmem, stream, NC,
                     ml, mr, mq, mqr, p);
 }
 
-template <int HC, int NC>
-int max_clusters() {  // clusters of NC that can be resident at once on this device
+template <int HC>
+int max_clusters() {  // CTA pairs that can be resident at once on this device
   static std::atomic<int> cached[128];  // per device (zero-initialised)
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 128 && cached[dev] > 0) return cached[dev];
-  if (cudaFuncSetAttribute(decode_pair_kernel<HC, NC, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           int(PairCfg<HC, NC>::kSmem)) != cudaSuccess)
+  if (cudaFuncSetAttribute(decode_pair_kernel<HC, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           int(PairCfg<HC>::kSmem)) != cudaSuccess)
     return 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(NC);
   cfg.blockDim = dim3(kPairThreads);
-  cfg.dynamicSmemBytes = PairCfg<HC, NC>::kSmem;
+  cfg.dynamicSmemBytes = PairCfg<HC>::kSmem;
   cudaLaunchAttribute at[1];
   at[0].id = cudaLaunchAttributeClusterDimension;
   at[0].val.clusterDim.x = NC;
@@ -635,23 +611,17 @@ int max_clusters() {  // clusters of NC that can be resident at once on this dev
   cfg.attrs = at;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, decode_pair_kernel<HC, NC, false>, &cfg) != cudaSuccess || n <= 0) return 0;
+  if (cudaOccupancyMaxActiveClusters(&n, decode_pair_kernel<HC, false>, &cfg) != cudaSuccess || n <= 0) return 0;
   if (dev >= 0 && dev < 128) cached[dev] = n;
   return n;
 }
 
 }  // namespace
 
-int decode_pair_cluster_size(int hc) { return hc == 16 ? kPairClusterHC16 : 2; }
-
-int decode_pair_capacity(int hc) {
-  if (hc == 16) return max_clusters<16, kPairClusterHC16>();
-  return max_clusters<32, 2>();
-}
+int decode_pair_capacity(int hc) { return hc == 16 ? max_clusters<16>() : max_clusters<32>(); }
 
 cudaError_t launch_decode_pair(const DecodeParams& p, int hc, int clusters_per_group, cudaStream_t stream) {
-  return hc == 16 ? launch_pair<16, kPairClusterHC16>(p, clusters_per_group, stream)
-                  : launch_pair<32, 2>(p, clusters_per_group, stream);
+  return hc == 16 ? launch_pair<16>(p, clusters_per_group, stream) : launch_pair<32>(p, clusters_per_group, stream);
 }
 
 }  // namespace mla

@@ -111,6 +111,25 @@ def test_host_validation_rejects_before_launch(lib):
     assert lib.mla_set_timing_events(None, None) == mla.MLA_OK
 
 
+def test_no_alloc_host_validation(lib):
+    """mla_decode_no_alloc returns what mla_decode returns for bad arguments,
+    and refuses shapes larger than its fixed scratch before touching a GPU."""
+    d = mla.dims(16, 64)
+    fake = ctypes.c_void_p(0x10000)
+
+    def call(dims, batch, splits):
+        return lib.mla_decode_no_alloc(ctypes.byref(dims), fake, fake, fake, None, 4, fake, 8, fake, batch, fake,
+                                       fake, ctypes.c_float(0.1), splits, fake, None, None, None)
+
+    assert call(d, 0, 4) == mla.MLA_ERR_INVALID_ARG
+    assert call(d, 4, -1) == mla.MLA_ERR_INVALID_ARG
+    assert call(mla.dims(24, 64), 4, 4) == mla.MLA_ERR_UNSUPPORTED
+    assert call(mla.dims(0, 64), 4, 4) == mla.MLA_ERR_INVALID_ARG
+    assert call(mla.dims(16, 64), 1 << 23, 4) == mla.MLA_ERR_INVALID_ARG  # beyond the query-row limit
+    assert lib.mla_decode_workspace_size(ctypes.byref(d), 4096, 152) > mla.NO_ALLOC_WORKSPACE_BYTES
+    assert call(d, 4096, 152) == mla.MLA_ERR_WORKSPACE
+
+
 def test_multi_token_workspace_and_validation(lib):
     d = mla.dims(16, 64)
     # q_len tokens of H heads need the workspace of a q_len * H-head decode
