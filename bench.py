@@ -113,6 +113,19 @@ def attention_kernel(fmt: str):
 BYTES_PER_TOKEN = {"bf16": 1152, "int8": 584, "fp8": 580}
 
 
+def workload_config(w, cache_bytes: int, world: int) -> dict:
+    """The `config` of a bench line: what the workload is, the same for both arms."""
+    T = w.chunk or w.q_len
+    return {"workload": w.name, "batch": w.batch, "heads": w.heads, "context": w.context, "page_size": w.page_size,
+            "q_len": T, "top_k": w.top_k or None, "chunk": w.chunk or None, "cache_bytes": cache_bytes,
+            "l2": ("inputs larger than L2 (no flush): each step reads one of "
+                   f"{IDX_SETS} top-k selections, {IDX_SETS * cache_bytes / 1e6:.0f} MB of rows together"
+                   if w.top_k else
+                   "inputs larger than L2 (no flush): the cache read each step exceeds the 126 MB L2"
+                   if cache_bytes > 200e6 else "cache smaller than L2"),
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
+
+
 def kernel_traffic(workload_name: str, tokens: int, fmt: str):
     """DRAM bytes per attention launch from the committed ncu summary, scaled
     to this launch's tokens; None if absent or taken on a different kernel."""
@@ -200,12 +213,13 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def cpu_baseline_prefill(w, inp, seconds, gpu_out=None, gpu_lse=None):
+def cpu_baseline_prefill(w, inp, seconds, gpu_out=None, gpu_lse=None, absorbed=False):
     """The oracle's chunked prefill on the host cores: per sampled sequence it
     appends the chunk to that sequence's pages itself and attends three of
     the chunk's tokens (first, middle, last) with every head, un-absorbed in
-    fp64, until about `seconds` have passed.  Returns (baseline, parity) as
-    cpu_baseline does, parity over the (token, head) rows computed."""
+    fp64 (or in the oracle's absorbed form), until about `seconds` have
+    passed.  Returns (baseline, parity) as cpu_baseline does, parity over the
+    (token, head) rows computed."""
     import numpy as np
     import oracle as O
     import torch
@@ -235,7 +249,7 @@ def cpu_baseline_prefill(w, inp, seconds, gpu_out=None, gpu_lse=None):
         triples = [(b, t, h) for t in toks for h in range(H)]
         t_start = time.perf_counter()
         ref_o, ref_l = O.prefill_chunk(cache, None, tab, lens, c_bits, k_bits, w.rope_theta, qn, qp, wk, wv,
-                                       inp["scale"], w.page_size, False, triples=triples)
+                                       inp["scale"], w.page_size, False, triples=triples, absorbed=absorbed)
         el += time.perf_counter() - t_start
         if gpu_out is not None and done < w.batch:
             for _, t, h in triples:
@@ -247,9 +261,11 @@ def cpu_baseline_prefill(w, inp, seconds, gpu_out=None, gpu_lse=None):
                 worst["lse"] = max(worst["lse"], abs(float(gpu_lse[b, t, h]) - float(ref_l[b, t, h])))
                 worst["rows"] += 1
         done += 1
-    base = {"value": done * len(toks) / el, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+    form = "absorbed" if absorbed else "un-absorbed"
+    base = {"value": done * len(toks) / el, "unit": "tokens/s", "cores": cores,
+            "kind": "oracle (absorbed form)" if absorbed else "oracle",
             "sample": f"{done} sequence(s) of {w.name}: the oracle appends the {T}-token chunk and attends "
-                      f"tokens {toks} with all {H} heads (un-absorbed fp64 oracle), {el:.1f} s"}
+                      f"tokens {toks} with all {H} heads ({form} fp64 oracle), {el:.1f} s"}
     parity = None
     if gpu_out is not None:
         ok = worst["abs"] <= 2e-2 and worst["rel"] <= 1e-2 and worst["lse"] <= 2e-2
@@ -260,14 +276,15 @@ def cpu_baseline_prefill(w, inp, seconds, gpu_out=None, gpu_lse=None):
     return base, parity
 
 
-def cpu_baseline(w, inp, seconds, gpu_out=None, gpu_lse=None):
+def cpu_baseline(w, inp, seconds, gpu_out=None, gpu_lse=None, absorbed=False):
     """The fp64 oracle as it stands, on the host cores, over whole sequences
-    (all heads) of this workload until about `seconds` have passed.  Returns
-    (baseline dict, parity dict or None): given the GPU's out / lse of the
-    same step, the oracle's results for the sequences it ran are compared
+    (all heads) of this workload until about `seconds` have passed: its
+    un-absorbed definition, or (absorbed=True) its absorbed cross-check form.
+    Returns (baseline dict, parity dict or None): given the GPU's out / lse of
+    the same step, the oracle's results for the sequences it ran are compared
     with them (max abs error, max per-row relative error, max lse error)."""
     if w.chunk:
-        return cpu_baseline_prefill(w, inp, seconds, gpu_out, gpu_lse)
+        return cpu_baseline_prefill(w, inp, seconds, gpu_out, gpu_lse, absorbed)
     import numpy as np
     import oracle as O
     from mla_decode_attention_paged_gb300 import workloads as W
@@ -331,23 +348,25 @@ def cpu_baseline(w, inp, seconds, gpu_out=None, gpu_lse=None):
         if w.top_k:
             idx = inp["token_indices"].cpu().numpy()
             ref = O.decode_sparse(qn, qp, cache, sz, tab, lens, idx, wk, wv, inp["scale"], w.page_size, w.int8,
-                                  pairs=[(b, h) for h in range(w.heads)], fp8=w.fp8)
+                                  pairs=[(b, h) for h in range(w.heads)], absorbed=absorbed, fp8=w.fp8)
         elif w.q_len == 1:
             ref = O.decode(qn, qp, cache, sz, tab, lens, wk, wv, inp["scale"], w.page_size, w.int8,
-                           pairs=[(b, h) for h in range(w.heads)], fp8=w.fp8)
+                           pairs=[(b, h) for h in range(w.heads)], absorbed=absorbed, fp8=w.fp8)
         else:
             ref = O.decode_multi_token(qn, qp, cache, sz, tab, lens, wk, wv, inp["scale"], w.page_size, w.int8,
                                        triples=[(b, t, h) for t in range(w.q_len) for h in range(w.heads)],
-                                       fp8=w.fp8)
+                                       absorbed=absorbed, fp8=w.fp8)
         el += time.perf_counter() - t_start
         if gpu_out is not None and done < w.batch:
             compare(b, *ref)
         done += 1
         tokens_attended += int((inp["token_indices"][b] >= 0).sum()) if w.top_k else int(lens[b])
-    base = {"value": done * w.q_len / el, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+    form = "absorbed" if absorbed else "un-absorbed"
+    base = {"value": done * w.q_len / el, "unit": "tokens/s", "cores": cores,
+            "kind": "oracle (absorbed form)" if absorbed else "oracle",
             "sample": f"{done} whole sequence(s) x {w.q_len} token(s) x {w.heads} heads of {w.name} "
                       f"({tokens_attended} cached tokens, "
-                      f"un-absorbed fp64 oracle), {el:.1f} s"}
+                      f"{form} fp64 oracle), {el:.1f} s"}
     parity = None
     if gpu_out is not None:
         ok = worst["abs"] <= 2e-2 and worst["rel"] <= 1e-2 and worst["lse"] <= 2e-2 and worst["bad"] == 0
@@ -585,15 +604,8 @@ def run_ours(args, rank, world):
         "scaling": "weak", "vs_baseline": None,
         "dtype": {"bf16": "bf16", "int8": "int8", "fp8": "fp8_e4m3"}[w.cache_format],
         "data": "synthetic (seeded; random-init weights of DeepSeek-V2 MLA shapes)",
-        "config": {"workload": w.name, "batch": B, "heads": H, "context": w.context, "page_size": w.page_size,
-                   "q_len": T, "top_k": w.top_k or None, "chunk": w.chunk or None, "num_splits": splits,
-                   "cache_bytes": cache_bytes,
-                   "l2": ("inputs larger than L2 (no flush): each step reads one of "
-                          f"{len(idx_sets)} top-k selections, {len(idx_sets) * cache_bytes / 1e6:.0f} MB of rows together"
-                          if w.top_k else
-                          "inputs larger than L2 (no flush): the cache read each step exceeds the 126 MB L2"
-                          if cache_bytes > 200e6 else "cache smaller than L2"),
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "config": workload_config(w, cache_bytes, world),
+        "num_splits": splits,
         "cache_gbs": round(step_cache_gbs, 1),
         "frac_of_8tbs": round(step_cache_gbs / NOMINAL_HBM_GBS, 4),
         "attention_kernel_ms": round(kern_ms, 5),
@@ -611,6 +623,8 @@ def run_ours(args, rank, world):
         torch.cuda.synchronize()
         res["cpu_baseline"], res["parity"] = cpu_baseline(w, inp, args.cpu_seconds, out.float().cpu().numpy(),
                                                           lse.cpu().numpy())
+        # the oracle's absorbed form: the same fp64 arithmetic after the weight absorption
+        res["cpu_baseline_absorbed"], _ = cpu_baseline(w, inp, max(2.0, args.cpu_seconds / 2), absorbed=True)
     return res
 
 
@@ -625,6 +639,12 @@ def run_reference(args, rank, world):
     dev = "cuda" if torch.cuda.is_available() else "cpu"
     inp = W.make_decode_inputs(w.scaled(batch=min(w.batch, 4)) if w.quantised else w, device=dev)
     inp["cache_dev"], inp["sz_dev"] = inp.get("cache"), None
+    # the bytes the attention of one full step reads, as the GPU arm counts them
+    if w.top_k:
+        attended = int((inp["token_indices"] >= 0).sum())
+    else:
+        attended = int(W.draw_seq_lens(w, W.generator(w.seed, dev)).to(torch.int64).sum())
+    cache_bytes = attended * BYTES_PER_TOKEN[w.cache_format]
     per_step = max(1.0, min(6.0, 150.0 / max(args.steps + args.warmup, 1)))
     for _ in range(args.warmup):
         cpu_baseline(w, inp, per_step * 0.2)
@@ -642,8 +662,7 @@ def run_reference(args, rank, world):
             "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(1e3 * el / args.steps, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
-            "config": {"workload": w.name, "batch": w.batch, "heads": w.heads, "context": w.context,
-                       "page_size": w.page_size, "q_len": w.q_len, "chunk": w.chunk or None}, "impl": "reference",
+            "config": workload_config(w, cache_bytes, world), "impl": "reference",
             "cpu_baseline": cb,
             "e2e": {"value": round(v, 5), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
