@@ -1,0 +1,725 @@
+// decode_hm.cu -- split-KV MLA decode attention for groups of 128 query rows
+// (128 heads; or q_len x heads rows of multi-token decode and prefill) on
+// CTA pairs, with the query rows as the tensor-core MMA's M extent.  Serves
+// bf16, INT8 and FP8 caches.
+//
+// What it computes ("The Weight Absorption Trick"; "Seven Ways LLMs Handle
+// Attention", section 5; "Flash-Decoding and FlashInfer"): for 128 rows h of
+// one sequence and one contiguous range of its tokens, with
+// q_full[h] = [W^UK_h^T q_nope_h | q_pe_h] (576 wide) and the cached rows
+// c_t = [latent | RoPE key] (576 wide),
+//     s[h][t] = scale * q_full[h] . c_t
+//     o_lat[h] = sum_t softmax(s[h, .])_t * c_t[0:512]
+// and emits o_lat (normalised within the range) with the range's lse.  All
+// 128 rows share every cached tile, so a tile is read once for all of them
+// (DeepSeek-V2's 128 heads share one 576-wide latent row: "Seven Ways LLMs
+// Handle Attention", section 5).
+//
+// Layout.  A 128-row group fills the MMA's M extent, so the rows are M and
+// the tokens N (the single-CTA and pair kernels, built for 16 / 32 heads,
+// put the tokens on M instead).  The two CTAs of a pair split every cached
+// row by columns, as in decode_pair.cu: CTA r holds latent columns
+// [256 r, 256 r + 256) and RoPE columns [512 + 32 r, + 32).  Tokens go in
+// sub-tiles of 64 (half a work-plan tile):
+//   QK: S_r [128 x 64] = Q_r [128 x 288] * C_r [64 x 288]^T, partial over the
+//       CTA's columns.  Q_r's latent part sits in tensor memory (A operand
+//       from TMEM, loaded once per segment), its RoPE part in shared memory;
+//       C_r is the sub-tile's boxes read K-major.
+//   exchange: each CTA sends its partial scores to the other through
+//       distributed shared memory (32 KB per sub-tile) and both add the two in
+//       rank order, so both hold the same scores and run the same softmax.
+//   softmax: one thread per row; the row's max, exponentials and sum are
+//       thread-local (no cross-thread reduction).  P is written back into
+//       tensor memory over the row's scores.
+//   PV: O_r [128 x 256] += P [128 x 64] * C_r [64 x 256] (A = P from TMEM,
+//       B = the same latent boxes read MN-major): each CTA accumulates its
+//       own 256 latent columns, in tensor memory for the whole segment.
+// Tensor memory (512 columns): Q latent 128, O_r 256, two score buffers of 64.
+//
+// 1-byte caches (INT8, FP8): the codes land by TMA in the back of each slot
+// and four warps expand them into fp16 operand boxes (exact, as in
+// decode_tc.cu); Q is fp16; the per-token scale (and INT8 zero point) is
+// applied to the scores and folded into P, with the zero-point term of the
+// output subtracted in the epilogue:
+//     s[h][t]  = scale * s_t * (q_h . code_t - zp_t * sum(q_h))
+//     o_lat[h] = (sum_t w_t code_t - sum_t w_t zp_t) / l,  w_t = p_t s_t.
+//
+// Warp roles (256 threads; 384 for 1-byte caches):
+//   warp 0       TMA producer: Q's RoPE part per segment; latent boxes 0-1 and
+//                the RoPE box of every sub-tile
+//   warp 1       TMEM allocation; lane 0 issues the QK MMAs
+//   warp 2       PV: lane 0 issues the MMAs; bf16: the warp first clears
+//                the rows past a sequence's end that the last MMA reads
+//   warp 3       TMA producer: latent boxes 2-3 (and 1-byte caches' scales)
+//   warps 4-7    Q latent into TMEM per segment, exchange, softmax, epilogue
+//   warps 8-11   1-byte caches: code expansion
+// Every wait is bounded: on timeout the CTA records MLA_ERR_DEVICE_TIMEOUT,
+// drains, frees its tensor memory and returns.
+#include <atomic>
+#include <cuda_fp16.h>
+
+#include "blackwell_ptx.cuh"
+#include "decode_common.cuh"
+#include "params.cuh"
+
+namespace mla {
+namespace {
+
+using namespace ptx;
+using namespace dc;
+
+constexpr int kRowsG = 128;                       // query rows per group (MMA M)
+constexpr int kSub = 64;                          // tokens per sub-tile (MMA N of QK, K of PV)
+constexpr int kNumSlots = 4;                      // sub-tile ring
+constexpr uint32_t kLatBox = kSub * 128;          // [64 tokens x 64 latent columns] 16-bit, SW128: 8 KB
+constexpr uint32_t kOffRopeBox = 4 * kLatBox;     // [64 tokens x 32 RoPE columns] 16-bit, SW64: 4 KB
+constexpr uint32_t kOffCodes = 18 * 1024;         // 1-byte: 4 latent code blocks [64 x 64 B], then RoPE codes
+constexpr uint32_t kOffCodeRope = kOffCodes + 4 * 4096;
+constexpr uint32_t kOffScales = 36 * 1024;        // 1-byte: per-token (scale, zero point) or scale
+constexpr uint32_t kXBytes = kRowsG * kSub * 4;   // one sub-tile's partial scores, fp32
+constexpr uint32_t kQRopeBytes = kRowsG * 32 * 2; // [128 rows x 32 RoPE columns] 16-bit, SW64
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+constexpr float kRescaleThreshold = 8.f;          // log2 units
+constexpr bool kPrefetchNext = true;              // L2 prefetch of the next sub-tile's boxes
+// tensor memory columns
+constexpr uint32_t kColQ = 0, kColO = 128, kColS = 384, kTmemCols = 512;
+
+template <bool kByte>
+struct HmCfg {
+  static constexpr int kThreads = kByte ? 384 : 256;
+  static constexpr uint32_t kSlotBytes = kByte ? 37 * 1024 : 36 * 1024;
+  static constexpr uint32_t kOffQRope = kNumSlots * kSlotBytes;
+  static constexpr uint32_t kOffX = kOffQRope + kQRopeBytes;  // [2] partial-score buffers from the peer
+  static constexpr uint32_t kOffMisc = kOffX + 2 * kXBytes;
+  static constexpr uint32_t kSmem = kOffMisc + 1024 + 1024;   // + barriers, + base alignment slack
+  static_assert(kSmem <= 232448, "dynamic shared memory of one CTA");
+  static_assert(kOffQRope % 1024 == 0 && kSlotBytes % 1024 == 0, "swizzle atoms");
+};
+
+struct HmBarriers {
+  uint64_t full[kNumSlots];    // sub-tile operands ready (bf16: TMA of both producers; 1-byte: expansion)
+  uint64_t landed[kNumSlots];  // 1-byte: codes and scales landed (TMA of both producers)
+  uint64_t empty[kNumSlots];   // PV of the sub-tile done: the slot may be refilled
+  uint64_t q_full, q_empty, s_full[2], x_full[2], p_full[2], pv_done[2], o_full, o_free, drain[2];
+  uint32_t tmem_base;
+  int abort;
+};
+
+__device__ __forceinline__ void fail(HmBarriers* B, int* status) {
+  B->abort = 1;
+  set_status(status, MLA_ERR_DEVICE_TIMEOUT);
+}
+
+// One 64-token half of a work-plan tile (the plan's unit is 128 tokens).
+struct SubTile {
+  int b, tok0, valid, seg;
+  bool first, last;  // first / last sub-tile of its segment
+};
+
+struct SubWalker {
+  TileWalkerT<true> w;
+  TileInfo t;
+  bool pending;  // the tile in t still has its second half to come
+  __device__ __forceinline__ void init(const DecodeParams& p, long long S, long long pa, long long pb) {
+    w.init(p.tile_start, p.seg_base, p.len, p.batch, int(S), pa, pb);
+    pending = false;
+  }
+  __device__ __forceinline__ bool next(SubTile& s) {
+    int half = 1;
+    if (pending) {
+      pending = false;
+    } else {
+      if (!w.next(t)) return false;
+      half = 0;
+      pending = t.valid > kSub;
+    }
+    s.b = t.b;
+    s.tok0 = t.tile * kTile + half * kSub;
+    s.valid = half ? t.valid - kSub : (t.valid < kSub ? t.valid : kSub);
+    s.seg = t.seg;
+    s.first = t.first && half == 0;
+    s.last = t.last && !pending;
+    return true;
+  }
+  __device__ __forceinline__ int len() const { return w.len_b; }  // length of the current sub-tile's sequence
+};
+
+// Cache rows of a sub-tile's boxes (box_rows = min(P, 64) tokens each),
+// block-table entries read one sub-tile ahead; checked at use.
+struct SubPages {
+  int raw[4], off[4], nb;
+  __device__ __forceinline__ void fetch(const DecodeParams& p, const SubTile& s, int box_rows) {
+    nb = (s.valid + box_rows - 1) / box_rows;
+    const int* bt = p.block_table + size_t(s.b) * p.max_pages;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int tk = s.tok0 + i * box_rows;
+      raw[i] = i < nb ? __ldg(bt + tk / p.page_size) : 0;
+      off[i] = tk % p.page_size;
+    }
+  }
+  __device__ __forceinline__ void rows(const DecodeParams& p, int (&r)[4], bool report) const {
+    bool bad = false;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const bool out = i < nb && uint32_t(raw[i]) >= uint32_t(p.num_pages);
+      bad |= out;
+      r[i] = (out ? 0 : raw[i]) * p.page_size + off[i];
+    }
+    if (bad && report) report_bad_page(p.status);
+  }
+};
+
+// kCode: CacheCode; kCausal: multi-token decode (q_len > 1) masks each row's
+// later positions on a sequence's last sub-tiles.
+template <int kCode, bool kCausal>
+__global__ void __launch_bounds__(HmCfg<kCode != kCodeBf16>::kThreads, 1)
+    decode_hm_kernel(const __grid_constant__ CUtensorMap tmap_lat, const __grid_constant__ CUtensorMap tmap_rope,
+                     const __grid_constant__ CUtensorMap tmap_qrope, DecodeParams p) {
+  constexpr bool kByte = kCode != kCodeBf16;
+  constexpr bool kZp = kCode == kCodeInt8;
+  using C = HmCfg<kByte>;
+  extern __shared__ uint8_t smem_raw[];
+  // the same offset in both CTAs: the peer's exchange buffers and barriers are found by mapa
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  HmBarriers* B = reinterpret_cast<HmBarriers*>(smem + C::kOffMisc);
+  const uint32_t sbase = smem_u32(smem);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kNumSlots; ++i) {
+      mbar_init(&B->full[i], kByte ? 1 : 2);
+      mbar_init(&B->landed[i], 2);
+      mbar_init(&B->empty[i], 1);
+    }
+    mbar_init(&B->q_full, 1 + 128);  // the RoPE part's TMA, and the 128 rows' latent parts
+    mbar_init(&B->q_empty, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&B->s_full[i], 1);
+      mbar_init(&B->x_full[i], 1);  // armed by one local thread; the peer's bytes complete it
+      mbar_init(&B->p_full[i], 128);
+      mbar_init(&B->pv_done[i], 1);
+      mbar_init(&B->drain[i], 1);
+    }
+    mbar_init(&B->o_full, 1);
+    mbar_init(&B->o_free, 128);
+    B->abort = 0;
+    fence_mbar_init();
+    prefetch_tensormap(&tmap_lat);
+    prefetch_tensormap(&tmap_rope);
+    prefetch_tensormap(&tmap_qrope);
+  }
+  if (warp == 1) {
+    tmem_alloc(&B->tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  cluster_sync();  // both CTAs' barriers exist before either sends to the other
+  tc_fence_after();
+  const uint32_t tmem = B->tmem_base;
+  griddep_wait();  // the plan and Q come from the kernel before
+  griddep_launch_dependents();
+
+  const int G = p.num_groups, clus = blockIdx.x / 2, g = clus % G, cp = clus / G, Cp = (gridDim.x / 2) / G;
+  const long long S = p.status[1];  // effective split count from the plan
+  const long long pa = (cp * S) / Cp, pb = ((cp + 1) * S) / Cp;
+  const volatile int* abort_flag = &B->abort;
+  const int P = p.page_size, box_rows = P < kSub ? P : kSub;
+  const int lat0 = 256 * int(rank), rope0 = kLatent + 32 * int(rank);  // this CTA's columns
+
+  if ((warp == 0 || warp == 3) && lane == 0) {
+    // ------------------------------------------------------------ producers
+    // Two threads share the copies (one cannot issue them fast enough for an
+    // SM's share of HBM): warp 0 the latent boxes 0-1 and the RoPE box, warp 3
+    // the latent boxes 2-3 (and, for 1-byte caches, the per-token scales).
+    const int role = warp == 0 ? 0 : 1;
+    const uint32_t sbytes = kZp ? 8 : 4;  // 1-byte caches: scale bytes per token
+    SubWalker walk, look;
+    walk.init(p, S, pa, pb);
+    look = walk;
+    SubTile s, sn;
+    SubPages cur, nxt;
+    bool have_next = look.next(sn);
+    if (have_next) nxt.fetch(p, sn, box_rows);
+    uint32_t k = 0, seg = 0;
+    bool ok = true;
+    while (ok && walk.next(s)) {
+      cur = nxt;
+      have_next = look.next(sn);
+      if (have_next) nxt.fetch(p, sn, box_rows);
+      if (s.first && role == 0) {
+        if (seg > 0 && !(ok = mbar_wait(&B->q_empty, (seg - 1) & 1, abort_flag, kWaitLimitNs))) break;
+        mbar_arrive_expect_tx(&B->q_full, kQRopeBytes);
+        tma_load_2d(smem + C::kOffQRope, &tmap_qrope, rope0, s.b * p.heads + g * kRowsG, &B->q_full);
+        ++seg;
+      }
+      int rows[4];
+      cur.rows(p, rows, role == 0);
+      const int nb = cur.nb;
+      if (kPrefetchNext && have_next && G == 1) {
+        // the next sub-tile's boxes into L2 now, so that its copies, issued
+        // once a slot frees, find them there
+        int nrows[4];
+        nxt.rows(p, nrows, false);
+#pragma unroll 1
+        for (int i = 0; i < nxt.nb; ++i) {
+          tma_prefetch_2d(&tmap_lat, lat0 + 128 * role, nrows[i]);
+          tma_prefetch_2d(&tmap_lat, lat0 + 128 * role + 64, nrows[i]);
+          if (role == 0) tma_prefetch_2d(&tmap_rope, rope0, nrows[i]);
+        }
+      }
+      const uint32_t slot = k % kNumSlots;
+      if (!(ok = mbar_wait(&B->empty[slot], ((k / kNumSlots) & 1) ^ 1, abort_flag, kWaitLimitNs))) break;
+      uint8_t* base = smem + slot * C::kSlotBytes;
+      const uint32_t rows_bytes = uint32_t(nb * box_rows);
+      if constexpr (!kByte) {
+        const uint32_t bytes = rows_bytes * (role == 0 ? 128 + 128 + 64 : 128 + 128);
+        mbar_arrive_expect_tx(&B->full[slot], bytes + (p.inject_wait_timeout && k == 0 && role == 0 ? 16 : 0));
+#pragma unroll 1
+        for (int i = 0; i < nb; ++i) {
+          for (int q = 2 * role; q < 2 * role + 2; ++q)
+            tma_load_2d(base + q * kLatBox + i * box_rows * 128, &tmap_lat, lat0 + 64 * q, rows[i], &B->full[slot]);
+          if (role == 0)
+            tma_load_2d(base + kOffRopeBox + i * box_rows * 64, &tmap_rope, rope0, rows[i], &B->full[slot]);
+        }
+      } else {
+        const uint32_t bytes = rows_bytes * (role == 0 ? 64 + 64 + 32 : 64 + 64 + sbytes);
+        mbar_arrive_expect_tx(&B->landed[slot], bytes + (p.inject_wait_timeout && k == 0 && role == 0 ? 16 : 0));
+#pragma unroll 1
+        for (int i = 0; i < nb; ++i) {
+          for (int q = 2 * role; q < 2 * role + 2; ++q)
+            tma_load_2d(base + kOffCodes + q * 4096 + i * box_rows * 64, &tmap_lat, lat0 + 64 * q, rows[i],
+                        &B->landed[slot]);
+          if (role == 0)
+            tma_load_2d(base + kOffCodeRope + i * box_rows * 32, &tmap_rope, rope0, rows[i], &B->landed[slot]);
+          else
+            bulk_copy_g2s(base + kOffScales + i * box_rows * sbytes, p.scale_zero + size_t(rows[i]) * (kZp ? 2 : 1),
+                          box_rows * sbytes, &B->landed[slot]);
+        }
+      }
+      ++k;
+    }
+    if (!ok) fail(B, p.status);
+  } else if (warp == 1 && lane == 0) {
+    // ------------------------------------------------------------ QK issuer
+    // S_r[k & 1] = Q_r * C_r^T: 16 MMAs on the latent columns (A = Q's latent
+    // part in TMEM), 2 on the RoPE columns (A = Q's RoPE part in shared
+    // memory).  Before overwriting S[k & 1] it waits for PV of sub-tile k - 2,
+    // which read P from there (and so for its softmax too).
+    SubWalker walk;
+    walk.init(p, S, pa, pb);
+    constexpr uint32_t id_qk = idesc_f32acc(kRowsG, kSub, false, false, kByte);
+    constexpr uint64_t kDescK = smem_desc(0, 16, 1024, kSwizzle128B);   // K-major SW128 (8-row groups of 1 KB)
+    constexpr uint64_t kDescRope = smem_desc(0, 16, 512, kSwizzle64B);  // K-major SW64 (8-row groups of 512 B)
+    uint32_t k = 0, seg = 0;
+    SubTile s;
+    bool ok = true;
+    while (ok && walk.next(s)) {
+      const uint32_t sb = k & 1, slot = k % kNumSlots;
+      if (k >= 2 && !(ok = mbar_wait(&B->pv_done[sb], ((k - 2) >> 1) & 1, abort_flag, kWaitLimitNs))) break;
+      if (s.first && !(ok = mbar_wait(&B->q_full, seg & 1, abort_flag, kWaitLimitNs))) break;
+      if (!(ok = mbar_wait(&B->full[slot], (k / kNumSlots) & 1, abort_flag, kWaitLimitNs))) break;
+      tc_fence_after();
+      const uint32_t d = tmem + kColS + sb * kSub;
+      const uint32_t bs = sbase + slot * C::kSlotBytes;
+#pragma unroll
+      for (int kk = 0; kk < 16; ++kk)
+        mma_f16_tmem_a(d, tmem + kColQ + 8 * kk, kDescK | desc_addr(bs + (kk >> 2) * kLatBox + 32 * (kk & 3)), id_qk,
+                       kk > 0);
+#pragma unroll
+      for (int kk = 0; kk < 2; ++kk)
+        mma_bf16(d, kDescRope | desc_addr(sbase + C::kOffQRope + 32 * kk),
+                 kDescRope | desc_addr(bs + kOffRopeBox + 32 * kk), id_qk, 1);
+      mma_commit(&B->s_full[sb]);
+      if (s.last) {
+        mma_commit(&B->q_empty);
+        ++seg;
+      }
+      ++k;
+    }
+    if (!ok) fail(B, p.status);
+    mma_commit(&B->drain[0]);  // every MMA this thread issued completes before teardown
+    mbar_wait(&B->drain[0], 0, abort_flag, kWaitLimitNs);
+  } else if (warp == 2) {
+    // ------------------------------------------------------------ PV issuer
+    // O_r (+)= P * C_r[:, latent] once the softmax of the sub-tile is done;
+    // the slot is released when its MMAs complete.
+    SubWalker walk;
+    walk.init(p, S, pa, pb);
+    constexpr uint32_t id_pv = idesc_f32acc(kRowsG, 256, false, true, kByte);
+    constexpr uint64_t kDescMN = smem_desc(0, kLatBox, 1024, kSwizzle128B);  // MN-major SW128, 64-column blocks
+    uint32_t k = 0, seg = 0;
+    SubTile s;
+    bool ok = true;
+    while (ok && walk.next(s)) {
+      const uint32_t sb = k & 1, slot = k % kNumSlots;
+      bool w = true;
+      if (lane == 0) {
+        w = mbar_wait(&B->p_full[sb], (k >> 1) & 1, abort_flag, kWaitLimitNs);
+        if (w && s.first && seg > 0) w = mbar_wait(&B->o_free, (seg - 1) & 1, abort_flag, kWaitLimitNs);
+      }
+      if (!(ok = __shfl_sync(0xffffffffu, w, 0))) break;
+      const int nk = (s.valid + 15) >> 4;
+      if (!kByte && 16 * nk > s.valid) {
+        // rows between the sequence's end and the last k-step's bound meet
+        // zero probabilities but must be finite (they hold whatever the page's
+        // tail or the slot's previous use left): clear them in all 4 boxes
+        uint8_t* base = smem + slot * C::kSlotBytes;
+        const int tail = 16 * nk - s.valid;
+        for (int i = lane; i < tail * 32; i += 32)
+          *reinterpret_cast<uint4*>(base + ((i >> 3) & 3) * kLatBox + (s.valid + (i >> 5)) * 128 + (i & 7) * 16) =
+              make_uint4(0, 0, 0, 0);
+        fence_proxy_async_smem();
+        __syncwarp();
+      }
+      if (lane == 0) {
+        tc_fence_after();
+        const uint32_t a = tmem + kColS + sb * kSub;  // P: columns [0, 32) of the sub-tile's score buffer
+        const uint32_t bs = sbase + slot * C::kSlotBytes;
+        for (int kk = 0; kk < nk; ++kk)
+          mma_f16_tmem_a(tmem + kColO, a + 8 * kk, kDescMN | desc_addr(bs + 2048 * kk), id_pv, !(s.first && kk == 0));
+        mma_commit(&B->empty[slot]);
+        mma_commit(&B->pv_done[sb]);
+        if (s.last) mma_commit(&B->o_full);
+      }
+      if (s.last) ++seg;
+      ++k;
+    }
+    if (lane == 0) {
+      if (!ok) fail(B, p.status);
+      mma_commit(&B->drain[1]);
+      mbar_wait(&B->drain[1], 0, abort_flag, kWaitLimitNs);
+    }
+  } else if (kByte && warp >= 8) {
+    if constexpr (kByte) {
+      // ------------------------------------------------------------ code expansion
+      // Each landed sub-tile's codes become fp16 operand boxes in the same
+      // slot: latent block q -> SW128 box q, RoPE codes -> the SW64 box.  The
+      // codes sit where boxes 2-3 and the RoPE box go, so every thread reads
+      // all of its codes before any thread writes.  Rows at and past the
+      // sequence's end are written as zeros (PV reads them with zero weight,
+      // and a code there is whatever the page's tail holds).
+      const int ct = threadIdx.x - 256;
+      SubWalker walk;
+      walk.init(p, S, pa, pb);
+      uint32_t k = 0;
+      SubTile s;
+      bool ok = true;
+      while (ok && walk.next(s)) {
+        const uint32_t slot = k % kNumSlots;
+        uint8_t* base = smem + slot * C::kSlotBytes;
+        const bool landed = mbar_wait(&B->landed[slot], (k / kNumSlots) & 1, abort_flag, kWaitLimitNs);
+        uint4 v[9];
+        if (landed) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int c = ct + 128 * i, q = c >> 8, r = (c >> 2) & 63, ch = c & 3;
+            v[i] = *reinterpret_cast<const uint4*>(base + kOffCodes + q * 4096 + r * 64 + ch * 16);
+          }
+          v[8] = *reinterpret_cast<const uint4*>(base + kOffCodeRope + (ct >> 1) * 32 + (ct & 1) * 16);
+        }
+        if (converters_any(!landed)) {  // also: all codes read before any write
+          ok = false;
+          break;
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int c = ct + 128 * i, q = c >> 8, r = (c >> 2) & 63, ch = c & 3;
+          uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
+          if (r < s.valid) {
+            if constexpr (kZp) expand_codes(v[i], lo, hi);
+            else expand_e4m3(v[i], lo, hi);
+          }
+          uint8_t* row = base + q * kLatBox + r * 128;
+          *reinterpret_cast<uint4*>(row + (((2 * ch) ^ (r & 7)) << 4)) = lo;
+          *reinterpret_cast<uint4*>(row + (((2 * ch + 1) ^ (r & 7)) << 4)) = hi;
+        }
+        {
+          const int r = ct >> 1, ch = ct & 1;
+          uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
+          if (r < s.valid) {
+            if constexpr (kZp) expand_codes(v[8], lo, hi);
+            else expand_e4m3(v[8], lo, hi);
+          }
+          uint8_t* row = base + kOffRopeBox + r * 64;  // 64-byte rows, 64-byte swizzle
+          *reinterpret_cast<uint4*>(row + (((2 * ch) ^ ((r >> 1) & 3)) << 4)) = lo;
+          *reinterpret_cast<uint4*>(row + (((2 * ch + 1) ^ ((r >> 1) & 3)) << 4)) = hi;
+        }
+        fence_proxy_async_smem();
+        converters_sync();
+        if (ct == 0) mbar_arrive(&B->full[slot]);
+        ++k;
+      }
+      if (!ok) fail(B, p.status);
+    }
+  } else if (warp >= 4 && warp < 8) {
+    // ------------------------------------------------------------ Q, exchange, softmax, epilogue
+    const int q4 = warp - 4, h = threadIdx.x - 128;  // h: row of the group = TMEM lane
+    const uint32_t lane_off = uint32_t(q4 * 32) << 16;
+    const int row = g * kRowsG + h;                   // row within the sequence's rows
+    const uint32_t x_local = sbase + C::kOffX + h * (kSub * 4);
+    const int xr_rot = h & 15;                        // 16-byte pieces rotated by row to spread banks
+    const uint32_t peer = rank ^ 1u;
+    SubWalker walk;
+    walk.init(p, S, pa, pb);
+    float m_run = 0.f, l_run = 0.f, corr = 0.f, qsum = 0.f;
+    uint32_t k = 0, seg = 0;
+    SubTile s;
+    while (walk.next(s)) {
+      const uint32_t sb = k & 1, slot = k % kNumSlots;
+      if (s.first) {
+        // Q's latent part for this segment's sequence into TMEM.  Every QK
+        // MMA of the previous segment has completed: this thread saw the
+        // s_full of its last sub-tile.
+        const uint4* src = reinterpret_cast<const uint4*>(p.q_full + (size_t(s.b) * p.heads + row) * kRow + lat0);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t r[32];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const uint4 v = __ldg(src + 8 * c + i);
+            r[4 * i] = v.x; r[4 * i + 1] = v.y; r[4 * i + 2] = v.z; r[4 * i + 3] = v.w;
+          }
+          tmem_st32(tmem + lane_off + kColQ + 32 * c, r);
+        }
+        tmem_st_wait();
+        if (kZp) {
+          const float* qs = p.q_sum + (size_t(s.b) * p.heads + row) * kQSumParts;
+          float t = qs[0];
+#pragma unroll
+          for (int c = 1; c < kQSumParts; ++c) t += qs[c];
+          qsum = t;
+        }
+        tc_fence_before();
+        mbar_arrive(&B->q_full);
+      }
+      bool ok = mbar_wait(&B->s_full[sb], (k >> 1) & 1, abort_flag, kWaitLimitNs);
+      if (bar_any(!ok)) break;
+      tc_fence_after();
+      float x[kSub];
+      {
+        uint32_t r[32];
+        tmem_ld32(tmem + lane_off + kColS + sb * kSub, r);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) x[i] = __uint_as_float(r[i]);
+        tmem_ld32(tmem + lane_off + kColS + sb * kSub + 32, r);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) x[32 + i] = __uint_as_float(r[i]);
+      }
+      // partial scores to the peer, into its buffer sb
+      {
+        const uint32_t rbar = mapa_shared(smem_u32(&B->x_full[sb]), peer);
+        const uint32_t xr = mapa_shared(x_local + sb * kXBytes, peer);
+#pragma unroll
+        for (int v = 0; v < kSub / 4; ++v)
+          st_async_v4(xr + (v ^ xr_rot) * 16, x[4 * v], x[4 * v + 1], x[4 * v + 2], x[4 * v + 3], rbar);
+      }
+      if (h == 0) mbar_arrive_expect_tx(&B->x_full[sb], kXBytes);
+      ok = mbar_wait_cluster(&B->x_full[sb], (k >> 1) & 1, abort_flag, kWaitLimitNs);
+      if (kByte && ok) ok = mbar_wait(&B->landed[slot], (k / kNumSlots) & 1, abort_flag, kWaitLimitNs);
+      if (bar_any(!ok)) break;
+      // S = S_0 + S_1 (addition is commutative: both CTAs get the same bits)
+#pragma unroll
+      for (int v = 0; v < kSub / 4; ++v) {
+        const float4 y = *reinterpret_cast<const float4*>(smem + C::kOffX + sb * kXBytes + h * (kSub * 4) +
+                                                          (v ^ xr_rot) * 16);
+        x[4 * v] += y.x; x[4 * v + 1] += y.y; x[4 * v + 2] += y.z; x[4 * v + 3] += y.w;
+      }
+      const float* sc = reinterpret_cast<const float*>(smem + slot * C::kSlotBytes + kOffScales);
+      // scores in log2 units; tokens past the sub-tile's end (and, for
+      // multi-token rows, positions after the row's own) are -inf
+      const int qpos = kCausal ? walk.len() - p.q_len + row / p.heads_w : 0x7fffffff;
+#pragma unroll
+      for (int t = 0; t < kSub; ++t) {
+        bool vis = t < s.valid;
+        if (kCausal) vis = vis && s.tok0 + t <= qpos;
+        float v = x[t];
+        if constexpr (kByte) {
+          const float ts = kZp ? sc[2 * t] : sc[t];
+          if constexpr (kZp) v = fmaf(-sc[2 * t + 1], qsum, v);
+          v = v * (p.scale_log2 * ts);
+        } else {
+          v = v * p.scale_log2;
+        }
+        x[t] = vis ? v : -INFINITY;
+      }
+      float mt = x[0];
+#pragma unroll
+      for (int t = 1; t < kSub; ++t) mt = fmaxf(mt, x[t]);
+      // running max: it only has to bound the row's scores within
+      // kRescaleThreshold; the first sub-tile of a segment sets it, a sub-tile
+      // that breaks the bound raises it and rescales O and l
+      float alpha = 1.f;
+      bool rescale = false;
+      if (s.first) {
+        m_run = fmaxf(mt, kEmptyRowMax);  // a row masked in the whole sub-tile stays empty
+        l_run = 0.f;
+        corr = 0.f;
+      } else if (mt > m_run + kRescaleThreshold) {
+        alpha = exp2f(m_run - mt);
+        m_run = mt;
+        l_run *= alpha;
+        corr *= alpha;
+        rescale = true;
+      }
+      if (__any_sync(0xffffffffu, rescale)) {
+        // PV of the previous sub-tile must be complete before O is rescaled
+        const bool ok3 = mbar_wait(&B->pv_done[(k - 1) & 1], ((k - 1) >> 1) & 1, abort_flag, kWaitLimitNs);
+        tc_fence_after();
+        if (__all_sync(0xffffffffu, ok3)) {
+#pragma unroll 1
+          for (int c = 0; c < 8; ++c) {
+            uint32_t r[32];
+            tmem_ld32(tmem + lane_off + kColO + 32 * c, r);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+            tmem_st32(tmem + lane_off + kColO + 32 * c, r);
+          }
+          tmem_st_wait();
+        } else {
+          ok = false;
+        }
+      }
+      if (bar_any(!ok)) break;
+      // probabilities -> P over the scores: bf16 (bf16 caches) or fp16 with
+      // the token's scale folded in (1-byte caches)
+      {
+        uint32_t pk[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const int ta = 2 * i, tb = ta + 1;
+          const float pa_ = ex2_ftz(x[ta] - m_run), pb_ = ex2_ftz(x[tb] - m_run);
+          if constexpr (kByte) {
+            const float sa = ta < s.valid ? (kZp ? sc[2 * ta] : sc[ta]) : 0.f;
+            const float sbv = tb < s.valid ? (kZp ? sc[2 * tb] : sc[tb]) : 0.f;
+            const __half wa = __float2half_rn(pa_ * sa), wb = __float2half_rn(pb_ * sbv);
+            l_run += pa_ + pb_;
+            if constexpr (kZp) {
+              const float za = ta < s.valid ? sc[2 * ta + 1] : 0.f, zb = tb < s.valid ? sc[2 * tb + 1] : 0.f;
+              corr = fmaf(__half2float(wa), za, corr);
+              corr = fmaf(__half2float(wb), zb, corr);
+            }
+            pk[i] = uint32_t(__half_as_ushort(wa)) | (uint32_t(__half_as_ushort(wb)) << 16);
+          } else {
+            const __nv_bfloat16 wa = __float2bfloat16_rn(pa_), wb = __float2bfloat16_rn(pb_);
+            l_run += __bfloat162float(wa) + __bfloat162float(wb);
+            pk[i] = uint32_t(__bfloat16_as_ushort(wa)) | (uint32_t(__bfloat16_as_ushort(wb)) << 16);
+          }
+        }
+        tmem_st32(tmem + lane_off + kColS + sb * kSub, pk);
+        tmem_st_wait();
+      }
+      tc_fence_before();
+      mbar_arrive(&B->p_full[sb]);
+      if (s.last) {
+        const bool ok2 = mbar_wait(&B->o_full, seg & 1, abort_flag, kWaitLimitNs);
+        if (bar_any(!ok2)) break;
+        tc_fence_after();
+        const float inv_l = l_run > 0.f ? __frcp_rn(l_run) : 0.f;  // 0: a row that saw no token
+        float4* dst = reinterpret_cast<float4*>(p.partial_o + (size_t(s.seg) * p.heads + row) * kLatent + lat0);
+#pragma unroll 1
+        for (int c = 0; c < 8; ++c) {
+          uint32_t r[32];
+          tmem_ld32(tmem + lane_off + kColO + 32 * c, r);
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            dst[8 * c + i] = make_float4((__uint_as_float(r[4 * i]) - corr) * inv_l,
+                                         (__uint_as_float(r[4 * i + 1]) - corr) * inv_l,
+                                         (__uint_as_float(r[4 * i + 2]) - corr) * inv_l,
+                                         (__uint_as_float(r[4 * i + 3]) - corr) * inv_l);
+        }
+        tc_fence_before();
+        mbar_arrive(&B->o_free);
+        if (rank == 0)
+          p.partial_lse[size_t(s.seg) * p.heads + row] = l_run > 0.f ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
+        ++seg;
+      }
+      ++k;
+    }
+  }
+  // ---------------------------------------------------------------- teardown
+  __syncthreads();
+  if (B->abort) {  // let copies already issued land before the CTA's shared memory is released
+    const uint64_t t0 = global_timer_ns();
+    while (global_timer_ns() - t0 < 20000) {
+    }
+  }
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+  cluster_sync();  // the peer may still be sending into this CTA's shared memory until here
+}
+
+template <int kCode>
+cudaError_t launch_hm(const DecodeParams& p, int clusters_per_group, cudaStream_t stream) {
+  constexpr bool kByte = kCode != kCodeBf16;
+  using C = HmCfg<kByte>;
+  CUtensorMap ml, mr, mqr;
+  const uint64_t rows = uint64_t(p.num_pages) * p.page_size, qrows = uint64_t(p.batch) * p.heads;
+  const uint32_t box_rows = p.page_size < kSub ? p.page_size : kSub;
+  const int eb = kByte ? 1 : 2;
+  if (!make_map_2d(&ml, p.cache, eb, kRow, rows, 64, box_rows,
+                   kByte ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_map_2d(&mr, p.cache, eb, kRow, rows, 32, box_rows,
+                   kByte ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_64B) ||
+      !make_map_2d(&mqr, p.q_full, 2, kRow, qrows, 32, kRowsG, CU_TENSOR_MAP_SWIZZLE_64B))
+    return cudaErrorInvalidValue;
+  static std::atomic<bool> attr[128];  // per device: attributes set (zero-initialised)
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 128 || !attr[dev]) {
+    for (auto* k : {decode_hm_kernel<kCode, false>, decode_hm_kernel<kCode, true>}) {
+      const cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, int(C::kSmem));
+      if (e != cudaSuccess) return e;
+    }
+    if (dev >= 0 && dev < 128) attr[dev] = true;
+  }
+  auto* kernel = p.q_len > 1 ? decode_hm_kernel<kCode, true> : decode_hm_kernel<kCode, false>;
+  return launch_pdl(kernel, dim3(2 * clusters_per_group * p.num_groups), dim3(C::kThreads), C::kSmem, stream, 2, ml,
+                    mr, mqr, p);
+}
+
+template <int kCode>
+int hm_capacity() {  // CTA pairs of this kernel that can be resident at once on this device
+  using C = HmCfg<kCode != kCodeBf16>;
+  static std::atomic<int> cached[128];  // per device (zero-initialised)
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 128 && cached[dev] > 0) return cached[dev];
+  if (cudaFuncSetAttribute(decode_hm_kernel<kCode, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           int(C::kSmem)) != cudaSuccess)
+    return 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2);
+  cfg.blockDim = dim3(C::kThreads);
+  cfg.dynamicSmemBytes = C::kSmem;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = 2;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, decode_hm_kernel<kCode, false>, &cfg) != cudaSuccess || n <= 0) {
+    cudaGetLastError();
+    return 0;
+  }
+  if (dev >= 0 && dev < 128) cached[dev] = n;
+  return n;
+}
+
+}  // namespace
+
+int decode_rows128_capacity(int code) {
+  return code == kCodeInt8 ? hm_capacity<kCodeInt8>() : code == kCodeE4m3 ? hm_capacity<kCodeE4m3>()
+                                                                          : hm_capacity<kCodeBf16>();
+}
+
+cudaError_t launch_decode_rows128(const DecodeParams& p, int code, int clusters_per_group, cudaStream_t stream) {
+  return code == kCodeInt8   ? launch_hm<kCodeInt8>(p, clusters_per_group, stream)
+         : code == kCodeE4m3 ? launch_hm<kCodeE4m3>(p, clusters_per_group, stream)
+                             : launch_hm<kCodeBf16>(p, clusters_per_group, stream);
+}
+
+}  // namespace mla

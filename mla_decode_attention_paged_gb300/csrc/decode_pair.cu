@@ -104,15 +104,6 @@ struct PairBarriers {
   int abort;
 };
 
-// 2^x with the hardware approximation (relative error about 2^-22, far
-// below the bf16 rounding the probabilities get next); flushes subnormal
-// results to zero, which only affects weights below 2^-126.
-__device__ __forceinline__ float ex2_ftz(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-
 __device__ __forceinline__ void fail(PairBarriers* B, int* status) {
   B->abort = 1;
   set_status(status, MLA_ERR_DEVICE_TIMEOUT);

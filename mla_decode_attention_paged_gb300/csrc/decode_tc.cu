@@ -143,62 +143,9 @@ __device__ __forceinline__ bool wait_progress(const int* counter, int k, const v
   }
 }
 
-// 1-byte caches: four warps (3, 8, 9, 10) expand the codes, named barrier 2
-constexpr int kConvThreads = 128;
-__device__ __forceinline__ bool converters_any(bool pred) {  // OR over the expansion threads (barrier 2)
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\t"
-      "setp.ne.u32 p, %1, 0;\n\t"
-      "bar.red.or.pred q, 2, %2, p;\n\t"
-      "selp.u32 %0, 1, 0, q;\n\t}"
-      : "=r"(r)
-      : "r"(uint32_t(pred)), "n"(kConvThreads)
-      : "memory");
-  return r != 0;
-}
-__device__ __forceinline__ void converters_sync() { asm volatile("bar.sync 2, %0;" ::"n"(kConvThreads) : "memory"); }
-
 __device__ __forceinline__ void fail(Barriers* B, int* status) {
   B->abort = 1;
   set_status(status, MLA_ERR_DEVICE_TIMEOUT);
-}
-
-// 16 int8 codes -> 16 fp16 values equal to the codes, as two 16-byte halves.
-__device__ __forceinline__ uint32_t codes_to_half2(uint32_t biased_bits) {  // (1152 + a, 1152 + b) -> (a, b)
-  const __half2 h = __hsub2(*reinterpret_cast<const __half2*>(&biased_bits), __floats2half2_rn(1152.f, 1152.f));
-  return *reinterpret_cast<const uint32_t*>(&h);
-}
-__device__ __forceinline__ void expand_codes(uint4 v, uint4& lo, uint4& hi) {
-  const uint32_t w[4] = {v.x ^ 0x80808080u, v.y ^ 0x80808080u, v.z ^ 0x80808080u, v.w ^ 0x80808080u};
-  uint32_t o[8];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    o[2 * i] = codes_to_half2(__byte_perm(w[i], 0x64646464u, 0x4140));      // bytes 0,1 -> 0x64xx 0x64xx
-    o[2 * i + 1] = codes_to_half2(__byte_perm(w[i], 0x64646464u, 0x4342));  // bytes 2,3
-  }
-  lo = make_uint4(o[0], o[1], o[2], o[3]);
-  hi = make_uint4(o[4], o[5], o[6], o[7]);
-}
-
-// 16 E4M3 codes -> 16 fp16 values equal to the codes' values (every E4M3
-// value is exact in fp16: at most 4 significant bits, magnitudes 2^-9..448),
-// one conversion instruction per pair; byte k of each word becomes half k.
-__device__ __forceinline__ uint32_t e4m3x2_to_half2(uint32_t two_codes) {
-  uint32_t r;
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(uint16_t(two_codes)));
-  return r;
-}
-__device__ __forceinline__ void expand_e4m3(uint4 v, uint4& lo, uint4& hi) {
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-  uint32_t o[8];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    o[2 * i] = e4m3x2_to_half2(w[i]);            // bytes 0,1
-    o[2 * i + 1] = e4m3x2_to_half2(w[i] >> 16);  // bytes 2,3
-  }
-  lo = make_uint4(o[0], o[1], o[2], o[3]);
-  hi = make_uint4(o[4], o[5], o[6], o[7]);
 }
 
 // kCode: CacheCode (bf16, INT8 or FP8 rows).

@@ -51,18 +51,37 @@ mla_dims row_dims(const mla_dims* d, int q_len) {
   return r;
 }
 
+// The attention kernel for `rows` query rows per sequence (heads, or
+// q_len x heads): groups of 128 rows run on the 128-row CTA-pair kernel (any
+// cache format); otherwise bf16 caches run on the 16/32-head CTA-pair kernel
+// and 1-byte caches (and devices that cannot place pairs) on single CTAs.
+// `units` = attention units resident at once (pairs or CTAs).
+enum AttnKind { kAttnRows128, kAttnPair, kAttnSingle };
+struct AttnChoice {
+  int kind, hc, units;
+};
+AttnChoice choose_attention(int rows, int code) {
+  const bool byte = code != kCodeBf16;
+  const bool single = g_force_single_cta.load() != 0;
+  if (rows % 128 == 0 && !single) {
+    const int cap = decode_rows128_capacity(code);
+    if (cap > 0) return {kAttnRows128, 128, cap};
+  }
+  const int hc = decode_head_group(rows, byte);
+  const int pairs = byte || single ? 0 : decode_pair_capacity(hc);
+  if (pairs > 0) return {kAttnPair, hc, pairs};
+  return {kAttnSingle, hc, sm_count()};
+}
+
 // Automatic split count: one partition per resident attention unit of a
-// head group -- a CTA cluster for bf16 caches, a CTA for 1-byte caches (more
-// partitions only add segment switches and partials to merge).
+// head group (more partitions only add segment switches and partials to
+// merge).
 int effective_splits(const mla_dims* d, int num_splits) {
   if (num_splits > 0) return num_splits;
-  const bool byte = cache_code(d) != kCodeBf16;
-  const int hc = decode_head_group(d->num_heads, byte);
-  const int clusters = byte || g_force_single_cta.load() ? 0 : decode_pair_capacity(hc);
-  const int n = clusters > 0 ? clusters : sm_count();
-  if (n <= 0) return -1;
-  const int groups = d->num_heads / hc;
-  return n / groups > 0 ? n / groups : 1;
+  const AttnChoice a = choose_attention(d->num_heads, cache_code(d));
+  if (a.units <= 0) return -1;
+  const int groups = d->num_heads / a.hc;
+  return a.units / groups > 0 ? a.units / groups : 1;
 }
 
 int decode_rows(const mla_dims* d, const void* q_nope, const void* q_pe, const void* cache,
@@ -277,7 +296,9 @@ int decode_rows(const mla_dims* d, const void* q_nope, const void* q_pe, const v
   const WorkspaceLayout L = workspace_layout(batch, dr.num_heads, S);
   if (!workspace || !aligned(workspace, 256) || workspace_bytes < L.total) return MLA_ERR_WORKSPACE;
 
-  const int H = dr.num_heads, hc = decode_head_group(H, byte), groups = H / hc;
+  const AttnChoice attn = choose_attention(dr.num_heads, code);
+  if (attn.units <= 0) return MLA_ERR_CUDA;
+  const int H = dr.num_heads, hc = attn.hc, groups = H / hc;
   char* ws = static_cast<char*>(workspace);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 
@@ -325,16 +346,13 @@ int decode_rows(const mla_dims* d, const void* q_nope, const void* q_pe, const v
   dp.heads_w = d->num_heads;
   dp.scale_log2 = softmax_scale * kLog2e;
   dp.inject_wait_timeout = g_inject_wait_timeout.load();
-  // bf16 caches run on CTA pairs (two SMs share each tile); 1-byte caches,
-  // and devices that cannot place the pairs, on single CTAs
-  const int pair_cap = byte || g_force_single_cta.load() ? 0 : decode_pair_capacity(hc);
-  const int units = pair_cap > 0 ? pair_cap : sm_count();
-  const int per_group = units / groups > 0 ? units / groups : 1;
+  const int per_group = attn.units / groups > 0 ? attn.units / groups : 1;
   const int per_group_used = S < per_group ? S : per_group;
   cudaEvent_t ev0 = g_ev_start.load(), ev1 = g_ev_stop.load();
   if (ev0 && ev1 && cudaEventRecord(ev0, s) != cudaSuccess) return MLA_ERR_CUDA;
-  const cudaError_t le = pair_cap > 0 ? launch_decode_pair(dp, hc, per_group_used, s)
-                                      : launch_decode_tc(dp, hc, code, per_group_used * groups, s);
+  const cudaError_t le = attn.kind == kAttnRows128 ? launch_decode_rows128(dp, code, per_group_used, s)
+                         : attn.kind == kAttnPair  ? launch_decode_pair(dp, hc, per_group_used, s)
+                                                   : launch_decode_tc(dp, hc, code, per_group_used * groups, s);
   if (le != cudaSuccess) return MLA_ERR_CUDA;
   if (ev0 && ev1 && cudaEventRecord(ev1, s) != cudaSuccess) return MLA_ERR_CUDA;
 

@@ -134,5 +134,9 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
 // bf16 caches: CTA-cluster kernel.  Capacity = clusters resident at once (0 if none).
 int decode_pair_capacity(int hc);
 cudaError_t launch_decode_pair(const DecodeParams& p, int hc, int clusters_per_group, cudaStream_t stream);
+// Groups of 128 query rows, any cache format (CacheCode): CTA-pair kernel
+// with the rows on the MMA's M extent.  Capacity = pairs resident at once (0 if none).
+int decode_rows128_capacity(int code);
+cudaError_t launch_decode_rows128(const DecodeParams& p, int code, int clusters_per_group, cudaStream_t stream);
 
 }  // namespace mla

@@ -40,9 +40,10 @@ def _decode(d, x, ws):
     return out, lse
 
 
+@pytest.mark.parametrize("heads", [16, 128], ids=["16-heads", "128-rows"])
 @pytest.mark.parametrize("fmt", ["bf16", "int8", "fp8"], ids=["bf16-pairs", "int8", "fp8"])
-def test_unsatisfiable_wait_reports_timeout_and_context_survives(cuda_lib, fmt):
-    d, x = _inputs(fmt)
+def test_unsatisfiable_wait_reports_timeout_and_context_survives(cuda_lib, fmt, heads):
+    d, x = _inputs(fmt, heads=heads)
     ws = torch.empty(mla.decode_workspace_size(d, 2, 8), dtype=torch.uint8, device="cuda")
     ref_out, ref_lse = _decode(d, x, ws)
     assert mla.read_device_status(ws) == mla.MLA_OK
