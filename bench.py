@@ -101,8 +101,12 @@ def prefill_flops(seq_lens, chunk: int, heads: int) -> float:
     return float(total) * heads * (2 * 576 + 2 * 512)
 
 
-def attention_kernel(fmt: str):
-    """(source file, kernel name) of the attention kernel the library runs for this cache format."""
+def attention_kernel(fmt: str, rows: int = 16):
+    """(source file, kernel name) of the attention kernel the library runs for
+    this cache format and number of query rows per sequence (heads x tokens)."""
+    if rows % 128 == 0:
+        return (os.path.join(ROOT, "mla_decode_attention_paged_gb300", "csrc", "decode_hm.cu"),
+                f"decode_hm_kernel (128-row groups on CTA pairs, {fmt.upper()} cache)")
     name = "decode_pair.cu" if fmt == "bf16" else "decode_tc.cu"
     return (os.path.join(ROOT, "mla_decode_attention_paged_gb300", "csrc", name),
             "decode_pair_kernel (split-KV attention on CTA pairs)" if fmt == "bf16"
@@ -126,7 +130,7 @@ def workload_config(w, cache_bytes: int, world: int) -> dict:
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
 
 
-def kernel_traffic(workload_name: str, tokens: int, fmt: str):
+def kernel_traffic(workload_name: str, tokens: int, fmt: str, rows: int = 16):
     """DRAM bytes per attention launch from the committed ncu summary, scaled
     to this launch's tokens; None if absent or taken on a different kernel."""
     path = os.path.join(ROOT, "profiles", "attention_dram_traffic.json")
@@ -135,7 +139,7 @@ def kernel_traffic(workload_name: str, tokens: int, fmt: str):
     e = json.load(open(path)).get("workloads", {}).get(workload_name)
     if not e:
         return None
-    src, _ = attention_kernel(fmt)
+    src, _ = attention_kernel(fmt, rows)
     if hashlib.sha256(open(src, "rb").read()).hexdigest() != e.get("kernel_sha256"):
         return None
     return round(e["dram_bytes_per_token"] * tokens)
@@ -583,20 +587,32 @@ def run_ours(args, rank, world):
     e2e_ms = max_over_ranks(e2e_ms, world)
 
     peak, peak_src = peaks()
+    tpeak, tpeak_src = tensor_peak()
     achieved = cache_bytes / (kern_ms / 1e3) / 1e9
-    traffic = kernel_traffic(w.name, lens_sum, w.cache_format)
-    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                "frac": round(achieved / peak, 4), "peak_source": peak_src,
-                "traffic": traffic, "kernel": attention_kernel(w.cache_format)[1],
-                "algorithmic_bytes_per_launch": cache_bytes}
+    traffic = kernel_traffic(w.name, lens_sum, w.cache_format, H * T)
+    kname = attention_kernel(w.cache_format, H * T)[1]
+    # the attention's algorithmic FLOPs (absorbed form): every (query row,
+    # visible token) pair scores a 576-wide row and adds a 512-wide one
+    flops = (prefill_flops(seq_lens.cpu().tolist(), T, H) if T > 1 else
+             float(lens_sum) * H * (2 * 576 + 2 * 512))
+    tflops = flops / (kern_ms / 1e3) / 1e12
+    hbm_frac, tensor_frac = achieved / peak, tflops / tpeak
+    # the binding bound: whichever peak the launch's work needs longer on
+    if flops / (tpeak * 1e12) > cache_bytes / (peak * 1e9):
+        roofline = {"bound": "tensor", "achieved": round(tflops, 2), "peak": tpeak, "unit": "TFLOP/s",
+                    "frac": round(tensor_frac, 4), "peak_source": tpeak_src, "traffic": traffic, "kernel": kname,
+                    "algorithmic_flops_per_launch": flops, "algorithmic_bytes_per_launch": cache_bytes,
+                    "hbm_frac": round(hbm_frac, 4)}
+    else:
+        roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                    "frac": round(hbm_frac, 4), "peak_source": peak_src, "traffic": traffic, "kernel": kname,
+                    "algorithmic_bytes_per_launch": cache_bytes, "algorithmic_flops_per_launch": flops,
+                    "tensor_frac": round(tensor_frac, 4)}
     if w.chunk:
         # prefill is compute-bound: FLOPs of the chunk's attention against the bf16 tensor peak
-        flops = prefill_flops(seq_lens.cpu().tolist(), T, H)
-        tpeak, tpeak_src = tensor_peak()
-        tflops = flops / (kern_ms / 1e3) / 1e12
         roofline = {"bound": "tensor", "achieved": round(tflops, 2), "peak": tpeak, "unit": "TFLOP/s",
                     "frac": round(tflops / tpeak, 4), "peak_source": tpeak_src, "traffic": traffic,
-                    "kernel": attention_kernel(w.cache_format)[1], "algorithmic_flops_per_launch": flops,
+                    "kernel": kname, "algorithmic_flops_per_launch": flops,
                     "history_bytes_per_launch": cache_bytes}
     res = {
         "metric": PREFILL_METRIC if w.chunk else METRIC, "value": round(tokens_per_s, 1), "unit": "tokens/s", "n_gpus": world,

@@ -58,6 +58,17 @@ __device__ __forceinline__ float ex2_ftz(float x) {
   return y;
 }
 
+// Two fp32 values rounded to fp16 (round to nearest even, magnitudes past
+// 65504 saturate to it) in one 32-bit word, `lo` in the low half.
+__device__ __forceinline__ uint32_t pack_f16x2_sat(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+__device__ __forceinline__ float2 unpack_f16x2(uint32_t v) {
+  return __half22float2(*reinterpret_cast<const __half2*>(&v));
+}
+
 // Multi-token decode ("The Architecture of Memory", "Speculative Decoding"
 // and "Tree Attention Verification": the new tokens see the history and the
 // new tokens before them).  Row h of head group g is query token

@@ -25,9 +25,10 @@
 //       CTA's columns.  Q_r's latent part sits in tensor memory (A operand
 //       from TMEM, loaded once per segment), its RoPE part in shared memory;
 //       C_r is the sub-tile's boxes read K-major.
-//   exchange: each CTA sends its partial scores to the other through
-//       distributed shared memory (32 KB per sub-tile) and both add the two in
-//       rank order, so both hold the same scores and run the same softmax.
+//   exchange: each CTA sends its partial scores, in log2 units rounded to
+//       fp16, to the other through distributed shared memory (16 KB per
+//       sub-tile); both add the same two fp16 values, so both hold the same
+//       scores and run the same softmax.
 //   softmax: one thread per row; the row's max, exponentials and sum are
 //       thread-local (no cross-thread reduction).  P is written back into
 //       tensor memory over the row's scores.
@@ -44,15 +45,16 @@
 //     s[h][t]  = scale * s_t * (q_h . code_t - zp_t * sum(q_h))
 //     o_lat[h] = (sum_t w_t code_t - sum_t w_t zp_t) / l,  w_t = p_t s_t.
 //
-// Warp roles (256 threads; 384 for 1-byte caches):
+// Warp roles (384 threads; 512 for 1-byte caches):
 //   warp 0       TMA producer: Q's RoPE part per segment; latent boxes 0-1 and
 //                the RoPE box of every sub-tile
 //   warp 1       TMEM allocation; lane 0 issues the QK MMAs
 //   warp 2       PV: lane 0 issues the MMAs; bf16: the warp first clears
 //                the rows past a sequence's end that the last MMA reads
 //   warp 3       TMA producer: latent boxes 2-3 (and 1-byte caches' scales)
-//   warps 4-7    Q latent into TMEM per segment, exchange, softmax, epilogue
-//   warps 8-11   1-byte caches: code expansion
+//   warps 4-11   Q latent into TMEM per segment, exchange, softmax, epilogue:
+//                two threads per row, each with half of the sub-tile's tokens
+//   warps 12-15  1-byte caches: code expansion
 // Every wait is bounded: on timeout the CTA records MLA_ERR_DEVICE_TIMEOUT,
 // drains, frees its tensor memory and returns.
 #include <atomic>
@@ -70,28 +72,47 @@ using namespace dc;
 
 constexpr int kRowsG = 128;                       // query rows per group (MMA M)
 constexpr int kSub = 64;                          // tokens per sub-tile (MMA N of QK, K of PV)
-constexpr int kNumSlots = 4;                      // sub-tile ring
+constexpr int kNumSlots = 5;                      // sub-tile ring
 constexpr uint32_t kLatBox = kSub * 128;          // [64 tokens x 64 latent columns] 16-bit, SW128: 8 KB
 constexpr uint32_t kOffRopeBox = 4 * kLatBox;     // [64 tokens x 32 RoPE columns] 16-bit, SW64: 4 KB
 constexpr uint32_t kOffCodes = 18 * 1024;         // 1-byte: 4 latent code blocks [64 x 64 B], then RoPE codes
 constexpr uint32_t kOffCodeRope = kOffCodes + 4 * 4096;
-constexpr uint32_t kOffScales = 36 * 1024;        // 1-byte: per-token (scale, zero point) or scale
-constexpr uint32_t kXBytes = kRowsG * kSub * 4;   // one sub-tile's partial scores, fp32
+constexpr uint32_t kScaleSlotBytes = 512;         // 1-byte: per-token (scale, zero point) or scale of a sub-tile
+constexpr uint32_t kXBytes = kRowsG * kSub * 2;   // one sub-tile's partial scores, fp16
 constexpr uint32_t kQRopeBytes = kRowsG * 32 * 2; // [128 rows x 32 RoPE columns] 16-bit, SW64
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 constexpr float kRescaleThreshold = 8.f;          // log2 units
 constexpr bool kPrefetchNext = true;              // L2 prefetch of the next sub-tile's boxes
 // tensor memory columns
+// tensor memory columns: Q's 256 latent values (bf16 / fp16 pairs), O_r, S x2
+// (P is written over its sub-tile's scores)
 constexpr uint32_t kColQ = 0, kColO = 128, kColS = 384, kTmemCols = 512;
+constexpr int kSoftWarps = 8;                     // softmax warps: two threads per row
+
+// OR over the softmax threads (named barrier 1), and their barrier
+__device__ __forceinline__ bool soft_any(bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, 1, %2, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(uint32_t(pred)), "n"(32 * kSoftWarps)
+      : "memory");
+  return r != 0;
+}
+__device__ __forceinline__ void soft_sync() { asm volatile("bar.sync 1, %0;" ::"n"(32 * kSoftWarps) : "memory"); }
 
 template <bool kByte>
 struct HmCfg {
-  static constexpr int kThreads = kByte ? 384 : 256;
-  static constexpr uint32_t kSlotBytes = kByte ? 37 * 1024 : 36 * 1024;
+  static constexpr int kThreads = 128 + 32 * kSoftWarps + (kByte ? 128 : 0);
+  static constexpr uint32_t kSlotBytes = 36 * 1024;
   static constexpr uint32_t kOffQRope = kNumSlots * kSlotBytes;
   static constexpr uint32_t kOffX = kOffQRope + kQRopeBytes;  // [2] partial-score buffers from the peer
-  static constexpr uint32_t kOffMisc = kOffX + 2 * kXBytes;
-  static constexpr uint32_t kSmem = kOffMisc + 1024 + 1024;   // + barriers, + base alignment slack
+  static constexpr uint32_t kOffScl = kOffX + 2 * kXBytes;    // 1-byte: [kNumSlots] per-token scales
+  static constexpr uint32_t kOffMisc = kOffScl + (kByte ? kNumSlots * kScaleSlotBytes : 0);
+  static constexpr uint32_t kSmem = kOffMisc + 512 + 2048 + 1024;  // + barriers, row maxima, alignment slack
   static_assert(kSmem <= 232448, "dynamic shared memory of one CTA");
   static_assert(kOffQRope % 1024 == 0 && kSlotBytes % 1024 == 0, "swizzle atoms");
 };
@@ -193,17 +214,17 @@ __global__ void __launch_bounds__(HmCfg<kCode != kCodeBf16>::kThreads, 1)
       mbar_init(&B->landed[i], 2);
       mbar_init(&B->empty[i], 1);
     }
-    mbar_init(&B->q_full, 1 + 128);  // the RoPE part's TMA, and the 128 rows' latent parts
+    mbar_init(&B->q_full, 1 + 32 * kSoftWarps);  // the RoPE part's TMA, and the rows' latent parts
     mbar_init(&B->q_empty, 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&B->s_full[i], 1);
       mbar_init(&B->x_full[i], 1);  // armed by one local thread; the peer's bytes complete it
-      mbar_init(&B->p_full[i], 128);
+      mbar_init(&B->p_full[i], 32 * kSoftWarps);
       mbar_init(&B->pv_done[i], 1);
       mbar_init(&B->drain[i], 1);
     }
     mbar_init(&B->o_full, 1);
-    mbar_init(&B->o_free, 128);
+    mbar_init(&B->o_free, 32 * kSoftWarps);
     B->abort = 0;
     fence_mbar_init();
     prefetch_tensormap(&tmap_lat);
@@ -294,8 +315,8 @@ __global__ void __launch_bounds__(HmCfg<kCode != kCodeBf16>::kThreads, 1)
           if (role == 0)
             tma_load_2d(base + kOffCodeRope + i * box_rows * 32, &tmap_rope, rope0, rows[i], &B->landed[slot]);
           else
-            bulk_copy_g2s(base + kOffScales + i * box_rows * sbytes, p.scale_zero + size_t(rows[i]) * (kZp ? 2 : 1),
-                          box_rows * sbytes, &B->landed[slot]);
+            bulk_copy_g2s(smem + C::kOffScl + slot * kScaleSlotBytes + i * box_rows * sbytes,
+                          p.scale_zero + size_t(rows[i]) * (kZp ? 2 : 1), box_rows * sbytes, &B->landed[slot]);
         }
       }
       ++k;
@@ -391,7 +412,7 @@ __global__ void __launch_bounds__(HmCfg<kCode != kCodeBf16>::kThreads, 1)
       mma_commit(&B->drain[1]);
       mbar_wait(&B->drain[1], 0, abort_flag, kWaitLimitNs);
     }
-  } else if (kByte && warp >= 8) {
+  } else if (kByte && warp >= 4 + kSoftWarps) {
     if constexpr (kByte) {
       // ------------------------------------------------------------ code expansion
       // Each landed sub-tile's codes become fp16 operand boxes in the same
@@ -400,7 +421,7 @@ __global__ void __launch_bounds__(HmCfg<kCode != kCodeBf16>::kThreads, 1)
       // all of its codes before any thread writes.  Rows at and past the
       // sequence's end are written as zeros (PV reads them with zero weight,
       // and a code there is whatever the page's tail holds).
-      const int ct = threadIdx.x - 256;
+      const int ct = threadIdx.x - 128 - 32 * kSoftWarps;
       SubWalker walk;
       walk.init(p, S, pa, pb);
       uint32_t k = 0;
@@ -453,103 +474,155 @@ __global__ void __launch_bounds__(HmCfg<kCode != kCodeBf16>::kThreads, 1)
       }
       if (!ok) fail(B, p.status);
     }
-  } else if (warp >= 4 && warp < 8) {
+  } else if (warp >= 4 && warp < 4 + kSoftWarps) {
     // ------------------------------------------------------------ Q, exchange, softmax, epilogue
-    const int q4 = warp - 4, h = threadIdx.x - 128;  // h: row of the group = TMEM lane
+    // Two threads per row: warp 4 + 4c + q covers rows [32 q, 32 q + 32) (its
+    // TMEM lane quarter) and the sub-tile's tokens [32 c, 32 c + 32); the
+    // pair of threads of a row combine their maxima (and, at the end, their
+    // sums) through shared memory.
+    const int sw = warp - 4, q4 = sw & 3, c = sw >> 2, tid = threadIdx.x - 128;
+    const int h = 32 * q4 + lane;                     // row of the group = TMEM lane
     const uint32_t lane_off = uint32_t(q4 * 32) << 16;
     const int row = g * kRowsG + h;                   // row within the sequence's rows
-    const uint32_t x_local = sbase + C::kOffX + h * (kSub * 4);
-    const int xr_rot = h & 15;                        // 16-byte pieces rotated by row to spread banks
+    const uint32_t x_local = sbase + C::kOffX + h * (kSub * 2) + c * kSub;  // this thread's half of its row
+    const int xr_rot = h & 3;                         // 16-byte pieces rotated by row to spread banks
     const uint32_t peer = rank ^ 1u;
+    // [2 sub-tile parities][2 halves][128] partial row maxima
+    float* red = reinterpret_cast<float*>(smem + C::kOffMisc + 512);
     SubWalker walk;
     walk.init(p, S, pa, pb);
     float m_run = 0.f, l_run = 0.f, corr = 0.f, qsum = 0.f;
     uint32_t k = 0, seg = 0;
-    SubTile s;
-    while (walk.next(s)) {
-      const uint32_t sb = k & 1, slot = k % kNumSlots;
-      if (s.first) {
-        // Q's latent part for this segment's sequence into TMEM.  Every QK
-        // MMA of the previous segment has completed: this thread saw the
-        // s_full of its last sub-tile.
-        const uint4* src = reinterpret_cast<const uint4*>(p.q_full + (size_t(s.b) * p.heads + row) * kRow + lat0);
+    // Q's latent part for a segment's sequence into TMEM: this thread's 128
+    // of the row's 256 latent values.  Every QK MMA of the previous segment
+    // has completed: this thread saw the s_full of its last sub-tile.
+    auto load_q = [&](const SubTile& t) {
+      const uint4* src =
+          reinterpret_cast<const uint4*>(p.q_full + (size_t(t.b) * p.heads + row) * kRow + lat0 + 128 * c);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t r[32];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const uint4 v = __ldg(src + 8 * c + i);
-            r[4 * i] = v.x; r[4 * i + 1] = v.y; r[4 * i + 2] = v.z; r[4 * i + 3] = v.w;
-          }
-          tmem_st32(tmem + lane_off + kColQ + 32 * c, r);
-        }
-        tmem_st_wait();
-        if (kZp) {
-          const float* qs = p.q_sum + (size_t(s.b) * p.heads + row) * kQSumParts;
-          float t = qs[0];
-#pragma unroll
-          for (int c = 1; c < kQSumParts; ++c) t += qs[c];
-          qsum = t;
-        }
-        tc_fence_before();
-        mbar_arrive(&B->q_full);
-      }
-      bool ok = mbar_wait(&B->s_full[sb], (k >> 1) & 1, abort_flag, kWaitLimitNs);
-      if (bar_any(!ok)) break;
-      tc_fence_after();
-      float x[kSub];
-      {
+      for (int j = 0; j < 2; ++j) {
         uint32_t r[32];
-        tmem_ld32(tmem + lane_off + kColS + sb * kSub, r);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) x[i] = __uint_as_float(r[i]);
-        tmem_ld32(tmem + lane_off + kColS + sb * kSub + 32, r);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) x[32 + i] = __uint_as_float(r[i]);
-      }
-      // partial scores to the peer, into its buffer sb
-      {
-        const uint32_t rbar = mapa_shared(smem_u32(&B->x_full[sb]), peer);
-        const uint32_t xr = mapa_shared(x_local + sb * kXBytes, peer);
-#pragma unroll
-        for (int v = 0; v < kSub / 4; ++v)
-          st_async_v4(xr + (v ^ xr_rot) * 16, x[4 * v], x[4 * v + 1], x[4 * v + 2], x[4 * v + 3], rbar);
-      }
-      if (h == 0) mbar_arrive_expect_tx(&B->x_full[sb], kXBytes);
-      ok = mbar_wait_cluster(&B->x_full[sb], (k >> 1) & 1, abort_flag, kWaitLimitNs);
-      if (kByte && ok) ok = mbar_wait(&B->landed[slot], (k / kNumSlots) & 1, abort_flag, kWaitLimitNs);
-      if (bar_any(!ok)) break;
-      // S = S_0 + S_1 (addition is commutative: both CTAs get the same bits)
-#pragma unroll
-      for (int v = 0; v < kSub / 4; ++v) {
-        const float4 y = *reinterpret_cast<const float4*>(smem + C::kOffX + sb * kXBytes + h * (kSub * 4) +
-                                                          (v ^ xr_rot) * 16);
-        x[4 * v] += y.x; x[4 * v + 1] += y.y; x[4 * v + 2] += y.z; x[4 * v + 3] += y.w;
-      }
-      const float* sc = reinterpret_cast<const float*>(smem + slot * C::kSlotBytes + kOffScales);
-      // scores in log2 units; tokens past the sub-tile's end (and, for
-      // multi-token rows, positions after the row's own) are -inf
-      const int qpos = kCausal ? walk.len() - p.q_len + row / p.heads_w : 0x7fffffff;
-#pragma unroll
-      for (int t = 0; t < kSub; ++t) {
-        bool vis = t < s.valid;
-        if (kCausal) vis = vis && s.tok0 + t <= qpos;
-        float v = x[t];
-        if constexpr (kByte) {
-          const float ts = kZp ? sc[2 * t] : sc[t];
-          if constexpr (kZp) v = fmaf(-sc[2 * t + 1], qsum, v);
-          v = v * (p.scale_log2 * ts);
-        } else {
-          v = v * p.scale_log2;
+        for (int i = 0; i < 8; ++i) {
+          const uint4 v = __ldg(src + 8 * j + i);
+          r[4 * i] = v.x; r[4 * i + 1] = v.y; r[4 * i + 2] = v.z; r[4 * i + 3] = v.w;
         }
-        x[t] = vis ? v : -INFINITY;
+        tmem_st32(tmem + lane_off + kColQ + 64 * c + 32 * j, r);
       }
-      float mt = x[0];
+      tmem_st_wait();
+      if (kZp) {
+        const float* qs = p.q_sum + (size_t(t.b) * p.heads + row) * kQSumParts;
+        float v = qs[0];
 #pragma unroll
-      for (int t = 1; t < kSub; ++t) mt = fmaxf(mt, x[t]);
+        for (int i = 1; i < kQSumParts; ++i) v += qs[i];
+        qsum = v;
+      }
+      tc_fence_before();
+      mbar_arrive(&B->q_full);
+    };
+    // Sub-tile kk's partial scores, this thread's 32 in log2 units rounded to
+    // fp16, to the peer (into its buffer kk & 1); kept in hx for the sum.
+    // The exchange sends fp16 (distributed shared memory moves only ~12-15
+    // GB/s per SM here, so its bytes set the pace) and both CTAs add the same
+    // two fp16 values, so both hold the same scores.  It is issued as soon as
+    // the sub-tile's QK is done, before the sub-tile ahead of it is
+    // finished, so that the peer's half is there when it is needed.
+    uint32_t hx[16];
+    auto send = [&](uint32_t kk) -> bool {
+      const uint32_t xb = kk & 1;
+      const bool w = mbar_wait(&B->s_full[xb], (kk >> 1) & 1, abort_flag, kWaitLimitNs);
+      if (!w) fail(B, p.status);  // carried to the next barrier; the waits after it return at once
+      tc_fence_after();
+      uint32_t r[32];
+      tmem_ld32(tmem + lane_off + kColS + xb * kSub + 32 * c, r);
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        hx[i] = pack_f16x2_sat(__uint_as_float(r[2 * i]) * p.scale_log2, __uint_as_float(r[2 * i + 1]) * p.scale_log2);
+      const uint32_t rbar = mapa_shared(smem_u32(&B->x_full[xb]), peer);
+      const uint32_t xr = mapa_shared(x_local + xb * kXBytes, peer);
+#pragma unroll
+      for (int v = 0; v < 4; ++v)
+        st_async_v4_b32(xr + (v ^ xr_rot) * 16, hx[4 * v], hx[4 * v + 1], hx[4 * v + 2], hx[4 * v + 3], rbar);
+      if (tid == 0) mbar_arrive_expect_tx(&B->x_full[xb], kXBytes);
+      return w;
+    };
+    SubTile s;
+    bool have = walk.next(s), sent_ok = true;
+    if (have) {
+      if (s.first) load_q(s);
+      sent_ok = send(0);
+    }
+    while (have) {
+      const uint32_t sb = k & 1, slot = k % kNumSlots;
+      // a failed wait is carried to the maxima's barrier below, where all
+      // softmax threads leave together (a named barrier must not be left half-way)
+      bool ok = sent_ok && mbar_wait_cluster(&B->x_full[sb], (k >> 1) & 1, abort_flag, kWaitLimitNs);
+      if (kByte && ok) ok = mbar_wait(&B->landed[slot], (k / kNumSlots) & 1, abort_flag, kWaitLimitNs);
+      if (!ok) fail(B, p.status);
+      // S = S_0 + S_1 (addition is commutative: both CTAs get the same bits)
+      float x[32];
+#pragma unroll
+      for (int v = 0; v < 4; ++v) {
+        const uint4 y = *reinterpret_cast<const uint4*>(smem + C::kOffX + sb * kXBytes + h * (kSub * 2) + c * kSub +
+                                                        (v ^ xr_rot) * 16);
+        const uint32_t yy[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float2 a = unpack_f16x2(hx[4 * v + i]), b = unpack_f16x2(yy[i]);
+          x[8 * v + 2 * i] = a.x + b.x;
+          x[8 * v + 2 * i + 1] = a.y + b.y;
+        }
+      }
+      // scores in log2 units; tokens past the sub-tile's end (and, for
+      // multi-token rows, positions after the row's own) are -inf.  1-byte
+      // caches: the token's zero-point term and scale
+      const int t0 = 32 * c;
+      const int qpos = kCausal ? walk.len() - p.q_len + row / p.heads_w : 0x7fffffff;
+      const float4* sc4 = reinterpret_cast<const float4*>(smem + C::kOffScl + slot * kScaleSlotBytes);
+      const float qsum_l2 = qsum * p.scale_log2;
+      // the token's (scale, zero point) or scale, 4 tokens at a time; tokens
+      // past the end get 0 (their parameters are whatever the page's tail holds)
+      auto scales4 = [&](int t4, float (&ts)[4], float (&tz)[4]) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) { ts[i] = 1.f; tz[i] = 0.f; }
+        if constexpr (kZp) {
+          const float4 a = sc4[(t0 >> 1) + 2 * t4], b = sc4[(t0 >> 1) + 2 * t4 + 1];
+          ts[0] = a.x; tz[0] = a.y; ts[1] = a.z; tz[1] = a.w; ts[2] = b.x; tz[2] = b.y; ts[3] = b.z; tz[3] = b.w;
+        } else if constexpr (kByte) {
+          const float4 a = sc4[(t0 >> 2) + t4];
+          ts[0] = a.x; ts[1] = a.y; ts[2] = a.z; ts[3] = a.w;
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          if (t0 + 4 * t4 + i >= s.valid) { ts[i] = 0.f; tz[i] = 0.f; }
+      };
+      float mt = -INFINITY;
+#pragma unroll
+      for (int t4 = 0; t4 < 8; ++t4) {
+        float ts[4], tz[4];
+        scales4(t4, ts, tz);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int i = 4 * t4 + j, t = t0 + i;
+          bool vis = t < s.valid;
+          if (kCausal) vis = vis && s.tok0 + t <= qpos;
+          float v = x[i];
+          if constexpr (kZp) v = fmaf(-tz[j], qsum_l2, v);
+          if constexpr (kByte) v *= ts[j];
+          x[i] = vis ? v : -INFINITY;
+          mt = fmaxf(mt, x[i]);
+        }
+      }
+      // the row's max over both halves; the buffer of this parity is written
+      // again two sub-tiles on, after the next sub-tile's barrier, which the
+      // reads below precede
+      red[sb * 256 + c * 128 + h] = mt;
+      if (soft_any(!ok)) break;
+      mt = fmaxf(mt, red[sb * 256 + (c ^ 1) * 128 + h]);
       // running max: it only has to bound the row's scores within
       // kRescaleThreshold; the first sub-tile of a segment sets it, a sub-tile
-      // that breaks the bound raises it and rescales O and l
+      // that breaks the bound raises it and rescales O and l (both threads of
+      // a row take the same decision from the same numbers)
       float alpha = 1.f;
       bool rescale = false;
       if (s.first) {
@@ -564,77 +637,99 @@ __global__ void __launch_bounds__(HmCfg<kCode != kCodeBf16>::kThreads, 1)
         rescale = true;
       }
       if (__any_sync(0xffffffffu, rescale)) {
-        // PV of the previous sub-tile must be complete before O is rescaled
+        // PV of the previous sub-tile must be complete before O is rescaled:
+        // this thread's 128 of the row's 256 columns
         const bool ok3 = mbar_wait(&B->pv_done[(k - 1) & 1], ((k - 1) >> 1) & 1, abort_flag, kWaitLimitNs);
         tc_fence_after();
-        if (__all_sync(0xffffffffu, ok3)) {
+        if (__all_sync(0xffffffffu, ok3) && !*abort_flag) {
 #pragma unroll 1
-          for (int c = 0; c < 8; ++c) {
+          for (int j = 0; j < 4; ++j) {
             uint32_t r[32];
-            tmem_ld32(tmem + lane_off + kColO + 32 * c, r);
+            const uint32_t a = tmem + lane_off + kColO + 128 * c + 32 * j;
+            tmem_ld32(a, r);
 #pragma unroll
             for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-            tmem_st32(tmem + lane_off + kColO + 32 * c, r);
+            tmem_st32(a, r);
           }
           tmem_st_wait();
         } else {
-          ok = false;
+          fail(B, p.status);  // carried to the next sub-tile's barrier
         }
       }
-      if (bar_any(!ok)) break;
-      // probabilities -> P over the scores: bf16 (bf16 caches) or fp16 with
-      // the token's scale folded in (1-byte caches)
+      // probabilities -> P over the scores (this thread's 16 columns): bf16
+      // (bf16 caches) or fp16 with the token's scale folded in (1-byte caches)
       {
-        uint32_t pk[32];
+        uint32_t pk[16];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int ta = 2 * i, tb = ta + 1;
-          const float pa_ = ex2_ftz(x[ta] - m_run), pb_ = ex2_ftz(x[tb] - m_run);
-          if constexpr (kByte) {
-            const float sa = ta < s.valid ? (kZp ? sc[2 * ta] : sc[ta]) : 0.f;
-            const float sbv = tb < s.valid ? (kZp ? sc[2 * tb] : sc[tb]) : 0.f;
-            const __half wa = __float2half_rn(pa_ * sa), wb = __float2half_rn(pb_ * sbv);
-            l_run += pa_ + pb_;
-            if constexpr (kZp) {
-              const float za = ta < s.valid ? sc[2 * ta + 1] : 0.f, zb = tb < s.valid ? sc[2 * tb + 1] : 0.f;
-              corr = fmaf(__half2float(wa), za, corr);
-              corr = fmaf(__half2float(wb), zb, corr);
+        for (int t4 = 0; t4 < 8; ++t4) {
+          float ts[4], tz[4];
+          scales4(t4, ts, tz);
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            const int ta = 4 * t4 + 2 * j, tb = ta + 1;
+            const float pa_ = ex2_ftz(x[ta] - m_run), pb_ = ex2_ftz(x[tb] - m_run);
+            if constexpr (kByte) {
+              const __half wa = __float2half_rn(pa_ * ts[2 * j]), wb = __float2half_rn(pb_ * ts[2 * j + 1]);
+              l_run += pa_ + pb_;
+              if constexpr (kZp) {
+                corr = fmaf(__half2float(wa), tz[2 * j], corr);
+                corr = fmaf(__half2float(wb), tz[2 * j + 1], corr);
+              }
+              pk[2 * t4 + j] = uint32_t(__half_as_ushort(wa)) | (uint32_t(__half_as_ushort(wb)) << 16);
+            } else {
+              const __nv_bfloat16 wa = __float2bfloat16_rn(pa_), wb = __float2bfloat16_rn(pb_);
+              l_run += __bfloat162float(wa) + __bfloat162float(wb);
+              pk[2 * t4 + j] = uint32_t(__bfloat16_as_ushort(wa)) | (uint32_t(__bfloat16_as_ushort(wb)) << 16);
             }
-            pk[i] = uint32_t(__half_as_ushort(wa)) | (uint32_t(__half_as_ushort(wb)) << 16);
-          } else {
-            const __nv_bfloat16 wa = __float2bfloat16_rn(pa_), wb = __float2bfloat16_rn(pb_);
-            l_run += __bfloat162float(wa) + __bfloat162float(wb);
-            pk[i] = uint32_t(__bfloat16_as_ushort(wa)) | (uint32_t(__bfloat16_as_ushort(wb)) << 16);
           }
         }
-        tmem_st32(tmem + lane_off + kColS + sb * kSub, pk);
+        tmem_st16u(tmem + lane_off + kColS + sb * kSub + 16 * c, pk);
         tmem_st_wait();
       }
       tc_fence_before();
       mbar_arrive(&B->p_full[sb]);
+      SubTile sn;
+      const bool have_next = walk.next(sn);
       if (s.last) {
         const bool ok2 = mbar_wait(&B->o_full, seg & 1, abort_flag, kWaitLimitNs);
-        if (bar_any(!ok2)) break;
+        // the row's sum (and INT8 zero-point term) over both halves, added in a fixed order
+        // the sums go through this sub-tile's exchange buffer, which every
+        // thread has read (before the maxima's barrier) and the peer refills
+        // only after this CTA's next send
+        float* rl = reinterpret_cast<float*>(smem + C::kOffX + sb * kXBytes);
+        rl[c * 128 + h] = l_run;
+        if (kZp) rl[256 + c * 128 + h] = corr;
+        if (soft_any(!ok2)) break;
+        const float l_row = rl[h] + rl[128 + h];
+        const float corr_row = kZp ? rl[256 + h] + rl[256 + 128 + h] : 0.f;
         tc_fence_after();
-        const float inv_l = l_run > 0.f ? __frcp_rn(l_run) : 0.f;  // 0: a row that saw no token
-        float4* dst = reinterpret_cast<float4*>(p.partial_o + (size_t(s.seg) * p.heads + row) * kLatent + lat0);
+        const float inv_l = l_row > 0.f ? __frcp_rn(l_row) : 0.f;  // 0: a row that saw no token
+        float4* dst =
+            reinterpret_cast<float4*>(p.partial_o + (size_t(s.seg) * p.heads + row) * kLatent + lat0 + 128 * c);
 #pragma unroll 1
-        for (int c = 0; c < 8; ++c) {
+        for (int j = 0; j < 4; ++j) {
           uint32_t r[32];
-          tmem_ld32(tmem + lane_off + kColO + 32 * c, r);
+          tmem_ld32(tmem + lane_off + kColO + 128 * c + 32 * j, r);
 #pragma unroll
           for (int i = 0; i < 8; ++i)
-            dst[8 * c + i] = make_float4((__uint_as_float(r[4 * i]) - corr) * inv_l,
-                                         (__uint_as_float(r[4 * i + 1]) - corr) * inv_l,
-                                         (__uint_as_float(r[4 * i + 2]) - corr) * inv_l,
-                                         (__uint_as_float(r[4 * i + 3]) - corr) * inv_l);
+            dst[8 * j + i] = make_float4((__uint_as_float(r[4 * i]) - corr_row) * inv_l,
+                                         (__uint_as_float(r[4 * i + 1]) - corr_row) * inv_l,
+                                         (__uint_as_float(r[4 * i + 2]) - corr_row) * inv_l,
+                                         (__uint_as_float(r[4 * i + 3]) - corr_row) * inv_l);
         }
         tc_fence_before();
         mbar_arrive(&B->o_free);
-        if (rank == 0)
-          p.partial_lse[size_t(s.seg) * p.heads + row] = l_run > 0.f ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
+        if (rank == 0 && c == 0)
+          p.partial_lse[size_t(s.seg) * p.heads + row] = l_row > 0.f ? (m_run + log2f(l_row)) * kLn2 : -INFINITY;
+        soft_sync();  // the sums are read before the next segment's epilogue rewrites them
         ++seg;
       }
+      if (have_next) {
+        if (sn.first) load_q(sn);
+        sent_ok = send(k + 1);
+      }
+      s = sn;
+      have = have_next;
       ++k;
     }
   }
