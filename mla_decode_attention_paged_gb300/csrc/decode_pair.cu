@@ -79,7 +79,7 @@ struct PairCfg {
   static constexpr int kBoxesPerProducer = 2;       // the two producers load one chunk (two boxes) each
   static constexpr uint32_t kQBytes = kChunks * 2 * HC * 128 + HC * kRopeCols * 2;
   static constexpr uint32_t kPBytes = kTile * HC * 2;  // P^T, bf16
-  static constexpr uint32_t kXBytes = kTile * HC * 4;  // one other CTA's partial S^T, fp32
+  static constexpr uint32_t kXBytes = kTile * HC * 2;  // the other CTA's partial S^T, fp16
   static constexpr uint32_t kOffPair = 0;
   static constexpr uint32_t kOffRope = kOffPair + kNumPair * kPairBytes;
   static constexpr uint32_t kOffQ = kOffRope + ((kNumRope * kRopeBytes + 1023) & ~1023u);
@@ -368,8 +368,8 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     const int q4 = warp - 4, st = threadIdx.x - 128;  // st = token row of S^T = TMEM lane
     const uint32_t lane_off = uint32_t(q4 * 32) << 16;
     // this thread's row of an exchange buffer; 16-byte pieces rotated by row to spread banks
-    constexpr int kV4 = HC / 4;
-    const uint32_t x_local = sbase + C::kOffX + st * HC * 4;
+    constexpr int kV4 = HC / 8;
+    const uint32_t x_local = sbase + C::kOffX + st * HC * 2;
     TileWalkerT<true> walk;
     walk.init(p.tile_start, p.seg_base, p.len, p.batch, int(S), pa, pb);
     float m_run[HC], l_run[HC];
@@ -384,12 +384,17 @@ __global__ void __launch_bounds__(kPairThreads, 1)
       tc_fence_after();
       float x[HC];
       if (ok) {
+        // this CTA's partial scores in log2 units, rounded to fp16: the
+        // exchange sends fp16 (distributed shared memory moves only ~12-15
+        // GB/s per SM here) and both CTAs add the same two fp16 values, so
+        // both get the same bits
+        uint32_t hx[HC / 2];
 #pragma unroll
         for (int h0 = 0; h0 < HC; h0 += 16) {
           float v[16];
           tmem_ld16(tmem + lane_off + C::kColS + buf * HC + h0, v);
 #pragma unroll
-          for (int i = 0; i < 16; ++i) x[h0 + i] = v[i];
+          for (int i = 0; i < 8; ++i) hx[h0 / 2 + i] = pack_f16x2_sat(v[2 * i] * p.scale_log2, v[2 * i + 1] * p.scale_log2);
         }
         // partial scores to the peer CTA, into its buffer `buf`
         {
@@ -398,24 +403,28 @@ __global__ void __launch_bounds__(kPairThreads, 1)
           const uint32_t xr = mapa_shared(x_local + buf * C::kXBytes, peer);
 #pragma unroll
           for (int v = 0; v < kV4; ++v)
-            st_async_v4(xr + (v ^ (st % kV4)) * 16, x[4 * v], x[4 * v + 1], x[4 * v + 2], x[4 * v + 3], rbar);
+            st_async_v4_b32(xr + (v ^ (st % kV4)) * 16, hx[4 * v], hx[4 * v + 1], hx[4 * v + 2], hx[4 * v + 3], rbar);
         }
         if (st == 0) mbar_arrive_expect_tx(&B->x_full[buf], C::kXBytes);
         ok = mbar_wait_cluster(&B->x_full[buf], (tile_i >> 1) & 1, abort_flag, kWaitLimitNs);
         if (ok) {
-          // S = S_0 + S_1 in rank order, so that both CTAs get the same bits
+          // S = S_0 + S_1 (addition is commutative: both CTAs get the same bits)
 #pragma unroll
           for (int v = 0; v < kV4; ++v) {
-            const float4 y = *reinterpret_cast<const float4*>(smem + C::kOffX + buf * C::kXBytes + st * HC * 4 +
-                                                              (v ^ (st % kV4)) * 16);
-            const float4 own = make_float4(x[4 * v], x[4 * v + 1], x[4 * v + 2], x[4 * v + 3]);
-            const float4 s0 = rank == 0 ? own : y, s1 = rank == 0 ? y : own;
-            x[4 * v] = s0.x + s1.x; x[4 * v + 1] = s0.y + s1.y; x[4 * v + 2] = s0.z + s1.z; x[4 * v + 3] = s0.w + s1.w;
+            const uint4 y = *reinterpret_cast<const uint4*>(smem + C::kOffX + buf * C::kXBytes + st * HC * 2 +
+                                                            (v ^ (st % kV4)) * 16);
+            const uint32_t yy[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const float2 a = unpack_f16x2(hx[4 * v + i]), b = unpack_f16x2(yy[i]);
+              x[8 * v + 2 * i] = a.x + b.x;
+              x[8 * v + 2 * i + 1] = a.y + b.y;
+            }
           }
         }
       }
 #pragma unroll
-      for (int h = 0; h < HC; ++h) x[h] = valid ? x[h] * p.scale_log2 : -INFINITY;
+      for (int h = 0; h < HC; ++h) x[h] = valid ? x[h] : -INFINITY;
       if (kCausal && causal_tile(p, t, walk.len_b)) causal_mask<HC>(x, p, g, walk.len_b, t.tile * kTile + st);
       // Running max: it only has to bound the scores to within
       // kRescaleThreshold (log2 units).  The first tile of a segment, and a
