@@ -1,8 +1,7 @@
-"""The single-CTA attention kernel for bf16 caches: the fallback for devices
-on which the CTA-pair kernel cannot be placed.  GB300 always places the
-pairs, so the test hook mla_test_force_single_cta routes bf16 decodes to the
-fallback and these cases check it against the fp64 oracle, and against the
-pair kernel within the tolerance."""
+"""The single-CTA attention kernel: the fallback for devices on which the
+CTA-pair kernels cannot be placed.  GB300 always places the pairs, so the
+test hook mla_test_force_single_cta routes decodes (bf16, INT8 and FP8
+caches) to the fallback and these cases check it against the fp64 oracle."""
 import pytest
 import torch
 
@@ -31,3 +30,8 @@ def test_single_cta_bf16_parity(single_cta, heads, P, lens):
 @pytest.mark.parametrize("splits", [1, 7, 300])
 def test_single_cta_bf16_splits(single_cta, splits):
     _run_small(*_small(lens=(1000, 5, 2500, 128), seed=splits), num_splits=splits)
+
+
+@pytest.mark.parametrize("fmt", ["int8", "fp8"])
+def test_single_cta_one_byte_parity(single_cta, fmt):
+    _run_small(*_small(lens=(1, 129, 700, 2000), int8=fmt == "int8", fp8=fmt == "fp8", seed=77))
