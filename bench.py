@@ -43,7 +43,18 @@ def parse():
     ap.add_argument("--num-splits", type=int, default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--batch", type=int, default=None,
+                    help="run the workload with this many sequences instead (small cases for profiler captures)")
     return ap.parse_args()
+
+
+def pick_workload(args):
+    """The named workload, or (--batch) the same workload with another number of sequences."""
+    from mla_decode_attention_paged_gb300 import workloads as W
+    w = W.WORKLOADS[args.workload]
+    if args.batch is not None and args.batch != w.batch:
+        w = w.scaled(batch=args.batch, name=f"{w.name}@batch{args.batch}")
+    return w
 
 
 def dist_setup(n):
@@ -388,7 +399,7 @@ def run_ours(args, rank, world):
 
     dev = torch.device("cuda", torch.cuda.current_device())
     mla.load_library(build_if_missing=True)
-    w = W.WORKLOADS[args.workload]
+    w = pick_workload(args)
     inp = W.make_decode_inputs(w, device=dev)
     d = mla.dims(w.heads, w.page_size, int8=w.int8, fp8=w.fp8)
     B, H, T = w.batch, w.heads, (w.chunk or w.q_len)
@@ -651,7 +662,7 @@ def run_reference(args, rank, world):
     from mla_decode_attention_paged_gb300 import workloads as W
     if rank != 0:
         return None
-    w = W.WORKLOADS[args.workload]
+    w = pick_workload(args)
     dev = "cuda" if torch.cuda.is_available() else "cpu"
     inp = W.make_decode_inputs(w.scaled(batch=min(w.batch, 4)) if w.quantised else w, device=dev)
     inp["cache_dev"], inp["sz_dev"] = inp.get("cache"), None
