@@ -183,6 +183,21 @@ __device__ __forceinline__ void expand_e4m3(uint4 v, uint4& lo, uint4& hi) {
   hi = make_uint4(o[4], o[5], o[6], o[7]);
 }
 
+// Dequantisation of 16 expanded codes (8 fp16 pairs equal to the codes'
+// values) in place: each becomes code * scale + nzs (nzs = -zero point x
+// scale; 0 for FP8), evaluated with one fp32 fused multiply-add and rounded
+// once to fp16 (magnitudes past 65504 saturate to it).
+__device__ __forceinline__ uint32_t dequant_half2(uint32_t codes, float scale, float nzs) {
+  const float2 f = unpack_f16x2(codes);
+  return pack_f16x2_sat(fmaf(f.x, scale, nzs), fmaf(f.y, scale, nzs));
+}
+__device__ __forceinline__ void dequant16(uint4& lo, uint4& hi, float scale, float nzs) {
+  lo = make_uint4(dequant_half2(lo.x, scale, nzs), dequant_half2(lo.y, scale, nzs), dequant_half2(lo.z, scale, nzs),
+                  dequant_half2(lo.w, scale, nzs));
+  hi = make_uint4(dequant_half2(hi.x, scale, nzs), dequant_half2(hi.y, scale, nzs), dequant_half2(hi.z, scale, nzs),
+                  dequant_half2(hi.w, scale, nzs));
+}
+
 // ----- host side: tensor maps ----------------------------------------------
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,

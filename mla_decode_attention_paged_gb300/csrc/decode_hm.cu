@@ -38,12 +38,11 @@
 // Tensor memory (512 columns): Q latent 128, O_r 256, two score buffers of 64.
 //
 // 1-byte caches (INT8, FP8): the codes land by TMA in the back of each slot
-// and four warps expand them into fp16 operand boxes (exact, as in
-// decode_tc.cu); Q is fp16; the per-token scale (and INT8 zero point) is
-// applied to the scores and folded into P, with the zero-point term of the
-// output subtracted in the epilogue:
-//     s[h][t]  = scale * s_t * (q_h . code_t - zp_t * sum(q_h))
-//     o_lat[h] = (sum_t w_t code_t - sum_t w_t zp_t) / l,  w_t = p_t s_t.
+// and four warps turn them into fp16 operand boxes of the dequantised values
+// ("KV Cache Optimization", section 3: x = s_t (code - zp_t), INT8; x = s_t
+// e4m3(code), FP8), each computed in fp32 and rounded once to fp16.  Q and P
+// are fp16, and from there the sub-tile runs exactly as for a bf16 cache: the
+// scale and zero point never reach the softmax.
 //
 // Warp roles (384 threads; 512 for 1-byte caches):
 //   warp 0       TMA producer: Q's RoPE part per segment; latent boxes 0-1 and
@@ -54,7 +53,7 @@
 //   warp 3       TMA producer: latent boxes 2-3 (and 1-byte caches' scales)
 //   warps 4-11   Q latent into TMEM per segment, exchange, softmax, epilogue:
 //                two threads per row, each with half of the sub-tile's tokens
-//   warps 12-15  1-byte caches: code expansion
+//   warps 12-15  1-byte caches: code expansion and dequantisation
 // Every wait is bounded: on timeout the CTA records MLA_ERR_DEVICE_TIMEOUT,
 // drains, frees its tensor memory and returns.
 #include <atomic>
@@ -415,13 +414,16 @@ __global__ void __launch_bounds__(HmCfg<kCode != kCodeBf16>::kThreads, 1)
   } else if (kByte && warp >= 4 + kSoftWarps) {
     if constexpr (kByte) {
       // ------------------------------------------------------------ code expansion
-      // Each landed sub-tile's codes become fp16 operand boxes in the same
-      // slot: latent block q -> SW128 box q, RoPE codes -> the SW64 box.  The
-      // codes sit where boxes 2-3 and the RoPE box go, so every thread reads
-      // all of its codes before any thread writes.  Rows at and past the
-      // sequence's end are written as zeros (PV reads them with zero weight,
-      // and a code there is whatever the page's tail holds).
+      // Each landed sub-tile's codes become fp16 operand boxes of the
+      // dequantised values in the same slot: latent block q -> SW128 box q,
+      // RoPE codes -> the SW64 box.  A thread covers tokens ct / 4 and
+      // ct / 4 + 32 (latent) and ct / 2 (RoPE).  The codes sit where boxes 2-3
+      // and the RoPE box go, so every thread reads all of its codes before
+      // any thread writes.  Rows at and past the sequence's end are written
+      // as zeros (PV reads them with zero weight, and a code or scale there is
+      // whatever the page's tail holds).
       const int ct = threadIdx.x - 128 - 32 * kSoftWarps;
+      const int ra = ct >> 2, rr = ct >> 1;
       SubWalker walk;
       walk.init(p, S, pa, pb);
       uint32_t k = 0;
@@ -438,7 +440,23 @@ __global__ void __launch_bounds__(HmCfg<kCode != kCodeBf16>::kThreads, 1)
             const int c = ct + 128 * i, q = c >> 8, r = (c >> 2) & 63, ch = c & 3;
             v[i] = *reinterpret_cast<const uint4*>(base + kOffCodes + q * 4096 + r * 64 + ch * 16);
           }
-          v[8] = *reinterpret_cast<const uint4*>(base + kOffCodeRope + (ct >> 1) * 32 + (ct & 1) * 16);
+          v[8] = *reinterpret_cast<const uint4*>(base + kOffCodeRope + rr * 32 + (ct & 1) * 16);
+        }
+        // the three tokens' scale and -zero point x scale (FP8: no zero point)
+        float sc[3] = {0.f, 0.f, 0.f}, nz[3] = {0.f, 0.f, 0.f};
+        if (landed) {
+          const float* scl = reinterpret_cast<const float*>(smem + C::kOffScl + slot * kScaleSlotBytes);
+          const int rows3[3] = {ra, ra + 32, rr};
+#pragma unroll
+          for (int j = 0; j < 3; ++j) {
+            if constexpr (kZp) {
+              const float2 a = reinterpret_cast<const float2*>(scl)[rows3[j]];
+              sc[j] = a.x;
+              nz[j] = -a.y * a.x;
+            } else {
+              sc[j] = scl[rows3[j]];
+            }
+          }
         }
         if (converters_any(!landed)) {  // also: all codes read before any write
           ok = false;
@@ -451,17 +469,19 @@ __global__ void __launch_bounds__(HmCfg<kCode != kCodeBf16>::kThreads, 1)
           if (r < s.valid) {
             if constexpr (kZp) expand_codes(v[i], lo, hi);
             else expand_e4m3(v[i], lo, hi);
+            dequant16(lo, hi, sc[i & 1], nz[i & 1]);
           }
           uint8_t* row = base + q * kLatBox + r * 128;
           *reinterpret_cast<uint4*>(row + (((2 * ch) ^ (r & 7)) << 4)) = lo;
           *reinterpret_cast<uint4*>(row + (((2 * ch + 1) ^ (r & 7)) << 4)) = hi;
         }
         {
-          const int r = ct >> 1, ch = ct & 1;
+          const int r = rr, ch = ct & 1;
           uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
           if (r < s.valid) {
             if constexpr (kZp) expand_codes(v[8], lo, hi);
             else expand_e4m3(v[8], lo, hi);
+            dequant16(lo, hi, sc[2], nz[2]);
           }
           uint8_t* row = base + kOffRopeBox + r * 64;  // 64-byte rows, 64-byte swizzle
           *reinterpret_cast<uint4*>(row + (((2 * ch) ^ ((r >> 1) & 3)) << 4)) = lo;
@@ -487,11 +507,12 @@ __global__ void __launch_bounds__(HmCfg<kCode != kCodeBf16>::kThreads, 1)
     const uint32_t x_local = sbase + C::kOffX + h * (kSub * 2) + c * kSub;  // this thread's half of its row
     const int xr_rot = h & 3;                         // 16-byte pieces rotated by row to spread banks
     const uint32_t peer = rank ^ 1u;
-    // [2 sub-tile parities][2 halves][128] partial row maxima
+    // [2 sub-tile parities][2 halves][128] partial row maxima; at a segment's
+    // end the other parity's half carries the rows' partial sums
     float* red = reinterpret_cast<float*>(smem + C::kOffMisc + 512);
     SubWalker walk;
     walk.init(p, S, pa, pb);
-    float m_run = 0.f, l_run = 0.f, corr = 0.f, qsum = 0.f;
+    float m_run = 0.f, l_run = 0.f;
     uint32_t k = 0, seg = 0;
     // Q's latent part for a segment's sequence into TMEM: this thread's 128
     // of the row's 256 latent values.  Every QK MMA of the previous segment
@@ -510,13 +531,6 @@ __global__ void __launch_bounds__(HmCfg<kCode != kCodeBf16>::kThreads, 1)
         tmem_st32(tmem + lane_off + kColQ + 64 * c + 32 * j, r);
       }
       tmem_st_wait();
-      if (kZp) {
-        const float* qs = p.q_sum + (size_t(t.b) * p.heads + row) * kQSumParts;
-        float v = qs[0];
-#pragma unroll
-        for (int i = 1; i < kQSumParts; ++i) v += qs[i];
-        qsum = v;
-      }
       tc_fence_before();
       mbar_arrive(&B->q_full);
     };
@@ -525,8 +539,11 @@ __global__ void __launch_bounds__(HmCfg<kCode != kCodeBf16>::kThreads, 1)
     // The exchange sends fp16 (distributed shared memory moves only ~12-15
     // GB/s per SM here, so its bytes set the pace) and both CTAs add the same
     // two fp16 values, so both hold the same scores.  It is issued as soon as
-    // the sub-tile's QK is done, before the sub-tile ahead of it is
-    // finished, so that the peer's half is there when it is needed.
+    // the sub-tile before has its probabilities in P (and, at a segment's
+    // end, its output written).  Issuing it earlier, right after the row
+    // maxima, measured slower: the wait for the next sub-tile's scores then
+    // holds back this sub-tile's P, and with it the PV that frees the score
+    // buffer for the QK after.
     uint32_t hx[16];
     auto send = [&](uint32_t kk) -> bool {
       const uint32_t xb = kk & 1;
@@ -553,14 +570,18 @@ __global__ void __launch_bounds__(HmCfg<kCode != kCodeBf16>::kThreads, 1)
       sent_ok = send(0);
     }
     while (have) {
-      const uint32_t sb = k & 1, slot = k % kNumSlots;
+      const uint32_t sb = k & 1;
       // a failed wait is carried to the maxima's barrier below, where all
       // softmax threads leave together (a named barrier must not be left half-way)
       bool ok = sent_ok && mbar_wait_cluster(&B->x_full[sb], (k >> 1) & 1, abort_flag, kWaitLimitNs);
-      if (kByte && ok) ok = mbar_wait(&B->landed[slot], (k / kNumSlots) & 1, abort_flag, kWaitLimitNs);
       if (!ok) fail(B, p.status);
-      // S = S_0 + S_1 (addition is commutative: both CTAs get the same bits)
+      // S = S_0 + S_1 (addition is commutative: both CTAs get the same bits),
+      // in log2 units; tokens past the sub-tile's end (and, for multi-token
+      // rows, positions after the row's own) are -inf
+      const int t0 = 32 * c;
+      const int qpos = kCausal ? walk.len() - p.q_len + row / p.heads_w : 0x7fffffff;
       float x[32];
+      float mt = -INFINITY;
 #pragma unroll
       for (int v = 0; v < 4; ++v) {
         const uint4 y = *reinterpret_cast<const uint4*>(smem + C::kOffX + sb * kXBytes + h * (kSub * 2) + c * kSub +
@@ -569,48 +590,14 @@ __global__ void __launch_bounds__(HmCfg<kCode != kCodeBf16>::kThreads, 1)
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const float2 a = unpack_f16x2(hx[4 * v + i]), b = unpack_f16x2(yy[i]);
-          x[8 * v + 2 * i] = a.x + b.x;
-          x[8 * v + 2 * i + 1] = a.y + b.y;
-        }
-      }
-      // scores in log2 units; tokens past the sub-tile's end (and, for
-      // multi-token rows, positions after the row's own) are -inf.  1-byte
-      // caches: the token's zero-point term and scale
-      const int t0 = 32 * c;
-      const int qpos = kCausal ? walk.len() - p.q_len + row / p.heads_w : 0x7fffffff;
-      const float4* sc4 = reinterpret_cast<const float4*>(smem + C::kOffScl + slot * kScaleSlotBytes);
-      const float qsum_l2 = qsum * p.scale_log2;
-      // the token's (scale, zero point) or scale, 4 tokens at a time; tokens
-      // past the end get 0 (their parameters are whatever the page's tail holds)
-      auto scales4 = [&](int t4, float (&ts)[4], float (&tz)[4]) {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) { ts[i] = 1.f; tz[i] = 0.f; }
-        if constexpr (kZp) {
-          const float4 a = sc4[(t0 >> 1) + 2 * t4], b = sc4[(t0 >> 1) + 2 * t4 + 1];
-          ts[0] = a.x; tz[0] = a.y; ts[1] = a.z; tz[1] = a.w; ts[2] = b.x; tz[2] = b.y; ts[3] = b.z; tz[3] = b.w;
-        } else if constexpr (kByte) {
-          const float4 a = sc4[(t0 >> 2) + t4];
-          ts[0] = a.x; ts[1] = a.y; ts[2] = a.z; ts[3] = a.w;
-        }
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-          if (t0 + 4 * t4 + i >= s.valid) { ts[i] = 0.f; tz[i] = 0.f; }
-      };
-      float mt = -INFINITY;
-#pragma unroll
-      for (int t4 = 0; t4 < 8; ++t4) {
-        float ts[4], tz[4];
-        scales4(t4, ts, tz);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int i = 4 * t4 + j, t = t0 + i;
-          bool vis = t < s.valid;
-          if (kCausal) vis = vis && s.tok0 + t <= qpos;
-          float v = x[i];
-          if constexpr (kZp) v = fmaf(-tz[j], qsum_l2, v);
-          if constexpr (kByte) v *= ts[j];
-          x[i] = vis ? v : -INFINITY;
-          mt = fmaxf(mt, x[i]);
+          for (int e = 0; e < 2; ++e) {
+            const int j = 8 * v + 2 * i + e, t = t0 + j;
+            bool vis = t < s.valid;
+            if (kCausal) vis = vis && s.tok0 + t <= qpos;
+            x[j] = vis ? (e ? a.y + b.y : a.x + b.x) : -INFINITY;
+            mt = fmaxf(mt, x[j]);
+          }
         }
       }
       // the row's max over both halves; the buffer of this parity is written
@@ -619,6 +606,8 @@ __global__ void __launch_bounds__(HmCfg<kCode != kCodeBf16>::kThreads, 1)
       red[sb * 256 + c * 128 + h] = mt;
       if (soft_any(!ok)) break;
       mt = fmaxf(mt, red[sb * 256 + (c ^ 1) * 128 + h]);
+      SubTile sn;
+      const bool have_next = walk.next(sn);
       // running max: it only has to bound the row's scores within
       // kRescaleThreshold; the first sub-tile of a segment sets it, a sub-tile
       // that breaks the bound raises it and rescales O and l (both threads of
@@ -628,12 +617,10 @@ __global__ void __launch_bounds__(HmCfg<kCode != kCodeBf16>::kThreads, 1)
       if (s.first) {
         m_run = fmaxf(mt, kEmptyRowMax);  // a row masked in the whole sub-tile stays empty
         l_run = 0.f;
-        corr = 0.f;
       } else if (mt > m_run + kRescaleThreshold) {
         alpha = exp2f(m_run - mt);
         m_run = mt;
         l_run *= alpha;
-        corr *= alpha;
         rescale = true;
       }
       if (__any_sync(0xffffffffu, rescale)) {
@@ -657,30 +644,21 @@ __global__ void __launch_bounds__(HmCfg<kCode != kCodeBf16>::kThreads, 1)
         }
       }
       // probabilities -> P over the scores (this thread's 16 columns): bf16
-      // (bf16 caches) or fp16 with the token's scale folded in (1-byte caches)
+      // for bf16 caches, fp16 for the dequantised 1-byte caches; l sums the
+      // rounded values PV multiplies by
       {
         uint32_t pk[16];
 #pragma unroll
-        for (int t4 = 0; t4 < 8; ++t4) {
-          float ts[4], tz[4];
-          scales4(t4, ts, tz);
-#pragma unroll
-          for (int j = 0; j < 2; ++j) {
-            const int ta = 4 * t4 + 2 * j, tb = ta + 1;
-            const float pa_ = ex2_ftz(x[ta] - m_run), pb_ = ex2_ftz(x[tb] - m_run);
-            if constexpr (kByte) {
-              const __half wa = __float2half_rn(pa_ * ts[2 * j]), wb = __float2half_rn(pb_ * ts[2 * j + 1]);
-              l_run += pa_ + pb_;
-              if constexpr (kZp) {
-                corr = fmaf(__half2float(wa), tz[2 * j], corr);
-                corr = fmaf(__half2float(wb), tz[2 * j + 1], corr);
-              }
-              pk[2 * t4 + j] = uint32_t(__half_as_ushort(wa)) | (uint32_t(__half_as_ushort(wb)) << 16);
-            } else {
-              const __nv_bfloat16 wa = __float2bfloat16_rn(pa_), wb = __float2bfloat16_rn(pb_);
-              l_run += __bfloat162float(wa) + __bfloat162float(wb);
-              pk[2 * t4 + j] = uint32_t(__bfloat16_as_ushort(wa)) | (uint32_t(__bfloat16_as_ushort(wb)) << 16);
-            }
+        for (int i = 0; i < 16; ++i) {
+          const float pa_ = ex2_ftz(x[2 * i] - m_run), pb_ = ex2_ftz(x[2 * i + 1] - m_run);
+          if constexpr (kByte) {
+            const __half wa = __float2half_rn(pa_), wb = __float2half_rn(pb_);
+            l_run += __half2float(wa) + __half2float(wb);
+            pk[i] = uint32_t(__half_as_ushort(wa)) | (uint32_t(__half_as_ushort(wb)) << 16);
+          } else {
+            const __nv_bfloat16 wa = __float2bfloat16_rn(pa_), wb = __float2bfloat16_rn(pb_);
+            l_run += __bfloat162float(wa) + __bfloat162float(wb);
+            pk[i] = uint32_t(__bfloat16_as_ushort(wa)) | (uint32_t(__bfloat16_as_ushort(wb)) << 16);
           }
         }
         tmem_st16u(tmem + lane_off + kColS + sb * kSub + 16 * c, pk);
@@ -688,20 +666,15 @@ __global__ void __launch_bounds__(HmCfg<kCode != kCodeBf16>::kThreads, 1)
       }
       tc_fence_before();
       mbar_arrive(&B->p_full[sb]);
-      SubTile sn;
-      const bool have_next = walk.next(sn);
       if (s.last) {
         const bool ok2 = mbar_wait(&B->o_full, seg & 1, abort_flag, kWaitLimitNs);
-        // the row's sum (and INT8 zero-point term) over both halves, added in a fixed order
-        // the sums go through this sub-tile's exchange buffer, which every
-        // thread has read (before the maxima's barrier) and the peer refills
-        // only after this CTA's next send
-        float* rl = reinterpret_cast<float*>(smem + C::kOffX + sb * kXBytes);
+        // the row's sum over both halves, added in a fixed order, through the
+        // other parity's maxima (every thread read them before this
+        // sub-tile's barrier; they are written again after the barrier below)
+        float* rl = red + (sb ^ 1) * 256;
         rl[c * 128 + h] = l_run;
-        if (kZp) rl[256 + c * 128 + h] = corr;
         if (soft_any(!ok2)) break;
         const float l_row = rl[h] + rl[128 + h];
-        const float corr_row = kZp ? rl[256 + h] + rl[256 + 128 + h] : 0.f;
         tc_fence_after();
         const float inv_l = l_row > 0.f ? __frcp_rn(l_row) : 0.f;  // 0: a row that saw no token
         float4* dst =
@@ -712,18 +685,18 @@ __global__ void __launch_bounds__(HmCfg<kCode != kCodeBf16>::kThreads, 1)
           tmem_ld32(tmem + lane_off + kColO + 128 * c + 32 * j, r);
 #pragma unroll
           for (int i = 0; i < 8; ++i)
-            dst[8 * j + i] = make_float4((__uint_as_float(r[4 * i]) - corr_row) * inv_l,
-                                         (__uint_as_float(r[4 * i + 1]) - corr_row) * inv_l,
-                                         (__uint_as_float(r[4 * i + 2]) - corr_row) * inv_l,
-                                         (__uint_as_float(r[4 * i + 3]) - corr_row) * inv_l);
+            dst[8 * j + i] = make_float4(__uint_as_float(r[4 * i]) * inv_l, __uint_as_float(r[4 * i + 1]) * inv_l,
+                                         __uint_as_float(r[4 * i + 2]) * inv_l, __uint_as_float(r[4 * i + 3]) * inv_l);
         }
         tc_fence_before();
         mbar_arrive(&B->o_free);
         if (rank == 0 && c == 0)
           p.partial_lse[size_t(s.seg) * p.heads + row] = l_row > 0.f ? (m_run + log2f(l_row)) * kLn2 : -INFINITY;
-        soft_sync();  // the sums are read before the next segment's epilogue rewrites them
+        soft_sync();  // the sums are read before the next sub-tile writes its maxima there
         ++seg;
       }
+      // the next sub-tile's partial scores to the peer (and, for a new
+      // segment, its Q first: every QK MMA of this segment is complete)
       if (have_next) {
         if (sn.first) load_q(sn);
         sent_ok = send(k + 1);
