@@ -417,11 +417,15 @@ __global__ void __launch_bounds__(HmCfg<kCode != kCodeBf16>::kThreads, 1)
       // Each landed sub-tile's codes become fp16 operand boxes of the
       // dequantised values in the same slot: latent block q -> SW128 box q,
       // RoPE codes -> the SW64 box.  A thread covers tokens ct / 4 and
-      // ct / 4 + 32 (latent) and ct / 2 (RoPE).  The codes sit where boxes 2-3
-      // and the RoPE box go, so every thread reads all of its codes before
-      // any thread writes.  Rows at and past the sequence's end are written
-      // as zeros (PV reads them with zero weight, and a code or scale there is
-      // whatever the page's tail holds).
+      // ct / 4 + 32 (latent) and ct / 2 (RoPE).  The codes sit at [18, 36) KB
+      // of the slot: boxes 0-1 ([0, 16) KB) overlap none of them and are
+      // written as their codes are read; boxes 2-3 and the RoPE box overlap
+      // code blocks, so every thread first reads all of its remaining codes,
+      // and the expansion barrier orders those reads before any write there.
+      // The loops stay rolled: the expansion's code would otherwise crowd the
+      // softmax's out of the instruction cache.  Rows at and past the
+      // sequence's end are written as zeros (PV reads them with zero weight,
+      // and a code or scale there is whatever the page's tail holds).
       const int ct = threadIdx.x - 128 - 32 * kSoftWarps;
       const int ra = ct >> 2, rr = ct >> 1;
       SubWalker walk;
@@ -433,15 +437,6 @@ __global__ void __launch_bounds__(HmCfg<kCode != kCodeBf16>::kThreads, 1)
         const uint32_t slot = k % kNumSlots;
         uint8_t* base = smem + slot * C::kSlotBytes;
         const bool landed = mbar_wait(&B->landed[slot], (k / kNumSlots) & 1, abort_flag, kWaitLimitNs);
-        uint4 v[9];
-        if (landed) {
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int c = ct + 128 * i, q = c >> 8, r = (c >> 2) & 63, ch = c & 3;
-            v[i] = *reinterpret_cast<const uint4*>(base + kOffCodes + q * 4096 + r * 64 + ch * 16);
-          }
-          v[8] = *reinterpret_cast<const uint4*>(base + kOffCodeRope + rr * 32 + (ct & 1) * 16);
-        }
         // the three tokens' scale and -zero point x scale (FP8: no zero point)
         float sc[3] = {0.f, 0.f, 0.f}, nz[3] = {0.f, 0.f, 0.f};
         if (landed) {
@@ -458,29 +453,52 @@ __global__ void __launch_bounds__(HmCfg<kCode != kCodeBf16>::kThreads, 1)
             }
           }
         }
-        if (converters_any(!landed)) {  // also: all codes read before any write
-          ok = false;
-          break;
-        }
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
+        // 16 codes of latent chunk i (0..7) of this thread, dequantised into box i / 2
+        const auto code_at = [&](int i) {
+          const int c = ct + 128 * i, q = c >> 8, r = (c >> 2) & 63, ch = c & 3;
+          return *reinterpret_cast<const uint4*>(base + kOffCodes + q * 4096 + r * 64 + ch * 16);
+        };
+        const auto put = [&](uint4 v, int i) {
           const int c = ct + 128 * i, q = c >> 8, r = (c >> 2) & 63, ch = c & 3;
           uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
           if (r < s.valid) {
-            if constexpr (kZp) expand_codes(v[i], lo, hi);
-            else expand_e4m3(v[i], lo, hi);
-            dequant16(lo, hi, sc[i & 1], nz[i & 1]);
+            if constexpr (kZp) expand_codes(v, lo, hi);
+            else expand_e4m3(v, lo, hi);
+            dequant16(lo, hi, (i & 1) ? sc[1] : sc[0], (i & 1) ? nz[1] : nz[0]);
           }
           uint8_t* row = base + q * kLatBox + r * 128;
           *reinterpret_cast<uint4*>(row + (((2 * ch) ^ (r & 7)) << 4)) = lo;
           *reinterpret_cast<uint4*>(row + (((2 * ch + 1) ^ (r & 7)) << 4)) = hi;
+        };
+        if (landed) {
+#pragma unroll 1
+          for (int i = 0; i < 4; ++i) put(code_at(i), i);  // blocks 0-1 -> boxes 0-1
+        }
+        uint4 v4 = make_uint4(0, 0, 0, 0), v5 = v4, v6 = v4, v7 = v4, vr = v4;
+        if (landed) {
+          v4 = code_at(4);
+          v5 = code_at(5);
+          v6 = code_at(6);
+          v7 = code_at(7);
+          vr = *reinterpret_cast<const uint4*>(base + kOffCodeRope + rr * 32 + (ct & 1) * 16);
+        }
+        if (converters_any(!landed)) {  // also: every code read before boxes 2-3 and RoPE are written
+          ok = false;
+          break;
+        }
+#pragma unroll 1
+        for (int i = 4; i < 8; ++i) {  // blocks 2-3 -> boxes 2-3, the registers shifted along
+          put(v4, i);
+          v4 = v5;
+          v5 = v6;
+          v6 = v7;
         }
         {
           const int r = rr, ch = ct & 1;
           uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
           if (r < s.valid) {
-            if constexpr (kZp) expand_codes(v[8], lo, hi);
-            else expand_e4m3(v[8], lo, hi);
+            if constexpr (kZp) expand_codes(vr, lo, hi);
+            else expand_e4m3(vr, lo, hi);
             dequant16(lo, hi, sc[2], nz[2]);
           }
           uint8_t* row = base + kOffRopeBox + r * 64;  // 64-byte rows, 64-byte swizzle
