@@ -29,12 +29,16 @@
 //       fp16, to the other through distributed shared memory (16 KB per
 //       sub-tile); both add the same two fp16 values, so both hold the same
 //       scores and run the same softmax.
-//   softmax: one thread per row; the row's max, exponentials and sum are
-//       thread-local (no cross-thread reduction).  P is written back into
-//       tensor memory over the row's scores.
-//   PV: O_r [128 x 256] += P [128 x 64] * C_r [64 x 256] (A = P from TMEM,
-//       B = the same latent boxes read MN-major): each CTA accumulates its
-//       own 256 latent columns, in tensor memory for the whole segment.
+//   softmax: two threads per row, each with half of the sub-tile's tokens;
+//       the pair's maxima meet through shared memory, sums stay per thread
+//       until the segment's end.  bf16 caches: P goes to shared memory
+//       (K-major, 128-byte swizzle), so a score buffer is free as soon as its
+//       scores are read and the next sub-tile's exchange can leave before
+//       this sub-tile's P is done.  1-byte caches: P is written into tensor
+//       memory over its scores, keeping a fifth ring slot instead.
+//   PV: O_r [128 x 256] += P [128 x 64] * C_r [64 x 256] (B = the same latent
+//       boxes read MN-major): each CTA accumulates its own 256 latent
+//       columns, in tensor memory for the whole segment.
 // Tensor memory (512 columns): Q latent 128, O_r 256, two score buffers of 64.
 //
 // 1-byte caches (INT8, FP8): the codes land by TMA in the back of each slot
@@ -71,13 +75,14 @@ using namespace dc;
 
 constexpr int kRowsG = 128;                       // query rows per group (MMA M)
 constexpr int kSub = 64;                          // tokens per sub-tile (MMA N of QK, K of PV)
-constexpr int kNumSlots = 5;                      // sub-tile ring
+constexpr int kMaxSlots = 5;                      // barrier arrays of the sub-tile ring
 constexpr uint32_t kLatBox = kSub * 128;          // [64 tokens x 64 latent columns] 16-bit, SW128: 8 KB
 constexpr uint32_t kOffRopeBox = 4 * kLatBox;     // [64 tokens x 32 RoPE columns] 16-bit, SW64: 4 KB
 constexpr uint32_t kOffCodes = 18 * 1024;         // 1-byte: 4 latent code blocks [64 x 64 B], then RoPE codes
 constexpr uint32_t kOffCodeRope = kOffCodes + 4 * 4096;
 constexpr uint32_t kScaleSlotBytes = 512;         // 1-byte: per-token (scale, zero point) or scale of a sub-tile
 constexpr uint32_t kXBytes = kRowsG * kSub * 2;   // one sub-tile's partial scores, fp16
+constexpr uint32_t kPBytes = kRowsG * kSub * 2;   // one sub-tile's P [128 x 64] 16-bit, K-major SW128
 constexpr uint32_t kQRopeBytes = kRowsG * 32 * 2; // [128 rows x 32 RoPE columns] 16-bit, SW64
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 constexpr float kRescaleThreshold = 8.f;          // log2 units
@@ -107,20 +112,26 @@ template <bool kByte>
 struct HmCfg {
   static constexpr int kThreads = 128 + 32 * kSoftWarps + (kByte ? 128 : 0);
   static constexpr uint32_t kSlotBytes = 36 * 1024;
-  static constexpr uint32_t kOffQRope = kNumSlots * kSlotBytes;
-  static constexpr uint32_t kOffX = kOffQRope + kQRopeBytes;  // [2] partial-score buffers from the peer
-  static constexpr uint32_t kOffScl = kOffX + 2 * kXBytes;    // 1-byte: [kNumSlots] per-token scales
-  static constexpr uint32_t kOffMisc = kOffScl + (kByte ? kNumSlots * kScaleSlotBytes : 0);
+  // bf16: P in shared memory (PV's A operand), four slots; 1-byte caches:
+  // P over its scores in TMEM, five slots (the expansion lengthens a slot's
+  // life, and the fifth slot pays more than the early exchange)
+  static constexpr bool kPSmem = !kByte;
+  static constexpr int kSlots = kByte ? 5 : 4;
+  static constexpr uint32_t kOffQRope = kSlots * kSlotBytes;
+  static constexpr uint32_t kOffP = kOffQRope + kQRopeBytes;  // [2] P buffers (PV's A operand)
+  static constexpr uint32_t kOffX = kOffP + (kPSmem ? 2 * kPBytes : 0);  // [2] partial-score buffers from the peer
+  static constexpr uint32_t kOffScl = kOffX + 2 * kXBytes;    // 1-byte: [kSlots] per-token scales
+  static constexpr uint32_t kOffMisc = kOffScl + (kByte ? kSlots * kScaleSlotBytes : 0);
   static constexpr uint32_t kSmem = kOffMisc + 512 + 2048 + 1024;  // + barriers, row maxima, alignment slack
   static_assert(kSmem <= 232448, "dynamic shared memory of one CTA");
-  static_assert(kOffQRope % 1024 == 0 && kSlotBytes % 1024 == 0, "swizzle atoms");
+  static_assert(kOffQRope % 1024 == 0 && kOffP % 1024 == 0 && kSlotBytes % 1024 == 0, "swizzle atoms");
 };
 
 struct HmBarriers {
-  uint64_t full[kNumSlots];    // sub-tile operands ready (bf16: TMA of both producers; 1-byte: expansion)
-  uint64_t landed[kNumSlots];  // 1-byte: codes and scales landed (TMA of both producers)
-  uint64_t empty[kNumSlots];   // PV of the sub-tile done: the slot may be refilled
-  uint64_t q_full, q_empty, s_full[2], x_full[2], p_full[2], pv_done[2], o_full, o_free, drain[2];
+  uint64_t full[kMaxSlots];    // sub-tile operands ready (bf16: TMA of both producers; 1-byte: expansion)
+  uint64_t landed[kMaxSlots];  // 1-byte: codes and scales landed (TMA of both producers)
+  uint64_t empty[kMaxSlots];   // PV of the sub-tile done: the slot may be refilled
+  uint64_t q_full, q_empty, s_full[2], s_free[2], x_full[2], p_full[2], pv_done[2], o_full, o_free, drain[2];
   uint32_t tmem_base;
   int abort;
 };
@@ -208,7 +219,7 @@ __global__ void __launch_bounds__(HmCfg<kCode != kCodeBf16>::kThreads, 1)
   const uint32_t rank = cluster_ctarank();
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kNumSlots; ++i) {
+    for (int i = 0; i < C::kSlots; ++i) {
       mbar_init(&B->full[i], kByte ? 1 : 2);
       mbar_init(&B->landed[i], 2);
       mbar_init(&B->empty[i], 1);
@@ -220,6 +231,7 @@ __global__ void __launch_bounds__(HmCfg<kCode != kCodeBf16>::kThreads, 1)
       mbar_init(&B->x_full[i], 1);  // armed by one local thread; the peer's bytes complete it
       mbar_init(&B->p_full[i], 32 * kSoftWarps);
       mbar_init(&B->pv_done[i], 1);
+      mbar_init(&B->s_free[i], 32 * kSoftWarps);  // every softmax thread has read its scores
       mbar_init(&B->drain[i], 1);
     }
     mbar_init(&B->o_full, 1);
@@ -289,8 +301,8 @@ __global__ void __launch_bounds__(HmCfg<kCode != kCodeBf16>::kThreads, 1)
           if (role == 0) tma_prefetch_2d(&tmap_rope, rope0, nrows[i]);
         }
       }
-      const uint32_t slot = k % kNumSlots;
-      if (!(ok = mbar_wait(&B->empty[slot], ((k / kNumSlots) & 1) ^ 1, abort_flag, kWaitLimitNs))) break;
+      const uint32_t slot = k % C::kSlots;
+      if (!(ok = mbar_wait(&B->empty[slot], ((k / C::kSlots) & 1) ^ 1, abort_flag, kWaitLimitNs))) break;
       uint8_t* base = smem + slot * C::kSlotBytes;
       const uint32_t rows_bytes = uint32_t(nb * box_rows);
       if constexpr (!kByte) {
@@ -325,8 +337,8 @@ __global__ void __launch_bounds__(HmCfg<kCode != kCodeBf16>::kThreads, 1)
     // ------------------------------------------------------------ QK issuer
     // S_r[k & 1] = Q_r * C_r^T: 16 MMAs on the latent columns (A = Q's latent
     // part in TMEM), 2 on the RoPE columns (A = Q's RoPE part in shared
-    // memory).  Before overwriting S[k & 1] it waits for PV of sub-tile k - 2,
-    // which read P from there (and so for its softmax too).
+    // memory).  Before overwriting S[k & 1] it waits until sub-tile k - 2 is
+    // done with the buffer.
     SubWalker walk;
     walk.init(p, S, pa, pb);
     constexpr uint32_t id_qk = idesc_f32acc(kRowsG, kSub, false, false, kByte);
@@ -336,10 +348,14 @@ __global__ void __launch_bounds__(HmCfg<kCode != kCodeBf16>::kThreads, 1)
     SubTile s;
     bool ok = true;
     while (ok && walk.next(s)) {
-      const uint32_t sb = k & 1, slot = k % kNumSlots;
-      if (k >= 2 && !(ok = mbar_wait(&B->pv_done[sb], ((k - 2) >> 1) & 1, abort_flag, kWaitLimitNs))) break;
+      const uint32_t sb = k & 1, slot = k % C::kSlots;
+      // bf16: every softmax thread has read sub-tile k - 2's scores; 1-byte:
+      // PV of sub-tile k - 2 has read its P from the buffer
+      if (k >= 2 && !(ok = mbar_wait(C::kPSmem ? &B->s_free[sb] : &B->pv_done[sb], ((k - 2) >> 1) & 1, abort_flag,
+                                     kWaitLimitNs)))
+        break;
       if (s.first && !(ok = mbar_wait(&B->q_full, seg & 1, abort_flag, kWaitLimitNs))) break;
-      if (!(ok = mbar_wait(&B->full[slot], (k / kNumSlots) & 1, abort_flag, kWaitLimitNs))) break;
+      if (!(ok = mbar_wait(&B->full[slot], (k / C::kSlots) & 1, abort_flag, kWaitLimitNs))) break;
       tc_fence_after();
       const uint32_t d = tmem + kColS + sb * kSub;
       const uint32_t bs = sbase + slot * C::kSlotBytes;
@@ -369,11 +385,12 @@ __global__ void __launch_bounds__(HmCfg<kCode != kCodeBf16>::kThreads, 1)
     walk.init(p, S, pa, pb);
     constexpr uint32_t id_pv = idesc_f32acc(kRowsG, 256, false, true, kByte);
     constexpr uint64_t kDescMN = smem_desc(0, kLatBox, 1024, kSwizzle128B);  // MN-major SW128, 64-column blocks
+    constexpr uint64_t kDescP = smem_desc(0, 16, 1024, kSwizzle128B);        // P: K-major SW128, 128-byte rows
     uint32_t k = 0, seg = 0;
     SubTile s;
     bool ok = true;
     while (ok && walk.next(s)) {
-      const uint32_t sb = k & 1, slot = k % kNumSlots;
+      const uint32_t sb = k & 1, slot = k % C::kSlots;
       bool w = true;
       if (lane == 0) {
         w = mbar_wait(&B->p_full[sb], (k >> 1) & 1, abort_flag, kWaitLimitNs);
@@ -395,10 +412,18 @@ __global__ void __launch_bounds__(HmCfg<kCode != kCodeBf16>::kThreads, 1)
       }
       if (lane == 0) {
         tc_fence_after();
-        const uint32_t a = tmem + kColS + sb * kSub;  // P: columns [0, 32) of the sub-tile's score buffer
         const uint32_t bs = sbase + slot * C::kSlotBytes;
-        for (int kk = 0; kk < nk; ++kk)
-          mma_f16_tmem_a(tmem + kColO, a + 8 * kk, kDescMN | desc_addr(bs + 2048 * kk), id_pv, !(s.first && kk == 0));
+        if constexpr (C::kPSmem) {
+          const uint32_t a = sbase + C::kOffP + sb * kPBytes;  // P of the sub-tile in shared memory
+          for (int kk = 0; kk < nk; ++kk)
+            mma_bf16(tmem + kColO, kDescP | desc_addr(a + 32 * kk), kDescMN | desc_addr(bs + 2048 * kk), id_pv,
+                     !(s.first && kk == 0));
+        } else {
+          const uint32_t a = tmem + kColS + sb * kSub;  // P: columns [0, 32) of the sub-tile's score buffer
+          for (int kk = 0; kk < nk; ++kk)
+            mma_f16_tmem_a(tmem + kColO, a + 8 * kk, kDescMN | desc_addr(bs + 2048 * kk), id_pv,
+                           !(s.first && kk == 0));
+        }
         mma_commit(&B->empty[slot]);
         mma_commit(&B->pv_done[sb]);
         if (s.last) mma_commit(&B->o_full);
@@ -434,9 +459,9 @@ __global__ void __launch_bounds__(HmCfg<kCode != kCodeBf16>::kThreads, 1)
       SubTile s;
       bool ok = true;
       while (ok && walk.next(s)) {
-        const uint32_t slot = k % kNumSlots;
+        const uint32_t slot = k % C::kSlots;
         uint8_t* base = smem + slot * C::kSlotBytes;
-        const bool landed = mbar_wait(&B->landed[slot], (k / kNumSlots) & 1, abort_flag, kWaitLimitNs);
+        const bool landed = mbar_wait(&B->landed[slot], (k / C::kSlots) & 1, abort_flag, kWaitLimitNs);
         // the three tokens' scale and -zero point x scale (FP8: no zero point)
         float sc[3] = {0.f, 0.f, 0.f}, nz[3] = {0.f, 0.f, 0.f};
         if (landed) {
@@ -556,12 +581,13 @@ __global__ void __launch_bounds__(HmCfg<kCode != kCodeBf16>::kThreads, 1)
     // fp16, to the peer (into its buffer kk & 1); kept in hx for the sum.
     // The exchange sends fp16 (distributed shared memory moves only ~12-15
     // GB/s per SM here, so its bytes set the pace) and both CTAs add the same
-    // two fp16 values, so both hold the same scores.  It is issued as soon as
-    // the sub-tile before has its probabilities in P (and, at a segment's
-    // end, its output written).  Issuing it earlier, right after the row
-    // maxima, measured slower: the wait for the next sub-tile's scores then
-    // holds back this sub-tile's P, and with it the PV that frees the score
-    // buffer for the QK after.
+    // two fp16 values, so both hold the same scores.  Sub-tile k + 1's
+    // partials leave as soon as sub-tile k's row maxima are known, so that
+    // they cross while sub-tile k's probabilities are computed.  That pays
+    // because P lives in shared memory: a score buffer is free once its
+    // scores are read here, so QK of sub-tile k + 1 does not wait for PV of
+    // sub-tile k - 1 (with P written over the scores in TMEM it did, and the
+    // early exchange then held back P instead).
     uint32_t hx[16];
     auto send = [&](uint32_t kk) -> bool {
       const uint32_t xb = kk & 1;
@@ -570,6 +596,10 @@ __global__ void __launch_bounds__(HmCfg<kCode != kCodeBf16>::kThreads, 1)
       tc_fence_after();
       uint32_t r[32];
       tmem_ld32(tmem + lane_off + kColS + xb * kSub + 32 * c, r);
+      if constexpr (C::kPSmem) {
+        tc_fence_before();
+        mbar_arrive(&B->s_free[xb]);  // QK of sub-tile kk + 2 may overwrite the buffer
+      }
 #pragma unroll
       for (int i = 0; i < 16; ++i)
         hx[i] = pack_f16x2_sat(__uint_as_float(r[2 * i]) * p.scale_log2, __uint_as_float(r[2 * i + 1]) * p.scale_log2);
@@ -624,8 +654,14 @@ __global__ void __launch_bounds__(HmCfg<kCode != kCodeBf16>::kThreads, 1)
       red[sb * 256 + c * 128 + h] = mt;
       if (soft_any(!ok)) break;
       mt = fmaxf(mt, red[sb * 256 + (c ^ 1) * 128 + h]);
+      // the next sub-tile's partial scores to the peer (and, for a new
+      // segment, its Q first: every QK MMA of this segment is complete)
       SubTile sn;
       const bool have_next = walk.next(sn);
+      if (C::kPSmem && have_next) {
+        if (sn.first) load_q(sn);
+        sent_ok = send(k + 1);
+      }
       // running max: it only has to bound the row's scores within
       // kRescaleThreshold; the first sub-tile of a segment sets it, a sub-tile
       // that breaks the bound raises it and rescales O and l (both threads of
@@ -661,9 +697,10 @@ __global__ void __launch_bounds__(HmCfg<kCode != kCodeBf16>::kThreads, 1)
           fail(B, p.status);  // carried to the next sub-tile's barrier
         }
       }
-      // probabilities -> P over the scores (this thread's 16 columns): bf16
-      // for bf16 caches, fp16 for the dequantised 1-byte caches; l sums the
-      // rounded values PV multiplies by
+      // probabilities -> P (this thread's 32 tokens of its row): bf16 for
+      // bf16 caches, fp16 for the dequantised 1-byte caches; l sums the
+      // rounded values PV multiplies by.  P goes to shared memory (K-major,
+      // 128-byte swizzle) once PV of sub-tile k - 2 has read the buffer.
       {
         uint32_t pk[16];
 #pragma unroll
@@ -679,10 +716,21 @@ __global__ void __launch_bounds__(HmCfg<kCode != kCodeBf16>::kThreads, 1)
             pk[i] = uint32_t(__bfloat16_as_ushort(wa)) | (uint32_t(__bfloat16_as_ushort(wb)) << 16);
           }
         }
-        tmem_st16u(tmem + lane_off + kColS + sb * kSub + 16 * c, pk);
-        tmem_st_wait();
+        if constexpr (C::kPSmem) {
+          const bool okp = k < 2 || mbar_wait(&B->pv_done[sb], ((k - 2) >> 1) & 1, abort_flag, kWaitLimitNs);
+          if (!okp) fail(B, p.status);  // carried to the next sub-tile's barrier
+          uint8_t* prow = smem + C::kOffP + sb * kPBytes + h * 128;
+#pragma unroll
+          for (int v = 0; v < 4; ++v)
+            *reinterpret_cast<uint4*>(prow + (((4 * c + v) ^ (h & 7)) << 4)) =
+                make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+          fence_proxy_async_smem();
+        } else {  // over the scores, which send() has read
+          tmem_st16u(tmem + lane_off + kColS + sb * kSub + 16 * c, pk);
+          tmem_st_wait();
+          tc_fence_before();
+        }
       }
-      tc_fence_before();
       mbar_arrive(&B->p_full[sb]);
       if (s.last) {
         const bool ok2 = mbar_wait(&B->o_full, seg & 1, abort_flag, kWaitLimitNs);
@@ -713,9 +761,7 @@ __global__ void __launch_bounds__(HmCfg<kCode != kCodeBf16>::kThreads, 1)
         soft_sync();  // the sums are read before the next sub-tile writes its maxima there
         ++seg;
       }
-      // the next sub-tile's partial scores to the peer (and, for a new
-      // segment, its Q first: every QK MMA of this segment is complete)
-      if (have_next) {
+      if (!C::kPSmem && have_next) {
         if (sn.first) load_q(sn);
         sent_ok = send(k + 1);
       }
