@@ -66,9 +66,11 @@ def _oracle(fmt, x):
                     f64(x["W_UK"]), f64(x["W_UV"]), SCALE, x["P"], fmt == "int8", fp8=fmt == "fp8")
 
 
-@pytest.mark.parametrize("fmt", ["bf16", "int8", "fp8"])
-def test_no_alloc_equals_decode_on_two_calls(cuda_lib, fmt):
-    d, host = _inputs(fmt)
+@pytest.mark.parametrize("fmt,heads", [("bf16", 16), ("int8", 16), ("fp8", 16), ("bf16", 128), ("int8", 128)])
+def test_no_alloc_equals_decode_on_two_calls(cuda_lib, fmt, heads):
+    # 16 heads: the pair (bf16) and single-CTA (1-byte) kernels; 128 heads: the 128-row kernel
+    d, host = _inputs(fmt, heads=heads, lens=(3000, 129, 4096, 1) if heads == 16 else (700, 129, 65, 1))
+    assert mla.decode_workspace_size(d, 4, SPLITS) <= mla.NO_ALLOC_WORKSPACE_BYTES
     x = _dev(host)
     ref_out, ref_lse = _decode(d, x)
     status = torch.full((1,), 12345, dtype=torch.int32, device="cuda")
@@ -78,7 +80,7 @@ def test_no_alloc_equals_decode_on_two_calls(cuda_lib, fmt):
         assert torch.equal(out, ref_out) and torch.equal(lse, ref_lse), call
     ref_o, ref_l = _oracle(fmt, host)
     B, H = ref_o.shape[:2]
-    assert_parity(out, lse, ref_o, ref_l, [(b, h) for b in range(B) for h in range(H)], f"no-alloc {fmt}")
+    assert_parity(out, lse, ref_o, ref_l, [(b, h) for b in range(B) for h in range(H)], f"no-alloc {fmt} {heads}")
 
 
 def test_no_alloc_reports_device_status_and_recovers(cuda_lib):
