@@ -87,9 +87,8 @@ constexpr uint32_t kQRopeBytes = kRowsG * 32 * 2; // [128 rows x 32 RoPE columns
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 constexpr float kRescaleThreshold = 8.f;          // log2 units
 constexpr bool kPrefetchNext = true;              // L2 prefetch of the next sub-tile's boxes
-// tensor memory columns
 // tensor memory columns: Q's 256 latent values (bf16 / fp16 pairs), O_r, S x2
-// (P is written over its sub-tile's scores)
+// (1-byte caches write P over its sub-tile's scores)
 constexpr uint32_t kColQ = 0, kColO = 128, kColS = 384, kTmemCols = 512;
 constexpr int kSoftWarps = 8;                     // softmax warps: two threads per row
 
@@ -122,7 +121,7 @@ struct HmCfg {
   static constexpr uint32_t kOffX = kOffP + (kPSmem ? 2 * kPBytes : 0);  // [2] partial-score buffers from the peer
   static constexpr uint32_t kOffScl = kOffX + 2 * kXBytes;    // 1-byte: [kSlots] per-token scales
   static constexpr uint32_t kOffMisc = kOffScl + (kByte ? kSlots * kScaleSlotBytes : 0);
-  static constexpr uint32_t kSmem = kOffMisc + 512 + 2048 + 1024;  // + barriers, row maxima, alignment slack
+  static constexpr uint32_t kSmem = kOffMisc + 512 + 2048 + 1024;  // + barriers, row maxima and sums, alignment slack
   static_assert(kSmem <= 232448, "dynamic shared memory of one CTA");
   static_assert(kOffQRope % 1024 == 0 && kOffP % 1024 == 0 && kSlotBytes % 1024 == 0, "swizzle atoms");
 };
