@@ -115,7 +115,7 @@ def prefill_flops(seq_lens, chunk: int, heads: int) -> float:
 def attention_kernel(fmt: str, rows: int = 16):
     """(source file, kernel name) of the attention kernel the library runs for
     this cache format and number of query rows per sequence (heads x tokens)."""
-    if rows % 128 == 0:
+    if rows % 128 == 0 or (rows > 32 and (fmt != "bf16" or rows > 64 or rows % 32)):
         return (os.path.join(ROOT, "mla_decode_attention_paged_gb300", "csrc", "decode_hm.cu"),
                 f"decode_hm_kernel (128-row groups on CTA pairs, {fmt.upper()} cache)")
     name = "decode_pair.cu" if fmt == "bf16" else "decode_tc.cu"

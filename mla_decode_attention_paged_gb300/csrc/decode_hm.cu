@@ -546,6 +546,9 @@ __global__ void __launch_bounds__(HmCfg<kCode != kCodeBf16>::kThreads, 1)
     const int h = 32 * q4 + lane;                     // row of the group = TMEM lane
     const uint32_t lane_off = uint32_t(q4 * 32) << 16;
     const int row = g * kRowsG + h;                   // row within the sequence's rows
+    // a sequence's last group may be padded (rows not a multiple of 128): its
+    // rows past the end run with a zero latent query and write nothing
+    const bool live = row < p.heads;
     const uint32_t x_local = sbase + C::kOffX + h * (kSub * 2) + c * kSub;  // this thread's half of its row
     const int xr_rot = h & 3;                         // 16-byte pieces rotated by row to spread banks
     const uint32_t peer = rank ^ 1u;
@@ -567,7 +570,7 @@ __global__ void __launch_bounds__(HmCfg<kCode != kCodeBf16>::kThreads, 1)
         uint32_t r[32];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          const uint4 v = __ldg(src + 8 * j + i);
+          const uint4 v = live ? __ldg(src + 8 * j + i) : make_uint4(0, 0, 0, 0);
           r[4 * i] = v.x; r[4 * i + 1] = v.y; r[4 * i + 2] = v.z; r[4 * i + 3] = v.w;
         }
         tmem_st32(tmem + lane_off + kColQ + 64 * c + 32 * j, r);
@@ -748,14 +751,16 @@ __global__ void __launch_bounds__(HmCfg<kCode != kCodeBf16>::kThreads, 1)
         for (int j = 0; j < 4; ++j) {
           uint32_t r[32];
           tmem_ld32(tmem + lane_off + kColO + 128 * c + 32 * j, r);
+          if (live) {
 #pragma unroll
-          for (int i = 0; i < 8; ++i)
-            dst[8 * j + i] = make_float4(__uint_as_float(r[4 * i]) * inv_l, __uint_as_float(r[4 * i + 1]) * inv_l,
-                                         __uint_as_float(r[4 * i + 2]) * inv_l, __uint_as_float(r[4 * i + 3]) * inv_l);
+            for (int i = 0; i < 8; ++i)
+              dst[8 * j + i] = make_float4(__uint_as_float(r[4 * i]) * inv_l, __uint_as_float(r[4 * i + 1]) * inv_l,
+                                           __uint_as_float(r[4 * i + 2]) * inv_l, __uint_as_float(r[4 * i + 3]) * inv_l);
+          }
         }
         tc_fence_before();
         mbar_arrive(&B->o_free);
-        if (rank == 0 && c == 0)
+        if (rank == 0 && c == 0 && live)
           p.partial_lse[size_t(s.seg) * p.heads + row] = l_row > 0.f ? (m_run + log2f(l_row)) * kLn2 : -INFINITY;
         soft_sync();  // the sums are read before the next sub-tile writes its maxima there
         ++seg;

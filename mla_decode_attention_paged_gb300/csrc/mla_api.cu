@@ -52,10 +52,16 @@ mla_dims row_dims(const mla_dims* d, int q_len) {
 }
 
 // The attention kernel for `rows` query rows per sequence (heads, or
-// q_len x heads): groups of 128 rows run on the 128-row CTA-pair kernel (any
-// cache format); otherwise bf16 caches run on the 16/32-head CTA-pair kernel
-// and 1-byte caches (and devices that cannot place pairs) on single CTAs.
-// `units` = attention units resident at once (pairs or CTAs).
+// q_len x heads): more than 32 rows run on the 128-row CTA-pair kernel (any
+// cache format; rows that are not a multiple of 128 pad the last group,
+// which still reads each tile once where the 16/32-row kernels would read it
+// once per group), except bf16 rows that make one or two 32-row groups of
+// the 16/32-head CTA-pair kernel (measured on the V2-Lite batch at 4 tokens
+// x 16 heads: 0.510 ms as two 32-row groups, 0.544 ms as one padded group;
+// at 6 tokens 0.754 against 0.547 ms).  The rest: bf16 caches on the
+// 16/32-head CTA-pair kernel, 1-byte caches (and devices that cannot place
+// pairs) on single CTAs.  `units` = attention units resident at once (pairs
+// or CTAs).
 enum AttnKind { kAttnRows128, kAttnPair, kAttnSingle };
 struct AttnChoice {
   int kind, hc, units;
@@ -63,7 +69,8 @@ struct AttnChoice {
 AttnChoice choose_attention(int rows, int code) {
   const bool byte = code != kCodeBf16;
   const bool single = g_force_single_cta.load() != 0;
-  if (rows % 128 == 0 && !single) {
+  const bool pair_groups = !byte && rows <= 64 && rows % 32 == 0;
+  if (!single && (rows % 128 == 0 || (rows > 32 && !pair_groups))) {
     const int cap = decode_rows128_capacity(code);
     if (cap > 0) return {kAttnRows128, 128, cap};
   }
@@ -80,7 +87,7 @@ int effective_splits(const mla_dims* d, int num_splits) {
   if (num_splits > 0) return num_splits;
   const AttnChoice a = choose_attention(d->num_heads, cache_code(d));
   if (a.units <= 0) return -1;
-  const int groups = d->num_heads / a.hc;
+  const int groups = (d->num_heads + a.hc - 1) / a.hc;
   return a.units / groups > 0 ? a.units / groups : 1;
 }
 
@@ -298,7 +305,7 @@ int decode_rows(const mla_dims* d, const void* q_nope, const void* q_pe, const v
 
   const AttnChoice attn = choose_attention(dr.num_heads, code);
   if (attn.units <= 0) return MLA_ERR_CUDA;
-  const int H = dr.num_heads, hc = attn.hc, groups = H / hc;
+  const int H = dr.num_heads, hc = attn.hc, groups = (H + hc - 1) / hc;
   char* ws = static_cast<char*>(workspace);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 

@@ -8,7 +8,8 @@ around both boundaries (63, 64, 65, 127, 128, 129, ...), for every page
 size (16 and 32: several pages per half; 64: one; 128: half a page), with
 split counts from one partition to one per half-tile, two row groups (256
 heads), multi-token rows (16 x 8, 32 x 4, 64 x 2), and the degenerate cases
-(empty sequence, one token, NaN patterns past a sequence's end)."""
+(empty sequence, one token, NaN patterns past a sequence's end).  Row counts
+above 32 that are not a multiple of 128 run here too, the last group padded."""
 import pytest
 import torch
 
@@ -48,6 +49,21 @@ def test_rows128_multi_token_rows(cuda_lib, heads, T, fmt):
     # rows v = t * heads + h: one group holds several query tokens, causal among themselves
     mt_check(_mt(heads=heads, T=T, lens=(1, 5, 64, 129, 700), int8=fmt == "int8", fp8=fmt == "fp8",
                  seed=900 + heads + T))
+
+
+@pytest.mark.parametrize("heads,T,fmt", [(16, 3, "bf16"), (16, 4, "int8"), (16, 5, "fp8"), (16, 6, "bf16"),
+                                          (32, 3, "int8"), (32, 5, "bf16"), (16, 7, "fp8")])
+def test_rows128_padded_groups_multi_token(cuda_lib, heads, T, fmt):
+    # 48 to 160 rows: one or two groups, the last padded past the sequence's
+    # rows (those rows run with a zero latent query and write nothing)
+    mt_check(_mt(heads=heads, T=T, lens=(1, 5, 64, 129, 700), int8=fmt == "int8", fp8=fmt == "fp8",
+                 seed=1300 + heads + T), num_splits=7)
+
+
+@pytest.mark.parametrize("heads,fmt", [(64, "int8"), (96, "bf16"), (96, "fp8"), (160, "bf16")])
+def test_rows128_padded_groups_single_token(cuda_lib, heads, fmt):
+    _run_small(*_small(heads=heads, lens=(700, 1, 130, 64), int8=fmt == "int8", fp8=fmt == "fp8", seed=400 + heads),
+               num_splits=5)
 
 
 def test_rows128_multi_token_invisible_segments(cuda_lib):
@@ -92,8 +108,13 @@ def test_rows128_bit_identical_run_to_run_and_under_a_shuffled_table(cuda_lib):
 
 
 def test_rows128_is_the_kernel_that_runs(cuda_lib):
-    """128 heads take the 128-row kernel's automatic split count (one
-    partition per resident pair for the single row group); as four 32-head
-    groups they would get a quarter of the pairs each, fewer than 96 heads'
-    three groups do."""
-    assert mla.auto_num_splits(mla.dims(128, 64), 4) > mla.auto_num_splits(mla.dims(96, 64), 4)
+    """More than 32 rows take the 128-row kernel's automatic split count (one
+    partition per resident pair and row group): 96 bf16 rows or 64 INT8 rows
+    make one group (padded below 128), 256 rows two, each with half the
+    pairs; 64 bf16 rows stay on the pair kernel as two 32-row groups."""
+    one = mla.auto_num_splits(mla.dims(128, 64), 4)
+    assert mla.auto_num_splits(mla.dims(96, 64), 4) == one
+    assert mla.auto_num_splits(mla.dims(64, 64, int8=True), 4) == one
+    assert mla.auto_num_splits(mla.dims(256, 64), 4) == one // 2
+    # bf16: 64 rows stay two 32-row groups of the pair kernel, half the pairs each
+    assert mla.auto_num_splits(mla.dims(64, 64), 4) == one // 2
