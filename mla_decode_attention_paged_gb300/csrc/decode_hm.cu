@@ -201,8 +201,9 @@ struct SubPages {
 };
 
 // kCode: CacheCode; kCausal: multi-token decode (q_len > 1) masks each row's
-// later positions on a sequence's last sub-tiles.
-template <int kCode, bool kCausal>
+// later positions on a sequence's last sub-tiles; kPad: rows per sequence
+// not a multiple of 128.
+template <int kCode, bool kCausal, bool kPad>
 __global__ void __launch_bounds__(HmCfg<kCode != kCodeBf16>::kThreads, 1)
     decode_hm_kernel(const __grid_constant__ CUtensorMap tmap_lat, const __grid_constant__ CUtensorMap tmap_rope,
                      const __grid_constant__ CUtensorMap tmap_qrope, DecodeParams p) {
@@ -546,9 +547,10 @@ __global__ void __launch_bounds__(HmCfg<kCode != kCodeBf16>::kThreads, 1)
     const int h = 32 * q4 + lane;                     // row of the group = TMEM lane
     const uint32_t lane_off = uint32_t(q4 * 32) << 16;
     const int row = g * kRowsG + h;                   // row within the sequence's rows
-    // a sequence's last group may be padded (rows not a multiple of 128): its
-    // rows past the end run with a zero latent query and write nothing
-    const bool live = row < p.heads;
+    // kPad: a sequence's last group is padded (rows not a multiple of 128):
+    // its rows past the end run with a zero latent query and write nothing
+    // (a separate instantiation: the check cost the unpadded kernel 2-3%)
+    const bool live = !kPad || row < p.heads;
     const uint32_t x_local = sbase + C::kOffX + h * (kSub * 2) + c * kSub;  // this thread's half of its row
     const int xr_rot = h & 3;                         // 16-byte pieces rotated by row to spread banks
     const uint32_t peer = rank ^ 1u;
@@ -804,13 +806,16 @@ cudaError_t launch_hm(const DecodeParams& p, int clusters_per_group, cudaStream_
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 128 || !attr[dev]) {
-    for (auto* k : {decode_hm_kernel<kCode, false>, decode_hm_kernel<kCode, true>}) {
+    for (auto* k : {decode_hm_kernel<kCode, false, false>, decode_hm_kernel<kCode, true, false>,
+                    decode_hm_kernel<kCode, false, true>, decode_hm_kernel<kCode, true, true>}) {
       const cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, int(C::kSmem));
       if (e != cudaSuccess) return e;
     }
     if (dev >= 0 && dev < 128) attr[dev] = true;
   }
-  auto* kernel = p.q_len > 1 ? decode_hm_kernel<kCode, true> : decode_hm_kernel<kCode, false>;
+  const bool pad = p.heads % kRowsG != 0;
+  auto* kernel = p.q_len > 1 ? (pad ? decode_hm_kernel<kCode, true, true> : decode_hm_kernel<kCode, true, false>)
+                             : (pad ? decode_hm_kernel<kCode, false, true> : decode_hm_kernel<kCode, false, false>);
   return launch_pdl(kernel, dim3(2 * clusters_per_group * p.num_groups), dim3(C::kThreads), C::kSmem, stream, 2, ml,
                     mr, mqr, p);
 }
@@ -822,7 +827,7 @@ int hm_capacity() {  // CTA pairs of this kernel that can be resident at once on
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 128 && cached[dev] > 0) return cached[dev];
-  if (cudaFuncSetAttribute(decode_hm_kernel<kCode, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (cudaFuncSetAttribute(decode_hm_kernel<kCode, false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            int(C::kSmem)) != cudaSuccess)
     return 0;
   cudaLaunchConfig_t cfg = {};
@@ -837,7 +842,7 @@ int hm_capacity() {  // CTA pairs of this kernel that can be resident at once on
   cfg.attrs = at;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, decode_hm_kernel<kCode, false>, &cfg) != cudaSuccess || n <= 0) {
+  if (cudaOccupancyMaxActiveClusters(&n, decode_hm_kernel<kCode, false, false>, &cfg) != cudaSuccess || n <= 0) {
     cudaGetLastError();
     return 0;
   }
