@@ -75,12 +75,14 @@ using namespace dc;
 
 constexpr int kRowsG = 128;                       // query rows per group (MMA M)
 constexpr int kSub = 64;                          // tokens per sub-tile (MMA N of QK, K of PV)
-constexpr int kMaxSlots = 5;                      // barrier arrays of the sub-tile ring
+constexpr int kMaxSlots = 4;                      // barrier arrays of the sub-tile ring
 constexpr uint32_t kLatBox = kSub * 128;          // [64 tokens x 64 latent columns] 16-bit, SW128: 8 KB
 constexpr uint32_t kOffRopeBox = 4 * kLatBox;     // [64 tokens x 32 RoPE columns] 16-bit, SW64: 4 KB
-constexpr uint32_t kOffCodes = 18 * 1024;         // 1-byte: 4 latent code blocks [64 x 64 B], then RoPE codes
-constexpr uint32_t kOffCodeRope = kOffCodes + 4 * 4096;
-constexpr uint32_t kScaleSlotBytes = 512;         // 1-byte: per-token (scale, zero point) or scale of a sub-tile
+// 1-byte caches: a code slot holds a sub-tile's 4 latent code blocks [64 x
+// 64 B], its RoPE codes [64 x 32 B] and its per-token (scale, zero point) or
+// scale
+constexpr int kCodeSlots = 2;
+constexpr uint32_t kCodeRope = 4 * 4096, kCodeScl = kCodeRope + 64 * 32, kCodeSlotBytes = 19 * 1024;
 constexpr uint32_t kXBytes = kRowsG * kSub * 2;   // one sub-tile's partial scores, fp16
 constexpr uint32_t kPBytes = kRowsG * kSub * 2;   // one sub-tile's P [128 x 64] 16-bit, K-major SW128
 constexpr uint32_t kQRopeBytes = kRowsG * 32 * 2; // [128 rows x 32 RoPE columns] 16-bit, SW64
@@ -111,25 +113,27 @@ template <bool kByte>
 struct HmCfg {
   static constexpr int kThreads = 128 + 32 * kSoftWarps + (kByte ? 128 : 0);
   static constexpr uint32_t kSlotBytes = 36 * 1024;
-  // bf16: P in shared memory (PV's A operand), four slots; 1-byte caches:
-  // P over its scores in TMEM, five slots (the expansion lengthens a slot's
-  // life, and the fifth slot pays more than the early exchange)
+  // Four operand slots.  bf16: P in shared memory (PV's A operand); 1-byte
+  // caches: P over its scores in TMEM, and a ring of two code slots that the
+  // copies land in, so that an operand slot is held only from its expansion
+  // to its PV (in shared memory P and the code ring do not both fit)
   static constexpr bool kPSmem = !kByte;
-  static constexpr int kSlots = kByte ? 5 : 4;
+  static constexpr int kSlots = 4;
   static constexpr uint32_t kOffQRope = kSlots * kSlotBytes;
-  static constexpr uint32_t kOffP = kOffQRope + kQRopeBytes;  // [2] P buffers (PV's A operand)
-  static constexpr uint32_t kOffX = kOffP + (kPSmem ? 2 * kPBytes : 0);  // [2] partial-score buffers from the peer
-  static constexpr uint32_t kOffScl = kOffX + 2 * kXBytes;    // 1-byte: [kSlots] per-token scales
-  static constexpr uint32_t kOffMisc = kOffScl + (kByte ? kSlots * kScaleSlotBytes : 0);
+  static constexpr uint32_t kOffP = kOffQRope + kQRopeBytes;  // bf16: [2] P buffers (PV's A operand)
+  static constexpr uint32_t kOffCode = kOffP + (kPSmem ? 2 * kPBytes : 0);  // 1-byte: [kCodeSlots] code slots
+  static constexpr uint32_t kOffX = kOffCode + (kByte ? kCodeSlots * kCodeSlotBytes : 0);  // [2] peer's partials
+  static constexpr uint32_t kOffMisc = kOffX + 2 * kXBytes;
   static constexpr uint32_t kSmem = kOffMisc + 512 + 2048 + 1024;  // + barriers, row maxima and sums, alignment slack
   static_assert(kSmem <= 232448, "dynamic shared memory of one CTA");
-  static_assert(kOffQRope % 1024 == 0 && kOffP % 1024 == 0 && kSlotBytes % 1024 == 0, "swizzle atoms");
+  static_assert(kOffQRope % 1024 == 0 && kOffP % 1024 == 0 && kSlotBytes % 1024 == 0 && kOffCode % 1024 == 0,
+                "swizzle atoms, copy alignment");
 };
 
 struct HmBarriers {
   uint64_t full[kMaxSlots];    // sub-tile operands ready (bf16: TMA of both producers; 1-byte: expansion)
-  uint64_t landed[kMaxSlots];  // 1-byte: codes and scales landed (TMA of both producers)
   uint64_t empty[kMaxSlots];   // PV of the sub-tile done: the slot may be refilled
+  uint64_t landed[kCodeSlots], code_empty[kCodeSlots];  // 1-byte: codes landed (TMA); codes read (expansion)
   uint64_t q_full, q_empty, s_full[2], s_free[2], x_full[2], p_full[2], pv_done[2], o_full, o_free, drain[2];
   uint32_t tmem_base;
   int abort;
@@ -221,8 +225,11 @@ __global__ void __launch_bounds__(HmCfg<kCode != kCodeBf16>::kThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::kSlots; ++i) {
       mbar_init(&B->full[i], kByte ? 1 : 2);
-      mbar_init(&B->landed[i], 2);
       mbar_init(&B->empty[i], 1);
+    }
+    for (int i = 0; i < kCodeSlots; ++i) {
+      mbar_init(&B->landed[i], 2);
+      mbar_init(&B->code_empty[i], 1);
     }
     mbar_init(&B->q_full, 1 + 32 * kSoftWarps);  // the RoPE part's TMA, and the rows' latent parts
     mbar_init(&B->q_empty, 1);
@@ -301,11 +308,11 @@ __global__ void __launch_bounds__(HmCfg<kCode != kCodeBf16>::kThreads, 1)
           if (role == 0) tma_prefetch_2d(&tmap_rope, rope0, nrows[i]);
         }
       }
-      const uint32_t slot = k % C::kSlots;
-      if (!(ok = mbar_wait(&B->empty[slot], ((k / C::kSlots) & 1) ^ 1, abort_flag, kWaitLimitNs))) break;
-      uint8_t* base = smem + slot * C::kSlotBytes;
       const uint32_t rows_bytes = uint32_t(nb * box_rows);
       if constexpr (!kByte) {
+        const uint32_t slot = k % C::kSlots;
+        if (!(ok = mbar_wait(&B->empty[slot], ((k / C::kSlots) & 1) ^ 1, abort_flag, kWaitLimitNs))) break;
+        uint8_t* base = smem + slot * C::kSlotBytes;
         const uint32_t bytes = rows_bytes * (role == 0 ? 128 + 128 + 64 : 128 + 128);
         mbar_arrive_expect_tx(&B->full[slot], bytes + (p.inject_wait_timeout && k == 0 && role == 0 ? 16 : 0));
 #pragma unroll 1
@@ -315,19 +322,21 @@ __global__ void __launch_bounds__(HmCfg<kCode != kCodeBf16>::kThreads, 1)
           if (role == 0)
             tma_load_2d(base + kOffRopeBox + i * box_rows * 64, &tmap_rope, rope0, rows[i], &B->full[slot]);
         }
-      } else {
+      } else {  // into the code ring; the expansion frees a code slot once it has read it
+        const uint32_t cs = k % kCodeSlots;
+        if (!(ok = mbar_wait(&B->code_empty[cs], ((k / kCodeSlots) & 1) ^ 1, abort_flag, kWaitLimitNs))) break;
+        uint8_t* code = smem + C::kOffCode + cs * kCodeSlotBytes;
         const uint32_t bytes = rows_bytes * (role == 0 ? 64 + 64 + 32 : 64 + 64 + sbytes);
-        mbar_arrive_expect_tx(&B->landed[slot], bytes + (p.inject_wait_timeout && k == 0 && role == 0 ? 16 : 0));
+        mbar_arrive_expect_tx(&B->landed[cs], bytes + (p.inject_wait_timeout && k == 0 && role == 0 ? 16 : 0));
 #pragma unroll 1
         for (int i = 0; i < nb; ++i) {
           for (int q = 2 * role; q < 2 * role + 2; ++q)
-            tma_load_2d(base + kOffCodes + q * 4096 + i * box_rows * 64, &tmap_lat, lat0 + 64 * q, rows[i],
-                        &B->landed[slot]);
+            tma_load_2d(code + q * 4096 + i * box_rows * 64, &tmap_lat, lat0 + 64 * q, rows[i], &B->landed[cs]);
           if (role == 0)
-            tma_load_2d(base + kOffCodeRope + i * box_rows * 32, &tmap_rope, rope0, rows[i], &B->landed[slot]);
+            tma_load_2d(code + kCodeRope + i * box_rows * 32, &tmap_rope, rope0, rows[i], &B->landed[cs]);
           else
-            bulk_copy_g2s(smem + C::kOffScl + slot * kScaleSlotBytes + i * box_rows * sbytes,
-                          p.scale_zero + size_t(rows[i]) * (kZp ? 2 : 1), box_rows * sbytes, &B->landed[slot]);
+            bulk_copy_g2s(code + kCodeScl + i * box_rows * sbytes, p.scale_zero + size_t(rows[i]) * (kZp ? 2 : 1),
+                          box_rows * sbytes, &B->landed[cs]);
         }
       }
       ++k;
@@ -440,17 +449,14 @@ __global__ void __launch_bounds__(HmCfg<kCode != kCodeBf16>::kThreads, 1)
     if constexpr (kByte) {
       // ------------------------------------------------------------ code expansion
       // Each landed sub-tile's codes become fp16 operand boxes of the
-      // dequantised values in the same slot: latent block q -> SW128 box q,
+      // dequantised values in an operand slot: latent block q -> SW128 box q,
       // RoPE codes -> the SW64 box.  A thread covers tokens ct / 4 and
-      // ct / 4 + 32 (latent) and ct / 2 (RoPE).  The codes sit at [18, 36) KB
-      // of the slot: boxes 0-1 ([0, 16) KB) overlap none of them and are
-      // written as their codes are read; boxes 2-3 and the RoPE box overlap
-      // code blocks, so every thread first reads all of its remaining codes,
-      // and the expansion barrier orders those reads before any write there.
-      // The loops stay rolled: the expansion's code would otherwise crowd the
-      // softmax's out of the instruction cache.  Rows at and past the
-      // sequence's end are written as zeros (PV reads them with zero weight,
-      // and a code or scale there is whatever the page's tail holds).
+      // ct / 4 + 32 (latent) and ct / 2 (RoPE): nine 16-code chunks, read,
+      // dequantised and written one at a time (the latent loop stays rolled:
+      // the expansion's code would otherwise crowd the softmax's out of the
+      // instruction cache).  Rows at and past the sequence's end are written
+      // as zeros (PV reads them with zero weight, and a code or scale there is
+      // whatever the page's tail holds).
       const int ct = threadIdx.x - 128 - 32 * kSoftWarps;
       const int ra = ct >> 2, rr = ct >> 1;
       SubWalker walk;
@@ -459,13 +465,20 @@ __global__ void __launch_bounds__(HmCfg<kCode != kCodeBf16>::kThreads, 1)
       SubTile s;
       bool ok = true;
       while (ok && walk.next(s)) {
-        const uint32_t slot = k % C::kSlots;
+        const uint32_t slot = k % C::kSlots, cs = k % kCodeSlots;
+        const uint8_t* code = smem + C::kOffCode + cs * kCodeSlotBytes;
         uint8_t* base = smem + slot * C::kSlotBytes;
-        const bool landed = mbar_wait(&B->landed[slot], (k / C::kSlots) & 1, abort_flag, kWaitLimitNs);
+        // the codes have landed and PV of sub-tile k - kSlots has freed the operand slot
+        bool w = mbar_wait(&B->landed[cs], (k / kCodeSlots) & 1, abort_flag, kWaitLimitNs);
+        w = w && mbar_wait(&B->empty[slot], ((k / C::kSlots) & 1) ^ 1, abort_flag, kWaitLimitNs);
+        if (converters_any(!w)) {
+          ok = false;
+          break;
+        }
         // the three tokens' scale and -zero point x scale (FP8: no zero point)
-        float sc[3] = {0.f, 0.f, 0.f}, nz[3] = {0.f, 0.f, 0.f};
-        if (landed) {
-          const float* scl = reinterpret_cast<const float*>(smem + C::kOffScl + slot * kScaleSlotBytes);
+        float sc[3], nz[3] = {0.f, 0.f, 0.f};
+        {
+          const float* scl = reinterpret_cast<const float*>(code + kCodeScl);
           const int rows3[3] = {ra, ra + 32, rr};
 #pragma unroll
           for (int j = 0; j < 3; ++j) {
@@ -478,52 +491,27 @@ __global__ void __launch_bounds__(HmCfg<kCode != kCodeBf16>::kThreads, 1)
             }
           }
         }
-        // 16 codes of latent chunk i (0..7) of this thread, dequantised into box i / 2
-        const auto code_at = [&](int i) {
+#pragma unroll 1
+        for (int i = 0; i < 8; ++i) {  // latent chunk i: token ra + 32 (i & 1), block i / 2
           const int c = ct + 128 * i, q = c >> 8, r = (c >> 2) & 63, ch = c & 3;
-          return *reinterpret_cast<const uint4*>(base + kOffCodes + q * 4096 + r * 64 + ch * 16);
-        };
-        const auto put = [&](uint4 v, int i) {
-          const int c = ct + 128 * i, q = c >> 8, r = (c >> 2) & 63, ch = c & 3;
+          const uint4 v = *reinterpret_cast<const uint4*>(code + q * 4096 + r * 64 + ch * 16);
           uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
           if (r < s.valid) {
             if constexpr (kZp) expand_codes(v, lo, hi);
             else expand_e4m3(v, lo, hi);
             dequant16(lo, hi, (i & 1) ? sc[1] : sc[0], (i & 1) ? nz[1] : nz[0]);
           }
-          uint8_t* row = base + q * kLatBox + r * 128;
+          uint8_t* row = base + q * kLatBox + r * 128;  // 128-byte rows, 128-byte swizzle
           *reinterpret_cast<uint4*>(row + (((2 * ch) ^ (r & 7)) << 4)) = lo;
           *reinterpret_cast<uint4*>(row + (((2 * ch + 1) ^ (r & 7)) << 4)) = hi;
-        };
-        if (landed) {
-#pragma unroll 1
-          for (int i = 0; i < 4; ++i) put(code_at(i), i);  // blocks 0-1 -> boxes 0-1
         }
-        uint4 v4 = make_uint4(0, 0, 0, 0), v5 = v4, v6 = v4, v7 = v4, vr = v4;
-        if (landed) {
-          v4 = code_at(4);
-          v5 = code_at(5);
-          v6 = code_at(6);
-          v7 = code_at(7);
-          vr = *reinterpret_cast<const uint4*>(base + kOffCodeRope + rr * 32 + (ct & 1) * 16);
-        }
-        if (converters_any(!landed)) {  // also: every code read before boxes 2-3 and RoPE are written
-          ok = false;
-          break;
-        }
-#pragma unroll 1
-        for (int i = 4; i < 8; ++i) {  // blocks 2-3 -> boxes 2-3, the registers shifted along
-          put(v4, i);
-          v4 = v5;
-          v5 = v6;
-          v6 = v7;
-        }
-        {
+        {  // RoPE chunk: token rr
           const int r = rr, ch = ct & 1;
+          const uint4 v = *reinterpret_cast<const uint4*>(code + kCodeRope + r * 32 + ch * 16);
           uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
           if (r < s.valid) {
-            if constexpr (kZp) expand_codes(vr, lo, hi);
-            else expand_e4m3(vr, lo, hi);
+            if constexpr (kZp) expand_codes(v, lo, hi);
+            else expand_e4m3(v, lo, hi);
             dequant16(lo, hi, sc[2], nz[2]);
           }
           uint8_t* row = base + kOffRopeBox + r * 64;  // 64-byte rows, 64-byte swizzle
@@ -532,7 +520,10 @@ __global__ void __launch_bounds__(HmCfg<kCode != kCodeBf16>::kThreads, 1)
         }
         fence_proxy_async_smem();
         converters_sync();
-        if (ct == 0) mbar_arrive(&B->full[slot]);
+        if (ct == 0) {
+          mbar_arrive(&B->code_empty[cs]);  // every thread has read its codes
+          mbar_arrive(&B->full[slot]);
+        }
         ++k;
       }
       if (!ok) fail(B, p.status);
