@@ -35,18 +35,18 @@
 //       (K-major, 128-byte swizzle), so a score buffer is free as soon as its
 //       scores are read and the next sub-tile's exchange can leave before
 //       this sub-tile's P is done.  1-byte caches: P is written into tensor
-//       memory over its scores, keeping a fifth ring slot instead.
+//       memory over its scores (shared memory holds their code ring instead).
 //   PV: O_r [128 x 256] += P [128 x 64] * C_r [64 x 256] (B = the same latent
 //       boxes read MN-major): each CTA accumulates its own 256 latent
 //       columns, in tensor memory for the whole segment.
 // Tensor memory (512 columns): Q latent 128, O_r 256, two score buffers of 64.
 //
-// 1-byte caches (INT8, FP8): the codes land by TMA in the back of each slot
-// and four warps turn them into fp16 operand boxes of the dequantised values
-// ("KV Cache Optimization", section 3: x = s_t (code - zp_t), INT8; x = s_t
-// e4m3(code), FP8), each computed in fp32 and rounded once to fp16.  Q and P
-// are fp16, and from there the sub-tile runs exactly as for a bf16 cache: the
-// scale and zero point never reach the softmax.
+// 1-byte caches (INT8, FP8): the codes land by TMA in a ring of two code
+// slots and four warps turn them into fp16 operand boxes of the dequantised
+// values ("KV Cache Optimization", section 3: x = s_t (code - zp_t), INT8;
+// x = s_t e4m3(code), FP8), each computed in fp32 and rounded once to fp16.
+// Q and P are fp16, and from there the sub-tile runs exactly as for a bf16
+// cache: the scale and zero point never reach the softmax.
 //
 // Warp roles (384 threads; 512 for 1-byte caches):
 //   warp 0       TMA producer: Q's RoPE part per segment; latent boxes 0-1 and
