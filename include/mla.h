@@ -128,7 +128,8 @@ int mla_cache_append(const mla_dims* dims, void* cache, float* cache_scale_zero,
                      int32_t* device_status, mla_stream_t stream);
 
 /* Number of KV partitions mla_decode uses when num_splits = 0 on the current
- * device (one per streaming multiprocessor and head group).  < 0 on error. */
+ * device: one per attention unit that can be resident at once (a CTA pair,
+ * or a CTA where pairs are not used) and row group.  < 0 on error. */
 int mla_auto_num_splits(const mla_dims* dims, int32_t batch);
 
 /* Bytes of workspace mla_decode needs for (dims, batch, num_splits); 0 if the
@@ -161,7 +162,7 @@ size_t mla_decode_workspace_size(const mla_dims* dims, int32_t batch, int32_t nu
  *   W_UK, W_UV  bf16 [H, 128, 512] (head h's W^UK_h, W^UV_h in R^{128x512})
  *   softmax_scale  multiplies the raw dot product (e.g. 1/sqrt(128+64))
  *   num_splits  KV partitions over the batch's total work (0 = automatic).
- *               The work of every head group is cut into num_splits equal
+ *               The work of every row group is cut into num_splits equal
  *               pieces, so a sequence holding a fraction f of all tokens is
  *               split into about f * num_splits chunks.
  *   workspace   device scratch, 256-byte aligned, at least
@@ -267,10 +268,12 @@ size_t mla_prefill_workspace_size(const mla_dims* dims, int32_t batch, int32_t c
  *   workspace   at least mla_prefill_workspace_size(dims, batch, chunk,
  *               num_splits) bytes; its first 4 bytes are the call's device
  *               status (mla_read_device_status), covering the append too.
- * The attention runs the decode kernels over chunk * H rows per sequence
- * (head groups of 16 or 32 (token, head) rows), so every head group
- * streams its sequence's cache: a first, functional form of prefill, far
- * from the tensor-core roofline a query-tiled kernel would reach.
+ * The attention is query-tiled: the chunk's chunk * H (token, head) rows of
+ * a sequence run in groups of 128 rows, each group on the MMA's M extent
+ * against 64-token sub-tiles of the sequence's pages (a group of fewer rows
+ * is padded; chunk * H of 32 or 64 rows on bf16 caches runs as 32-row
+ * groups).  Each group streams its sequence's pages, from L2 after the
+ * first.
  */
 int mla_prefill(const mla_dims* dims, void* cache, float* cache_scale_zero, int32_t num_pages,
                 const int32_t* block_table, int32_t max_pages_per_seq, const int32_t* seq_lens, int32_t batch,
