@@ -2,7 +2,8 @@
 batch, ragged lengths (with 0, 1 and tile-boundary lengths mixed in), split
 count, cache type and query-token count (or a sparse selection), and checks
 the library against the fp64 oracle through the C ABI.  Complements the
-hand-picked cases with combinations nobody wrote down."""
+hand-picked cases with combinations nobody wrote down; a second family
+draws row counts (heads x tokens) around the 128-row kernel's groups."""
 import numpy as np
 import pytest
 import torch
@@ -30,9 +31,35 @@ def _case(seed):
     return dict(P=P, H=H, lens=lens, fmt=fmt, mode=str(mode), T=T, splits=splits)
 
 
+def _wide_case(seed):
+    """Row counts around the 128-row kernel's groups: 32-96 heads with 1-5
+    query tokens (32 to 480 rows: single and several groups, padded or not),
+    shorter sequences to keep the oracle quick."""
+    rng = np.random.default_rng(7000 + seed)
+    P = int(rng.choice([16, 32, 64, 128]))
+    H = int(rng.choice([32, 64, 96]))
+    B = int(rng.integers(1, 4))
+    special = [0, 1, 63, 64, 65, 127, 128, 129]
+    lens = [int(rng.choice(special)) if rng.random() < 0.4 else int(rng.integers(1, 700)) for _ in range(B)]
+    r = rng.random()
+    fmt = "int8" if r < 0.3 else "fp8" if r < 0.55 else "bf16"
+    T = int(rng.integers(1, 6))
+    mode = "multi" if T > 1 else str(rng.choice(["dense", "sparse"], p=[0.7, 0.3]))
+    splits = int(rng.choice([0, 1, 5, 40]))
+    return dict(P=P, H=H, lens=lens, fmt=fmt, mode=mode, T=T, splits=splits)
+
+
 @pytest.mark.parametrize("seed", range(16))
 def test_random_configuration(cuda_lib, seed):
-    c = _case(seed)
+    _run_case(_case(seed), seed)
+
+
+@pytest.mark.parametrize("seed", range(32))
+def test_random_row_groups(cuda_lib, seed):
+    _run_case(_wide_case(seed), 100 + seed)
+
+
+def _run_case(c, seed):
     P, H, T = c["P"], c["H"], c["T"]
     int8, fp8 = c["fmt"] == "int8", c["fmt"] == "fp8"
     g = W.generator(5000 + seed)
