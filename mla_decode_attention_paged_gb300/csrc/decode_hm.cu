@@ -1,5 +1,6 @@
 // decode_hm.cu -- split-KV MLA decode attention for groups of 128 query rows
-// (128 heads; or q_len x heads rows of multi-token decode and prefill) on
+// (128 heads; or q_len x heads rows of multi-token decode and prefill; a
+// sequence's last group padded when its rows are not a multiple of 128) on
 // CTA pairs, with the query rows as the tensor-core MMA's M extent.  Serves
 // bf16, INT8 and FP8 caches.
 //
@@ -50,7 +51,8 @@
 //
 // Warp roles (384 threads; 512 for 1-byte caches):
 //   warp 0       TMA producer: Q's RoPE part per segment; latent boxes 0-1 and
-//                the RoPE box of every sub-tile
+//                the RoPE box of every sub-tile (1-byte caches: their codes,
+//                into the code ring)
 //   warp 1       TMEM allocation; lane 0 issues the QK MMAs
 //   warp 2       PV: lane 0 issues the MMAs; bf16: the warp first clears
 //                the rows past a sequence's end that the last MMA reads
