@@ -19,10 +19,11 @@
 // [512 + 32 r, 512 + 32 r + 32): 72 KB per tile, so each SM keeps two tiles
 // in flight.
 //   * QK^T: each CTA forms the partial scores over its columns, S_r^T
-//     [128 tok x HC] = C_r [128 x 288] * Q_r^T, and sends them to the other
-//     CTA through distributed shared memory (8 KB for 16 heads);
-//   * both CTAs add the two partials in rank order (so both get the same
-//     bits), run the same softmax and hold the same P^T;
+//     [128 tok x HC] = C_r [128 x 288] * Q_r^T, and sends them, in log2
+//     units rounded to fp16, to the other CTA through distributed shared
+//     memory (4 KB for 16 heads);
+//   * both CTAs add the same two fp16 values (so both get the same bits),
+//     run the same softmax and hold the same P^T;
 //   * PV: each CTA accumulates its own 256 latent columns of O^T.
 // Every page is read from HBM once for all heads of the group.
 //
