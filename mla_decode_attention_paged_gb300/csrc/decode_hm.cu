@@ -128,6 +128,7 @@ struct HmCfg {
   static constexpr uint32_t kOffMisc = kOffX + 2 * kXBytes;
   static constexpr uint32_t kSmem = kOffMisc + 512 + 2048 + 1024;  // + barriers, row maxima and sums, alignment slack
   static_assert(kSmem <= 232448, "dynamic shared memory of one CTA");
+  static_assert(kSlots <= kMaxSlots, "barrier arrays");
   static_assert(kOffQRope % 1024 == 0 && kOffP % 1024 == 0 && kSlotBytes % 1024 == 0 && kOffCode % 1024 == 0,
                 "swizzle atoms, copy alignment");
 };
