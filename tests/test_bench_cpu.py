@@ -34,3 +34,17 @@ def test_prefill_flops_closed_forms():
 def test_whole_job_rate_units():
     # 32 tokens in 0.25 ms on one rank
     assert bench.whole_job_rate(32, 1, 0.25) == pytest.approx(128000.0)
+
+
+@pytest.mark.parametrize("fmt,rows,kernel", [
+    ("bf16", 16, "decode_pair.cu"), ("bf16", 32, "decode_pair.cu"), ("bf16", 64, "decode_pair.cu"),
+    ("bf16", 48, "decode_hm.cu"), ("bf16", 96, "decode_hm.cu"), ("bf16", 128, "decode_hm.cu"),
+    ("bf16", 8192, "decode_hm.cu"), ("int8", 16, "decode_tc.cu"), ("int8", 32, "decode_tc.cu"),
+    ("int8", 64, "decode_hm.cu"), ("fp8", 48, "decode_hm.cu"), ("fp8", 128, "decode_hm.cu"),
+])
+def test_attention_kernel_follows_the_library_choice(fmt, rows, kernel):
+    """The source the bench hashes for its DRAM-traffic record is the kernel
+    the library runs for these rows (mla_api.cu, choose_attention: more than
+    32 rows on the 128-row kernel, except bf16 rows of one or two 32-row
+    groups; else bf16 on CTA pairs, 1-byte caches on single CTAs)."""
+    assert os.path.basename(bench.attention_kernel(fmt, rows)[0]) == kernel
