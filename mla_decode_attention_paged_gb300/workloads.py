@@ -91,9 +91,12 @@ WORKLOADS = {
 def num_splits_for(w: Workload, auto_splits: int) -> int:
     """KV partitions to run ``w`` with: the automatic count, raised where the
     workload asks for a minimum number of chunks per sequence (equal-length
-    sequences get num_splits / batch chunks each)."""
+    sequences get num_splits / batch chunks each) -- to a multiple of the
+    automatic count, so that every CTA pair (one partition each at the
+    automatic count) walks the same number of equal partitions."""
     if w.min_splits_per_seq:
-        return max(auto_splits, w.min_splits_per_seq * w.batch)
+        need = max(auto_splits, w.min_splits_per_seq * w.batch)
+        return -(-need // auto_splits) * auto_splits
     return 0
 
 
