@@ -88,13 +88,14 @@ struct PairCfg {
   static constexpr uint32_t kOffP = kOffQ + ((kQBytes + 1023) & ~1023u);
   static constexpr uint32_t kOffX = kOffP + 2 * kPBytes;  // [2 buffers] of the peer's partials
   static constexpr uint32_t kOffMisc = kOffX + 2 * kXBytes;
-  static constexpr uint32_t kMiscBytes = 2048;
+  static constexpr uint32_t kMiscBytes = 2560;
   static constexpr uint32_t kSmem = kOffMisc + kMiscBytes + 1024;  // +1024: base alignment slack
   static constexpr uint32_t kColS = 0;                             // + buf * HC
   static constexpr uint32_t kColO = 2 * HC;                        // + c * HC
   static constexpr uint32_t kTmemCols = (2 + kChunks) * HC <= 64 ? 64 : ((2 + kChunks) * HC <= 128 ? 128 : 256);
   static_assert(kSmem <= 232448, "dynamic shared memory of one CTA");
   static_assert(kNumPair <= kMaxSlots && kNumRope <= kMaxSlots, "barrier arrays");
+  static_assert(512 + 13 * HC * 4 <= kMiscBytes, "barriers, maxima, sums and reciprocal sums");
   static_assert(kOffQ % 1024 == 0 && kOffQRope % 256 == 0, "swizzle atoms");
 };
 
@@ -123,7 +124,8 @@ __global__ void __launch_bounds__(kPairThreads, 1)
   // the same offset in every CTA: the others' exchange buffers and barriers are found by mapa
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   PairBarriers* B = reinterpret_cast<PairBarriers*>(smem + C::kOffMisc);
-  float* red = reinterpret_cast<float*>(smem + C::kOffMisc + 512);  // [2][HC][4] maxima, [HC][4] sums
+  // [2][HC][4] maxima, [HC][4] sums of l, [HC] 1 / l
+  float* red = reinterpret_cast<float*>(smem + C::kOffMisc + 512);
   const uint32_t sbase = smem_u32(smem);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();
@@ -521,12 +523,26 @@ __global__ void __launch_bounds__(kPairThreads, 1)
           if (HC == 32 || !(lane & 1)) rl[(HC == 32 ? lane : lane >> 1) * 4 + q4] = ls;
         }
         if (bar_any(!ok2)) break;
+        // thread h computes head h's 1 / l once: sixteen or thirty-two IEEE
+        // reciprocals in a row in every thread took ~1.3 us, at every
+        // segment end, with the pipeline stalled behind it
+        float* rinv = red + 12 * HC;  // [HC]
+        float ih = 0.f;
+        if (st < HC) {
+          const float4 l4 = reinterpret_cast<const float4*>(rl)[st];
+          const float l = (l4.x + l4.y) + (l4.z + l4.w);
+          ih = l > 0.f ? __frcp_rn(l) : 0.f;  // 0: a row with no visible token (multi-token decode)
+          rinv[st] = ih;
+        }
+        bar_any(false);
         float inv_l[HC];
 #pragma unroll
-        for (int h = 0; h < HC; ++h) {
-          const float4 l4 = reinterpret_cast<const float4*>(rl)[h];
-          const float l = (l4.x + l4.y) + (l4.z + l4.w);
-          inv_l[h] = l > 0.f ? __frcp_rn(l) : 0.f;  // 0: a row with no visible token (multi-token decode)
+        for (int j = 0; j < HC / 4; ++j) {
+          const float4 v = reinterpret_cast<const float4*>(rinv)[j];
+          inv_l[4 * j] = v.x;
+          inv_l[4 * j + 1] = v.y;
+          inv_l[4 * j + 2] = v.z;
+          inv_l[4 * j + 3] = v.w;
         }
         float* dst = p.partial_o + (size_t(t.seg) * p.heads + g * HC) * kLatent + lat0;
 #pragma unroll
@@ -541,13 +557,10 @@ __global__ void __launch_bounds__(kPairThreads, 1)
         tc_fence_before();
         mbar_arrive(&B->o_free);
         if (rank == 0 && st < HC) {  // thread h writes head h's lse
-          float mh = 0.f, ih = 1.f;
+          float mh = 0.f;
 #pragma unroll
           for (int h = 0; h < HC; ++h)
-            if (st == h) {
-              mh = m_run[h];
-              ih = inv_l[h];
-            }
+            if (st == h) mh = m_run[h];
           p.partial_lse[size_t(t.seg) * p.heads + g * HC + st] = ih > 0.f ? (mh - log2f(ih)) * kLn2 : -INFINITY;
         }
         ++seg;

@@ -112,6 +112,7 @@ struct Cfg {
   static constexpr uint32_t kColO = 2 * HC;                        // + c * HC
   static_assert(kSmem <= 232448, "dynamic shared memory of one CTA");
   static_assert(kQkRing <= 8 && kNumPair <= 5 && kNumRope <= 2, "barrier arrays");
+  static_assert(1024 + 17 * HC * 4 <= kMiscBytes, "barriers, maxima, sums and reciprocal sums");
 };
 
 struct Barriers {
@@ -160,7 +161,8 @@ __global__ void __launch_bounds__(Cfg<HC, kCode != kCodeBf16>::kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Barriers* B = reinterpret_cast<Barriers*>(smem + C::kOffMisc);
-  float* red = reinterpret_cast<float*>(smem + C::kOffMisc + 1024);  // [2][HC][4] maxima, [HC][4] sums x2
+  // [2][HC][4] maxima, [HC][4] sums of l, [HC][4] sums of corr, [HC] 1 / l
+  float* red = reinterpret_cast<float*>(smem + C::kOffMisc + 1024);
   const uint32_t sbase = smem_u32(smem);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   constexpr uint32_t kFullCount = 1;  // TMA (bf16) or expansion thread 0 (1-byte caches) completes a slot
@@ -714,16 +716,32 @@ __global__ void __launch_bounds__(Cfg<HC, kCode != kCodeBf16>::kThreads, 1)
           }
         }
         if (bar_any(!ok2)) break;
-        float inv_l[HC];
-#pragma unroll
-        for (int h = 0; h < HC; ++h) {
-          const float4 l4 = reinterpret_cast<const float4*>(rl)[h];
+        // thread h divides for head h once (a division per head in every
+        // thread sits on the pipeline's critical path at every segment end)
+        float* rinv = red + 16 * HC;  // [HC]
+        float ih = 0.f;
+        if (st < HC) {
+          const float4 l4 = reinterpret_cast<const float4*>(rl)[st];
           const float l = (l4.x + l4.y) + (l4.z + l4.w);
-          inv_l[h] = l > 0.f ? 1.f / l : 0.f;  // 0: a row with no visible token (multi-token decode)
-          if (kZp) {
+          ih = l > 0.f ? 1.f / l : 0.f;  // 0: a row with no visible token (multi-token decode)
+          rinv[st] = ih;
+        }
+        if (kZp) {
+#pragma unroll
+          for (int h = 0; h < HC; ++h) {
             const float4 c4 = reinterpret_cast<const float4*>(rc)[h];
             corr[h] = (c4.x + c4.y) + (c4.z + c4.w);
           }
+        }
+        bar_any(false);
+        float inv_l[HC];
+#pragma unroll
+        for (int j = 0; j < HC / 4; ++j) {
+          const float4 v = reinterpret_cast<const float4*>(rinv)[j];
+          inv_l[4 * j] = v.x;
+          inv_l[4 * j + 1] = v.y;
+          inv_l[4 * j + 2] = v.z;
+          inv_l[4 * j + 3] = v.w;
         }
         float* dst = p.partial_o + (size_t(t.seg) * p.heads + g * HC) * kLatent;
 #pragma unroll
@@ -738,11 +756,13 @@ __global__ void __launch_bounds__(Cfg<HC, kCode != kCodeBf16>::kThreads, 1)
           }
         tc_fence_before();
         mbar_arrive(&B->o_free);
+        if (st < HC) {  // thread h writes head h's lse
+          float mh = 0.f;
 #pragma unroll
-        for (int h = 0; h < HC; ++h)
-          if (st == h)
-            p.partial_lse[size_t(t.seg) * p.heads + g * HC + h] =
-                inv_l[h] > 0.f ? (m_run[h] - log2f(inv_l[h])) * kLn2 : -INFINITY;
+          for (int h = 0; h < HC; ++h)
+            if (st == h) mh = m_run[h];
+          p.partial_lse[size_t(t.seg) * p.heads + g * HC + st] = ih > 0.f ? (mh - log2f(ih)) * kLn2 : -INFINITY;
+        }
         ++seg;
       }
     }
