@@ -671,7 +671,7 @@ __global__ void __launch_bounds__(Cfg<HC, kCode != kCodeBf16>::kThreads, 1)
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int ha = h0 + 2 * i, hb = ha + 1;
-          const float pa_ = exp2f(x[ha] - m_run[ha]), pb_ = exp2f(x[hb] - m_run[hb]);
+          const float pa_ = ex2_ftz(x[ha] - m_run[ha]), pb_ = ex2_ftz(x[hb] - m_run[hb]);
           if constexpr (kByte) {
             const __half wa = __float2half_rn(pa_ * tok_s), wb = __float2half_rn(pb_ * tok_s);
             l_run[ha] += pa_;
