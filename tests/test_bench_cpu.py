@@ -48,3 +48,19 @@ def test_attention_kernel_follows_the_library_choice(fmt, rows, kernel):
     32 rows on the 128-row kernel, except bf16 rows of one or two 32-row
     groups; else bf16 on CTA pairs, 1-byte caches on single CTAs)."""
     assert os.path.basename(bench.attention_kernel(fmt, rows)[0]) == kernel
+
+
+@pytest.mark.parametrize("auto", [76, 64, 148])
+def test_minimum_chunks_round_up_to_whole_partitions_per_unit(auto):
+    """A workload that asks for a minimum number of KV chunks per sequence
+    runs with a multiple of the automatic split count (every attention unit
+    then walks the same number of equal partitions), never fewer chunks than
+    asked, and the smallest such multiple."""
+    from mla_decode_attention_paged_gb300 import workloads as W
+    w = W.WORKLOADS["ctx1m"]
+    s = W.num_splits_for(w, auto)
+    assert s % auto == 0
+    assert s >= w.min_splits_per_seq * w.batch
+    assert s - auto < max(auto, w.min_splits_per_seq * w.batch)
+    # workloads without a minimum keep the automatic count (0 = automatic)
+    assert W.num_splits_for(W.WORKLOADS["v2lite"], auto) == 0
