@@ -52,17 +52,23 @@ __global__ void __launch_bounds__(256) append_kernel(AppendParams p) {
   const uint4* src = reinterpret_cast<const uint4*>(p.c_kv + size_t(i) * kLatent) + 2 * lane;
   uint4 c0 = src[0], c1 = src[1];
 
-  // RoPE pair `lane`: angle = pos * theta^(-2 lane / 64), evaluated in fp64
+  // RoPE pair `lane`: angle = pos * theta^(-2 lane / 64) in fp64 (up to
+  // ~2^31 rad), reduced modulo 2 pi in fp64 to [-pi, pi]; sine, cosine and
+  // the rotation then in fp32 ahead of the one rounding to bf16.  A full
+  // fp64 sincos per lane kept the few SMs an append runs on busy for
+  // microseconds (the fp64 units are a small fraction of this part's), and
+  // the reduced fp32 result stays far inside the bf16 rounding.
   const __nv_bfloat162 kp = reinterpret_cast<const __nv_bfloat162*>(p.k_pe + size_t(i) * kRope)[lane];
   __nv_bfloat162 kr = kp;
   if (p.rope_theta > 0.0) {
+    constexpr double kTwoPi = 6.283185307179586476925286766559, kInvTwoPi = 0.15915494309189533576888376337251;
     const double ang = __dmul_rn(double(pos), p.inv_freq[lane]);
-    double sn, cs;
-    sincos(ang, &sn, &cs);
-    const double x0 = double(__low2float(kp)), x1 = double(__high2float(kp));
-    const double y0 = __dsub_rn(__dmul_rn(x0, cs), __dmul_rn(x1, sn));
-    const double y1 = __dadd_rn(__dmul_rn(x0, sn), __dmul_rn(x1, cs));
-    kr = __halves2bfloat162(__double2bfloat16(y0), __double2bfloat16(y1));
+    const double turns = rint(__dmul_rn(ang, kInvTwoPi));
+    const float red = float(__fma_rn(-turns, kTwoPi, ang));
+    float sn, cs;
+    sincosf(red, &sn, &cs);
+    const float x0 = __low2float(kp), x1 = __high2float(kp);
+    kr = __floats2bfloat162_rn(fmaf(x0, cs, -x1 * sn), fmaf(x0, sn, x1 * cs));
   }
 
   if constexpr (kCode == kCodeBf16) {
