@@ -494,8 +494,8 @@ def run_ours(args, rank, world):
         torch.distributed.barrier()
     torch.cuda.synchronize()
     with ClockSampler(dev.index) as clk:
-        # untimed steps while the sampler starts (~0.3 s): a GPU left idle that
-        # long lowers its clocks, and the first timed steps would pay the ramp
+        # untimed steps while the sampler starts (~0.3 s): after that long
+        # idle the first steps ran slower, and a short timed run paid for it
         t_end = time.perf_counter() + 0.3
         i = 0
         while time.perf_counter() < t_end:
