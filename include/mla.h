@@ -164,7 +164,9 @@ size_t mla_decode_workspace_size(const mla_dims* dims, int32_t batch, int32_t nu
  *   num_splits  KV partitions over the batch's total work (0 = automatic).
  *               The work of every row group is cut into num_splits equal
  *               pieces, so a sequence holding a fraction f of all tokens is
- *               split into about f * num_splits chunks.
+ *               split into about f * num_splits chunks.  The attention units
+ *               take contiguous blocks of partitions: above the automatic
+ *               count, a multiple of it gives every unit the same work.
  *   workspace   device scratch, 256-byte aligned, at least
  *               mla_decode_workspace_size(dims, batch, num_splits) bytes.
  *               Its first 4 bytes hold the device status of this call.
